@@ -1,0 +1,205 @@
+"""Exhaustive interleaving explorer for the SYNCALL soft-mode epoch barrier.
+
+TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).
+
+Model ("PTO-ISA SYNCALL cross-core barrier guide", lmnt.cn/news/269652, §5.2):
+each of P participants runs its barriers one after another; one barrier is
+
+    before = atomic fetch-and-increment(counter)
+    target = (before / P + 1) * P
+    spin until the counter has reached target
+
+The explorer treats the increment and each successful poll as atomic steps
+and enumerates every order in which participants can take them (depth-first,
+with a visited-state set).  A failed poll changes nothing, so a polling
+participant is simply not enabled until its condition holds.  For every
+reachable state it checks
+
+  safety    no participant leaves barrier k before (k+1)*P arrivals happened
+            ("any core may continue only after every participant has
+            executed the barrier", §2);
+  epochs    the values returned to the arrivals of barrier k are exactly
+            start + kP .. start + kP + P-1 (mod the cycle length);
+  liveness  no reachable state has every unfinished participant blocked.
+
+Counter arithmetic variants:
+  "modular"  the wrap-safe reading: counter in Z_M with M a multiple of P,
+             target taken mod M, reached <=> (cur - target) mod M < P;
+  "literal"  a W-value word (W = 2^bits) with the pages' literal formula and
+             an unsigned >= compare, wrapping at W;
+  "equal"    modular counter but the poll waits for cur == target exactly.
+The last two exist to show that the explorer does catch broken protocols.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+
+@dataclass(frozen=True)
+class Arith:
+    kind: str        # "modular" | "literal" | "equal"
+    P: int
+    M: int           # cycle length (modular/equal) or word size W (literal)
+
+    def arrive(self, c: int) -> int:
+        return (c + 1) % self.M
+
+    def target(self, before: int) -> int:
+        return ((before // self.P) + 1) * self.P % self.M
+
+    def reached(self, cur: int, t: int) -> bool:
+        if self.kind == "modular":
+            return (cur - t) % self.M < self.P
+        if self.kind == "equal":
+            return cur == t
+        if self.kind == "literal":
+            return cur >= t
+        raise ValueError(self.kind)
+
+
+@dataclass
+class Result:
+    states: int = 0
+    safety_violations: int = 0
+    epoch_violations: int = 0
+    deadlocks: int = 0
+    completed: int = 0          # terminal states with everyone done
+
+    @property
+    def ok(self) -> bool:
+        return self.safety_violations == 0 and self.epoch_violations == 0 and self.deadlocks == 0
+
+
+def explore(arith: Arith, rounds, start: int = 0, max_states: int = 2_000_000) -> Result:
+    """Enumerate all interleavings.
+
+    rounds: per-participant barrier count (sequence of length P), or an int for
+    all participants.  start: counter value before the first arrival.
+    """
+    P = arith.P
+    if isinstance(rounds, int):
+        rounds = [rounds] * P
+    rounds = tuple(rounds)
+    assert len(rounds) == P
+    res = Result()
+    # participant state: (k barriers finished, phase 0 = next is arrive /
+    # 1 = polling, target)
+    init = (start % arith.M, tuple((0, 0, 0) for _ in range(P)))
+    seen = set()
+    stack = [init]
+    while stack:
+        state = stack.pop()
+        if state in seen:
+            continue
+        seen.add(state)
+        res.states += 1
+        if res.states > max_states:
+            raise RuntimeError("state space larger than max_states")
+        c, parts = state
+        arrivals = sum(k + ph for (k, ph, _) in parts)
+        succ = []
+        for i, (k, ph, t) in enumerate(parts):
+            if k == rounds[i]:
+                continue
+            if ph == 0:
+                before = c
+                # epochs: the j-th arrival of barrier k gets start + kP + j
+                if (before - start - k * P) % arith.M >= P:
+                    res.epoch_violations += 1
+                nt = arith.target(before)
+                nparts = parts[:i] + ((k, 1, nt),) + parts[i + 1:]
+                succ.append((arith.arrive(c), nparts))
+            elif arith.reached(c, t):
+                # leaving barrier k: all (k+1)*P arrivals must have happened
+                if arrivals < (k + 1) * P:
+                    res.safety_violations += 1
+                nparts = parts[:i] + ((k + 1, 0, 0),) + parts[i + 1:]
+                succ.append((c, nparts))
+        if not succ:
+            if all(parts[i][0] == rounds[i] for i in range(P)):
+                res.completed += 1
+            else:
+                res.deadlocks += 1
+        stack.extend(succ)
+    return res
+
+
+def sequential_final_counter(arith: Arith, rounds: int, start: int = 0) -> int:
+    """Counter after `rounds` barriers taken in participant order (one schedule)."""
+    c = start % arith.M
+    for _ in range(rounds):
+        for _ in range(arith.P):
+            c = arith.arrive(c)
+    return c
+
+
+# Two-level (cluster) barrier -------------------------------------------------
+#
+# The hard path replaces the per-participant arrive with: every member of a
+# group of C arrives on a group barrier; the group leader alone arrives on the
+# global counter (Pg = number of groups) and polls it; a second group barrier
+# releases the members.  The pages' MIX hard path has this shape (the cube core
+# waits for its paired vector cores, takes part in the cross-core sync, then
+# releases them, §5.1).  The model checks the same safety property at
+# participant level.
+
+def explore_two_level(P: int, C: int, rounds: int, M: int | None = None, start: int = 0,
+                      max_states: int = 2_000_000) -> Result:
+    assert P % C == 0
+    G = P // C
+    arith = Arith("modular", G, M if M is not None else 4 * G)
+    res = Result()
+    # member phases: 0 = before group-arrive, 1 = waiting in group barrier 1,
+    # 2 = waiting in group barrier 2 (leader: 2 = arrived globally, polling),
+    # member k counter.  group state: count in barrier 1, count in barrier 2,
+    # generation.  Modelled per participant: (k, phase, target)
+    init = (start % arith.M, tuple((0, 0, 0) for _ in range(P)))
+    seen = set()
+    stack = [init]
+    while stack:
+        state = stack.pop()
+        if state in seen:
+            continue
+        seen.add(state)
+        res.states += 1
+        if res.states > max_states:
+            raise RuntimeError("state space larger than max_states")
+        c, parts = state
+        succ = []
+        for i, (k, ph, t) in enumerate(parts):
+            if k == rounds:
+                continue
+            g, lead = i // C, (i % C == 0)
+            grp = parts[g * C:(g + 1) * C]
+            if ph == 0:
+                # group barrier 1 arrive
+                succ.append((c, parts[:i] + ((k, 1, 0),) + parts[i + 1:]))
+            elif ph == 1:
+                # group barrier 1 opens when all members of the group are at
+                # phase >= 1 of the same barrier k
+                if all(m[0] == k and m[1] >= 1 for m in grp):
+                    if lead:
+                        before = c
+                        if (before - start - k * G) % arith.M >= G:
+                            res.epoch_violations += 1
+                        succ.append((arith.arrive(c), parts[:i] + ((k, 3, arith.target(before)),) + parts[i + 1:]))
+                    else:
+                        succ.append((c, parts[:i] + ((k, 2, 0),) + parts[i + 1:]))
+            elif ph == 3:
+                if arith.reached(c, t):
+                    succ.append((c, parts[:i] + ((k, 2, 0),) + parts[i + 1:]))
+            elif ph == 2:
+                # group barrier 2 opens when all members are at phase 2 (leader
+                # got there only after its global poll succeeded)
+                if all((m[0] == k and m[1] == 2) or m[0] == k + 1 for m in grp):
+                    # leaving barrier k: every participant must have arrived
+                    if not all(m[0] > k or (m[0] == k and m[1] >= 1) for m in parts):
+                        res.safety_violations += 1
+                    succ.append((c, parts[:i] + ((k + 1, 0, 0),) + parts[i + 1:]))
+        if not succ:
+            if all(p[0] == rounds for p in parts):
+                res.completed += 1
+            else:
+                res.deadlocks += 1
+        stack.extend(succ)
+    return res

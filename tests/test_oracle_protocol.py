@@ -1,0 +1,89 @@
+"""All-interleaving checks of the soft-barrier protocol (no GPU).
+
+The explorer enumerates every order of atomic arrive/poll steps for tiny
+participant counts; the wrap-safe arithmetic must be safe and live for every
+start value, and the broken variants (a participant that skips a barrier, an
+exact-equality poll, the literal unsigned compare at the wrap) must be caught.
+"""
+import pytest
+
+import oracle
+from oracle.protocol import Arith, explore, explore_two_level, sequential_final_counter
+
+U32 = 1 << 32
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4])
+@pytest.mark.parametrize("R", [1, 2, 3])
+def test_modular_counter_safe_and_live_for_every_start(P, R):
+    for mult in (2, 3, 4):
+        M = mult * P
+        for start in range(0, M, P):
+            res = explore(Arith("modular", P, M), R, start)
+            assert res.ok and res.completed == 1, (P, R, M, start, res)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4])
+def test_full_width_counter(P):
+    M = oracle.counter_modulus(P)
+    for start in (0, M - P, M - 2 * P):
+        res = explore(Arith("modular", P, M), 3, start)
+        assert res.ok and res.completed == 1
+
+
+def test_oracle_arithmetic_agrees_with_explorer_model():
+    # the C oracle's arrive/target/reached are the same functions the explorer uses
+    for P, M in [(3, 9), (4, 8), (3, oracle.counter_modulus(3)), (148, oracle.counter_modulus(148))]:
+        a = Arith("modular", P, M)
+        for before in list(range(0, min(M, 40))) + [M - 1, M - 2, M - P]:
+            assert oracle.target_mod(before, P, M) == a.target(before)
+            assert oracle.arrive_mod(before, M) == a.arrive(before)
+            t = a.target(before)
+            for cur in (t, (t + P - 1) % M, (t + P) % M, (t + M - 1) % M, (before + 1) % M):
+                assert oracle.reached_mod(cur, t, P, M) == a.reached(cur, t)
+
+
+def test_skipped_barrier_deadlocks():
+    # one participant enters one barrier fewer ("same order, same count", guide §6.2)
+    res = explore(Arith("modular", 3, 9), [2, 2, 1])
+    assert res.deadlocks > 0 and res.completed == 0
+
+
+def test_extra_barrier_deadlocks():
+    res = explore(Arith("modular", 2, 8), [3, 2])
+    assert res.deadlocks > 0
+
+
+def test_equality_poll_can_miss_the_target():
+    res = explore(Arith("equal", 3, 9), 2)
+    assert res.deadlocks > 0
+
+
+def test_literal_unsigned_compare_breaks_at_the_wrap():
+    # a 5-bit word stands in for u32: near the wrap the literal target wraps to a
+    # small value and `cur >= target` lets participants through early, or hangs
+    broken = 0
+    for P in (3, 4):
+        for start in range(0, 32, P):
+            res = explore(Arith("literal", P, 32), 2, start)
+            broken += not res.ok
+    assert broken > 0
+    # far from the wrap the literal form is fine
+    assert explore(Arith("literal", 3, U32), 3, 0).ok
+
+
+def test_start_not_multiple_of_p_breaks():
+    res = explore(Arith("modular", 4, 16), 2, 1)
+    assert not res.ok
+
+
+def test_sequential_final_counter():
+    a = Arith("modular", 148, oracle.counter_modulus(148))
+    assert sequential_final_counter(a, 1000) == 148_000
+
+
+@pytest.mark.parametrize("P,C", [(2, 1), (2, 2), (4, 2), (4, 4), (6, 3), (6, 2)])
+@pytest.mark.parametrize("R", [1, 2, 3])
+def test_two_level_barrier_safe_and_live(P, C, R):
+    res = explore_two_level(P, C, R)
+    assert res.ok and res.completed == 1, res
