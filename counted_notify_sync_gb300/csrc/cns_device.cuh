@@ -1,0 +1,310 @@
+// cns_device.cuh -- sm_103a device primitives for the epoch barrier and the
+// counted notify: scoped atomics and loads in inline PTX, the global timer,
+// thread-block-cluster barriers, and the bounded poll.
+//
+// Every wait here is bounded: after `timeout_ns` of polling the waiter
+// records CNS_ERR_TIMEOUT in a status word, raises an abort flag that the
+// other waiters also watch, and returns.  Nothing traps or asserts.
+#pragma once
+
+#include <cstdint>
+
+#include "cns.h"
+
+namespace cns {
+
+// ---------------------------------------------------------------------------
+// Scoped memory operations (PTX ISA memory consistency model, .gpu scope)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t atom_inc_release_gpu(uint32_t *p, uint32_t bound)
+{
+    // old = *p; *p = (old >= bound) ? 0 : old + 1
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_exch_release_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_exch_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_cas_relaxed_gpu(uint32_t *p, uint32_t cmp, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "l"(p), "r"(cmp), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_or_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.or.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_and_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.and.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu()
+{
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smid()
+{
+    uint32_t s;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives (release) and waits
+// (acquire): the cluster-scope barrier.  The calling warp must be converged.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store a 32-bit value into the shared memory of CTA `rank` of this cluster,
+// at the address that `local` has in this CTA.
+__device__ __forceinline__ void st_shared_cluster(const void *local, uint32_t rank, uint32_t v)
+{
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Epoch arithmetic of the soft barrier ("PTO-ISA SYNCALL cross-core barrier
+// guide", §5.2).  The counter lives in Z_M with M = P * floor(2^32 / P): the
+// arrival is atom.inc with bound M - 1, the target is ((before / P) + 1) * P
+// taken mod M, and the count has reached the target when (cur - target) mod M
+// is below P -- a waiter sees counts in [before + 1, target + P - 1] only.
+// For a power-of-two P, M = 2^32 and this is the plain wrapping add.
+// ---------------------------------------------------------------------------
+
+struct Epoch {
+    uint32_t P;     // participants arriving on this counter
+    uint32_t Mm1;   // M - 1 (the atom.inc bound)
+};
+
+__device__ __forceinline__ uint32_t epoch_target(uint32_t before, const Epoch &e)
+{
+    const uint64_t M = static_cast<uint64_t>(e.Mm1) + 1u;
+    uint64_t t = (static_cast<uint64_t>(before / e.P) + 1u) * e.P;   // <= M since before < M
+    return t == M ? 0u : static_cast<uint32_t>(t);
+}
+
+__device__ __forceinline__ bool epoch_reached(uint32_t cur, uint32_t target, const Epoch &e)
+{
+    const uint64_t M = static_cast<uint64_t>(e.Mm1) + 1u;
+    uint64_t d = cur >= target ? static_cast<uint64_t>(cur - target)
+                               : static_cast<uint64_t>(cur) + (M - target);
+    return d < e.P;
+}
+
+// Status line of the workspace: [0] status, [1] abort flag, [2] round of the
+// first timeout, [3] CTA of the first timeout.
+__device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t round, uint32_t who)
+{
+    if (atom_cas_relaxed_gpu(status_line, 0u, static_cast<uint32_t>(CNS_ERR_TIMEOUT)) == 0u) {
+        st_relaxed_gpu(status_line + 2, round);
+        st_relaxed_gpu(status_line + 3, who);
+    }
+    atom_exch_release_gpu(status_line + 1, 1u);
+}
+
+// Poll `ctr` until it reaches `target`.  Returns false when released, true
+// when the wait gave up (timeout here, or an abort raised by another waiter).
+// The abort flag and the clock are looked at once every 64 polls.
+__device__ __forceinline__ bool poll_epoch(const uint32_t *ctr, uint32_t target, const Epoch &e,
+                                           uint32_t *status_line, uint64_t timeout_ns, uint32_t round,
+                                           uint32_t who)
+{
+    uint32_t spins = 0;
+    uint64_t deadline = 0;
+    for (;;) {
+        const uint32_t cur = ld_acquire_gpu(ctr);
+        if (epoch_reached(cur, target, e))
+            return false;
+        if ((++spins & 63u) == 0u) {
+            if (ld_relaxed_gpu(status_line + 1) != 0u)
+                return true;
+            const uint64_t now = globaltimer_ns();
+            if (deadline == 0)
+                deadline = now + timeout_ns;
+            else if (now > deadline) {
+                raise_timeout(status_line, round, who);
+                return true;
+            }
+        }
+    }
+}
+
+// One soft barrier for the calling CTA: drain the CTA, one elected thread
+// arrives and polls, drain again.  All threads of the CTA must call it.
+// Returns true if the CTA must stop (timeout / abort).
+__device__ __forceinline__ bool soft_barrier(uint32_t *ctr, const Epoch &e, uint32_t *status_line,
+                                             uint64_t timeout_ns, uint32_t round, int *s_flag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t before = atom_inc_release_gpu(ctr, e.Mm1);
+        const uint32_t target = epoch_target(before, e);
+        *s_flag = poll_epoch(ctr, target, e, status_line, timeout_ns, round, blockIdx.x) ? 1 : 0;
+    }
+    __syncthreads();
+    return *s_flag != 0;
+}
+
+// One hard barrier: cluster barrier; cluster rank 0 arrives on the
+// per-cluster counter (P = number of clusters) and polls it; on a timeout it
+// writes the stop flag into every CTA of its cluster; second cluster barrier.
+// All threads of all CTAs of the cluster must call it.
+__device__ __forceinline__ bool hard_barrier(uint32_t *ctr, const Epoch &e, uint32_t *status_line,
+                                             uint64_t timeout_ns, uint32_t round, int *s_flag)
+{
+    __syncwarp();
+    cluster_sync_all();
+    if (threadIdx.x == 0 && cluster_ctarank() == 0) {
+        const uint32_t before = atom_inc_release_gpu(ctr, e.Mm1);
+        const uint32_t target = epoch_target(before, e);
+        if (poll_epoch(ctr, target, e, status_line, timeout_ns, round, blockIdx.x)) {
+            const uint32_t n = cluster_nctarank();
+            for (uint32_t r = 0; r < n; ++r)
+                st_shared_cluster(s_flag, r, 1u);
+        }
+    }
+    __syncwarp();   // the .aligned cluster barrier needs a converged warp
+    cluster_sync_all();
+    return *reinterpret_cast<volatile int *>(s_flag) != 0;
+}
+
+// ---------------------------------------------------------------------------
+// Counted-notify record and wait rules ("CANN Runtime CntNotify management
+// API", §3.1 and §3.2)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ bool cnt_record_valid(uint32_t mode)
+{
+    return mode == CNS_REC_SET || mode == CNS_REC_ADD || mode == CNS_REC_BIT_OR || mode == CNS_REC_BIT_AND;
+}
+
+// New count for a record (pure function; the caller checked the mode).
+__device__ __forceinline__ uint32_t cnt_record_apply(uint32_t c, uint32_t mode, uint32_t v)
+{
+    switch (mode) {
+    case CNS_REC_SET: return v;
+    case CNS_REC_ADD: return c + v;
+    case CNS_REC_BIT_OR: return c | v;
+    default: return c & v;   // CNS_REC_BIT_AND
+    }
+}
+
+// Whether a wait with this mode/value is released at count c (mode checked
+// by the caller, <= 4).
+__device__ __forceinline__ bool cnt_wait_released(uint32_t c, uint32_t mode, uint32_t v)
+{
+    switch (mode) {
+    case CNS_WAIT_LESS: return c < v;
+    case CNS_WAIT_EQUAL: return c == v;
+    case CNS_WAIT_BIGGER: return c > v;
+    case CNS_WAIT_BIGGER_OR_EQUAL: return c >= v;
+    default: return (c & v) == v;   // CNS_WAIT_EQUAL_WITH_BITMASK
+    }
+}
+
+// A record as one device atomic with release semantics.  Usable from inside
+// any kernel (one thread per record).
+__device__ __forceinline__ void cnt_record_device(uint32_t *count, uint32_t mode, uint32_t v)
+{
+    switch (mode) {
+    case CNS_REC_SET: atom_exch_release_gpu(count, v); break;
+    case CNS_REC_ADD: red_add_release_gpu(count, v); break;
+    case CNS_REC_BIT_OR: red_or_release_gpu(count, v); break;
+    case CNS_REC_BIT_AND: red_and_release_gpu(count, v); break;
+    default: break;
+    }
+}
+
+}  // namespace cns

@@ -1,0 +1,634 @@
+// cntnotify.cu -- the counted notify ("CANN Runtime CntNotify management
+// API"): a device-resident pool of counters, handle registry, stream-ordered
+// record / wait / reset kernels, the op-stream state machine and the
+// two-stream counting pipeline.
+//
+// Each notify owns one 128-byte line of the pool: word 0 is the count,
+// word 1 a sticky status that a timed-out wait sets to CNS_ERR_TIMEOUT,
+// word 2 an abort word used by the pipeline.  A record is one device atomic
+// (release); a wait is one thread polling the count with acquire loads under
+// a time bound, so the *stream* is blocked, not the host (§4.3).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "cns.h"
+#include "cns_device.cuh"
+#include "cns_host.h"
+
+struct cns_cnt_notify_s {
+    uint32_t magic;
+    int device;
+    uint32_t slot;
+    uint32_t *line;   // device: [0] count, [1] sticky status, [2] abort word
+};
+
+namespace cns {
+
+constexpr uint32_t kMagic = 0x434E5446u;   // "CNTF"
+constexpr uint32_t kWordsPerSlot = 32;     // 128 B
+
+struct Pool {
+    uint32_t *base = nullptr;
+    uint32_t cap = 0;
+    std::vector<uint32_t> free_slots;   // LIFO
+};
+
+static std::mutex g_mu;
+static std::unordered_map<int, Pool> g_pools;
+static std::unordered_set<cns_cnt_notify_s *> g_live;
+
+static uint32_t pool_cap()
+{
+    const char *e = std::getenv("CNS_POOL_CAP");
+    if (e && *e) {
+        long v = std::atol(e);
+        if (v > 0 && v <= (1 << 20))
+            return static_cast<uint32_t>(v);
+    }
+    return 1024;
+}
+
+// A live handle, or nullptr.  The handle pointer is only dereferenced once it
+// is known to be live, so stale or foreign pointers give an error instead of
+// a crash ([CNTN] §6.1: handles are validated and unwrapped).
+static cns_cnt_notify_s *lookup(cns_cnt_notify_t h)
+{
+    if (!h)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_live.find(h) == g_live.end() || h->magic != kMagic)
+        return nullptr;
+    return h;
+}
+
+// Makes the handle's device current for the call, restoring the caller's.
+struct DeviceGuard {
+    int prev = -1;
+    bool switched = false;
+    int set(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return CNS_ERR_CUDA;
+        }
+        if (prev != dev) {
+            if (cudaSetDevice(dev) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return CNS_ERR_CUDA;
+            }
+            switched = true;
+        }
+        return CNS_SUCCESS;
+    }
+    ~DeviceGuard()
+    {
+        if (switched)
+            cudaSetDevice(prev);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Record / wait kernels
+// ---------------------------------------------------------------------------
+
+__global__ void cnt_record_kernel(uint32_t *count, uint32_t mode, uint32_t v)
+{
+    if (threadIdx.x == 0)
+        cnt_record_device(count, mode, v);
+}
+
+// One thread polls the count until the predicate holds; then the optional
+// clear.  On timeout the sticky status is set and the kernel returns.  With
+// an `abort` word (used by the pipeline), a wait that finds it raised returns
+// at once and a wait that times out raises it, so one lost signal costs one
+// timeout rather than one per remaining round.
+__global__ void cnt_wait_kernel(uint32_t *line, uint32_t mode, uint32_t v, uint32_t clear, uint64_t timeout_ns,
+                                uint32_t *observed, uint32_t *abort)
+{
+    if (threadIdx.x != 0)
+        return;
+    if (abort && ld_relaxed_gpu(abort) != 0u)
+        return;
+    uint32_t spins = 0;
+    uint64_t deadline = 0;
+    for (;;) {
+        const uint32_t c = ld_acquire_gpu(line);
+        if (cnt_wait_released(c, mode, v)) {
+            if (observed)
+                *observed = c;
+            if (clear)
+                atom_exch_relaxed_gpu(line, 0u);   // the clear comes after the release
+            return;
+        }
+        if ((++spins & 63u) == 0u) {
+            if (abort && ld_relaxed_gpu(abort) != 0u)
+                return;
+            const uint64_t now = globaltimer_ns();
+            if (deadline == 0)
+                deadline = now + timeout_ns;
+            else if (now > deadline) {
+                atom_exch_relaxed_gpu(line + 1, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
+                if (abort)
+                    atom_exch_relaxed_gpu(abort, 1u);
+                return;
+            }
+        }
+    }
+}
+
+// Zero the count, the sticky status and the abort word of a notify line.
+__global__ void cnt_clear_line_kernel(uint32_t *line)
+{
+    if (threadIdx.x < 3)
+        line[threadIdx.x] = 0u;
+}
+
+static uint64_t wait_timeout_ns(uint32_t timeout_s)
+{
+    const uint64_t cap = notify_timeout_cap_ns();
+    if (timeout_s == 0)
+        return cap;
+    return std::min<uint64_t>(static_cast<uint64_t>(timeout_s) * 1000000000ull, cap);
+}
+
+static bool record_mode_ok(int32_t m)
+{
+    return m == CNS_REC_SET || m == CNS_REC_ADD || m == CNS_REC_BIT_OR || m == CNS_REC_BIT_AND;
+}
+
+static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info_t *info, uint32_t *observed,
+                        uint32_t *abort = nullptr)
+{
+    cnt_wait_kernel<<<1, 32, 0, s>>>(n->line, static_cast<uint32_t>(info->mode), info->value,
+                                     info->is_clear ? 1u : 0u, wait_timeout_ns(info->timeout), observed, abort);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Op-stream state machine.  The stream is cut into chunks of kChunk ops.  A
+// SET record gives a count that does not depend on what came before, so from
+// the first SET of a chunk to the chunk's end the trace can be computed at
+// once (suffix kernel).  The ops before that first SET are replayed by the
+// thread of the nearest earlier chunk that ends in a known count ("chain
+// head"), which runs forward until it meets the next SET (prefix kernel).
+// Every op is applied exactly once, in order along its chain.
+// ---------------------------------------------------------------------------
+
+constexpr int kChunk = 16;
+
+__device__ __forceinline__ uint32_t sm_apply(uint32_t c, const uint4 &op, uint32_t *outcome)
+{
+    if (op.x == 0u) {
+        if (cnt_record_valid(op.y)) {
+            *outcome = CNS_OUT_RECORD;
+            return cnt_record_apply(c, op.y, op.z);
+        }
+    } else if (op.x == 1u && op.y <= 4u) {
+        const bool rel = cnt_wait_released(c, op.y, op.z);
+        *outcome = rel ? CNS_OUT_WAIT_RELEASED : CNS_OUT_WAIT_HELD;
+        return (rel && op.w) ? 0u : c;
+    }
+    *outcome = CNS_OUT_INVALID;
+    return c;
+}
+
+__device__ __forceinline__ bool is_set_record(const uint4 &op) { return op.x == 0u && op.y == CNS_REC_SET; }
+
+__global__ void __launch_bounds__(256) sm_suffix_kernel(const uint4 *ops, int64_t n, uint2 *trace, uint2 *summ,
+                                                        uint32_t *final_count)
+{
+    const int64_t T = (n + kChunk - 1) / kChunk;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= T)
+        return;
+    const int64_t s0 = t * kChunk;
+    const int m = (n - s0 < kChunk) ? static_cast<int>(n - s0) : kChunk;
+    uint4 op[kChunk];
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k)
+        op[k] = (k < m) ? ops[s0 + k] : make_uint4(2u, 0u, 0u, 0u);
+    int first = -1;
+#pragma unroll
+    for (int k = kChunk - 1; k >= 0; --k)
+        if (k < m && is_set_record(op[k]))
+            first = k;
+    if (first < 0) {
+        summ[t] = make_uint2(0u, 0u);
+        return;
+    }
+    uint32_t c = 0;
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+        if (k >= first && k < m) {
+            uint32_t o;
+            c = sm_apply(c, op[k], &o);
+            trace[s0 + k] = make_uint2(c, o);
+        }
+    }
+    summ[t] = make_uint2(1u, c);
+    if (t == T - 1)
+        *final_count = c;
+}
+
+__global__ void __launch_bounds__(256) sm_prefix_kernel(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace,
+                                                        const uint2 *summ, uint32_t *final_count)
+{
+    const int64_t T = (n + kChunk - 1) / kChunk;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= T)
+        return;
+    uint32_t c;
+    if (t == 0) {
+        c = init;
+    } else {
+        const uint2 prev = summ[t - 1];
+        if (!prev.x)
+            return;   // an earlier chain runs through this chunk
+        c = prev.y;
+    }
+    for (int64_t i = t * kChunk; i < n; ++i) {
+        const uint4 op = ops[i];
+        if (is_set_record(op))
+            return;   // the suffix kernel traced from here on
+        uint32_t o;
+        c = sm_apply(c, op, &o);
+        trace[i] = make_uint2(c, o);
+    }
+    *final_count = c;   // no SET after the chain start: this chain ends the stream
+}
+
+__global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
+
+// ---------------------------------------------------------------------------
+// Two-stream pipeline kernels
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) pipeline_producer_kernel(uint32_t *tiles, int64_t n_tiles, int tile_words,
+                                                                uint32_t round, uint32_t *done)
+{
+    const int q = tile_words >> 2;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        uint4 *d = reinterpret_cast<uint4 *>(tiles + t * tile_words);
+        const uint32_t w0 = static_cast<uint32_t>(t * tile_words);
+        for (int i = threadIdx.x; i < q; i += blockDim.x) {
+            const uint32_t w = w0 + 4u * i;
+            d[i] = make_uint4(w * 2654435761u + round, (w + 1u) * 2654435761u + round,
+                              (w + 2u) * 2654435761u + round, (w + 3u) * 2654435761u + round);
+        }
+        __syncthreads();   // the whole tile is stored ...
+        if (threadIdx.x == 0)
+            cnt_record_device(done, CNS_REC_ADD, 1u);   // ... before it is counted (release)
+    }
+}
+
+__global__ void __launch_bounds__(256) pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words,
+                                                                uint32_t *checksum)
+{
+    const uint4 *t4 = reinterpret_cast<const uint4 *>(tiles);
+    uint32_t s = 0;
+    const int64_t n4 = n_words >> 2;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint4 v = t4[i];
+        s += v.x + v.y + v.z + v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31u) == 0u)
+        atomicAdd(checksum, s);
+}
+
+}  // namespace cns
+
+using namespace cns;
+
+// ---------------------------------------------------------------------------
+// Handle lifecycle
+// ---------------------------------------------------------------------------
+
+extern "C" int cntnotify_create(cns_cnt_notify_t *out, uint64_t flag)
+{
+    if (!out)
+        return CNS_ERR_NULL_PTR;
+    if (flag != 0)
+        return CNS_ERR_INVALID_VALUE;   // [CNTN] §4.1: flag is reserved and must be 0
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    Pool &pool = g_pools[dev.device];
+    if (!pool.base) {
+        const uint32_t cap = pool_cap();
+        void *p = nullptr;
+        CNS_CUDA(cudaMalloc(&p, static_cast<size_t>(cap) * kWordsPerSlot * 4));
+        CNS_CUDA(cudaMemset(p, 0, static_cast<size_t>(cap) * kWordsPerSlot * 4));
+        pool.base = static_cast<uint32_t *>(p);
+        pool.cap = cap;
+        pool.free_slots.reserve(cap);
+        for (uint32_t i = cap; i-- > 0;)
+            pool.free_slots.push_back(i);
+    }
+    if (pool.free_slots.empty()) {
+        CNS_LOG(1, "too many counted notifies (pool of %u)", pool.cap);
+        return CNS_ERR_RESOURCE;
+    }
+    const uint32_t slot = pool.free_slots.back();
+    uint32_t *line = pool.base + static_cast<size_t>(slot) * kWordsPerSlot;
+    // a fresh notify starts at count 0 with a clear status
+    CNS_CUDA(cudaMemset(line, 0, kWordsPerSlot * 4));
+    pool.free_slots.pop_back();
+    auto *h = new cns_cnt_notify_s{kMagic, dev.device, slot, line};
+    g_live.insert(h);
+    *out = h;
+    return CNS_SUCCESS;
+}
+
+extern "C" int cntnotify_destroy(cns_cnt_notify_t h)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = h ? g_live.find(h) : g_live.end();
+    if (it == g_live.end())
+        return CNS_ERR_INVALID_HANDLE;
+    g_live.erase(it);
+    g_pools[h->device].free_slots.push_back(h->slot);
+    h->magic = 0;
+    delete h;
+    return CNS_SUCCESS;
+}
+
+extern "C" int cntnotify_get_id(cns_cnt_notify_t h, uint32_t *id)
+{
+    cns_cnt_notify_s *n = lookup(h);
+    if (!n)
+        return CNS_ERR_INVALID_HANDLE;
+    if (!id)
+        return CNS_ERR_NULL_PTR;
+    *id = (static_cast<uint32_t>(n->device) << 24) | n->slot;
+    return CNS_SUCCESS;
+}
+
+extern "C" int cntnotify_get_device_ptr(cns_cnt_notify_t h, uint32_t **count_dev)
+{
+    cns_cnt_notify_s *n = lookup(h);
+    if (!n)
+        return CNS_ERR_INVALID_HANDLE;
+    if (!count_dev)
+        return CNS_ERR_NULL_PTR;
+    *count_dev = n->line;
+    return CNS_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Stream-ordered operations
+// ---------------------------------------------------------------------------
+
+extern "C" int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const cns_record_info_t *info)
+{
+    cns_cnt_notify_s *n = lookup(h);
+    if (!n)
+        return CNS_ERR_INVALID_HANDLE;
+    if (!info)
+        return CNS_ERR_NULL_PTR;
+    if (!record_mode_ok(info->mode))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceGuard g;
+    if (int rc = g.set(n->device))
+        return rc;
+    cnt_record_kernel<<<1, 32, 0, to_stream(stream)>>>(n->line, static_cast<uint32_t>(info->mode), info->value);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+extern "C" int cntnotify_wait_with_timeout(cns_cnt_notify_t h, cns_stream_t stream, const cns_wait_info_t *info)
+{
+    cns_cnt_notify_s *n = lookup(h);
+    if (!n)
+        return CNS_ERR_INVALID_HANDLE;
+    if (!info)
+        return CNS_ERR_NULL_PTR;
+    if (info->mode < CNS_WAIT_LESS || info->mode > CNS_WAIT_EQUAL_WITH_BITMASK)
+        return CNS_ERR_INVALID_VALUE;
+    DeviceGuard g;
+    if (int rc = g.set(n->device))
+        return rc;
+    return enqueue_wait(n, to_stream(stream), info, nullptr);
+}
+
+extern "C" int cntnotify_reset(cns_cnt_notify_t h, cns_stream_t stream)
+{
+    cns_cnt_notify_s *n = lookup(h);
+    if (!n)
+        return CNS_ERR_INVALID_HANDLE;
+    DeviceGuard g;
+    if (int rc = g.set(n->device))
+        return rc;
+    cnt_record_kernel<<<1, 32, 0, to_stream(stream)>>>(n->line, CNS_REC_SET, 0u);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+extern "C" int cntnotify_query_status(cns_cnt_notify_t h, int32_t *status, uint32_t *count)
+{
+    cns_cnt_notify_s *n = lookup(h);
+    if (!n)
+        return CNS_ERR_INVALID_HANDLE;
+    if (!status)
+        return CNS_ERR_NULL_PTR;
+    DeviceGuard g;
+    if (int rc = g.set(n->device))
+        return rc;
+    // a private non-blocking stream: reads the words as they are now, without
+    // waiting for work on other streams
+    cudaStream_t s;
+    CNS_CUDA(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    uint32_t w[2] = {0, 0};
+    cudaError_t e = cudaMemcpyAsync(w, n->line, sizeof(w), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    cudaStreamDestroy(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cntnotify_query_status");
+    *status = static_cast<int32_t>(w[1]);
+    if (count)
+        *count = w[0];
+    return CNS_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// State machine
+// ---------------------------------------------------------------------------
+
+extern "C" size_t cns_statemachine_scratch_bytes(int64_t n)
+{
+    if (n <= 0)
+        return 0;
+    return static_cast<size_t>((n + kChunk - 1) / kChunk) * sizeof(uint2);
+}
+
+extern "C" int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t init, uint32_t *trace_dev,
+                                    uint32_t *final_dev, void *scratch_dev, size_t scratch_bytes,
+                                    cns_stream_t stream)
+{
+    if (n < 0)
+        return CNS_ERR_INVALID_VALUE;
+    if (!final_dev)
+        return CNS_ERR_NULL_PTR;
+    if (n > 0 && (!ops_dev || !trace_dev || !scratch_dev))
+        return CNS_ERR_NULL_PTR;
+    if ((reinterpret_cast<uintptr_t>(ops_dev) & 15) || (reinterpret_cast<uintptr_t>(trace_dev) & 7) ||
+        (reinterpret_cast<uintptr_t>(scratch_dev) & 7))
+        return CNS_ERR_INVALID_VALUE;
+    if (scratch_bytes < cns_statemachine_scratch_bytes(n))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    cudaStream_t s = to_stream(stream);
+    if (n == 0) {
+        write_word_kernel<<<1, 1, 0, s>>>(final_dev, init);
+        CNS_CUDA(cudaGetLastError());
+        return CNS_SUCCESS;
+    }
+    const int64_t T = (n + kChunk - 1) / kChunk;
+    const int threads = 256;
+    const int64_t blocks = (T + threads - 1) / threads;
+    if (blocks > 0x7fffffff)
+        return CNS_ERR_INVALID_VALUE;
+    const uint4 *ops = reinterpret_cast<const uint4 *>(ops_dev);
+    uint2 *trace = reinterpret_cast<uint2 *>(trace_dev);
+    uint2 *summ = static_cast<uint2 *>(scratch_dev);
+    sm_suffix_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(ops, n, trace, summ, final_dev);
+    CNS_CUDA(cudaGetLastError());
+    sm_prefix_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(ops, n, init, trace, summ, final_dev);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Two-stream pipeline
+// ---------------------------------------------------------------------------
+
+extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
+{
+    if (!cfg)
+        return CNS_ERR_NULL_PTR;
+    cns_cnt_notify_s *done = lookup(cfg->done);
+    cns_cnt_notify_s *ack = lookup(cfg->ack);
+    if (!done || !ack || done == ack)
+        return CNS_ERR_INVALID_HANDLE;
+    if (!cfg->tiles_dev || !cfg->checksums_dev)
+        return CNS_ERR_NULL_PTR;
+    if (cfg->tiles < 1 || cfg->rounds < 0 || cfg->tile_words < 4 || cfg->tile_words > 8192 ||
+        cfg->tile_words % 4 != 0 || cfg->producer_ctas < 0 || cfg->tiles > (int64_t(1) << 32) / cfg->tile_words)
+        return CNS_ERR_INVALID_VALUE;
+    if (reinterpret_cast<uintptr_t>(cfg->tiles_dev) & 15)
+        return CNS_ERR_INVALID_VALUE;
+    if (done->device != ack->device)
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    if (dev.device != done->device)
+        return CNS_ERR_INVALID_VALUE;
+    cudaStream_t sp = to_stream(cfg->producer_stream), sc = to_stream(cfg->consumer_stream);
+    const int pgrid = cfg->producer_ctas ? cfg->producer_ctas : 4 * dev.sm_count;
+    const int64_t n_words = cfg->tiles * cfg->tile_words;
+    const int cgrid = static_cast<int>(std::min<int64_t>(2 * dev.sm_count, (n_words / 4 + 255) / 256));
+
+    std::vector<cudaEvent_t> ev;
+    auto cleanup = [&] {
+        for (cudaEvent_t e : ev)
+            cudaEventDestroy(e);
+    };
+    cudaEvent_t join;
+    CNS_CUDA(cudaEventCreateWithFlags(&join, cudaEventDisableTiming));
+    ev.push_back(join);
+    const bool timed = cfg->sync != 0;
+    const int64_t n_ev = timed ? 2 * cfg->rounds + 2 : 0;
+    for (int64_t i = 0; i < n_ev; ++i) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            cleanup();
+            return CNS_ERR_CUDA;
+        }
+        ev.push_back(e);
+    }
+    auto T = [&](int64_t i) { return ev[1 + i]; };   // timing events
+    int rc = CNS_SUCCESS;
+    auto check = [&](cudaError_t e, const char *what) {
+        if (e != cudaSuccess && rc == CNS_SUCCESS)
+            rc = cuda_fail(e, what);
+        return e == cudaSuccess;
+    };
+
+    // start state: both counts and statuses 0, checksums 0, then let the
+    // consumer stream follow.  Word 2 of `done` is the pipeline's abort word.
+    uint32_t *abort = done->line + 2;
+    cnt_clear_line_kernel<<<1, 32, 0, sp>>>(done->line);
+    cnt_clear_line_kernel<<<1, 32, 0, sp>>>(ack->line);
+    check(cudaMemsetAsync(cfg->checksums_dev, 0, cfg->rounds * sizeof(uint32_t), sp), "memset checksums");
+    if (cfg->released_dev)
+        check(cudaMemsetAsync(cfg->released_dev, 0, cfg->rounds * sizeof(uint32_t), sp), "memset released");
+    check(cudaEventRecord(join, sp), "event");
+    check(cudaStreamWaitEvent(sc, join, 0), "stream wait");
+    if (timed)
+        check(cudaEventRecord(T(2 * cfg->rounds), sp), "event");
+
+    cns_wait_info_t w_done = {CNS_WAIT_BIGGER_OR_EQUAL, static_cast<uint32_t>(cfg->tiles), cfg->timeout_s, 1, {0, 0, 0}};
+    cns_wait_info_t w_ack = {CNS_WAIT_EQUAL, 1u, cfg->timeout_s, 1, {0, 0, 0}};
+    for (int64_t r = 0; r < cfg->rounds && rc == CNS_SUCCESS; ++r) {
+        if (timed)
+            check(cudaEventRecord(T(2 * r), sp), "event");
+        pipeline_producer_kernel<<<pgrid, 256, 0, sp>>>(cfg->tiles_dev, cfg->tiles, cfg->tile_words,
+                                                        static_cast<uint32_t>(r), done->line);
+        check(cudaGetLastError(), "producer launch");
+        if (timed)
+            check(cudaEventRecord(T(2 * r + 1), sp), "event");
+        if (int e = enqueue_wait(ack, sp, &w_ack, nullptr, abort))
+            rc = e;
+        if (int e = enqueue_wait(done, sc, &w_done, cfg->released_dev ? cfg->released_dev + r : nullptr, abort))
+            rc = e;
+        pipeline_consumer_kernel<<<cgrid, 256, 0, sc>>>(cfg->tiles_dev, n_words, cfg->checksums_dev + r);
+        check(cudaGetLastError(), "consumer launch");
+        cnt_record_kernel<<<1, 32, 0, sc>>>(ack->line, CNS_REC_SET, 1u);
+        check(cudaGetLastError(), "ack record");
+    }
+    check(cudaEventRecord(join, sc), "event");
+    check(cudaStreamWaitEvent(sp, join, 0), "stream wait");
+    if (timed)
+        check(cudaEventRecord(T(2 * cfg->rounds + 1), sp), "event");
+    if (rc != CNS_SUCCESS || !timed) {
+        cleanup();
+        return rc;
+    }
+    if (!check(cudaEventSynchronize(T(2 * cfg->rounds + 1)), "sync")) {
+        cleanup();
+        return rc;
+    }
+    float total = 0.f, prod = 0.f;
+    check(cudaEventElapsedTime(&total, T(2 * cfg->rounds), T(2 * cfg->rounds + 1)), "elapsed");
+    for (int64_t r = 0; r < cfg->rounds; ++r) {
+        float ms = 0.f;
+        check(cudaEventElapsedTime(&ms, T(2 * r), T(2 * r + 1)), "elapsed");
+        prod += ms;
+    }
+    cleanup();
+    cfg->elapsed_ms = total;
+    cfg->producer_ms = prod;
+    int32_t st_done = 0, st_ack = 0;
+    if (int e = cntnotify_query_status(cfg->done, &st_done, nullptr))
+        return e;
+    if (int e = cntnotify_query_status(cfg->ack, &st_ack, nullptr))
+        return e;
+    cfg->device_status = (st_done || st_ack) ? CNS_ERR_TIMEOUT : 0;
+    return rc != CNS_SUCCESS ? rc : (cfg->device_status ? CNS_ERR_TIMEOUT : CNS_SUCCESS);
+}

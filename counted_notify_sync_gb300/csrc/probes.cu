@@ -1,0 +1,85 @@
+// probes.cu -- latency and throughput probes that give the barrier its
+// roofline: the round trip of one L2 atomic (and of one load, and of the
+// arrive/poll pair) from a single thread, and the rate at which the L2 can
+// apply same-address reductions.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cns.h"
+#include "cns_device.cuh"
+#include "cns_host.h"
+
+namespace cns {
+
+// A chain of `iters` operations where each address depends on the previous
+// result (the count stays below 2^31, so the offset is always 0): nothing
+// can overlap, each link costs one round trip.
+__global__ void probe_rtt_kernel(int kind, int probe_cta, int iters, uint32_t *line, uint64_t *out)
+{
+    if (static_cast<int>(blockIdx.x) != probe_cta || threadIdx.x != 0)
+        return;
+    uint32_t x = 0;
+    // one untimed link brings the line into L2
+    x = atom_add_relaxed_gpu(line, 0u);
+    const uint64_t t0 = globaltimer_ns();
+    for (int i = 0; i < iters; ++i) {
+        uint32_t *p = line + (x >> 31);
+        if (kind == 0) {
+            x = atom_add_relaxed_gpu(p, 1u);
+        } else if (kind == 1) {
+            x = ld_relaxed_gpu(p);
+        } else {
+            x = atom_add_release_gpu(p, 1u);
+            x = ld_acquire_gpu(line + (x >> 31));
+        }
+    }
+    const uint64_t t1 = globaltimer_ns();
+    out[0] = t1 - t0;
+    out[1] = smid() | (static_cast<uint64_t>(x & 0u) << 32);
+}
+
+__global__ void probe_red_kernel(int iters, uint32_t *word)
+{
+    for (int i = 0; i < iters; ++i)
+        red_add_relaxed_gpu(word, 1u);
+}
+
+}  // namespace cns
+
+using namespace cns;
+
+extern "C" int cns_probe_atomic_rtt(int kind, int32_t grid, int32_t probe_cta, int32_t iters, uint32_t *line_dev,
+                                    uint64_t *out_dev, cns_stream_t stream)
+{
+    if (!line_dev || !out_dev)
+        return CNS_ERR_NULL_PTR;
+    if (kind < 0 || kind > 2 || grid < 1 || grid > (1 << 20) || probe_cta < 0 || probe_cta >= grid || iters < 1 ||
+        iters > (1 << 24))
+        return CNS_ERR_INVALID_VALUE;
+    if (reinterpret_cast<uintptr_t>(line_dev) & (CNS_SYNCALL_LINE_BYTES - 1))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    cudaStream_t s = to_stream(stream);
+    CNS_CUDA(cudaMemsetAsync(line_dev, 0, CNS_SYNCALL_LINE_BYTES, s));
+    probe_rtt_kernel<<<grid, 32, 0, s>>>(kind, probe_cta, iters, line_dev, out_dev);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+extern "C" int cns_probe_same_address_throughput(int32_t grid, int32_t threads, int32_t iters, uint32_t *word_dev,
+                                                 cns_stream_t stream)
+{
+    if (!word_dev)
+        return CNS_ERR_NULL_PTR;
+    if (grid < 1 || grid > (1 << 20) || threads < 32 || threads > 1024 || threads % 32 || iters < 1)
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    probe_red_kernel<<<grid, threads, 0, to_stream(stream)>>>(iters, word_dev);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}

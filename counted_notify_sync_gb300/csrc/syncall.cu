@@ -1,0 +1,475 @@
+// syncall.cu -- the persistent multi-round SYNCALL kernel and its host entry
+// points (syncall_workspace_init, syncall_run, syncall_read_workspace).
+//
+// One launch runs R rounds of { data phase; barrier }.  The barrier is the
+// soft-mode epoch barrier of the "PTO-ISA SYNCALL cross-core barrier guide"
+// (§5.2: arrive with an atomic increment that returns `before`, target =
+// (before / P + 1) * P, poll until reached) or its hard counterpart built on
+// thread-block clusters (§5.1's two-level shape: the group synchronises
+// locally, one member takes part in the device-wide step, then releases the
+// group).  Participants are CTAs; see cns.h for the role classes (§3.1) and
+// the participant count (§4.2).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "cns.h"
+#include "cns_device.cuh"
+#include "cns_host.h"
+
+namespace cns {
+
+struct SyncallParams {
+    void *buf0;
+    void *buf1;
+    int64_t elems;          // ring: slots per participant; Jacobi: field length
+    int64_t rounds;
+    uint32_t *ctr;          // the counter this path arrives on
+    uint32_t *status_line;  // workspace line 1
+    int32_t *cta_status;    // optional per-CTA marks
+    uint64_t timeout_ns;
+    Epoch epoch;            // P and bound of `ctr`
+    uint32_t P;             // participants (ring length / Jacobi chunks)
+    uint32_t group;         // MIX group size, else 1
+    int32_t core_type;
+};
+
+// ---------------------------------------------------------------------------
+// Data phases
+// ---------------------------------------------------------------------------
+
+template <int WL>
+__device__ __forceinline__ uint32_t ring_op(uint32_t x, uint32_t r)
+{
+    if (WL == CNS_WL_RING_AFFINE)
+        return x * 3u + r;
+    if (WL == CNS_WL_XORSHIFT) {
+        // Marsaglia's xorshift32 step, shifts (13, 17, 5), then the round index
+        x ^= x << 13;
+        x ^= x >> 17;
+        x ^= x << 5;
+        return x ^ r;
+    }
+    return x;   // ring rotate
+}
+
+// Participant p writes its own row of dst from row (p + 1) mod P of src.
+template <int WL>
+__device__ __forceinline__ void ring_phase(const uint32_t *src, uint32_t *dst, uint32_t p, uint32_t P,
+                                           int64_t elems, uint32_t r)
+{
+    const uint32_t q = (p + 1u == P) ? 0u : p + 1u;
+    const uint32_t *s = src + static_cast<int64_t>(q) * elems;
+    uint32_t *d = dst + static_cast<int64_t>(p) * elems;
+    if ((elems & 3) == 0) {
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(s);
+        uint4 *d4 = reinterpret_cast<uint4 *>(d);
+        const int64_t n4 = elems >> 2;
+        for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+            uint4 v = s4[i];
+            v.x = ring_op<WL>(v.x, r);
+            v.y = ring_op<WL>(v.y, r);
+            v.z = ring_op<WL>(v.z, r);
+            v.w = ring_op<WL>(v.w, r);
+            d4[i] = v;
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < elems; i += blockDim.x)
+            d[i] = ring_op<WL>(s[i], r);
+    }
+}
+
+// One Jacobi sweep over participant p's chunk of the field:
+// u'[i] = (u[i-1] + u[i+1]) * 0.5f for interior points, ends copied.
+// The field is cut into N/4 float4 columns shared out as evenly as possible;
+// neighbouring float4s inside a warp trade their edge values by shuffle, and
+// the two values beyond a warp's span come from global memory.  The scalar
+// tail (N mod 4 points) belongs to the last participant.
+__device__ __forceinline__ void jacobi_phase(const float *src, float *dst, int64_t N, uint32_t p, uint32_t P)
+{
+    const int64_t N4 = N >> 2;
+    const int64_t base = N4 / P, rem = N4 % P;
+    const int64_t j0 = static_cast<int64_t>(p) * base + (p < rem ? p : rem);
+    const int64_t j1 = j0 + base + (p < rem ? 1 : 0);
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    const uint32_t lane = threadIdx.x & 31u;
+    const int64_t stride = blockDim.x;
+    constexpr int U = 4;
+    for (int64_t it = j0; it < j1; it += U * stride) {   // uniform trip count across the CTA
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t j = it + u * stride + threadIdx.x;
+            v[u] = (j < j1) ? s4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t j = it + u * stride + threadIdx.x;
+            float lw = __shfl_up_sync(0xffffffffu, v[u].w, 1);
+            float rx = __shfl_down_sync(0xffffffffu, v[u].x, 1);
+            if (j < j1) {
+                if (lane == 0)
+                    lw = (j > 0) ? src[4 * j - 1] : 0.f;
+                if (lane == 31 || j + 1 >= j1)
+                    rx = (4 * j + 4 < N) ? src[4 * j + 4] : 0.f;
+                float4 o;
+                o.x = (j == 0) ? v[u].x : (lw + v[u].y) * 0.5f;
+                o.y = (v[u].x + v[u].z) * 0.5f;
+                o.z = (v[u].y + v[u].w) * 0.5f;
+                o.w = (4 * j + 3 == N - 1) ? v[u].w : (v[u].z + rx) * 0.5f;
+                d4[j] = o;
+            }
+        }
+    }
+    if (p == P - 1) {
+        for (int64_t i = 4 * N4 + threadIdx.x; i < N; i += stride)
+            dst[i] = (i == 0 || i == N - 1) ? src[i] : (src[i - 1] + src[i + 1]) * 0.5f;
+    }
+}
+
+template <int WL>
+__device__ __forceinline__ void data_phase(const SyncallParams &p, int64_t r, uint32_t part)
+{
+    if (WL == CNS_WL_EMPTY)
+        return;
+    const bool odd = (r & 1) != 0;
+    void *src = odd ? p.buf1 : p.buf0;
+    void *dst = odd ? p.buf0 : p.buf1;
+    if (WL == CNS_WL_JACOBI)
+        jacobi_phase(static_cast<const float *>(src), static_cast<float *>(dst), p.elems, part, p.P);
+    else
+        ring_phase<WL>(static_cast<const uint32_t *>(src), static_cast<uint32_t *>(dst), part, p.P, p.elems,
+                       static_cast<uint32_t>(r));
+}
+
+// ---------------------------------------------------------------------------
+// The persistent kernel
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cta_role(const SyncallParams &p, uint32_t b)
+{
+    if (p.core_type == CNS_MIX)
+        return (b % p.group == 0) ? 1u : 0u;   // group rank 0 plays the AIC part
+    return p.core_type == CNS_AIC_ONLY ? 1u : 0u;
+}
+
+template <int MODE, int WL>
+__global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
+{
+    __shared__ int s_flag;
+    const uint32_t b = blockIdx.x;
+    const uint32_t role = cta_role(p, b);
+    if (MODE == CNS_SYNCALL_SOFT && b >= p.P) {
+        // not a participant: never touches the counter ([SYNCALL] §4.2, §7.2)
+        if (threadIdx.x == 0 && p.cta_status)
+            p.cta_status[b] = static_cast<int32_t>(CNS_CTA_IDLE | (role << 8));
+        return;
+    }
+    if (threadIdx.x == 0)
+        s_flag = 0;
+    if (MODE == CNS_SYNCALL_HARD) {
+        __syncwarp();
+        cluster_sync_all();   // every CTA's flag is initialised before anyone may write it
+    } else {
+        __syncthreads();
+    }
+
+    bool stop = false;
+    for (int64_t r = 0; r < p.rounds; ++r) {
+        data_phase<WL>(p, r, b);
+        stop = (MODE == CNS_SYNCALL_SOFT)
+                   ? soft_barrier(p.ctr, p.epoch, p.status_line, p.timeout_ns, static_cast<uint32_t>(r), &s_flag)
+                   : hard_barrier(p.ctr, p.epoch, p.status_line, p.timeout_ns, static_cast<uint32_t>(r), &s_flag);
+        if (stop)
+            break;
+    }
+    if (threadIdx.x == 0 && p.cta_status)
+        p.cta_status[b] = static_cast<int32_t>((stop ? CNS_CTA_ABORTED : CNS_CTA_DONE) | (role << 8));
+}
+
+__global__ void workspace_init_kernel(uint32_t *ws, uint32_t n_words, uint32_t start)
+{
+    for (uint32_t i = threadIdx.x; i < n_words; i += blockDim.x)
+        ws[i] = 0u;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ws[0] = start;                                  // soft counter
+        ws[2 * CNS_SYNCALL_LINE_BYTES / 4] = start;     // hard counter
+    }
+}
+
+using KernelFn = void (*)(const SyncallParams);
+
+static KernelFn pick_kernel(int mode, int wl)
+{
+    static const KernelFn soft[5] = {syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_EMPTY>,
+                                     syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_RING_AFFINE>,
+                                     syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_RING_ROTATE>,
+                                     syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_XORSHIFT>,
+                                     syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_JACOBI>};
+    static const KernelFn hard[5] = {syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_EMPTY>,
+                                     syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_RING_AFFINE>,
+                                     syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_RING_ROTATE>,
+                                     syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_XORSHIFT>,
+                                     syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_JACOBI>};
+    return mode == CNS_SYNCALL_SOFT ? soft[wl] : hard[wl];
+}
+
+// Can `grid` CTAs (in clusters of C when C > 0) be resident at once?
+static int fits(KernelFn k, int grid, int threads, int C, cudaStream_t s, const DeviceInfo &dev, bool *ok)
+{
+    if (C <= 0) {
+        int per_sm = 0;
+        CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void *>(k), threads, 0));
+        *ok = static_cast<int64_t>(per_sm) * dev.sm_count >= grid;
+        return CNS_SUCCESS;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = C;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void *>(k), &cfg);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        *ok = false;
+        return CNS_SUCCESS;
+    }
+    *ok = static_cast<int64_t>(n) * C >= grid;
+    return CNS_SUCCESS;
+}
+
+static bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Two timing events, destroyed on every exit path.
+struct EventPair {
+    cudaEvent_t a = nullptr, b = nullptr;
+    ~EventPair()
+    {
+        if (a)
+            cudaEventDestroy(a);
+        if (b)
+            cudaEventDestroy(b);
+    }
+};
+
+}  // namespace cns
+
+using namespace cns;
+
+extern "C" int syncall_workspace_init(void *ws_dev, size_t bytes, uint32_t start_value, cns_stream_t stream)
+{
+    if (!ws_dev)
+        return CNS_ERR_NULL_PTR;
+    if (bytes < CNS_SYNCALL_WORKSPACE_BYTES || !aligned(ws_dev, CNS_SYNCALL_LINE_BYTES))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    workspace_init_kernel<<<1, 128, 0, to_stream(stream)>>>(static_cast<uint32_t *>(ws_dev),
+                                                             CNS_SYNCALL_WORKSPACE_BYTES / 4, start_value);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+extern "C" int syncall_read_workspace(const void *ws_dev, cns_stream_t stream, uint32_t *soft_counter,
+                                      uint32_t *hard_counter, int32_t *status)
+{
+    if (!ws_dev)
+        return CNS_ERR_NULL_PTR;
+    uint32_t w[CNS_SYNCALL_WORKSPACE_BYTES / 4];
+    CNS_CUDA(cudaStreamSynchronize(to_stream(stream)));
+    CNS_CUDA(cudaMemcpy(w, ws_dev, sizeof(w), cudaMemcpyDeviceToHost));
+    if (soft_counter)
+        *soft_counter = w[0];
+    if (status)
+        *status = static_cast<int32_t>(w[CNS_SYNCALL_LINE_BYTES / 4]);
+    if (hard_counter)
+        *hard_counter = w[2 * CNS_SYNCALL_LINE_BYTES / 4];
+    return CNS_SUCCESS;
+}
+
+extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t aiv_ratio, int64_t rounds,
+                           cns_syncall_data_t *d)
+{
+    // ---- argument checks (no CUDA call before these) ----
+    if (!d)
+        return CNS_ERR_NULL_PTR;
+    if (mode != CNS_SYNCALL_SOFT && mode != CNS_SYNCALL_HARD)
+        return CNS_ERR_INVALID_VALUE;
+    if (core_type < CNS_AIV_ONLY || core_type > CNS_MIX)
+        return CNS_ERR_INVALID_VALUE;
+    if (d->workload < CNS_WL_EMPTY || d->workload > CNS_WL_JACOBI)
+        return CNS_ERR_INVALID_VALUE;
+    if (rounds < 0 || used_cores < 0 || aiv_ratio < 0 || d->launch_ctas <= 0 || d->elems < 0)
+        return CNS_ERR_INVALID_VALUE;
+    const int threads = d->threads ? d->threads : 256;
+    if (threads < 32 || threads > 1024 || threads % 32 != 0)
+        return CNS_ERR_INVALID_VALUE;
+    const int ratio = core_type == CNS_MIX ? (aiv_ratio ? aiv_ratio : 1) : 0;
+    const int64_t group = core_type == CNS_MIX ? 1 + ratio : 1;
+    const int64_t grid64 = static_cast<int64_t>(d->launch_ctas) * group;
+    if (grid64 > (1 << 24))
+        return CNS_ERR_INVALID_VALUE;
+    const int grid = static_cast<int>(grid64);
+    if (used_cores > grid)
+        return CNS_ERR_INVALID_VALUE;   // [SYNCALL] §6.3: the set must match the launch
+    const uint32_t P = (mode == CNS_SYNCALL_HARD) ? grid : (used_cores ? used_cores : grid);
+    if (!d->workspace_dev)
+        return CNS_ERR_NULL_PTR;
+    if (!aligned(d->workspace_dev, CNS_SYNCALL_LINE_BYTES))
+        return CNS_ERR_INVALID_VALUE;
+    const bool has_payload = d->workload != CNS_WL_EMPTY && d->elems > 0;
+    if (has_payload && (!d->buf0_dev || !d->buf1_dev))
+        return CNS_ERR_NULL_PTR;
+    if (has_payload && (!aligned(d->buf0_dev, 16) || !aligned(d->buf1_dev, 16)))
+        return CNS_ERR_INVALID_VALUE;
+    int C = 1;
+    if (mode == CNS_SYNCALL_HARD) {
+        if (core_type == CNS_MIX) {
+            if (group > 8)
+                return CNS_ERR_INVALID_VALUE;
+            C = static_cast<int>(group);
+        } else if (d->cluster_dim != 0) {
+            if (d->cluster_dim < 1 || d->cluster_dim > 8 || grid % d->cluster_dim != 0)
+                return CNS_ERR_INVALID_VALUE;
+            C = d->cluster_dim;
+        } else {
+            C = 0;   // choose below
+        }
+    }
+    const int64_t payload_bytes = !has_payload ? 0
+                                  : d->workload == CNS_WL_JACOBI ? d->elems * 4
+                                                                 : static_cast<int64_t>(P) * d->elems * 4;
+    if ((d->host_in || d->host_out) && !has_payload)
+        return CNS_ERR_INVALID_VALUE;
+
+    // ---- device ----
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    cudaStream_t s = to_stream(d->stream);
+    KernelFn k = pick_kernel(mode, d->workload);
+    bool ok = false;
+    if (mode == CNS_SYNCALL_HARD && C == 0) {
+        for (int c : {4, 2, 1}) {
+            if (grid % c != 0)
+                continue;
+            if (int rc = fits(k, grid, threads, c, s, dev, &ok))
+                return rc;
+            if (ok) {
+                C = c;
+                break;
+            }
+        }
+        if (!ok)
+            return CNS_ERR_NOT_RESIDENT;
+    } else {
+        if (int rc = fits(k, grid, threads, mode == CNS_SYNCALL_HARD ? C : 0, s, dev, &ok))
+            return rc;
+        if (!ok)
+            return CNS_ERR_NOT_RESIDENT;
+    }
+
+    SyncallParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.buf0 = d->buf0_dev;
+    prm.buf1 = d->buf1_dev;
+    prm.elems = d->elems;
+    prm.rounds = rounds;
+    uint32_t *ws = static_cast<uint32_t *>(d->workspace_dev);
+    prm.status_line = ws + CNS_SYNCALL_LINE_BYTES / 4;
+    prm.cta_status = d->cta_status_dev;
+    prm.timeout_ns = barrier_timeout_ns(d->timeout_ms);
+    prm.P = P;
+    prm.group = static_cast<uint32_t>(group);
+    prm.core_type = core_type;
+    if (mode == CNS_SYNCALL_SOFT) {
+        prm.ctr = ws;
+        prm.epoch.P = P;
+    } else {
+        prm.ctr = ws + 2 * CNS_SYNCALL_LINE_BYTES / 4;
+        prm.epoch.P = static_cast<uint32_t>(grid / C);
+    }
+    prm.epoch.Mm1 = counter_bound(prm.epoch.P);
+
+    d->grid_ctas = grid;
+    d->participants = static_cast<int32_t>(P);
+    d->cluster_used = mode == CNS_SYNCALL_HARD ? C : 1;
+
+    EventPair ev;
+    if (d->sync) {
+        CNS_CUDA(cudaEventCreate(&ev.a));
+        CNS_CUDA(cudaEventCreate(&ev.b));
+        CNS_CUDA(cudaEventRecord(ev.a, s));
+    }
+    if (d->host_in)
+        CNS_CUDA(cudaMemcpyAsync(d->buf0_dev, d->host_in, payload_bytes, cudaMemcpyHostToDevice, s));
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeCooperative;
+    attrs[na].val.cooperative = 1;
+    ++na;
+    if (mode == CNS_SYNCALL_HARD) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = C;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    void *args[] = {&prm};
+    cudaError_t le = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(k), args);
+    if (le == cudaErrorCooperativeLaunchTooLarge) {
+        (void)cudaGetLastError();
+        return CNS_ERR_NOT_RESIDENT;
+    }
+    if (le != cudaSuccess && mode == CNS_SYNCALL_HARD) {
+        // the cooperative attribute together with clusters may be refused;
+        // residency was checked above, so launch without it
+        CNS_LOG(1, "cooperative cluster launch refused (%s); launching without it", cudaGetErrorString(le));
+        (void)cudaGetLastError();
+        cfg.attrs = attrs + 1;
+        cfg.numAttrs = 1;
+        le = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(k), args);
+    }
+    if (le != cudaSuccess)
+        return cuda_fail(le, "syncall launch");
+
+    if (d->host_out) {
+        void *fin = (rounds & 1) ? d->buf1_dev : d->buf0_dev;
+        CNS_CUDA(cudaMemcpyAsync(d->host_out, fin, payload_bytes, cudaMemcpyDeviceToHost, s));
+    }
+    if (!d->sync)
+        return CNS_SUCCESS;
+
+    CNS_CUDA(cudaEventRecord(ev.b, s));
+    CNS_CUDA(cudaEventSynchronize(ev.b));
+    float ms = 0.f;
+    CNS_CUDA(cudaEventElapsedTime(&ms, ev.a, ev.b));
+    d->elapsed_ms = ms;
+    uint32_t sc = 0, hc = 0;
+    int32_t st = 0;
+    if (int rc = syncall_read_workspace(d->workspace_dev, d->stream, &sc, &hc, &st))
+        return rc;
+    d->final_counter = mode == CNS_SYNCALL_SOFT ? sc : hc;
+    d->device_status = st;
+    return st == CNS_ERR_TIMEOUT ? CNS_ERR_TIMEOUT : CNS_SUCCESS;
+}

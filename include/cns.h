@@ -1,0 +1,414 @@
+/*
+ * cns.h -- C ABI of libcns: a device-wide epoch barrier (SYNCALL) and a
+ * counted notify (CntNotify) for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operations follow two public descriptions:
+ *   [SYNCALL] "PTO-ISA 跨核同步屏障 SYNCALL 实战指南" (the PTO-ISA SYNCALL
+ *             cross-core barrier guide), lmnt.cn/news/269652;
+ *   [CNTN]    "CANN Runtime CntNotify（计数型通知）管理接口详解" (the CANN
+ *             Runtime CntNotify management API), bjdmk.com.cn/news/4842886.
+ * Section numbers below are the pages' own.
+ *
+ * Conventions for every function here:
+ *   - The return value is 0 (CNS_SUCCESS) or a cns_error_t ([CNTN] §4: 0 is
+ *     success, anything else is an error code).
+ *   - Pointers named *_dev are device pointers (cudaMalloc / torch memory);
+ *     all other pointers are host pointers.  The caller owns every buffer it
+ *     passes and every stream; the library owns only its notify pool and the
+ *     notify handles.
+ *   - A cns_stream_t is a cudaStream_t passed as void*; NULL is the legacy
+ *     default stream ([CNTN] §5: "use NULL for the default stream").
+ *   - Argument and handle checks happen before any CUDA call, so they give
+ *     the documented error code on a machine without a GPU.
+ *   - The library needs a compute-capability 10.3 device; others give
+ *     CNS_ERR_ARCH ([SYNCALL] §3.3 gates SYNCALL to named back ends; [CNTN] §2
+ *     restricts CntNotify to named products).
+ *   - No device code traps or asserts.  Every device-side wait is bounded in
+ *     time; when the bound is hit the kernel records CNS_ERR_TIMEOUT in a
+ *     status word and returns.
+ */
+#ifndef CNS_H
+#define CNS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *cns_stream_t;
+
+typedef enum {
+    CNS_SUCCESS = 0,
+    CNS_ERR_INVALID_VALUE = 1,  /* bad enum, flag != 0, size or alignment ([CNTN] §4.1) */
+    CNS_ERR_NULL_PTR = 2,       /* a required pointer is NULL ([CNTN] §4.2, §4.3, §6.3) */
+    CNS_ERR_INVALID_HANDLE = 3, /* unknown or destroyed notify handle ([CNTN] §6.1) */
+    CNS_ERR_RESOURCE = 4,       /* notify pool exhausted ([CNTN] §4.1, EE1023) */
+    CNS_ERR_TIMEOUT = 5,        /* a bounded device wait ran out ([SYNCALL] §5.2, [CNTN] §3.3) */
+    CNS_ERR_NOT_RESIDENT = 6,   /* the grid cannot be co-resident ([SYNCALL] §6.3) */
+    CNS_ERR_CUDA = 7,           /* a CUDA runtime call failed (or no device) */
+    CNS_ERR_ARCH = 8            /* the device is not compute capability 10.3 */
+} cns_error_t;
+
+/* ========================================================================= */
+/* SYNCALL                                                                    */
+/* ========================================================================= */
+
+/* [SYNCALL] §3.2: Hard = hardware path, Soft = global-memory atomic counter. */
+typedef enum { CNS_SYNCALL_HARD = 0, CNS_SYNCALL_SOFT = 1 } cns_syncall_mode_t;
+
+/* [SYNCALL] §3.1: which class of cores takes part.  Here a "core" is a CTA:
+ * AIV-only and AIC-only launch `launch_ctas` CTAs of one role; MIX launches
+ * `launch_ctas` groups of 1 + aiv_ratio CTAs, rank 0 of each group in the
+ * AIC role and the others in the AIV role. */
+typedef enum { CNS_AIV_ONLY = 0, CNS_AIC_ONLY = 1, CNS_MIX = 2 } cns_core_type_t;
+
+/* Data phase run between barriers (one pass per round).  State is [P][elems]
+ * uint32 for the ring workloads (participant p owns row p) and a length-elems
+ * float32 field for Jacobi.  Round r (0-based) reads buffer r&1 and writes
+ * buffer (r+1)&1, so the final state is in buffer (rounds & 1).
+ *   RING_AFFINE  new[p][i] = old[(p+1)%P][i] * 3 + r          (mod 2^32)
+ *   RING_ROTATE  new[p][i] = old[(p+1)%P][i]
+ *   XORSHIFT     x = old[(p+1)%P][i]; x ^= x<<13; x ^= x>>17; x ^= x<<5;
+ *                new[p][i] = x ^ r
+ *   JACOBI       u'[i] = (u[i-1] + u[i+1]) * 0.5f, ends fixed; the field is
+ *                split into contiguous chunks, one per participant
+ *   EMPTY        no data phase: back-to-back barriers */
+typedef enum {
+    CNS_WL_EMPTY = 0,
+    CNS_WL_RING_AFFINE = 1,
+    CNS_WL_RING_ROTATE = 2,
+    CNS_WL_XORSHIFT = 3,
+    CNS_WL_JACOBI = 4
+} cns_workload_t;
+
+/* Workspace layout: three 128-byte lines (the GB300 L2 line; also one of the
+ * 64-byte lines [SYNCALL] §4.1 asks the counter to own exclusively):
+ *   line 0  word 0: soft counter
+ *   line 1  words 0..3: status (0 or CNS_ERR_TIMEOUT), abort flag,
+ *           round at which a wait gave up, CTA that gave up
+ *   line 2  word 0: hard-path counter (one arrival per cluster)
+ * The base must be 128-byte aligned.  [SYNCALL] §4.1: it must be zeroed
+ * before first use and shared with no other data. */
+#define CNS_SYNCALL_LINE_BYTES 128
+#define CNS_SYNCALL_WORKSPACE_BYTES 384
+
+/* CTA status words written to cns_syncall_data_t.cta_status_dev (optional).
+ * The low byte is the outcome, bits 8..15 the role (0 AIV, 1 AIC). */
+#define CNS_CTA_DONE 1u    /* took part in every round */
+#define CNS_CTA_IDLE 2u    /* launched but not a participant: skipped every
+                              barrier ([SYNCALL] §8 idle-core mark 2) */
+#define CNS_CTA_ABORTED 4u /* left early after a wait timed out */
+
+/*
+ * syncall_workspace_init -- zero a workspace and preset both counters.
+ *   ws_dev       device pointer, 128-byte aligned, `bytes` long
+ *   bytes        >= CNS_SYNCALL_WORKSPACE_BYTES
+ *   start_value  value of both counters before the first arrival; 0 is the
+ *                documented initial state ([SYNCALL] §4.1).  A multiple of
+ *                the participant count below its wrap modulus models a
+ *                workspace reused after earlier complete runs; any other
+ *                value desynchronises the epochs and the run times out.
+ *   stream       stream to enqueue on (asynchronous)
+ * Errors: NULL_PTR, INVALID_VALUE (size or alignment), CUDA.
+ */
+int syncall_workspace_init(void *ws_dev, size_t bytes, uint32_t start_value, cns_stream_t stream);
+
+/* Description of one syncall_run: the launch, the payload and the outputs.
+ * Fields marked (in) are read, (out) are written by syncall_run. */
+typedef struct {
+    int32_t workload;        /* (in) cns_workload_t */
+    int32_t launch_ctas;     /* (in) AIV/AIC-only: CTAs launched; MIX: AIC groups */
+    int32_t threads;         /* (in) threads per CTA, multiple of 32, <= 1024; 0 = 256 */
+    int32_t cluster_dim;     /* (in) HARD, AIV/AIC-only: CTAs per cluster (1..8); 0 = the
+                                largest of 4, 2, 1 that divides the grid and can be resident.
+                                MIX always uses clusters of 1 + aiv_ratio. */
+    void *buf0_dev;          /* (in) payload buffer 0 (round-0 input), 16-byte aligned */
+    void *buf1_dev;          /* (in) payload buffer 1, same size */
+    int64_t elems;           /* (in) ring: uint32 slots per participant; Jacobi: field length.
+                                With elems == 0 the buffers may be NULL. */
+    void *workspace_dev;     /* (in) CNS_SYNCALL_WORKSPACE_BYTES, initialised */
+    int32_t *cta_status_dev; /* (in, optional) int32[grid CTAs] for CNS_CTA_* marks */
+    cns_stream_t stream;     /* (in) stream to run on */
+    uint32_t timeout_ms;     /* (in) bound on each barrier wait; 0 = library default
+                                (2000 ms, or the CNS_TIMEOUT_MS environment variable) */
+    int32_t sync;            /* (in) 1: wait for the run, time it, read the workspace
+                                back and return its status; 0: enqueue and return */
+    const void *host_in;     /* (in, optional) host copy of buffer 0, copied in before the
+                                launch on `stream` (pinned memory keeps it asynchronous) */
+    void *host_out;          /* (in, optional) host buffer that receives the final payload
+                                buffer after the run */
+    float elapsed_ms;        /* (out, sync=1) device time from before the first copy to
+                                after the last, CUDA events on `stream` */
+    uint32_t final_counter;  /* (out, sync=1) counter of the path used after the run */
+    int32_t device_status;   /* (out, sync=1) 0 or CNS_ERR_TIMEOUT */
+    int32_t grid_ctas;       /* (out) CTAs launched */
+    int32_t participants;    /* (out) resolved participant count P */
+    int32_t cluster_used;    /* (out) CTAs per cluster (1 for SOFT) */
+    int32_t reserved[4];
+} cns_syncall_data_t;
+
+/*
+ * syncall_run -- one persistent launch that runs `rounds` rounds of
+ * { data phase; SYNCALL } ([SYNCALL] §2: no participant continues past a
+ * barrier until every participant has executed it).
+ *
+ *   mode        CNS_SYNCALL_SOFT: every participant arrives with one atomic
+ *               increment of the workspace counter, gets back `before`,
+ *               computes target = (before / P + 1) * P and polls until the
+ *               counter reaches it ([SYNCALL] §5.2).  The counter cycles
+ *               through Z_M, M = P * floor(2^32 / P), so the epochs survive the
+ *               32-bit wrap; for a power-of-two P this is the plain wrapping add.
+ *               CNS_SYNCALL_HARD: a thread-block-cluster barrier, one arrival
+ *               per cluster on the hard counter by cluster rank 0, then a
+ *               second cluster barrier that releases the cluster (the two-level
+ *               shape of the guide's MIX hard path, §5.1).
+ *   core_type   cns_core_type_t ([SYNCALL] §3.1)
+ *   used_cores  participants; 0 = automatic: the CTAs launched for AIV/AIC-
+ *               only, launch_ctas * (1 + ratio) for MIX ([SYNCALL] §4.2).  A
+ *               non-zero value makes CTAs 0..used_cores-1 the participants;
+ *               the rest write CNS_CTA_IDLE and exit without touching the
+ *               counter (the guide's partial-participation example, §7.2).
+ *               Ignored by HARD, as [SYNCALL] §3.2 says of the hard path.
+ *   aiv_ratio   MIX only: AIV CTAs per AIC CTA; 0 = 1 ([SYNCALL] §4.2).
+ *   rounds      number of rounds R >= 0
+ *   data        launch/payload description, see cns_syncall_data_t
+ *
+ * Memory ordering: the arrival is a release and the poll an acquire at GPU
+ * scope, each CTA draining its threads before arriving, so a round sees every
+ * payload write of the previous round.  [SYNCALL] §6.1 promises arrival only;
+ * this is stronger.
+ *
+ * The launch is cooperative (co-residency is guaranteed or the launch fails
+ * with CNS_ERR_NOT_RESIDENT).  A workspace left by a timed-out run keeps its
+ * abort flag: re-initialise it before reusing it.
+ *
+ * Errors: NULL_PTR (data, workspace, payload buffers the workload needs),
+ * INVALID_VALUE (enum, sizes, used_cores > launched CTAs, cluster shape,
+ * alignment), ARCH, NOT_RESIDENT, CUDA; with sync=1 also TIMEOUT when a
+ * barrier wait ran out on the device.
+ */
+int syncall_run(int mode, int core_type, int32_t used_cores, int32_t aiv_ratio,
+                int64_t rounds, cns_syncall_data_t *data);
+
+/*
+ * syncall_read_workspace -- wait for `stream`, then copy the workspace's
+ * counters and status to the host.  Any output pointer may be NULL.
+ * Errors: NULL_PTR (ws_dev), CUDA.
+ */
+int syncall_read_workspace(const void *ws_dev, cns_stream_t stream, uint32_t *soft_counter,
+                           uint32_t *hard_counter, int32_t *status);
+
+/* ========================================================================= */
+/* CntNotify                                                                  */
+/* ========================================================================= */
+
+/* [CNTN] §1: an opaque handle. */
+typedef struct cns_cnt_notify_s *cns_cnt_notify_t;
+
+/* [CNTN] §3.1: record modes.  SET: count = value; ADD: count = count + value
+ * (mod 2^32); BIT_OR: count |= value; BIT_AND: count &= value.  3 is unused. */
+typedef enum {
+    CNS_REC_SET = 0,
+    CNS_REC_ADD = 1,
+    CNS_REC_BIT_OR = 2,
+    CNS_REC_BIT_AND = 4
+} cns_record_mode_t;
+
+/* [CNTN] §3.2: wait modes; the wait is released when the predicate holds.
+ * LESS: count < value; EQUAL: count == value; BIGGER: count > value;
+ * BIGGER_OR_EQUAL: count >= value; EQUAL_WITH_BITMASK: (count & value) == value.
+ * Unsigned 32-bit compares. */
+typedef enum {
+    CNS_WAIT_LESS = 0,
+    CNS_WAIT_EQUAL = 1,
+    CNS_WAIT_BIGGER = 2,
+    CNS_WAIT_BIGGER_OR_EQUAL = 3,
+    CNS_WAIT_EQUAL_WITH_BITMASK = 4
+} cns_wait_mode_t;
+
+/* [CNTN] §3.3 */
+typedef struct {
+    int32_t mode;   /* cns_record_mode_t */
+    uint32_t value;
+} cns_record_info_t;
+
+/* [CNTN] §3.3.  timeout in seconds, 0 = wait without a time limit; the device
+ * still stops after the library's cap (CNS_TIMEOUT_MS, default 30 s) so a
+ * shared GPU is never held forever.  is_clear = 1 sets the count to 0 once the
+ * wait is released.  rev is reserved (fill with 0; ignored). */
+typedef struct {
+    int32_t mode;   /* cns_wait_mode_t */
+    uint32_t value;
+    uint32_t timeout;
+    uint8_t is_clear;
+    uint8_t rev[3];
+} cns_wait_info_t;
+
+/*
+ * cntnotify_create -- create a counted notify with count 0 on the current
+ * device ([CNTN] §4.1).  Its counter is one uint32 on a 128-byte line of a
+ * device-resident pool owned by the library.
+ *   out   receives the handle
+ *   flag  reserved, must be 0
+ * Errors: NULL_PTR (out), INVALID_VALUE (flag != 0), RESOURCE (pool of
+ * CNS_POOL_CAP notifies exhausted, default 1024; [CNTN] EE1023), ARCH, CUDA.
+ */
+int cntnotify_create(cns_cnt_notify_t *out, uint64_t flag);
+
+/*
+ * cntnotify_record -- enqueue one record on `stream` ([CNTN] §4.2): when the
+ * stream reaches it, the count becomes f(count, value) for info->mode, as one
+ * device atomic with release semantics (work earlier on `stream` is visible
+ * to whoever observes the new count).  Asynchronous.
+ * Errors: INVALID_HANDLE, NULL_PTR (info), INVALID_VALUE (mode), CUDA.
+ */
+int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const cns_record_info_t *info);
+
+/*
+ * cntnotify_wait_with_timeout -- block `stream` (not the calling thread)
+ * until the count satisfies info->mode/value ([CNTN] §4.3).  One thread on
+ * the device polls the count with acquire loads; once released it clears the
+ * count to 0 if info->is_clear ([CNTN] §7 item 4: the clear comes after the
+ * release; a record that lands between the two is overwritten).  If the
+ * timeout passes first, the wait records CNS_ERR_TIMEOUT in the notify's
+ * sticky status (see cntnotify_query_status) and the stream continues.
+ * Errors: INVALID_HANDLE, NULL_PTR (info), INVALID_VALUE (mode), CUDA.
+ */
+int cntnotify_wait_with_timeout(cns_cnt_notify_t h, cns_stream_t stream, const cns_wait_info_t *info);
+
+/* cntnotify_reset -- enqueue count = 0 on `stream` ([CNTN] §4.4).
+ * Errors: INVALID_HANDLE, CUDA. */
+int cntnotify_reset(cns_cnt_notify_t h, cns_stream_t stream);
+
+/* cntnotify_get_id -- the notify's id, unique among live notifies of the
+ * process ([CNTN] §4.5).  Errors: INVALID_HANDLE, NULL_PTR (id). */
+int cntnotify_get_id(cns_cnt_notify_t h, uint32_t *id);
+
+/* cntnotify_destroy -- release the notify ([CNTN] §4.6).  The handle is
+ * invalid afterwards; work already enqueued on it must have finished.
+ * Errors: INVALID_HANDLE. */
+int cntnotify_destroy(cns_cnt_notify_t h);
+
+/* cntnotify_get_device_ptr -- device address of the notify's uint32 count,
+ * for records issued from inside user kernels (the count word plays the part
+ * of the hardware notify slice of [CNTN] §6.2).  Valid until destroy.
+ * Errors: INVALID_HANDLE, NULL_PTR. */
+int cntnotify_get_device_ptr(cns_cnt_notify_t h, uint32_t **count_dev);
+
+/* cntnotify_query_status -- read the notify's sticky status (0 or
+ * CNS_ERR_TIMEOUT left by a wait that timed out) and, if count is not NULL,
+ * its current count.  Synchronous; does not wait for other streams.
+ * Errors: INVALID_HANDLE, NULL_PTR (status), CUDA. */
+int cntnotify_query_status(cns_cnt_notify_t h, int32_t *status, uint32_t *count);
+
+/* ------------------------------------------------------------------------- */
+/* Counted-notify op streams and the two-stream counting pipeline             */
+/* ------------------------------------------------------------------------- */
+
+/* Trace outcome codes of cns_statemachine_run. */
+#define CNS_OUT_WAIT_HELD 0u
+#define CNS_OUT_WAIT_RELEASED 1u
+#define CNS_OUT_RECORD 2u
+#define CNS_OUT_INVALID 3u
+
+/* Scratch bytes cns_statemachine_run needs for n ops. */
+size_t cns_statemachine_scratch_bytes(int64_t n);
+
+/*
+ * cns_statemachine_run -- apply a stream of n counted-notify ops to one count,
+ * in order, and trace every step.  Each op is four uint32: kind (0 record,
+ * 1 try-wait), mode, value, is_clear.  A record applies the [CNTN] §3.1 rule;
+ * a try-wait tests the §3.2 predicate once and, if it holds and is_clear is
+ * set, clears the count to 0 (it never blocks).  Undefined kinds or modes
+ * leave the count unchanged with outcome CNS_OUT_INVALID.
+ *   ops_dev      [n][4] uint32, 16-byte aligned
+ *   n            op count >= 0
+ *   init         count before the first op
+ *   trace_dev    out [n][2] uint32: count after the op, outcome code
+ *   final_dev    out uint32: count after the last op
+ *   scratch_dev  cns_statemachine_scratch_bytes(n) bytes, no initial content
+ *   stream       stream to run on (asynchronous)
+ * The result is the sequential result exactly; the kernels split the stream
+ * at SET records (whose result does not depend on the count before them).
+ * Errors: NULL_PTR, INVALID_VALUE (n < 0, alignment, scratch too small), CUDA.
+ */
+int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t init, uint32_t *trace_dev,
+                         uint32_t *final_dev, void *scratch_dev, size_t scratch_bytes,
+                         cns_stream_t stream);
+
+/* Two-stream counting pipeline ([CNTN] §5: producers record ADD 1, the waiter
+ * waits BIGGER_OR_EQUAL N with isClear = 1 and then continues). */
+typedef struct {
+    cns_cnt_notify_t done;   /* (in) producer -> consumer: ADD 1 per tile */
+    cns_cnt_notify_t ack;    /* (in) consumer -> producer: SET 1 once a round is consumed */
+    uint32_t *tiles_dev;     /* (in) tiles * tile_words uint32 */
+    uint32_t *checksums_dev; /* (in/out) uint32[rounds], zeroed by the call */
+    uint32_t *released_dev;  /* (in/out, optional) uint32[rounds]: count seen at release */
+    int64_t tiles;           /* (in) K tiles per round, >= 1 */
+    int32_t tile_words;      /* (in) words per tile, multiple of 4, 4..8192 */
+    int32_t producer_ctas;   /* (in) producer grid; 0 = 4 per SM */
+    int64_t rounds;          /* (in) rounds */
+    cns_stream_t producer_stream; /* (in) the recording stream */
+    cns_stream_t consumer_stream; /* (in) the waiting stream */
+    uint32_t timeout_s;      /* (in) per-wait timeout in seconds; 0 = library cap */
+    int32_t sync;            /* (in) 1: wait, time, check the notifies' status */
+    float elapsed_ms;        /* (out, sync=1) first producer launch to last record */
+    float producer_ms;       /* (out, sync=1) summed producer-kernel time */
+    int32_t device_status;   /* (out, sync=1) 0 or CNS_ERR_TIMEOUT */
+    int32_t reserved[3];
+} cns_pipeline_t;
+
+/*
+ * cns_pipeline_run -- `rounds` rounds of: on the producer stream, a producer
+ * kernel writes word w of the tile area as w * 2654435761 + round and, after
+ * each tile is stored, adds 1 to `done` from the device; then it waits for
+ * `ack` EQUAL 1 (clear).  On the consumer stream: wait `done`
+ * BIGGER_OR_EQUAL tiles (clear), a consumer kernel sums the tile area mod 2^32
+ * into checksums[round], then record `ack` SET 1.  The streams meet only
+ * through the two counts.  The call first clears both notifies (count and
+ * status); once one of its waits times out, the pipeline's remaining waits
+ * return at once, so a lost signal costs one timeout, not one per round.
+ * Errors: INVALID_HANDLE, NULL_PTR, INVALID_VALUE, CUDA; with sync=1 also
+ * TIMEOUT.
+ */
+int cns_pipeline_run(cns_pipeline_t *cfg);
+
+/* ------------------------------------------------------------------------- */
+/* Latency and throughput probes (roofline denominators)                      */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * cns_probe_atomic_rtt -- one thread of CTA `probe_cta` (of a `grid`-CTA
+ * launch whose other CTAs exit at once) issues `iters` dependent operations
+ * on the 128-byte line at line_dev (zeroed first) and times them with the
+ * global timer.
+ *   kind 0: atom.add.relaxed.gpu (L2 atomic round trip)
+ *   kind 1: ld.relaxed.gpu of the line (L2 load round trip)
+ *   kind 2: atom.add.release.gpu + ld.acquire.gpu (the arrive/poll pair)
+ *   out_dev  uint64[2]: total nanoseconds, SM id the probe ran on
+ * Errors: NULL_PTR, INVALID_VALUE, CUDA.
+ */
+int cns_probe_atomic_rtt(int kind, int32_t grid, int32_t probe_cta, int32_t iters, uint32_t *line_dev,
+                         uint64_t *out_dev, cns_stream_t stream);
+
+/*
+ * cns_probe_same_address_throughput -- grid x threads threads each add 1 to
+ * the same word `iters` times with red.relaxed.gpu (fire-and-forget).
+ * Time it with events around the call.  Errors: NULL_PTR, INVALID_VALUE, CUDA.
+ */
+int cns_probe_same_address_throughput(int32_t grid, int32_t threads, int32_t iters, uint32_t *word_dev,
+                                      cns_stream_t stream);
+
+/* Library version and the compute capability it was built for (103). */
+int cns_version(int32_t *version, int32_t *built_sm);
+
+/* Human-readable name of an error code (static string). */
+const char *cns_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CNS_H */

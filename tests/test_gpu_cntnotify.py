@@ -1,0 +1,279 @@
+"""CntNotify on the GPU against the CPU oracle: single records and waits from
+the hand-built truth table, the op-stream state machine (bit-exact trace),
+cross-stream waits, the two-stream counting pipeline and the timeout."""
+import numpy as np
+import pytest
+
+import cns_inputs as ci
+import oracle
+from tests.conftest import read_golden
+from tests.gpu_helpers import from_dev_u32, to_dev_u32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cns():
+    import torch
+    import counted_notify_sync_gb300 as c
+    c.build()
+    torch.cuda.set_device(0)
+    return c
+
+
+@pytest.fixture
+def notify(cns):
+    rc, h = cns.cntnotify_create(0)
+    assert rc == 0
+    yield h
+    assert cns.cntnotify_destroy(h) == 0
+
+
+def count_of(cns, h):
+    import torch
+    torch.cuda.synchronize()
+    rc, st, c = cns.cntnotify_query_status(h)
+    assert rc == 0
+    return st, c
+
+
+def test_record_truth_table(cns, notify):
+    rows = [r for r in read_golden("cntnotify_truth_table.txt") if r[0] == "record"]
+    for _, mode, c, v, want in rows:
+        mode, c, v = int(mode, 0), int(c, 0), int(v, 0)
+        assert cns.cntnotify_record(notify, None, cns.CNS_REC_SET, c) == 0
+        rc = cns.cntnotify_record(notify, None, mode, v)
+        if want == "invalid":
+            assert rc == cns.CNS_ERR_INVALID_VALUE
+            continue
+        assert rc == 0
+        st, got = count_of(cns, notify)
+        exp, ok = oracle.cnt_record(c, mode, v)
+        assert ok and got == exp == int(want, 0) and st == 0
+
+
+@pytest.mark.parametrize("clear", [0, 1])
+def test_blocking_wait_released_rows(cns, notify, clear):
+    """Every released row of the truth table: the wait returns, and clears if asked."""
+    rows = [r for r in read_golden("cntnotify_truth_table.txt") if r[0] == "wait" and r[4] == "1"]
+    assert len(rows) >= 15
+    for _, mode, c, v, _ in rows:
+        mode, c, v = int(mode, 0), int(c, 0), int(v, 0)
+        assert oracle.cnt_wait_satisfied(c, mode, v) == 1
+        assert cns.cntnotify_record(notify, None, cns.CNS_REC_SET, c) == 0
+        assert cns.cntnotify_wait_with_timeout(notify, None, mode, v, 5, clear) == 0
+        st, got = count_of(cns, notify)
+        assert st == 0 and got == (0 if clear else c)
+
+
+def test_invalid_wait_mode_rejected(cns, notify):
+    assert cns.cntnotify_wait_with_timeout(notify, None, 5, 0, 1, 0) == cns.CNS_ERR_INVALID_VALUE
+    assert cns.cntnotify_wait_with_timeout(notify, None, info=None) == cns.CNS_ERR_NULL_PTR
+    assert cns.cntnotify_record(notify, None, info=None) == cns.CNS_ERR_NULL_PTR
+    assert cns.cntnotify_get_id(notify, out=False)[0] == cns.CNS_ERR_NULL_PTR
+
+
+def test_usage_example_two_streams(cns, notify):
+    """Stream 2 waits for count >= 1 (timeout 10 s, clear); stream 1 records ADD 1."""
+    import torch
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    assert cns.cntnotify_wait_with_timeout(notify, s2, cns.CNS_WAIT_BIGGER_OR_EQUAL, 1, 10, 1) == 0
+    assert cns.cntnotify_record(notify, s1, cns.CNS_REC_ADD, 1) == 0
+    s1.synchronize()
+    s2.synchronize()
+    st, c = count_of(cns, notify)
+    assert st == 0 and c == 0
+    rc, nid = cns.cntnotify_get_id(notify)
+    assert rc == 0
+    assert cns.cntnotify_reset(notify, s2) == 0
+
+
+def test_n_producer_streams_fan_in(cns, notify):
+    """N producer streams each ADD 1; the waiter uses BIGGER_OR_EQUAL N."""
+    import torch
+    n = 6
+    waiter = torch.cuda.Stream()
+    prods = [torch.cuda.Stream() for _ in range(n)]
+    assert cns.cntnotify_wait_with_timeout(notify, waiter, cns.CNS_WAIT_BIGGER_OR_EQUAL, n, 10, 0) == 0
+    for s in prods:
+        assert cns.cntnotify_record(notify, s, cns.CNS_REC_ADD, 1) == 0
+    torch.cuda.synchronize()
+    st, c = count_of(cns, notify)
+    assert st == 0 and c == n
+
+
+def test_bitmask_multi_signal(cns, notify):
+    import torch
+    waiter = torch.cuda.Stream()
+    bits = [1 << k for k in (0, 3, 9, 31)]
+    mask = sum(bits)
+    assert cns.cntnotify_wait_with_timeout(notify, waiter, cns.CNS_WAIT_EQUAL_WITH_BITMASK, mask, 10, 1) == 0
+    streams = [torch.cuda.Stream() for _ in bits]
+    for b, s in zip(bits, streams):
+        assert cns.cntnotify_record(notify, s, cns.CNS_REC_BIT_OR, b) == 0
+    torch.cuda.synchronize()
+    st, c = count_of(cns, notify)
+    assert st == 0 and c == 0
+
+
+def test_wait_timeout_sets_sticky_status(cns, notify):
+    """LESS 0 can never be released (the unit-test WaitInfo of the API page)."""
+    import time
+    t0 = time.time()
+    assert cns.cntnotify_wait_with_timeout(notify, None, cns.CNS_WAIT_LESS, 0, 1, 1) == 0
+    st, c = count_of(cns, notify)
+    assert st == cns.CNS_ERR_TIMEOUT and c == 0
+    assert 0.9 < time.time() - t0 < 10
+    # the stream and the device keep working
+    assert cns.cntnotify_record(notify, None, cns.CNS_REC_ADD, 5) == 0
+    assert count_of(cns, notify)[1] == 5
+
+
+def test_ids_unique_and_destroy_invalidates(cns):
+    hs = []
+    for _ in range(20):
+        rc, h = cns.cntnotify_create(0)
+        assert rc == 0
+        hs.append(h)
+    ids = [cns.cntnotify_get_id(h)[1] for h in hs]
+    assert len(set(ids)) == 20
+    h = hs.pop()
+    assert cns.cntnotify_destroy(h) == 0
+    assert cns.cntnotify_destroy(h) == cns.CNS_ERR_INVALID_HANDLE
+    assert cns.cntnotify_record(h, None, cns.CNS_REC_ADD, 1) == cns.CNS_ERR_INVALID_HANDLE
+    for h in hs:
+        assert cns.cntnotify_destroy(h) == 0
+
+
+def test_pool_exhaustion_and_recovery(cns):
+    hs = []
+    while True:
+        rc, h = cns.cntnotify_create(0)
+        if rc != 0:
+            break
+        hs.append(h)
+        assert len(hs) <= 1 << 20
+    assert rc == cns.CNS_ERR_RESOURCE and len(hs) >= 1
+    assert cns.cntnotify_destroy(hs.pop()) == 0
+    rc, h = cns.cntnotify_create(0)
+    assert rc == 0
+    st, c = count_of(cns, h)        # a reused slot starts clean
+    assert st == 0 and c == 0
+    hs.append(h)
+    for h in hs:
+        assert cns.cntnotify_destroy(h) == 0
+
+
+# --- op-stream state machine ---------------------------------------------------------------
+
+def run_sm(cns, ops, init):
+    import torch
+    n = ops.shape[0]
+    dev = to_dev_u32(ops) if n else torch.empty((0, 4), dtype=torch.int32, device="cuda")
+    trace, final = cns.run_statemachine(dev, init)
+    return (from_dev_u32(trace) if n else np.zeros((0, 2), np.uint32)), int(from_dev_u32(final)[0])
+
+
+def test_statemachine_1e6_ops_bit_exact(cns):
+    ops = ci.notify_ops(1_000_000)
+    got_t, got_f = run_sm(cns, ops, 0)
+    want_t, want_f = oracle.cnt_statemachine(ops, 0)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
+def test_statemachine_hand_sequence(cns):
+    rows = read_golden("cntnotify_sequence.txt")
+    ops = np.array([[int(k, 0), int(m, 0), int(v, 0), int(c, 0)] for k, m, v, c, _, _, _ in rows], dtype=np.uint32)
+    got_t, got_f = run_sm(cns, ops, 0)
+    want = np.array([[int(a, 0), int(o)] for *_, a, o in rows], dtype=np.uint32)
+    np.testing.assert_array_equal(got_t, want)
+
+
+@pytest.mark.parametrize("n", [0, 1, 15, 16, 17, 33, 4097])
+def test_statemachine_ragged_lengths(cns, n):
+    ops = ci.notify_ops(n, seed=1000 + n)
+    got_t, got_f = run_sm(cns, ops, 0xDEAD)
+    want_t, want_f = oracle.cnt_statemachine(ops, 0xDEAD)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
+def test_statemachine_without_any_set(cns):
+    """No SET record at all: one chain runs the whole stream."""
+    ops = ci.notify_ops(50_000, seed=77)
+    ops = ops[~((ops[:, 0] == 0) & (ops[:, 1] == 0))]
+    got_t, got_f = run_sm(cns, ops, 3)
+    want_t, want_f = oracle.cnt_statemachine(ops, 3)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
+def test_statemachine_all_sets_and_invalid_ops(cns):
+    ops = ci.notify_ops(3000, seed=5)
+    ops[::2, 0] = 0
+    ops[::2, 1] = 0
+    ops[1::7, 1] = 3          # record mode 3 / wait mode 3
+    ops[5::11, 0] = 2         # undefined kind
+    ops[6::13, 0] = 1
+    ops[6::13, 1] = 9         # undefined wait mode
+    got_t, got_f = run_sm(cns, ops, 1)
+    want_t, want_f = oracle.cnt_statemachine(ops, 1)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
+# --- two-stream counting pipeline --------------------------------------------------------
+
+def test_pipeline_4096_tiles_1000_rounds(cns):
+    import torch
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    assert rc == rc2 == 0
+    try:
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 4096, 256, 1000, s1, s2, timeout_s=10)
+        assert rc == 0 and cfg.device_status == 0
+        want_cs, want_rel = oracle.pipeline(4096, 256, 1000)
+        np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
+        np.testing.assert_array_equal(from_dev_u32(released), want_rel)
+        assert count_of(cns, done) == (0, 0) and count_of(cns, ack) == (0, 0)
+        assert cfg.elapsed_ms > 0 and 0 < cfg.producer_ms <= cfg.elapsed_ms
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
+
+
+def test_pipeline_small_odd_shapes(cns):
+    import torch
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    try:
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 7, 12, 5, s1, s2, timeout_s=10,
+                                                        producer_ctas=3)
+        assert rc == 0
+        want_cs, want_rel = oracle.pipeline(7, 12, 5)
+        np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
+        np.testing.assert_array_equal(from_dev_u32(released), want_rel)
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
+
+
+# --- probes ------------------------------------------------------------------------------------
+
+def test_probes_return_plausible_times(cns):
+    import torch
+    line = torch.zeros(32, dtype=torch.int32, device="cuda")
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for kind in (0, 1, 2):
+        assert cns.cns_probe_atomic_rtt(kind, sms, sms // 2, 200, line, out) == 0
+        torch.cuda.synchronize()
+        ns, sm = out.tolist()
+        assert 200 * 50 < ns < 200 * 20000 and 0 <= sm < sms
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert cns.cns_probe_same_address_throughput(sms, 256, 10, word) == 0
+    torch.cuda.synchronize()
+    assert int(word.item()) == sms * 256 * 10

@@ -1,0 +1,272 @@
+"""SYNCALL on the GPU against the CPU oracle (bit-exact for every u32 round
+and counter; the fp32 Jacobi within 1e-5 relative and in fact bit-exact)."""
+import numpy as np
+import pytest
+
+import cns_inputs as ci
+import oracle
+from tests.gpu_helpers import from_dev_u32, to_dev_f32, to_dev_u32
+
+pytestmark = pytest.mark.gpu
+
+SOFT, HARD = 1, 0
+AIV, AIC, MIX = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def cns():
+    import torch
+    import counted_notify_sync_gb300 as c
+    c.build()
+    torch.cuda.set_device(0)
+    return c
+
+
+def run_ring(cns, mode, core, wl, launch_ctas, v0, rounds, used=0, ratio=0, start=0, threads=256,
+             cluster_dim=0, timeout_ms=0, check=True):
+    import torch
+    P, slots = v0.shape
+    b0 = to_dev_u32(v0) if v0.size else None
+    b1 = torch.zeros_like(b0) if v0.size else None
+    ws = cns.new_workspace(start_value=start)
+    group = (1 + (ratio or 1)) if core == MIX else 1
+    status = torch.zeros(launch_ctas * group, dtype=torch.int32, device="cuda")
+    d, rc = cns.run_syncall(mode, core, wl, launch_ctas, b0, b1, rounds, used_cores=used, aiv_ratio=ratio,
+                            elems=slots, threads=threads, cluster_dim=cluster_dim, workspace=ws,
+                            cta_status=status, timeout_ms=timeout_ms, check=check)
+    torch.cuda.synchronize()
+    final = from_dev_u32(b1 if rounds & 1 else b0).reshape(P, slots) if v0.size else v0.copy()
+    return d, rc, final, status.cpu().numpy()
+
+
+def expect_ring(wl, v0, rounds, start=0):
+    out, fc, rc = oracle.syncall_run_ring(wl, v0, rounds, start)
+    assert rc == oracle.OK
+    return out, fc
+
+
+# --- ring-affine, 8 participants (256 uint32 each, 1000 rounds) --------------------------
+
+def test_ring_affine_p8_1000_rounds(cns):
+    v0 = ci.ring_payload(ci.SEED_RING_AFFINE, 8, 256)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, 1000)
+    want, fc = expect_ring(oracle.WL_RING_AFFINE, v0, 1000)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == fc == 8000 and d.device_status == 0
+    assert d.participants == 8 and d.grid_ctas == 8
+    assert (st == cns.CNS_CTA_DONE).all()
+
+
+@pytest.mark.parametrize("P,slots,R,threads", [(3, 7, 5, 32), (5, 1030, 17, 256), (1, 4, 9, 64), (2, 0, 4, 32),
+                                                (13, 4096, 3, 1024), (16, 9, 2, 96)])
+def test_ring_affine_ragged_shapes(cns, P, slots, R, threads):
+    v0 = ci.ring_payload(ci.SEED_RING_AFFINE + P, P, slots)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, P, v0, R, threads=threads)
+    want, fc = expect_ring(oracle.WL_RING_AFFINE, v0, R)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == fc
+
+
+def test_zero_rounds_leaves_everything(cns):
+    v0 = ci.ring_payload(1, 4, 8)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 0)
+    np.testing.assert_array_equal(got, v0)
+    assert d.final_counter == 0
+
+
+# --- ring-rotate, 148 participants, 100000 rounds, soft and hard -------------------------
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_ring_rotate_p148_100000_rounds(cns, mode):
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, 100000)
+    want, fc = expect_ring(oracle.WL_RING_ROTATE, v0, 100000)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(got, np.roll(v0, -100000, axis=0))
+    assert d.device_status == 0 and (st == cns.CNS_CTA_DONE).all()
+    if mode == SOFT:
+        assert d.final_counter == fc == 14_800_000 and d.cluster_used == 1
+    else:
+        assert d.cluster_used in (1, 2, 4)
+        assert d.final_counter == 100000 * (148 // d.cluster_used)
+
+
+@pytest.mark.parametrize("C", [1, 2, 4])
+def test_hard_explicit_cluster_dims(cns, C):
+    v0 = ci.ring_payload(7, 16, 12)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_AFFINE, 16, v0, 301, cluster_dim=C)
+    want, _ = expect_ring(oracle.WL_RING_AFFINE, v0, 301)
+    np.testing.assert_array_equal(got, want)
+    assert d.cluster_used == C and d.final_counter == 301 * (16 // C)
+
+
+# --- MIX role classes and the used_cores subset (xorshift payload) --------------------------
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_mix_37_groups_ratio_2(cns, mode):
+    v0 = ci.ring_payload(ci.SEED_XORSHIFT, 111, 256)
+    d, rc, got, st = run_ring(cns, mode, MIX, cns.CNS_WL_XORSHIFT, 37, v0, 10000, ratio=2)
+    want, fc = expect_ring(oracle.WL_XORSHIFT, v0, 10000)
+    np.testing.assert_array_equal(got, want)
+    assert d.participants == 111 and d.grid_ctas == 111
+    roles = st >> 8
+    np.testing.assert_array_equal(roles, (np.arange(111) % 3 == 0).astype(np.int32))
+    assert ((st & 0xFF) == cns.CNS_CTA_DONE).all()
+    if mode == SOFT:
+        assert d.final_counter == fc
+    else:
+        assert d.cluster_used == 3 and d.final_counter == 10000 * 37
+
+
+def test_mix_default_ratio_is_one(cns):
+    v0 = ci.ring_payload(11, 10, 8)
+    d, rc, got, st = run_ring(cns, SOFT, MIX, cns.CNS_WL_XORSHIFT, 5, v0, 33, ratio=0)
+    want, _ = expect_ring(oracle.WL_XORSHIFT, v0, 33)
+    np.testing.assert_array_equal(got, want)
+    assert d.participants == 10
+
+
+def test_used_cores_subset_64_of_148(cns):
+    import torch
+    v0 = ci.ring_payload(ci.SEED_XORSHIFT, 64, 256)
+    b0 = to_dev_u32(v0)
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    status = torch.zeros(148, dtype=torch.int32, device="cuda")
+    d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_XORSHIFT, 148, b0, b1, 10000, used_cores=64, elems=256,
+                            workspace=ws, cta_status=status)
+    got = from_dev_u32(b0).reshape(64, 256)
+    want, fc = expect_ring(oracle.WL_XORSHIFT, v0, 10000)
+    np.testing.assert_array_equal(got, want)
+    st = status.cpu().numpy()
+    assert (st[:64] == cns.CNS_CTA_DONE).all() and (st[64:] == cns.CNS_CTA_IDLE).all()
+    assert d.final_counter == fc == 640000 and d.participants == 64
+
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_aic_only(cns, mode):
+    v0 = ci.ring_payload(5, 24, 64)
+    d, rc, got, st = run_ring(cns, mode, AIC, cns.CNS_WL_RING_AFFINE, 24, v0, 99)
+    want, _ = expect_ring(oracle.WL_RING_AFFINE, v0, 99)
+    np.testing.assert_array_equal(got, want)
+    assert ((st >> 8) == 1).all()
+
+
+# --- counter arithmetic -------------------------------------------------------------------
+
+def test_empty_payload_counter_only(cns):
+    ws = cns.new_workspace()
+    d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_EMPTY, 148, None, None, 5000, workspace=ws)
+    fc, _ = oracle.syncall_run_empty(148, 5000)
+    assert d.final_counter == fc == 740000
+
+
+@pytest.mark.parametrize("P", [148, 3, 111])
+def test_counter_wraps_through_zm(cns, P):
+    M = oracle.counter_modulus(P)
+    start = M - 5 * P
+    v0 = ci.ring_payload(9, P, 4)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, P, v0, 12, start=start)
+    want, fc = expect_ring(oracle.WL_RING_AFFINE, v0, 12, start)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == fc == 7 * P
+
+
+def test_workspace_reused_across_runs(cns):
+    ws = cns.new_workspace()
+    total = 0
+    for R in (10, 1, 77):
+        d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_EMPTY, 37, None, None, R, workspace=ws)
+        total += R
+        assert d.final_counter == 37 * total
+
+
+# --- Jacobi -------------------------------------------------------------------------------
+
+def run_jacobi(cns, u0, sweeps, ctas, mode=SOFT, threads=256):
+    import torch
+    b0 = to_dev_f32(u0)
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_JACOBI, ctas, b0, b1, sweeps, elems=u0.size,
+                            threads=threads, workspace=ws)
+    out = (b1 if sweeps & 1 else b0).cpu().numpy()
+    return d, out
+
+
+@pytest.mark.parametrize("N,sweeps,ctas,threads", [(100003, 20, 37, 256), (4099, 7, 5, 64), (5, 3, 2, 32),
+                                                   (1, 2, 1, 32), (2, 5, 3, 32), (64, 11, 20, 32),
+                                                   (1 << 20, 9, 592, 256)])
+def test_jacobi_small_bit_exact(cns, N, sweeps, ctas, threads):
+    u0 = ci.jacobi_field(N)
+    d, got = run_jacobi(cns, u0, sweeps, ctas, threads=threads)
+    want, fc, rc = oracle.syncall_run_jacobi(u0, sweeps, ctas)
+    np.testing.assert_allclose(got, want, rtol=1e-5, atol=0)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == fc
+
+
+def test_jacobi_hard_path(cns):
+    u0 = ci.jacobi_field(200003)
+    d, got = run_jacobi(cns, u0, 10, 64, mode=HARD)
+    want, _, _ = oracle.syncall_run_jacobi(u0, 10, 64)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_jacobi_full_size_sampled(cns):
+    """2^26 points, 592 CTAs, 200 sweeps: sampled points from the oracle's
+    light-cone evaluation, plus chunk edges and both ends."""
+    N, S, C = 1 << 26, 200, 592
+    u0 = ci.jacobi_field(N)
+    d, got = run_jacobi(cns, u0, S, C)
+    assert d.device_status == 0 and d.final_counter == S * C
+    n4 = N // 4
+    edges = []
+    for p in range(0, C, 37):
+        j0 = p * (n4 // C) + min(p, n4 % C)
+        edges += [4 * j0 - 1, 4 * j0, 4 * j0 + 3, 4 * j0 + 4]
+    idx = np.unique(np.concatenate([ci.sample_indices(3, N, 300), np.clip(np.array(edges), 0, N - 1)]))
+    want = oracle.jacobi_points(u0, S, idx)
+    np.testing.assert_allclose(got[idx], want, rtol=1e-5, atol=0)
+    np.testing.assert_array_equal(got[idx], want)
+    assert got[0] == u0[0] and got[-1] == u0[-1]
+
+
+# --- host buffers through the same call -----------------------------------------------------
+
+def test_host_in_host_out(cns):
+    import torch
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    hin = torch.from_numpy(v0.view(np.int32).copy()).pin_memory()
+    hout = torch.empty_like(hin).pin_memory()
+    b0 = torch.empty(148 * 4, dtype=torch.int32, device="cuda")
+    b1 = torch.empty_like(b0)
+    ws = cns.new_workspace()
+    d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_RING_ROTATE, 148, b0, b1, 1001, elems=4, workspace=ws,
+                            host_in=hin, host_out=hout)
+    np.testing.assert_array_equal(hout.numpy().view(np.uint32).reshape(148, 4), np.roll(v0, -1001, axis=0))
+
+
+# --- failures reported as status, never a hang ---------------------------------------------
+
+def test_unzeroed_workspace_times_out_and_context_survives(cns):
+    """A counter left at 1 ("counter garbage": the workspace was not zeroed) puts
+    the participants in different epochs; the bounded poll gives up."""
+    v0 = ci.ring_payload(3, 4, 4)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3, start=1, timeout_ms=300,
+                              check=False)
+    assert rc == cns.CNS_ERR_TIMEOUT and d.device_status == cns.CNS_ERR_TIMEOUT
+    assert ((st & 0xFF) == cns.CNS_CTA_ABORTED).any()
+    # the device still works
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3)
+    want, _ = expect_ring(oracle.WL_RING_AFFINE, v0, 3)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_grid_that_cannot_be_resident_is_refused(cns):
+    import torch
+    ws = cns.new_workspace()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_EMPTY, sms * 64 + 1, None, None, 1, threads=1024, workspace=ws,
+                            check=False)
+    assert rc == cns.CNS_ERR_NOT_RESIDENT
