@@ -15,7 +15,7 @@ __all__ = [n for n in dir(_native) if not n.startswith("_")] + [
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    from .build import build as _b
+    from .builder import build as _b
     return _b(force=force, verbose=verbose)
 
 

@@ -127,7 +127,7 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(
-                    f"libcns.so is not built ({LIB_PATH}); run `python -m counted_notify_sync_gb300.build`")
+                    f"libcns.so is not built ({LIB_PATH}); run `python -m counted_notify_sync_gb300.builder`")
             L = ctypes.CDLL(LIB_PATH)
             for name, (res, args) in _SIGS.items():
                 fn = getattr(L, name)

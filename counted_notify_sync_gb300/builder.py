@@ -1,6 +1,6 @@
 """Build libcns.so in-tree with nvcc for sm_103a.
 
-    python -m counted_notify_sync_gb300.build [--force] [--verbose]
+    python -m counted_notify_sync_gb300.builder [--force] [--verbose]
 
 Each csrc/*.cu is compiled to an object in parallel, then linked into
 counted_notify_sync_gb300/libcns.so against the shared CUDA runtime.

@@ -593,14 +593,19 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
         check(cudaGetLastError(), "producer launch");
         if (timed)
             check(cudaEventRecord(T(2 * r + 1), sp), "event");
-        if (int e = enqueue_wait(ack, sp, &w_ack, nullptr, abort))
-            rc = e;
+        // Submission order = a valid serial schedule: every wait is submitted
+        // after the records that release it.  CUDA may feed both streams
+        // through one hardware queue in submission order; a wait submitted
+        // ahead of its record would then hold the record back until it timed
+        // out.
         if (int e = enqueue_wait(done, sc, &w_done, cfg->released_dev ? cfg->released_dev + r : nullptr, abort))
             rc = e;
         pipeline_consumer_kernel<<<cgrid, 256, 0, sc>>>(cfg->tiles_dev, n_words, cfg->checksums_dev + r);
         check(cudaGetLastError(), "consumer launch");
         cnt_record_kernel<<<1, 32, 0, sc>>>(ack->line, CNS_REC_SET, 1u);
         check(cudaGetLastError(), "ack record");
+        if (int e = enqueue_wait(ack, sp, &w_ack, nullptr, abort))
+            rc = e;
     }
     check(cudaEventRecord(join, sc), "event");
     check(cudaStreamWaitEvent(sp, join, 0), "stream wait");

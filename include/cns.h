@@ -274,6 +274,10 @@ int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const cns_record_i
  * release; a record that lands between the two is overwritten).  If the
  * timeout passes first, the wait records CNS_ERR_TIMEOUT in the notify's
  * sticky status (see cntnotify_query_status) and the stream continues.
+ * Submission order: CUDA may run two streams through one hardware queue in
+ * the order their work was submitted.  A wait submitted before the records
+ * that release it can then hold those records back until it times out, so
+ * submit (from the host) the records a wait depends on before the wait.
  * Errors: INVALID_HANDLE, NULL_PTR (info), INVALID_VALUE (mode), CUDA.
  */
 int cntnotify_wait_with_timeout(cns_cnt_notify_t h, cns_stream_t stream, const cns_wait_info_t *info);

@@ -77,8 +77,9 @@ def test_usage_example_two_streams(cns, notify):
     """Stream 2 waits for count >= 1 (timeout 10 s, clear); stream 1 records ADD 1."""
     import torch
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-    assert cns.cntnotify_wait_with_timeout(notify, s2, cns.CNS_WAIT_BIGGER_OR_EQUAL, 1, 10, 1) == 0
+    # the record is submitted first: the streams may share one hardware queue
     assert cns.cntnotify_record(notify, s1, cns.CNS_REC_ADD, 1) == 0
+    assert cns.cntnotify_wait_with_timeout(notify, s2, cns.CNS_WAIT_BIGGER_OR_EQUAL, 1, 10, 1) == 0
     s1.synchronize()
     s2.synchronize()
     st, c = count_of(cns, notify)
@@ -94,9 +95,9 @@ def test_n_producer_streams_fan_in(cns, notify):
     n = 6
     waiter = torch.cuda.Stream()
     prods = [torch.cuda.Stream() for _ in range(n)]
-    assert cns.cntnotify_wait_with_timeout(notify, waiter, cns.CNS_WAIT_BIGGER_OR_EQUAL, n, 10, 0) == 0
     for s in prods:
         assert cns.cntnotify_record(notify, s, cns.CNS_REC_ADD, 1) == 0
+    assert cns.cntnotify_wait_with_timeout(notify, waiter, cns.CNS_WAIT_BIGGER_OR_EQUAL, n, 10, 0) == 0
     torch.cuda.synchronize()
     st, c = count_of(cns, notify)
     assert st == 0 and c == n
@@ -107,10 +108,10 @@ def test_bitmask_multi_signal(cns, notify):
     waiter = torch.cuda.Stream()
     bits = [1 << k for k in (0, 3, 9, 31)]
     mask = sum(bits)
-    assert cns.cntnotify_wait_with_timeout(notify, waiter, cns.CNS_WAIT_EQUAL_WITH_BITMASK, mask, 10, 1) == 0
     streams = [torch.cuda.Stream() for _ in bits]
     for b, s in zip(bits, streams):
         assert cns.cntnotify_record(notify, s, cns.CNS_REC_BIT_OR, b) == 0
+    assert cns.cntnotify_wait_with_timeout(notify, waiter, cns.CNS_WAIT_EQUAL_WITH_BITMASK, mask, 10, 1) == 0
     torch.cuda.synchronize()
     st, c = count_of(cns, notify)
     assert st == 0 and c == 0
