@@ -109,6 +109,7 @@ _SIGS = {
     "cntnotify_query_status": (c_int, [c_void_p, POINTER(c_int32), POINTER(c_uint32)]),
     "cns_statemachine_scratch_bytes": (c_size_t, [c_int64]),
     "cns_statemachine_run": (c_int, [c_void_p, c_int64, c_uint32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "cns_statemachine_run_noalloc": (c_int, [c_void_p, c_int64, c_uint32, c_void_p, c_void_p, c_void_p]),
     "cns_pipeline_run": (c_int, [POINTER(Pipeline)]),
     "cns_probe_atomic_rtt": (c_int, [c_int, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "cns_probe_same_address_throughput": (c_int, [c_int32, c_int32, c_int32, c_void_p, c_void_p]),
@@ -250,6 +251,13 @@ def cns_statemachine_scratch_bytes(n: int) -> int:
 def cns_statemachine_run(ops, n: int, init: int, trace, final, scratch, scratch_bytes: int, stream=None) -> int:
     return lib().cns_statemachine_run(ptr(ops), n, init, ptr(trace), ptr(final), ptr(scratch), scratch_bytes,
                                       stream_handle(stream))
+
+
+CNS_STATEMACHINE_NOALLOC_MAX_OPS = 2097152
+
+
+def cns_statemachine_run_noalloc(ops, n: int, init: int, trace, final, stream=None) -> int:
+    return lib().cns_statemachine_run_noalloc(ptr(ops), n, init, ptr(trace), ptr(final), stream_handle(stream))
 
 
 def cns_pipeline_run(cfg: Pipeline) -> int:

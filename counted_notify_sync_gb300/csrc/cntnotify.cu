@@ -514,6 +514,73 @@ extern "C" int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t
 }
 
 // ---------------------------------------------------------------------------
+// State machine for callers that cannot allocate device memory
+// ---------------------------------------------------------------------------
+
+// The chunk summaries of cns_statemachine_run_noalloc live in this fixed
+// 1 MiB array, part of the library's own device image: every GPU that loads
+// the library holds it until the process exits.  On the host the name is
+// only a stand-in for the symbol, not a device address; the address comes
+// from cudaGetSymbolAddress, looked up once per device on first use.
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+static_assert(static_cast<size_t>(CNS_STATEMACHINE_NOALLOC_MAX_OPS) / kChunk * sizeof(uint2) == kNoAllocScratchBytes,
+              "the op limit must match the scratch array");
+static __device__ __align__(256) uint2 g_sm_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint2)];
+
+static std::mutex g_noalloc_mu;
+static uint2 *g_noalloc_scratch_addr[64];   // per device; filled on the first call there
+
+extern "C" int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, uint32_t init, uint32_t *trace_dev,
+                                            uint32_t *final_dev, cns_stream_t stream)
+{
+    if (n < 0 || n > CNS_STATEMACHINE_NOALLOC_MAX_OPS)
+        return CNS_ERR_INVALID_VALUE;
+    if (!final_dev)
+        return CNS_ERR_NULL_PTR;
+    if (n > 0 && (!ops_dev || !trace_dev))
+        return CNS_ERR_NULL_PTR;
+    if ((reinterpret_cast<uintptr_t>(ops_dev) & 15) || (reinterpret_cast<uintptr_t>(trace_dev) & 7))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    uint2 *summ = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (dev.device < 0 || dev.device >= 64)
+            return CNS_ERR_CUDA;
+        if (!g_noalloc_scratch_addr[dev.device]) {
+            void *p = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&p, g_sm_noalloc_scratch);
+            if (e != cudaSuccess || !p) {
+                (void)cudaGetLastError();
+                return cuda_fail(e, "cudaGetSymbolAddress(state-machine scratch)");
+            }
+            g_noalloc_scratch_addr[dev.device] = static_cast<uint2 *>(p);
+        }
+        summ = g_noalloc_scratch_addr[dev.device];
+    }
+    cudaStream_t s = to_stream(stream);
+    if (n == 0) {
+        write_word_kernel<<<1, 1, 0, s>>>(final_dev, init);
+        CNS_CUDA(cudaGetLastError());
+        return CNS_SUCCESS;
+    }
+    // The suffix kernel writes every summary the prefix kernel reads, so
+    // whatever an earlier call left in the array never matters.
+    const int64_t T = (n + kChunk - 1) / kChunk;
+    const int threads = 256;
+    const int64_t blocks = (T + threads - 1) / threads;
+    const uint4 *ops = reinterpret_cast<const uint4 *>(ops_dev);
+    uint2 *trace = reinterpret_cast<uint2 *>(trace_dev);
+    sm_suffix_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(ops, n, trace, summ, final_dev);
+    CNS_CUDA(cudaGetLastError());
+    sm_prefix_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(ops, n, init, trace, summ, final_dev);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
 // Two-stream pipeline
 // ---------------------------------------------------------------------------
 

@@ -342,6 +342,34 @@ int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t init, uint
                          uint32_t *final_dev, void *scratch_dev, size_t scratch_bytes,
                          cns_stream_t stream);
 
+/* Largest op count cns_statemachine_run_noalloc accepts (2^21). */
+#define CNS_STATEMACHINE_NOALLOC_MAX_OPS 2097152
+
+/*
+ * cns_statemachine_run_noalloc -- cns_statemachine_run for callers that may
+ * not allocate device memory.  The pages have no counterpart: this entry
+ * point exists for users of this library whose device memory is not theirs
+ * to allocate -- a plug-in running inside a host framework that owns every
+ * byte of the GPU through its own pool and refuses outside cudaMalloc calls
+ * once it is running, or a latency-critical loop that cannot afford
+ * cudaMalloc/cudaFree, which may synchronise the whole device and stall
+ * unrelated streams.  Such a caller still passes its inputs and outputs;
+ * the working space comes from a fixed 1 MiB array built into the library,
+ * which every GPU that loads the library holds until the process exits.
+ *   ops_dev, n, init, trace_dev, final_dev, stream: as cns_statemachine_run;
+ *   n may be at most CNS_STATEMACHINE_NOALLOC_MAX_OPS.
+ * The first call on each device looks up the array's device address there
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls on a device share the one array and
+ * it keeps what the last call left in it (nothing in it needs to start at
+ * zero): calls whose kernels overlap on the GPU, e.g. on two streams at once,
+ * race and give wrong traces.  No allocation happens in any call.
+ * Errors: INVALID_VALUE (n < 0 or above the limit, alignment), NULL_PTR,
+ * CUDA.
+ */
+int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, uint32_t init, uint32_t *trace_dev,
+                                 uint32_t *final_dev, cns_stream_t stream);
+
 /* Two-stream counting pipeline ([CNTN] §5: producers record ADD 1, the waiter
  * waits BIGGER_OR_EQUAL N with isClear = 1 and then continues). */
 typedef struct {
