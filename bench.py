@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-secondary", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
+                    help="run one small launch pattern for a profiler capture and exit")
     return ap.parse_args()
 
 
@@ -423,8 +425,72 @@ def run_native(args):
         torch.distributed.destroy_process_group()
 
 
+def case_soft148_small():
+    """Three launches of the headline kernel with 2000 rounds each (profiling)."""
+    import torch
+    import counted_notify_sync_gb300 as cns
+    cns.build()
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P_HEAD, SLOTS_HEAD)
+    b0 = torch.from_numpy(v0.view(np.int32).copy()).cuda()
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    for _ in range(3):
+        cns.run_syncall(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1, 2000,
+                        elems=SLOTS_HEAD, workspace=ws)
+    print("case soft148-small: ok")
+
+
+def case_hard148_small():
+    """Three launches of the hard-path kernel with 2000 rounds each (profiling)."""
+    import torch
+    import counted_notify_sync_gb300 as cns
+    cns.build()
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P_HEAD, SLOTS_HEAD)
+    b0 = torch.from_numpy(v0.view(np.int32).copy()).cuda()
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    for _ in range(3):
+        cns.run_syncall(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1, 2000,
+                        elems=SLOTS_HEAD, workspace=ws)
+    print("case hard148-small: ok")
+
+
+def case_jacobi_small():
+    """Three Jacobi launches, N = 2^25 fp32 (2 x 128 MiB, above L2), 592 CTAs, 4 sweeps (profiling)."""
+    import torch
+    import counted_notify_sync_gb300 as cns
+    cns.build()
+    N = 1 << 25
+    b0 = torch.from_numpy(ci.jacobi_field(N)).cuda()
+    b1 = torch.empty_like(b0)
+    ws = cns.new_workspace()
+    for _ in range(3):
+        cns.run_syncall(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_JACOBI, 592, b0, b1, 4, elems=N,
+                        workspace=ws)
+    print("case jacobi-small: ok")
+
+
+def case_statemachine():
+    """Three runs of the op-stream state machine on 1e6 ops (profiling)."""
+    import torch
+    import counted_notify_sync_gb300 as cns
+    cns.build()
+    ops_d = torch.from_numpy(ci.notify_ops(1_000_000).view(np.int32)).cuda()
+    for _ in range(3):
+        cns.run_statemachine(ops_d, 0)
+    torch.cuda.synchronize()
+    print("case statemachine: ok")
+
+
+CASES = {"soft148-small": case_soft148_small, "hard148-small": case_hard148_small,
+         "jacobi-small": case_jacobi_small, "statemachine": case_statemachine}
+
+
 def main():
     args = parse()
+    if args.case:
+        CASES[args.case]()
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
