@@ -240,7 +240,7 @@ def e2e_headline(cns, torch, args):
                         np.roll(v0, -ROUNDS_HEAD % P_HEAD, axis=0))
     ms = statistics.mean(times)
     return {"value": round(ms * 1e6 / ROUNDS_HEAD, 3), "unit": UNIT, "h2d_bytes_per_step": v0.nbytes,
-            "d2h_bytes_per_step": v0.nbytes + 384, "ms_per_step": round(ms, 3), "correct": bool(ok),
+            "d2h_bytes_per_step": v0.nbytes + cns.CNS_SYNCALL_WORKSPACE_BYTES, "ms_per_step": round(ms, 3), "correct": bool(ok),
             "path": "syncall_run(sync=1, host_in/host_out pinned): H2D + kernel + D2H + workspace read"}
 
 
@@ -257,7 +257,7 @@ def timed_run(torch, fn):
 def secondary(cns, torch, peaks):
     out = {}
 
-    def ring(mode, core, wl, ctas, P, slots, R, ratio=0, used=0, label=""):
+    def ring(mode, core, wl, ctas, P, slots, R, ratio=0, used=0, label="", variant=0):
         v0 = ci.ring_payload(1, P, slots)
         b0 = torch.from_numpy(v0.view(np.int32).copy()).cuda() if v0.size else None
         b1 = torch.zeros_like(b0) if v0.size else None
@@ -266,13 +266,20 @@ def secondary(cns, torch, peaks):
         for _ in range(3):
             ms, (d, rc) = timed_run(torch, lambda: cns.run_syncall(
                 mode, core, wl, ctas, b0, b1, R, used_cores=used, aiv_ratio=ratio, elems=slots, workspace=ws,
-                sync=False))
+                sync=False, variant=variant))
             runs.append(ms)
         rc, soft, hard, st = cns.syncall_read_workspace(ws)
         ms = min(runs)
         out[label] = {"ns_per_round": round(ms * 1e6 / R, 2), "rounds": R, "participants": P,
                       "cluster": d.cluster_used, "status": st}
 
+    for v in range(5):
+        ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
+             label=f"soft_148_ring_rotate_variant{v}")
+        ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_EMPTY, 148, 148, 0, 100000, variant=v,
+             label=f"soft_148_empty_variant{v}")
+        ring(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
+             label=f"hard_148_ring_rotate_variant{v}")
     ring(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000,
          label="hard_148_ring_rotate")
     ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_EMPTY, 148, 148, 0, 100000, label="soft_148_empty")

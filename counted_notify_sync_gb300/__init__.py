@@ -27,7 +27,7 @@ def _torch():
 
 
 def new_workspace(device=None, start_value: int = 0, stream=None):
-    """A zeroed SYNCALL workspace (384 bytes, 128-byte aligned) on `device`."""
+    """A zeroed SYNCALL workspace (CNS_SYNCALL_WORKSPACE_BYTES, 128-byte aligned) on `device`."""
     torch = _torch()
     ws = torch.empty(_native.CNS_SYNCALL_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device or "cuda")
     _native.check(_native.syncall_workspace_init(ws, ws.numel() * 4, start_value, stream), "syncall_workspace_init")
@@ -36,7 +36,7 @@ def new_workspace(device=None, start_value: int = 0, stream=None):
 
 def run_syncall(mode, core_type, workload, launch_ctas, buf0, buf1, rounds, *, used_cores=0, aiv_ratio=0,
                 elems=0, threads=256, cluster_dim=0, timeout_ms=0, workspace=None, cta_status=None,
-                stream=None, sync=True, host_in=None, host_out=None, check=True):
+                stream=None, sync=True, host_in=None, host_out=None, check=True, variant=0):
     """Call syncall_run with device buffers (torch tensors); returns the filled SyncallData and the code."""
     d = _native.SyncallData()
     d.workload = workload
@@ -53,6 +53,7 @@ def run_syncall(mode, core_type, workload, launch_ctas, buf0, buf1, rounds, *, u
     d.sync = 1 if sync else 0
     d.host_in = _native.ptr(host_in)
     d.host_out = _native.ptr(host_out)
+    d.barrier_variant = variant
     rc = _native.syncall_run(mode, core_type, used_cores, aiv_ratio, rounds, d)
     if check and rc != _native.CNS_SUCCESS:
         raise _native.CnsError(rc, "syncall_run")

@@ -25,6 +25,13 @@ __device__ __forceinline__ uint32_t atom_inc_release_gpu(uint32_t *p, uint32_t b
     return old;
 }
 
+__device__ __forceinline__ uint32_t atom_inc_acq_rel_gpu(uint32_t *p, uint32_t bound)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v)
 {
     uint32_t old;
@@ -97,6 +104,11 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
 __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void fence_acq_rel_gpu()
@@ -194,19 +206,48 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
     atom_exch_release_gpu(status_line + 1, 1u);
 }
 
-// Poll `ctr` until it reaches `target`.  Returns false when released, true
-// when the wait gave up (timeout here, or an abort raised by another waiter).
-// The abort flag and the clock are looked at once every 64 polls.
-__device__ __forceinline__ bool poll_epoch(const uint32_t *ctr, uint32_t target, const Epoch &e,
+// Barrier variants (cns_syncall_data_t.barrier_variant).  All of them arrive
+// with one atomic increment of the counter and take the target from the
+// value it returns, as the guide's soft barrier does; they differ in how a
+// participant learns that the target was reached.
+//   0  poll the counter with acquire loads (the guide's form, every arrival
+//      polls, even the last one)
+//   1  as 0, but the arrival is acquire-release and the last arriver of a
+//      round, whose own increment reached the target, does not poll
+//   2  as 1, with relaxed polling loads and one acquire fence once released
+//   3  as 2, with a 32 ns pause between polls (less traffic on the line)
+//   4  flag broadcast: the last arriver publishes the target to a release
+//      word on its own line; the others poll that word, not the counter
+enum : int { kBvCounterAcquire = 0, kBvLastSkips = 1, kBvRelaxedPoll = 2, kBvBackoff = 3, kBvFlag = 4 };
+
+struct Barrier {
+    uint32_t *ctr;          // arrival counter
+    uint32_t *flag;         // release word (variant 4)
+    uint32_t *status_line;  // status, abort, fail round, fail CTA
+    Epoch e;
+    uint64_t timeout_ns;
+    int variant;
+};
+
+// Wait until *word has reached `target` (in Z_M).  Returns false when
+// released, true when the wait gave up (timeout here, or an abort raised by
+// another waiter).  The abort flag and the clock are looked at once every 64
+// polls.  With relaxed polls, one acquire fence follows the successful load.
+__device__ __forceinline__ bool poll_epoch(const uint32_t *word, uint32_t target, const Epoch &e,
                                            uint32_t *status_line, uint64_t timeout_ns, uint32_t round,
-                                           uint32_t who)
+                                           uint32_t who, bool relaxed = false, uint32_t pause_ns = 0)
 {
     uint32_t spins = 0;
     uint64_t deadline = 0;
     for (;;) {
-        const uint32_t cur = ld_acquire_gpu(ctr);
-        if (epoch_reached(cur, target, e))
+        const uint32_t cur = relaxed ? ld_relaxed_gpu(word) : ld_acquire_gpu(word);
+        if (epoch_reached(cur, target, e)) {
+            if (relaxed)
+                fence_acq_rel_gpu();
             return false;
+        }
+        if (pause_ns)
+            __nanosleep(pause_ns);
         if ((++spins & 63u) == 0u) {
             if (ld_relaxed_gpu(status_line + 1) != 0u)
                 return true;
@@ -221,35 +262,52 @@ __device__ __forceinline__ bool poll_epoch(const uint32_t *ctr, uint32_t target,
     }
 }
 
+// The elected thread's part of one barrier: arrive, compute the target from
+// the returned value, wait for it.  Returns true if the caller must stop.
+__device__ __forceinline__ bool arrive_and_wait(const Barrier &b, uint32_t round, uint32_t who)
+{
+    const int v = b.variant;
+    const uint32_t before = (v == kBvCounterAcquire) ? atom_inc_release_gpu(b.ctr, b.e.Mm1)
+                                                     : atom_inc_acq_rel_gpu(b.ctr, b.e.Mm1);
+    const uint32_t target = epoch_target(before, b.e);
+    if (v != kBvCounterAcquire) {
+        const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;   // the count after this arrival
+        if (epoch_reached(mine, target, b.e)) {
+            // the last arrival of the round: its acquire-release increment has
+            // already seen every other arrival of the round
+            if (v == kBvFlag)
+                st_release_gpu(b.flag, target);
+            return false;
+        }
+    }
+    if (v == kBvFlag)
+        return poll_epoch(b.flag, target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
+    return poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who, v >= kBvRelaxedPoll,
+                      v == kBvBackoff ? 32u : 0u);
+}
+
 // One soft barrier for the calling CTA: drain the CTA, one elected thread
-// arrives and polls, drain again.  All threads of the CTA must call it.
+// arrives and waits, drain again.  All threads of the CTA must call it.
 // Returns true if the CTA must stop (timeout / abort).
-__device__ __forceinline__ bool soft_barrier(uint32_t *ctr, const Epoch &e, uint32_t *status_line,
-                                             uint64_t timeout_ns, uint32_t round, int *s_flag)
+__device__ __forceinline__ bool soft_barrier(const Barrier &b, uint32_t round, int *s_flag)
 {
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t before = atom_inc_release_gpu(ctr, e.Mm1);
-        const uint32_t target = epoch_target(before, e);
-        *s_flag = poll_epoch(ctr, target, e, status_line, timeout_ns, round, blockIdx.x) ? 1 : 0;
-    }
+    if (threadIdx.x == 0)
+        *s_flag = arrive_and_wait(b, round, blockIdx.x) ? 1 : 0;
     __syncthreads();
     return *s_flag != 0;
 }
 
 // One hard barrier: cluster barrier; cluster rank 0 arrives on the
-// per-cluster counter (P = number of clusters) and polls it; on a timeout it
+// per-cluster counter (P = number of clusters) and waits; on a timeout it
 // writes the stop flag into every CTA of its cluster; second cluster barrier.
 // All threads of all CTAs of the cluster must call it.
-__device__ __forceinline__ bool hard_barrier(uint32_t *ctr, const Epoch &e, uint32_t *status_line,
-                                             uint64_t timeout_ns, uint32_t round, int *s_flag)
+__device__ __forceinline__ bool hard_barrier(const Barrier &b, uint32_t round, int *s_flag)
 {
     __syncwarp();
     cluster_sync_all();
     if (threadIdx.x == 0 && cluster_ctarank() == 0) {
-        const uint32_t before = atom_inc_release_gpu(ctr, e.Mm1);
-        const uint32_t target = epoch_target(before, e);
-        if (poll_epoch(ctr, target, e, status_line, timeout_ns, round, blockIdx.x)) {
+        if (arrive_and_wait(b, round, blockIdx.x)) {
             const uint32_t n = cluster_nctarank();
             for (uint32_t r = 0; r < n; ++r)
                 st_shared_cluster(s_flag, r, 1u);

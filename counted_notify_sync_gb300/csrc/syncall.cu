@@ -26,11 +26,8 @@ struct SyncallParams {
     void *buf1;
     int64_t elems;          // ring: slots per participant; Jacobi: field length
     int64_t rounds;
-    uint32_t *ctr;          // the counter this path arrives on
-    uint32_t *status_line;  // workspace line 1
+    Barrier bar;            // counter, release word, status line, epoch, timeout, variant
     int32_t *cta_status;    // optional per-CTA marks
-    uint64_t timeout_ns;
-    Epoch epoch;            // P and bound of `ctr`
     uint32_t P;             // participants (ring length / Jacobi chunks)
     uint32_t group;         // MIX group size, else 1
     int32_t core_type;
@@ -180,9 +177,8 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
     bool stop = false;
     for (int64_t r = 0; r < p.rounds; ++r) {
         data_phase<WL>(p, r, b);
-        stop = (MODE == CNS_SYNCALL_SOFT)
-                   ? soft_barrier(p.ctr, p.epoch, p.status_line, p.timeout_ns, static_cast<uint32_t>(r), &s_flag)
-                   : hard_barrier(p.ctr, p.epoch, p.status_line, p.timeout_ns, static_cast<uint32_t>(r), &s_flag);
+        stop = (MODE == CNS_SYNCALL_SOFT) ? soft_barrier(p.bar, static_cast<uint32_t>(r), &s_flag)
+                                          : hard_barrier(p.bar, static_cast<uint32_t>(r), &s_flag);
         if (stop)
             break;
     }
@@ -198,6 +194,8 @@ __global__ void workspace_init_kernel(uint32_t *ws, uint32_t n_words, uint32_t s
     if (threadIdx.x == 0) {
         ws[0] = start;                                  // soft counter
         ws[2 * CNS_SYNCALL_LINE_BYTES / 4] = start;     // hard counter
+        ws[3 * CNS_SYNCALL_LINE_BYTES / 4] = start;     // soft release word
+        ws[3 * CNS_SYNCALL_LINE_BYTES / 4 + 16] = start;  // hard release word
     }
 }
 
@@ -311,6 +309,8 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return CNS_ERR_INVALID_VALUE;
     if (d->workload < CNS_WL_EMPTY || d->workload > CNS_WL_JACOBI)
         return CNS_ERR_INVALID_VALUE;
+    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_FLAG_BROADCAST)
+        return CNS_ERR_INVALID_VALUE;
     if (rounds < 0 || used_cores < 0 || aiv_ratio < 0 || d->launch_ctas <= 0 || d->elems < 0)
         return CNS_ERR_INVALID_VALUE;
     const int threads = d->threads ? d->threads : 256;
@@ -388,20 +388,23 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     prm.elems = d->elems;
     prm.rounds = rounds;
     uint32_t *ws = static_cast<uint32_t *>(d->workspace_dev);
-    prm.status_line = ws + CNS_SYNCALL_LINE_BYTES / 4;
+    prm.bar.status_line = ws + CNS_SYNCALL_LINE_BYTES / 4;
+    prm.bar.timeout_ns = barrier_timeout_ns(d->timeout_ms);
+    prm.bar.variant = d->barrier_variant;
     prm.cta_status = d->cta_status_dev;
-    prm.timeout_ns = barrier_timeout_ns(d->timeout_ms);
     prm.P = P;
     prm.group = static_cast<uint32_t>(group);
     prm.core_type = core_type;
     if (mode == CNS_SYNCALL_SOFT) {
-        prm.ctr = ws;
-        prm.epoch.P = P;
+        prm.bar.ctr = ws;
+        prm.bar.flag = ws + 3 * CNS_SYNCALL_LINE_BYTES / 4;
+        prm.bar.e.P = P;
     } else {
-        prm.ctr = ws + 2 * CNS_SYNCALL_LINE_BYTES / 4;
-        prm.epoch.P = static_cast<uint32_t>(grid / C);
+        prm.bar.ctr = ws + 2 * CNS_SYNCALL_LINE_BYTES / 4;
+        prm.bar.flag = ws + 3 * CNS_SYNCALL_LINE_BYTES / 4 + 16;
+        prm.bar.e.P = static_cast<uint32_t>(grid / C);
     }
-    prm.epoch.Mm1 = counter_bound(prm.epoch.P);
+    prm.bar.e.Mm1 = counter_bound(prm.bar.e.P);
 
     d->grid_ctas = grid;
     d->participants = static_cast<int32_t>(P);

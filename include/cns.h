@@ -83,16 +83,40 @@ typedef enum {
     CNS_WL_JACOBI = 4
 } cns_workload_t;
 
-/* Workspace layout: three 128-byte lines (the GB300 L2 line; also one of the
+/* Workspace layout: four 128-byte lines (the GB300 L2 line; also one of the
  * 64-byte lines [SYNCALL] §4.1 asks the counter to own exclusively):
  *   line 0  word 0: soft counter
  *   line 1  words 0..3: status (0 or CNS_ERR_TIMEOUT), abort flag,
  *           round at which a wait gave up, CTA that gave up
  *   line 2  word 0: hard-path counter (one arrival per cluster)
+ *   line 3  word 0: soft release word, word 16: hard release word (used by
+ *           CNS_BARRIER_FLAG_BROADCAST only)
  * The base must be 128-byte aligned.  [SYNCALL] §4.1: it must be zeroed
  * before first use and shared with no other data. */
 #define CNS_SYNCALL_LINE_BYTES 128
-#define CNS_SYNCALL_WORKSPACE_BYTES 384
+#define CNS_SYNCALL_WORKSPACE_BYTES 512
+
+/* How a participant learns that a round's target was reached
+ * (cns_syncall_data_t.barrier_variant).  Every variant arrives with one atomic
+ * increment and takes target = (before / P + 1) * P from the value returned
+ * ([SYNCALL] §5.2); they differ only in the wait:
+ *   COUNTER_ACQUIRE   poll the counter with acquire loads, every arrival
+ *                     (the guide's form)
+ *   LAST_SKIPS        acquire-release arrival; the arrival that itself reaches
+ *                     the target does not poll; the others poll as above
+ *   RELAXED_POLL      as LAST_SKIPS, polling with relaxed loads and one acquire
+ *                     fence once released
+ *   BACKOFF           as RELAXED_POLL, pausing 32 ns between polls
+ *   FLAG_BROADCAST    the last arrival publishes the target to a release word on
+ *                     its own line (workspace line 3) and the others poll that
+ *                     word instead of the counter line */
+typedef enum {
+    CNS_BARRIER_COUNTER_ACQUIRE = 0,
+    CNS_BARRIER_LAST_SKIPS = 1,
+    CNS_BARRIER_RELAXED_POLL = 2,
+    CNS_BARRIER_BACKOFF = 3,
+    CNS_BARRIER_FLAG_BROADCAST = 4
+} cns_barrier_variant_t;
 
 /* CTA status words written to cns_syncall_data_t.cta_status_dev (optional).
  * The low byte is the outcome, bits 8..15 the role (0 AIV, 1 AIC). */
@@ -146,7 +170,8 @@ typedef struct {
     int32_t grid_ctas;       /* (out) CTAs launched */
     int32_t participants;    /* (out) resolved participant count P */
     int32_t cluster_used;    /* (out) CTAs per cluster (1 for SOFT) */
-    int32_t reserved[4];
+    int32_t barrier_variant; /* (in) cns_barrier_variant_t; 0 = the guide's counter poll */
+    int32_t reserved[3];
 } cns_syncall_data_t;
 
 /*
@@ -164,6 +189,7 @@ typedef struct {
  *               per cluster on the hard counter by cluster rank 0, then a
  *               second cluster barrier that releases the cluster (the two-level
  *               shape of the guide's MIX hard path, §5.1).
+ *               Both paths wait as data->barrier_variant says.
  *   core_type   cns_core_type_t ([SYNCALL] §3.1)
  *   used_cores  participants; 0 = automatic: the CTAs launched for AIV/AIC-
  *               only, launch_ctas * (1 + ratio) for MIX ([SYNCALL] §4.2).  A

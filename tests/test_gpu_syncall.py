@@ -23,7 +23,7 @@ def cns():
 
 
 def run_ring(cns, mode, core, wl, launch_ctas, v0, rounds, used=0, ratio=0, start=0, threads=256,
-             cluster_dim=0, timeout_ms=0, check=True):
+             cluster_dim=0, timeout_ms=0, check=True, variant=0):
     import torch
     P, slots = v0.shape
     b0 = to_dev_u32(v0) if v0.size else None
@@ -33,7 +33,7 @@ def run_ring(cns, mode, core, wl, launch_ctas, v0, rounds, used=0, ratio=0, star
     status = torch.zeros(launch_ctas * group, dtype=torch.int32, device="cuda")
     d, rc = cns.run_syncall(mode, core, wl, launch_ctas, b0, b1, rounds, used_cores=used, aiv_ratio=ratio,
                             elems=slots, threads=threads, cluster_dim=cluster_dim, workspace=ws,
-                            cta_status=status, timeout_ms=timeout_ms, check=check)
+                            cta_status=status, timeout_ms=timeout_ms, check=check, variant=variant)
     torch.cuda.synchronize()
     final = from_dev_u32(b1 if rounds & 1 else b0).reshape(P, slots) if v0.size else v0.copy()
     return d, rc, final, status.cpu().numpy()
@@ -270,3 +270,57 @@ def test_grid_that_cannot_be_resident_is_refused(cns):
     d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_EMPTY, sms * 64 + 1, None, None, 1, threads=1024, workspace=ws,
                             check=False)
     assert rc == cns.CNS_ERR_NOT_RESIDENT
+
+
+# --- barrier variants: same results, every wait form ----------------------------------------
+
+VARIANTS = [0, 1, 2, 3, 4]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_variants_ring_rotate_148(cns, variant, mode):
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, 20001, variant=variant)
+    np.testing.assert_array_equal(got, np.roll(v0, -20001, axis=0))
+    assert d.device_status == 0 and (st == cns.CNS_CTA_DONE).all()
+    assert d.final_counter == 20001 * (148 if mode == SOFT else 148 // d.cluster_used)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_variants_affine_and_mix(cns, variant):
+    v0 = ci.ring_payload(ci.SEED_RING_AFFINE, 8, 256)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, 1000, variant=variant)
+    want, fc = expect_ring(oracle.WL_RING_AFFINE, v0, 1000)
+    np.testing.assert_array_equal(got, want)
+    v1 = ci.ring_payload(ci.SEED_XORSHIFT, 111, 256)
+    d, rc, got, st = run_ring(cns, HARD, MIX, cns.CNS_WL_XORSHIFT, 37, v1, 2000, ratio=2, variant=variant)
+    want, _ = expect_ring(oracle.WL_XORSHIFT, v1, 2000)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_variants_wrap_and_jacobi(cns, variant):
+    P = 111
+    M = oracle.counter_modulus(P)
+    v0 = ci.ring_payload(9, P, 4)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, P, v0, 12, start=M - 5 * P, variant=variant)
+    want, fc = expect_ring(oracle.WL_RING_AFFINE, v0, 12, M - 5 * P)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == fc
+    import torch
+    u0 = ci.jacobi_field(300007)
+    b0 = to_dev_f32(u0)
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    cns.run_syncall(SOFT, AIV, cns.CNS_WL_JACOBI, 592, b0, b1, 8, elems=u0.size, workspace=ws, variant=variant)
+    want, _, _ = oracle.syncall_run_jacobi(u0, 8, 592)
+    np.testing.assert_array_equal(b0.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_variants_time_out_cleanly(cns, variant):
+    v0 = ci.ring_payload(3, 4, 4)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3, start=1, timeout_ms=200,
+                              check=False, variant=variant)
+    assert rc == cns.CNS_ERR_TIMEOUT
