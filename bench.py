@@ -38,6 +38,7 @@ UNIT = "ns/round"
 P_HEAD, SLOTS_HEAD, ROUNDS_HEAD = 148, 4, 100000
 WORKLOAD = ("soft SYNCALL, AIV-only, 148 CTAs x 256 threads (1 per SM), ring-rotate payload of 4 uint32 per CTA, "
             "100000 rounds per launch, counter zeroed at start")
+VARIANT_NAMES = ["counter_acquire", "last_skips", "relaxed_poll", "backoff", "flag_broadcast", "die_local"]
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -48,6 +49,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-secondary", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--variant", type=int, default=5, help="barrier variant of the headline (cns_barrier_variant_t)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="run one small launch pattern for a profiler capture and exit")
@@ -195,7 +197,7 @@ def headline(cns, torch, args, stream):
 
     def step(s):
         cns.run_syncall(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1,
-                        ROUNDS_HEAD, elems=SLOTS_HEAD, workspace=ws, stream=s, sync=False)
+                        ROUNDS_HEAD, elems=SLOTS_HEAD, workspace=ws, stream=s, sync=False, variant=args.variant)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -233,7 +235,8 @@ def e2e_headline(cns, torch, args):
     times = []
     for i in range(args.warmup + args.steps):
         d, rc = cns.run_syncall(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1,
-                                ROUNDS_HEAD, elems=SLOTS_HEAD, workspace=ws, sync=True, host_in=hin, host_out=hout)
+                                ROUNDS_HEAD, elems=SLOTS_HEAD, workspace=ws, sync=True, host_in=hin, host_out=hout,
+                                variant=args.variant)
         if i >= args.warmup:
             times.append(d.elapsed_ms)
     ok = np.array_equal(hout.numpy().view(np.uint32).reshape(P_HEAD, SLOTS_HEAD),
@@ -273,7 +276,7 @@ def secondary(cns, torch, peaks):
         out[label] = {"ns_per_round": round(ms * 1e6 / R, 2), "rounds": R, "participants": P,
                       "cluster": d.cluster_used, "status": st}
 
-    for v in range(5):
+    for v in range(6):
         ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
              label=f"soft_148_ring_rotate_variant{v}")
         ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_EMPTY, 148, 148, 0, 100000, variant=v,
@@ -406,6 +409,7 @@ def run_native(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "u32", "data": "synthetic (SplitMix64 seeded uniform uint32)",
         "config": {"workload": WORKLOAD, "participants": P_HEAD, "threads_per_cta": 256, "rounds": ROUNDS_HEAD,
+                   "barrier_variant": VARIANT_NAMES[args.variant],
                    "payload_bytes": P_HEAD * SLOTS_HEAD * 4, "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (256 MiB write), outside the step events",
                    "timed_region_wall_s": round(wall, 4)},

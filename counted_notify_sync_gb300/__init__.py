@@ -26,10 +26,12 @@ def _torch():
     return torch
 
 
-def new_workspace(device=None, start_value: int = 0, stream=None):
-    """A zeroed SYNCALL workspace (CNS_SYNCALL_WORKSPACE_BYTES, 128-byte aligned) on `device`."""
+def new_workspace(device=None, start_value: int = 0, stream=None, die_local: bool = True):
+    """A zeroed SYNCALL workspace on `device`: CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES long (usable by every
+    barrier variant) or, with die_local=False, the minimal CNS_SYNCALL_WORKSPACE_BYTES."""
     torch = _torch()
-    ws = torch.empty(_native.CNS_SYNCALL_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device or "cuda")
+    nbytes = _native.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES if die_local else _native.CNS_SYNCALL_WORKSPACE_BYTES
+    ws = torch.empty(nbytes // 4, dtype=torch.int32, device=device or "cuda")
     _native.check(_native.syncall_workspace_init(ws, ws.numel() * 4, start_value, stream), "syncall_workspace_init")
     return ws
 
@@ -54,6 +56,7 @@ def run_syncall(mode, core_type, workload, launch_ctas, buf0, buf1, rounds, *, u
     d.host_in = _native.ptr(host_in)
     d.host_out = _native.ptr(host_out)
     d.barrier_variant = variant
+    d.workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
     rc = _native.syncall_run(mode, core_type, used_cores, aiv_ratio, rounds, d)
     if check and rc != _native.CNS_SUCCESS:
         raise _native.CnsError(rc, "syncall_run")

@@ -44,6 +44,9 @@ CNS_BARRIER_LAST_SKIPS = 1
 CNS_BARRIER_RELAXED_POLL = 2
 CNS_BARRIER_BACKOFF = 3
 CNS_BARRIER_FLAG_BROADCAST = 4
+CNS_BARRIER_DIE_LOCAL = 5
+CNS_SYNCALL_REPLICA_OFFSET = 4096
+CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES = 8192
 CNS_CTA_DONE = 1
 CNS_CTA_IDLE = 2
 CNS_CTA_ABORTED = 4
@@ -77,7 +80,7 @@ class SyncallData(Structure):
         ("cta_status_dev", c_void_p), ("stream", c_void_p), ("timeout_ms", c_uint32), ("sync", c_int32),
         ("host_in", c_void_p), ("host_out", c_void_p), ("elapsed_ms", c_float), ("final_counter", c_uint32),
         ("device_status", c_int32), ("grid_ctas", c_int32), ("participants", c_int32), ("cluster_used", c_int32),
-        ("barrier_variant", c_int32), ("reserved", c_int32 * 3),
+        ("barrier_variant", c_int32), ("workspace_bytes", c_uint32), ("reserved", c_int32 * 2),
     ]
 
 

@@ -174,11 +174,16 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         __syncthreads();
     }
 
+    // the elected thread's copy of the barrier description (variant 5 turns
+    // its counter pair into near / far for this SM)
+    Barrier bar = p.bar;
+    if (bar.variant == kBvDieLocal && threadIdx.x == 0 && (MODE == CNS_SYNCALL_SOFT || cluster_ctarank() == 0))
+        choose_near_copy(bar);
     bool stop = false;
     for (int64_t r = 0; r < p.rounds; ++r) {
         data_phase<WL>(p, r, b);
-        stop = (MODE == CNS_SYNCALL_SOFT) ? soft_barrier(p.bar, static_cast<uint32_t>(r), &s_flag)
-                                          : hard_barrier(p.bar, static_cast<uint32_t>(r), &s_flag);
+        stop = (MODE == CNS_SYNCALL_SOFT) ? soft_barrier(bar, static_cast<uint32_t>(r), &s_flag)
+                                          : hard_barrier(bar, static_cast<uint32_t>(r), &s_flag);
         if (stop)
             break;
     }
@@ -186,16 +191,28 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         p.cta_status[b] = static_cast<int32_t>((stop ? CNS_CTA_ABORTED : CNS_CTA_DONE) | (role << 8));
 }
 
-__global__ void workspace_init_kernel(uint32_t *ws, uint32_t n_words, uint32_t start)
+// Word offsets of the second copies of the counters (die-local variant).
+constexpr uint32_t kSoftCopyWord = CNS_SYNCALL_REPLICA_OFFSET / 4;
+constexpr uint32_t kHardCopyWord = (CNS_SYNCALL_REPLICA_OFFSET + 2 * CNS_SYNCALL_LINE_BYTES) / 4;
+
+__global__ void workspace_init_kernel(uint32_t *ws, uint32_t n_words, uint32_t start, int with_copies)
 {
     for (uint32_t i = threadIdx.x; i < n_words; i += blockDim.x)
         ws[i] = 0u;
+    if (with_copies) {
+        for (uint32_t i = threadIdx.x; i < 3 * CNS_SYNCALL_LINE_BYTES / 4; i += blockDim.x)
+            ws[kSoftCopyWord + i] = 0u;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         ws[0] = start;                                  // soft counter
         ws[2 * CNS_SYNCALL_LINE_BYTES / 4] = start;     // hard counter
         ws[3 * CNS_SYNCALL_LINE_BYTES / 4] = start;     // soft release word
         ws[3 * CNS_SYNCALL_LINE_BYTES / 4 + 16] = start;  // hard release word
+        if (with_copies) {
+            ws[kSoftCopyWord] = start;
+            ws[kHardCopyWord] = start;
+        }
     }
 }
 
@@ -274,8 +291,10 @@ extern "C" int syncall_workspace_init(void *ws_dev, size_t bytes, uint32_t start
     DeviceInfo dev;
     if (int rc = current_device(&dev))
         return rc;
+    const int with_copies = bytes >= CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES ? 1 : 0;
     workspace_init_kernel<<<1, 128, 0, to_stream(stream)>>>(static_cast<uint32_t *>(ws_dev),
-                                                             CNS_SYNCALL_WORKSPACE_BYTES / 4, start_value);
+                                                             CNS_SYNCALL_WORKSPACE_BYTES / 4, start_value,
+                                                             with_copies);
     CNS_CUDA(cudaGetLastError());
     return CNS_SUCCESS;
 }
@@ -309,7 +328,11 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return CNS_ERR_INVALID_VALUE;
     if (d->workload < CNS_WL_EMPTY || d->workload > CNS_WL_JACOBI)
         return CNS_ERR_INVALID_VALUE;
-    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_FLAG_BROADCAST)
+    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_DIE_LOCAL)
+        return CNS_ERR_INVALID_VALUE;
+    if (d->workspace_bytes != 0 && d->workspace_bytes < CNS_SYNCALL_WORKSPACE_BYTES)
+        return CNS_ERR_INVALID_VALUE;
+    if (d->barrier_variant == CNS_BARRIER_DIE_LOCAL && d->workspace_bytes < CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES)
         return CNS_ERR_INVALID_VALUE;
     if (rounds < 0 || used_cores < 0 || aiv_ratio < 0 || d->launch_ctas <= 0 || d->elems < 0)
         return CNS_ERR_INVALID_VALUE;
@@ -397,10 +420,12 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     prm.core_type = core_type;
     if (mode == CNS_SYNCALL_SOFT) {
         prm.bar.ctr = ws;
+        prm.bar.ctr2 = ws + kSoftCopyWord;
         prm.bar.flag = ws + 3 * CNS_SYNCALL_LINE_BYTES / 4;
         prm.bar.e.P = P;
     } else {
         prm.bar.ctr = ws + 2 * CNS_SYNCALL_LINE_BYTES / 4;
+        prm.bar.ctr2 = ws + kHardCopyWord;
         prm.bar.flag = ws + 3 * CNS_SYNCALL_LINE_BYTES / 4 + 16;
         prm.bar.e.P = static_cast<uint32_t>(grid / C);
     }

@@ -58,7 +58,7 @@ int main(void) {
   F(cns_syncall_data_t, buf0_dev); F(cns_syncall_data_t, elems); F(cns_syncall_data_t, stream);
   F(cns_syncall_data_t, timeout_ms); F(cns_syncall_data_t, host_in); F(cns_syncall_data_t, elapsed_ms);
   F(cns_syncall_data_t, final_counter); F(cns_syncall_data_t, cluster_used); F(cns_syncall_data_t, barrier_variant);
-  F(cns_syncall_data_t, reserved);
+  F(cns_syncall_data_t, workspace_bytes); F(cns_syncall_data_t, reserved);
   printf("cns_record_info_t %zu\n", sizeof(cns_record_info_t));
   printf("cns_wait_info_t %zu\n", sizeof(cns_wait_info_t));
   F(cns_wait_info_t, is_clear);
@@ -84,7 +84,7 @@ def test_ctypes_structs_match_c_layout():
     S, P, W = _native.SyncallData, _native.Pipeline, _native.WaitInfo
     assert lay["cns_syncall_data_t"] == ctypes.sizeof(S)
     for f in ["buf0_dev", "elems", "stream", "timeout_ms", "host_in", "elapsed_ms", "final_counter",
-              "cluster_used", "barrier_variant", "reserved"]:
+              "cluster_used", "barrier_variant", "workspace_bytes", "reserved"]:
         assert lay[f"cns_syncall_data_t.{f}"] == getattr(S, f).offset, f
     assert lay["cns_record_info_t"] == ctypes.sizeof(_native.RecordInfo) == 8
     assert lay["cns_wait_info_t"] == ctypes.sizeof(W) == 16
@@ -139,8 +139,12 @@ def test_syncall_argument_checks(built):
     d.threads, d.cluster_dim = 256, 3
     assert cns.syncall_run(0, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # 3 does not divide 8
     assert cns.syncall_run(0, cns.CNS_MIX, 0, 8, 1, d) == cns.CNS_ERR_INVALID_VALUE  # cluster of 9
-    d.cluster_dim, d.barrier_variant = 0, 5
+    d.cluster_dim, d.barrier_variant = 0, 6
     assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # barrier variant
+    d.barrier_variant, d.workspace_bytes = cns.CNS_BARRIER_DIE_LOCAL, 512
+    assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # die-local needs 8 KB
+    d.barrier_variant, d.workspace_bytes = 0, 256
+    assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # workspace too small
     assert L.syncall_workspace_init(None, 512, 0, None) == cns.CNS_ERR_NULL_PTR
     assert L.syncall_workspace_init(0x1000, 511, 0, None) == cns.CNS_ERR_INVALID_VALUE
 

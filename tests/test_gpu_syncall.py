@@ -274,7 +274,7 @@ def test_grid_that_cannot_be_resident_is_refused(cns):
 
 # --- barrier variants: same results, every wait form ----------------------------------------
 
-VARIANTS = [0, 1, 2, 3, 4]
+VARIANTS = [0, 1, 2, 3, 4, 5]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
