@@ -202,67 +202,157 @@ __device__ __forceinline__ uint32_t sm_apply(uint32_t c, const uint4 &op, uint32
 
 __device__ __forceinline__ bool is_set_record(const uint4 &op) { return op.x == 0u && op.y == CNS_REC_SET; }
 
-__global__ void __launch_bounds__(256) sm_suffix_kernel(const uint4 *ops, int64_t n, uint2 *trace, uint2 *summ,
-                                                        uint32_t *final_count)
+// Both kernels stage one CTA's 256 chunks (4096 ops) through shared memory
+// so that every global access is coalesced.  Chunk k of the CTA sits at slot
+// k * (kChunk + 1): the one-slot pad spreads the per-thread walks over all
+// banks.  Trace entries are staged the same way with a sentinel outcome; only
+// the entries a kernel computed are written back.
+constexpr int kSmThreads = 256;
+constexpr int kCtaOps = kChunk * kSmThreads;
+constexpr int kPad = kChunk + 1;
+constexpr uint32_t kNoEntry = 0xFFFFFFFFu;
+constexpr size_t kSmSmemBytes = static_cast<size_t>(kSmThreads) * kPad * (sizeof(uint4) + sizeof(uint2));
+
+__device__ __forceinline__ int sm_slot(int i) { return (i / kChunk) * kPad + (i % kChunk); }
+
+// Load this CTA's ops into shared memory and mark every trace slot empty.
+__device__ __forceinline__ int sm_stage(const uint4 *ops, int64_t n, int64_t base, uint4 *s_ops, uint2 *s_tr)
 {
-    const int64_t T = (n + kChunk - 1) / kChunk;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (t >= T)
-        return;
-    const int64_t s0 = t * kChunk;
-    const int m = (n - s0 < kChunk) ? static_cast<int>(n - s0) : kChunk;
-    uint4 op[kChunk];
-#pragma unroll
-    for (int k = 0; k < kChunk; ++k)
-        op[k] = (k < m) ? ops[s0 + k] : make_uint4(2u, 0u, 0u, 0u);
-    int first = -1;
-#pragma unroll
-    for (int k = kChunk - 1; k >= 0; --k)
-        if (k < m && is_set_record(op[k]))
-            first = k;
-    if (first < 0) {
-        summ[t] = make_uint2(0u, 0u);
-        return;
-    }
-    uint32_t c = 0;
-#pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-        if (k >= first && k < m) {
-            uint32_t o;
-            c = sm_apply(c, op[k], &o);
-            trace[s0 + k] = make_uint2(c, o);
-        }
-    }
-    summ[t] = make_uint2(1u, c);
-    if (t == T - 1)
-        *final_count = c;
+    const int cnt = (n - base < kCtaOps) ? static_cast<int>(n - base) : kCtaOps;
+    for (int i = threadIdx.x; i < cnt; i += kSmThreads)
+        s_ops[sm_slot(i)] = ops[base + i];
+    for (int i = threadIdx.x; i < kCtaOps; i += kSmThreads)
+        s_tr[sm_slot(i)] = make_uint2(0u, kNoEntry);
+    __syncthreads();
+    return cnt;
 }
 
-__global__ void __launch_bounds__(256) sm_prefix_kernel(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace,
-                                                        const uint2 *summ, uint32_t *final_count)
+__device__ __forceinline__ void sm_flush(uint2 *trace, int64_t base, int cnt, const uint2 *s_tr)
 {
+    __syncthreads();
+    for (int i = threadIdx.x; i < cnt; i += kSmThreads) {
+        const uint2 v = s_tr[sm_slot(i)];
+        if (v.y != kNoEntry)
+            trace[base + i] = v;
+    }
+}
+
+__global__ void __launch_bounds__(kSmThreads) sm_suffix_kernel(const uint4 *ops, int64_t n, uint2 *trace,
+                                                               uint2 *summ, uint32_t *final_count)
+{
+    extern __shared__ uint4 sm_smem[];
+    uint4 *s_ops = sm_smem;
+    uint2 *s_tr = reinterpret_cast<uint2 *>(sm_smem + kSmThreads * kPad);
     const int64_t T = (n + kChunk - 1) / kChunk;
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (t >= T)
-        return;
-    uint32_t c;
-    if (t == 0) {
-        c = init;
-    } else {
-        const uint2 prev = summ[t - 1];
-        if (!prev.x)
-            return;   // an earlier chain runs through this chunk
-        c = prev.y;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
+    const int cnt = sm_stage(ops, n, base, s_ops, s_tr);
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kSmThreads + threadIdx.x;
+    if (t < T) {
+        const int off = threadIdx.x * kPad;
+        const int m = (n - t * kChunk < kChunk) ? static_cast<int>(n - t * kChunk) : kChunk;
+        int first = -1;
+        for (int k = 0; k < m; ++k)
+            if (is_set_record(s_ops[off + k])) {
+                first = k;
+                break;
+            }
+        if (first < 0) {
+            summ[t] = make_uint2(0u, 0u);
+        } else {
+            uint32_t c = 0;
+            for (int k = first; k < m; ++k) {
+                uint32_t o;
+                c = sm_apply(c, s_ops[off + k], &o);
+                s_tr[off + k] = make_uint2(c, o);
+            }
+            summ[t] = make_uint2(1u, c);
+            if (t == T - 1)
+                *final_count = c;
+        }
     }
-    for (int64_t i = t * kChunk; i < n; ++i) {
-        const uint4 op = ops[i];
-        if (is_set_record(op))
-            return;   // the suffix kernel traced from here on
-        uint32_t o;
-        c = sm_apply(c, op, &o);
-        trace[i] = make_uint2(c, o);
+    sm_flush(trace, base, cnt, s_tr);
+}
+
+__global__ void __launch_bounds__(kSmThreads) sm_prefix_kernel(const uint4 *ops, int64_t n, uint32_t init,
+                                                               uint2 *trace, const uint2 *summ,
+                                                               uint32_t *final_count)
+{
+    extern __shared__ uint4 sm_smem[];
+    uint4 *s_ops = sm_smem;
+    uint2 *s_tr = reinterpret_cast<uint2 *>(sm_smem + kSmThreads * kPad);
+    const int64_t T = (n + kChunk - 1) / kChunk;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
+    const int cnt = sm_stage(ops, n, base, s_ops, s_tr);
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kSmThreads + threadIdx.x;
+    bool head = false;
+    uint32_t c = init;
+    if (t < T) {
+        if (t == 0) {
+            head = true;
+        } else {
+            const uint2 prev = summ[t - 1];
+            head = prev.x != 0;   // otherwise an earlier chain runs through this chunk
+            c = prev.y;
+        }
     }
-    *final_count = c;   // no SET after the chain start: this chain ends the stream
+    if (head) {
+        // replay from the chunk start until the next SET (the suffix kernel
+        // traced from there on) or the end of the stream
+        int64_t i = t * kChunk;
+        bool ended = true;
+        for (; i < n; ++i) {
+            const bool local = i < base + cnt;
+            const uint4 op = local ? s_ops[sm_slot(static_cast<int>(i - base))] : ops[i];
+            if (is_set_record(op)) {
+                ended = false;
+                break;
+            }
+            uint32_t o;
+            c = sm_apply(c, op, &o);
+            if (local)
+                s_tr[sm_slot(static_cast<int>(i - base))] = make_uint2(c, o);
+            else
+                trace[i] = make_uint2(c, o);
+        }
+        if (ended)
+            *final_count = c;   // no SET after the chain start: this chain ends the stream
+    }
+    sm_flush(trace, base, cnt, s_tr);
+}
+
+// Shared-memory opt-in for both kernels, once per device.
+static int sm_prepare(int device)
+{
+    static std::mutex mu;
+    static bool done[64];
+    std::lock_guard<std::mutex> lk(mu);
+    if (device < 0 || device >= 64)
+        return CNS_ERR_CUDA;
+    if (!done[device]) {
+        CNS_CUDA(cudaFuncSetAttribute(sm_suffix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSmSmemBytes)));
+        CNS_CUDA(cudaFuncSetAttribute(sm_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSmSmemBytes)));
+        done[device] = true;
+    }
+    return CNS_SUCCESS;
+}
+
+// The two launches of one state-machine run (n > 0).
+static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, uint2 *summ, uint32_t *final_dev,
+                     int device, cudaStream_t s)
+{
+    if (int rc = sm_prepare(device))
+        return rc;
+    const int64_t blocks = (n + kCtaOps - 1) / kCtaOps;
+    if (blocks > 0x7fffffff)
+        return CNS_ERR_INVALID_VALUE;
+    sm_suffix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, trace, summ, final_dev);
+    CNS_CUDA(cudaGetLastError());
+    sm_prefix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, init, trace, summ,
+                                                                                    final_dev);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
 }
 
 __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
@@ -498,19 +588,8 @@ extern "C" int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t
         CNS_CUDA(cudaGetLastError());
         return CNS_SUCCESS;
     }
-    const int64_t T = (n + kChunk - 1) / kChunk;
-    const int threads = 256;
-    const int64_t blocks = (T + threads - 1) / threads;
-    if (blocks > 0x7fffffff)
-        return CNS_ERR_INVALID_VALUE;
-    const uint4 *ops = reinterpret_cast<const uint4 *>(ops_dev);
-    uint2 *trace = reinterpret_cast<uint2 *>(trace_dev);
-    uint2 *summ = static_cast<uint2 *>(scratch_dev);
-    sm_suffix_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(ops, n, trace, summ, final_dev);
-    CNS_CUDA(cudaGetLastError());
-    sm_prefix_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(ops, n, init, trace, summ, final_dev);
-    CNS_CUDA(cudaGetLastError());
-    return CNS_SUCCESS;
+    return sm_launch(reinterpret_cast<const uint4 *>(ops_dev), n, init, reinterpret_cast<uint2 *>(trace_dev),
+                     static_cast<uint2 *>(scratch_dev), final_dev, dev.device, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -568,16 +647,8 @@ extern "C" int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, 
     }
     // The suffix kernel writes every summary the prefix kernel reads, so
     // whatever an earlier call left in the array never matters.
-    const int64_t T = (n + kChunk - 1) / kChunk;
-    const int threads = 256;
-    const int64_t blocks = (T + threads - 1) / threads;
-    const uint4 *ops = reinterpret_cast<const uint4 *>(ops_dev);
-    uint2 *trace = reinterpret_cast<uint2 *>(trace_dev);
-    sm_suffix_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(ops, n, trace, summ, final_dev);
-    CNS_CUDA(cudaGetLastError());
-    sm_prefix_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(ops, n, init, trace, summ, final_dev);
-    CNS_CUDA(cudaGetLastError());
-    return CNS_SUCCESS;
+    return sm_launch(reinterpret_cast<const uint4 *>(ops_dev), n, init, reinterpret_cast<uint2 *>(trace_dev), summ,
+                     final_dev, dev.device, s);
 }
 
 // ---------------------------------------------------------------------------
