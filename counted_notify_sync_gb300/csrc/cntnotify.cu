@@ -300,19 +300,40 @@ __global__ void __launch_bounds__(kSmThreads) sm_prefix_kernel(const uint4 *ops,
         // traced from there on) or the end of the stream
         int64_t i = t * kChunk;
         bool ended = true;
-        for (; i < n; ++i) {
-            const bool local = i < base + cnt;
-            const uint4 op = local ? s_ops[sm_slot(static_cast<int>(i - base))] : ops[i];
+        const int64_t staged_end = base + cnt;
+        for (; i < staged_end; ++i) {
+            const uint4 op = s_ops[sm_slot(static_cast<int>(i - base))];
             if (is_set_record(op)) {
                 ended = false;
                 break;
             }
             uint32_t o;
             c = sm_apply(c, op, &o);
-            if (local)
-                s_tr[sm_slot(static_cast<int>(i - base))] = make_uint2(c, o);
-            else
-                trace[i] = make_uint2(c, o);
+            s_tr[sm_slot(static_cast<int>(i - base))] = make_uint2(c, o);
+        }
+        // a chain that runs past this CTA's ops reads the rest from global
+        // memory, eight independent loads at a time
+        constexpr int kBatch = 8;
+        while (ended && i < n) {
+            uint4 op[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k)
+                op[k] = (i + k < n) ? ops[i + k] : make_uint4(0u, CNS_REC_SET, 0u, 0u);
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (!ended)
+                    break;
+                if (i + k >= n)
+                    break;
+                if (is_set_record(op[k])) {
+                    ended = false;
+                    break;
+                }
+                uint32_t o;
+                c = sm_apply(c, op[k], &o);
+                trace[i + k] = make_uint2(c, o);
+            }
+            i += kBatch;
         }
         if (ended)
             *final_count = c;   // no SET after the chain start: this chain ends the stream
@@ -678,7 +699,10 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     if (dev.device != done->device)
         return CNS_ERR_INVALID_VALUE;
     cudaStream_t sp = to_stream(cfg->producer_stream), sc = to_stream(cfg->consumer_stream);
-    const int pgrid = cfg->producer_ctas ? cfg->producer_ctas : 4 * dev.sm_count;
+    // default: one tile per CTA (up to 65535 CTAs), so the release fence in
+    // front of each tile's count overlaps with the other tiles' work
+    const int pgrid = cfg->producer_ctas ? cfg->producer_ctas : static_cast<int>(std::min<int64_t>(cfg->tiles, 65535));
+    const int pthreads = std::min(256, std::max(32, ((cfg->tile_words / 4 + 31) / 32) * 32));
     const int64_t n_words = cfg->tiles * cfg->tile_words;
     const int cgrid = static_cast<int>(std::min<int64_t>(2 * dev.sm_count, (n_words / 4 + 255) / 256));
 
@@ -726,7 +750,7 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     for (int64_t r = 0; r < cfg->rounds && rc == CNS_SUCCESS; ++r) {
         if (timed)
             check(cudaEventRecord(T(2 * r), sp), "event");
-        pipeline_producer_kernel<<<pgrid, 256, 0, sp>>>(cfg->tiles_dev, cfg->tiles, cfg->tile_words,
+        pipeline_producer_kernel<<<pgrid, pthreads, 0, sp>>>(cfg->tiles_dev, cfg->tiles, cfg->tile_words,
                                                         static_cast<uint32_t>(r), done->line);
         check(cudaGetLastError(), "producer launch");
         if (timed)

@@ -427,7 +427,7 @@ typedef struct {
     uint32_t *released_dev;  /* (in/out, optional) uint32[rounds]: count seen at release */
     int64_t tiles;           /* (in) K tiles per round, >= 1 */
     int32_t tile_words;      /* (in) words per tile, multiple of 4, 4..8192 */
-    int32_t producer_ctas;   /* (in) producer grid; 0 = 4 per SM */
+    int32_t producer_ctas;   /* (in) producer grid; 0 = one CTA per tile (at most 65535) */
     int64_t rounds;          /* (in) rounds */
     cns_stream_t producer_stream; /* (in) the recording stream */
     cns_stream_t consumer_stream; /* (in) the waiting stream */
