@@ -143,10 +143,11 @@ __global__ void cnt_wait_kernel(uint32_t *line, uint32_t mode, uint32_t v, uint3
     }
 }
 
-// Zero the count, the sticky status and the abort word of a notify line.
+// Zero the count, the sticky status, the abort word and the pipeline's
+// finish counter of a notify line.
 __global__ void cnt_clear_line_kernel(uint32_t *line)
 {
-    if (threadIdx.x < 3)
+    if (threadIdx.x < 4)
         line[threadIdx.x] = 0u;
 }
 
@@ -382,9 +383,42 @@ __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
 // Two-stream pipeline kernels
 // ---------------------------------------------------------------------------
 
+// Producer of one round.  Before touching the tiles every CTA waits, on the
+// device, until the consumer has released the previous round (ack >= round);
+// then it stores its tile and adds 1 to `done` (a release record).
 __global__ void __launch_bounds__(256) pipeline_producer_kernel(uint32_t *tiles, int64_t n_tiles, int tile_words,
-                                                                uint32_t round, uint32_t *done)
+                                                                uint32_t round, uint32_t *done, uint32_t *ack,
+                                                                uint64_t timeout_ns, uint32_t *abort)
 {
+    __shared__ int s_skip;
+    if (threadIdx.x == 0) {
+        int skip = 0;
+        if (round != 0) {
+            uint32_t spins = 0;
+            uint64_t deadline = 0;
+            while (ld_acquire_gpu(ack) < round) {
+                if ((++spins & 63u) == 0u) {
+                    if (ld_relaxed_gpu(abort) != 0u) {
+                        skip = 1;
+                        break;
+                    }
+                    const uint64_t now = globaltimer_ns();
+                    if (deadline == 0) {
+                        deadline = now + timeout_ns;
+                    } else if (now > deadline) {
+                        atom_exch_relaxed_gpu(ack + 1, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
+                        atom_exch_relaxed_gpu(abort, 1u);
+                        skip = 1;
+                        break;
+                    }
+                }
+            }
+        }
+        s_skip = skip;
+    }
+    __syncthreads();
+    if (s_skip)
+        return;
     const int q = tile_words >> 2;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
         uint4 *d = reinterpret_cast<uint4 *>(tiles + t * tile_words);
@@ -400,8 +434,12 @@ __global__ void __launch_bounds__(256) pipeline_producer_kernel(uint32_t *tiles,
     }
 }
 
+// Consumer of one round: sums the tile area mod 2^32 into *checksum; the last
+// CTA to finish (counted on `finish`) records ack = ack_value, which lets the
+// next round's producer overwrite the tiles.
 __global__ void __launch_bounds__(256) pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words,
-                                                                uint32_t *checksum)
+                                                                uint32_t *checksum, uint32_t *ack,
+                                                                uint32_t ack_value, uint32_t *finish)
 {
     const uint4 *t4 = reinterpret_cast<const uint4 *>(tiles);
     uint32_t s = 0;
@@ -416,6 +454,15 @@ __global__ void __launch_bounds__(256) pipeline_consumer_kernel(const uint32_t *
         s += __shfl_xor_sync(0xffffffffu, s, o);
     if ((threadIdx.x & 31u) == 0u)
         atomicAdd(checksum, s);
+    __syncthreads();   // every read of this CTA is done ...
+    if (threadIdx.x == 0) {
+        // ... before it counts itself finished (release); the last CTA has
+        // acquired every other CTA's count when it releases the producer
+        if (atom_add_acq_rel_gpu(finish, 1u) == gridDim.x - 1u) {
+            atom_exch_relaxed_gpu(finish, 0u);
+            cnt_record_device(ack, CNS_REC_SET, ack_value);
+        }
+    }
 }
 
 }  // namespace cns
@@ -699,10 +746,15 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     if (dev.device != done->device)
         return CNS_ERR_INVALID_VALUE;
     cudaStream_t sp = to_stream(cfg->producer_stream), sc = to_stream(cfg->consumer_stream);
-    // default: one tile per CTA (up to 65535 CTAs), so the release fence in
-    // front of each tile's count overlaps with the other tiles' work
-    const int pgrid = cfg->producer_ctas ? cfg->producer_ctas : static_cast<int>(std::min<int64_t>(cfg->tiles, 65535));
+    // Producer CTAs wait on the device for the consumer's release before they
+    // start, so together they may hold at most half of each SM's thread slots:
+    // the consumer kernel and the wait kernel always find room to run.  Within
+    // that cap, one tile per CTA, so the release fence in front of each tile's
+    // count overlaps with the other tiles' work.
     const int pthreads = std::min(256, std::max(32, ((cfg->tile_words / 4 + 31) / 32) * 32));
+    const int64_t pcap = static_cast<int64_t>(dev.sm_count) * (1024 / pthreads);
+    const int64_t pwant = cfg->producer_ctas ? cfg->producer_ctas : cfg->tiles;
+    const int pgrid = static_cast<int>(std::max<int64_t>(1, std::min(pwant, pcap)));
     const int64_t n_words = cfg->tiles * cfg->tile_words;
     const int cgrid = static_cast<int>(std::min<int64_t>(2 * dev.sm_count, (n_words / 4 + 255) / 256));
 
@@ -746,28 +798,27 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
         check(cudaEventRecord(T(2 * cfg->rounds), sp), "event");
 
     cns_wait_info_t w_done = {CNS_WAIT_BIGGER_OR_EQUAL, static_cast<uint32_t>(cfg->tiles), cfg->timeout_s, 1, {0, 0, 0}};
-    cns_wait_info_t w_ack = {CNS_WAIT_EQUAL, 1u, cfg->timeout_s, 1, {0, 0, 0}};
+    const uint64_t ack_timeout = wait_timeout_ns(cfg->timeout_s);
+    uint32_t *finish = ack->line + 3;
     for (int64_t r = 0; r < cfg->rounds && rc == CNS_SUCCESS; ++r) {
+        // Submission order is a valid serial schedule: every wait (the
+        // producer's device-side wait on ack, the stream wait on done) comes
+        // after the work that releases it.  CUDA may feed both streams through
+        // one hardware queue in submission order, and a wait ahead of its
+        // record would then hold that record back until it timed out.
         if (timed)
             check(cudaEventRecord(T(2 * r), sp), "event");
         pipeline_producer_kernel<<<pgrid, pthreads, 0, sp>>>(cfg->tiles_dev, cfg->tiles, cfg->tile_words,
-                                                        static_cast<uint32_t>(r), done->line);
+                                                             static_cast<uint32_t>(r), done->line, ack->line,
+                                                             ack_timeout, abort);
         check(cudaGetLastError(), "producer launch");
         if (timed)
             check(cudaEventRecord(T(2 * r + 1), sp), "event");
-        // Submission order = a valid serial schedule: every wait is submitted
-        // after the records that release it.  CUDA may feed both streams
-        // through one hardware queue in submission order; a wait submitted
-        // ahead of its record would then hold the record back until it timed
-        // out.
         if (int e = enqueue_wait(done, sc, &w_done, cfg->released_dev ? cfg->released_dev + r : nullptr, abort))
             rc = e;
-        pipeline_consumer_kernel<<<cgrid, 256, 0, sc>>>(cfg->tiles_dev, n_words, cfg->checksums_dev + r);
+        pipeline_consumer_kernel<<<cgrid, 256, 0, sc>>>(cfg->tiles_dev, n_words, cfg->checksums_dev + r, ack->line,
+                                                        static_cast<uint32_t>(r + 1), finish);
         check(cudaGetLastError(), "consumer launch");
-        cnt_record_kernel<<<1, 32, 0, sc>>>(ack->line, CNS_REC_SET, 1u);
-        check(cudaGetLastError(), "ack record");
-        if (int e = enqueue_wait(ack, sp, &w_ack, nullptr, abort))
-            rc = e;
     }
     check(cudaEventRecord(join, sc), "event");
     check(cudaStreamWaitEvent(sp, join, 0), "stream wait");

@@ -421,34 +421,39 @@ int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, uint32_t in
  * waits BIGGER_OR_EQUAL N with isClear = 1 and then continues). */
 typedef struct {
     cns_cnt_notify_t done;   /* (in) producer -> consumer: ADD 1 per tile */
-    cns_cnt_notify_t ack;    /* (in) consumer -> producer: SET 1 once a round is consumed */
+    cns_cnt_notify_t ack;    /* (in) consumer -> producer: SET round+1 once a round is consumed */
     uint32_t *tiles_dev;     /* (in) tiles * tile_words uint32 */
     uint32_t *checksums_dev; /* (in/out) uint32[rounds], zeroed by the call */
     uint32_t *released_dev;  /* (in/out, optional) uint32[rounds]: count seen at release */
     int64_t tiles;           /* (in) K tiles per round, >= 1 */
     int32_t tile_words;      /* (in) words per tile, multiple of 4, 4..8192 */
-    int32_t producer_ctas;   /* (in) producer grid; 0 = one CTA per tile (at most 65535) */
+    int32_t producer_ctas;   /* (in) producer grid; 0 = one CTA per tile.  Capped so that the
+                                producer CTAs hold at most half of each SM's thread slots */
     int64_t rounds;          /* (in) rounds */
     cns_stream_t producer_stream; /* (in) the recording stream */
     cns_stream_t consumer_stream; /* (in) the waiting stream */
     uint32_t timeout_s;      /* (in) per-wait timeout in seconds; 0 = library cap */
     int32_t sync;            /* (in) 1: wait, time, check the notifies' status */
     float elapsed_ms;        /* (out, sync=1) first producer launch to last record */
-    float producer_ms;       /* (out, sync=1) summed producer-kernel time */
+    float producer_ms;       /* (out, sync=1) summed producer-kernel time, including each
+                                producer's wait for the previous round's release */
     int32_t device_status;   /* (out, sync=1) 0 or CNS_ERR_TIMEOUT */
     int32_t reserved[3];
 } cns_pipeline_t;
 
 /*
- * cns_pipeline_run -- `rounds` rounds of: on the producer stream, a producer
- * kernel writes word w of the tile area as w * 2654435761 + round and, after
- * each tile is stored, adds 1 to `done` from the device; then it waits for
- * `ack` EQUAL 1 (clear).  On the consumer stream: wait `done`
- * BIGGER_OR_EQUAL tiles (clear), a consumer kernel sums the tile area mod 2^32
- * into checksums[round], then record `ack` SET 1.  The streams meet only
- * through the two counts.  The call first clears both notifies (count and
- * status); once one of its waits times out, the pipeline's remaining waits
- * return at once, so a lost signal costs one timeout, not one per round.
+ * cns_pipeline_run -- `rounds` rounds of a producer and a consumer on two
+ * streams that meet only through two counted notifies.
+ *   producer stream: a producer kernel whose CTAs first wait on the device
+ *     until ack >= round (the consumer has finished reading the previous
+ *     round), then write word w of the tile area as w * 2654435761 + round,
+ *     and after each tile is stored add 1 to `done` from the device;
+ *   consumer stream: cntnotify wait on `done` BIGGER_OR_EQUAL tiles with
+ *     isClear = 1, then a consumer kernel that sums the tile area mod 2^32
+ *     into checksums[round]; its last CTA to finish records ack = round + 1.
+ * The call first clears both notifies (count and status); `done` ends at 0
+ * and `ack` at `rounds`.  Once a wait times out the pipeline's remaining
+ * waits return at once, so a lost signal costs one timeout, not one per round.
  * Errors: INVALID_HANDLE, NULL_PTR, INVALID_VALUE, CUDA; with sync=1 also
  * TIMEOUT.
  */

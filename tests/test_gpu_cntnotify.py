@@ -238,7 +238,7 @@ def test_pipeline_4096_tiles_1000_rounds(cns):
         want_cs, want_rel = oracle.pipeline(4096, 256, 1000)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
         np.testing.assert_array_equal(from_dev_u32(released), want_rel)
-        assert count_of(cns, done) == (0, 0) and count_of(cns, ack) == (0, 0)
+        assert count_of(cns, done) == (0, 0) and count_of(cns, ack) == (0, 1000)
         assert cfg.elapsed_ms > 0 and 0 < cfg.producer_ms <= cfg.elapsed_ms
     finally:
         cns.cntnotify_destroy(done)
