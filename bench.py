@@ -446,8 +446,8 @@ def run_native(args):
         torch.distributed.destroy_process_group()
 
 
-def case_soft148_small():
-    """Three launches of the headline kernel with 2000 rounds each (profiling)."""
+def case_soft148_small(args):
+    """Three launches of the headline kernel (bench's --variant) with 2000 rounds each (profiling)."""
     import torch
     import counted_notify_sync_gb300 as cns
     cns.build()
@@ -457,11 +457,11 @@ def case_soft148_small():
     ws = cns.new_workspace()
     for _ in range(3):
         cns.run_syncall(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1, 2000,
-                        elems=SLOTS_HEAD, workspace=ws)
+                        elems=SLOTS_HEAD, workspace=ws, variant=args.variant)
     print("case soft148-small: ok")
 
 
-def case_hard148_small():
+def case_hard148_small(args):
     """Three launches of the hard-path kernel with 2000 rounds each (profiling)."""
     import torch
     import counted_notify_sync_gb300 as cns
@@ -476,7 +476,7 @@ def case_hard148_small():
     print("case hard148-small: ok")
 
 
-def case_jacobi_small():
+def case_jacobi_small(args):
     """Three Jacobi launches, N = 2^25 fp32 (2 x 128 MiB, above L2), 592 CTAs, 4 sweeps (profiling)."""
     import torch
     import counted_notify_sync_gb300 as cns
@@ -491,7 +491,7 @@ def case_jacobi_small():
     print("case jacobi-small: ok")
 
 
-def case_statemachine():
+def case_statemachine(args):
     """Three runs of the op-stream state machine on 1e6 ops (profiling)."""
     import torch
     import counted_notify_sync_gb300 as cns
@@ -503,14 +503,29 @@ def case_statemachine():
     print("case statemachine: ok")
 
 
+def case_pipeline(args):
+    """The two-stream pipeline, 4096 tiles x 256 words, 20 rounds (profiling)."""
+    import torch
+    import counted_notify_sync_gb300 as cns
+    cns.build()
+    rc1, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    cfg, rc, cs, rel = cns.run_pipeline(done, ack, 4096, 256, 20, s1, s2, timeout_s=10)
+    cns.cntnotify_destroy(done)
+    cns.cntnotify_destroy(ack)
+    assert rc == 0, rc
+    print("case pipeline: ok")
+
+
 CASES = {"soft148-small": case_soft148_small, "hard148-small": case_hard148_small,
-         "jacobi-small": case_jacobi_small, "statemachine": case_statemachine}
+         "jacobi-small": case_jacobi_small, "statemachine": case_statemachine, "pipeline": case_pipeline}
 
 
 def main():
     args = parse()
     if args.case:
-        CASES[args.case]()
+        CASES[args.case](args)
         return
     if args.impl == "reference":
         run_reference(args)
