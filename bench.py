@@ -60,6 +60,17 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """The largest `value` over all ranks (the slowest replica's step time); `value` itself when alone."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --- CPU oracle timing ------------------------------------------------------------------
 
 def time_oracle(budget_s: float):
@@ -396,12 +407,7 @@ def run_native(args):
 
     stream = torch.cuda.Stream()
     times, wall, status, correct, clocks = headline(cns, torch, args, stream)
-    ms_step = statistics.mean(times)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(statistics.mean(times), world, device="cuda")
     ns_round = ms_step * 1e6 / ROUNDS_HEAD
     e2e = e2e_headline(cns, torch, args)
     sec = {} if args.no_secondary else secondary(cns, torch, peaks)
