@@ -80,55 +80,99 @@ __device__ __forceinline__ void ring_phase(const uint32_t *src, uint32_t *dst, u
 
 // One Jacobi sweep over participant p's chunk of the field:
 // u'[i] = (u[i-1] + u[i+1]) * 0.5f for interior points, ends copied.
-// The field is cut into N/4 float4 columns shared out as evenly as possible;
-// neighbouring float4s inside a warp trade their edge values by shuffle, and
-// the two values beyond a warp's span come from global memory.  The scalar
-// tail (N mod 4 points) belongs to the last participant.
-__device__ __forceinline__ void jacobi_phase(const float *src, float *dst, int64_t N, uint32_t p, uint32_t P)
+// The field is cut into N/4 float4 columns shared out as evenly as possible.
+// The chunk is streamed through shared memory in tiles of kJacTile float4:
+// thread 0 arms an mbarrier and starts one bulk copy (TMA engine) of the
+// tile plus one float4 of halo on each side; every thread then waits for it,
+// computes its outputs from shared memory and stores them with plain float4
+// stores.  One tile in flight per CTA and four CTAs per SM measured fastest
+// on GB300 (deeper pipelines and register-only streaming were slower).  The
+// scalar tail (N mod 4 points) belongs to the last participant.
+constexpr int kJacTile = 1024;
+constexpr uint32_t kJacSmemBytes = (kJacTile + 2) * 16;
+
+struct JacState {
+    float4 *stage;     // kJacTile + 2 float4 of shared memory
+    uint64_t *bar;     // its mbarrier
+    uint32_t parity;   // phase to wait for next
+    int *flag;         // shared: a wait in this sweep gave up
+};
+
+// Returns after the sweep; a bulk copy that never completes within the
+// barrier timeout is recorded as CNS_ERR_TIMEOUT (the round's barrier then
+// stops every participant).
+__device__ __forceinline__ void jacobi_phase(const float *src, float *dst, int64_t N, uint32_t p, uint32_t P,
+                                             JacState &js, uint32_t *status_line, uint64_t timeout_ns,
+                                             uint32_t round)
 {
     const int64_t N4 = N >> 2;
     const int64_t base = N4 / P, rem = N4 % P;
     const int64_t j0 = static_cast<int64_t>(p) * base + (p < rem ? p : rem);
     const int64_t j1 = j0 + base + (p < rem ? 1 : 0);
+    const int64_t nT = (j1 - j0 + kJacTile - 1) / kJacTile;
     const float4 *s4 = reinterpret_cast<const float4 *>(src);
     float4 *d4 = reinterpret_cast<float4 *>(dst);
-    const uint32_t lane = threadIdx.x & 31u;
-    const int64_t stride = blockDim.x;
-    constexpr int U = 4;
-    for (int64_t it = j0; it < j1; it += U * stride) {   // uniform trip count across the CTA
-        float4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t j = it + u * stride + threadIdx.x;
-            v[u] = (j < j1) ? s4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t k = 0; k < nT; ++k) {
+        const int64_t o0 = j0 + k * kJacTile;
+        const int64_t o1 = (o0 + kJacTile < j1) ? o0 + kJacTile : j1;
+        if (threadIdx.x == 0) {
+            // the stage was read by everyone (barrier below / previous round)
+            // and src was written by generic stores: order both before the copy
+            if (k == 0)
+                fence_proxy_async_global();
+            fence_proxy_async_shared();
+            const int64_t lo = (o0 - 1 < 0) ? 0 : o0 - 1;
+            const int64_t hi = (o1 + 1 > N4) ? N4 : o1 + 1;
+            const uint32_t bytes = static_cast<uint32_t>((hi - lo) * 16);
+            mbar_arrive_expect_tx(js.bar, bytes);
+            bulk_copy_g2s(js.stage + (lo - (o0 - 1)), s4 + lo, bytes, js.bar);
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t j = it + u * stride + threadIdx.x;
-            float lw = __shfl_up_sync(0xffffffffu, v[u].w, 1);
-            float rx = __shfl_down_sync(0xffffffffu, v[u].x, 1);
-            if (j < j1) {
-                if (lane == 0)
-                    lw = (j > 0) ? src[4 * j - 1] : 0.f;
-                if (lane == 31 || j + 1 >= j1)
-                    rx = (4 * j + 4 < N) ? src[4 * j + 4] : 0.f;
-                float4 o;
-                o.x = (j == 0) ? v[u].x : (lw + v[u].y) * 0.5f;
-                o.y = (v[u].x + v[u].z) * 0.5f;
-                o.z = (v[u].y + v[u].w) * 0.5f;
-                o.w = (4 * j + 3 == N - 1) ? v[u].w : (v[u].z + rx) * 0.5f;
-                d4[j] = o;
+        // bounded wait for the tile: every thread observes the completion
+        uint32_t spins = 0;
+        uint64_t deadline = 0;
+        bool ok = true;
+        while (!mbar_try_wait(js.bar, js.parity)) {
+            if ((++spins & 63u) == 0u) {
+                const uint64_t now = globaltimer_ns();
+                if (deadline == 0) {
+                    deadline = now + timeout_ns;
+                } else if (now > deadline) {
+                    ok = false;
+                    break;
+                }
             }
+        }
+        if (!ok)
+            *js.flag = 1;
+        js.parity ^= 1u;
+        const float4 *t = js.stage;
+        for (int64_t j = o0 + threadIdx.x; j < o1 && ok; j += blockDim.x) {
+            const int i = static_cast<int>(j - o0) + 1;
+            const float4 v = t[i];
+            const float lw = (j > 0) ? t[i - 1].w : 0.f;
+            const float rx = (j + 1 < N4) ? t[i + 1].x : ((4 * j + 4 < N) ? src[4 * j + 4] : 0.f);
+            float4 o;
+            o.x = (j == 0) ? v.x : (lw + v.y) * 0.5f;
+            o.y = (v.x + v.z) * 0.5f;
+            o.z = (v.y + v.w) * 0.5f;
+            o.w = (4 * j + 3 == N - 1) ? v.w : (v.z + rx) * 0.5f;
+            d4[j] = o;
+        }
+        __syncthreads();   // everyone is done with the stage (and sees the flag)
+        if (*js.flag) {
+            if (threadIdx.x == 0)
+                raise_timeout(status_line, round, blockIdx.x);
+            return;
         }
     }
     if (p == P - 1) {
-        for (int64_t i = 4 * N4 + threadIdx.x; i < N; i += stride)
+        for (int64_t i = 4 * N4 + threadIdx.x; i < N; i += blockDim.x)
             dst[i] = (i == 0 || i == N - 1) ? src[i] : (src[i - 1] + src[i + 1]) * 0.5f;
     }
 }
 
 template <int WL>
-__device__ __forceinline__ void data_phase(const SyncallParams &p, int64_t r, uint32_t part)
+__device__ __forceinline__ void data_phase(const SyncallParams &p, int64_t r, uint32_t part, JacState &js)
 {
     if (WL == CNS_WL_EMPTY)
         return;
@@ -136,7 +180,8 @@ __device__ __forceinline__ void data_phase(const SyncallParams &p, int64_t r, ui
     void *src = odd ? p.buf1 : p.buf0;
     void *dst = odd ? p.buf0 : p.buf1;
     if (WL == CNS_WL_JACOBI)
-        jacobi_phase(static_cast<const float *>(src), static_cast<float *>(dst), p.elems, part, p.P);
+        jacobi_phase(static_cast<const float *>(src), static_cast<float *>(dst), p.elems, part, p.P, js,
+                     p.bar.status_line, p.bar.timeout_ns, static_cast<uint32_t>(r));
     else
         ring_phase<WL>(static_cast<const uint32_t *>(src), static_cast<uint32_t *>(dst), part, p.P, p.elems,
                        static_cast<uint32_t>(r));
@@ -157,6 +202,9 @@ template <int MODE, int WL>
 __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
 {
     __shared__ int s_flag;
+    __shared__ __align__(8) uint64_t s_jac_bar;
+    __shared__ int s_jac_flag;
+    extern __shared__ float4 s_jac_stage[];   // JACOBI only: kJacSmemBytes
     const uint32_t b = blockIdx.x;
     const uint32_t role = cta_role(p, b);
     if (MODE == CNS_SYNCALL_SOFT && b >= p.P) {
@@ -165,8 +213,15 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
             p.cta_status[b] = static_cast<int32_t>(CNS_CTA_IDLE | (role << 8));
         return;
     }
-    if (threadIdx.x == 0)
+    JacState js{s_jac_stage, &s_jac_bar, 0u, &s_jac_flag};
+    if (threadIdx.x == 0) {
         s_flag = 0;
+        if (WL == CNS_WL_JACOBI) {
+            s_jac_flag = 0;
+            mbar_init(&s_jac_bar, 1);
+            mbar_init_fence();
+        }
+    }
     if (MODE == CNS_SYNCALL_HARD) {
         __syncwarp();
         cluster_sync_all();   // every CTA's flag is initialised before anyone may write it
@@ -181,7 +236,7 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         choose_near_copy(bar);
     bool stop = false;
     for (int64_t r = 0; r < p.rounds; ++r) {
-        data_phase<WL>(p, r, b);
+        data_phase<WL>(p, r, b, js);
         stop = (MODE == CNS_SYNCALL_SOFT) ? soft_barrier(bar, static_cast<uint32_t>(r), &s_flag)
                                           : hard_barrier(bar, static_cast<uint32_t>(r), &s_flag);
         if (stop)
@@ -234,17 +289,18 @@ static KernelFn pick_kernel(int mode, int wl)
 }
 
 // Can `grid` CTAs (in clusters of C when C > 0) be resident at once?
-static int fits(KernelFn k, int grid, int threads, int C, cudaStream_t s, const DeviceInfo &dev, bool *ok)
+static int fits(KernelFn k, int grid, int threads, int C, size_t smem, cudaStream_t s, const DeviceInfo &dev, bool *ok)
 {
     if (C <= 0) {
         int per_sm = 0;
-        CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void *>(k), threads, 0));
+        CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void *>(k), threads, smem));
         *ok = static_cast<int64_t>(per_sm) * dev.sm_count >= grid;
         return CNS_SUCCESS;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -383,12 +439,13 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return rc;
     cudaStream_t s = to_stream(d->stream);
     KernelFn k = pick_kernel(mode, d->workload);
+    const size_t smem = d->workload == CNS_WL_JACOBI ? kJacSmemBytes : 0;
     bool ok = false;
     if (mode == CNS_SYNCALL_HARD && C == 0) {
         for (int c : {4, 2, 1}) {
             if (grid % c != 0)
                 continue;
-            if (int rc = fits(k, grid, threads, c, s, dev, &ok))
+            if (int rc = fits(k, grid, threads, c, smem, s, dev, &ok))
                 return rc;
             if (ok) {
                 C = c;
@@ -398,7 +455,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         if (!ok)
             return CNS_ERR_NOT_RESIDENT;
     } else {
-        if (int rc = fits(k, grid, threads, mode == CNS_SYNCALL_HARD ? C : 0, s, dev, &ok))
+        if (int rc = fits(k, grid, threads, mode == CNS_SYNCALL_HARD ? C : 0, smem, s, dev, &ok))
             return rc;
         if (!ok)
             return CNS_ERR_NOT_RESIDENT;
@@ -447,7 +504,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attrs[2];
     int na = 0;
