@@ -452,9 +452,19 @@ __global__ void __launch_bounds__(256) pipeline_consumer_kernel(const uint32_t *
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         s += __shfl_xor_sync(0xffffffffu, s, o);
+    // one add per CTA, not per warp: same-address atomics serialise in L2
+    __shared__ uint32_t warp_sum[32];
     if ((threadIdx.x & 31u) == 0u)
-        atomicAdd(checksum, s);
+        warp_sum[threadIdx.x >> 5] = s;
     __syncthreads();   // every read of this CTA is done ...
+    if (threadIdx.x < 32) {
+        uint32_t w = (threadIdx.x < (blockDim.x >> 5)) ? warp_sum[threadIdx.x] : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (threadIdx.x == 0)
+            atomicAdd(checksum, w);
+    }
     if (threadIdx.x == 0) {
         // ... before it counts itself finished (release); the last CTA has
         // acquired every other CTA's count when it releases the producer
