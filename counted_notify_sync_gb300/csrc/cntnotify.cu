@@ -238,62 +238,16 @@ __device__ __forceinline__ void sm_flush(uint2 *trace, int64_t base, int cnt, co
     }
 }
 
-// Replay a chain from op `i` with count `c` until the next SET record (the
-// chunk kernel traced from there on) or the end of the stream.  Ops inside
-// [base, base + cnt) come from the staged copy and are traced into the staged
-// trace; beyond it they are read from global memory eight at a time and
-// traced directly.  The chain that runs off the end writes the final count.
-__device__ __forceinline__ void sm_replay(const uint4 *ops, int64_t n, int64_t i, uint32_t c, uint2 *trace,
-                                          uint32_t *final_count, int64_t base, int cnt, const uint4 *s_ops,
-                                          uint2 *s_tr)
-{
-    const int64_t staged_end = base + cnt;
-    for (; i < staged_end && i >= base; ++i) {
-        const uint4 op = s_ops[sm_slot(static_cast<int>(i - base))];
-        if (is_set_record(op))
-            return;
-        uint32_t o;
-        c = sm_apply(c, op, &o);
-        s_tr[sm_slot(static_cast<int>(i - base))] = make_uint2(c, o);
-    }
-    constexpr int kBatch = 8;
-    while (i < n) {
-        uint4 op[kBatch];
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k)
-            op[k] = (i + k < n) ? ops[i + k] : make_uint4(0u, CNS_REC_SET, 0u, 0u);
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-            if (i + k >= n)
-                break;
-            if (is_set_record(op[k]))
-                return;
-            uint32_t o;
-            c = sm_apply(c, op[k], &o);
-            trace[i + k] = make_uint2(c, o);
-        }
-        i += kBatch;
-    }
-    *final_count = c;
-}
-
-// Kernel 1: per chunk, the trace from its first SET on (its count is known
-// there) and the chunk summary; then, inside the CTA, every chunk whose
-// predecessor ends in a known count replays its own prefix (and on, past
-// SET-free chunks).  Chains that start at the CTA's first chunk are left to
-// kernel 2: their starting count comes from another CTA.
 __global__ void __launch_bounds__(kSmThreads) sm_suffix_kernel(const uint4 *ops, int64_t n, uint2 *trace,
                                                                uint2 *summ, uint32_t *final_count)
 {
     extern __shared__ uint4 sm_smem[];
     uint4 *s_ops = sm_smem;
     uint2 *s_tr = reinterpret_cast<uint2 *>(sm_smem + kSmThreads * kPad);
-    __shared__ uint2 s_summ[kSmThreads];
     const int64_t T = (n + kChunk - 1) / kChunk;
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
     const int cnt = sm_stage(ops, n, base, s_ops, s_tr);
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kSmThreads + threadIdx.x;
-    uint2 sm = make_uint2(0u, 0u);
     if (t < T) {
         const int off = threadIdx.x * kPad;
         const int m = (n - t * kChunk < kChunk) ? static_cast<int>(n - t * kChunk) : kChunk;
@@ -303,44 +257,89 @@ __global__ void __launch_bounds__(kSmThreads) sm_suffix_kernel(const uint4 *ops,
                 first = k;
                 break;
             }
-        if (first >= 0) {
+        if (first < 0) {
+            summ[t] = make_uint2(0u, 0u);
+        } else {
             uint32_t c = 0;
             for (int k = first; k < m; ++k) {
                 uint32_t o;
                 c = sm_apply(c, s_ops[off + k], &o);
                 s_tr[off + k] = make_uint2(c, o);
             }
-            sm = make_uint2(1u, c);
+            summ[t] = make_uint2(1u, c);
             if (t == T - 1)
                 *final_count = c;
         }
-        summ[t] = sm;
     }
-    s_summ[threadIdx.x] = sm;
-    __syncthreads();
-    if (t < T && threadIdx.x > 0 && s_summ[threadIdx.x - 1].x)
-        sm_replay(ops, n, t * kChunk, s_summ[threadIdx.x - 1].y, trace, final_count, base, cnt, s_ops, s_tr);
     sm_flush(trace, base, cnt, s_tr);
 }
 
-// Kernel 2: the chains that start at the first chunk of each CTA's range,
-// one thread per range: from the initial count (range 0) or from the count
-// the previous range's last chunk ends in, if it has a SET.
-__global__ void __launch_bounds__(256) sm_prefix_kernel(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace,
-                                                        const uint2 *summ, uint32_t *final_count)
+__global__ void __launch_bounds__(kSmThreads) sm_prefix_kernel(const uint4 *ops, int64_t n, uint32_t init,
+                                                               uint2 *trace, const uint2 *summ,
+                                                               uint32_t *final_count)
 {
-    const int64_t ranges = (n + kCtaOps - 1) / kCtaOps;
-    const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (b >= ranges)
-        return;
+    extern __shared__ uint4 sm_smem[];
+    uint4 *s_ops = sm_smem;
+    uint2 *s_tr = reinterpret_cast<uint2 *>(sm_smem + kSmThreads * kPad);
+    const int64_t T = (n + kChunk - 1) / kChunk;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
+    const int cnt = sm_stage(ops, n, base, s_ops, s_tr);
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kSmThreads + threadIdx.x;
+    bool head = false;
     uint32_t c = init;
-    if (b > 0) {
-        const uint2 prev = summ[b * kSmThreads - 1];
-        if (!prev.x)
-            return;   // an earlier chain runs through this range's first chunk
-        c = prev.y;
+    if (t < T) {
+        if (t == 0) {
+            head = true;
+        } else {
+            const uint2 prev = summ[t - 1];
+            head = prev.x != 0;   // otherwise an earlier chain runs through this chunk
+            c = prev.y;
+        }
     }
-    sm_replay(ops, n, b * kCtaOps, c, trace, final_count, 0, 0, nullptr, nullptr);
+    if (head) {
+        // replay from the chunk start until the next SET (the suffix kernel
+        // traced from there on) or the end of the stream
+        int64_t i = t * kChunk;
+        bool ended = true;
+        const int64_t staged_end = base + cnt;
+        for (; i < staged_end; ++i) {
+            const uint4 op = s_ops[sm_slot(static_cast<int>(i - base))];
+            if (is_set_record(op)) {
+                ended = false;
+                break;
+            }
+            uint32_t o;
+            c = sm_apply(c, op, &o);
+            s_tr[sm_slot(static_cast<int>(i - base))] = make_uint2(c, o);
+        }
+        // a chain that runs past this CTA's ops reads the rest from global
+        // memory, eight independent loads at a time
+        constexpr int kBatch = 8;
+        while (ended && i < n) {
+            uint4 op[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k)
+                op[k] = (i + k < n) ? ops[i + k] : make_uint4(0u, CNS_REC_SET, 0u, 0u);
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (!ended)
+                    break;
+                if (i + k >= n)
+                    break;
+                if (is_set_record(op[k])) {
+                    ended = false;
+                    break;
+                }
+                uint32_t o;
+                c = sm_apply(c, op[k], &o);
+                trace[i + k] = make_uint2(c, o);
+            }
+            i += kBatch;
+        }
+        if (ended)
+            *final_count = c;   // no SET after the chain start: this chain ends the stream
+    }
+    sm_flush(trace, base, cnt, s_tr);
 }
 
 // Shared-memory opt-in for both kernels, once per device.
@@ -353,6 +352,8 @@ static int sm_prepare(int device)
         return CNS_ERR_CUDA;
     if (!done[device]) {
         CNS_CUDA(cudaFuncSetAttribute(sm_suffix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSmSmemBytes)));
+        CNS_CUDA(cudaFuncSetAttribute(sm_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmSmemBytes)));
         done[device] = true;
     }
@@ -370,8 +371,8 @@ static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, u
         return CNS_ERR_INVALID_VALUE;
     sm_suffix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, trace, summ, final_dev);
     CNS_CUDA(cudaGetLastError());
-    const int64_t blocks2 = (blocks + 255) / 256;
-    sm_prefix_kernel<<<static_cast<unsigned>(blocks2), 256, 0, s>>>(ops, n, init, trace, summ, final_dev);
+    sm_prefix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, init, trace, summ,
+                                                                                    final_dev);
     CNS_CUDA(cudaGetLastError());
     return CNS_SUCCESS;
 }
