@@ -419,32 +419,18 @@ __global__ void __launch_bounds__(256) pipeline_producer_kernel(uint32_t *tiles,
     __syncthreads();
     if (s_skip)
         return;
-    // Each warp produces groups of 32 consecutive tiles: the lanes store the
-    // group's tiles together, then every lane records ADD 1 for one of those
-    // tiles in the same instruction.  The hardware merges same-address
-    // reductions of one warp instruction, so the count's L2 line sees one
-    // operation per 32 records instead of 32.
     const int q = tile_words >> 2;
-    const uint32_t lane = threadIdx.x & 31u;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    const int64_t groups = (n_tiles + 31) / 32;
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); g < groups;
-         g += warps) {
-        const int64_t t0 = g * 32;
-        const int in_group = static_cast<int>((n_tiles - t0 < 32) ? n_tiles - t0 : 32);
-        for (int k = 0; k < in_group; ++k) {
-            const int64_t t = t0 + k;
-            uint4 *d = reinterpret_cast<uint4 *>(tiles + t * tile_words);
-            const uint32_t w0 = static_cast<uint32_t>(t * tile_words);
-            for (int i = lane; i < q; i += 32) {
-                const uint32_t w = w0 + 4u * i;
-                d[i] = make_uint4(w * 2654435761u + round, (w + 1u) * 2654435761u + round,
-                                  (w + 2u) * 2654435761u + round, (w + 3u) * 2654435761u + round);
-            }
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+        uint4 *d = reinterpret_cast<uint4 *>(tiles + t * tile_words);
+        const uint32_t w0 = static_cast<uint32_t>(t * tile_words);
+        for (int i = threadIdx.x; i < q; i += blockDim.x) {
+            const uint32_t w = w0 + 4u * i;
+            d[i] = make_uint4(w * 2654435761u + round, (w + 1u) * 2654435761u + round,
+                              (w + 2u) * 2654435761u + round, (w + 3u) * 2654435761u + round);
         }
-        __syncwarp();   // every tile of the group is stored ...
-        if (static_cast<int>(lane) < in_group)
-            cnt_record_device(done, CNS_REC_ADD, 1u);   // ... before it is counted (release), one per tile
+        __syncthreads();   // the whole tile is stored ...
+        if (threadIdx.x == 0)
+            cnt_record_device(done, CNS_REC_ADD, 1u);   // ... before it is counted (release)
     }
 }
 
@@ -773,10 +759,11 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     // Producer CTAs wait on the device for the consumer's release before they
     // start, so together they may hold at most half of each SM's thread slots:
     // the consumer kernel and the wait kernel always find room to run.  Within
-    // that cap, one warp per group of 32 tiles.
-    const int pthreads = 64;   // two warps, each producing groups of 32 tiles
+    // that cap, one tile per CTA, so the release fence in front of each tile's
+    // count overlaps with the other tiles' work.
+    const int pthreads = std::min(256, std::max(32, ((cfg->tile_words / 4 + 31) / 32) * 32));
     const int64_t pcap = static_cast<int64_t>(dev.sm_count) * (1024 / pthreads);
-    const int64_t pwant = cfg->producer_ctas ? cfg->producer_ctas : ((cfg->tiles + 31) / 32 + 1) / 2;
+    const int64_t pwant = cfg->producer_ctas ? cfg->producer_ctas : cfg->tiles;
     const int pgrid = static_cast<int>(std::max<int64_t>(1, std::min(pwant, pcap)));
     const int64_t n_words = cfg->tiles * cfg->tile_words;
     const int cgrid = static_cast<int>(std::min<int64_t>(2 * dev.sm_count, (n_words / 4 + 255) / 256));

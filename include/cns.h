@@ -427,9 +427,8 @@ typedef struct {
     uint32_t *released_dev;  /* (in/out, optional) uint32[rounds]: count seen at release */
     int64_t tiles;           /* (in) K tiles per round, >= 1 */
     int32_t tile_words;      /* (in) words per tile, multiple of 4, 4..8192 */
-    int32_t producer_ctas;   /* (in) producer grid of 64-thread CTAs; 0 = one warp per 32 tiles.
-                                Capped so that the producer CTAs hold at most half of each
-                                SM's thread slots */
+    int32_t producer_ctas;   /* (in) producer grid; 0 = one CTA per tile.  Capped so that the
+                                producer CTAs hold at most half of each SM's thread slots */
     int64_t rounds;          /* (in) rounds */
     cns_stream_t producer_stream; /* (in) the recording stream */
     cns_stream_t consumer_stream; /* (in) the waiting stream */
@@ -448,8 +447,7 @@ typedef struct {
  *   producer stream: a producer kernel whose CTAs first wait on the device
  *     until ack >= round (the consumer has finished reading the previous
  *     round), then write word w of the tile area as w * 2654435761 + round,
- *     and after each tile is stored add 1 to `done` from the device (a warp
- *     stores 32 tiles, then records their 32 ADD 1 in one instruction);
+ *     and after each tile is stored add 1 to `done` from the device;
  *   consumer stream: cntnotify wait on `done` BIGGER_OR_EQUAL tiles with
  *     isClear = 1, then a consumer kernel that sums the tile area mod 2^32
  *     into checksums[round]; its last CTA to finish records ack = round + 1.
