@@ -359,6 +359,18 @@ def secondary(cns, torch, peaks):
                                       "bytes_per_op": 24,
                                       "gbs_algorithmic": round(24 * n / (ms * 1e-3) / 1e9, 1)}
 
+    # the same ring-rotate rounds separated by the CUDA runtime's cooperative-groups grid barrier
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P_HEAD, SLOTS_HEAD)
+    g0 = torch.from_numpy(v0.view(np.int32).copy()).cuda()
+    g1 = torch.zeros_like(g0)
+    runs = []
+    for _ in range(3):
+        ms, _ = timed_run(torch, lambda: cns.check(cns.cns_probe_grid_sync(P_HEAD, 256, 100000, g0, g1), "grid sync"))
+        runs.append(ms)
+    ok = np.array_equal(g0.cpu().numpy().view(np.uint32).reshape(P_HEAD, SLOTS_HEAD),
+                        np.roll(v0, -(3 * 100000) % P_HEAD, axis=0))
+    out["cg_grid_sync_148_ring_rotate"] = {"ns_per_round": round(min(runs) * 1e6 / 100000, 2), "correct": bool(ok)}
+
     # same-address reduction throughput (all SMs)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     word = torch.zeros(1, dtype=torch.int32, device="cuda")

@@ -121,6 +121,7 @@ _SIGS = {
     "cns_pipeline_run": (c_int, [POINTER(Pipeline)]),
     "cns_probe_atomic_rtt": (c_int, [c_int, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "cns_probe_same_address_throughput": (c_int, [c_int32, c_int32, c_int32, c_void_p, c_void_p]),
+    "cns_probe_grid_sync": (c_int, [c_int32, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
     "cns_version": (c_int, [POINTER(c_int32), POINTER(c_int32)]),
     "cns_error_string": (c_char_p, [c_int]),
 }
@@ -278,6 +279,10 @@ def cns_probe_atomic_rtt(kind: int, grid: int, probe_cta: int, iters: int, line,
 
 def cns_probe_same_address_throughput(grid: int, threads: int, iters: int, word, stream=None) -> int:
     return lib().cns_probe_same_address_throughput(grid, threads, iters, ptr(word), stream_handle(stream))
+
+
+def cns_probe_grid_sync(ctas: int, threads: int, rounds: int, buf0, buf1, stream=None) -> int:
+    return lib().cns_probe_grid_sync(ctas, threads, rounds, ptr(buf0), ptr(buf1), stream_handle(stream))
 
 
 def cns_version():

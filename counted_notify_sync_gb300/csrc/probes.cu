@@ -2,6 +2,7 @@
 // roofline: the round trip of one L2 atomic (and of one load, and of the
 // arrive/poll pair) from a single thread, and the rate at which the L2 can
 // apply same-address reductions.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -37,6 +38,21 @@ __global__ void probe_rtt_kernel(int kind, int probe_cta, int iters, uint32_t *l
     const uint64_t t1 = globaltimer_ns();
     out[0] = t1 - t0;
     out[1] = smid() | (static_cast<uint64_t>(x & 0u) << 32);
+}
+
+// The same ring-rotate rounds as the headline workload, separated by the
+// CUDA runtime's own grid barrier (cooperative groups), for comparison.
+__global__ void probe_grid_sync_kernel(uint4 *buf0, uint4 *buf1, int64_t rounds)
+{
+    cooperative_groups::grid_group grid = cooperative_groups::this_grid();
+    const uint32_t P = gridDim.x, p = blockIdx.x;
+    for (int64_t r = 0; r < rounds; ++r) {
+        const uint4 *src = (r & 1) ? buf1 : buf0;
+        uint4 *dst = (r & 1) ? buf0 : buf1;
+        if (threadIdx.x == 0)
+            dst[p] = src[(p + 1u == P) ? 0u : p + 1u];
+        grid.sync();
+    }
 }
 
 __global__ void probe_red_kernel(int iters, uint32_t *word)
@@ -81,5 +97,31 @@ extern "C" int cns_probe_same_address_throughput(int32_t grid, int32_t threads, 
         return rc;
     probe_red_kernel<<<grid, threads, 0, to_stream(stream)>>>(iters, word_dev);
     CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+extern "C" int cns_probe_grid_sync(int32_t ctas, int32_t threads, int64_t rounds, void *buf0_dev, void *buf1_dev,
+                                   cns_stream_t stream)
+{
+    if (!buf0_dev || !buf1_dev)
+        return CNS_ERR_NULL_PTR;
+    if (ctas < 1 || threads < 32 || threads > 1024 || threads % 32 || rounds < 0)
+        return CNS_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(buf0_dev) & 15) || (reinterpret_cast<uintptr_t>(buf1_dev) & 15))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    uint4 *b0 = static_cast<uint4 *>(buf0_dev);
+    uint4 *b1 = static_cast<uint4 *>(buf1_dev);
+    void *args[] = {&b0, &b1, &rounds};
+    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(probe_grid_sync_kernel), dim3(ctas),
+                                                dim3(threads), args, 0, to_stream(stream));
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        (void)cudaGetLastError();
+        return CNS_ERR_NOT_RESIDENT;
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "grid-sync probe launch");
     return CNS_SUCCESS;
 }

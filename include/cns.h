@@ -485,6 +485,18 @@ int cns_probe_atomic_rtt(int kind, int32_t grid, int32_t probe_cta, int32_t iter
 int cns_probe_same_address_throughput(int32_t grid, int32_t threads, int32_t iters, uint32_t *word_dev,
                                       cns_stream_t stream);
 
+/*
+ * cns_probe_grid_sync -- the headline's ring-rotate rounds (each CTA copies
+ * one uint4 from its ring neighbour, buffers swap every round) separated by
+ * the CUDA runtime's cooperative-groups grid barrier instead of SYNCALL: a
+ * reference point for the barrier's cost.  No timeout: the launch is
+ * cooperative, so the grid is co-resident or the call fails.
+ *   buf0_dev, buf1_dev  ctas uint4 each, 16-byte aligned
+ * Errors: NULL_PTR, INVALID_VALUE, NOT_RESIDENT, CUDA.
+ */
+int cns_probe_grid_sync(int32_t ctas, int32_t threads, int64_t rounds, void *buf0_dev, void *buf1_dev,
+                        cns_stream_t stream);
+
 /* Library version and the compute capability it was built for (103). */
 int cns_version(int32_t *version, int32_t *built_sm);
 

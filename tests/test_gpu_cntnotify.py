@@ -278,3 +278,13 @@ def test_probes_return_plausible_times(cns):
     assert cns.cns_probe_same_address_throughput(sms, 256, 10, word) == 0
     torch.cuda.synchronize()
     assert int(word.item()) == sms * 256 * 10
+
+
+def test_grid_sync_probe_ring_rotate(cns):
+    import torch
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    b0 = to_dev_u32(v0)
+    b1 = torch.zeros_like(b0)
+    assert cns.cns_probe_grid_sync(148, 256, 1001, b0, b1) == 0
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(from_dev_u32(b1).reshape(148, 4), np.roll(v0, -1001, axis=0))
