@@ -180,7 +180,11 @@ class ClockSampler:
 
 
 def probe_rtt(cns, torch, sms, kind, iters=2000):
-    """Per-CTA-position round trips of one dependent chain; returns (median ns, min, max, by SM)."""
+    """Per-CTA-position round trips of one dependent chain; returns (median ns, min, max, by SM).
+
+    On a two-die part the per-SM values are bimodal (the die that homes the
+    line answers in ~150 ns, the other in ~350 ns), so the median jumps between
+    the modes with the SM split; the mean over SMs is the stable summary."""
     line = torch.zeros(32, dtype=torch.int32, device="cuda")
     out = torch.zeros(2, dtype=torch.int64, device="cuda")
     per = {}
@@ -413,7 +417,8 @@ def run_native(args):
     peaks = load_peaks()
     sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
 
-    rtt_med, rtt_min, rtt_max, _ = probe_rtt(cns, torch, sms, 0)
+    rtt_med, rtt_min, rtt_max, rtt_per = probe_rtt(cns, torch, sms, 0)
+    rtt_mean = statistics.mean(rtt_per.values())
     pair_med, _, _, _ = probe_rtt(cns, torch, sms, 2)
     ld_med, _, _, _ = probe_rtt(cns, torch, sms, 1)
 
@@ -431,7 +436,7 @@ def run_native(args):
     cpu = time_oracle(args.cpu_seconds) if world == 1 else None
     traffic = load_traffic().get("syncall_soft_ring_rotate_148", {})
     achieved = 1e3 / ns_round            # barrier rounds per microsecond
-    peak = 1e3 / rtt_med                 # one round per L2 atomic round trip
+    peak = 1e3 / rtt_mean                # one round per L2 atomic round trip (mean over SMs)
     line = {
         "metric": METRIC, "value": round(ns_round, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": False, "scaling": "weak",
@@ -446,12 +451,13 @@ def run_native(args):
         "roofline": {"bound": "l2_atomic_latency", "achieved": round(achieved, 5), "peak": round(peak, 5),
                      "unit": "barrier rounds/us", "frac": round(achieved / peak, 4),
                      "traffic": traffic.get("dram_bytes_per_launch"),
-                     "peak_source": "live probe: median over all SMs of one thread's dependent "
+                     "peak_source": "live probe: mean over all SMs of one thread's dependent "
                                     "atom.add.relaxed.gpu chain on one 128 B line",
-                     "rtt_ns": {"atom_median": round(rtt_med, 1), "atom_min": round(rtt_min, 1),
+                     "rtt_ns": {"atom_mean": round(rtt_mean, 1), "atom_median": round(rtt_med, 1),
+                                "atom_min": round(rtt_min, 1),
                                 "atom_max": round(rtt_max, 1), "arrive_poll_pair_median": round(pair_med, 1),
                                 "ld_relaxed_median": round(ld_med, 1)},
-                     "ns_per_round_over_rtt": round(ns_round / rtt_med, 3)},
+                     "ns_per_round_over_rtt": round(ns_round / rtt_mean, 3)},
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,

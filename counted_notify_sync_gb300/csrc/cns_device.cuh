@@ -263,12 +263,41 @@ __device__ __forceinline__ uint32_t epoch_target(uint32_t before, const Epoch &e
     return t == M ? 0u : static_cast<uint32_t>(t);
 }
 
+// (cur - target) mod M < P in 32-bit arithmetic: the wrapping difference is
+// the distance in Z_M unless it wrapped, in which case it exceeds that
+// distance by 2^32 - M (= ~Mm1; zero when M = 2^32).
 __device__ __forceinline__ bool epoch_reached(uint32_t cur, uint32_t target, const Epoch &e)
 {
-    const uint64_t M = static_cast<uint64_t>(e.Mm1) + 1u;
-    uint64_t d = cur >= target ? static_cast<uint64_t>(cur - target)
-                               : static_cast<uint64_t>(cur) + (M - target);
+    uint32_t d = cur - target;
+    if (cur < target)
+        d -= ~e.Mm1;
     return d < e.P;
+}
+
+// The epoch that the caller's previous barrier closed: [start, start + P) in
+// Z_M, start a multiple of P.  In a well-formed round an arrival's `before`
+// lies in that epoch, so ((before / P) + 1) * P mod M is just `end`; the
+// cursor gives the same target as the formula without the division, and the
+// formula is still evaluated whenever `before` falls outside (first round, or
+// a counter that someone else moved).
+struct EpochCursor {
+    uint32_t start;
+    uint32_t end;     // start + P in Z_M
+    bool valid;
+};
+
+__device__ __forceinline__ uint32_t epoch_target(uint32_t before, const Epoch &e, const EpochCursor &c)
+{
+    if (c.valid && before - c.start < e.P)   // wraps to >= P when before < start (start <= M - P)
+        return c.end;
+    return epoch_target(before, e);
+}
+
+__device__ __forceinline__ void epoch_advance(EpochCursor &c, uint32_t target, const Epoch &e)
+{
+    c.start = target;
+    c.end = (target == e.Mm1 + 1u - e.P) ? 0u : target + e.P;   // M - P wraps to 0
+    c.valid = true;
 }
 
 // Status line of the workspace: [0] status, [1] abort flag, [2] round of the
@@ -373,56 +402,63 @@ __device__ __forceinline__ void choose_near_copy(Barrier &b)
     }
 }
 
-__device__ __forceinline__ bool arrive_and_wait(const Barrier &b, uint32_t round, uint32_t who)
+__device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c, uint32_t round, uint32_t who)
 {
     const int v = b.variant;
+    uint32_t target;
+    bool stop;
     if (v == kBvDieLocal) {
         fence_release_gpu();
         red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
         const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
-        return poll_epoch(b.ctr, epoch_target(before, b.e), b.e, b.status_line, b.timeout_ns, round, who);
-    }
-    const uint32_t before = (v == kBvCounterAcquire) ? atom_inc_release_gpu(b.ctr, b.e.Mm1)
-                                                     : atom_inc_acq_rel_gpu(b.ctr, b.e.Mm1);
-    const uint32_t target = epoch_target(before, b.e);
-    if (v != kBvCounterAcquire) {
+        target = epoch_target(before, b.e, c);
+        stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who);
+    } else {
+        const uint32_t before = (v == kBvCounterAcquire) ? atom_inc_release_gpu(b.ctr, b.e.Mm1)
+                                                         : atom_inc_acq_rel_gpu(b.ctr, b.e.Mm1);
+        target = epoch_target(before, b.e, c);
         const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;   // the count after this arrival
-        if (epoch_reached(mine, target, b.e)) {
+        if (v != kBvCounterAcquire && epoch_reached(mine, target, b.e)) {
             // the last arrival of the round: its acquire-release increment has
             // already seen every other arrival of the round
             if (v == kBvFlag)
                 st_release_gpu(b.flag, target);
-            return false;
+            stop = false;
+        } else if (v == kBvFlag) {
+            stop = poll_epoch(b.flag, target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
+        } else {
+            stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who, v >= kBvRelaxedPoll,
+                              v == kBvBackoff ? 32u : 0u);
         }
     }
-    if (v == kBvFlag)
-        return poll_epoch(b.flag, target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
-    return poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who, v >= kBvRelaxedPoll,
-                      v == kBvBackoff ? 32u : 0u);
+    epoch_advance(c, target, b.e);
+    return stop;
 }
 
 // One soft barrier for the calling CTA: drain the CTA, one elected thread
-// arrives and waits, drain again.  All threads of the CTA must call it.
-// Returns true if the CTA must stop (timeout / abort).
-__device__ __forceinline__ bool soft_barrier(const Barrier &b, uint32_t round, int *s_flag)
+// arrives and waits, then a block barrier whose OR reduction hands the
+// elected thread's stop decision to every thread.  All threads of the CTA
+// must call it; only thread 0's cursor is used.  Returns true if the CTA must
+// stop (timeout / abort).
+__device__ __forceinline__ bool soft_barrier(const Barrier &b, EpochCursor &c, uint32_t round)
 {
     __syncthreads();
+    int stop = 0;
     if (threadIdx.x == 0)
-        *s_flag = arrive_and_wait(b, round, blockIdx.x) ? 1 : 0;
-    __syncthreads();
-    return *s_flag != 0;
+        stop = arrive_and_wait(b, c, round, blockIdx.x) ? 1 : 0;
+    return __syncthreads_or(stop) != 0;
 }
 
 // One hard barrier: cluster barrier; cluster rank 0 arrives on the
 // per-cluster counter (P = number of clusters) and waits; on a timeout it
 // writes the stop flag into every CTA of its cluster; second cluster barrier.
 // All threads of all CTAs of the cluster must call it.
-__device__ __forceinline__ bool hard_barrier(const Barrier &b, uint32_t round, int *s_flag)
+__device__ __forceinline__ bool hard_barrier(const Barrier &b, EpochCursor &c, uint32_t round, int *s_flag)
 {
     __syncwarp();
     cluster_sync_all();
     if (threadIdx.x == 0 && cluster_ctarank() == 0) {
-        if (arrive_and_wait(b, round, blockIdx.x)) {
+        if (arrive_and_wait(b, c, round, blockIdx.x)) {
             const uint32_t n = cluster_nctarank();
             for (uint32_t r = 0; r < n; ++r)
                 st_shared_cluster(s_flag, r, 1u);

@@ -234,11 +234,12 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
     Barrier bar = p.bar;
     if (bar.variant == kBvDieLocal && threadIdx.x == 0 && (MODE == CNS_SYNCALL_SOFT || cluster_ctarank() == 0))
         choose_near_copy(bar);
+    EpochCursor cursor{0u, 0u, false};
     bool stop = false;
     for (int64_t r = 0; r < p.rounds; ++r) {
         data_phase<WL>(p, r, b, js);
-        stop = (MODE == CNS_SYNCALL_SOFT) ? soft_barrier(bar, static_cast<uint32_t>(r), &s_flag)
-                                          : hard_barrier(bar, static_cast<uint32_t>(r), &s_flag);
+        stop = (MODE == CNS_SYNCALL_SOFT) ? soft_barrier(bar, cursor, static_cast<uint32_t>(r))
+                                          : hard_barrier(bar, cursor, static_cast<uint32_t>(r), &s_flag);
         if (stop)
             break;
     }
