@@ -242,6 +242,14 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst_smem, const void *src_gm
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream, if it was launched with programmatic stream serialization, be
+// scheduled before this grid ends; that kernel's dependency_wait returns once
+// every prerequisite grid has completed and its memory operations are visible
+// (at once when there is none).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Epoch arithmetic of the soft barrier ("PTO-ISA SYNCALL cross-core barrier
 // guide", §5.2).  The counter lives in Z_M with M = P * floor(2^32 / P): the

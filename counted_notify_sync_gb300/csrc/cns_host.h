@@ -48,6 +48,7 @@ inline int cuda_fail(cudaError_t e, const char *what)
 struct DeviceInfo {
     int device = -1;
     int sm_count = 0;
+    int max_threads_per_sm = 0;
     int cc_major = 0, cc_minor = 0;
 };
 

@@ -108,10 +108,16 @@ __global__ void cnt_record_kernel(uint32_t *count, uint32_t mode, uint32_t v)
 // clear.  On timeout the sticky status is set and the kernel returns.  With
 // an `abort` word (used by the pipeline), a wait that finds it raised returns
 // at once and a wait that times out raises it, so one lost signal costs one
-// timeout rather than one per remaining round.
+// timeout rather than one per remaining round.  kEarlyNext (the pipeline's
+// own waits) lets the stream's next kernel, launched with programmatic
+// stream serialization, be scheduled while this one polls; that kernel waits
+// on the device for this one to end (grid_dependency_wait).
+template <bool kEarlyNext>
 __global__ void cnt_wait_kernel(uint32_t *line, uint32_t mode, uint32_t v, uint32_t clear, uint64_t timeout_ns,
-                                uint32_t *observed, uint32_t *abort)
+                                uint32_t *observed, uint32_t *abort, uint64_t *released_at)
 {
+    if (kEarlyNext)
+        grid_launch_dependents();
     if (threadIdx.x != 0)
         return;
     if (abort && ld_relaxed_gpu(abort) != 0u)
@@ -121,6 +127,8 @@ __global__ void cnt_wait_kernel(uint32_t *line, uint32_t mode, uint32_t v, uint3
     for (;;) {
         const uint32_t c = ld_acquire_gpu(line);
         if (cnt_wait_released(c, mode, v)) {
+            if (released_at)
+                *released_at = globaltimer_ns();
             if (observed)
                 *observed = c;
             if (clear)
@@ -165,10 +173,11 @@ static bool record_mode_ok(int32_t m)
 }
 
 static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info_t *info, uint32_t *observed,
-                        uint32_t *abort = nullptr)
+                        uint32_t *abort = nullptr, bool early_next = false, uint64_t *released_at = nullptr)
 {
-    cnt_wait_kernel<<<1, 32, 0, s>>>(n->line, static_cast<uint32_t>(info->mode), info->value,
-                                     info->is_clear ? 1u : 0u, wait_timeout_ns(info->timeout), observed, abort);
+    auto k = early_next ? cnt_wait_kernel<true> : cnt_wait_kernel<false>;
+    k<<<1, 32, 0, s>>>(n->line, static_cast<uint32_t>(info->mode), info->value, info->is_clear ? 1u : 0u,
+                       wait_timeout_ns(info->timeout), observed, abort, released_at);
     CNS_CUDA(cudaGetLastError());
     return CNS_SUCCESS;
 }
@@ -384,11 +393,21 @@ __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
 // ---------------------------------------------------------------------------
 
 // Producer of one round.  Before touching the tiles every CTA waits, on the
-// device, until the consumer has released the previous round (ack >= round);
-// then it stores its tile and adds 1 to `done` (a release record).
-__global__ void __launch_bounds__(256) pipeline_producer_kernel(uint32_t *tiles, int64_t n_tiles, int tile_words,
-                                                                uint32_t round, uint32_t *done, uint32_t *ack,
-                                                                uint64_t timeout_ns, uint32_t *abort)
+// device, until the consumer has released the previous round (ack >= round).
+// CTA b owns tiles b, b + grid, b + 2 grid, ...; all of its threads store
+// them, then, after the block barrier, lane j of warp 0 adds 1 to `done` for
+// the CTA's tile j (j < 32, then the next 32, ...).  Each of those is one
+// release ADD 1 record of the counted notify; the lanes of one instruction
+// reach the same word, and the memory system combines them into one L2
+// operation, so a CTA with k <= 32 tiles costs the count line one operation,
+// not k.  (Same-address operations are served one at a time by the L2 slice
+// that homes the line, about 1.25 ns each on GB300: one record per tile from
+// 4096 CTAs costs 5 us per round on that line alone.)
+constexpr int kPipeProducerThreads = 256;
+
+__global__ void __launch_bounds__(kPipeProducerThreads, 8)
+    pipeline_producer_kernel(uint32_t *tiles, int64_t n_tiles, int tile_words, uint32_t round, uint32_t *done,
+                             uint32_t *ack, uint64_t timeout_ns, uint32_t *abort, uint64_t *started_at)
 {
     __shared__ int s_skip;
     if (threadIdx.x == 0) {
@@ -415,32 +434,46 @@ __global__ void __launch_bounds__(256) pipeline_producer_kernel(uint32_t *tiles,
             }
         }
         s_skip = skip;
+        if (started_at && blockIdx.x == 0)
+            *started_at = globaltimer_ns();   // CTA 0 released: the round's recording phase begins
     }
     __syncthreads();
     if (s_skip)
         return;
-    const int q = tile_words >> 2;
-    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const int64_t grid = gridDim.x;
+    const int64_t mine = (n_tiles - blockIdx.x + grid - 1) / grid;   // tiles of this CTA (blockIdx.x < n_tiles)
+    const uint32_t q = static_cast<uint32_t>(tile_words) >> 2;      // uint4 per tile
+    const uint32_t total = static_cast<uint32_t>(mine) * q;          // <= 2^30: tiles * tile_words <= 2^32
+    for (uint32_t e = threadIdx.x; e < total; e += blockDim.x) {
+        const uint32_t j = e / q;
+        const uint32_t i = e - j * q;
+        const int64_t t = blockIdx.x + static_cast<int64_t>(j) * grid;
         uint4 *d = reinterpret_cast<uint4 *>(tiles + t * tile_words);
-        const uint32_t w0 = static_cast<uint32_t>(t * tile_words);
-        for (int i = threadIdx.x; i < q; i += blockDim.x) {
-            const uint32_t w = w0 + 4u * i;
-            d[i] = make_uint4(w * 2654435761u + round, (w + 1u) * 2654435761u + round,
-                              (w + 2u) * 2654435761u + round, (w + 3u) * 2654435761u + round);
-        }
-        __syncthreads();   // the whole tile is stored ...
-        if (threadIdx.x == 0)
-            cnt_record_device(done, CNS_REC_ADD, 1u);   // ... before it is counted (release)
+        const uint32_t w = static_cast<uint32_t>(t * tile_words) + 4u * static_cast<uint32_t>(i);
+        d[i] = make_uint4(w * 2654435761u + round, (w + 1u) * 2654435761u + round, (w + 2u) * 2654435761u + round,
+                          (w + 3u) * 2654435761u + round);
+    }
+    __syncthreads();   // every tile of the CTA is stored ...
+    if (threadIdx.x < 32) {
+        for (int64_t j0 = 0; j0 < mine; j0 += 32)
+            if (j0 + threadIdx.x < mine)
+                cnt_record_device(done, CNS_REC_ADD, 1u);   // ... before any of them is counted (release)
     }
 }
 
 // Consumer of one round: sums the tile area mod 2^32 into *checksum; the last
 // CTA to finish (counted on `finish`) records ack = ack_value, which lets the
 // next round's producer overwrite the tiles.
-__global__ void __launch_bounds__(256) pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words,
-                                                                uint32_t *checksum, uint32_t *ack,
-                                                                uint32_t ack_value, uint32_t *finish)
+// It is launched with programmatic stream serialization behind the wait, so
+// its CTAs may be scheduled while the wait still polls: they first wait on the
+// device until the wait kernel has ended.
+constexpr int kPipeConsumerThreads = 256;
+
+__global__ void __launch_bounds__(kPipeConsumerThreads, 8)
+    pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words, uint32_t *checksum, uint32_t *ack,
+                             uint32_t ack_value, uint32_t *finish)
 {
+    grid_dependency_wait();
     const uint4 *t4 = reinterpret_cast<const uint4 *>(tiles);
     uint32_t s = 0;
     const int64_t n4 = n_words >> 2;
@@ -756,17 +789,34 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     if (dev.device != done->device)
         return CNS_ERR_INVALID_VALUE;
     cudaStream_t sp = to_stream(cfg->producer_stream), sc = to_stream(cfg->consumer_stream);
-    // Producer CTAs wait on the device for the consumer's release before they
-    // start, so together they may hold at most half of each SM's thread slots:
-    // the consumer kernel and the wait kernel always find room to run.  Within
-    // that cap, one tile per CTA, so the release fence in front of each tile's
-    // count overlaps with the other tiles' work.
-    const int pthreads = std::min(256, std::max(32, ((cfg->tile_words / 4 + 31) / 32) * 32));
-    const int64_t pcap = static_cast<int64_t>(dev.sm_count) * (1024 / pthreads);
+    // Residency.  Producer CTAs wait on the device for the consumer's release
+    // (ack), and the consumer's CTAs, scheduled early behind the stream wait,
+    // wait on the device for that wait to end; neither group may keep the
+    // other from being placed.  Producer CTAs hold at most half of the GPU's
+    // thread slots, consumer CTAs at most a quarter, both at <= 32 registers
+    // a thread (launch bounds), so registers run in step with thread slots.
+    // A producer CTA (256 threads) that found no SM with room would need every
+    // SM to have more than (slots - 256) threads in use, i.e. more than 7/8 of
+    // the GPU, while everything here holds at most 3/4 plus two one-warp wait
+    // kernels.  (Work of other streams running at the same time can still
+    // starve a round; the bounded waits then end it with CNS_ERR_TIMEOUT.)
+    const int per_sm = dev.max_threads_per_sm > 0 ? dev.max_threads_per_sm : 2048;
+    const int64_t pcap = static_cast<int64_t>(dev.sm_count) * std::max(1, per_sm / 2 / kPipeProducerThreads);
     const int64_t pwant = cfg->producer_ctas ? cfg->producer_ctas : cfg->tiles;
-    const int pgrid = static_cast<int>(std::max<int64_t>(1, std::min(pwant, pcap)));
+    const int pgrid = static_cast<int>(std::max<int64_t>(1, std::min(std::min(pwant, pcap), cfg->tiles)));
     const int64_t n_words = cfg->tiles * cfg->tile_words;
-    const int cgrid = static_cast<int>(std::min<int64_t>(2 * dev.sm_count, (n_words / 4 + 255) / 256));
+    const int64_t ccap = static_cast<int64_t>(dev.sm_count) * std::max(1, per_sm / 4 / kPipeConsumerThreads);
+    const int cgrid = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>(ccap, (n_words / 4 + kPipeConsumerThreads - 1) / kPipeConsumerThreads)));
+    cudaLaunchAttribute early[1];
+    early[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    early[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3(cgrid);
+    ccfg.blockDim = dim3(kPipeConsumerThreads);
+    ccfg.stream = sc;
+    ccfg.attrs = early;
+    ccfg.numAttrs = 1;
 
     std::vector<cudaEvent_t> ev;
     auto cleanup = [&] {
@@ -776,8 +826,13 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     cudaEvent_t join;
     CNS_CUDA(cudaEventCreateWithFlags(&join, cudaEventDisableTiming));
     ev.push_back(join);
+    // Timing (sync=1): two events around the whole run, and per round two
+    // device timestamps -- CTA 0 of the producer passing its release, the
+    // stream wait releasing -- whose differences sum to producer_ms.  (An
+    // event pair per round would sit between the producer launches and slow
+    // the round trip it measures.)
     const bool timed = cfg->sync != 0;
-    const int64_t n_ev = timed ? 2 * cfg->rounds + 2 : 0;
+    const int64_t n_ev = timed ? 2 : 0;
     for (int64_t i = 0; i < n_ev; ++i) {
         cudaEvent_t e;
         if (cudaEventCreate(&e) != cudaSuccess) {
@@ -802,10 +857,16 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     check(cudaMemsetAsync(cfg->checksums_dev, 0, cfg->rounds * sizeof(uint32_t), sp), "memset checksums");
     if (cfg->released_dev)
         check(cudaMemsetAsync(cfg->released_dev, 0, cfg->rounds * sizeof(uint32_t), sp), "memset released");
+    uint64_t *stamps = nullptr;   // [2][rounds]: producer started, wait released
+    if (timed && cfg->rounds > 0) {
+        if (check(cudaMallocAsync(reinterpret_cast<void **>(&stamps), 2 * cfg->rounds * sizeof(uint64_t), sp),
+                  "stamp buffer"))
+            check(cudaMemsetAsync(stamps, 0, 2 * cfg->rounds * sizeof(uint64_t), sp), "memset stamps");
+    }
     check(cudaEventRecord(join, sp), "event");
     check(cudaStreamWaitEvent(sc, join, 0), "stream wait");
     if (timed)
-        check(cudaEventRecord(T(2 * cfg->rounds), sp), "event");
+        check(cudaEventRecord(T(0), sp), "event");
 
     cns_wait_info_t w_done = {CNS_WAIT_BIGGER_OR_EQUAL, static_cast<uint32_t>(cfg->tiles), cfg->timeout_s, 1, {0, 0, 0}};
     const uint64_t ack_timeout = wait_timeout_ns(cfg->timeout_s);
@@ -816,40 +877,47 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
         // after the work that releases it.  CUDA may feed both streams through
         // one hardware queue in submission order, and a wait ahead of its
         // record would then hold that record back until it timed out.
-        if (timed)
-            check(cudaEventRecord(T(2 * r), sp), "event");
-        pipeline_producer_kernel<<<pgrid, pthreads, 0, sp>>>(cfg->tiles_dev, cfg->tiles, cfg->tile_words,
-                                                             static_cast<uint32_t>(r), done->line, ack->line,
-                                                             ack_timeout, abort);
+        pipeline_producer_kernel<<<pgrid, kPipeProducerThreads, 0, sp>>>(
+            cfg->tiles_dev, cfg->tiles, cfg->tile_words, static_cast<uint32_t>(r), done->line, ack->line, ack_timeout,
+            abort, stamps ? stamps + r : nullptr);
         check(cudaGetLastError(), "producer launch");
-        if (timed)
-            check(cudaEventRecord(T(2 * r + 1), sp), "event");
-        if (int e = enqueue_wait(done, sc, &w_done, cfg->released_dev ? cfg->released_dev + r : nullptr, abort))
+        if (int e = enqueue_wait(done, sc, &w_done, cfg->released_dev ? cfg->released_dev + r : nullptr, abort, true,
+                                 stamps ? stamps + cfg->rounds + r : nullptr))
             rc = e;
-        pipeline_consumer_kernel<<<cgrid, 256, 0, sc>>>(cfg->tiles_dev, n_words, cfg->checksums_dev + r, ack->line,
-                                                        static_cast<uint32_t>(r + 1), finish);
-        check(cudaGetLastError(), "consumer launch");
+        check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel, static_cast<const uint32_t *>(cfg->tiles_dev),
+                                 n_words, cfg->checksums_dev + r, ack->line, static_cast<uint32_t>(r + 1), finish),
+              "consumer launch");
     }
     check(cudaEventRecord(join, sc), "event");
     check(cudaStreamWaitEvent(sp, join, 0), "stream wait");
     if (timed)
-        check(cudaEventRecord(T(2 * cfg->rounds + 1), sp), "event");
+        check(cudaEventRecord(T(1), sp), "event");
+    std::vector<uint64_t> host_stamps;
+    if (stamps) {
+        host_stamps.resize(2 * cfg->rounds);
+        check(cudaMemcpyAsync(host_stamps.data(), stamps, 2 * cfg->rounds * sizeof(uint64_t), cudaMemcpyDeviceToHost,
+                              sp),
+              "read stamps");
+        check(cudaFreeAsync(stamps, sp), "free stamps");
+    }
     if (rc != CNS_SUCCESS || !timed) {
         cleanup();
         return rc;
     }
-    if (!check(cudaEventSynchronize(T(2 * cfg->rounds + 1)), "sync")) {
+    if (!check(cudaStreamSynchronize(sp), "sync")) {
         cleanup();
         return rc;
     }
-    float total = 0.f, prod = 0.f;
-    check(cudaEventElapsedTime(&total, T(2 * cfg->rounds), T(2 * cfg->rounds + 1)), "elapsed");
-    for (int64_t r = 0; r < cfg->rounds; ++r) {
-        float ms = 0.f;
-        check(cudaEventElapsedTime(&ms, T(2 * r), T(2 * r + 1)), "elapsed");
-        prod += ms;
-    }
+    float total = 0.f;
+    check(cudaEventElapsedTime(&total, T(0), T(1)), "elapsed");
     cleanup();
+    double prod_ns = 0.0;
+    for (int64_t r = 0; r < cfg->rounds; ++r) {
+        const uint64_t a = host_stamps[r], b = host_stamps[cfg->rounds + r];
+        if (a && b > a)
+            prod_ns += static_cast<double>(b - a);
+    }
+    const float prod = static_cast<float>(prod_ns * 1e-6);
     cfg->elapsed_ms = total;
     cfg->producer_ms = prod;
     int32_t st_done = 0, st_ack = 0;

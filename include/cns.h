@@ -427,16 +427,18 @@ typedef struct {
     uint32_t *released_dev;  /* (in/out, optional) uint32[rounds]: count seen at release */
     int64_t tiles;           /* (in) K tiles per round, >= 1 */
     int32_t tile_words;      /* (in) words per tile, multiple of 4, 4..8192 */
-    int32_t producer_ctas;   /* (in) producer grid; 0 = one CTA per tile.  Capped so that the
-                                producer CTAs hold at most half of each SM's thread slots */
+    int32_t producer_ctas;   /* (in) producer grid of 256-thread CTAs; 0 = one CTA per tile.
+                                Capped at the tile count and so that the producer holds at most
+                                half of the GPU's thread slots (4 CTAs per SM on GB300) */
     int64_t rounds;          /* (in) rounds */
     cns_stream_t producer_stream; /* (in) the recording stream */
     cns_stream_t consumer_stream; /* (in) the waiting stream */
     uint32_t timeout_s;      /* (in) per-wait timeout in seconds; 0 = library cap */
     int32_t sync;            /* (in) 1: wait, time, check the notifies' status */
     float elapsed_ms;        /* (out, sync=1) first producer launch to last record */
-    float producer_ms;       /* (out, sync=1) summed producer-kernel time, including each
-                                producer's wait for the previous round's release */
+    float producer_ms;       /* (out, sync=1) summed recording phases: per round, from CTA 0 of
+                                the producer passing its wait for the previous round's
+                                release to the consumer-side wait releasing (device clock) */
     int32_t device_status;   /* (out, sync=1) 0 or CNS_ERR_TIMEOUT */
     int32_t reserved[3];
 } cns_pipeline_t;
@@ -446,11 +448,17 @@ typedef struct {
  * streams that meet only through two counted notifies.
  *   producer stream: a producer kernel whose CTAs first wait on the device
  *     until ack >= round (the consumer has finished reading the previous
- *     round), then write word w of the tile area as w * 2654435761 + round,
- *     and after each tile is stored add 1 to `done` from the device;
+ *     round), then write word w of the tile area as w * 2654435761 + round;
+ *     CTA b writes tiles b, b + grid, ... and, once they are all stored,
+ *     records ADD 1 on `done` from the device for each of them (one lane of
+ *     one warp per tile, so the lanes' records travel as one L2 operation);
  *   consumer stream: cntnotify wait on `done` BIGGER_OR_EQUAL tiles with
  *     isClear = 1, then a consumer kernel that sums the tile area mod 2^32
  *     into checksums[round]; its last CTA to finish records ack = round + 1.
+ *     The consumer is launched with programmatic stream serialization: its
+ *     CTAs may be scheduled while the wait polls and wait on the device for
+ *     it to end.  Grids are sized so that producer and consumer CTAs always
+ *     fit on the GPU together (half and a quarter of its thread slots).
  * The call first clears both notifies (count and status); `done` ends at 0
  * and `ack` at `rounds`.  Once a wait times out the pipeline's remaining
  * waits return at once, so a lost signal costs one timeout, not one per round.

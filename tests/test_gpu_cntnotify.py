@@ -262,6 +262,32 @@ def test_pipeline_small_odd_shapes(cns):
         cns.cntnotify_destroy(ack)
 
 
+@pytest.mark.parametrize("tiles,tile_words,rounds,producer_ctas", [
+    (4096, 256, 20, 1),        # one CTA records all 4096 tiles, 32 lanes at a time
+    (4096, 256, 20, 33),       # 124 or 125 tiles per CTA: a ragged last group of lanes
+    (4096, 256, 20, 100000),   # more CTAs than the cap and than tiles
+    (1000, 4, 30, 0),          # one uint4 per tile
+    (40, 8192, 6, 0),          # large tiles, 2048 uint4 each
+    (1, 4, 3, 0),              # one tile
+])
+def test_pipeline_producer_grids(cns, tiles, tile_words, rounds, producer_ctas):
+    import torch
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    try:
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, tiles, tile_words, rounds, s1, s2, timeout_s=10,
+                                                        producer_ctas=producer_ctas)
+        assert rc == 0 and cfg.device_status == 0
+        want_cs, want_rel = oracle.pipeline(tiles, tile_words, rounds)
+        np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
+        np.testing.assert_array_equal(from_dev_u32(released), want_rel)
+        assert count_of(cns, done) == (0, 0) and count_of(cns, ack) == (0, rounds)
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
+
+
 # --- probes ------------------------------------------------------------------------------------
 
 def test_probes_return_plausible_times(cns):
