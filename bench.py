@@ -93,6 +93,31 @@ def time_oracle(budget_s: float):
             "host_cores_available": os.cpu_count()}
 
 
+def time_twin():
+    """The multithreaded CPU timing twin on all host cores, beside the GPU figures:
+    the headline ring (148 participants, 100000 rounds), Jacobi at N = 2^26 for 200
+    sweeps, and the two-thread pipeline (4096 tiles x 256 words, 100 rounds)."""
+    from oracle import twin
+    twin.build()
+    T = twin.host_threads()
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P_HEAD, SLOTS_HEAD)
+    out, sec, fc = twin.syncall_ring(twin.RING_ROTATE, v0, ROUNDS_HEAD, T)
+    ok_ring = np.array_equal(out, np.roll(v0, -(ROUNDS_HEAD % P_HEAD), axis=0)) and fc == ROUNDS_HEAD * min(T, P_HEAD)
+    N, S = 1 << 26, 200
+    u0 = ci.jacobi_field(N)
+    _, jsec = twin.jacobi(u0, S, T)
+    del u0
+    n = 4096 * 256
+    cs, psec = twin.pipeline(4096, 256, 100)
+    want = np.array([(2654435761 * (n * (n - 1) // 2) + n * r) % (1 << 32) for r in range(100)], dtype=np.uint32)
+    return {"kind": "multithreaded CPU timing twin (pthreads, C11 atomics, the pages' epoch barrier among threads)",
+            "threads": T,
+            "soft_148_ring_rotate_ns_per_round": round(sec * 1e9 / ROUNDS_HEAD, 1), "ring_correct": bool(ok_ring),
+            "jacobi_2p26_200sweeps_gbs": round(S * 8 * N / jsec / 1e9, 1),
+            "pipeline_4096x256_round_trips_per_s": round(100 / psec, 1),
+            "pipeline_correct": bool(np.array_equal(cs, want))}
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle, one full workload per step."""
     rank, _, world = dist_env()
@@ -452,6 +477,8 @@ def run_native(args):
             torch.distributed.destroy_process_group()
         return
     cpu = time_oracle(args.cpu_seconds) if world == 1 else None
+    if cpu is not None and not args.no_secondary:
+        cpu["twin"] = time_twin()
     traffic = load_traffic().get("syncall_soft_ring_rotate_148", {})
     achieved = 1e3 / ns_round            # barrier rounds per microsecond
     peak = 1e3 / rtt_mean                # one round per L2 atomic round trip (mean over SMs)
