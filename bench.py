@@ -38,7 +38,8 @@ UNIT = "ns/round"
 P_HEAD, SLOTS_HEAD, ROUNDS_HEAD = 148, 4, 100000
 WORKLOAD = ("soft SYNCALL, AIV-only, 148 CTAs x 256 threads (1 per SM), ring-rotate payload of 4 uint32 per CTA, "
             "100000 rounds per launch, counter zeroed at start")
-VARIANT_NAMES = ["counter_acquire", "last_skips", "relaxed_poll", "backoff", "flag_broadcast", "die_local"]
+VARIANT_NAMES = ["counter_acquire", "last_skips", "relaxed_poll", "backoff", "flag_broadcast", "die_local",
+                 "sense_flip"]
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -316,7 +317,7 @@ def secondary(cns, torch, peaks):
         out[label] = {"ns_per_round": round(ms * 1e6 / R, 2), "rounds": R, "participants": P,
                       "cluster": d.cluster_used, "status": st}
 
-    for v in range(6):
+    for v in range(len(VARIANT_NAMES)):
         ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
              label=f"soft_148_ring_rotate_variant{v}")
         ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_EMPTY, 148, 148, 0, 100000, variant=v,
@@ -462,6 +463,10 @@ def run_native(args):
 
     rtt_med, rtt_min, rtt_max, rtt_per = probe_rtt(cns, torch, sms, 0)
     rtt_mean = statistics.mean(rtt_per.values())
+    # per die: the SMs split into the die that homes the probed line (near) and the other (far)
+    thr = (rtt_min + rtt_max) / 2
+    near = [v for v in rtt_per.values() if v < thr]
+    far = [v for v in rtt_per.values() if v >= thr]
     pair_med, _, _, _ = probe_rtt(cns, torch, sms, 2)
     ld_med, _, _, _ = probe_rtt(cns, torch, sms, 1)
 
@@ -499,6 +504,9 @@ def run_native(args):
                      "peak_source": "live probe: mean over all SMs of one thread's dependent "
                                     "atom.add.relaxed.gpu chain on one 128 B line",
                      "rtt_ns": {"atom_mean": round(rtt_mean, 1), "atom_median": round(rtt_med, 1),
+                                "atom_near_die_mean": round(statistics.mean(near), 1) if near else None,
+                                "atom_far_die_mean": round(statistics.mean(far), 1) if far else None,
+                                "sms_near_far": [len(near), len(far)],
                                 "atom_min": round(rtt_min, 1),
                                 "atom_max": round(rtt_max, 1), "arrive_poll_pair_median": round(pair_med, 1),
                                 "ld_relaxed_median": round(ld_med, 1)},

@@ -310,13 +310,18 @@ __device__ __forceinline__ void epoch_advance(EpochCursor &c, uint32_t target, c
 
 // Status line of the workspace: [0] status, [1] abort flag, [2] round of the
 // first timeout, [3] CTA of the first timeout.
-__device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t round, uint32_t who)
+__device__ __forceinline__ void raise_status(uint32_t *status_line, uint32_t code, uint32_t round, uint32_t who)
 {
-    if (atom_cas_relaxed_gpu(status_line, 0u, static_cast<uint32_t>(CNS_ERR_TIMEOUT)) == 0u) {
+    if (atom_cas_relaxed_gpu(status_line, 0u, code) == 0u) {
         st_relaxed_gpu(status_line + 2, round);
         st_relaxed_gpu(status_line + 3, who);
     }
     atom_exch_release_gpu(status_line + 1, 1u);
+}
+
+__device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t round, uint32_t who)
+{
+    raise_status(status_line, static_cast<uint32_t>(CNS_ERR_TIMEOUT), round, who);
 }
 
 // Barrier variants (cns_syncall_data_t.barrier_variant).  All of them arrive
@@ -331,6 +336,14 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //   3  as 2, with a 32 ns pause between polls (less traffic on the line)
 //   4  flag broadcast: the last arriver publishes the target to a release
 //      word on its own line; the others poll that word, not the counter
+//   6  sense flip (a comparison protocol, not the guide's arithmetic; the
+//      runtime's grid barrier of CUDA cooperative groups works this way):
+//      participant 0 adds 2^31 - (P - 1), every other participant adds 1, so
+//      a round's P additions total 2^31 and bit 31 flips exactly when the
+//      last one lands; each participant polls until bit 31 differs from the
+//      bit in the value its own addition returned.  Needs the count's low
+//      31 bits to be 0 when the run starts; an arrival that sees low bits no
+//      round of this scheme can produce stops the run (CNS_ERR_INVALID_VALUE).
 //   5  die-local replicas: the counter is kept twice, 4 KB apart.  On GB300
 //      an atomic is performed in the L2 of the die that homes its line (about
 //      150 ns from that die's SMs, 350 ns from the other's), and consecutive
@@ -342,7 +355,7 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //      arrivals of every round, so each runs the same epoch arithmetic; which
 //      die homes which copy only changes the speed, never the result.
 enum : int { kBvCounterAcquire = 0, kBvLastSkips = 1, kBvRelaxedPoll = 2, kBvBackoff = 3, kBvFlag = 4,
-             kBvDieLocal = 5 };
+             kBvDieLocal = 5, kBvSenseFlip = 6 };
 
 struct Barrier {
     uint32_t *ctr;          // arrival counter (variant 5: the near copy, once chosen)
@@ -354,19 +367,20 @@ struct Barrier {
     int variant;
 };
 
-// Wait until *word has reached `target` (in Z_M).  Returns false when
-// released, true when the wait gave up (timeout here, or an abort raised by
-// another waiter).  The abort flag and the clock are looked at once every 64
-// polls.  With relaxed polls, one acquire fence follows the successful load.
-__device__ __forceinline__ bool poll_epoch(const uint32_t *word, uint32_t target, const Epoch &e,
-                                           uint32_t *status_line, uint64_t timeout_ns, uint32_t round,
-                                           uint32_t who, bool relaxed = false, uint32_t pause_ns = 0)
+// Poll *word until `released(value)` holds.  Returns false when released,
+// true when the wait gave up (timeout here, or an abort raised by another
+// waiter).  The abort flag and the clock are looked at once every 64 polls.
+// With relaxed polls, one acquire fence follows the successful load.
+template <class Released>
+__device__ __forceinline__ bool poll_until(const uint32_t *word, Released released, uint32_t *status_line,
+                                           uint64_t timeout_ns, uint32_t round, uint32_t who, bool relaxed = false,
+                                           uint32_t pause_ns = 0)
 {
     uint32_t spins = 0;
     uint64_t deadline = 0;
     for (;;) {
         const uint32_t cur = relaxed ? ld_relaxed_gpu(word) : ld_acquire_gpu(word);
-        if (epoch_reached(cur, target, e)) {
+        if (released(cur)) {
             if (relaxed)
                 fence_acq_rel_gpu();
             return false;
@@ -385,6 +399,15 @@ __device__ __forceinline__ bool poll_epoch(const uint32_t *word, uint32_t target
             }
         }
     }
+}
+
+// Wait until *word has reached `target` (in Z_M).
+__device__ __forceinline__ bool poll_epoch(const uint32_t *word, uint32_t target, const Epoch &e,
+                                           uint32_t *status_line, uint64_t timeout_ns, uint32_t round,
+                                           uint32_t who, bool relaxed = false, uint32_t pause_ns = 0)
+{
+    return poll_until(word, [&](uint32_t cur) { return epoch_reached(cur, target, e); }, status_line, timeout_ns,
+                      round, who, relaxed, pause_ns);
 }
 
 // The elected thread's part of one barrier: arrive, compute the target from
@@ -410,9 +433,30 @@ __device__ __forceinline__ void choose_near_copy(Barrier &b)
     }
 }
 
+// Variant 6.  `who` is the CTA index; CTA 0 is participant 0 on both paths
+// (soft: participants are CTAs 0..P-1; hard: the leader of cluster 0).
+__device__ __forceinline__ bool arrive_and_wait_flip(const Barrier &b, uint32_t round, uint32_t who)
+{
+    constexpr uint32_t kSense = 0x80000000u;
+    const uint32_t P = b.e.P;
+    const uint32_t before = atom_add_release_gpu(b.ctr, who == 0u ? kSense - (P - 1u) : 1u);
+    // a round of this scheme leaves the low bits in [0, P-1] (before participant
+    // 0's addition) or [2^31 - (P-1), 2^31 - 1] (after it)
+    const uint32_t low = before & ~kSense;
+    if (low >= P && low <= kSense - P) {
+        raise_status(b.status_line, static_cast<uint32_t>(CNS_ERR_INVALID_VALUE), round, who);
+        return true;
+    }
+    const uint32_t sense = before & kSense;
+    return poll_until(b.ctr, [&](uint32_t cur) { return (cur & kSense) != sense; }, b.status_line, b.timeout_ns,
+                      round, who);
+}
+
 __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c, uint32_t round, uint32_t who)
 {
     const int v = b.variant;
+    if (v == kBvSenseFlip)
+        return arrive_and_wait_flip(b, round, who);
     uint32_t target;
     bool stop;
     if (v == kBvDieLocal) {

@@ -385,7 +385,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return CNS_ERR_INVALID_VALUE;
     if (d->workload < CNS_WL_EMPTY || d->workload > CNS_WL_JACOBI)
         return CNS_ERR_INVALID_VALUE;
-    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_DIE_LOCAL)
+    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_SENSE_FLIP)
         return CNS_ERR_INVALID_VALUE;
     if (d->workspace_bytes != 0 && d->workspace_bytes < CNS_SYNCALL_WORKSPACE_BYTES)
         return CNS_ERR_INVALID_VALUE;
@@ -557,5 +557,5 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return rc;
     d->final_counter = mode == CNS_SYNCALL_SOFT ? sc : hc;
     d->device_status = st;
-    return st == CNS_ERR_TIMEOUT ? CNS_ERR_TIMEOUT : CNS_SUCCESS;
+    return (st == CNS_ERR_TIMEOUT || st == CNS_ERR_INVALID_VALUE) ? st : CNS_SUCCESS;
 }

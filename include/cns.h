@@ -104,9 +104,10 @@ typedef enum {
 #define CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES 8192
 
 /* How a participant learns that a round's target was reached
- * (cns_syncall_data_t.barrier_variant).  Every variant arrives with one atomic
- * increment and takes target = (before / P + 1) * P from the value returned
- * ([SYNCALL] §5.2); they differ only in the wait:
+ * (cns_syncall_data_t.barrier_variant).  Variants 0-5 arrive with one atomic
+ * increment and take target = (before / P + 1) * P from the value returned
+ * ([SYNCALL] §5.2); they differ only in the wait.  Variant 6 is a comparison
+ * protocol with other arithmetic:
  *   COUNTER_ACQUIRE   poll the counter with acquire loads, every arrival
  *                     (the guide's form)
  *   LAST_SKIPS        acquire-release arrival; the arrival that itself reaches
@@ -126,14 +127,27 @@ typedef enum {
  *                     near copy (whose old value gives the target); it then polls
  *                     the near copy.  Each copy counts every arrival, so each
  *                     runs the same epoch arithmetic.  Needs a workspace of
- *                     CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES. */
+ *                     CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES.
+ *   SENSE_FLIP        not the guide's arithmetic (the scheme of the CUDA
+ *                     runtime's grid barrier, for comparison): participant 0
+ *                     (CTA 0) adds 2^31 - (P - 1) and every other participant 1,
+ *                     so one round adds 2^31 in total and bit 31 flips when the
+ *                     last arrival lands; each participant polls until bit 31
+ *                     differs from the one its own addition returned.  The
+ *                     count's low 31 bits must be 0 when the run starts
+ *                     (syncall_workspace_init with start 0 or 2^31, or a counter
+ *                     left by earlier runs of this variant); after R rounds the
+ *                     count is start + R * 2^31 mod 2^32.  An arrival that sees
+ *                     low bits no round of the scheme produces stops the run with
+ *                     device status CNS_ERR_INVALID_VALUE. */
 typedef enum {
     CNS_BARRIER_COUNTER_ACQUIRE = 0,
     CNS_BARRIER_LAST_SKIPS = 1,
     CNS_BARRIER_RELAXED_POLL = 2,
     CNS_BARRIER_BACKOFF = 3,
     CNS_BARRIER_FLAG_BROADCAST = 4,
-    CNS_BARRIER_DIE_LOCAL = 5
+    CNS_BARRIER_DIE_LOCAL = 5,
+    CNS_BARRIER_SENSE_FLIP = 6
 } cns_barrier_variant_t;
 
 /* CTA status words written to cns_syncall_data_t.cta_status_dev (optional).
@@ -234,7 +248,9 @@ typedef struct {
  * Errors: NULL_PTR (data, workspace, payload buffers the workload needs),
  * INVALID_VALUE (enum, sizes, used_cores > launched CTAs, cluster shape,
  * alignment), ARCH, NOT_RESIDENT, CUDA; with sync=1 also TIMEOUT when a
- * barrier wait ran out on the device.
+ * barrier wait ran out on the device, and INVALID_VALUE when a SENSE_FLIP
+ * arrival found a count that the scheme cannot produce (device_status says
+ * which).
  */
 int syncall_run(int mode, int core_type, int32_t used_cores, int32_t aiv_ratio,
                 int64_t rounds, cns_syncall_data_t *data);

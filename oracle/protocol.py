@@ -203,3 +203,68 @@ def explore_two_level(P: int, C: int, rounds: int, M: int | None = None, start: 
                 res.deadlocks += 1
         stack.extend(succ)
     return res
+
+
+# Sense-flip counter --------------------------------------------------------
+#
+# A comparison protocol, not the pages' arithmetic: the word has `bits` bits
+# and its top bit is the sense.  Participant 0 adds 2^(bits-1) - (P-1), every
+# other participant adds 1, so one barrier's P additions total exactly
+# 2^(bits-1): the low bits return to where they were and the sense flips once
+# the last participant has added.  A participant polls until the sense differs
+# from the one in the value its own addition returned.  The low bits must be
+# 0 at the start (start is 0 or 2^(bits-1)).  The runtime's grid barrier of
+# CUDA cooperative groups uses this scheme with bits = 32.
+
+def explore_flip(P: int, rounds, bits: int = 8, start: int = 0, max_states: int = 2_000_000,
+                 master_add: int | None = None) -> Result:
+    """All interleavings of the sense-flip barrier.  master_add overrides
+    participant 0's addition (the tests use it to plant a wrong constant)."""
+    W = 1 << bits
+    top = W >> 1
+    assert P >= 1 and P < top
+    m_add = (top - (P - 1)) % W if master_add is None else master_add % W
+    if isinstance(rounds, int):
+        rounds = [rounds] * P
+    rounds = tuple(rounds)
+    res = Result()
+    init = (start % W, tuple((0, 0, 0) for _ in range(P)))
+    seen = set()
+    stack = [init]
+    while stack:
+        state = stack.pop()
+        if state in seen:
+            continue
+        seen.add(state)
+        res.states += 1
+        if res.states > max_states:
+            raise RuntimeError("state space larger than max_states")
+        c, parts = state
+        arrivals = sum(k + ph for (k, ph, _) in parts)
+        succ = []
+        for i, (k, ph, s) in enumerate(parts):
+            if k == rounds[i]:
+                continue
+            if ph == 0:
+                before = c
+                add = m_add if i == 0 else 1
+                nparts = parts[:i] + ((k, 1, before & top),) + parts[i + 1:]
+                succ.append(((c + add) % W, nparts))
+            elif (c & top) != s:
+                if arrivals < (k + 1) * P:
+                    res.safety_violations += 1
+                nparts = parts[:i] + ((k + 1, 0, 0),) + parts[i + 1:]
+                succ.append((c, nparts))
+        if not succ:
+            if all(parts[i][0] == rounds[i] for i in range(P)):
+                res.completed += 1
+            else:
+                res.deadlocks += 1
+        stack.extend(succ)
+    return res
+
+
+def flip_final_counter(P: int, rounds: int, bits: int = 32, start: int = 0) -> int:
+    """Word after `rounds` complete sense-flip barriers: each adds 2^(bits-1) in total."""
+    W = 1 << bits
+    return (start + rounds * (W >> 1)) % W

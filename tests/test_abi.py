@@ -139,7 +139,7 @@ def test_syncall_argument_checks(built):
     d.threads, d.cluster_dim = 256, 3
     assert cns.syncall_run(0, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # 3 does not divide 8
     assert cns.syncall_run(0, cns.CNS_MIX, 0, 8, 1, d) == cns.CNS_ERR_INVALID_VALUE  # cluster of 9
-    d.cluster_dim, d.barrier_variant = 0, 6
+    d.cluster_dim, d.barrier_variant = 0, 7
     assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # barrier variant
     d.barrier_variant, d.workspace_bytes = cns.CNS_BARRIER_DIE_LOCAL, 512
     assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # die-local needs 8 KB

@@ -324,3 +324,57 @@ def test_variants_time_out_cleanly(cns, variant):
     d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3, start=1, timeout_ms=200,
                               check=False, variant=variant)
     assert rc == cns.CNS_ERR_TIMEOUT
+
+
+# --- sense-flip comparison variant (not the guide's arithmetic) ---------------------------
+
+from oracle.protocol import flip_final_counter  # noqa: E402
+
+FLIP = 6
+SENSE = 1 << 31
+
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+@pytest.mark.parametrize("start", [0, SENSE])
+def test_sense_flip_ring_rotate_148(cns, mode, start):
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, 20001, start=start, variant=FLIP)
+    np.testing.assert_array_equal(got, np.roll(v0, -20001, axis=0))
+    assert rc == 0 and d.device_status == 0 and (st == cns.CNS_CTA_DONE).all()
+    assert d.final_counter == flip_final_counter(148, 20001, start=start) == start ^ SENSE
+
+
+def test_sense_flip_affine_mix_and_jacobi(cns):
+    import torch
+    v0 = ci.ring_payload(ci.SEED_RING_AFFINE, 8, 256)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, 1000, variant=FLIP)
+    want, _ = expect_ring(oracle.WL_RING_AFFINE, v0, 1000)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == 0
+    v1 = ci.ring_payload(ci.SEED_XORSHIFT, 111, 256)
+    d, rc, got, st = run_ring(cns, HARD, MIX, cns.CNS_WL_XORSHIFT, 37, v1, 2000, ratio=2, variant=FLIP)
+    want, _ = expect_ring(oracle.WL_XORSHIFT, v1, 2000)
+    np.testing.assert_array_equal(got, want)
+    v2 = ci.ring_payload(ci.SEED_XORSHIFT, 64, 256)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_XORSHIFT, 148, v2, 999, used=64, variant=FLIP)
+    want, _ = expect_ring(oracle.WL_XORSHIFT, v2, 999)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == SENSE
+    u0 = ci.jacobi_field(300007)
+    b0 = to_dev_f32(u0)
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_JACOBI, 592, b0, b1, 8, elems=u0.size, workspace=ws, variant=FLIP)
+    want, _, _ = oracle.syncall_run_jacobi(u0, 8, 592)
+    np.testing.assert_array_equal(b0.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_sense_flip_rejects_a_foreign_count(cns, mode):
+    """A workspace whose count has low bits no round of the scheme produces
+    (left, say, by a run of another variant) stops the run with INVALID_VALUE."""
+    v0 = ci.ring_payload(3, 148, 4)
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, 50, start=0x12345678, check=False,
+                              variant=FLIP)
+    assert rc == cns.CNS_ERR_INVALID_VALUE and d.device_status == cns.CNS_ERR_INVALID_VALUE
+    assert ((st & 0xFF) == cns.CNS_CTA_ABORTED).all()

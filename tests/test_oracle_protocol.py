@@ -87,3 +87,42 @@ def test_sequential_final_counter():
 def test_two_level_barrier_safe_and_live(P, C, R):
     res = explore_two_level(P, C, R)
     assert res.ok and res.completed == 1, res
+
+
+# --- sense-flip comparison protocol --------------------------------------------------------
+
+from oracle.protocol import explore_flip, flip_final_counter  # noqa: E402
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4])
+@pytest.mark.parametrize("R", [1, 2, 3])
+def test_flip_barrier_safe_and_live(P, R):
+    res = explore_flip(P, R, bits=6)
+    assert res.ok and res.completed == 1
+
+
+def test_flip_barrier_from_the_other_sense():
+    assert explore_flip(3, 3, bits=6, start=32).ok
+
+
+def test_flip_barrier_needs_zero_low_bits():
+    res = explore_flip(3, 2, bits=6, start=1)
+    assert not res.ok
+
+
+@pytest.mark.parametrize("wrong", [lambda top, P: top - P, lambda top, P: top - (P - 2), lambda top, P: top])
+def test_flip_barrier_wrong_master_constant_is_caught(wrong):
+    P, bits = 3, 6
+    res = explore_flip(P, 2, bits=bits, master_add=wrong(1 << (bits - 1), P))
+    assert not res.ok
+
+
+def test_flip_barrier_skipped_barrier_deadlocks():
+    res = explore_flip(3, [2, 2, 1], bits=6)
+    assert res.deadlocks > 0
+
+
+def test_flip_final_counter():
+    assert flip_final_counter(148, 1) == 1 << 31
+    assert flip_final_counter(148, 2) == 0
+    assert flip_final_counter(148, 3, start=1 << 31) == 0
