@@ -50,7 +50,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-secondary", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--variant", type=int, default=5, help="barrier variant of the headline (cns_barrier_variant_t)")
+    ap.add_argument("--variant", type=int, default=0,
+                    help="barrier variant of the headline (cns_barrier_variant_t); 0, the guide's counter poll, "
+                         "measured fastest with the ring payload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="run one small launch pattern for a profiler capture and exit")
