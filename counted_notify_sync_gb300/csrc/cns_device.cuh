@@ -96,6 +96,13 @@ __device__ __forceinline__ void fence_release_gpu()
     asm volatile("fence.release.gpu;" ::: "memory");
 }
 
+// After a strong read (here: the read half of an atomic), makes the reading
+// thread see what the writers it read from released.
+__device__ __forceinline__ void fence_acquire_gpu()
+{
+    asm volatile("fence.acquire.gpu;" ::: "memory");
+}
+
 __device__ __forceinline__ void red_add_relaxed_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -330,8 +337,10 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 // participant learns that the target was reached.
 //   0  poll the counter with acquire loads (the guide's form, every arrival
 //      polls, even the last one)
-//   1  as 0, but the arrival is acquire-release and the last arriver of a
-//      round, whose own increment reached the target, does not poll
+//   1  as 0, but the last arriver of a round, whose own increment reached
+//      the target, does not poll: an acquire fence after its release
+//      increment makes it see every earlier arrival's writes (the increments
+//      of one round form a release sequence on the counter)
 //   2  as 1, with relaxed polling loads and one acquire fence once released
 //   3  as 2, with a 32 ns pause between polls (less traffic on the line)
 //   4  flag broadcast: the last arriver publishes the target to a release
@@ -355,7 +364,7 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //      arrivals of every round, so each runs the same epoch arithmetic; which
 //      die homes which copy only changes the speed, never the result.
 enum : int { kBvCounterAcquire = 0, kBvLastSkips = 1, kBvRelaxedPoll = 2, kBvBackoff = 3, kBvFlag = 4,
-             kBvDieLocal = 5, kBvSenseFlip = 6 };
+             kBvDieLocal = 5, kBvSenseFlip = 6, kBvCount = 7 };
 
 struct Barrier {
     uint32_t *ctr;          // arrival counter (variant 5: the near copy, once chosen)
@@ -433,9 +442,21 @@ __device__ __forceinline__ void choose_near_copy(Barrier &b)
     }
 }
 
+// An arrival whose wait has not been taken yet.  barrier_arrive performs a
+// participant's arrival (the atomic, and whatever the variant does at that
+// point) and returns what its wait needs; barrier_wait polls for the round's
+// release.  Taken back to back they are one barrier; a caller may also do
+// work between them that neither reads what other participants wrote before
+// the barrier nor overwrites what they may still read (split phase).
+struct Pending {
+    uint32_t target;   // epoch target (variants 0-5) or the sense bit (variant 6)
+    bool released;     // nothing to wait for: this arrival completed the round
+    bool stop;         // the arrival itself found an error
+};
+
 // Variant 6.  `who` is the CTA index; CTA 0 is participant 0 on both paths
 // (soft: participants are CTAs 0..P-1; hard: the leader of cluster 0).
-__device__ __forceinline__ bool arrive_and_wait_flip(const Barrier &b, uint32_t round, uint32_t who)
+__device__ __forceinline__ Pending arrive_flip(const Barrier &b, uint32_t round, uint32_t who)
 {
     constexpr uint32_t kSense = 0x80000000u;
     const uint32_t P = b.e.P;
@@ -445,46 +466,118 @@ __device__ __forceinline__ bool arrive_and_wait_flip(const Barrier &b, uint32_t 
     const uint32_t low = before & ~kSense;
     if (low >= P && low <= kSense - P) {
         raise_status(b.status_line, static_cast<uint32_t>(CNS_ERR_INVALID_VALUE), round, who);
-        return true;
+        return Pending{0u, false, true};
     }
-    const uint32_t sense = before & kSense;
-    return poll_until(b.ctr, [&](uint32_t cur) { return (cur & kSense) != sense; }, b.status_line, b.timeout_ns,
-                      round, who);
+    return Pending{before & kSense, false, false};
 }
 
+// The variant is a compile-time parameter of everything below: each
+// variant's kernel carries only its own path.  (With one kernel for all
+// variants, a change in one variant's code moved another's round time by
+// 10-20 ns.)
+template <int V>
+__device__ __forceinline__ Pending barrier_arrive(const Barrier &b, EpochCursor &c, uint32_t round, uint32_t who)
+{
+    if constexpr (V == kBvSenseFlip) {
+        return arrive_flip(b, round, who);
+    } else {
+        Pending pd{0u, false, false};
+        if constexpr (V == kBvDieLocal) {
+            fence_release_gpu();
+            red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
+            const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
+            pd.target = epoch_target(before, b.e, c);
+        } else {
+            const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
+            pd.target = epoch_target(before, b.e, c);
+            if constexpr (V != kBvCounterAcquire) {
+                const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;   // the count after this arrival
+                if (epoch_reached(mine, pd.target, b.e)) {
+                    // the last arrival of the round (see arrive_and_wait)
+                    fence_acquire_gpu();
+                    if constexpr (V == kBvFlag)
+                        st_release_gpu(b.flag, pd.target);
+                    pd.released = true;
+                }
+            }
+        }
+        epoch_advance(c, pd.target, b.e);
+        return pd;
+    }
+}
+
+// Returns true if the caller must stop (timeout, abort, or an error found by
+// the arrival).
+template <int V>
+__device__ __forceinline__ bool barrier_wait(const Barrier &b, const Pending &pd, uint32_t round, uint32_t who)
+{
+    if (pd.stop)
+        return true;
+    if (pd.released)
+        return false;
+    if constexpr (V == kBvSenseFlip) {
+        const uint32_t sense = pd.target;
+        return poll_until(b.ctr, [&](uint32_t cur) { return (cur & 0x80000000u) != sense; }, b.status_line,
+                          b.timeout_ns, round, who);
+    } else if constexpr (V == kBvFlag) {
+        return poll_epoch(b.flag, pd.target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
+    } else {
+        constexpr bool relaxed = V == kBvRelaxedPoll || V == kBvBackoff;
+        return poll_epoch(b.ctr, pd.target, b.e, b.status_line, b.timeout_ns, round, who, relaxed,
+                          V == kBvBackoff ? 32u : 0u);
+    }
+}
+
+// Arrive and wait back to back.  Written out rather than as barrier_wait(
+// barrier_arrive(...)): here the first poll is issued as soon as the target
+// is known and the bookkeeping comes after it.  The last arrival of a round
+// is released only by its own poll, so every instruction between its atomic
+// and that poll lengthens the round.
+template <int V>
 __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c, uint32_t round, uint32_t who)
 {
-    const int v = b.variant;
-    if (v == kBvSenseFlip)
-        return arrive_and_wait_flip(b, round, who);
-    uint32_t target;
-    bool stop;
-    if (v == kBvDieLocal) {
-        fence_release_gpu();
-        red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
-        const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
-        target = epoch_target(before, b.e, c);
-        stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who);
+    if constexpr (V == kBvSenseFlip) {
+        const Pending pd = arrive_flip(b, round, who);
+        if (pd.stop)
+            return true;
+        const uint32_t sense = pd.target;
+        return poll_until(b.ctr, [&](uint32_t cur) { return (cur & 0x80000000u) != sense; }, b.status_line,
+                          b.timeout_ns, round, who);
     } else {
-        const uint32_t before = (v == kBvCounterAcquire) ? atom_inc_release_gpu(b.ctr, b.e.Mm1)
-                                                         : atom_inc_acq_rel_gpu(b.ctr, b.e.Mm1);
-        target = epoch_target(before, b.e, c);
-        const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;   // the count after this arrival
-        if (v != kBvCounterAcquire && epoch_reached(mine, target, b.e)) {
-            // the last arrival of the round: its acquire-release increment has
-            // already seen every other arrival of the round
-            if (v == kBvFlag)
-                st_release_gpu(b.flag, target);
-            stop = false;
-        } else if (v == kBvFlag) {
-            stop = poll_epoch(b.flag, target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
+        uint32_t target;
+        bool stop;
+        if constexpr (V == kBvDieLocal) {
+            fence_release_gpu();
+            red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
+            const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
+            target = epoch_target(before, b.e, c);
+            stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who);
+        } else if constexpr (V == kBvCounterAcquire) {
+            const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
+            target = epoch_target(before, b.e, c);
+            stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who);
         } else {
-            stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who, v >= kBvRelaxedPoll,
-                              v == kBvBackoff ? 32u : 0u);
+            const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
+            target = epoch_target(before, b.e, c);
+            const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;   // the count after this arrival
+            if (epoch_reached(mine, target, b.e)) {
+                // the last arrival of the round: its increment read the count
+                // that every other arrival of the round had built; the fence
+                // turns that read into an acquire of their writes
+                fence_acquire_gpu();
+                if constexpr (V == kBvFlag)
+                    st_release_gpu(b.flag, target);
+                stop = false;
+            } else if constexpr (V == kBvFlag) {
+                stop = poll_epoch(b.flag, target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
+            } else {
+                stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who,
+                                  V == kBvRelaxedPoll || V == kBvBackoff, V == kBvBackoff ? 32u : 0u);
+            }
         }
+        epoch_advance(c, target, b.e);
+        return stop;
     }
-    epoch_advance(c, target, b.e);
-    return stop;
 }
 
 // One soft barrier for the calling CTA: drain the CTA, one elected thread
@@ -492,12 +585,33 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
 // elected thread's stop decision to every thread.  All threads of the CTA
 // must call it; only thread 0's cursor is used.  Returns true if the CTA must
 // stop (timeout / abort).
+template <int V>
 __device__ __forceinline__ bool soft_barrier(const Barrier &b, EpochCursor &c, uint32_t round)
 {
     __syncthreads();
     int stop = 0;
     if (threadIdx.x == 0)
-        stop = arrive_and_wait(b, c, round, blockIdx.x) ? 1 : 0;
+        stop = arrive_and_wait<V>(b, c, round, blockIdx.x) ? 1 : 0;
+    return __syncthreads_or(stop) != 0;
+}
+
+// The two halves of soft_barrier.  soft_arrive drains the CTA and lets thread
+// 0 arrive (its Pending lives in thread 0's registers); soft_wait lets thread
+// 0 wait and hands its decision to every thread.  All threads call both.
+template <int V>
+__device__ __forceinline__ void soft_arrive(const Barrier &b, EpochCursor &c, uint32_t round, Pending &pd)
+{
+    __syncthreads();
+    if (threadIdx.x == 0)
+        pd = barrier_arrive<V>(b, c, round, blockIdx.x);
+}
+
+template <int V>
+__device__ __forceinline__ bool soft_wait(const Barrier &b, const Pending &pd, uint32_t round)
+{
+    int stop = 0;
+    if (threadIdx.x == 0)
+        stop = barrier_wait<V>(b, pd, round, blockIdx.x) ? 1 : 0;
     return __syncthreads_or(stop) != 0;
 }
 
@@ -505,12 +619,13 @@ __device__ __forceinline__ bool soft_barrier(const Barrier &b, EpochCursor &c, u
 // per-cluster counter (P = number of clusters) and waits; on a timeout it
 // writes the stop flag into every CTA of its cluster; second cluster barrier.
 // All threads of all CTAs of the cluster must call it.
+template <int V>
 __device__ __forceinline__ bool hard_barrier(const Barrier &b, EpochCursor &c, uint32_t round, int *s_flag)
 {
     __syncwarp();
     cluster_sync_all();
     if (threadIdx.x == 0 && cluster_ctarank() == 0) {
-        if (arrive_and_wait(b, c, round, blockIdx.x)) {
+        if (arrive_and_wait<V>(b, c, round, blockIdx.x)) {
             const uint32_t n = cluster_nctarank();
             for (uint32_t r = 0; r < n; ++r)
                 st_shared_cluster(s_flag, r, 1u);

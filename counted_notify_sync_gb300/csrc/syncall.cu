@@ -12,7 +12,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <cstdint>
+#include <utility>
 #include <cstring>
 
 #include "cns.h"
@@ -98,31 +100,51 @@ struct JacState {
     int *flag;         // shared: a wait in this sweep gave up
 };
 
-// Returns after the sweep; a bulk copy that never completes within the
-// barrier timeout is recorded as CNS_ERR_TIMEOUT (the round's barrier then
-// stops every participant).
-__device__ __forceinline__ void jacobi_phase(const float *src, float *dst, int64_t N, uint32_t p, uint32_t P,
-                                             JacState &js, uint32_t *status_line, uint64_t timeout_ns,
-                                             uint32_t round)
+// One output float4 column j of a sweep from its input v, the last float of
+// the column on its left (lw) and the first float on its right (rx).
+__device__ __forceinline__ float4 jacobi_column(const float4 v, float lw, float rx, int64_t j, int64_t N)
+{
+    float4 o;
+    o.x = (j == 0) ? v.x : (lw + v.y) * 0.5f;
+    o.y = (v.x + v.z) * 0.5f;
+    o.z = (v.y + v.w) * 0.5f;
+    o.w = (4 * j + 3 == N - 1) ? v.w : (v.z + rx) * 0.5f;
+    return o;
+}
+
+// Participant p's float4 columns [j0, j1): N/4 columns shared out as evenly as possible.
+__device__ __forceinline__ void jacobi_chunk(int64_t N4, uint32_t p, uint32_t P, int64_t *j0, int64_t *j1)
+{
+    const int64_t base = N4 / P, rem = N4 % P;
+    *j0 = static_cast<int64_t>(p) * base + (p < rem ? p : rem);
+    *j1 = *j0 + base + (p < rem ? 1 : 0);
+}
+
+// Sweep of columns [c0, c1) through shared memory.  The bulk copies read
+// columns clipped to [r0, r1): the whole field for a full sweep; only the
+// participant's own chunk for the interior of a split-phase sweep, which
+// then needs nothing another participant wrote.  Returns after the columns;
+// a bulk copy that never completes within the barrier timeout is recorded as
+// CNS_ERR_TIMEOUT (the round's barrier then stops every participant).
+__device__ __forceinline__ void jacobi_tiles(const float *src, float *dst, int64_t N, int64_t c0, int64_t c1,
+                                             int64_t r0, int64_t r1, JacState &js, uint32_t *status_line,
+                                             uint64_t timeout_ns, uint32_t round)
 {
     const int64_t N4 = N >> 2;
-    const int64_t base = N4 / P, rem = N4 % P;
-    const int64_t j0 = static_cast<int64_t>(p) * base + (p < rem ? p : rem);
-    const int64_t j1 = j0 + base + (p < rem ? 1 : 0);
-    const int64_t nT = (j1 - j0 + kJacTile - 1) / kJacTile;
+    const int64_t nT = (c1 > c0) ? (c1 - c0 + kJacTile - 1) / kJacTile : 0;
     const float4 *s4 = reinterpret_cast<const float4 *>(src);
     float4 *d4 = reinterpret_cast<float4 *>(dst);
     for (int64_t k = 0; k < nT; ++k) {
-        const int64_t o0 = j0 + k * kJacTile;
-        const int64_t o1 = (o0 + kJacTile < j1) ? o0 + kJacTile : j1;
+        const int64_t o0 = c0 + k * kJacTile;
+        const int64_t o1 = (o0 + kJacTile < c1) ? o0 + kJacTile : c1;
         if (threadIdx.x == 0) {
             // the stage was read by everyone (barrier below / previous round)
             // and src was written by generic stores: order both before the copy
             if (k == 0)
                 fence_proxy_async_global();
             fence_proxy_async_shared();
-            const int64_t lo = (o0 - 1 < 0) ? 0 : o0 - 1;
-            const int64_t hi = (o1 + 1 > N4) ? N4 : o1 + 1;
+            const int64_t lo = (o0 - 1 < r0) ? r0 : o0 - 1;
+            const int64_t hi = (o1 + 1 > r1) ? r1 : o1 + 1;
             const uint32_t bytes = static_cast<uint32_t>((hi - lo) * 16);
             mbar_arrive_expect_tx(js.bar, bytes);
             bulk_copy_g2s(js.stage + (lo - (o0 - 1)), s4 + lo, bytes, js.bar);
@@ -145,18 +167,12 @@ __device__ __forceinline__ void jacobi_phase(const float *src, float *dst, int64
         if (!ok)
             *js.flag = 1;
         js.parity ^= 1u;
-        const float4 *t = js.stage;
+        const float4 *t = js.stage;   // t[i] holds column o0 - 1 + i
         for (int64_t j = o0 + threadIdx.x; j < o1 && ok; j += blockDim.x) {
             const int i = static_cast<int>(j - o0) + 1;
-            const float4 v = t[i];
             const float lw = (j > 0) ? t[i - 1].w : 0.f;
             const float rx = (j + 1 < N4) ? t[i + 1].x : ((4 * j + 4 < N) ? src[4 * j + 4] : 0.f);
-            float4 o;
-            o.x = (j == 0) ? v.x : (lw + v.y) * 0.5f;
-            o.y = (v.x + v.z) * 0.5f;
-            o.z = (v.y + v.w) * 0.5f;
-            o.w = (4 * j + 3 == N - 1) ? v.w : (v.z + rx) * 0.5f;
-            d4[j] = o;
+            d4[j] = jacobi_column(t[i], lw, rx, j, N);
         }
         __syncthreads();   // everyone is done with the stage (and sees the flag)
         if (*js.flag) {
@@ -165,10 +181,49 @@ __device__ __forceinline__ void jacobi_phase(const float *src, float *dst, int64
             return;
         }
     }
+}
+
+// The scalar tail (N mod 4 points) belongs to the last participant.
+__device__ __forceinline__ void jacobi_tail(const float *src, float *dst, int64_t N, uint32_t p, uint32_t P)
+{
     if (p == P - 1) {
-        for (int64_t i = 4 * N4 + threadIdx.x; i < N; i += blockDim.x)
+        for (int64_t i = 4 * (N >> 2) + threadIdx.x; i < N; i += blockDim.x)
             dst[i] = (i == 0 || i == N - 1) ? src[i] : (src[i - 1] + src[i + 1]) * 0.5f;
     }
+}
+
+// One Jacobi sweep over participant p's chunk (fused barrier form).
+__device__ __forceinline__ void jacobi_phase(const float *src, float *dst, int64_t N, uint32_t p, uint32_t P,
+                                             JacState &js, uint32_t *status_line, uint64_t timeout_ns,
+                                             uint32_t round)
+{
+    int64_t j0, j1;
+    jacobi_chunk(N >> 2, p, P, &j0, &j1);
+    jacobi_tiles(src, dst, N, j0, j1, 0, N >> 2, js, status_line, timeout_ns, round);
+    if (*js.flag)
+        return;
+    jacobi_tail(src, dst, N, p, P);
+}
+
+// The part of a split-phase sweep that waits for the previous round's
+// barrier: the chunk's first and last column (they read the neighbours'
+// columns), straight from global memory, and the tail.
+__device__ __forceinline__ void jacobi_edges(const float *src, float *dst, int64_t N, uint32_t p, uint32_t P)
+{
+    const int64_t N4 = N >> 2;
+    int64_t j0, j1;
+    jacobi_chunk(N4, p, P, &j0, &j1);
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    if (threadIdx.x < 2 && j1 > j0) {
+        const int64_t j = (threadIdx.x == 0) ? j0 : j1 - 1;
+        if (threadIdx.x == 0 || j > j0) {
+            const float lw = (j > 0) ? s4[j - 1].w : 0.f;
+            const float rx = (j + 1 < N4) ? s4[j + 1].x : ((4 * j + 4 < N) ? src[4 * j + 4] : 0.f);
+            d4[j] = jacobi_column(s4[j], lw, rx, j, N);
+        }
+    }
+    jacobi_tail(src, dst, N, p, P);
 }
 
 template <int WL>
@@ -198,7 +253,7 @@ __device__ __forceinline__ uint32_t cta_role(const SyncallParams &p, uint32_t b)
     return p.core_type == CNS_AIC_ONLY ? 1u : 0u;
 }
 
-template <int MODE, int WL>
+template <int MODE, int WL, int V>
 __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
 {
     __shared__ int s_flag;
@@ -232,16 +287,47 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
     // the elected thread's copy of the barrier description (variant 5 turns
     // its counter pair into near / far for this SM)
     Barrier bar = p.bar;
-    if (bar.variant == kBvDieLocal && threadIdx.x == 0 && (MODE == CNS_SYNCALL_SOFT || cluster_ctarank() == 0))
+    if (V == kBvDieLocal && threadIdx.x == 0 && (MODE == CNS_SYNCALL_SOFT || cluster_ctarank() == 0))
         choose_near_copy(bar);
     EpochCursor cursor{0u, 0u, false};
     bool stop = false;
-    for (int64_t r = 0; r < p.rounds; ++r) {
-        data_phase<WL>(p, r, b, js);
-        stop = (MODE == CNS_SYNCALL_SOFT) ? soft_barrier(bar, cursor, static_cast<uint32_t>(r))
-                                          : hard_barrier(bar, cursor, static_cast<uint32_t>(r), &s_flag);
-        if (stop)
-            break;
+    if constexpr (MODE == CNS_SYNCALL_SOFT && WL == CNS_WL_JACOBI) {
+        // Split phase: a sweep's interior columns read only this chunk's own
+        // columns and overwrite only columns no neighbour reads, so they run
+        // between this CTA's arrival at the previous round's barrier and its
+        // wait; the chunk's first and last column (and the tail) follow the
+        // wait.  Same barriers, same arithmetic; the wait overlaps the sweep.
+        int64_t j0, j1;
+        jacobi_chunk(p.elems >> 2, b, p.P, &j0, &j1);
+        Pending pd{0u, true, false};
+        for (int64_t r = 0; r < p.rounds; ++r) {
+            const bool odd = (r & 1) != 0;
+            const float *src = static_cast<const float *>(odd ? p.buf1 : p.buf0);
+            float *dst = static_cast<float *>(odd ? p.buf0 : p.buf1);
+            if (r == 0) {
+                jacobi_phase(src, dst, p.elems, b, p.P, js, bar.status_line, bar.timeout_ns, 0u);
+            } else {
+                jacobi_tiles(src, dst, p.elems, j0 + 1, j1 - 1, j0, j1, js, bar.status_line, bar.timeout_ns,
+                             static_cast<uint32_t>(r));
+                stop = soft_wait<V>(bar, pd, static_cast<uint32_t>(r - 1));
+                if (stop)
+                    break;
+                jacobi_edges(src, dst, p.elems, b, p.P);
+            }
+            soft_arrive<V>(bar, cursor, static_cast<uint32_t>(r), pd);
+        }
+        if (!stop && p.rounds > 0)
+            stop = soft_wait<V>(bar, pd, static_cast<uint32_t>(p.rounds - 1));
+    } else {
+        for (int64_t r = 0; r < p.rounds; ++r) {
+            data_phase<WL>(p, r, b, js);
+            if constexpr (MODE == CNS_SYNCALL_SOFT)
+                stop = soft_barrier<V>(bar, cursor, static_cast<uint32_t>(r));
+            else
+                stop = hard_barrier<V>(bar, cursor, static_cast<uint32_t>(r), &s_flag);
+            if (stop)
+                break;
+        }
     }
     if (threadIdx.x == 0 && p.cta_status)
         p.cta_status[b] = static_cast<int32_t>((stop ? CNS_CTA_ABORTED : CNS_CTA_DONE) | (role << 8));
@@ -274,19 +360,24 @@ __global__ void workspace_init_kernel(uint32_t *ws, uint32_t n_words, uint32_t s
 
 using KernelFn = void (*)(const SyncallParams);
 
-static KernelFn pick_kernel(int mode, int wl)
+// One kernel per (mode, workload, barrier variant).
+template <int MODE, int WL, int... Vs>
+static constexpr std::array<KernelFn, sizeof...(Vs)> variants_of(std::integer_sequence<int, Vs...>)
 {
-    static const KernelFn soft[5] = {syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_EMPTY>,
-                                     syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_RING_AFFINE>,
-                                     syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_RING_ROTATE>,
-                                     syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_XORSHIFT>,
-                                     syncall_kernel<CNS_SYNCALL_SOFT, CNS_WL_JACOBI>};
-    static const KernelFn hard[5] = {syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_EMPTY>,
-                                     syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_RING_AFFINE>,
-                                     syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_RING_ROTATE>,
-                                     syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_XORSHIFT>,
-                                     syncall_kernel<CNS_SYNCALL_HARD, CNS_WL_JACOBI>};
-    return mode == CNS_SYNCALL_SOFT ? soft[wl] : hard[wl];
+    return {{syncall_kernel<MODE, WL, Vs>...}};
+}
+
+template <int MODE, int... WLs>
+static constexpr std::array<std::array<KernelFn, kBvCount>, sizeof...(WLs)> table_of(std::integer_sequence<int, WLs...>)
+{
+    return {{variants_of<MODE, WLs>(std::make_integer_sequence<int, kBvCount>{})...}};
+}
+
+static KernelFn pick_kernel(int mode, int wl, int variant)
+{
+    static constexpr auto soft = table_of<CNS_SYNCALL_SOFT>(std::make_integer_sequence<int, 5>{});
+    static constexpr auto hard = table_of<CNS_SYNCALL_HARD>(std::make_integer_sequence<int, 5>{});
+    return mode == CNS_SYNCALL_SOFT ? soft[wl][variant] : hard[wl][variant];
 }
 
 // Can `grid` CTAs (in clusters of C when C > 0) be resident at once?
@@ -439,7 +530,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     if (int rc = current_device(&dev))
         return rc;
     cudaStream_t s = to_stream(d->stream);
-    KernelFn k = pick_kernel(mode, d->workload);
+    KernelFn k = pick_kernel(mode, d->workload, d->barrier_variant);
     const size_t smem = d->workload == CNS_WL_JACOBI ? kJacSmemBytes : 0;
     bool ok = false;
     if (mode == CNS_SYNCALL_HARD && C == 0) {

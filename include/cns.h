@@ -110,8 +110,9 @@ typedef enum {
  * protocol with other arithmetic:
  *   COUNTER_ACQUIRE   poll the counter with acquire loads, every arrival
  *                     (the guide's form)
- *   LAST_SKIPS        acquire-release arrival; the arrival that itself reaches
- *                     the target does not poll; the others poll as above
+ *   LAST_SKIPS        the arrival that itself reaches the target does not poll
+ *                     (an acquire fence after its increment stands in for the
+ *                     poll's acquire); the others poll as above
  *   RELAXED_POLL      as LAST_SKIPS, polling with relaxed loads and one acquire
  *                     fence once released
  *   BACKOFF           as RELAXED_POLL, pausing 32 ns between polls
