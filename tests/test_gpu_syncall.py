@@ -206,6 +206,28 @@ def test_jacobi_small_bit_exact(cns, N, sweeps, ctas, threads):
     assert d.final_counter == fc
 
 
+@pytest.mark.parametrize("variant", [0, 1, 5, 6])
+@pytest.mark.parametrize("cols_per_cta,extra", [(0, 3), (1, 0), (1, 2), (2, 1), (3, 0), (2050, 3)])
+@pytest.mark.parametrize("sweeps", [1, 2, 7])
+def test_jacobi_split_phase_chunk_shapes(cns, variant, cols_per_cta, extra, sweeps):
+    """The soft Jacobi runs its sweeps split-phase (interior before the wait,
+    first/last column and tail after it): chunks of 0, 1, 2, 3 and >2 tiles of
+    float4 columns, with and without a scalar tail, for several variants."""
+    import torch
+    ctas = 37
+    N = 4 * (cols_per_cta * ctas + (5 if cols_per_cta == 0 else 0)) + extra
+    u0 = ci.jacobi_field(N, seed=cols_per_cta * 10 + extra)
+    b0 = to_dev_f32(u0)
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_JACOBI, ctas, b0, b1, sweeps, elems=N, threads=128, workspace=ws,
+                            variant=variant)
+    got = (b1 if sweeps & 1 else b0).cpu().numpy()
+    want, fc, orc = oracle.syncall_run_jacobi(u0, sweeps, ctas)
+    np.testing.assert_array_equal(got, want)
+    assert rc == 0 and d.device_status == 0
+
+
 def test_jacobi_hard_path(cns):
     u0 = ci.jacobi_field(200003)
     d, got = run_jacobi(cns, u0, 10, 64, mode=HARD)
