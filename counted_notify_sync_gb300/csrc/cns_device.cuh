@@ -615,23 +615,103 @@ __device__ __forceinline__ bool soft_wait(const Barrier &b, const Pending &pd, u
     return __syncthreads_or(stop) != 0;
 }
 
-// One hard barrier: cluster barrier; cluster rank 0 arrives on the
-// per-cluster counter (P = number of clusters) and waits; on a timeout it
-// writes the stop flag into every CTA of its cluster; second cluster barrier.
+// The epoch a follower tracks on the hard path: for variants 0-5 the
+// cursor (the target of the round just taken, and the next); for variant 6
+// the sense bit of the round just taken, kept in c.start.
+template <int V>
+__device__ __forceinline__ uint32_t predicted_epoch(const EpochCursor &c)
+{
+    if constexpr (V == kBvSenseFlip)
+        return c.start ^ 0x80000000u;   // each round flips the sense
+    else
+        return c.end;
+}
+
+template <int V>
+__device__ __forceinline__ void follow_epoch(EpochCursor &c, uint32_t epoch, const Epoch &e)
+{
+    if constexpr (V == kBvSenseFlip) {
+        c.start = epoch;
+        c.valid = true;
+    } else {
+        epoch_advance(c, epoch, e);
+    }
+}
+
+// One hard barrier.  Every CTA of the cluster takes a cluster barrier (its
+// writes reach the cluster); cluster rank 0 then arrives on the per-cluster
+// counter (P = number of clusters) and every CTA's elected thread waits on
+// the counter itself.
+//   The members need the round's epoch.  In the launch's first barrier the
+// leader arrives and waits alone and hands its epoch to the members through
+// their shared memory before a second cluster barrier; from then on each
+// member follows the epochs itself (each round's target is the last one plus
+// P), and the leader checks each arrival against the same prediction
+// (CNS_ERR_INVALID_VALUE if the count was moved by anyone else).
+//   A CTA that must stop (timeout, abort, error) writes the stop flag into
+// every CTA of its cluster and carries on to the next cluster barrier, after
+// which the whole cluster sees the flag and stops together: no member is left
+// waiting at a cluster barrier.  After its last round the kernel takes one
+// more cluster barrier for the same reason (hard_barrier_finish).
 // All threads of all CTAs of the cluster must call it.
 template <int V>
-__device__ __forceinline__ bool hard_barrier(const Barrier &b, EpochCursor &c, uint32_t round, int *s_flag)
+__device__ __forceinline__ bool hard_barrier(const Barrier &b, EpochCursor &c, uint32_t round, bool first,
+                                             int *s_flag, uint32_t *s_epoch)
 {
-    __syncwarp();
+    __syncwarp();   // the .aligned cluster barrier needs a converged warp
     cluster_sync_all();
-    if (threadIdx.x == 0 && cluster_ctarank() == 0) {
-        if (arrive_and_wait<V>(b, c, round, blockIdx.x)) {
-            const uint32_t n = cluster_nctarank();
-            for (uint32_t r = 0; r < n; ++r)
-                st_shared_cluster(s_flag, r, 1u);
+    const bool leader = cluster_ctarank() == 0;
+    const uint32_t n = cluster_nctarank();
+    if (first) {
+        if (threadIdx.x == 0 && leader) {
+            const Pending pd = barrier_arrive<V>(b, c, round, blockIdx.x);
+            const bool stop = barrier_wait<V>(b, pd, round, blockIdx.x);
+            if constexpr (V == kBvSenseFlip)
+                follow_epoch<V>(c, pd.target, b.e);
+            for (uint32_t m = 1; m < n; ++m)
+                st_shared_cluster(s_epoch, m, pd.target);
+            if (stop) {
+                for (uint32_t m = 0; m < n; ++m)
+                    st_shared_cluster(s_flag, m, 1u);
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();
+        if (threadIdx.x == 0 && !leader)
+            follow_epoch<V>(c, *reinterpret_cast<volatile uint32_t *>(s_epoch), b.e);
+        return *reinterpret_cast<volatile int *>(s_flag) != 0;
+    }
+    if (*reinterpret_cast<volatile int *>(s_flag) != 0)
+        return true;   // a CTA of the cluster stopped in the last round
+    if (threadIdx.x == 0) {
+        const uint32_t expect = predicted_epoch<V>(c);
+        Pending pd;
+        if (leader) {
+            pd = barrier_arrive<V>(b, c, round, blockIdx.x);
+            if constexpr (V == kBvSenseFlip)
+                follow_epoch<V>(c, pd.target, b.e);
+            if (!pd.stop && pd.target != expect) {
+                raise_status(b.status_line, static_cast<uint32_t>(CNS_ERR_INVALID_VALUE), round, blockIdx.x);
+                pd.stop = true;
+            }
+        } else {
+            pd = Pending{expect, false, false};
+            follow_epoch<V>(c, expect, b.e);
+        }
+        if (barrier_wait<V>(b, pd, round, blockIdx.x)) {
+            for (uint32_t m = 0; m < n; ++m)
+                st_shared_cluster(s_flag, m, 1u);
         }
     }
-    __syncwarp();   // the .aligned cluster barrier needs a converged warp
+    __syncthreads();   // the CTA leaves the barrier when its elected thread does
+    return false;
+}
+
+// After the last round: one more cluster barrier so that a stop raised in the
+// last round reaches the whole cluster.  Returns true if it did.
+__device__ __forceinline__ bool hard_barrier_finish(int *s_flag)
+{
+    __syncwarp();
     cluster_sync_all();
     return *reinterpret_cast<volatile int *>(s_flag) != 0;
 }

@@ -257,6 +257,7 @@ template <int MODE, int WL, int V>
 __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
 {
     __shared__ int s_flag;
+    __shared__ uint32_t s_epoch;   // hard path: the epoch the cluster leader hands on
     __shared__ __align__(8) uint64_t s_jac_bar;
     __shared__ int s_jac_flag;
     extern __shared__ float4 s_jac_stage[];   // JACOBI only: kJacSmemBytes
@@ -287,8 +288,8 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
     // the elected thread's copy of the barrier description (variant 5 turns
     // its counter pair into near / far for this SM)
     Barrier bar = p.bar;
-    if (V == kBvDieLocal && threadIdx.x == 0 && (MODE == CNS_SYNCALL_SOFT || cluster_ctarank() == 0))
-        choose_near_copy(bar);
+    if (V == kBvDieLocal && threadIdx.x == 0)
+        choose_near_copy(bar);   // every CTA polls its own near copy (hard path: the leader arrives on both)
     EpochCursor cursor{0u, 0u, false};
     bool stop = false;
     if constexpr (MODE == CNS_SYNCALL_SOFT && WL == CNS_WL_JACOBI) {
@@ -324,10 +325,12 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
             if constexpr (MODE == CNS_SYNCALL_SOFT)
                 stop = soft_barrier<V>(bar, cursor, static_cast<uint32_t>(r));
             else
-                stop = hard_barrier<V>(bar, cursor, static_cast<uint32_t>(r), &s_flag);
+                stop = hard_barrier<V>(bar, cursor, static_cast<uint32_t>(r), r == 0, &s_flag, &s_epoch);
             if (stop)
                 break;
         }
+        if constexpr (MODE == CNS_SYNCALL_HARD)
+            stop = hard_barrier_finish(&s_flag);
     }
     if (threadIdx.x == 0 && p.cta_status)
         p.cta_status[b] = static_cast<int32_t>((stop ? CNS_CTA_ABORTED : CNS_CTA_DONE) | (role << 8));

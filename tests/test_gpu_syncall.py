@@ -285,6 +285,36 @@ def test_unzeroed_workspace_times_out_and_context_survives(cns):
     np.testing.assert_array_equal(got, want)
 
 
+@pytest.mark.parametrize("variant", [0, 1, 4, 5])
+@pytest.mark.parametrize("rounds", [1, 3, 6])
+def test_hard_path_unzeroed_workspace_times_out(cns, variant, rounds):
+    """The hard path with a counter left at 1: the clusters' leaders fall into
+    different epochs and the bounded waits give up.  A CTA that stops takes its
+    whole cluster with it at the next cluster barrier, so the run ends (no CTA
+    is left at a cluster barrier) and reports the timeout."""
+    v0 = ci.ring_payload(3, 8, 4)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, rounds, start=1, timeout_ms=300,
+                              cluster_dim=4, check=False, variant=variant)
+    assert rc == cns.CNS_ERR_TIMEOUT and d.device_status == cns.CNS_ERR_TIMEOUT
+    assert ((st & 0xFF) == cns.CNS_CTA_ABORTED).any()
+    # CTAs of one cluster agree
+    assert len(set((st[:4] & 0xFF).tolist())) == 1 and len(set((st[4:] & 0xFF).tolist())) == 1
+
+
+def test_hard_path_long_run_with_many_clusters(cns):
+    """Members follow the epochs themselves after the first round: a long run on
+    37 clusters of 4 lands exactly where the oracle does, near the wrap too."""
+    P = 148
+    v0 = ci.ring_payload(11, P, 8)
+    Pc = 37
+    M = oracle.counter_modulus(Pc)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_XORSHIFT, P, v0, 5001, start=M - 7 * Pc, cluster_dim=4)
+    want, _ = expect_ring(oracle.WL_XORSHIFT, v0, 5001)
+    np.testing.assert_array_equal(got, want)
+    assert d.device_status == 0 and d.final_counter == (M - 7 * Pc + 5001 * Pc) % M
+    assert (st == cns.CNS_CTA_DONE).all()
+
+
 def test_grid_that_cannot_be_resident_is_refused(cns):
     import torch
     ws = cns.new_workspace()
