@@ -221,10 +221,14 @@ typedef struct {
  *               counter reaches it ([SYNCALL] §5.2).  The counter cycles
  *               through Z_M, M = P * floor(2^32 / P), so the epochs survive the
  *               32-bit wrap; for a power-of-two P this is the plain wrapping add.
- *               CNS_SYNCALL_HARD: a thread-block-cluster barrier, one arrival
- *               per cluster on the hard counter by cluster rank 0, then a
- *               second cluster barrier that releases the cluster (the two-level
- *               shape of the guide's MIX hard path, §5.1).
+ *               CNS_SYNCALL_HARD: a thread-block-cluster barrier, then one
+ *               arrival per cluster on the hard counter by cluster rank 0
+ *               (the two-level shape of the guide's MIX hard path, §5.1);
+ *               every CTA then waits on the hard counter itself.  In the
+ *               launch's first round the leader waits alone and hands the
+ *               epoch to its cluster behind a second cluster barrier; later
+ *               rounds take one cluster barrier.  A CTA that stops takes its
+ *               whole cluster with it at the next cluster barrier.
  *               Both paths wait as data->barrier_variant says.
  *   core_type   cns_core_type_t ([SYNCALL] §3.1)
  *   used_cores  participants; 0 = automatic: the CTAs launched for AIV/AIC-
