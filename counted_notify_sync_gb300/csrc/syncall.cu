@@ -537,7 +537,11 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     const size_t smem = d->workload == CNS_WL_JACOBI ? kJacSmemBytes : 0;
     bool ok = false;
     if (mode == CNS_SYNCALL_HARD && C == 0) {
-        for (int c : {4, 2, 1}) {
+        // clusters of 2 first: measured 1634-1663 ns/round on the 148-CTA ring
+        // against 1786-1819 for clusters of 4 (a cluster barrier waits for its
+        // slowest member's payload) and 1616-1648 for clusters of 1, which
+        // however costs ~80 ns more without a payload
+        for (int c : {2, 4, 1}) {
             if (grid % c != 0)
                 continue;
             if (int rc = fits(k, grid, threads, c, smem, s, dev, &ok))

@@ -181,7 +181,7 @@ typedef struct {
     int32_t launch_ctas;     /* (in) AIV/AIC-only: CTAs launched; MIX: AIC groups */
     int32_t threads;         /* (in) threads per CTA, multiple of 32, <= 1024; 0 = 256 */
     int32_t cluster_dim;     /* (in) HARD, AIV/AIC-only: CTAs per cluster (1..8); 0 = the
-                                largest of 4, 2, 1 that divides the grid and can be resident.
+                                first of 2, 4, 1 that divides the grid and can be resident.
                                 MIX always uses clusters of 1 + aiv_ratio. */
     void *buf0_dev;          /* (in) payload buffer 0 (round-0 input), 16-byte aligned */
     void *buf1_dev;          /* (in) payload buffer 1, same size */
