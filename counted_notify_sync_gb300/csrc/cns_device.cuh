@@ -137,6 +137,18 @@ __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -727,27 +739,25 @@ __device__ __forceinline__ bool cnt_record_valid(uint32_t mode)
 }
 
 // New count for a record (pure function; the caller checked the mode).
+// Written as selects, not a switch: the op-stream state machine applies a
+// different mode in every lane of a warp, and a switch there serialises the
+// lanes' paths.
 __device__ __forceinline__ uint32_t cnt_record_apply(uint32_t c, uint32_t mode, uint32_t v)
 {
-    switch (mode) {
-    case CNS_REC_SET: return v;
-    case CNS_REC_ADD: return c + v;
-    case CNS_REC_BIT_OR: return c | v;
-    default: return c & v;   // CNS_REC_BIT_AND
-    }
+    const uint32_t r = (mode == CNS_REC_ADD) ? c + v : v;   // SET
+    return (mode == CNS_REC_BIT_OR) ? (c | v) : (mode == CNS_REC_BIT_AND) ? (c & v) : r;
 }
 
 // Whether a wait with this mode/value is released at count c (mode checked
-// by the caller, <= 4).
+// by the caller, <= 4).  Selects, as above.
 __device__ __forceinline__ bool cnt_wait_released(uint32_t c, uint32_t mode, uint32_t v)
 {
-    switch (mode) {
-    case CNS_WAIT_LESS: return c < v;
-    case CNS_WAIT_EQUAL: return c == v;
-    case CNS_WAIT_BIGGER: return c > v;
-    case CNS_WAIT_BIGGER_OR_EQUAL: return c >= v;
-    default: return (c & v) == v;   // CNS_WAIT_EQUAL_WITH_BITMASK
-    }
+    const bool lt = c < v, eq = c == v, gt = c > v, mask = (c & v) == v;
+    return (mode == CNS_WAIT_LESS) ? lt
+         : (mode == CNS_WAIT_EQUAL) ? eq
+         : (mode == CNS_WAIT_BIGGER) ? gt
+         : (mode == CNS_WAIT_BIGGER_OR_EQUAL) ? (gt || eq)
+                                              : mask;   // CNS_WAIT_EQUAL_WITH_BITMASK
 }
 
 // A record as one device atomic with release semantics.  Usable from inside

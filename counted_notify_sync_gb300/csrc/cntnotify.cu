@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -194,20 +195,20 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 
 constexpr int kChunk = 16;
 
+// One op (kind, mode, value, is_clear) applied to count c.  Branch-free:
+// neighbouring lanes of a warp apply different kinds and modes, so every
+// candidate is computed and the right one selected.
 __device__ __forceinline__ uint32_t sm_apply(uint32_t c, const uint4 &op, uint32_t *outcome)
 {
-    if (op.x == 0u) {
-        if (cnt_record_valid(op.y)) {
-            *outcome = CNS_OUT_RECORD;
-            return cnt_record_apply(c, op.y, op.z);
-        }
-    } else if (op.x == 1u && op.y <= 4u) {
-        const bool rel = cnt_wait_released(c, op.y, op.z);
-        *outcome = rel ? CNS_OUT_WAIT_RELEASED : CNS_OUT_WAIT_HELD;
-        return (rel && op.w) ? 0u : c;
-    }
-    *outcome = CNS_OUT_INVALID;
-    return c;
+    const bool rec = op.x == 0u && cnt_record_valid(op.y);
+    const bool wait = op.x == 1u && op.y <= 4u;
+    const uint32_t after_rec = cnt_record_apply(c, op.y, op.z);
+    const bool rel = cnt_wait_released(c, op.y, op.z);
+    const uint32_t after_wait = (rel && op.w) ? 0u : c;
+    *outcome = rec ? static_cast<uint32_t>(CNS_OUT_RECORD)
+             : wait ? static_cast<uint32_t>(rel ? CNS_OUT_WAIT_RELEASED : CNS_OUT_WAIT_HELD)
+                    : static_cast<uint32_t>(CNS_OUT_INVALID);
+    return rec ? after_rec : wait ? after_wait : c;
 }
 
 __device__ __forceinline__ bool is_set_record(const uint4 &op) { return op.x == 0u && op.y == CNS_REC_SET; }
@@ -226,11 +227,25 @@ constexpr size_t kSmSmemBytes = static_cast<size_t>(kSmThreads) * kPad * (sizeof
 __device__ __forceinline__ int sm_slot(int i) { return (i / kChunk) * kPad + (i % kChunk); }
 
 // Load this CTA's ops into shared memory and mark every trace slot empty.
+// Each thread has all of its 16 loads in flight before it stores any of them
+// (a load-store loop would wait out 16 memory latencies in a row).
 __device__ __forceinline__ int sm_stage(const uint4 *ops, int64_t n, int64_t base, uint4 *s_ops, uint2 *s_tr)
 {
     const int cnt = (n - base < kCtaOps) ? static_cast<int>(n - base) : kCtaOps;
-    for (int i = threadIdx.x; i < cnt; i += kSmThreads)
-        s_ops[sm_slot(i)] = ops[base + i];
+    constexpr int kPerThread = kCtaOps / kSmThreads;
+    uint4 v[kPerThread];
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        const int i = threadIdx.x + j * kSmThreads;
+        if (i < cnt)
+            v[j] = __ldg(ops + base + i);
+    }
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+        const int i = threadIdx.x + j * kSmThreads;
+        if (i < cnt)
+            s_ops[sm_slot(i)] = v[j];
+    }
     for (int i = threadIdx.x; i < kCtaOps; i += kSmThreads)
         s_tr[sm_slot(i)] = make_uint2(0u, kNoEntry);
     __syncthreads();
@@ -351,7 +366,136 @@ __global__ void __launch_bounds__(kSmThreads) sm_prefix_kernel(const uint4 *ops,
     sm_flush(trace, base, cnt, s_tr);
 }
 
-// Shared-memory opt-in for both kernels, once per device.
+// Single pass, for a launch whose CTAs are all resident at once (a
+// cooperative launch).  Each CTA stages its 4096 ops and:
+//   A  every chunk with a SET traces from its first SET to its end;
+//   B  the thread of such a chunk carries its end count on through the
+//      following chunks up to the next SET; the chain that reaches the CTA's
+//      end publishes the CTA's end count (tagged with this call's tag) for
+//      the next CTA;
+//   C  thread 0 takes the previous CTA's end count (init for CTA 0), waiting
+//      on the device until it is published, and replays the ops in front of
+//      the CTA's first SET -- all of them if the CTA has none, in which case
+//      it publishes the CTA's end count itself.
+// A CTA with a SET publishes before it waits, so a CTA waits only as long as
+// a run of SET-free CTAs in front of it takes.  The tag makes the link words
+// need no initial content: a word holds (tag << 32) | count, and a word from
+// an earlier call carries an earlier tag.  The wait is bounded; if it runs out
+// (only a stalled GPU can make it), the CTA's leading entries get count 0 and
+// outcome CNS_OUT_INVALID.
+constexpr uint64_t kSmLinkTimeoutNs = 10ull * 1000000000ull;
+
+__device__ __forceinline__ void sm_publish(uint64_t *link, uint32_t tag, uint32_t c)
+{
+    st_release_gpu_u64(link, (static_cast<uint64_t>(tag) << 32) | c);
+}
+
+// Returns false if the wait ran out.
+__device__ __forceinline__ bool sm_take(const uint64_t *link, uint32_t tag, uint32_t *c)
+{
+    uint32_t spins = 0;
+    uint64_t deadline = 0;
+    for (;;) {
+        const uint64_t v = ld_acquire_gpu_u64(link);
+        if (static_cast<uint32_t>(v >> 32) == tag) {
+            *c = static_cast<uint32_t>(v);
+            return true;
+        }
+        if ((++spins & 63u) == 0u) {
+            const uint64_t now = globaltimer_ns();
+            if (deadline == 0)
+                deadline = now + kSmLinkTimeoutNs;
+            else if (now > deadline)
+                return false;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kSmThreads) sm_fused_kernel(const uint4 *ops, int64_t n, uint32_t init,
+                                                              uint2 *trace, uint64_t *link, uint32_t tag,
+                                                              uint32_t *final_count)
+{
+    extern __shared__ uint4 sm_smem[];
+    uint4 *s_ops = sm_smem;
+    uint2 *s_tr = reinterpret_cast<uint2 *>(sm_smem + kSmThreads * kPad);
+    __shared__ int s_first[kSmThreads];   // index of the chunk's first SET, -1 if none
+    __shared__ int s_first_chunk;         // first chunk of the CTA with a SET (kSmThreads if none)
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
+    if (threadIdx.x == 0)
+        s_first_chunk = kSmThreads;
+    const int cnt = sm_stage(ops, n, base, s_ops, s_tr);
+    const bool last_cta = base + cnt == n;
+    const int nchunks = (cnt + kChunk - 1) / kChunk;
+    const int k = threadIdx.x;
+    int first = -1;
+    uint32_t c = 0;
+    if (k < nchunks) {   // A
+        const int off = k * kPad;
+        const int m = (cnt - k * kChunk < kChunk) ? cnt - k * kChunk : kChunk;
+#pragma unroll
+        for (int q = kChunk - 1; q >= 0; --q)   // all 16 looks at once: the first SET wins
+            if (q < m && is_set_record(s_ops[off + q]))
+                first = q;
+        for (int q = (first < 0 ? m : first); q < m; ++q) {
+            uint32_t o;
+            c = sm_apply(c, s_ops[off + q], &o);
+            s_tr[off + q] = make_uint2(c, o);
+        }
+    }
+    s_first[k] = first;
+    if (first >= 0)
+        atomicMin(&s_first_chunk, k);
+    __syncthreads();
+    if (first >= 0) {   // B
+        int j = k + 1;
+        for (; j < nchunks; ++j) {
+            const int fj = s_first[j];
+            const int off = j * kPad;
+            const int m = fj >= 0 ? fj : ((cnt - j * kChunk < kChunk) ? cnt - j * kChunk : kChunk);
+            for (int q = 0; q < m; ++q) {
+                uint32_t o;
+                c = sm_apply(c, s_ops[off + q], &o);
+                s_tr[off + q] = make_uint2(c, o);
+            }
+            if (fj >= 0)
+                break;
+        }
+        if (j >= nchunks) {
+            sm_publish(link + blockIdx.x, tag, c);
+            if (last_cta)
+                *final_count = c;
+        }
+    }
+    if (k == 0) {   // C
+        const int fc = s_first_chunk;
+        const int lead = fc < nchunks ? fc * kChunk + s_first[fc] : cnt;
+        uint32_t cp = init;
+        const bool ok = blockIdx.x == 0 || sm_take(link + blockIdx.x - 1, tag, &cp);
+        for (int i = 0; i < lead; ++i) {
+            uint32_t o;
+            if (ok) {
+                cp = sm_apply(cp, s_ops[sm_slot(i)], &o);
+            } else {
+                cp = 0u;
+                o = CNS_OUT_INVALID;
+            }
+            s_tr[sm_slot(i)] = make_uint2(cp, o);
+        }
+        if (fc >= nchunks) {
+            sm_publish(link + blockIdx.x, tag, cp);
+            if (last_cta)
+                *final_count = cp;
+        }
+    }
+    sm_flush(trace, base, cnt, s_tr);
+}
+
+// CTAs of sm_fused_kernel that fit on each device at once (set by sm_prepare).
+static int64_t g_sm_fused_max_blocks[64];
+static std::atomic<uint32_t> g_sm_tag{0};
+
+// Shared-memory opt-in for the kernels and the fused kernel's co-residency
+// limit, once per device.
 static int sm_prepare(int device)
 {
     static std::mutex mu;
@@ -364,6 +508,13 @@ static int sm_prepare(int device)
                                       static_cast<int>(kSmSmemBytes)));
         CNS_CUDA(cudaFuncSetAttribute(sm_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmSmemBytes)));
+        CNS_CUDA(cudaFuncSetAttribute(sm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSmSmemBytes)));
+        int per_sm = 0;
+        CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sm_fused_kernel, kSmThreads, kSmSmemBytes));
+        int sms = 0;
+        CNS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
+        g_sm_fused_max_blocks[device] = static_cast<int64_t>(per_sm) * sms;
         done[device] = true;
     }
     return CNS_SUCCESS;
@@ -378,6 +529,27 @@ static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, u
     const int64_t blocks = (n + kCtaOps - 1) / kCtaOps;
     if (blocks > 0x7fffffff)
         return CNS_ERR_INVALID_VALUE;
+    if (blocks <= g_sm_fused_max_blocks[device] &&
+        static_cast<size_t>(blocks) * sizeof(uint64_t) <= cns_statemachine_scratch_bytes(n)) {
+        // one pass: every CTA resident at once, so a CTA waiting for the one
+        // before it always sees it finish
+        uint32_t tag = ++g_sm_tag;
+        if (tag == 0)
+            tag = ++g_sm_tag;
+        uint64_t *link = reinterpret_cast<uint64_t *>(summ);
+        const uint4 *a0 = ops;
+        int64_t a1 = n;
+        uint32_t a2 = init;
+        uint2 *a3 = trace;
+        uint64_t *a4 = link;
+        uint32_t a5 = tag;
+        uint32_t *a6 = final_dev;
+        void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5, &a6};
+        CNS_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(sm_fused_kernel),
+                                             dim3(static_cast<unsigned>(blocks)), dim3(kSmThreads), args,
+                                             kSmSmemBytes, s));
+        return CNS_SUCCESS;
+    }
     sm_suffix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, trace, summ, final_dev);
     CNS_CUDA(cudaGetLastError());
     sm_prefix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, init, trace, summ,
@@ -756,8 +928,9 @@ extern "C" int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, 
         CNS_CUDA(cudaGetLastError());
         return CNS_SUCCESS;
     }
-    // The suffix kernel writes every summary the prefix kernel reads, so
-    // whatever an earlier call left in the array never matters.
+    // Whatever an earlier call left in the array never matters: the suffix
+    // kernel writes every summary the prefix kernel reads, and the one-pass
+    // kernel's link words carry the tag of their call.
     return sm_launch(reinterpret_cast<const uint4 *>(ops_dev), n, init, reinterpret_cast<uint2 *>(trace_dev), summ,
                      final_dev, dev.device, s);
 }

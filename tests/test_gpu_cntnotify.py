@@ -210,6 +210,60 @@ def test_statemachine_without_any_set(cns):
     assert got_f == want_f
 
 
+def _fused_limit():
+    """Largest op count the one-pass kernel takes on this GPU: 2 CTAs of 4096 ops per SM."""
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count * 2 * 4096
+
+
+@pytest.mark.parametrize("where", ["at_limit", "over_limit", "three_million"])
+def test_statemachine_one_pass_and_two_pass_sizes(cns, where):
+    """Streams that the one-pass kernel takes (all CTAs resident) and streams
+    just over that, which take the two-launch path, both bit for bit."""
+    lim = _fused_limit()
+    n = {"at_limit": lim, "over_limit": lim + 1, "three_million": 3_000_000}[where]
+    ops = ci.notify_ops(n, seed=n % 1000)
+    got_t, got_f = run_sm(cns, ops, 7)
+    want_t, want_f = oracle.cnt_statemachine(ops, 7)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
+@pytest.mark.parametrize("gap", [1000, 9000, 70000])
+def test_statemachine_rare_sets(cns, gap):
+    """SET records only every `gap` ops: chains cross many CTAs (each CTA
+    without a SET waits for the one before it and replays all its ops)."""
+    ops = ci.notify_ops(400_000, seed=gap)
+    is_set = (ops[:, 0] == 0) & (ops[:, 1] == 0)
+    ops[is_set, 1] = 1                                   # every SET becomes an ADD ...
+    ops[::gap, 0] = 0                                    # ... except one every `gap` ops
+    ops[::gap, 1] = 0
+    got_t, got_f = run_sm(cns, ops, 11)
+    want_t, want_f = oracle.cnt_statemachine(ops, 11)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
+def test_statemachine_back_to_back_calls_reuse_scratch(cns):
+    """Consecutive calls on one scratch buffer: the one-pass kernel's link
+    words from the earlier call must not be taken by the later one."""
+    import torch
+    n = 200_000
+    scratch = torch.empty(cns.cns_statemachine_scratch_bytes(n) // 4 + 2, dtype=torch.int32, device="cuda")
+    for seed in (1, 2, 3):
+        ops = ci.notify_ops(n, seed=seed)
+        ops_d = to_dev_u32(ops)
+        trace = torch.empty((n, 2), dtype=torch.int32, device="cuda")
+        final = torch.empty(1, dtype=torch.int32, device="cuda")
+        rc = cns._native.lib().cns_statemachine_run(ops_d.data_ptr(), n, seed, trace.data_ptr(), final.data_ptr(),
+                                                    scratch.data_ptr(), scratch.numel() * 4, None)
+        assert rc == 0
+        torch.cuda.synchronize()
+        want_t, want_f = oracle.cnt_statemachine(ops, seed)
+        np.testing.assert_array_equal(trace.cpu().numpy().view(np.uint32), want_t)
+        assert int(final.cpu().numpy().view(np.uint32)[0]) == want_f
+
+
 def test_statemachine_all_sets_and_invalid_ops(cns):
     ops = ci.notify_ops(3000, seed=5)
     ops[::2, 0] = 0
