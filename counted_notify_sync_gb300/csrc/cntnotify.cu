@@ -769,6 +769,7 @@ extern "C" int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const c
     cns_cnt_notify_s *n = lookup(h);
     if (!n)
         return CNS_ERR_INVALID_HANDLE;
+    TraceRange tr("cntnotify_record", n->slot);
     if (!info)
         return CNS_ERR_NULL_PTR;
     if (!record_mode_ok(info->mode))
@@ -786,6 +787,7 @@ extern "C" int cntnotify_wait_with_timeout(cns_cnt_notify_t h, cns_stream_t stre
     cns_cnt_notify_s *n = lookup(h);
     if (!n)
         return CNS_ERR_INVALID_HANDLE;
+    TraceRange tr("cntnotify_wait_with_timeout", n->slot);
     if (!info)
         return CNS_ERR_NULL_PTR;
     if (info->mode < CNS_WAIT_LESS || info->mode > CNS_WAIT_EQUAL_WITH_BITMASK)
@@ -801,6 +803,7 @@ extern "C" int cntnotify_reset(cns_cnt_notify_t h, cns_stream_t stream)
     cns_cnt_notify_s *n = lookup(h);
     if (!n)
         return CNS_ERR_INVALID_HANDLE;
+    TraceRange tr("cntnotify_reset", n->slot);
     DeviceGuard g;
     if (int rc = g.set(n->device))
         return rc;
@@ -851,6 +854,7 @@ extern "C" int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t
                                     uint32_t *final_dev, void *scratch_dev, size_t scratch_bytes,
                                     cns_stream_t stream)
 {
+    TraceRange tr("cns_statemachine_run");
     if (n < 0)
         return CNS_ERR_INVALID_VALUE;
     if (!final_dev)
@@ -895,6 +899,7 @@ static uint2 *g_noalloc_scratch_addr[64];   // per device; filled on the first c
 extern "C" int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, uint32_t init, uint32_t *trace_dev,
                                             uint32_t *final_dev, cns_stream_t stream)
 {
+    TraceRange tr("cns_statemachine_run_noalloc");
     if (n < 0 || n > CNS_STATEMACHINE_NOALLOC_MAX_OPS)
         return CNS_ERR_INVALID_VALUE;
     if (!final_dev)
@@ -941,6 +946,7 @@ extern "C" int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, 
 
 extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
 {
+    TraceRange tr("cns_pipeline_run");
     if (!cfg)
         return CNS_ERR_NULL_PTR;
     cns_cnt_notify_s *done = lookup(cfg->done);

@@ -470,6 +470,7 @@ extern "C" int syncall_read_workspace(const void *ws_dev, cns_stream_t stream, u
 extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t aiv_ratio, int64_t rounds,
                            cns_syncall_data_t *d)
 {
+    TraceRange tr("syncall_run", static_cast<uint64_t>(rounds));
     // ---- argument checks (no CUDA call before these) ----
     if (!d)
         return CNS_ERR_NULL_PTR;
