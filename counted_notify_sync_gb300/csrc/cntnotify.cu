@@ -152,8 +152,8 @@ __global__ void cnt_wait_kernel(uint32_t *line, uint32_t mode, uint32_t v, uint3
     }
 }
 
-// Zero the count, the sticky status, the abort word and the pipeline's
-// finish counter of a notify line.
+// Zero the count, the sticky status, the abort word and the spare word of a
+// notify line.
 __global__ void cnt_clear_line_kernel(uint32_t *line)
 {
     if (threadIdx.x < 4)
@@ -565,7 +565,8 @@ __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
 // ---------------------------------------------------------------------------
 
 // Producer of one round.  Before touching the tiles every CTA waits, on the
-// device, until the consumer has released the previous round (ack >= round).
+// device, until every consumer CTA of the previous round has recorded its
+// ADD 1 on `ack` (ack >= round * consumer CTAs).
 // CTA b owns tiles b, b + grid, b + 2 grid, ...; all of its threads store
 // them, then, after the block barrier, lane j of warp 0 adds 1 to `done` for
 // the CTA's tile j (j < 32, then the next 32, ...).  Each of those is one
@@ -578,8 +579,9 @@ __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
 constexpr int kPipeProducerThreads = 256;
 
 __global__ void __launch_bounds__(kPipeProducerThreads, 8)
-    pipeline_producer_kernel(uint32_t *tiles, int64_t n_tiles, int tile_words, uint32_t round, uint32_t *done,
-                             uint32_t *ack, uint64_t timeout_ns, uint32_t *abort, uint64_t *started_at)
+    pipeline_producer_kernel(uint32_t *tiles, int64_t n_tiles, int tile_words, uint32_t round, uint32_t ack_target,
+                             uint32_t *done, uint32_t *ack, uint64_t timeout_ns, uint32_t *abort,
+                             uint64_t *started_at)
 {
     __shared__ int s_skip;
     if (threadIdx.x == 0) {
@@ -587,7 +589,9 @@ __global__ void __launch_bounds__(kPipeProducerThreads, 8)
         if (round != 0) {
             uint32_t spins = 0;
             uint64_t deadline = 0;
-            while (ld_acquire_gpu(ack) < round) {
+            // ack counts consumer CTAs (mod 2^32); it never runs more than one
+            // round's worth past the target, so the signed difference decides
+            while (static_cast<int32_t>(ld_acquire_gpu(ack) - ack_target) < 0) {
                 if ((++spins & 63u) == 0u) {
                     if (ld_relaxed_gpu(abort) != 0u) {
                         skip = 1;
@@ -633,17 +637,17 @@ __global__ void __launch_bounds__(kPipeProducerThreads, 8)
     }
 }
 
-// Consumer of one round: sums the tile area mod 2^32 into *checksum; the last
-// CTA to finish (counted on `finish`) records ack = ack_value, which lets the
-// next round's producer overwrite the tiles.
+// Consumer of one round: sums the tile area mod 2^32 into *checksum; each
+// CTA, once its reads are done, records ADD 1 on `ack` (release), and the
+// next round's producer waits for all of them.  One record per CTA, no
+// returning atomic: nobody has to find out which CTA finished last.
 // It is launched with programmatic stream serialization behind the wait, so
 // its CTAs may be scheduled while the wait still polls: they first wait on the
 // device until the wait kernel has ended.
 constexpr int kPipeConsumerThreads = 256;
 
 __global__ void __launch_bounds__(kPipeConsumerThreads, 8)
-    pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words, uint32_t *checksum, uint32_t *ack,
-                             uint32_t ack_value, uint32_t *finish)
+    pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words, uint32_t *checksum, uint32_t *ack)
 {
     grid_dependency_wait();
     const uint4 *t4 = reinterpret_cast<const uint4 *>(tiles);
@@ -667,15 +671,9 @@ __global__ void __launch_bounds__(kPipeConsumerThreads, 8)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             w += __shfl_xor_sync(0xffffffffu, w, o);
-        if (threadIdx.x == 0)
+        if (threadIdx.x == 0) {
             atomicAdd(checksum, w);
-    }
-    if (threadIdx.x == 0) {
-        // ... before it counts itself finished (release); the last CTA has
-        // acquired every other CTA's count when it releases the producer
-        if (atom_add_acq_rel_gpu(finish, 1u) == gridDim.x - 1u) {
-            atom_exch_relaxed_gpu(finish, 0u);
-            cnt_record_device(ack, CNS_REC_SET, ack_value);
+            cnt_record_device(ack, CNS_REC_ADD, 1u);   // ... before the CTA counts itself done (release)
         }
     }
 }
@@ -996,6 +994,7 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     ccfg.stream = sc;
     ccfg.attrs = early;
     ccfg.numAttrs = 1;
+    cfg->consumer_ctas = cgrid;   // ack grows by this much per round
 
     std::vector<cudaEvent_t> ev;
     auto cleanup = [&] {
@@ -1049,7 +1048,6 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
 
     cns_wait_info_t w_done = {CNS_WAIT_BIGGER_OR_EQUAL, static_cast<uint32_t>(cfg->tiles), cfg->timeout_s, 1, {0, 0, 0}};
     const uint64_t ack_timeout = wait_timeout_ns(cfg->timeout_s);
-    uint32_t *finish = ack->line + 3;
     for (int64_t r = 0; r < cfg->rounds && rc == CNS_SUCCESS; ++r) {
         // Submission order is a valid serial schedule: every wait (the
         // producer's device-side wait on ack, the stream wait on done) comes
@@ -1057,14 +1055,15 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
         // one hardware queue in submission order, and a wait ahead of its
         // record would then hold that record back until it timed out.
         pipeline_producer_kernel<<<pgrid, kPipeProducerThreads, 0, sp>>>(
-            cfg->tiles_dev, cfg->tiles, cfg->tile_words, static_cast<uint32_t>(r), done->line, ack->line, ack_timeout,
-            abort, stamps ? stamps + r : nullptr);
+            cfg->tiles_dev, cfg->tiles, cfg->tile_words, static_cast<uint32_t>(r),
+            static_cast<uint32_t>(r) * static_cast<uint32_t>(cgrid), done->line, ack->line, ack_timeout, abort,
+            stamps ? stamps + r : nullptr);
         check(cudaGetLastError(), "producer launch");
         if (int e = enqueue_wait(done, sc, &w_done, cfg->released_dev ? cfg->released_dev + r : nullptr, abort, true,
                                  stamps ? stamps + cfg->rounds + r : nullptr))
             rc = e;
         check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel, static_cast<const uint32_t *>(cfg->tiles_dev),
-                                 n_words, cfg->checksums_dev + r, ack->line, static_cast<uint32_t>(r + 1), finish),
+                                 n_words, cfg->checksums_dev + r, ack->line),
               "consumer launch");
     }
     check(cudaEventRecord(join, sc), "event");

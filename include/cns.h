@@ -442,7 +442,8 @@ int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, uint32_t in
  * waits BIGGER_OR_EQUAL N with isClear = 1 and then continues). */
 typedef struct {
     cns_cnt_notify_t done;   /* (in) producer -> consumer: ADD 1 per tile */
-    cns_cnt_notify_t ack;    /* (in) consumer -> producer: SET round+1 once a round is consumed */
+    cns_cnt_notify_t ack;    /* (in) consumer -> producer: ADD 1 per consumer CTA once it has read
+                                the round; a round is consumed at ack = (round+1) * consumer_ctas */
     uint32_t *tiles_dev;     /* (in) tiles * tile_words uint32 */
     uint32_t *checksums_dev; /* (in/out) uint32[rounds], zeroed by the call */
     uint32_t *released_dev;  /* (in/out, optional) uint32[rounds]: count seen at release */
@@ -461,27 +462,30 @@ typedef struct {
                                 the producer passing its wait for the previous round's
                                 release to the consumer-side wait releasing (device clock) */
     int32_t device_status;   /* (out, sync=1) 0 or CNS_ERR_TIMEOUT */
-    int32_t reserved[3];
+    int32_t consumer_ctas;   /* (out) consumer CTAs per round (ack's increment per round) */
+    int32_t reserved[2];
 } cns_pipeline_t;
 
 /*
  * cns_pipeline_run -- `rounds` rounds of a producer and a consumer on two
  * streams that meet only through two counted notifies.
  *   producer stream: a producer kernel whose CTAs first wait on the device
- *     until ack >= round (the consumer has finished reading the previous
- *     round), then write word w of the tile area as w * 2654435761 + round;
+ *     until ack >= round * consumer_ctas (every consumer CTA has finished
+ *     reading the previous round), then write word w of the tile area as
+ *     w * 2654435761 + round;
  *     CTA b writes tiles b, b + grid, ... and, once they are all stored,
  *     records ADD 1 on `done` from the device for each of them (one lane of
  *     one warp per tile, so the lanes' records travel as one L2 operation);
  *   consumer stream: cntnotify wait on `done` BIGGER_OR_EQUAL tiles with
  *     isClear = 1, then a consumer kernel that sums the tile area mod 2^32
- *     into checksums[round]; its last CTA to finish records ack = round + 1.
+ *     into checksums[round]; each of its CTAs records ADD 1 on `ack` once
+ *     its reads are done.
  *     The consumer is launched with programmatic stream serialization: its
  *     CTAs may be scheduled while the wait polls and wait on the device for
  *     it to end.  Grids are sized so that producer and consumer CTAs always
  *     fit on the GPU together (half and a quarter of its thread slots).
  * The call first clears both notifies (count and status); `done` ends at 0
- * and `ack` at `rounds`.  Once a wait times out the pipeline's remaining
+ * and `ack` at rounds * consumer_ctas (mod 2^32).  Once a wait times out the pipeline's remaining
  * waits return at once, so a lost signal costs one timeout, not one per round.
  * Errors: INVALID_HANDLE, NULL_PTR, INVALID_VALUE, CUDA; with sync=1 also
  * TIMEOUT.
