@@ -39,7 +39,8 @@ P_HEAD, SLOTS_HEAD, ROUNDS_HEAD = 148, 4, 100000
 WORKLOAD = ("soft SYNCALL, AIV-only, 148 CTAs x 256 threads (1 per SM), ring-rotate payload of 4 uint32 per CTA, "
             "100000 rounds per launch, counter zeroed at start")
 VARIANT_NAMES = ["counter_acquire", "last_skips", "relaxed_poll", "backoff", "flag_broadcast", "die_local",
-                 "sense_flip"]
+                 "sense_flip", "arrival_only"]
+ARRIVAL_ONLY = 7   # empty rounds only: the variant orders no data
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -50,7 +51,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-secondary", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--variant", type=int, default=0,
+    ap.add_argument("--variant", type=int, default=0, choices=range(7),
                     help="barrier variant of the headline (cns_barrier_variant_t); 0, the guide's counter poll, "
                          "measured fastest with the ring payload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
@@ -320,12 +321,17 @@ def secondary(cns, torch, peaks):
                       "cluster": d.cluster_used, "status": st}
 
     for v in range(len(VARIANT_NAMES)):
-        ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
-             label=f"soft_148_ring_rotate_variant{v}")
+        if v != ARRIVAL_ONLY:
+            ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
+                 label=f"soft_148_ring_rotate_variant{v}")
         ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_EMPTY, 148, 148, 0, 100000, variant=v,
              label=f"soft_148_empty_variant{v}")
-        ring(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
-             label=f"hard_148_ring_rotate_variant{v}")
+        if v != ARRIVAL_ONLY:
+            ring(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
+                 label=f"hard_148_ring_rotate_variant{v}")
+        else:
+            ring(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_EMPTY, 148, 148, 0, 100000, variant=v,
+                 label=f"hard_148_empty_variant{v}")
     ring(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000,
          label="hard_148_ring_rotate")
     ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_EMPTY, 148, 148, 0, 100000, label="soft_148_empty")

@@ -365,6 +365,10 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //      bit in the value its own addition returned.  Needs the count's low
 //      31 bits to be 0 when the run starts; an arrival that sees low bits no
 //      round of this scheme can produce stops the run (CNS_ERR_INVALID_VALUE).
+//   7  arrival only: the guide's bare contract (arrival, no visibility of
+//      other participants' writes): a relaxed increment and relaxed polls, no
+//      fence.  Only for rounds that exchange no data through memory (the host
+//      refuses it for workloads with a payload).
 //   5  die-local replicas: the counter is kept twice, 4 KB apart.  On GB300
 //      an atomic is performed in the L2 of the die that homes its line (about
 //      150 ns from that die's SMs, 350 ns from the other's), and consecutive
@@ -376,7 +380,7 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //      arrivals of every round, so each runs the same epoch arithmetic; which
 //      die homes which copy only changes the speed, never the result.
 enum : int { kBvCounterAcquire = 0, kBvLastSkips = 1, kBvRelaxedPoll = 2, kBvBackoff = 3, kBvFlag = 4,
-             kBvDieLocal = 5, kBvSenseFlip = 6, kBvCount = 7 };
+             kBvDieLocal = 5, kBvSenseFlip = 6, kBvArrivalOnly = 7, kBvCount = 8 };
 
 struct Barrier {
     uint32_t *ctr;          // arrival counter (variant 5: the near copy, once chosen)
@@ -391,18 +395,19 @@ struct Barrier {
 // Poll *word until `released(value)` holds.  Returns false when released,
 // true when the wait gave up (timeout here, or an abort raised by another
 // waiter).  The abort flag and the clock are looked at once every 64 polls.
-// With relaxed polls, one acquire fence follows the successful load.
+// With relaxed polls, one acquire fence follows the successful load (unless
+// acquire_after is false: arrival-only waits order nothing).
 template <class Released>
 __device__ __forceinline__ bool poll_until(const uint32_t *word, Released released, uint32_t *status_line,
                                            uint64_t timeout_ns, uint32_t round, uint32_t who, bool relaxed = false,
-                                           uint32_t pause_ns = 0)
+                                           uint32_t pause_ns = 0, bool acquire_after = true)
 {
     uint32_t spins = 0;
     uint64_t deadline = 0;
     for (;;) {
         const uint32_t cur = relaxed ? ld_relaxed_gpu(word) : ld_acquire_gpu(word);
         if (released(cur)) {
-            if (relaxed)
+            if (relaxed && acquire_after)
                 fence_acq_rel_gpu();
             return false;
         }
@@ -499,6 +504,9 @@ __device__ __forceinline__ Pending barrier_arrive(const Barrier &b, EpochCursor 
             red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             pd.target = epoch_target(before, b.e, c);
+        } else if constexpr (V == kBvArrivalOnly) {
+            const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
+            pd.target = epoch_target(before, b.e, c);
         } else {
             const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
             pd.target = epoch_target(before, b.e, c);
@@ -533,6 +541,9 @@ __device__ __forceinline__ bool barrier_wait(const Barrier &b, const Pending &pd
                           b.timeout_ns, round, who);
     } else if constexpr (V == kBvFlag) {
         return poll_epoch(b.flag, pd.target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
+    } else if constexpr (V == kBvArrivalOnly) {
+        return poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, pd.target, b.e); }, b.status_line,
+                          b.timeout_ns, round, who, true, 0, false);
     } else {
         constexpr bool relaxed = V == kBvRelaxedPoll || V == kBvBackoff;
         return poll_epoch(b.ctr, pd.target, b.e, b.status_line, b.timeout_ns, round, who, relaxed,
@@ -568,6 +579,11 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
             const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);
             stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who);
+        } else if constexpr (V == kBvArrivalOnly) {
+            const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
+            target = epoch_target(before, b.e, c);
+            stop = poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, target, b.e); }, b.status_line,
+                              b.timeout_ns, round, who, true, 0, false);
         } else {
             const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);

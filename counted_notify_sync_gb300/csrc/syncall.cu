@@ -480,7 +480,10 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return CNS_ERR_INVALID_VALUE;
     if (d->workload < CNS_WL_EMPTY || d->workload > CNS_WL_JACOBI)
         return CNS_ERR_INVALID_VALUE;
-    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_SENSE_FLIP)
+    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_ARRIVAL_ONLY)
+        return CNS_ERR_INVALID_VALUE;
+    // arrival only orders no data: refuse it where rounds exchange data
+    if (d->barrier_variant == CNS_BARRIER_ARRIVAL_ONLY && d->workload != CNS_WL_EMPTY)
         return CNS_ERR_INVALID_VALUE;
     if (d->workspace_bytes != 0 && d->workspace_bytes < CNS_SYNCALL_WORKSPACE_BYTES)
         return CNS_ERR_INVALID_VALUE;

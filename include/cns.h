@@ -140,7 +140,12 @@ typedef enum {
  *                     left by earlier runs of this variant); after R rounds the
  *                     count is start + R * 2^31 mod 2^32.  An arrival that sees
  *                     low bits no round of the scheme produces stops the run with
- *                     device status CNS_ERR_INVALID_VALUE. */
+ *                     device status CNS_ERR_INVALID_VALUE.
+ *   ARRIVAL_ONLY      the guide's bare contract ([SYNCALL] §6.1: the barrier
+ *                     guarantees arrival, not visibility of other cores' writes):
+ *                     a relaxed increment and relaxed polls, no fence.  Accepted
+ *                     only with CNS_WL_EMPTY; syncall_run refuses it
+ *                     (INVALID_VALUE) for workloads that exchange data. */
 typedef enum {
     CNS_BARRIER_COUNTER_ACQUIRE = 0,
     CNS_BARRIER_LAST_SKIPS = 1,
@@ -148,7 +153,8 @@ typedef enum {
     CNS_BARRIER_BACKOFF = 3,
     CNS_BARRIER_FLAG_BROADCAST = 4,
     CNS_BARRIER_DIE_LOCAL = 5,
-    CNS_BARRIER_SENSE_FLIP = 6
+    CNS_BARRIER_SENSE_FLIP = 6,
+    CNS_BARRIER_ARRIVAL_ONLY = 7
 } cns_barrier_variant_t;
 
 /* CTA status words written to cns_syncall_data_t.cta_status_dev (optional).
