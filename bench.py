@@ -39,8 +39,8 @@ P_HEAD, SLOTS_HEAD, ROUNDS_HEAD = 148, 4, 100000
 WORKLOAD = ("soft SYNCALL, AIV-only, 148 CTAs x 256 threads (1 per SM), ring-rotate payload of 4 uint32 per CTA, "
             "100000 rounds per launch, counter zeroed at start")
 VARIANT_NAMES = ["counter_acquire", "last_skips", "relaxed_poll", "backoff", "flag_broadcast", "die_local",
-                 "sense_flip", "arrival_only"]
-ARRIVAL_ONLY = 7   # empty rounds only: the variant orders no data
+                 "sense_flip", "arrival_only", "arrival_only_die_local"]
+ARRIVAL_ONLY = (7, 8)   # empty rounds only: these variants order no data
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -321,12 +321,12 @@ def secondary(cns, torch, peaks):
                       "cluster": d.cluster_used, "status": st}
 
     for v in range(len(VARIANT_NAMES)):
-        if v != ARRIVAL_ONLY:
+        if v not in ARRIVAL_ONLY:
             ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
                  label=f"soft_148_ring_rotate_variant{v}")
         ring(cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_EMPTY, 148, 148, 0, 100000, variant=v,
              label=f"soft_148_empty_variant{v}")
-        if v != ARRIVAL_ONLY:
+        if v not in ARRIVAL_ONLY:
             ring(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, 148, 148, 4, 100000, variant=v,
                  label=f"hard_148_ring_rotate_variant{v}")
         else:

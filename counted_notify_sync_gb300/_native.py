@@ -47,6 +47,7 @@ CNS_BARRIER_FLAG_BROADCAST = 4
 CNS_BARRIER_DIE_LOCAL = 5
 CNS_BARRIER_SENSE_FLIP = 6
 CNS_BARRIER_ARRIVAL_ONLY = 7
+CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL = 8
 CNS_SYNCALL_REPLICA_OFFSET = 4096
 CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES = 8192
 CNS_CTA_DONE = 1

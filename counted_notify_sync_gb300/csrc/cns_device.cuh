@@ -369,6 +369,8 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //      other participants' writes): a relaxed increment and relaxed polls, no
 //      fence.  Only for rounds that exchange no data through memory (the host
 //      refuses it for workloads with a payload).
+//   8  arrival only on die-local copies: 7's contract with 5's counters (a
+//      relaxed increment of each copy, relaxed polls of the near one).
 //   5  die-local replicas: the counter is kept twice, 4 KB apart.  On GB300
 //      an atomic is performed in the L2 of the die that homes its line (about
 //      150 ns from that die's SMs, 350 ns from the other's), and consecutive
@@ -380,7 +382,7 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //      arrivals of every round, so each runs the same epoch arithmetic; which
 //      die homes which copy only changes the speed, never the result.
 enum : int { kBvCounterAcquire = 0, kBvLastSkips = 1, kBvRelaxedPoll = 2, kBvBackoff = 3, kBvFlag = 4,
-             kBvDieLocal = 5, kBvSenseFlip = 6, kBvArrivalOnly = 7, kBvCount = 8 };
+             kBvDieLocal = 5, kBvSenseFlip = 6, kBvArrivalOnly = 7, kBvArrivalDieLocal = 8, kBvCount = 9 };
 
 struct Barrier {
     uint32_t *ctr;          // arrival counter (variant 5: the near copy, once chosen)
@@ -499,8 +501,9 @@ __device__ __forceinline__ Pending barrier_arrive(const Barrier &b, EpochCursor 
         return arrive_flip(b, round, who);
     } else {
         Pending pd{0u, false, false};
-        if constexpr (V == kBvDieLocal) {
-            fence_release_gpu();
+        if constexpr (V == kBvDieLocal || V == kBvArrivalDieLocal) {
+            if constexpr (V == kBvDieLocal)
+                fence_release_gpu();
             red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             pd.target = epoch_target(before, b.e, c);
@@ -541,7 +544,7 @@ __device__ __forceinline__ bool barrier_wait(const Barrier &b, const Pending &pd
                           b.timeout_ns, round, who);
     } else if constexpr (V == kBvFlag) {
         return poll_epoch(b.flag, pd.target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
-    } else if constexpr (V == kBvArrivalOnly) {
+    } else if constexpr (V == kBvArrivalOnly || V == kBvArrivalDieLocal) {
         return poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, pd.target, b.e); }, b.status_line,
                           b.timeout_ns, round, who, true, 0, false);
     } else {
@@ -575,6 +578,12 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);
             stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who);
+        } else if constexpr (V == kBvArrivalDieLocal) {
+            red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
+            const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
+            target = epoch_target(before, b.e, c);
+            stop = poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, target, b.e); }, b.status_line,
+                              b.timeout_ns, round, who, true, 0, false);
         } else if constexpr (V == kBvCounterAcquire) {
             const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);

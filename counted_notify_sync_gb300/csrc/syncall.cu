@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
     // the elected thread's copy of the barrier description (variant 5 turns
     // its counter pair into near / far for this SM)
     Barrier bar = p.bar;
-    if (V == kBvDieLocal && threadIdx.x == 0)
+    if ((V == kBvDieLocal || V == kBvArrivalDieLocal) && threadIdx.x == 0)
         choose_near_copy(bar);   // every CTA polls its own near copy (hard path: the leader arrives on both)
     EpochCursor cursor{0u, 0u, false};
     bool stop = false;
@@ -480,14 +480,17 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return CNS_ERR_INVALID_VALUE;
     if (d->workload < CNS_WL_EMPTY || d->workload > CNS_WL_JACOBI)
         return CNS_ERR_INVALID_VALUE;
-    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_ARRIVAL_ONLY)
+    if (d->barrier_variant < 0 || d->barrier_variant > CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL)
         return CNS_ERR_INVALID_VALUE;
     // arrival only orders no data: refuse it where rounds exchange data
-    if (d->barrier_variant == CNS_BARRIER_ARRIVAL_ONLY && d->workload != CNS_WL_EMPTY)
+    const bool arrival_only = d->barrier_variant == CNS_BARRIER_ARRIVAL_ONLY ||
+                              d->barrier_variant == CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL;
+    if (arrival_only && d->workload != CNS_WL_EMPTY)
         return CNS_ERR_INVALID_VALUE;
     if (d->workspace_bytes != 0 && d->workspace_bytes < CNS_SYNCALL_WORKSPACE_BYTES)
         return CNS_ERR_INVALID_VALUE;
-    if (d->barrier_variant == CNS_BARRIER_DIE_LOCAL && d->workspace_bytes < CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES)
+    if ((d->barrier_variant == CNS_BARRIER_DIE_LOCAL || d->barrier_variant == CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL) &&
+        d->workspace_bytes < CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES)
         return CNS_ERR_INVALID_VALUE;
     if (rounds < 0 || used_cores < 0 || aiv_ratio < 0 || d->launch_ctas <= 0 || d->elems < 0)
         return CNS_ERR_INVALID_VALUE;

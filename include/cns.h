@@ -145,7 +145,10 @@ typedef enum {
  *                     guarantees arrival, not visibility of other cores' writes):
  *                     a relaxed increment and relaxed polls, no fence.  Accepted
  *                     only with CNS_WL_EMPTY; syncall_run refuses it
- *                     (INVALID_VALUE) for workloads that exchange data. */
+ *                     (INVALID_VALUE) for workloads that exchange data.
+ *   ARRIVAL_ONLY_DIE_LOCAL  ARRIVAL_ONLY on DIE_LOCAL's two counter copies
+ *                     (relaxed increments of both, relaxed polls of the near
+ *                     one); same restriction, same workspace size as DIE_LOCAL. */
 typedef enum {
     CNS_BARRIER_COUNTER_ACQUIRE = 0,
     CNS_BARRIER_LAST_SKIPS = 1,
@@ -154,7 +157,8 @@ typedef enum {
     CNS_BARRIER_FLAG_BROADCAST = 4,
     CNS_BARRIER_DIE_LOCAL = 5,
     CNS_BARRIER_SENSE_FLIP = 6,
-    CNS_BARRIER_ARRIVAL_ONLY = 7
+    CNS_BARRIER_ARRIVAL_ONLY = 7,
+    CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL = 8
 } cns_barrier_variant_t;
 
 /* CTA status words written to cns_syncall_data_t.cta_status_dev (optional).

@@ -139,7 +139,7 @@ def test_syncall_argument_checks(built):
     d.threads, d.cluster_dim = 256, 3
     assert cns.syncall_run(0, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # 3 does not divide 8
     assert cns.syncall_run(0, cns.CNS_MIX, 0, 8, 1, d) == cns.CNS_ERR_INVALID_VALUE  # cluster of 9
-    d.cluster_dim, d.barrier_variant = 0, 8
+    d.cluster_dim, d.barrier_variant = 0, 9
     assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # barrier variant
     wl = d.workload
     d.barrier_variant, d.workload = cns.CNS_BARRIER_ARRIVAL_ONLY, cns.CNS_WL_RING_AFFINE

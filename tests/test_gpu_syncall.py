@@ -434,27 +434,30 @@ def test_sense_flip_rejects_a_foreign_count(cns, mode):
 
 # --- arrival-only variant (the guide's bare contract), empty rounds only -------------------
 
+@pytest.mark.parametrize("variant", [7, 8])
 @pytest.mark.parametrize("mode", [SOFT, HARD])
 @pytest.mark.parametrize("start_rounds", [(0, 10001), ("wrap", 500)])
-def test_arrival_only_empty_rounds(cns, mode, start_rounds):
+def test_arrival_only_empty_rounds(cns, mode, start_rounds, variant):
     import torch
     start, R = start_rounds
     P = 148
     Pc = P if mode == SOFT else None
     ws = cns.new_workspace()
-    d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_EMPTY, P, None, None, 1, workspace=ws, variant=7)
+    d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_EMPTY, P, None, None, 1, workspace=ws, variant=variant)
     Pc = P if mode == SOFT else P // d.cluster_used
     M = oracle.counter_modulus(Pc)
     s0 = 0 if start == 0 else M - 3 * Pc
     ws = cns.new_workspace(start_value=s0)
     status = torch.zeros(P, dtype=torch.int32, device="cuda")
-    d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_EMPTY, P, None, None, R, workspace=ws, cta_status=status, variant=7)
+    d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_EMPTY, P, None, None, R, workspace=ws, cta_status=status,
+                            variant=variant)
     assert rc == 0 and d.device_status == 0
     assert d.final_counter == (s0 + R * Pc) % M
     assert (status.cpu().numpy() == cns.CNS_CTA_DONE).all()
 
 
-def test_arrival_only_refused_with_a_payload(cns):
+@pytest.mark.parametrize("variant", [7, 8])
+def test_arrival_only_refused_with_a_payload(cns, variant):
     v0 = ci.ring_payload(3, 8, 4)
-    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, 3, check=False, variant=7)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, 3, check=False, variant=variant)
     assert rc == cns.CNS_ERR_INVALID_VALUE
