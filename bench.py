@@ -435,6 +435,23 @@ def secondary(cns, torch, peaks):
     return out
 
 
+def barrier_context(sec, rtt_mean, far):
+    """The empty-round barrier in its two contracts, against the same round trips: with the release and
+    acquire that data rounds need (variant 0), and arrival only as the pages define SYNCALL (variant 8,
+    on die-local counter copies)."""
+    out = {}
+    far_mean = statistics.mean(far) if far else None
+    for key, label in (("soft_148_empty_variant0", "empty_release_acquire"),
+                       ("soft_148_empty_variant8", "empty_arrival_only_die_local")):
+        v = sec.get(key, {}).get("ns_per_round")
+        if v:
+            out[label + "_ns"] = v
+            out[label + "_over_mean_rtt"] = round(v / rtt_mean, 3)
+            if far_mean:
+                out[label + "_over_far_die_rtt"] = round(v / far_mean, 3)
+    return out
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -518,7 +535,8 @@ def run_native(args):
                                 "atom_min": round(rtt_min, 1),
                                 "atom_max": round(rtt_max, 1), "arrive_poll_pair_median": round(pair_med, 1),
                                 "ld_relaxed_median": round(ld_med, 1)},
-                     "ns_per_round_over_rtt": round(ns_round / rtt_mean, 3)},
+                     "ns_per_round_over_rtt": round(ns_round / rtt_mean, 3),
+                     "context": barrier_context(sec, rtt_mean, far)},
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,
