@@ -25,24 +25,10 @@ __device__ __forceinline__ uint32_t atom_inc_release_gpu(uint32_t *p, uint32_t b
     return old;
 }
 
-__device__ __forceinline__ uint32_t atom_inc_acq_rel_gpu(uint32_t *p, uint32_t bound)
-{
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound) : "memory");
-    return old;
-}
-
 __device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v)
 {
     uint32_t old;
     asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
 
