@@ -461,3 +461,21 @@ def test_arrival_only_refused_with_a_payload(cns, variant):
     v0 = ci.ring_payload(3, 8, 4)
     d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, 3, check=False, variant=variant)
     assert rc == cns.CNS_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_jacobi_unzeroed_workspace_times_out(cns, mode):
+    """Jacobi sweeps (split phase on the soft path, fused on the hard path)
+    with the counter left at 1: the bounded waits end the run with a timeout,
+    and the device keeps working."""
+    import torch
+    u0 = ci.jacobi_field(100003, seed=5)
+    b0 = to_dev_f32(u0)
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace(start_value=1)
+    d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_JACOBI, 16, b0, b1, 6, elems=u0.size, workspace=ws,
+                            timeout_ms=300, check=False, cluster_dim=4 if mode == HARD else 0)
+    assert rc == cns.CNS_ERR_TIMEOUT and d.device_status == cns.CNS_ERR_TIMEOUT
+    d, got = run_jacobi(cns, u0, 4, 16, mode=mode)
+    want, _, _ = oracle.syncall_run_jacobi(u0, 4, 16)
+    np.testing.assert_array_equal(got, want)
