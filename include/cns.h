@@ -128,7 +128,12 @@ typedef enum {
  *                     near copy (whose old value gives the target); it then polls
  *                     the near copy.  Each copy counts every arrival, so each
  *                     runs the same epoch arithmetic.  Needs a workspace of
- *                     CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES.
+ *                     CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES.  Each copy sees
+ *                     the arrivals in its own order, so a count that does not
+ *                     start at a multiple of P (a workspace reused across runs
+ *                     with different P without re-initialising it) can release
+ *                     participants early rather than time out: re-initialise
+ *                     the workspace whenever P changes.
  *   SENSE_FLIP        not the guide's arithmetic (the scheme of the CUDA
  *                     runtime's grid barrier, for comparison): participant 0
  *                     (CTA 0) adds 2^31 - (P - 1) and every other participant 1,

@@ -285,13 +285,15 @@ def test_unzeroed_workspace_times_out_and_context_survives(cns):
     np.testing.assert_array_equal(got, want)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 4, 5])
+@pytest.mark.parametrize("variant", [0, 1, 4])
 @pytest.mark.parametrize("rounds", [1, 3, 6])
 def test_hard_path_unzeroed_workspace_times_out(cns, variant, rounds):
     """The hard path with a counter left at 1: the clusters' leaders fall into
     different epochs and the bounded waits give up.  A CTA that stops takes its
     whole cluster with it at the next cluster barrier, so the run ends (no CTA
-    is left at a cluster barrier) and reports the timeout."""
+    is left at a cluster barrier) and reports the timeout.  (Not the die-local
+    variant: each copy sees the arrivals in its own order, so a misaligned
+    start need not put anyone in a later epoch there.)"""
     v0 = ci.ring_payload(3, 8, 4)
     d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, rounds, start=1, timeout_ms=300,
                               cluster_dim=4, check=False, variant=variant)
