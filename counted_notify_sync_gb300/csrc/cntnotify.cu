@@ -195,20 +195,39 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 
 constexpr int kChunk = 16;
 
-// One op (kind, mode, value, is_clear) applied to count c.  Branch-free:
-// neighbouring lanes of a warp apply different kinds and modes, so every
-// candidate is computed and the right one selected.
-__device__ __forceinline__ uint32_t sm_apply(uint32_t c, const uint4 &op, uint32_t *outcome)
+// An op packed into 8 bytes: x = value, y = kind code (0 record, 1 wait,
+// 2 anything else) | mode (clamped to 7, which no kind accepts) << 2 |
+// is_clear << 5.  Nothing the rules look at is lost.
+__device__ __forceinline__ uint2 sm_pack(const uint4 &op)
 {
-    const bool rec = op.x == 0u && cnt_record_valid(op.y);
-    const bool wait = op.x == 1u && op.y <= 4u;
-    const uint32_t after_rec = cnt_record_apply(c, op.y, op.z);
-    const bool rel = cnt_wait_released(c, op.y, op.z);
-    const uint32_t after_wait = (rel && op.w) ? 0u : c;
+    const uint32_t kind = op.x == 0u ? 0u : (op.x == 1u ? 1u : 2u);
+    const uint32_t mode = op.y < 7u ? op.y : 7u;
+    return make_uint2(op.z, kind | (mode << 2) | ((op.w != 0u ? 1u : 0u) << 5));
+}
+
+// One packed op applied to count c.  Branch-free: neighbouring lanes of a
+// warp apply different kinds and modes, so every candidate is computed and
+// the right one selected.
+__device__ __forceinline__ uint32_t sm_apply_packed(uint32_t c, const uint2 op, uint32_t *outcome)
+{
+    const uint32_t kind = op.y & 3u, mode = (op.y >> 2) & 7u, v = op.x;
+    const bool clear = ((op.y >> 5) & 1u) != 0u;
+    const bool rec = kind == 0u && cnt_record_valid(mode);
+    const bool wait = kind == 1u && mode <= 4u;
+    const uint32_t after_rec = cnt_record_apply(c, mode, v);
+    const bool rel = cnt_wait_released(c, mode, v);
+    const uint32_t after_wait = (rel && clear) ? 0u : c;
     *outcome = rec ? static_cast<uint32_t>(CNS_OUT_RECORD)
              : wait ? static_cast<uint32_t>(rel ? CNS_OUT_WAIT_RELEASED : CNS_OUT_WAIT_HELD)
                     : static_cast<uint32_t>(CNS_OUT_INVALID);
     return rec ? after_rec : wait ? after_wait : c;
+}
+
+__device__ __forceinline__ bool is_set_packed(const uint2 op) { return (op.y & 0x1Fu) == 0u; }   // record, SET
+
+__device__ __forceinline__ uint32_t sm_apply(uint32_t c, const uint4 &op, uint32_t *outcome)
+{
+    return sm_apply_packed(c, sm_pack(op), outcome);
 }
 
 __device__ __forceinline__ bool is_set_record(const uint4 &op) { return op.x == 0u && op.y == CNS_REC_SET; }
@@ -411,50 +430,78 @@ __device__ __forceinline__ bool sm_take(const uint64_t *link, uint32_t tag, uint
     }
 }
 
-__global__ void __launch_bounds__(kSmThreads) sm_fused_kernel(const uint4 *ops, int64_t n, uint32_t init,
-                                                              uint2 *trace, uint64_t *link, uint32_t tag,
-                                                              uint32_t *final_count)
+// Shape of the one-pass kernel: 512 threads, chunks of 8 ops (the same 4096
+// ops per CTA), ops packed to 8 bytes in shared memory.  Twice the warps of
+// the two-launch kernels, and per-thread walks half as long.
+constexpr int kFChunk = 8;
+constexpr int kFThreads = 512;
+constexpr int kFPad = kFChunk + 1;   // with 8-byte entries: conflict-free per-thread walks
+static_assert(kFChunk * kFThreads == kCtaOps, "one-pass CTAs hold as many ops as the two-launch ones");
+constexpr size_t kFSmemBytes = static_cast<size_t>(kFThreads) * kFPad * 2 * sizeof(uint2);
+
+__device__ __forceinline__ int f_slot(int i) { return (i / kFChunk) * kFPad + (i % kFChunk); }
+
+__global__ void __launch_bounds__(kFThreads, 2) sm_fused_kernel(const uint4 *ops, int64_t n, uint32_t init,
+                                                                uint2 *trace, uint64_t *link, uint32_t tag,
+                                                                uint32_t *final_count)
 {
-    extern __shared__ uint4 sm_smem[];
-    uint4 *s_ops = sm_smem;
-    uint2 *s_tr = reinterpret_cast<uint2 *>(sm_smem + kSmThreads * kPad);
-    __shared__ int s_first[kSmThreads];   // index of the chunk's first SET, -1 if none
-    __shared__ int s_first_chunk;         // first chunk of the CTA with a SET (kSmThreads if none)
+    extern __shared__ uint2 f_smem[];
+    uint2 *s_ops = f_smem;
+    uint2 *s_tr = f_smem + kFThreads * kFPad;
+    __shared__ int s_first[kFThreads];   // index of the chunk's first SET, -1 if none
+    __shared__ int s_wmin[kFThreads / 32];
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
-    if (threadIdx.x == 0)
-        s_first_chunk = kSmThreads;
-    const int cnt = sm_stage(ops, n, base, s_ops, s_tr);
+    const int cnt = (n - base < kCtaOps) ? static_cast<int>(n - base) : kCtaOps;
+    {   // stage: all 8 loads of a thread in flight, packed on the way in
+        uint2 v[kFChunk];
+#pragma unroll
+        for (int j = 0; j < kFChunk; ++j) {
+            const int i = threadIdx.x + j * kFThreads;
+            if (i < cnt)
+                v[j] = sm_pack(__ldg(ops + base + i));
+        }
+#pragma unroll
+        for (int j = 0; j < kFChunk; ++j) {
+            const int i = threadIdx.x + j * kFThreads;
+            if (i < cnt)
+                s_ops[f_slot(i)] = v[j];
+        }
+    }
+    __syncthreads();
     const bool last_cta = base + cnt == n;
-    const int nchunks = (cnt + kChunk - 1) / kChunk;
+    const int nchunks = (cnt + kFChunk - 1) / kFChunk;
     const int k = threadIdx.x;
     int first = -1;
     uint32_t c = 0;
     if (k < nchunks) {   // A
-        const int off = k * kPad;
-        const int m = (cnt - k * kChunk < kChunk) ? cnt - k * kChunk : kChunk;
+        const int off = k * kFPad;
+        const int m = (cnt - k * kFChunk < kFChunk) ? cnt - k * kFChunk : kFChunk;
 #pragma unroll
-        for (int q = kChunk - 1; q >= 0; --q)   // all 16 looks at once: the first SET wins
-            if (q < m && is_set_record(s_ops[off + q]))
+        for (int q = kFChunk - 1; q >= 0; --q)   // all looks at once: the first SET wins
+            if (q < m && is_set_packed(s_ops[off + q]))
                 first = q;
         for (int q = (first < 0 ? m : first); q < m; ++q) {
             uint32_t o;
-            c = sm_apply(c, s_ops[off + q], &o);
+            c = sm_apply_packed(c, s_ops[off + q], &o);
             s_tr[off + q] = make_uint2(c, o);
         }
     }
     s_first[k] = first;
-    if (first >= 0)
-        atomicMin(&s_first_chunk, k);
+    {   // the CTA's first chunk with a SET: a ballot per warp, then the warps' minimum
+        const uint32_t has = __ballot_sync(0xffffffffu, first >= 0);
+        if ((k & 31) == 0)
+            s_wmin[k >> 5] = has ? (k & ~31) + __ffs(has) - 1 : kFThreads;
+    }
     __syncthreads();
     if (first >= 0) {   // B
         int j = k + 1;
         for (; j < nchunks; ++j) {
             const int fj = s_first[j];
-            const int off = j * kPad;
-            const int m = fj >= 0 ? fj : ((cnt - j * kChunk < kChunk) ? cnt - j * kChunk : kChunk);
+            const int off = j * kFPad;
+            const int m = fj >= 0 ? fj : ((cnt - j * kFChunk < kFChunk) ? cnt - j * kFChunk : kFChunk);
             for (int q = 0; q < m; ++q) {
                 uint32_t o;
-                c = sm_apply(c, s_ops[off + q], &o);
+                c = sm_apply_packed(c, s_ops[off + q], &o);
                 s_tr[off + q] = make_uint2(c, o);
             }
             if (fj >= 0)
@@ -467,19 +514,21 @@ __global__ void __launch_bounds__(kSmThreads) sm_fused_kernel(const uint4 *ops, 
         }
     }
     if (k == 0) {   // C
-        const int fc = s_first_chunk;
-        const int lead = fc < nchunks ? fc * kChunk + s_first[fc] : cnt;
+        int fc = kFThreads;
+        for (int w = 0; w < kFThreads / 32; ++w)
+            fc = s_wmin[w] < fc ? s_wmin[w] : fc;
+        const int lead = fc < nchunks ? fc * kFChunk + s_first[fc] : cnt;
         uint32_t cp = init;
         const bool ok = blockIdx.x == 0 || sm_take(link + blockIdx.x - 1, tag, &cp);
         for (int i = 0; i < lead; ++i) {
             uint32_t o;
             if (ok) {
-                cp = sm_apply(cp, s_ops[sm_slot(i)], &o);
+                cp = sm_apply_packed(cp, s_ops[f_slot(i)], &o);
             } else {
                 cp = 0u;
                 o = CNS_OUT_INVALID;
             }
-            s_tr[sm_slot(i)] = make_uint2(cp, o);
+            s_tr[f_slot(i)] = make_uint2(cp, o);
         }
         if (fc >= nchunks) {
             sm_publish(link + blockIdx.x, tag, cp);
@@ -487,7 +536,9 @@ __global__ void __launch_bounds__(kSmThreads) sm_fused_kernel(const uint4 *ops, 
                 *final_count = cp;
         }
     }
-    sm_flush(trace, base, cnt, s_tr);
+    __syncthreads();
+    for (int i = threadIdx.x; i < cnt; i += kFThreads)   // every entry was written once
+        trace[base + i] = s_tr[f_slot(i)];
 }
 
 // CTAs of sm_fused_kernel that fit on each device at once (set by sm_prepare).
@@ -509,9 +560,9 @@ static int sm_prepare(int device)
         CNS_CUDA(cudaFuncSetAttribute(sm_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmSmemBytes)));
         CNS_CUDA(cudaFuncSetAttribute(sm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kSmSmemBytes)));
+                                      static_cast<int>(kFSmemBytes)));
         int per_sm = 0;
-        CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sm_fused_kernel, kSmThreads, kSmSmemBytes));
+        CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sm_fused_kernel, kFThreads, kFSmemBytes));
         int sms = 0;
         CNS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
         g_sm_fused_max_blocks[device] = static_cast<int64_t>(per_sm) * sms;
@@ -546,8 +597,8 @@ static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, u
         uint32_t *a6 = final_dev;
         void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5, &a6};
         CNS_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(sm_fused_kernel),
-                                             dim3(static_cast<unsigned>(blocks)), dim3(kSmThreads), args,
-                                             kSmSmemBytes, s));
+                                             dim3(static_cast<unsigned>(blocks)), dim3(kFThreads), args,
+                                             kFSmemBytes, s));
         return CNS_SUCCESS;
     }
     sm_suffix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, trace, summ, final_dev);
