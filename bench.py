@@ -51,9 +51,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-secondary", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--variant", type=int, default=0, choices=range(7),
-                    help="barrier variant of the headline (cns_barrier_variant_t); 0, the guide's counter poll, "
-                         "measured fastest with the ring payload")
+    ap.add_argument("--variant", type=int, default=2, choices=range(7),
+                    help="barrier variant of the headline (cns_barrier_variant_t); 2, the pages' arithmetic with "
+                         "relaxed polls and one acquire fence (the last arrival skips its poll), measured fastest "
+                         "with the ring payload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="run one small launch pattern for a profiler capture and exit")
@@ -304,7 +305,7 @@ def timed_run(torch, fn):
 def secondary(cns, torch, peaks):
     out = {}
 
-    def ring(mode, core, wl, ctas, P, slots, R, ratio=0, used=0, label="", variant=0):
+    def ring(mode, core, wl, ctas, P, slots, R, ratio=0, used=0, label="", variant=2):
         v0 = ci.ring_payload(1, P, slots)
         b0 = torch.from_numpy(v0.view(np.int32).copy()).cuda() if v0.size else None
         b1 = torch.zeros_like(b0) if v0.size else None
@@ -437,11 +438,11 @@ def secondary(cns, torch, peaks):
 
 def barrier_context(sec, rtt_mean, far):
     """The empty-round barrier in its two contracts, against the same round trips: with the release and
-    acquire that data rounds need (variant 0), and arrival only as the pages define SYNCALL (variant 8,
+    acquire that data rounds need (variant 2), and arrival only as the pages define SYNCALL (variant 8,
     on die-local counter copies)."""
     out = {}
     far_mean = statistics.mean(far) if far else None
-    for key, label in (("soft_148_empty_variant0", "empty_release_acquire"),
+    for key, label in (("soft_148_empty_variant2", "empty_release_acquire"),
                        ("soft_148_empty_variant8", "empty_arrival_only_die_local")):
         v = sec.get(key, {}).get("ns_per_round")
         if v:

@@ -396,7 +396,7 @@ __device__ __forceinline__ bool poll_until(const uint32_t *word, Released releas
         const uint32_t cur = relaxed ? ld_relaxed_gpu(word) : ld_acquire_gpu(word);
         if (released(cur)) {
             if (relaxed && acquire_after)
-                fence_acq_rel_gpu();
+                fence_acquire_gpu();   // the relaxed load that saw the release becomes an acquire
             return false;
         }
         if (pause_ns)
@@ -527,14 +527,14 @@ __device__ __forceinline__ bool barrier_wait(const Barrier &b, const Pending &pd
     if constexpr (V == kBvSenseFlip) {
         const uint32_t sense = pd.target;
         return poll_until(b.ctr, [&](uint32_t cur) { return (cur & 0x80000000u) != sense; }, b.status_line,
-                          b.timeout_ns, round, who);
+                          b.timeout_ns, round, who, true);
     } else if constexpr (V == kBvFlag) {
         return poll_epoch(b.flag, pd.target, b.e, b.status_line, b.timeout_ns, round, who, true, 0);
     } else if constexpr (V == kBvArrivalOnly || V == kBvArrivalDieLocal) {
         return poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, pd.target, b.e); }, b.status_line,
                           b.timeout_ns, round, who, true, 0, false);
     } else {
-        constexpr bool relaxed = V == kBvRelaxedPoll || V == kBvBackoff;
+        constexpr bool relaxed = V == kBvRelaxedPoll || V == kBvBackoff || V == kBvDieLocal;
         return poll_epoch(b.ctr, pd.target, b.e, b.status_line, b.timeout_ns, round, who, relaxed,
                           V == kBvBackoff ? 32u : 0u);
     }
@@ -554,7 +554,7 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
             return true;
         const uint32_t sense = pd.target;
         return poll_until(b.ctr, [&](uint32_t cur) { return (cur & 0x80000000u) != sense; }, b.status_line,
-                          b.timeout_ns, round, who);
+                          b.timeout_ns, round, who, true);
     } else {
         uint32_t target;
         bool stop;
@@ -563,7 +563,7 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
             red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);
-            stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who);
+            stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who, true);
         } else if constexpr (V == kBvArrivalDieLocal) {
             red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
