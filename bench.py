@@ -145,7 +145,9 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "u32", "data": "synthetic (SplitMix64 seeded uniform uint32)",
             "impl": "reference",
-            "config": {"workload": WORKLOAD, "participants": P_HEAD, "rounds": ROUNDS_HEAD},
+            "config": {"workload": WORKLOAD, "participants": P_HEAD, "threads_per_cta": 256, "rounds": ROUNDS_HEAD,
+                       "payload_bytes": P_HEAD * SLOTS_HEAD * 4,
+                       "parallelism": "the sequential CPU oracle, one host thread"},
             "cpu_baseline": {"value": round(val, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"one full workload ({ROUNDS_HEAD} rounds) per step, sequential C oracle"},
             "e2e": {"value": round(val, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
