@@ -184,15 +184,35 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 }
 
 // ---------------------------------------------------------------------------
-// Op-stream state machine.  The stream is cut into chunks of kChunk ops.  A
-// SET record gives a count that does not depend on what came before, so from
-// the first SET of a chunk to the chunk's end the trace can be computed at
-// once (suffix kernel).  The ops before that first SET are replayed by the
-// thread of the nearest earlier chunk that ends in a known count ("chain
-// head"), which runs forward until it meets the next SET (prefix kernel).
-// Every op is applied exactly once, in order along its chain.
+// Op-stream state machine.  A SET record gives a count that does not depend
+// on what came before, so the stream can be cut at SETs: from a SET on, the
+// trace can be computed without knowing the earlier count.
+//
+// One persistent cooperative launch.  The stream is cut into tiles of 4096
+// ops; CTA b takes tiles b, b + grid, b + 2 grid, ...  Within a tile, 512
+// threads each own a chunk of 8 ops:
+//   A  every chunk with a SET traces from its first SET to its end;
+//   B  the thread of such a chunk carries its end count on through the
+//      following chunks up to the next SET; the chain that reaches the tile's
+//      end publishes the tile's end count (tagged with this call's tag) for
+//      the next tile;
+//   C  thread 0 takes the previous tile's end count (init for tile 0),
+//      waiting on the device until it is published, and replays the ops in
+//      front of the tile's first SET -- all of them if the tile has none, in
+//      which case it publishes the tile's end count itself.
+// Every op is applied exactly once, in stream order along its chain.  A tile
+// with a SET publishes before it waits, so a wait lasts only as long as a run
+// of SET-free tiles in front of it.  Every CTA is resident (cooperative
+// launch) and takes its tiles in increasing order, so the tile a CTA waits
+// for is always held by a running CTA (or done).  The tag makes the link words
+// need no initial content: a word holds (tag << 32) | count, and a word from
+// an earlier call carries an earlier tag.  The wait is bounded; if it runs out
+// (only a stalled GPU can make it), the tile's leading entries get count 0 and
+// outcome CNS_OUT_INVALID.
 // ---------------------------------------------------------------------------
 
+// Granularity of cns_statemachine_scratch_bytes (8 bytes per 16 ops): more
+// than the one link word per 4096-op tile the kernel uses.
 constexpr int kChunk = 16;
 
 // An op packed into 8 bytes: x = value, y = kind code (0 record, 1 wait,
@@ -225,183 +245,6 @@ __device__ __forceinline__ uint32_t sm_apply_packed(uint32_t c, const uint2 op, 
 
 __device__ __forceinline__ bool is_set_packed(const uint2 op) { return (op.y & 0x1Fu) == 0u; }   // record, SET
 
-__device__ __forceinline__ uint32_t sm_apply(uint32_t c, const uint4 &op, uint32_t *outcome)
-{
-    return sm_apply_packed(c, sm_pack(op), outcome);
-}
-
-__device__ __forceinline__ bool is_set_record(const uint4 &op) { return op.x == 0u && op.y == CNS_REC_SET; }
-
-// Both kernels stage one CTA's 256 chunks (4096 ops) through shared memory
-// so that every global access is coalesced.  Chunk k of the CTA sits at slot
-// k * (kChunk + 1): the one-slot pad spreads the per-thread walks over all
-// banks.  Trace entries are staged the same way with a sentinel outcome; only
-// the entries a kernel computed are written back.
-constexpr int kSmThreads = 256;
-constexpr int kCtaOps = kChunk * kSmThreads;
-constexpr int kPad = kChunk + 1;
-constexpr uint32_t kNoEntry = 0xFFFFFFFFu;
-constexpr size_t kSmSmemBytes = static_cast<size_t>(kSmThreads) * kPad * (sizeof(uint4) + sizeof(uint2));
-
-__device__ __forceinline__ int sm_slot(int i) { return (i / kChunk) * kPad + (i % kChunk); }
-
-// Load this CTA's ops into shared memory and mark every trace slot empty.
-// Each thread has all of its 16 loads in flight before it stores any of them
-// (a load-store loop would wait out 16 memory latencies in a row).
-__device__ __forceinline__ int sm_stage(const uint4 *ops, int64_t n, int64_t base, uint4 *s_ops, uint2 *s_tr)
-{
-    const int cnt = (n - base < kCtaOps) ? static_cast<int>(n - base) : kCtaOps;
-    constexpr int kPerThread = kCtaOps / kSmThreads;
-    uint4 v[kPerThread];
-#pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-        const int i = threadIdx.x + j * kSmThreads;
-        if (i < cnt)
-            v[j] = __ldg(ops + base + i);
-    }
-#pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-        const int i = threadIdx.x + j * kSmThreads;
-        if (i < cnt)
-            s_ops[sm_slot(i)] = v[j];
-    }
-    for (int i = threadIdx.x; i < kCtaOps; i += kSmThreads)
-        s_tr[sm_slot(i)] = make_uint2(0u, kNoEntry);
-    __syncthreads();
-    return cnt;
-}
-
-__device__ __forceinline__ void sm_flush(uint2 *trace, int64_t base, int cnt, const uint2 *s_tr)
-{
-    __syncthreads();
-    for (int i = threadIdx.x; i < cnt; i += kSmThreads) {
-        const uint2 v = s_tr[sm_slot(i)];
-        if (v.y != kNoEntry)
-            trace[base + i] = v;
-    }
-}
-
-__global__ void __launch_bounds__(kSmThreads) sm_suffix_kernel(const uint4 *ops, int64_t n, uint2 *trace,
-                                                               uint2 *summ, uint32_t *final_count)
-{
-    extern __shared__ uint4 sm_smem[];
-    uint4 *s_ops = sm_smem;
-    uint2 *s_tr = reinterpret_cast<uint2 *>(sm_smem + kSmThreads * kPad);
-    const int64_t T = (n + kChunk - 1) / kChunk;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
-    const int cnt = sm_stage(ops, n, base, s_ops, s_tr);
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * kSmThreads + threadIdx.x;
-    if (t < T) {
-        const int off = threadIdx.x * kPad;
-        const int m = (n - t * kChunk < kChunk) ? static_cast<int>(n - t * kChunk) : kChunk;
-        int first = -1;
-        for (int k = 0; k < m; ++k)
-            if (is_set_record(s_ops[off + k])) {
-                first = k;
-                break;
-            }
-        if (first < 0) {
-            summ[t] = make_uint2(0u, 0u);
-        } else {
-            uint32_t c = 0;
-            for (int k = first; k < m; ++k) {
-                uint32_t o;
-                c = sm_apply(c, s_ops[off + k], &o);
-                s_tr[off + k] = make_uint2(c, o);
-            }
-            summ[t] = make_uint2(1u, c);
-            if (t == T - 1)
-                *final_count = c;
-        }
-    }
-    sm_flush(trace, base, cnt, s_tr);
-}
-
-__global__ void __launch_bounds__(kSmThreads) sm_prefix_kernel(const uint4 *ops, int64_t n, uint32_t init,
-                                                               uint2 *trace, const uint2 *summ,
-                                                               uint32_t *final_count)
-{
-    extern __shared__ uint4 sm_smem[];
-    uint4 *s_ops = sm_smem;
-    uint2 *s_tr = reinterpret_cast<uint2 *>(sm_smem + kSmThreads * kPad);
-    const int64_t T = (n + kChunk - 1) / kChunk;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
-    const int cnt = sm_stage(ops, n, base, s_ops, s_tr);
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * kSmThreads + threadIdx.x;
-    bool head = false;
-    uint32_t c = init;
-    if (t < T) {
-        if (t == 0) {
-            head = true;
-        } else {
-            const uint2 prev = summ[t - 1];
-            head = prev.x != 0;   // otherwise an earlier chain runs through this chunk
-            c = prev.y;
-        }
-    }
-    if (head) {
-        // replay from the chunk start until the next SET (the suffix kernel
-        // traced from there on) or the end of the stream
-        int64_t i = t * kChunk;
-        bool ended = true;
-        const int64_t staged_end = base + cnt;
-        for (; i < staged_end; ++i) {
-            const uint4 op = s_ops[sm_slot(static_cast<int>(i - base))];
-            if (is_set_record(op)) {
-                ended = false;
-                break;
-            }
-            uint32_t o;
-            c = sm_apply(c, op, &o);
-            s_tr[sm_slot(static_cast<int>(i - base))] = make_uint2(c, o);
-        }
-        // a chain that runs past this CTA's ops reads the rest from global
-        // memory, eight independent loads at a time
-        constexpr int kBatch = 8;
-        while (ended && i < n) {
-            uint4 op[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k)
-                op[k] = (i + k < n) ? ops[i + k] : make_uint4(0u, CNS_REC_SET, 0u, 0u);
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-                if (!ended)
-                    break;
-                if (i + k >= n)
-                    break;
-                if (is_set_record(op[k])) {
-                    ended = false;
-                    break;
-                }
-                uint32_t o;
-                c = sm_apply(c, op[k], &o);
-                trace[i + k] = make_uint2(c, o);
-            }
-            i += kBatch;
-        }
-        if (ended)
-            *final_count = c;   // no SET after the chain start: this chain ends the stream
-    }
-    sm_flush(trace, base, cnt, s_tr);
-}
-
-// Single pass, for a launch whose CTAs are all resident at once (a
-// cooperative launch).  Each CTA stages its 4096 ops and:
-//   A  every chunk with a SET traces from its first SET to its end;
-//   B  the thread of such a chunk carries its end count on through the
-//      following chunks up to the next SET; the chain that reaches the CTA's
-//      end publishes the CTA's end count (tagged with this call's tag) for
-//      the next CTA;
-//   C  thread 0 takes the previous CTA's end count (init for CTA 0), waiting
-//      on the device until it is published, and replays the ops in front of
-//      the CTA's first SET -- all of them if the CTA has none, in which case
-//      it publishes the CTA's end count itself.
-// A CTA with a SET publishes before it waits, so a CTA waits only as long as
-// a run of SET-free CTAs in front of it takes.  The tag makes the link words
-// need no initial content: a word holds (tag << 32) | count, and a word from
-// an earlier call carries an earlier tag.  The wait is bounded; if it runs out
-// (only a stalled GPU can make it), the CTA's leading entries get count 0 and
-// outcome CNS_OUT_INVALID.
 constexpr uint64_t kSmLinkTimeoutNs = 10ull * 1000000000ull;
 
 __device__ __forceinline__ void sm_publish(uint64_t *link, uint32_t tag, uint32_t c)
@@ -430,123 +273,130 @@ __device__ __forceinline__ bool sm_take(const uint64_t *link, uint32_t tag, uint
     }
 }
 
-// Shape of the one-pass kernel: 512 threads, chunks of 8 ops (the same 4096
-// ops per CTA), ops packed to 8 bytes in shared memory.  Twice the warps of
-// the two-launch kernels, and per-thread walks half as long.
+// Tile shape: 512 threads x chunks of 8 ops, ops packed to 8 bytes in shared
+// memory with a one-entry pad per chunk (conflict-free per-thread walks).
 constexpr int kFChunk = 8;
 constexpr int kFThreads = 512;
-constexpr int kFPad = kFChunk + 1;   // with 8-byte entries: conflict-free per-thread walks
-static_assert(kFChunk * kFThreads == kCtaOps, "one-pass CTAs hold as many ops as the two-launch ones");
+constexpr int kTileOps = kFChunk * kFThreads;
+constexpr int kFPad = kFChunk + 1;
 constexpr size_t kFSmemBytes = static_cast<size_t>(kFThreads) * kFPad * 2 * sizeof(uint2);
 
 __device__ __forceinline__ int f_slot(int i) { return (i / kFChunk) * kFPad + (i % kFChunk); }
 
-__global__ void __launch_bounds__(kFThreads, 2) sm_fused_kernel(const uint4 *ops, int64_t n, uint32_t init,
-                                                                uint2 *trace, uint64_t *link, uint32_t tag,
-                                                                uint32_t *final_count)
+__global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *ops, int64_t n, uint32_t init,
+                                                                  uint2 *trace, uint64_t *link, uint32_t tag,
+                                                                  uint32_t *final_count)
 {
     extern __shared__ uint2 f_smem[];
     uint2 *s_ops = f_smem;
     uint2 *s_tr = f_smem + kFThreads * kFPad;
     __shared__ int s_first[kFThreads];   // index of the chunk's first SET, -1 if none
     __shared__ int s_wmin[kFThreads / 32];
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kCtaOps;
-    const int cnt = (n - base < kCtaOps) ? static_cast<int>(n - base) : kCtaOps;
-    {   // stage: all 8 loads of a thread in flight, packed on the way in
-        uint2 v[kFChunk];
-#pragma unroll
-        for (int j = 0; j < kFChunk; ++j) {
-            const int i = threadIdx.x + j * kFThreads;
-            if (i < cnt)
-                v[j] = sm_pack(__ldg(ops + base + i));
-        }
-#pragma unroll
-        for (int j = 0; j < kFChunk; ++j) {
-            const int i = threadIdx.x + j * kFThreads;
-            if (i < cnt)
-                s_ops[f_slot(i)] = v[j];
-        }
-    }
-    __syncthreads();
-    const bool last_cta = base + cnt == n;
-    const int nchunks = (cnt + kFChunk - 1) / kFChunk;
+    const int64_t tiles = (n + kTileOps - 1) / kTileOps;
     const int k = threadIdx.x;
-    int first = -1;
-    uint32_t c = 0;
-    if (k < nchunks) {   // A
-        const int off = k * kFPad;
-        const int m = (cnt - k * kFChunk < kFChunk) ? cnt - k * kFChunk : kFChunk;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t base = t * kTileOps;
+        const int cnt = (n - base < kTileOps) ? static_cast<int>(n - base) : kTileOps;
+        {   // stage: the 8 loads of a thread in flight four at a time, packed on the way in
+            const uint4 *src = ops + base;
 #pragma unroll
-        for (int q = kFChunk - 1; q >= 0; --q)   // all looks at once: the first SET wins
-            if (q < m && is_set_packed(s_ops[off + q]))
-                first = q;
-        for (int q = (first < 0 ? m : first); q < m; ++q) {
-            uint32_t o;
-            c = sm_apply_packed(c, s_ops[off + q], &o);
-            s_tr[off + q] = make_uint2(c, o);
+            for (int h = 0; h < kFChunk; h += 4) {
+                uint4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i = k + (h + j) * kFThreads;
+                    if (i < cnt)
+                        v[j] = __ldg(src + i);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int i = k + (h + j) * kFThreads;
+                    if (i < cnt)
+                        s_ops[f_slot(i)] = sm_pack(v[j]);
+                }
+            }
         }
-    }
-    s_first[k] = first;
-    {   // the CTA's first chunk with a SET: a ballot per warp, then the warps' minimum
-        const uint32_t has = __ballot_sync(0xffffffffu, first >= 0);
-        if ((k & 31) == 0)
-            s_wmin[k >> 5] = has ? (k & ~31) + __ffs(has) - 1 : kFThreads;
-    }
-    __syncthreads();
-    if (first >= 0) {   // B
-        int j = k + 1;
-        for (; j < nchunks; ++j) {
-            const int fj = s_first[j];
-            const int off = j * kFPad;
-            const int m = fj >= 0 ? fj : ((cnt - j * kFChunk < kFChunk) ? cnt - j * kFChunk : kFChunk);
-            for (int q = 0; q < m; ++q) {
+        __syncthreads();
+        const bool last_tile = base + cnt == n;
+        const int nchunks = (cnt + kFChunk - 1) / kFChunk;
+        int first = -1;
+        uint32_t c = 0;
+        if (k < nchunks) {   // A
+            const int off = k * kFPad;
+            const int m = (cnt - k * kFChunk < kFChunk) ? cnt - k * kFChunk : kFChunk;
+#pragma unroll
+            for (int q = kFChunk - 1; q >= 0; --q)   // all looks at once: the first SET wins
+                if (q < m && is_set_packed(s_ops[off + q]))
+                    first = q;
+            for (int q = (first < 0 ? m : first); q < m; ++q) {
                 uint32_t o;
                 c = sm_apply_packed(c, s_ops[off + q], &o);
                 s_tr[off + q] = make_uint2(c, o);
             }
-            if (fj >= 0)
-                break;
         }
-        if (j >= nchunks) {
-            sm_publish(link + blockIdx.x, tag, c);
-            if (last_cta)
-                *final_count = c;
+        s_first[k] = first;
+        {   // the tile's first chunk with a SET: a ballot per warp, then the warps' minimum
+            const uint32_t has = __ballot_sync(0xffffffffu, first >= 0);
+            if ((k & 31) == 0)
+                s_wmin[k >> 5] = has ? (k & ~31) + __ffs(has) - 1 : kFThreads;
         }
-    }
-    if (k == 0) {   // C
-        int fc = kFThreads;
-        for (int w = 0; w < kFThreads / 32; ++w)
-            fc = s_wmin[w] < fc ? s_wmin[w] : fc;
-        const int lead = fc < nchunks ? fc * kFChunk + s_first[fc] : cnt;
-        uint32_t cp = init;
-        const bool ok = blockIdx.x == 0 || sm_take(link + blockIdx.x - 1, tag, &cp);
-        for (int i = 0; i < lead; ++i) {
-            uint32_t o;
-            if (ok) {
-                cp = sm_apply_packed(cp, s_ops[f_slot(i)], &o);
-            } else {
-                cp = 0u;
-                o = CNS_OUT_INVALID;
+        __syncthreads();
+        if (first >= 0) {   // B
+            int j = k + 1;
+            for (; j < nchunks; ++j) {
+                const int fj = s_first[j];
+                const int off = j * kFPad;
+                const int m = fj >= 0 ? fj : ((cnt - j * kFChunk < kFChunk) ? cnt - j * kFChunk : kFChunk);
+                for (int q = 0; q < m; ++q) {
+                    uint32_t o;
+                    c = sm_apply_packed(c, s_ops[off + q], &o);
+                    s_tr[off + q] = make_uint2(c, o);
+                }
+                if (fj >= 0)
+                    break;
             }
-            s_tr[f_slot(i)] = make_uint2(cp, o);
+            if (j >= nchunks) {
+                sm_publish(link + t, tag, c);
+                if (last_tile)
+                    *final_count = c;
+            }
         }
-        if (fc >= nchunks) {
-            sm_publish(link + blockIdx.x, tag, cp);
-            if (last_cta)
-                *final_count = cp;
+        if (k == 0) {   // C
+            int fc = kFThreads;
+            for (int w = 0; w < kFThreads / 32; ++w)
+                fc = s_wmin[w] < fc ? s_wmin[w] : fc;
+            const int lead = fc < nchunks ? fc * kFChunk + s_first[fc] : cnt;
+            uint32_t cp = init;
+            const bool ok = t == 0 || sm_take(link + t - 1, tag, &cp);
+            for (int i = 0; i < lead; ++i) {
+                uint32_t o;
+                if (ok) {
+                    cp = sm_apply_packed(cp, s_ops[f_slot(i)], &o);
+                } else {
+                    cp = 0u;
+                    o = CNS_OUT_INVALID;
+                }
+                s_tr[f_slot(i)] = make_uint2(cp, o);
+            }
+            if (fc >= nchunks) {
+                sm_publish(link + t, tag, cp);
+                if (last_tile)
+                    *final_count = cp;
+            }
         }
+        __syncthreads();
+        for (int i = k; i < cnt; i += kFThreads)   // every entry was written once
+            trace[base + i] = s_tr[f_slot(i)];
+        __syncthreads();   // the shared tile is free for the next one
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < cnt; i += kFThreads)   // every entry was written once
-        trace[base + i] = s_tr[f_slot(i)];
 }
 
-// CTAs of sm_fused_kernel that fit on each device at once (set by sm_prepare).
-static int64_t g_sm_fused_max_blocks[64];
+// The kernel's co-resident CTAs per device (set by sm_prepare) and the call
+// tags of this process.
+static int64_t g_sm_max_ctas[64];
 static std::atomic<uint32_t> g_sm_tag{0};
 
-// Shared-memory opt-in for the kernels and the fused kernel's co-residency
-// limit, once per device.
+// Shared-memory opt-in and the co-residency limit, once per device.
 static int sm_prepare(int device)
 {
     static std::mutex mu;
@@ -555,57 +405,42 @@ static int sm_prepare(int device)
     if (device < 0 || device >= 64)
         return CNS_ERR_CUDA;
     if (!done[device]) {
-        CNS_CUDA(cudaFuncSetAttribute(sm_suffix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kSmSmemBytes)));
-        CNS_CUDA(cudaFuncSetAttribute(sm_prefix_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kSmSmemBytes)));
-        CNS_CUDA(cudaFuncSetAttribute(sm_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        CNS_CUDA(cudaFuncSetAttribute(sm_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kFSmemBytes)));
         int per_sm = 0;
-        CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sm_fused_kernel, kFThreads, kFSmemBytes));
+        CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sm_onepass_kernel, kFThreads, kFSmemBytes));
         int sms = 0;
         CNS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
-        g_sm_fused_max_blocks[device] = static_cast<int64_t>(per_sm) * sms;
+        if (per_sm < 1)
+            return CNS_ERR_CUDA;
+        g_sm_max_ctas[device] = static_cast<int64_t>(per_sm) * sms;
         done[device] = true;
     }
     return CNS_SUCCESS;
 }
 
-// The two launches of one state-machine run (n > 0).
-static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, uint2 *summ, uint32_t *final_dev,
+// One state-machine run (n > 0): one cooperative launch of at most as many
+// CTAs as fit at once.  `link` needs one 8-byte word per 4096-op tile.
+static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, uint64_t *link, uint32_t *final_dev,
                      int device, cudaStream_t s)
 {
     if (int rc = sm_prepare(device))
         return rc;
-    const int64_t blocks = (n + kCtaOps - 1) / kCtaOps;
-    if (blocks > 0x7fffffff)
-        return CNS_ERR_INVALID_VALUE;
-    if (blocks <= g_sm_fused_max_blocks[device] &&
-        static_cast<size_t>(blocks) * sizeof(uint64_t) <= cns_statemachine_scratch_bytes(n)) {
-        // one pass: every CTA resident at once, so a CTA waiting for the one
-        // before it always sees it finish
-        uint32_t tag = ++g_sm_tag;
-        if (tag == 0)
-            tag = ++g_sm_tag;
-        uint64_t *link = reinterpret_cast<uint64_t *>(summ);
-        const uint4 *a0 = ops;
-        int64_t a1 = n;
-        uint32_t a2 = init;
-        uint2 *a3 = trace;
-        uint64_t *a4 = link;
-        uint32_t a5 = tag;
-        uint32_t *a6 = final_dev;
-        void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5, &a6};
-        CNS_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(sm_fused_kernel),
-                                             dim3(static_cast<unsigned>(blocks)), dim3(kFThreads), args,
-                                             kFSmemBytes, s));
-        return CNS_SUCCESS;
-    }
-    sm_suffix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, trace, summ, final_dev);
-    CNS_CUDA(cudaGetLastError());
-    sm_prefix_kernel<<<static_cast<unsigned>(blocks), kSmThreads, kSmSmemBytes, s>>>(ops, n, init, trace, summ,
-                                                                                    final_dev);
-    CNS_CUDA(cudaGetLastError());
+    const int64_t tiles = (n + kTileOps - 1) / kTileOps;
+    const int64_t grid = tiles < g_sm_max_ctas[device] ? tiles : g_sm_max_ctas[device];
+    uint32_t tag = ++g_sm_tag;
+    if (tag == 0)
+        tag = ++g_sm_tag;
+    const uint4 *a0 = ops;
+    int64_t a1 = n;
+    uint32_t a2 = init;
+    uint2 *a3 = trace;
+    uint64_t *a4 = link;
+    uint32_t a5 = tag;
+    uint32_t *a6 = final_dev;
+    void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5, &a6};
+    CNS_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(sm_onepass_kernel),
+                                         dim3(static_cast<unsigned>(grid)), dim3(kFThreads), args, kFSmemBytes, s));
     return CNS_SUCCESS;
 }
 
@@ -925,7 +760,7 @@ extern "C" int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t
         return CNS_SUCCESS;
     }
     return sm_launch(reinterpret_cast<const uint4 *>(ops_dev), n, init, reinterpret_cast<uint2 *>(trace_dev),
-                     static_cast<uint2 *>(scratch_dev), final_dev, dev.device, s);
+                     static_cast<uint64_t *>(scratch_dev), final_dev, dev.device, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -982,11 +817,10 @@ extern "C" int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, 
         CNS_CUDA(cudaGetLastError());
         return CNS_SUCCESS;
     }
-    // Whatever an earlier call left in the array never matters: the suffix
-    // kernel writes every summary the prefix kernel reads, and the one-pass
-    // kernel's link words carry the tag of their call.
-    return sm_launch(reinterpret_cast<const uint4 *>(ops_dev), n, init, reinterpret_cast<uint2 *>(trace_dev), summ,
-                     final_dev, dev.device, s);
+    // Whatever an earlier call left in the array never matters: the link
+    // words carry the tag of their call.
+    return sm_launch(reinterpret_cast<const uint4 *>(ops_dev), n, init, reinterpret_cast<uint2 *>(trace_dev),
+                     reinterpret_cast<uint64_t *>(summ), final_dev, dev.device, s);
 }
 
 // ---------------------------------------------------------------------------

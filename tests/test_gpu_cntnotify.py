@@ -211,15 +211,16 @@ def test_statemachine_without_any_set(cns):
 
 
 def _fused_limit():
-    """Largest op count the one-pass kernel takes on this GPU: 2 CTAs of 4096 ops per SM."""
+    """Op count that gives every resident CTA exactly one 4096-op tile: 2 CTAs per SM."""
     import torch
     return torch.cuda.get_device_properties(0).multi_processor_count * 2 * 4096
 
 
 @pytest.mark.parametrize("where", ["at_limit", "over_limit", "three_million"])
-def test_statemachine_one_pass_and_two_pass_sizes(cns, where):
-    """Streams that the one-pass kernel takes (all CTAs resident) and streams
-    just over that, which take the two-launch path, both bit for bit."""
+def test_statemachine_one_and_several_tiles_per_cta(cns, where):
+    """Streams with exactly one 4096-op tile per resident CTA, one tile more
+    (a CTA takes a second tile, waiting on a tile of the previous wave), and
+    3e6 ops (several waves), bit for bit."""
     lim = _fused_limit()
     n = {"at_limit": lim, "over_limit": lim + 1, "three_million": 3_000_000}[where]
     ops = ci.notify_ops(n, seed=n % 1000)
