@@ -268,3 +268,97 @@ def flip_final_counter(P: int, rounds: int, bits: int = 32, start: int = 0) -> i
     """Word after `rounds` complete sense-flip barriers: each adds 2^(bits-1) in total."""
     W = 1 << bits
     return (start + rounds * (W >> 1)) % W
+
+
+# Hard path with one group barrier per round --------------------------------
+#
+# The first barrier of a run is the two-level form above, except that the
+# leader hands the round's target to its members as the second group barrier
+# opens.  From then on a round is: group barrier; the leader arrives on the
+# counter; every participant -- leader and members alike -- polls the counter
+# for its own target, the members' target being the previous one plus G.  A
+# leader whose returned count puts it in another epoch than that prediction
+# counts as an epoch violation (the kernel stops the run there).
+
+def explore_hard_one_barrier(P: int, C: int, rounds: int, M: int | None = None, start: int = 0,
+                             max_states: int = 2_000_000, member_step: int | None = None) -> Result:
+    """All interleavings of the one-barrier hard path.  member_step overrides
+    the members' prediction step (G; the tests plant wrong ones)."""
+    assert P % C == 0
+    G = P // C
+    step = G if member_step is None else member_step
+    arith = Arith("modular", G, M if M is not None else 4 * G)
+    res = Result()
+    # participant: (k rounds done, phase, target, cursor)
+    #   phase 0 before the group barrier, 1 in it, 3 polling,
+    #   2 in the first round's second group barrier
+    init = (start % arith.M, tuple((0, 0, 0, 0) for _ in range(P)))
+    seen = set()
+    stack = [init]
+
+    def arrived(m, k):
+        return m[0] > k or (m[0] == k and m[1] >= 1)
+
+    while stack:
+        state = stack.pop()
+        if state in seen:
+            continue
+        seen.add(state)
+        res.states += 1
+        if res.states > max_states:
+            raise RuntimeError("state space larger than max_states")
+        c, parts = state
+        succ = []
+        for i, (k, ph, t, cur) in enumerate(parts):
+            if k == rounds:
+                continue
+            g, lead = i // C, (i % C == 0)
+            grp = parts[g * C:(g + 1) * C]
+
+            def put(v, nc=c):
+                succ.append((nc, parts[:i] + (v,) + parts[i + 1:]))
+
+            if ph == 0:
+                put((k, 1, 0, cur))
+            elif ph == 1:
+                if not all(arrived(m, k) for m in grp):
+                    continue
+                if lead:
+                    before = c
+                    if (before - start - k * G) % arith.M >= G:
+                        res.epoch_violations += 1
+                    tgt = arith.target(before)
+                    if k > 0 and tgt != (cur + G) % arith.M:
+                        res.epoch_violations += 1
+                    put((k, 3, tgt, cur), arith.arrive(c))
+                elif k == 0:
+                    put((k, 2, 0, cur))          # members wait for the leader's hand-over
+                else:
+                    put((k, 3, (cur + step) % arith.M, cur))
+            elif ph == 3:
+                if not arith.reached(c, t):
+                    continue
+                if k == 0 and lead:
+                    put((k, 2, t, t))            # the leader joins the second group barrier
+                    continue
+                if not all(arrived(m, k) for m in parts):
+                    res.safety_violations += 1
+                put((k + 1, 0, 0, t))
+            elif ph == 2:
+                # the first round's second group barrier opens once every member
+                # is in it (or already through); the leader reached it holding
+                # the round's target, which the members take as their cursor
+                if not all((m[0] == 0 and m[1] == 2) or m[0] > 0 for m in grp):
+                    continue
+                if not all(arrived(m, 0) for m in parts):
+                    res.safety_violations += 1
+                leader = grp[0]
+                tgt = t if lead else (leader[2] if leader[0] == 0 else leader[3])
+                put((1, 0, 0, tgt))
+        if not succ:
+            if all(p[0] == rounds for p in parts):
+                res.completed += 1
+            else:
+                res.deadlocks += 1
+        stack.extend(succ)
+    return res

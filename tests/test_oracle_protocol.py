@@ -126,3 +126,33 @@ def test_flip_final_counter():
     assert flip_final_counter(148, 1) == 1 << 31
     assert flip_final_counter(148, 2) == 0
     assert flip_final_counter(148, 3, start=1 << 31) == 0
+
+
+# --- hard path with one group barrier per round (members poll the counter themselves) -------
+
+from oracle.protocol import explore_hard_one_barrier  # noqa: E402
+
+
+@pytest.mark.parametrize("P,C", [(2, 1), (2, 2), (4, 2), (4, 4), (6, 2), (6, 3)])
+@pytest.mark.parametrize("R", [1, 2, 3])
+def test_hard_one_barrier_safe_and_live(P, C, R):
+    res = explore_hard_one_barrier(P, C, R)
+    assert res.ok and res.completed == 1
+
+
+@pytest.mark.parametrize("start_mult", [1, 3])
+def test_hard_one_barrier_from_an_aligned_start_near_the_wrap(start_mult):
+    G = 2
+    M = 4 * G
+    assert explore_hard_one_barrier(4, 2, 3, M=M, start=M - start_mult * G).ok
+
+
+def test_hard_one_barrier_misaligned_start_is_caught():
+    res = explore_hard_one_barrier(4, 2, 2, start=1)
+    assert not res.ok
+
+
+@pytest.mark.parametrize("step", [0, 1, 3])
+def test_hard_one_barrier_wrong_member_prediction_is_caught(step):
+    # G = 2: members that step by anything else leave early or never
+    assert not explore_hard_one_barrier(4, 2, 3, member_step=step).ok
