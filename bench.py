@@ -352,21 +352,27 @@ def secondary(cns, torch, peaks):
     u0 = ci.jacobi_field(N)
     b0 = torch.from_numpy(u0).cuda()
     b1 = torch.empty_like(b0)
-    ws = cns.new_workspace()
-    runs = []
-    for _ in range(3):
-        b0.copy_(torch.from_numpy(u0))
-        ms, _ = timed_run(torch, lambda: cns.run_syncall(
-            cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_JACOBI, C, b0, b1, S, elems=N, workspace=ws,
-            sync=False))
-        runs.append(ms)
-    rc, soft, hard, st = cns.syncall_read_workspace(ws)
-    ms = min(runs)
+    by_variant, best = {}, None
+    for v in (0, 2, 5):
+        ws = cns.new_workspace()
+        runs = []
+        for _ in range(3):
+            b0.copy_(torch.from_numpy(u0))
+            ms, _ = timed_run(torch, lambda: cns.run_syncall(
+                cns.CNS_SYNCALL_SOFT, cns.CNS_AIV_ONLY, cns.CNS_WL_JACOBI, C, b0, b1, S, elems=N, workspace=ws,
+                sync=False, variant=v))
+            runs.append(ms)
+        rc, soft, hard, st = cns.syncall_read_workspace(ws)
+        by_variant[VARIANT_NAMES[v]] = round(S * 8 * N / (min(runs) * 1e-3) / 1e9, 1)
+        if st == 0 and (best is None or min(runs) < best[0]):
+            best = (min(runs), v, st)
+    ms, v, st = best if best else (min(runs), 0, st)
     gbs = S * 8 * N / (ms * 1e-3) / 1e9
     out["jacobi_2p26_592ctas_200sweeps"] = {
         "ms": round(ms, 3), "us_per_sweep": round(ms * 1e3 / S, 2), "hbm_gbs": round(gbs, 1),
         "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4) if peaks.get("hbm_gbs") else None,
-        "algorithmic_bytes_per_sweep": 8 * N, "status": st}
+        "algorithmic_bytes_per_sweep": 8 * N, "status": st, "barrier_variant": VARIANT_NAMES[v],
+        "hbm_gbs_by_variant": by_variant}
 
     # counted-notify pipeline: 4096 tiles x 256 words, 1000 rounds, two streams
     rc1, done = cns.cntnotify_create(0)
