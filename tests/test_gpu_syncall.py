@@ -493,3 +493,30 @@ def test_jacobi_unzeroed_workspace_times_out(cns, mode):
     d, got = run_jacobi(cns, u0, 4, 16, mode=mode)
     want, _, _ = oracle.syncall_run_jacobi(u0, 4, 16)
     np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_largest_resident_grid(cns, mode):
+    """The most CTAs the GPU holds at once (32 per SM at 32 threads on the soft
+    path; fewer in clusters): every participant arrives every round, and the
+    xorshift ring comes out exact.  Larger grids are refused before launch."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # 32 is the hardware's CTA limit per SM; clusters allow fewer (the library
+    # measured 8 per SM for clusters of 1 and 2, 4 for clusters of 4)
+    for per_sm in (32, 16, 8, 4, 2, 1):
+        P = sms * per_sm
+        v0 = ci.ring_payload(77, P, 4)
+        d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_XORSHIFT, P, v0, 40, threads=32,
+                                  cluster_dim=4 if mode == HARD else 0, check=False)
+        if rc != cns.CNS_ERR_NOT_RESIDENT:
+            break
+    want, fc = expect_ring(oracle.WL_XORSHIFT, v0, 40)
+    np.testing.assert_array_equal(got, want)
+    assert rc == 0 and d.device_status == 0 and d.grid_ctas == P
+    Pc = P if mode == SOFT else P // d.cluster_used
+    assert d.final_counter == (40 * Pc) % oracle.counter_modulus(Pc)
+    if per_sm == 32:   # a cluster more than 32 CTAs per SM can never be resident: refused before launch
+        d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_XORSHIFT, P + 4, ci.ring_payload(77, P + 4, 4), 1,
+                                  threads=32, cluster_dim=4 if mode == HARD else 0, check=False)
+        assert rc == cns.CNS_ERR_NOT_RESIDENT
