@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +57,8 @@ def parse():
                          "relaxed polls and one acquire fence (the last arrival skips its poll), measured fastest "
                          "with the ring payload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="where the nvidia-smi clock samples of the timed region are written (default: temp dir)")
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="run one small launch pattern for a profiler capture and exit")
     return ap.parse_args()
@@ -162,15 +165,16 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, out_dir: str | None = None):
         self.idx = gpu_index
+        self.out_dir = out_dir or tempfile.gettempdir()
         self.proc = None
         self.path = None
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.idx}.csv")
+            os.makedirs(self.out_dir, exist_ok=True)
+            self.path = os.path.join(self.out_dir, f"clocks_rank{self.idx}.csv")
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -254,7 +258,7 @@ def headline(cns, torch, args, stream):
         if dist_env()[2] > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        with ClockSampler(torch.cuda.current_device()) as clk:
+        with ClockSampler(torch.cuda.current_device(), args.clocks_dir) as clk:
             wall0 = time.perf_counter()
             for i in range(args.steps):
                 flush.zero_()                     # L2 flush between steps, outside the step events
