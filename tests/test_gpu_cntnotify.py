@@ -370,3 +370,21 @@ def test_grid_sync_probe_ring_rotate(cns):
     assert cns.cns_probe_grid_sync(148, 256, 1001, b0, b1) == 0
     torch.cuda.synchronize()
     np.testing.assert_array_equal(from_dev_u32(b1).reshape(148, 4), np.roll(v0, -1001, axis=0))
+
+
+def test_pipeline_on_one_stream(cns):
+    """Producer and consumer on the same stream: every device wait is then
+    already satisfied when it starts, and the result is the same."""
+    import torch
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    try:
+        s = torch.cuda.Stream()
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 300, 64, 12, s, s, timeout_s=10)
+        assert rc == 0 and cfg.device_status == 0
+        want_cs, want_rel = oracle.pipeline(300, 64, 12)
+        np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
+        np.testing.assert_array_equal(from_dev_u32(released), want_rel)
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
