@@ -140,11 +140,6 @@ __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void fence_acq_rel_gpu()
-{
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;
