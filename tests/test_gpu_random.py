@@ -49,7 +49,7 @@ def cns():
     return c
 
 
-@pytest.mark.parametrize("cfg", configs(48), ids=lambda c: f"m{c['mode']}c{c['core']}v{c['variant']}w{c['wl']}P{c['P']}")
+@pytest.mark.parametrize("cfg", configs(96), ids=lambda c: f"m{c['mode']}c{c['core']}v{c['variant']}w{c['wl']}P{c['P']}")
 def test_random_config(cns, cfg):
     import torch
     c = cfg
@@ -123,7 +123,7 @@ def configs_more(n, seed=4242):
     return out
 
 
-@pytest.mark.parametrize("cfg", configs_more(36), ids=lambda c: f"m{c['mode']}c{c['core']}v{c['variant']}w{c['wl']}P{c['P']}")
+@pytest.mark.parametrize("cfg", configs_more(60), ids=lambda c: f"m{c['mode']}c{c['core']}v{c['variant']}w{c['wl']}P{c['P']}")
 def test_random_config_later_variants(cns, cfg):
     import torch
     c = cfg
