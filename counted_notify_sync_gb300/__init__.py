@@ -77,11 +77,12 @@ def run_statemachine(ops_dev, init: int, stream=None):
 
 
 def run_pipeline(done, ack, tiles: int, tile_words: int, rounds: int, producer_stream, consumer_stream,
-                 timeout_s: int = 10, producer_ctas: int = 0, sync: bool = True, buffers=None):
-    """Run the two-stream counting pipeline; returns (Pipeline struct, code, checksums, released)."""
+                 timeout_s: int = 10, producer_ctas: int = 0, sync: bool = True, buffers=None, areas: int = 1):
+    """Run the two-stream counting pipeline; returns (Pipeline struct, code, checksums, released).
+    areas = 2 alternates the rounds between two tile areas (the tile buffer then holds both)."""
     torch = _torch()
     if buffers is None:
-        tiles_buf = torch.empty(tiles * tile_words, dtype=torch.int32, device="cuda")
+        tiles_buf = torch.empty(max(1, areas) * tiles * tile_words, dtype=torch.int32, device="cuda")
         checksums = torch.empty(rounds, dtype=torch.int32, device="cuda")
         released = torch.empty(rounds, dtype=torch.int32, device="cuda")
     else:
@@ -100,5 +101,6 @@ def run_pipeline(done, ack, tiles: int, tile_words: int, rounds: int, producer_s
     cfg.consumer_stream = _native.stream_handle(consumer_stream)
     cfg.timeout_s = timeout_s
     cfg.sync = 1 if sync else 0
+    cfg.areas = areas
     rc = _native.cns_pipeline_run(cfg)
     return cfg, rc, checksums, released

@@ -112,44 +112,51 @@ __global__ void cnt_record_kernel(uint32_t *count, uint32_t mode, uint32_t v)
 // timeout rather than one per remaining round.  kEarlyNext (the pipeline's
 // own waits) lets the stream's next kernel, launched with programmatic
 // stream serialization, be scheduled while this one polls; that kernel waits
-// on the device for this one to end (grid_dependency_wait).
-template <bool kEarlyNext>
+// on the device for this one to end (grid_dependency_wait).  kAfterPrev (the
+// two-area pipeline, whose waits are themselves launched that way behind the
+// previous consumer): before it ends, the kernel waits on the device for
+// that consumer to complete, so the kernels of the stream still complete in
+// stream order.
+template <bool kEarlyNext, bool kAfterPrev>
 __global__ void cnt_wait_kernel(uint32_t *line, uint32_t mode, uint32_t v, uint32_t clear, uint64_t timeout_ns,
                                 uint32_t *observed, uint32_t *abort, uint64_t *released_at)
 {
     if (kEarlyNext)
         grid_launch_dependents();
-    if (threadIdx.x != 0)
-        return;
-    if (abort && ld_relaxed_gpu(abort) != 0u)
-        return;
-    uint32_t spins = 0;
-    uint64_t deadline = 0;
-    for (;;) {
-        const uint32_t c = ld_acquire_gpu(line);
-        if (cnt_wait_released(c, mode, v)) {
-            if (released_at)
-                *released_at = globaltimer_ns();
-            if (observed)
-                *observed = c;
-            if (clear)
-                atom_exch_relaxed_gpu(line, 0u);   // the clear comes after the release
-            return;
-        }
-        if ((++spins & 63u) == 0u) {
-            if (abort && ld_relaxed_gpu(abort) != 0u)
-                return;
-            const uint64_t now = globaltimer_ns();
-            if (deadline == 0)
-                deadline = now + timeout_ns;
-            else if (now > deadline) {
-                atom_exch_relaxed_gpu(line + 1, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
-                if (abort)
-                    atom_exch_relaxed_gpu(abort, 1u);
-                return;
+    if (threadIdx.x == 0 && !(abort && ld_relaxed_gpu(abort) != 0u)) {
+        uint32_t spins = 0;
+        uint64_t deadline = 0;
+        for (;;) {
+            // relaxed polls; the fence after the one that releases makes it an
+            // acquire of the records it read from (they are release operations)
+            const uint32_t c = ld_relaxed_gpu(line);
+            if (cnt_wait_released(c, mode, v)) {
+                fence_acquire_gpu();
+                if (released_at)
+                    *released_at = globaltimer_ns();
+                if (observed)
+                    *observed = c;
+                if (clear)
+                    atom_exch_relaxed_gpu(line, 0u);   // the clear comes after the release
+                break;
+            }
+            if ((++spins & 63u) == 0u) {
+                if (abort && ld_relaxed_gpu(abort) != 0u)
+                    break;
+                const uint64_t now = globaltimer_ns();
+                if (deadline == 0)
+                    deadline = now + timeout_ns;
+                else if (now > deadline) {
+                    atom_exch_relaxed_gpu(line + 1, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
+                    if (abort)
+                        atom_exch_relaxed_gpu(abort, 1u);
+                    break;
+                }
             }
         }
     }
+    if (kAfterPrev)
+        grid_dependency_wait();
 }
 
 // Zero the count, the sticky status, the abort word and the spare word of a
@@ -176,7 +183,7 @@ static bool record_mode_ok(int32_t m)
 static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info_t *info, uint32_t *observed,
                         uint32_t *abort = nullptr, bool early_next = false, uint64_t *released_at = nullptr)
 {
-    auto k = early_next ? cnt_wait_kernel<true> : cnt_wait_kernel<false>;
+    auto k = early_next ? cnt_wait_kernel<true, false> : cnt_wait_kernel<false, false>;
     k<<<1, 32, 0, s>>>(n->line, static_cast<uint32_t>(info->mode), info->value, info->is_clear ? 1u : 0u,
                        wait_timeout_ns(info->timeout), observed, abort, released_at);
     CNS_CUDA(cudaGetLastError());
@@ -450,9 +457,37 @@ __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
 // Two-stream pipeline kernels
 // ---------------------------------------------------------------------------
 
-// Producer of one round.  Before touching the tiles every CTA waits, on the
-// device, until every consumer CTA of the previous round has recorded its
-// ADD 1 on `ack` (ack >= round * consumer CTAs).
+// The pipeline's device-side waits: thread 0 polls *word (relaxed) until
+// `ok(value)`, then an acquire fence.  Returns true if the caller must skip
+// the round: the pipeline's abort word is raised, or the wait ran out, in
+// which case it records CNS_ERR_TIMEOUT in status_word and raises the abort.
+template <class Ok>
+__device__ __forceinline__ bool pipe_wait(const uint32_t *word, Ok ok, uint64_t timeout_ns, uint32_t *abort,
+                                          uint32_t *status_word)
+{
+    uint32_t spins = 0;
+    uint64_t deadline = 0;
+    for (;;) {
+        if (ok(ld_relaxed_gpu(word))) {
+            fence_acquire_gpu();
+            return false;
+        }
+        if ((++spins & 63u) == 0u) {
+            if (ld_relaxed_gpu(abort) != 0u)
+                return true;
+            const uint64_t now = globaltimer_ns();
+            if (deadline == 0) {
+                deadline = now + timeout_ns;
+            } else if (now > deadline) {
+                atom_exch_relaxed_gpu(status_word, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
+                atom_exch_relaxed_gpu(abort, 1u);
+                return true;
+            }
+        }
+    }
+}
+
+// Producer of one round, writing the tile area `area`.
 // CTA b owns tiles b, b + grid, b + 2 grid, ...; all of its threads store
 // them, then, after the block barrier, lane j of warp 0 adds 1 to `done` for
 // the CTA's tile j (j < 32, then the next 32, ...).  Each of those is one
@@ -462,41 +497,36 @@ __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
 // not k.  (Same-address operations are served one at a time by the L2 slice
 // that homes the line, about 1.25 ns each on GB300: one record per tile from
 // 4096 CTAs costs 5 us per round on that line alone.)
+//   Before storing, every CTA waits on the device (if wait_ack) until
+// ack >= ack_target: every consumer CTA that read this area last has
+// finished.
+//   kTwoAreas: rounds alternate between two areas, so this round's stores
+// overlap the previous round's reads.  Its records must still come after the
+// consumer-side wait has cleared the previous round's count (a record that
+// landed before that clear would be wiped by it), so after storing, the CTA
+// waits for the previous producer grid to complete (it is launched behind it
+// with programmatic stream serialization) and then for done < tiles, which
+// holds from the clear on: the previous round left exactly `tiles` on done,
+// and this round's own records total `tiles`, the last of them added after
+// the CTA that makes it has looked.  Only then does the CTA let the next
+// producer grid be scheduled, so at most two producer grids are resident.
 constexpr int kPipeProducerThreads = 256;
 
+template <bool kTwoAreas>
 __global__ void __launch_bounds__(kPipeProducerThreads, 8)
-    pipeline_producer_kernel(uint32_t *tiles, int64_t n_tiles, int tile_words, uint32_t round, uint32_t ack_target,
-                             uint32_t *done, uint32_t *ack, uint64_t timeout_ns, uint32_t *abort,
+    pipeline_producer_kernel(uint32_t *area, int64_t n_tiles, int tile_words, uint32_t round, bool wait_ack,
+                             uint32_t ack_target, uint32_t *done, uint32_t *ack, uint64_t timeout_ns, uint32_t *abort,
                              uint64_t *started_at)
 {
-    __shared__ int s_skip;
+    __shared__ int s_skip, s_skip_rec;
     if (threadIdx.x == 0) {
-        int skip = 0;
-        if (round != 0) {
-            uint32_t spins = 0;
-            uint64_t deadline = 0;
-            // ack counts consumer CTAs (mod 2^32); it never runs more than one
-            // round's worth past the target, so the signed difference decides
-            while (static_cast<int32_t>(ld_acquire_gpu(ack) - ack_target) < 0) {
-                if ((++spins & 63u) == 0u) {
-                    if (ld_relaxed_gpu(abort) != 0u) {
-                        skip = 1;
-                        break;
-                    }
-                    const uint64_t now = globaltimer_ns();
-                    if (deadline == 0) {
-                        deadline = now + timeout_ns;
-                    } else if (now > deadline) {
-                        atom_exch_relaxed_gpu(ack + 1, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
-                        atom_exch_relaxed_gpu(abort, 1u);
-                        skip = 1;
-                        break;
-                    }
-                }
-            }
-        }
-        s_skip = skip;
-        if (started_at && blockIdx.x == 0)
+        // ack counts consumer CTAs (mod 2^32); it never runs more than one
+        // round's worth past the target, so the signed difference decides
+        const bool skip = wait_ack && pipe_wait(ack, [&](uint32_t a) {
+            return static_cast<int32_t>(a - ack_target) >= 0;
+        }, timeout_ns, abort, ack + 1);
+        s_skip = skip ? 1 : 0;
+        if (!kTwoAreas && started_at && blockIdx.x == 0)
             *started_at = globaltimer_ns();   // CTA 0 released: the round's recording phase begins
     }
     __syncthreads();
@@ -510,12 +540,24 @@ __global__ void __launch_bounds__(kPipeProducerThreads, 8)
         const uint32_t j = e / q;
         const uint32_t i = e - j * q;
         const int64_t t = blockIdx.x + static_cast<int64_t>(j) * grid;
-        uint4 *d = reinterpret_cast<uint4 *>(tiles + t * tile_words);
+        uint4 *d = reinterpret_cast<uint4 *>(area + t * tile_words);
         const uint32_t w = static_cast<uint32_t>(t * tile_words) + 4u * static_cast<uint32_t>(i);
         d[i] = make_uint4(w * 2654435761u + round, (w + 1u) * 2654435761u + round, (w + 2u) * 2654435761u + round,
                           (w + 3u) * 2654435761u + round);
     }
+    if constexpr (kTwoAreas) {
+        grid_dependency_wait();   // the previous round's producer has completed
+        if (threadIdx.x == 0) {
+            const uint32_t k = static_cast<uint32_t>(n_tiles);
+            s_skip_rec = pipe_wait(done, [&](uint32_t c) { return c < k; }, timeout_ns, abort, done + 1) ? 1 : 0;
+            if (started_at && blockIdx.x == 0)
+                *started_at = globaltimer_ns();   // CTA 0 may record: the round's recording phase begins
+        }
+        grid_launch_dependents();
+    }
     __syncthreads();   // every tile of the CTA is stored ...
+    if (kTwoAreas && s_skip_rec)
+        return;
     if (threadIdx.x < 32) {
         for (int64_t j0 = 0; j0 < mine; j0 += 32)
             if (j0 + threadIdx.x < mine)
@@ -525,22 +567,38 @@ __global__ void __launch_bounds__(kPipeProducerThreads, 8)
 
 // Consumer of one round: sums the tile area mod 2^32 into *checksum; each
 // CTA, once its reads are done, records ADD 1 on `ack` (release), and the
-// next round's producer waits for all of them.  One record per CTA, no
-// returning atomic: nobody has to find out which CTA finished last.
+// producer that next writes this area waits for all of them.  One record per
+// CTA, no returning atomic: nobody has to find out which CTA finished last.
+// The record comes before the checksum's atomic add, so that its release
+// waits for the reads only.
 // It is launched with programmatic stream serialization behind the wait, so
 // its CTAs may be scheduled while the wait still polls: they first wait on the
-// device until the wait kernel has ended.
+// device until the wait kernel has ended.  Each thread issues four
+// independent loads at a time.
+//   kTwoAreas: the next round's wait is launched the same way behind this
+// kernel; once the CTA is past its own dependency wait (the wait before it,
+// and its clear, are complete), it lets that wait be scheduled.
 constexpr int kPipeConsumerThreads = 256;
 
+template <bool kTwoAreas>
 __global__ void __launch_bounds__(kPipeConsumerThreads, 8)
     pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words, uint32_t *checksum, uint32_t *ack)
 {
     grid_dependency_wait();
+    if (kTwoAreas)
+        grid_launch_dependents();
     const uint4 *t4 = reinterpret_cast<const uint4 *>(tiles);
     uint32_t s = 0;
     const int64_t n4 = n_words >> 2;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+#pragma unroll 1
+    for (; i + 3 * stride < n4; i += 4 * stride) {
+        const uint4 a = t4[i], b = t4[i + stride], c = t4[i + 2 * stride], d = t4[i + 3 * stride];
+        s += (a.x + a.y + a.z + a.w) + (b.x + b.y + b.z + b.w) + (c.x + c.y + c.z + c.w) + (d.x + d.y + d.z + d.w);
+    }
+#pragma unroll 1
+    for (; i < n4; i += stride) {
         const uint4 v = t4[i];
         s += v.x + v.y + v.z + v.w;
     }
@@ -558,8 +616,8 @@ __global__ void __launch_bounds__(kPipeConsumerThreads, 8)
         for (int o = 16; o > 0; o >>= 1)
             w += __shfl_xor_sync(0xffffffffu, w, o);
         if (threadIdx.x == 0) {
-            atomicAdd(checksum, w);
             cnt_record_device(ack, CNS_REC_ADD, 1u);   // ... before the CTA counts itself done (release)
+            atomicAdd(checksum, w);
         }
     }
 }
@@ -839,7 +897,8 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     if (!cfg->tiles_dev || !cfg->checksums_dev)
         return CNS_ERR_NULL_PTR;
     if (cfg->tiles < 1 || cfg->rounds < 0 || cfg->tile_words < 4 || cfg->tile_words > 8192 ||
-        cfg->tile_words % 4 != 0 || cfg->producer_ctas < 0 || cfg->tiles > (int64_t(1) << 32) / cfg->tile_words)
+        cfg->tile_words % 4 != 0 || cfg->producer_ctas < 0 || cfg->tiles > (int64_t(1) << 32) / cfg->tile_words ||
+        cfg->areas < 0 || cfg->areas > 2)
         return CNS_ERR_INVALID_VALUE;
     if (reinterpret_cast<uintptr_t>(cfg->tiles_dev) & 15)
         return CNS_ERR_INVALID_VALUE;
@@ -854,16 +913,23 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     // Residency.  Producer CTAs wait on the device for the consumer's release
     // (ack), and the consumer's CTAs, scheduled early behind the stream wait,
     // wait on the device for that wait to end; neither group may keep the
-    // other from being placed.  Producer CTAs hold at most half of the GPU's
-    // thread slots, consumer CTAs at most a quarter, both at <= 32 registers
-    // a thread (launch bounds), so registers run in step with thread slots.
-    // A producer CTA (256 threads) that found no SM with room would need every
-    // SM to have more than (slots - 256) threads in use, i.e. more than 7/8 of
-    // the GPU, while everything here holds at most 3/4 plus two one-warp wait
-    // kernels.  (Work of other streams running at the same time can still
-    // starve a round; the bounded waits then end it with CNS_ERR_TIMEOUT.)
+    // other from being placed.  One area: the producer grid holds at most half
+    // of the GPU's thread slots, the consumer grid a quarter.  Two areas: a
+    // grid is scheduled early only once every CTA of the grid before it in its
+    // stream is past its own dependency wait, and every kernel of the pipeline
+    // waits for its predecessor before it ends, so at most two producer grids
+    // (an eighth each), two consumer grids (a quarter each) and one wait
+    // kernel are resident.  All CTAs run at <= 32 registers a thread (launch
+    // bounds), so registers run in step with thread slots.  A CTA (256
+    // threads) that found no SM with room would need every SM to have more
+    // than (slots - 256) threads in use, i.e. more than 7/8 of the GPU, while
+    // everything here holds at most 3/4 plus two one-warp wait kernels.  (Work
+    // of other streams running at the same time can still starve a round; the
+    // bounded waits then end it with CNS_ERR_TIMEOUT.)
+    const bool two = cfg->areas == 2;
     const int per_sm = dev.max_threads_per_sm > 0 ? dev.max_threads_per_sm : 2048;
-    const int64_t pcap = static_cast<int64_t>(dev.sm_count) * std::max(1, per_sm / 2 / kPipeProducerThreads);
+    const int pshare = two ? 8 : 2;   // a producer grid holds at most 1/pshare of the slots
+    const int64_t pcap = static_cast<int64_t>(dev.sm_count) * std::max(1, per_sm / pshare / kPipeProducerThreads);
     const int64_t pwant = cfg->producer_ctas ? cfg->producer_ctas : cfg->tiles;
     const int pgrid = static_cast<int>(std::max<int64_t>(1, std::min(std::min(pwant, pcap), cfg->tiles)));
     const int64_t n_words = cfg->tiles * cfg->tile_words;
@@ -879,6 +945,18 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     ccfg.stream = sc;
     ccfg.attrs = early;
     ccfg.numAttrs = 1;
+    cudaLaunchConfig_t wcfg = {};   // two areas: each wait behind the last consumer, scheduled early
+    wcfg.gridDim = dim3(1);
+    wcfg.blockDim = dim3(32);
+    wcfg.stream = sc;
+    wcfg.attrs = early;
+    wcfg.numAttrs = 1;
+    cudaLaunchConfig_t pcfg = {};   // two areas: each producer behind the last, scheduled early
+    pcfg.gridDim = dim3(pgrid);
+    pcfg.blockDim = dim3(kPipeProducerThreads);
+    pcfg.stream = sp;
+    pcfg.attrs = early;
+    pcfg.numAttrs = 1;
     cfg->consumer_ctas = cgrid;   // ack grows by this much per round
 
     std::vector<cudaEvent_t> ev;
@@ -939,17 +1017,38 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
         // after the work that releases it.  CUDA may feed both streams through
         // one hardware queue in submission order, and a wait ahead of its
         // record would then hold that record back until it timed out.
-        pipeline_producer_kernel<<<pgrid, kPipeProducerThreads, 0, sp>>>(
-            cfg->tiles_dev, cfg->tiles, cfg->tile_words, static_cast<uint32_t>(r),
-            static_cast<uint32_t>(r) * static_cast<uint32_t>(cgrid), done->line, ack->line, ack_timeout, abort,
-            stamps ? stamps + r : nullptr);
-        check(cudaGetLastError(), "producer launch");
-        if (int e = enqueue_wait(done, sc, &w_done, cfg->released_dev ? cfg->released_dev + r : nullptr, abort, true,
-                                 stamps ? stamps + cfg->rounds + r : nullptr))
-            rc = e;
-        check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel, static_cast<const uint32_t *>(cfg->tiles_dev),
-                                 n_words, cfg->checksums_dev + r, ack->line),
-              "consumer launch");
+        const uint32_t r32 = static_cast<uint32_t>(r);
+        uint32_t *area = cfg->tiles_dev + (two ? (r & 1) * n_words : 0);
+        uint64_t *started = stamps ? stamps + r : nullptr;
+        if (two) {
+            // the area was last read in round r - 2
+            check(cudaLaunchKernelEx(&pcfg, pipeline_producer_kernel<true>, area, cfg->tiles, cfg->tile_words, r32,
+                                     r >= 2, (r32 - 1u) * static_cast<uint32_t>(cgrid), done->line, ack->line,
+                                     ack_timeout, abort, started),
+                  "producer launch");
+        } else {
+            pipeline_producer_kernel<false><<<pgrid, kPipeProducerThreads, 0, sp>>>(
+                area, cfg->tiles, cfg->tile_words, r32, r >= 1, r32 * static_cast<uint32_t>(cgrid), done->line,
+                ack->line, ack_timeout, abort, started);
+            check(cudaGetLastError(), "producer launch");
+        }
+        uint32_t *observed = cfg->released_dev ? cfg->released_dev + r : nullptr;
+        uint64_t *released = stamps ? stamps + cfg->rounds + r : nullptr;
+        if (two) {
+            check(cudaLaunchKernelEx(&wcfg, cnt_wait_kernel<true, true>, done->line,
+                                     static_cast<uint32_t>(w_done.mode), w_done.value, 1u,
+                                     wait_timeout_ns(w_done.timeout), observed, abort, released),
+                  "wait launch");
+            check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel<true>, static_cast<const uint32_t *>(area),
+                                     n_words, cfg->checksums_dev + r, ack->line),
+                  "consumer launch");
+        } else {
+            if (int e = enqueue_wait(done, sc, &w_done, observed, abort, true, released))
+                rc = e;
+            check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel<false>, static_cast<const uint32_t *>(area),
+                                     n_words, cfg->checksums_dev + r, ack->line),
+                  "consumer launch");
+        }
     }
     check(cudaEventRecord(join, sc), "event");
     check(cudaStreamWaitEvent(sp, join, 0), "stream wait");

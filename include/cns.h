@@ -478,32 +478,42 @@ typedef struct {
                                 release to the consumer-side wait releasing (device clock) */
     int32_t device_status;   /* (out, sync=1) 0 or CNS_ERR_TIMEOUT */
     int32_t consumer_ctas;   /* (out) consumer CTAs per round (ack's increment per round) */
-    int32_t reserved[2];
+    int32_t areas;           /* (in) tile areas: 0 or 1 = one area of tiles * tile_words uint32 at
+                                tiles_dev; 2 = two such areas back to back (2 * tiles * tile_words
+                                uint32), round r writing and reading area r % 2 */
+    int32_t reserved;
 } cns_pipeline_t;
 
 /*
  * cns_pipeline_run -- `rounds` rounds of a producer and a consumer on two
  * streams that meet only through two counted notifies.
  *   producer stream: a producer kernel whose CTAs first wait on the device
- *     until ack >= round * consumer_ctas (every consumer CTA has finished
- *     reading the previous round), then write word w of the tile area as
+ *     until every consumer CTA that last read the round's tile area has
+ *     finished (one area: ack >= round * consumer_ctas; two areas:
+ *     ack >= (round - 1) * consumer_ctas), then write word w of the area as
  *     w * 2654435761 + round;
  *     CTA b writes tiles b, b + grid, ... and, once they are all stored,
  *     records ADD 1 on `done` from the device for each of them (one lane of
- *     one warp per tile, so the lanes' records travel as one L2 operation);
+ *     one warp per tile, so the lanes' records travel as one L2 operation).
+ *     With two areas a round's stores overlap the previous round's reads;
+ *     its records wait until the consumer-side wait has cleared the
+ *     previous round's count (the producer grid is launched behind the
+ *     previous one with programmatic stream serialization, waits on the
+ *     device for it to complete, then for done < tiles);
  *   consumer stream: cntnotify wait on `done` BIGGER_OR_EQUAL tiles with
- *     isClear = 1, then a consumer kernel that sums the tile area mod 2^32
- *     into checksums[round]; each of its CTAs records ADD 1 on `ack` once
- *     its reads are done.
+ *     isClear = 1, then a consumer kernel that sums the round's area mod
+ *     2^32 into checksums[round]; each of its CTAs records ADD 1 on `ack`
+ *     once its reads are done.
  *     The consumer is launched with programmatic stream serialization: its
  *     CTAs may be scheduled while the wait polls and wait on the device for
  *     it to end.  Grids are sized so that producer and consumer CTAs always
- *     fit on the GPU together (half and a quarter of its thread slots).
+ *     fit on the GPU together (producers half of its thread slots -- two
+ *     grids of a quarter each with two areas -- consumers a quarter).
  * The call first clears both notifies (count and status); `done` ends at 0
  * and `ack` at rounds * consumer_ctas (mod 2^32).  Once a wait times out the pipeline's remaining
  * waits return at once, so a lost signal costs one timeout, not one per round.
- * Errors: INVALID_HANDLE, NULL_PTR, INVALID_VALUE, CUDA; with sync=1 also
- * TIMEOUT.
+ * Errors: INVALID_HANDLE, NULL_PTR, INVALID_VALUE (also areas outside 0..2),
+ * CUDA; with sync=1 also TIMEOUT.
  */
 int cns_pipeline_run(cns_pipeline_t *cfg);
 

@@ -281,14 +281,16 @@ def test_statemachine_all_sets_and_invalid_ops(cns):
 
 # --- two-stream counting pipeline --------------------------------------------------------
 
-def test_pipeline_4096_tiles_1000_rounds(cns):
+@pytest.mark.parametrize("areas", [1, 2])
+def test_pipeline_4096_tiles_1000_rounds(cns, areas):
     import torch
     rc, done = cns.cntnotify_create(0)
     rc2, ack = cns.cntnotify_create(0)
     assert rc == rc2 == 0
     try:
         s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 4096, 256, 1000, s1, s2, timeout_s=10)
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 4096, 256, 1000, s1, s2, timeout_s=10,
+                                                        areas=areas)
         assert rc == 0 and cfg.device_status == 0
         want_cs, want_rel = oracle.pipeline(4096, 256, 1000)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
@@ -301,14 +303,15 @@ def test_pipeline_4096_tiles_1000_rounds(cns):
         cns.cntnotify_destroy(ack)
 
 
-def test_pipeline_small_odd_shapes(cns):
+@pytest.mark.parametrize("areas", [0, 1, 2])
+def test_pipeline_small_odd_shapes(cns, areas):
     import torch
     rc, done = cns.cntnotify_create(0)
     rc2, ack = cns.cntnotify_create(0)
     try:
         s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
         cfg, rc, checksums, released = cns.run_pipeline(done, ack, 7, 12, 5, s1, s2, timeout_s=10,
-                                                        producer_ctas=3)
+                                                        producer_ctas=3, areas=areas)
         assert rc == 0
         want_cs, want_rel = oracle.pipeline(7, 12, 5)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
@@ -326,14 +329,15 @@ def test_pipeline_small_odd_shapes(cns):
     (40, 8192, 6, 0),          # large tiles, 2048 uint4 each
     (1, 4, 3, 0),              # one tile
 ])
-def test_pipeline_producer_grids(cns, tiles, tile_words, rounds, producer_ctas):
+@pytest.mark.parametrize("areas", [1, 2])
+def test_pipeline_producer_grids(cns, tiles, tile_words, rounds, producer_ctas, areas):
     import torch
     rc, done = cns.cntnotify_create(0)
     rc2, ack = cns.cntnotify_create(0)
     try:
         s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
         cfg, rc, checksums, released = cns.run_pipeline(done, ack, tiles, tile_words, rounds, s1, s2, timeout_s=10,
-                                                        producer_ctas=producer_ctas)
+                                                        producer_ctas=producer_ctas, areas=areas)
         assert rc == 0 and cfg.device_status == 0
         want_cs, want_rel = oracle.pipeline(tiles, tile_words, rounds)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
@@ -372,7 +376,8 @@ def test_grid_sync_probe_ring_rotate(cns):
     np.testing.assert_array_equal(from_dev_u32(b1).reshape(148, 4), np.roll(v0, -1001, axis=0))
 
 
-def test_pipeline_on_one_stream(cns):
+@pytest.mark.parametrize("areas", [1, 2])
+def test_pipeline_on_one_stream(cns, areas):
     """Producer and consumer on the same stream: every device wait is then
     already satisfied when it starts, and the result is the same."""
     import torch
@@ -380,11 +385,58 @@ def test_pipeline_on_one_stream(cns):
     rc2, ack = cns.cntnotify_create(0)
     try:
         s = torch.cuda.Stream()
-        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 300, 64, 12, s, s, timeout_s=10)
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 300, 64, 12, s, s, timeout_s=10, areas=areas)
         assert rc == 0 and cfg.device_status == 0
         want_cs, want_rel = oracle.pipeline(300, 64, 12)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
         np.testing.assert_array_equal(from_dev_u32(released), want_rel)
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
+
+
+@pytest.mark.parametrize("rounds", [1, 2, 7, 8])
+def test_pipeline_two_areas_hold_the_last_two_rounds(cns, rounds):
+    """With two areas, round r writes area r % 2: after the run the area of the
+    last round holds its words and the other area those of the round before
+    (or is untouched after a single round)."""
+    import torch
+    tiles, words = 96, 16
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    try:
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        buf = torch.full((2 * tiles * words,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+        cs = torch.empty(rounds, dtype=torch.int32, device="cuda")
+        rel = torch.empty(rounds, dtype=torch.int32, device="cuda")
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, tiles, words, rounds, s1, s2, timeout_s=10,
+                                                        buffers=(buf, cs, rel), areas=2)
+        assert rc == 0 and cfg.device_status == 0
+        got = from_dev_u32(buf).reshape(2, tiles * words)
+        w = np.arange(tiles * words, dtype=np.uint64)
+        for r in (rounds - 1, rounds - 2):
+            if r >= 0:
+                want = np.array([oracle.pipeline_word(int(x), r) for x in w], dtype=np.uint32)
+                np.testing.assert_array_equal(got[r % 2], want)
+        if rounds == 1:
+            assert (got[1] == 0x5A5A5A5A).all()
+        want_cs, want_rel = oracle.pipeline(tiles, words, rounds)
+        np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
+        np.testing.assert_array_equal(from_dev_u32(released), want_rel)
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
+
+
+def test_pipeline_rejects_bad_area_count(cns):
+    import torch
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    try:
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        for areas in (-1, 3):
+            cfg, rc, _, _ = cns.run_pipeline(done, ack, 8, 4, 2, s1, s2, timeout_s=10, areas=areas)
+            assert rc == cns.CNS_ERR_INVALID_VALUE
     finally:
         cns.cntnotify_destroy(done)
         cns.cntnotify_destroy(ack)
