@@ -105,7 +105,8 @@ def time_oracle(budget_s: float):
 def time_twin():
     """The multithreaded CPU timing twin on all host cores, beside the GPU figures:
     the headline ring (148 participants, 100000 rounds), Jacobi at N = 2^26 for 200
-    sweeps, and the two-thread pipeline (4096 tiles x 256 words, 100 rounds)."""
+    sweeps, and the two-thread pipeline (4096 tiles x 256 words, 100 rounds, two tile
+    areas as on the GPU, and one)."""
     from oracle import twin
     twin.build()
     T = twin.host_threads()
@@ -117,14 +118,16 @@ def time_twin():
     _, jsec = twin.jacobi(u0, S, T)
     del u0
     n = 4096 * 256
-    cs, psec = twin.pipeline(4096, 256, 100)
     want = np.array([(2654435761 * (n * (n - 1) // 2) + n * r) % (1 << 32) for r in range(100)], dtype=np.uint32)
+    cs, psec = twin.pipeline(4096, 256, 100, areas=2)
+    cs1, psec1 = twin.pipeline(4096, 256, 100, areas=1)
     return {"kind": "multithreaded CPU timing twin (pthreads, C11 atomics, the pages' epoch barrier among threads)",
             "threads": T,
             "soft_148_ring_rotate_ns_per_round": round(sec * 1e9 / ROUNDS_HEAD, 1), "ring_correct": bool(ok_ring),
             "jacobi_2p26_200sweeps_gbs": round(S * 8 * N / jsec / 1e9, 1),
             "pipeline_4096x256_round_trips_per_s": round(100 / psec, 1),
-            "pipeline_correct": bool(np.array_equal(cs, want))}
+            "pipeline_one_area_round_trips_per_s": round(100 / psec1, 1),
+            "pipeline_correct": bool(np.array_equal(cs, want) and np.array_equal(cs1, want))}
 
 
 def run_reference(args):

@@ -267,18 +267,29 @@ typedef struct {
     _Alignas(128) atomic_uint ack;
     uint32_t *tiles;
     int64_t n_tiles, rounds;
-    int tile_words;
+    int tile_words, areas;
     uint32_t *checksums;
 } pipe_t;
 
+/* Round r writes area r % areas.  With one area the producer waits until the
+ * consumer has read round r - 1; with two, until it has read round r - 2 (the
+ * area's last use) and has cleared round r - 1's count, which every record of
+ * round r must follow. */
 static void *pipe_producer(void *arg)
 {
     pipe_t *p = (pipe_t *)arg;
+    const int64_t n = p->n_tiles * p->tile_words;
     for (int64_t r = 0; r < p->rounds; ++r) {
-        while (atomic_load_explicit(&p->ack, memory_order_acquire) < (uint32_t)r) {
+        const uint32_t need = p->areas == 2 ? (r >= 1 ? (uint32_t)(r - 1) : 0u) : (uint32_t)r;
+        while (atomic_load_explicit(&p->ack, memory_order_acquire) < need) {
         }
+        if (p->areas == 2) {
+            while (atomic_load_explicit(&p->done, memory_order_acquire) >= (uint32_t)p->n_tiles) {
+            }
+        }
+        uint32_t *area = p->tiles + (p->areas == 2 ? (r & 1) * n : 0);
         for (int64_t t = 0; t < p->n_tiles; ++t) {
-            uint32_t *d = p->tiles + t * p->tile_words;
+            uint32_t *d = area + t * p->tile_words;
             const uint32_t w0 = (uint32_t)(t * p->tile_words);
             for (int i = 0; i < p->tile_words; ++i)
                 d[i] = (w0 + (uint32_t)i) * 2654435761u + (uint32_t)r;
@@ -295,30 +306,32 @@ static void pipe_consume(pipe_t *p)
         while (atomic_load_explicit(&p->done, memory_order_acquire) < (uint32_t)p->n_tiles) {
         }
         atomic_store_explicit(&p->done, 0u, memory_order_relaxed);              /* isClear */
+        const uint32_t *area = p->tiles + (p->areas == 2 ? (r & 1) * n : 0);
         uint32_t s = 0;
         for (int64_t i = 0; i < n; ++i)
-            s += p->tiles[i];
+            s += area[i];
         p->checksums[r] = s;
         atomic_store_explicit(&p->ack, (uint32_t)(r + 1), memory_order_release);   /* record SET r + 1 */
     }
 }
 
-/* `rounds` rounds of the two-thread pipeline over tiles x tile_words words.
- * Out: checksums[rounds], seconds of the whole run. */
-int twin_pipeline(int64_t n_tiles, int tile_words, int64_t rounds, uint32_t *checksums, double *seconds)
+/* `rounds` rounds of the two-thread pipeline over tiles x tile_words words in
+ * `areas` (1 or 2) tile areas.  Out: checksums[rounds], seconds of the whole run. */
+int twin_pipeline(int64_t n_tiles, int tile_words, int64_t rounds, int areas, uint32_t *checksums, double *seconds)
 {
-    if (n_tiles < 1 || tile_words < 1 || rounds < 0 || !checksums || !seconds)
+    if (n_tiles < 1 || tile_words < 1 || rounds < 0 || !checksums || !seconds || areas < 1 || areas > 2)
         return TW_BAD_ARG;
     if (n_tiles > ((int64_t)1 << 32) / tile_words)
         return TW_BAD_ARG;
     pipe_t p;
     atomic_init(&p.done, 0u);
     atomic_init(&p.ack, 0u);
-    p.tiles = malloc((size_t)(n_tiles * tile_words) * sizeof(uint32_t));
+    p.tiles = malloc((size_t)(areas * n_tiles * tile_words) * sizeof(uint32_t));
     if (!p.tiles)
         return TW_NO_THREAD;
     p.n_tiles = n_tiles;
     p.tile_words = tile_words;
+    p.areas = areas;
     p.rounds = rounds;
     p.checksums = checksums;
     pthread_t prod;

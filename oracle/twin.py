@@ -49,7 +49,7 @@ def lib() -> ctypes.CDLL:
             L.twin_syncall_ring.restype = i32
             L.twin_jacobi.argtypes = [vp, vp, i64, i64, i32, dp]
             L.twin_jacobi.restype = i32
-            L.twin_pipeline.argtypes = [i64, i32, i64, vp, dp]
+            L.twin_pipeline.argtypes = [i64, i32, i64, i32, vp, dp]
             L.twin_pipeline.restype = i32
             _lib = L
     return _lib
@@ -88,11 +88,11 @@ def jacobi(u0: np.ndarray, sweeps: int, threads: int):
     return b[sweeps & 1], sec.value
 
 
-def pipeline(tiles: int, tile_words: int, rounds: int):
-    """(checksums[rounds], seconds) of the two-thread pipeline."""
+def pipeline(tiles: int, tile_words: int, rounds: int, areas: int = 1):
+    """(checksums[rounds], seconds) of the two-thread pipeline over `areas` tile areas."""
     cs = np.zeros(rounds, dtype=np.uint32)
     sec = ctypes.c_double()
-    rc = lib().twin_pipeline(tiles, tile_words, rounds, cs.ctypes.data, ctypes.byref(sec))
+    rc = lib().twin_pipeline(tiles, tile_words, rounds, areas, cs.ctypes.data, ctypes.byref(sec))
     if rc != 0:
         raise RuntimeError(f"twin_pipeline: {rc}")
     return cs, sec.value

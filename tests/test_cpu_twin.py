@@ -29,9 +29,10 @@ def test_twin_jacobi_matches_oracle(n, sweeps, threads):
     np.testing.assert_array_equal(got, want)
 
 
-@pytest.mark.parametrize("tiles,tile_words,rounds", [(64, 8, 5), (7, 12, 9), (1, 4, 3)])
-def test_twin_pipeline_matches_oracle(tiles, tile_words, rounds):
-    cs, sec = twin.pipeline(tiles, tile_words, rounds)
+@pytest.mark.parametrize("areas", [1, 2])
+@pytest.mark.parametrize("tiles,tile_words,rounds", [(64, 8, 5), (7, 12, 9), (1, 4, 3), (300, 16, 40)])
+def test_twin_pipeline_matches_oracle(tiles, tile_words, rounds, areas):
+    cs, sec = twin.pipeline(tiles, tile_words, rounds, areas)
     want, _ = oracle.pipeline(tiles, tile_words, rounds)
     np.testing.assert_array_equal(cs, want)
 
@@ -41,3 +42,5 @@ def test_twin_rejects_bad_arguments():
         twin.syncall_ring(9, np.zeros((2, 2), np.uint32), 1, 1)
     with pytest.raises(RuntimeError):
         twin.pipeline(0, 4, 1)
+    with pytest.raises(RuntimeError):
+        twin.pipeline(4, 4, 1, areas=3)
