@@ -222,35 +222,58 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 // than the one link word per 4096-op tile the kernel uses.
 constexpr int kChunk = 16;
 
-// An op packed into 8 bytes: x = value, y = kind code (0 record, 1 wait,
-// 2 anything else) | mode (clamped to 7, which no kind accepts) << 2 |
-// is_clear << 5.  Nothing the rules look at is lost.
-__device__ __forceinline__ uint2 sm_pack(const uint4 &op)
+// An op turned into a micro-op that one short branch-free sequence applies
+// (neighbouring lanes of a warp apply different kinds and modes):
+//   x  AND mask a (record) / compare mask (wait: the value for
+//      EQUAL_WITH_BITMASK, all ones otherwise)
+//   y  OR value o (record) / compare value (wait)
+//   z  addend d (record) / 0 (wait)
+//   w  flags: bits 0-2 the compare results that release a wait (1 below,
+//      2 equal, 4 above), bits 4-6 the same when the wait also clears, bit 8
+//      wait, bits 9-10 the outcome of anything else (CNS_OUT_RECORD or
+//      CNS_OUT_INVALID), bit 11 SET.
+// A record makes the count ((c & a) | o) + d: SET v is (0, v, 0), ADD v
+// (~0, 0, v), OR v (~0, v, 0), AND v (v, 0, 0).  A wait compares (c & mask)
+// with its value: LESS releases below, EQUAL and EQUAL_WITH_BITMASK on equal,
+// BIGGER above, BIGGER_OR_EQUAL on equal or above.  An op of no valid kind
+// and mode is the record (~0, 0, 0) with outcome CNS_OUT_INVALID.
+constexpr uint32_t kMicroWait = 1u << 8;
+constexpr uint32_t kMicroSet = 1u << 11;
+
+__device__ __forceinline__ uint4 sm_micro(const uint4 &op)
 {
-    const uint32_t kind = op.x == 0u ? 0u : (op.x == 1u ? 1u : 2u);
-    const uint32_t mode = op.y < 7u ? op.y : 7u;
-    return make_uint2(op.z, kind | (mode << 2) | ((op.w != 0u ? 1u : 0u) << 5));
+    const uint32_t kind = op.x, mode = op.y, v = op.z;
+    const bool clear = op.w != 0u;
+    const uint32_t rec = static_cast<uint32_t>(CNS_OUT_RECORD) << 9;
+    if (kind == 0u) {
+        switch (mode) {
+        case CNS_REC_SET: return make_uint4(0u, v, 0u, rec | kMicroSet);
+        case CNS_REC_ADD: return make_uint4(~0u, 0u, v, rec);
+        case CNS_REC_BIT_OR: return make_uint4(~0u, v, 0u, rec);
+        case CNS_REC_BIT_AND: return make_uint4(v, 0u, 0u, rec);
+        default: break;
+        }
+    } else if (kind == 1u && mode <= 4u) {
+        const uint32_t bits = mode == CNS_WAIT_LESS ? 1u
+                            : mode == CNS_WAIT_BIGGER ? 4u
+                            : mode == CNS_WAIT_BIGGER_OR_EQUAL ? 6u
+                                                               : 2u;   // EQUAL, EQUAL_WITH_BITMASK
+        const uint32_t mask = mode == CNS_WAIT_EQUAL_WITH_BITMASK ? v : ~0u;
+        return make_uint4(mask, v, 0u, bits | (clear ? bits << 4 : 0u) | kMicroWait);
+    }
+    return make_uint4(~0u, 0u, 0u, static_cast<uint32_t>(CNS_OUT_INVALID) << 9);
 }
 
-// One packed op applied to count c.  Branch-free: neighbouring lanes of a
-// warp apply different kinds and modes, so every candidate is computed and
-// the right one selected.
-__device__ __forceinline__ uint32_t sm_apply_packed(uint32_t c, const uint2 op, uint32_t *outcome)
+// One micro-op applied to count c; *outcome gets the op's CNS_OUT_* code.
+__device__ __forceinline__ uint32_t sm_apply_micro(uint32_t c, const uint4 m, uint32_t *outcome)
 {
-    const uint32_t kind = op.y & 3u, mode = (op.y >> 2) & 7u, v = op.x;
-    const bool clear = ((op.y >> 5) & 1u) != 0u;
-    const bool rec = kind == 0u && cnt_record_valid(mode);
-    const bool wait = kind == 1u && mode <= 4u;
-    const uint32_t after_rec = cnt_record_apply(c, mode, v);
-    const bool rel = cnt_wait_released(c, mode, v);
-    const uint32_t after_wait = (rel && clear) ? 0u : c;
-    *outcome = rec ? static_cast<uint32_t>(CNS_OUT_RECORD)
-             : wait ? static_cast<uint32_t>(rel ? CNS_OUT_WAIT_RELEASED : CNS_OUT_WAIT_HELD)
-                    : static_cast<uint32_t>(CNS_OUT_INVALID);
-    return rec ? after_rec : wait ? after_wait : c;
+    const uint32_t x = c & m.x;
+    const uint32_t idx = (x > m.y ? 1u : 0u) + (x >= m.y ? 1u : 0u);   // 0 below, 1 equal, 2 above
+    const uint32_t f = m.w >> idx;   // a record's bits 0-6 are 0: it is never released nor cleared
+    const uint32_t keep = (m.w & kMicroWait) ? c : (x | m.y) + m.z;
+    *outcome = (f & 1u) + ((m.w >> 9) & 3u);   // a wait: HELD (0) or RELEASED (1)
+    return (f & 16u) ? 0u : keep;
 }
-
-__device__ __forceinline__ bool is_set_packed(const uint2 op) { return (op.y & 0x1Fu) == 0u; }   // record, SET
 
 constexpr uint64_t kSmLinkTimeoutNs = 10ull * 1000000000ull;
 
@@ -280,31 +303,42 @@ __device__ __forceinline__ bool sm_take(const uint64_t *link, uint32_t tag, uint
     }
 }
 
-// Tile shape: 512 threads x chunks of 8 ops, ops packed to 8 bytes in shared
-// memory with a one-entry pad per chunk (conflict-free per-thread walks).
+// Tile shape: 512 threads x chunks of 8 ops, micro-ops in shared memory with
+// a one-entry pad per chunk (conflict-free per-thread walks), and a bit per op
+// telling whether it is a SET, gathered by warp ballots while staging: 32
+// consecutive ops per word, byte j of word w covering chunk 4w + j.
 constexpr int kFChunk = 8;
 constexpr int kFThreads = 512;
 constexpr int kTileOps = kFChunk * kFThreads;
 constexpr int kFPad = kFChunk + 1;
-constexpr size_t kFSmemBytes = static_cast<size_t>(kFThreads) * kFPad * 2 * sizeof(uint2);
+constexpr size_t kFSmemBytes = static_cast<size_t>(kFThreads) * kFPad * (sizeof(uint4) + sizeof(uint2)) +
+                               kTileOps / 32 * sizeof(uint32_t);
 
 __device__ __forceinline__ int f_slot(int i) { return (i / kFChunk) * kFPad + (i % kFChunk); }
+
+// Index of the first SET in chunk j (-1 if none) from the tile's SET bits.
+__device__ __forceinline__ int f_first_set(const uint32_t *s_setm, int j)
+{
+    const uint32_t byte = (s_setm[j >> 2] >> ((j & 3) * 8)) & 0xFFu;
+    return __ffs(byte) - 1;
+}
 
 __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *ops, int64_t n, uint32_t init,
                                                                   uint2 *trace, uint64_t *link, uint32_t tag,
                                                                   uint32_t *final_count)
 {
-    extern __shared__ uint2 f_smem[];
-    uint2 *s_ops = f_smem;
-    uint2 *s_tr = f_smem + kFThreads * kFPad;
-    __shared__ int s_first[kFThreads];   // index of the chunk's first SET, -1 if none
+    extern __shared__ uint4 f_smem[];
+    uint4 *s_ops = f_smem;
+    uint2 *s_tr = reinterpret_cast<uint2 *>(f_smem + kFThreads * kFPad);
+    uint32_t *s_setm = reinterpret_cast<uint32_t *>(s_tr + kFThreads * kFPad);
     __shared__ int s_wmin[kFThreads / 32];
     const int64_t tiles = (n + kTileOps - 1) / kTileOps;
     const int k = threadIdx.x;
+    const int lane = k & 31;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t base = t * kTileOps;
         const int cnt = (n - base < kTileOps) ? static_cast<int>(n - base) : kTileOps;
-        {   // stage: the 8 loads of a thread in flight four at a time, packed on the way in
+        {   // stage: the 8 loads of a thread in flight four at a time, turned into micro-ops on the way in
             const uint4 *src = ops + base;
 #pragma unroll
             for (int h = 0; h < kFChunk; h += 4) {
@@ -312,14 +346,17 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int i = k + (h + j) * kFThreads;
-                    if (i < cnt)
-                        v[j] = __ldg(src + i);
+                    v[j] = i < cnt ? __ldg(src + i) : make_uint4(2u, 0u, 0u, 0u);   // past the end: no SET
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int i = k + (h + j) * kFThreads;
+                    const uint4 m = sm_micro(v[j]);
                     if (i < cnt)
-                        s_ops[f_slot(i)] = sm_pack(v[j]);
+                        s_ops[f_slot(i)] = m;
+                    const uint32_t sets = __ballot_sync(0xffffffffu, (m.w & kMicroSet) != 0u);
+                    if (lane == 0)
+                        s_setm[i >> 5] = sets;
                 }
             }
         }
@@ -331,32 +368,28 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
         if (k < nchunks) {   // A
             const int off = k * kFPad;
             const int m = (cnt - k * kFChunk < kFChunk) ? cnt - k * kFChunk : kFChunk;
-#pragma unroll
-            for (int q = kFChunk - 1; q >= 0; --q)   // all looks at once: the first SET wins
-                if (q < m && is_set_packed(s_ops[off + q]))
-                    first = q;
+            first = f_first_set(s_setm, k);
             for (int q = (first < 0 ? m : first); q < m; ++q) {
                 uint32_t o;
-                c = sm_apply_packed(c, s_ops[off + q], &o);
+                c = sm_apply_micro(c, s_ops[off + q], &o);
                 s_tr[off + q] = make_uint2(c, o);
             }
         }
-        s_first[k] = first;
         {   // the tile's first chunk with a SET: a ballot per warp, then the warps' minimum
             const uint32_t has = __ballot_sync(0xffffffffu, first >= 0);
-            if ((k & 31) == 0)
+            if (lane == 0)
                 s_wmin[k >> 5] = has ? (k & ~31) + __ffs(has) - 1 : kFThreads;
         }
         __syncthreads();
         if (first >= 0) {   // B
             int j = k + 1;
             for (; j < nchunks; ++j) {
-                const int fj = s_first[j];
+                const int fj = f_first_set(s_setm, j);
                 const int off = j * kFPad;
                 const int m = fj >= 0 ? fj : ((cnt - j * kFChunk < kFChunk) ? cnt - j * kFChunk : kFChunk);
                 for (int q = 0; q < m; ++q) {
                     uint32_t o;
-                    c = sm_apply_packed(c, s_ops[off + q], &o);
+                    c = sm_apply_micro(c, s_ops[off + q], &o);
                     s_tr[off + q] = make_uint2(c, o);
                 }
                 if (fj >= 0)
@@ -372,13 +405,13 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
             int fc = kFThreads;
             for (int w = 0; w < kFThreads / 32; ++w)
                 fc = s_wmin[w] < fc ? s_wmin[w] : fc;
-            const int lead = fc < nchunks ? fc * kFChunk + s_first[fc] : cnt;
+            const int lead = fc < nchunks ? fc * kFChunk + f_first_set(s_setm, fc) : cnt;
             uint32_t cp = init;
             const bool ok = t == 0 || sm_take(link + t - 1, tag, &cp);
             for (int i = 0; i < lead; ++i) {
                 uint32_t o;
                 if (ok) {
-                    cp = sm_apply_packed(cp, s_ops[f_slot(i)], &o);
+                    cp = sm_apply_micro(cp, s_ops[f_slot(i)], &o);
                 } else {
                     cp = 0u;
                     o = CNS_OUT_INVALID;
