@@ -198,18 +198,17 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 // One persistent cooperative launch.  The stream is cut into tiles of 4096
 // ops; CTA b takes tiles b, b + grid, b + 2 grid, ...  Within a tile, 512
 // threads each own a chunk of 8 ops:
-//   A  every chunk with a SET traces from its first SET to its end;
-//   B  the thread of such a chunk carries its end count on through the
-//      following chunks up to the next SET; the chain that reaches the tile's
-//      end publishes the tile's end count (tagged with this call's tag) for
-//      the next tile;
+//   A  the thread of every chunk with a SET walks from the chunk's first SET
+//      up to the tile's next SET after the chunk (or the tile's end, in which
+//      case it publishes the tile's end count, tagged with this call's tag,
+//      for the next tile) -- one contiguous stretch of ops per thread;
 //   C  thread 0 takes the previous tile's end count (init for tile 0),
 //      waiting on the device until it is published, and replays the ops in
 //      front of the tile's first SET -- all of them if the tile has none, in
 //      which case it publishes the tile's end count itself.
-// Every op is applied exactly once, in stream order along its chain.  A tile
-// with a SET publishes before it waits, so a wait lasts only as long as a run
-// of SET-free tiles in front of it.  Every CTA is resident (cooperative
+// Every op is applied exactly once, in stream order along its stretch.  A
+// tile with a SET publishes before it waits, so a wait lasts only as long as
+// a run of SET-free tiles in front of it.  Every CTA is resident (cooperative
 // launch) and takes its tiles in increasing order, so the tile a CTA waits
 // for is always held by a running CTA (or done).  The tag makes the link words
 // need no initial content: a word holds (tag << 32) | count, and a word from
@@ -316,11 +315,30 @@ constexpr size_t kFSmemBytes = static_cast<size_t>(kFThreads) * kFPad * (sizeof(
 
 __device__ __forceinline__ int f_slot(int i) { return (i / kFChunk) * kFPad + (i % kFChunk); }
 
-// Index of the first SET in chunk j (-1 if none) from the tile's SET bits.
-__device__ __forceinline__ int f_first_set(const uint32_t *s_setm, int j)
+// Position of the tile's first SET at or after `from` (cnt if none) from the
+// tile's SET bits; positions at or past cnt carry no SET bit.
+__device__ __forceinline__ int f_next_set(const uint32_t *s_setm, int from, int cnt)
 {
-    const uint32_t byte = (s_setm[j >> 2] >> ((j & 3) * 8)) & 0xFFu;
-    return __ffs(byte) - 1;
+    if (from >= cnt)
+        return cnt;
+    int w = from >> 5;
+    uint32_t bits = s_setm[w] & (~0u << (from & 31));
+    while (bits == 0u && ++w < kTileOps / 32)
+        bits = s_setm[w];
+    return bits ? (w << 5) + __ffs(bits) - 1 : cnt;
+}
+
+// Apply ops [p, end) of the tile to count c, writing their trace entries.
+__device__ __forceinline__ uint32_t f_walk(const uint4 *s_ops, uint2 *s_tr, int p, int end, uint32_t c)
+{
+    int slot = f_slot(p);
+    for (; p < end; ++p) {
+        uint32_t o;
+        c = sm_apply_micro(c, s_ops[slot], &o);
+        s_tr[slot] = make_uint2(c, o);
+        slot += (p & (kFChunk - 1)) == kFChunk - 1 ? 2 : 1;   // step over the chunk's pad entry
+    }
+    return c;
 }
 
 __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *ops, int64_t n, uint32_t init,
@@ -331,7 +349,6 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
     uint4 *s_ops = f_smem;
     uint2 *s_tr = reinterpret_cast<uint2 *>(f_smem + kFThreads * kFPad);
     uint32_t *s_setm = reinterpret_cast<uint32_t *>(s_tr + kFThreads * kFPad);
-    __shared__ int s_wmin[kFThreads / 32];
     const int64_t tiles = (n + kTileOps - 1) / kTileOps;
     const int k = threadIdx.x;
     const int lane = k & 31;
@@ -362,63 +379,30 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
         }
         __syncthreads();
         const bool last_tile = base + cnt == n;
-        const int nchunks = (cnt + kFChunk - 1) / kFChunk;
-        int first = -1;
-        uint32_t c = 0;
-        if (k < nchunks) {   // A
-            const int off = k * kFPad;
-            const int m = (cnt - k * kFChunk < kFChunk) ? cnt - k * kFChunk : kFChunk;
-            first = f_first_set(s_setm, k);
-            for (int q = (first < 0 ? m : first); q < m; ++q) {
-                uint32_t o;
-                c = sm_apply_micro(c, s_ops[off + q], &o);
-                s_tr[off + q] = make_uint2(c, o);
-            }
-        }
-        {   // the tile's first chunk with a SET: a ballot per warp, then the warps' minimum
-            const uint32_t has = __ballot_sync(0xffffffffu, first >= 0);
-            if (lane == 0)
-                s_wmin[k >> 5] = has ? (k & ~31) + __ffs(has) - 1 : kFThreads;
-        }
-        __syncthreads();
-        if (first >= 0) {   // B
-            int j = k + 1;
-            for (; j < nchunks; ++j) {
-                const int fj = f_first_set(s_setm, j);
-                const int off = j * kFPad;
-                const int m = fj >= 0 ? fj : ((cnt - j * kFChunk < kFChunk) ? cnt - j * kFChunk : kFChunk);
-                for (int q = 0; q < m; ++q) {
-                    uint32_t o;
-                    c = sm_apply_micro(c, s_ops[off + q], &o);
-                    s_tr[off + q] = make_uint2(c, o);
+        const int chunk0 = k * kFChunk;
+        if (chunk0 < cnt) {   // A
+            const int start = f_next_set(s_setm, chunk0, cnt);
+            if (start < chunk0 + kFChunk && start < cnt) {   // the chunk has a SET
+                const int end = f_next_set(s_setm, chunk0 + kFChunk, cnt);
+                const uint32_t c = f_walk(s_ops, s_tr, start, end, 0u);   // starts with a SET: any count will do
+                if (end >= cnt) {
+                    sm_publish(link + t, tag, c);
+                    if (last_tile)
+                        *final_count = c;
                 }
-                if (fj >= 0)
-                    break;
-            }
-            if (j >= nchunks) {
-                sm_publish(link + t, tag, c);
-                if (last_tile)
-                    *final_count = c;
             }
         }
         if (k == 0) {   // C
-            int fc = kFThreads;
-            for (int w = 0; w < kFThreads / 32; ++w)
-                fc = s_wmin[w] < fc ? s_wmin[w] : fc;
-            const int lead = fc < nchunks ? fc * kFChunk + f_first_set(s_setm, fc) : cnt;
+            const int lead = f_next_set(s_setm, 0, cnt);
             uint32_t cp = init;
-            const bool ok = t == 0 || sm_take(link + t - 1, tag, &cp);
-            for (int i = 0; i < lead; ++i) {
-                uint32_t o;
-                if (ok) {
-                    cp = sm_apply_micro(cp, s_ops[f_slot(i)], &o);
-                } else {
-                    cp = 0u;
-                    o = CNS_OUT_INVALID;
-                }
-                s_tr[f_slot(i)] = make_uint2(cp, o);
+            if (t == 0 || sm_take(link + t - 1, tag, &cp)) {
+                cp = f_walk(s_ops, s_tr, 0, lead, cp);
+            } else {
+                for (int i = 0; i < lead; ++i)
+                    s_tr[f_slot(i)] = make_uint2(0u, CNS_OUT_INVALID);
+                cp = 0u;
             }
-            if (fc >= nchunks) {
+            if (lead >= cnt) {
                 sm_publish(link + t, tag, cp);
                 if (last_tile)
                     *final_count = cp;
