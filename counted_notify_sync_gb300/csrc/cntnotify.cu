@@ -195,8 +195,8 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 // on what came before, so the stream can be cut at SETs: from a SET on, the
 // trace can be computed without knowing the earlier count.
 //
-// One persistent cooperative launch.  The stream is cut into tiles of 4096
-// ops; CTA b takes tiles b, b + grid, b + 2 grid, ...  Within a tile, 512
+// One persistent cooperative launch.  The stream is cut into tiles of up to
+// 4096 ops; CTA b takes tiles b, b + grid, b + 2 grid, ...  Within a tile, 512
 // threads each own a chunk of 8 ops:
 //   A  the thread of every chunk with a SET walks from the chunk's first SET
 //      up to the tile's next SET after the chunk (or the tile's end, in which
@@ -217,8 +217,9 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 // outcome CNS_OUT_INVALID.
 // ---------------------------------------------------------------------------
 
-// Granularity of cns_statemachine_scratch_bytes (8 bytes per 16 ops): more
-// than the one link word per 4096-op tile the kernel uses.
+// Granularity of cns_statemachine_scratch_bytes (8 bytes per 16 ops): at
+// least the one link word per tile the kernel uses (a tile holds 16 ops or
+// more).
 constexpr int kChunk = 16;
 
 // An op turned into a micro-op that one short branch-free sequence applies
@@ -341,20 +342,20 @@ __device__ __forceinline__ uint32_t f_walk(const uint4 *s_ops, uint2 *s_tr, int 
     return c;
 }
 
-__global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *ops, int64_t n, uint32_t init,
-                                                                  uint2 *trace, uint64_t *link, uint32_t tag,
-                                                                  uint32_t *final_count)
+__global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *ops, int64_t n, int tile_ops,
+                                                                  uint32_t init, uint2 *trace, uint64_t *link,
+                                                                  uint32_t tag, uint32_t *final_count)
 {
     extern __shared__ uint4 f_smem[];
     uint4 *s_ops = f_smem;
     uint2 *s_tr = reinterpret_cast<uint2 *>(f_smem + kFThreads * kFPad);
     uint32_t *s_setm = reinterpret_cast<uint32_t *>(s_tr + kFThreads * kFPad);
-    const int64_t tiles = (n + kTileOps - 1) / kTileOps;
+    const int64_t tiles = (n + tile_ops - 1) / tile_ops;
     const int k = threadIdx.x;
     const int lane = k & 31;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int64_t base = t * kTileOps;
-        const int cnt = (n - base < kTileOps) ? static_cast<int>(n - base) : kTileOps;
+        const int64_t base = t * tile_ops;
+        const int cnt = (n - base < tile_ops) ? static_cast<int>(n - base) : tile_ops;
         {   // stage: the 8 loads of a thread in flight four at a time, turned into micro-ops on the way in
             const uint4 *src = ops + base;
 #pragma unroll
@@ -444,25 +445,34 @@ static int sm_prepare(int device)
 }
 
 // One state-machine run (n > 0): one cooperative launch of at most as many
-// CTAs as fit at once.  `link` needs one 8-byte word per 4096-op tile.
+// CTAs as fit at once.  A tile holds up to 4096 ops; when the GPU holds more
+// CTAs than that needs, the ops are spread evenly over all of them instead
+// (tiles of ceil(n / CTAs) ops rounded up to a multiple of 8, at least 16), so
+// that every SM gets the same share.  `link` needs one 8-byte word per tile,
+// at most one per 16 ops.
 static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, uint64_t *link, uint32_t *final_dev,
                      int device, cudaStream_t s)
 {
     if (int rc = sm_prepare(device))
         return rc;
-    const int64_t tiles = (n + kTileOps - 1) / kTileOps;
-    const int64_t grid = tiles < g_sm_max_ctas[device] ? tiles : g_sm_max_ctas[device];
+    const int64_t max_ctas = g_sm_max_ctas[device];
+    int64_t tile_ops = (n + max_ctas - 1) / max_ctas;
+    tile_ops = (tile_ops + kFChunk - 1) / kFChunk * kFChunk;
+    tile_ops = std::min<int64_t>(std::max<int64_t>(tile_ops, 16), kTileOps);
+    const int64_t tiles = (n + tile_ops - 1) / tile_ops;
+    const int64_t grid = tiles < max_ctas ? tiles : max_ctas;
     uint32_t tag = ++g_sm_tag;
     if (tag == 0)
         tag = ++g_sm_tag;
     const uint4 *a0 = ops;
     int64_t a1 = n;
-    uint32_t a2 = init;
-    uint2 *a3 = trace;
-    uint64_t *a4 = link;
-    uint32_t a5 = tag;
-    uint32_t *a6 = final_dev;
-    void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5, &a6};
+    int a2 = static_cast<int>(tile_ops);
+    uint32_t a3 = init;
+    uint2 *a4 = trace;
+    uint64_t *a5 = link;
+    uint32_t a6 = tag;
+    uint32_t *a7 = final_dev;
+    void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5, &a6, &a7};
     CNS_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(sm_onepass_kernel),
                                          dim3(static_cast<unsigned>(grid)), dim3(kFThreads), args, kFSmemBytes, s));
     return CNS_SUCCESS;

@@ -230,6 +230,18 @@ def test_statemachine_one_and_several_tiles_per_cta(cns, where):
     assert got_f == want_f
 
 
+@pytest.mark.parametrize("n", [17, 1000, 4863, 5000, 100_003, 999_999])
+def test_statemachine_spread_over_all_ctas(cns, n):
+    """Streams shorter than one 4096-op tile per resident CTA are cut into
+    tiles of ceil(n / CTAs) ops (a multiple of 8, at least 16): small tiles,
+    tiles that do not divide n, many tiles without a SET; bit for bit."""
+    ops = ci.notify_ops(n, seed=n % 997)
+    got_t, got_f = run_sm(cns, ops, 5)
+    want_t, want_f = oracle.cnt_statemachine(ops, 5)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
 @pytest.mark.parametrize("gap", [1000, 9000, 70000])
 def test_statemachine_rare_sets(cns, gap):
     """SET records only every `gap` ops: chains cross many CTAs (each CTA
