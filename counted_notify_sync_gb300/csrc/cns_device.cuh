@@ -10,149 +10,9 @@
 #include <cstdint>
 
 #include "cns.h"
+#include "cns_device.h"   // scoped memory operations, the epoch arithmetic, the user-kernel API
 
 namespace cns {
-
-// ---------------------------------------------------------------------------
-// Scoped memory operations (PTX ISA memory consistency model, .gpu scope)
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t atom_inc_release_gpu(uint32_t *p, uint32_t bound)
-{
-    // old = *p; *p = (old >= bound) ? 0 : old + 1
-    uint32_t old;
-    asm volatile("atom.release.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ uint32_t atom_exch_release_gpu(uint32_t *p, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.release.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ uint32_t atom_exch_relaxed_gpu(uint32_t *p, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.relaxed.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ uint32_t atom_cas_relaxed_gpu(uint32_t *p, uint32_t cmp, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.relaxed.gpu.global.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "l"(p), "r"(cmp), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t atom_inc_relaxed_gpu(uint32_t *p, uint32_t bound)
-{
-    uint32_t old;
-    asm volatile("atom.relaxed.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ void red_inc_relaxed_gpu(uint32_t *p, uint32_t bound)
-{
-    asm volatile("red.relaxed.gpu.global.inc.u32 [%0], %1;" ::"l"(p), "r"(bound) : "memory");
-}
-
-__device__ __forceinline__ void fence_release_gpu()
-{
-    asm volatile("fence.release.gpu;" ::: "memory");
-}
-
-// After a strong read (here: the read half of an atomic), makes the reading
-// thread see what the writers it read from released.
-__device__ __forceinline__ void fence_acquire_gpu()
-{
-    asm volatile("fence.acquire.gpu;" ::: "memory");
-}
-
-__device__ __forceinline__ void red_add_relaxed_gpu(uint32_t *p, uint32_t v)
-{
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_or_release_gpu(uint32_t *p, uint32_t v)
-{
-    asm volatile("red.release.gpu.global.or.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_and_release_gpu(uint32_t *p, uint32_t v)
-{
-    asm volatile("red.release.gpu.global.and.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
-{
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *p)
-{
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_gpu_u64(uint64_t *p, uint64_t v)
-{
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint64_t globaltimer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ uint32_t smid()
-{
-    uint32_t s;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
-    return s;
-}
 
 // ---------------------------------------------------------------------------
 // Thread-block clusters
@@ -249,38 +109,6 @@ __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence
 // (at once when there is none).
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// ---------------------------------------------------------------------------
-// Epoch arithmetic of the soft barrier ("PTO-ISA SYNCALL cross-core barrier
-// guide", §5.2).  The counter lives in Z_M with M = P * floor(2^32 / P): the
-// arrival is atom.inc with bound M - 1, the target is ((before / P) + 1) * P
-// taken mod M, and the count has reached the target when (cur - target) mod M
-// is below P -- a waiter sees counts in [before + 1, target + P - 1] only.
-// For a power-of-two P, M = 2^32 and this is the plain wrapping add.
-// ---------------------------------------------------------------------------
-
-struct Epoch {
-    uint32_t P;     // participants arriving on this counter
-    uint32_t Mm1;   // M - 1 (the atom.inc bound)
-};
-
-__device__ __forceinline__ uint32_t epoch_target(uint32_t before, const Epoch &e)
-{
-    const uint64_t M = static_cast<uint64_t>(e.Mm1) + 1u;
-    uint64_t t = (static_cast<uint64_t>(before / e.P) + 1u) * e.P;   // <= M since before < M
-    return t == M ? 0u : static_cast<uint32_t>(t);
-}
-
-// (cur - target) mod M < P in 32-bit arithmetic: the wrapping difference is
-// the distance in Z_M unless it wrapped, in which case it exceeds that
-// distance by 2^32 - M (= ~Mm1; zero when M = 2^32).
-__device__ __forceinline__ bool epoch_reached(uint32_t cur, uint32_t target, const Epoch &e)
-{
-    uint32_t d = cur - target;
-    if (cur < target)
-        d -= ~e.Mm1;
-    return d < e.P;
-}
 
 // The epoch that the caller's previous barrier closed: [start, start + P) in
 // Z_M, start a multiple of P.  In a well-formed round an arrival's `before`
@@ -732,51 +560,6 @@ __device__ __forceinline__ bool hard_barrier_finish(int *s_flag)
     __syncwarp();
     cluster_sync_all();
     return *reinterpret_cast<volatile int *>(s_flag) != 0;
-}
-
-// ---------------------------------------------------------------------------
-// Counted-notify record and wait rules ("CANN Runtime CntNotify management
-// API", §3.1 and §3.2)
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ bool cnt_record_valid(uint32_t mode)
-{
-    return mode == CNS_REC_SET || mode == CNS_REC_ADD || mode == CNS_REC_BIT_OR || mode == CNS_REC_BIT_AND;
-}
-
-// New count for a record (pure function; the caller checked the mode).
-// Written as selects, not a switch: the op-stream state machine applies a
-// different mode in every lane of a warp, and a switch there serialises the
-// lanes' paths.
-__device__ __forceinline__ uint32_t cnt_record_apply(uint32_t c, uint32_t mode, uint32_t v)
-{
-    const uint32_t r = (mode == CNS_REC_ADD) ? c + v : v;   // SET
-    return (mode == CNS_REC_BIT_OR) ? (c | v) : (mode == CNS_REC_BIT_AND) ? (c & v) : r;
-}
-
-// Whether a wait with this mode/value is released at count c (mode checked
-// by the caller, <= 4).  Selects, as above.
-__device__ __forceinline__ bool cnt_wait_released(uint32_t c, uint32_t mode, uint32_t v)
-{
-    const bool lt = c < v, eq = c == v, gt = c > v, mask = (c & v) == v;
-    return (mode == CNS_WAIT_LESS) ? lt
-         : (mode == CNS_WAIT_EQUAL) ? eq
-         : (mode == CNS_WAIT_BIGGER) ? gt
-         : (mode == CNS_WAIT_BIGGER_OR_EQUAL) ? (gt || eq)
-                                              : mask;   // CNS_WAIT_EQUAL_WITH_BITMASK
-}
-
-// A record as one device atomic with release semantics.  Usable from inside
-// any kernel (one thread per record).
-__device__ __forceinline__ void cnt_record_device(uint32_t *count, uint32_t mode, uint32_t v)
-{
-    switch (mode) {
-    case CNS_REC_SET: atom_exch_release_gpu(count, v); break;
-    case CNS_REC_ADD: red_add_release_gpu(count, v); break;
-    case CNS_REC_BIT_OR: red_or_release_gpu(count, v); break;
-    case CNS_REC_BIT_AND: red_and_release_gpu(count, v); break;
-    default: break;
-    }
 }
 
 }  // namespace cns

@@ -1,0 +1,362 @@
+/*
+ * cns_device.h -- the device side of counted_notify_sync for code that runs
+ * inside the caller's own CUDA kernels (nvcc, sm_103a): record on a counted
+ * notify, wait on one, and take the soft SYNCALL barrier, with no library
+ * call and no kernel boundary.  Header only; include it from .cu files
+ * compiled with -gencode arch=compute_103a,code=sm_103a, with the directory
+ * of cns.h on the include path.
+ *
+ *   cns_cnt_record_dev   one record ("CANN Runtime CntNotify management API"
+ *                        §3.1: SET, ADD, BIT_OR, BIT_AND) as one release
+ *                        atomic on the notify's count word
+ *                        (cntnotify_get_device_ptr gives its address)
+ *   cns_cnt_wait_dev     a bounded wait on that word (§3.2: LESS, EQUAL,
+ *                        BIGGER, BIGGER_OR_EQUAL, EQUAL_WITH_BITMASK, with
+ *                        isClear) from one thread
+ *   cns_syncall_soft     the soft SYNCALL barrier ("PTO-ISA SYNCALL
+ *                        cross-core barrier guide" §5.2) among the first P
+ *                        CTAs of a grid, on a workspace that
+ *                        syncall_workspace_init prepared, called by every
+ *                        thread of each of those CTAs
+ *
+ * Every wait is bounded and reports CNS_ERR_TIMEOUT instead of trapping.  The
+ * caller makes the participating CTAs co-resident (a cooperative launch, or a
+ * grid no larger than the GPU holds at once): a barrier whose participants
+ * are not all running at the same time ends in that timeout.
+ *
+ * The library's own kernels are built on the same primitives (namespace cns).
+ */
+#ifndef CNS_DEVICE_H
+#define CNS_DEVICE_H
+
+#include <stdint.h>
+
+#include "cns.h"
+
+#if defined(__CUDACC__)
+
+namespace cns {
+
+// ---------------------------------------------------------------------------
+// Scoped memory operations (PTX ISA memory consistency model, .gpu scope)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t atom_inc_release_gpu(uint32_t *p, uint32_t bound)
+{
+    // old = *p; *p = (old >= bound) ? 0 : old + 1
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_exch_release_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_exch_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_cas_relaxed_gpu(uint32_t *p, uint32_t cmp, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "l"(p), "r"(cmp), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_inc_relaxed_gpu(uint32_t *p, uint32_t bound)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void red_inc_relaxed_gpu(uint32_t *p, uint32_t bound)
+{
+    asm volatile("red.relaxed.gpu.global.inc.u32 [%0], %1;" ::"l"(p), "r"(bound) : "memory");
+}
+
+__device__ __forceinline__ void fence_release_gpu()
+{
+    asm volatile("fence.release.gpu;" ::: "memory");
+}
+
+// After a strong read (here: the read half of an atomic), makes the reading
+// thread see what the writers it read from released.
+__device__ __forceinline__ void fence_acquire_gpu()
+{
+    asm volatile("fence.acquire.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_or_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.or.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_and_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.and.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(uint64_t *p, uint64_t v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smid()
+{
+    uint32_t s;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+    return s;
+}
+
+// ---------------------------------------------------------------------------
+// Epoch arithmetic of the soft barrier ("PTO-ISA SYNCALL cross-core barrier
+// guide", §5.2).  The counter lives in Z_M with M = P * floor(2^32 / P): the
+// arrival is atom.inc with bound M - 1, the target is ((before / P) + 1) * P
+// taken mod M, and the count has reached the target when (cur - target) mod M
+// is below P -- a waiter sees counts in [before + 1, target + P - 1] only.
+// For a power-of-two P, M = 2^32 and this is the plain wrapping add.
+// ---------------------------------------------------------------------------
+
+struct Epoch {
+    uint32_t P;     // participants arriving on this counter
+    uint32_t Mm1;   // M - 1 (the atom.inc bound)
+};
+
+__device__ __forceinline__ uint32_t epoch_target(uint32_t before, const Epoch &e)
+{
+    const uint64_t M = static_cast<uint64_t>(e.Mm1) + 1u;
+    uint64_t t = (static_cast<uint64_t>(before / e.P) + 1u) * e.P;   // <= M since before < M
+    return t == M ? 0u : static_cast<uint32_t>(t);
+}
+
+// (cur - target) mod M < P in 32-bit arithmetic: the wrapping difference is
+// the distance in Z_M unless it wrapped, in which case it exceeds that
+// distance by 2^32 - M (= ~Mm1; zero when M = 2^32).
+__device__ __forceinline__ bool epoch_reached(uint32_t cur, uint32_t target, const Epoch &e)
+{
+    uint32_t d = cur - target;
+    if (cur < target)
+        d -= ~e.Mm1;
+    return d < e.P;
+}
+
+// The epoch of P participants: M - 1 = P * floor(2^32 / P) - 1.
+__device__ __forceinline__ Epoch epoch_of(uint32_t P)
+{
+    const uint64_t M = static_cast<uint64_t>(P) * ((static_cast<uint64_t>(1) << 32) / P);
+    return Epoch{P, static_cast<uint32_t>(M - 1u)};
+}
+
+// ---------------------------------------------------------------------------
+// Counted-notify record and wait rules ("CANN Runtime CntNotify management
+// API", §3.1 and §3.2)
+// ---------------------------------------------------------------------------
+
+// Whether a wait with this mode/value is released at count c (mode checked
+// by the caller, <= 4).
+__device__ __forceinline__ bool cnt_wait_released(uint32_t c, uint32_t mode, uint32_t v)
+{
+    const bool lt = c < v, eq = c == v, gt = c > v, mask = (c & v) == v;
+    return (mode == CNS_WAIT_LESS) ? lt
+         : (mode == CNS_WAIT_EQUAL) ? eq
+         : (mode == CNS_WAIT_BIGGER) ? gt
+         : (mode == CNS_WAIT_BIGGER_OR_EQUAL) ? (gt || eq)
+                                              : mask;   // CNS_WAIT_EQUAL_WITH_BITMASK
+}
+
+// A record as one device atomic with release semantics.  Usable from inside
+// any kernel (one thread per record).
+__device__ __forceinline__ void cnt_record_device(uint32_t *count, uint32_t mode, uint32_t v)
+{
+    switch (mode) {
+    case CNS_REC_SET: atom_exch_release_gpu(count, v); break;
+    case CNS_REC_ADD: red_add_release_gpu(count, v); break;
+    case CNS_REC_BIT_OR: red_or_release_gpu(count, v); break;
+    case CNS_REC_BIT_AND: red_and_release_gpu(count, v); break;
+    default: break;
+    }
+}
+
+}  // namespace cns
+
+/* One record on a counted notify's count word: SET, ADD, BIT_OR or BIT_AND
+ * with value v, one release atomic (the caller's earlier writes are visible
+ * to whoever is released by it).  Any thread may call it; each call is one
+ * record.  Other modes do nothing (the host API refuses them). */
+__device__ __forceinline__ void cns_cnt_record_dev(uint32_t *count, int mode, uint32_t v)
+{
+    cns::cnt_record_device(count, static_cast<uint32_t>(mode), v);
+}
+
+/* Wait, from the calling thread only, until the count word satisfies
+ * (mode, v); then, with is_clear, set it to 0 (an exchange right after the
+ * release was seen).  Polls with relaxed loads and takes one acquire fence
+ * once released, so the records' earlier writes are visible afterwards.
+ * timeout_ns = 0 means 2 s.  Returns CNS_SUCCESS, CNS_ERR_TIMEOUT, or
+ * CNS_ERR_INVALID_VALUE for a mode outside 0..4; *observed (if not NULL)
+ * gets the count that released the wait. */
+__device__ __forceinline__ int cns_cnt_wait_dev(uint32_t *count, int mode, uint32_t v, int is_clear,
+                                                uint64_t timeout_ns, uint32_t *observed)
+{
+    if (mode < 0 || mode > 4)
+        return CNS_ERR_INVALID_VALUE;
+    const uint64_t limit = timeout_ns ? timeout_ns : 2000000000ull;
+    uint32_t spins = 0;
+    uint64_t deadline = 0;
+    for (;;) {
+        const uint32_t c = cns::ld_relaxed_gpu(count);
+        if (cns::cnt_wait_released(c, static_cast<uint32_t>(mode), v)) {
+            cns::fence_acquire_gpu();
+            if (observed)
+                *observed = c;
+            if (is_clear)
+                cns::atom_exch_relaxed_gpu(count, 0u);
+            return CNS_SUCCESS;
+        }
+        if ((++spins & 63u) == 0u) {
+            const uint64_t now = cns::globaltimer_ns();
+            if (deadline == 0)
+                deadline = now + limit;
+            else if (now > deadline)
+                return CNS_ERR_TIMEOUT;
+        }
+    }
+}
+
+/* The soft SYNCALL barrier among CTAs 0 .. participants - 1 of the grid.
+ * Every thread of each participating CTA calls it, the same number of times
+ * in each CTA; CTAs with blockIdx.x >= participants must not call it.  The
+ * CTA's threads first finish what they were doing (a block barrier), one
+ * thread arrives with an increment of the workspace's soft counter (line 0,
+ * word 0; release), takes target = (before / P + 1) * P in the wrap-safe
+ * counter arithmetic of syncall_run, and polls until the count reaches it
+ * (the last arrival of a round skips the poll); a second block barrier
+ * releases the CTA.  Writes made by any participant before its call are
+ * visible to every participant after the barrier.
+ *   workspace    CNS_SYNCALL_WORKSPACE_BYTES, 128-byte aligned, prepared by
+ *                syncall_workspace_init (start 0 or a multiple of P; again
+ *                whenever P changes) and used by no other barrier at the
+ *                same time
+ *   timeout_ns   per wait; 0 = 2 s.  A wait that runs out records
+ *                CNS_ERR_TIMEOUT in the workspace status line (line 1, with
+ *                the CTA that gave up) and raises its abort flag; the other
+ *                participants' waits then give up too.
+ * Returns CNS_SUCCESS, or CNS_ERR_TIMEOUT in every thread of the CTA once
+ * the barrier failed (the caller should then leave its kernel). */
+__device__ __forceinline__ int cns_syncall_soft(void *workspace, uint32_t participants, uint64_t timeout_ns)
+{
+    uint32_t *ctr = static_cast<uint32_t *>(workspace);
+    uint32_t *status = ctr + CNS_SYNCALL_LINE_BYTES / 4;
+    int stop = 0;
+    __syncthreads();
+    if (threadIdx.x == 0 && threadIdx.y == 0 && threadIdx.z == 0) {
+        const cns::Epoch e = cns::epoch_of(participants);
+        const uint32_t before = cns::atom_inc_release_gpu(ctr, e.Mm1);
+        const uint32_t target = cns::epoch_target(before, e);
+        const uint32_t mine = (before == e.Mm1) ? 0u : before + 1u;
+        if (cns::epoch_reached(mine, target, e)) {
+            cns::fence_acquire_gpu();   // the last arrival: its increment read every other one's
+        } else {
+            const uint64_t limit = timeout_ns ? timeout_ns : 2000000000ull;
+            uint32_t spins = 0;
+            uint64_t deadline = 0;
+            for (;;) {
+                if (cns::epoch_reached(cns::ld_relaxed_gpu(ctr), target, e)) {
+                    cns::fence_acquire_gpu();
+                    break;
+                }
+                if ((++spins & 63u) == 0u) {
+                    if (cns::ld_relaxed_gpu(status + 1) != 0u) {
+                        stop = 1;
+                        break;
+                    }
+                    const uint64_t now = cns::globaltimer_ns();
+                    if (deadline == 0) {
+                        deadline = now + limit;
+                    } else if (now > deadline) {
+                        if (cns::atom_cas_relaxed_gpu(status, 0u, static_cast<uint32_t>(CNS_ERR_TIMEOUT)) == 0u)
+                            cns::st_relaxed_gpu(status + 3, blockIdx.x);
+                        cns::atom_exch_release_gpu(status + 1, 1u);
+                        stop = 1;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    return __syncthreads_or(stop) ? CNS_ERR_TIMEOUT : CNS_SUCCESS;
+}
+
+#endif /* __CUDACC__ */
+
+#endif /* CNS_DEVICE_H */

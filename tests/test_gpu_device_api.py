@@ -1,0 +1,170 @@
+"""The device-side API of include/cns_device.h inside user kernels
+(tests/fused/user_kernels.cu, built here into a library of its own): the soft
+barrier between ring rounds against the sequential oracle, over a subset of
+the grid and through the counter's wrap; records from user threads released
+by the library's stream wait; device waits on every mode against the oracle's
+rule; and bounded timeouts (a barrier one CTA never reaches, a count nobody
+records)."""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import cns_inputs as ci
+import oracle
+from tests.gpu_helpers import from_dev_u32, to_dev_u32
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "tests", "fused", "user_kernels.cu")
+OUT = os.path.join(ROOT, "tests", "fused", "_build", "libcns_user_kernels.so")
+HDR = os.path.join(ROOT, "include", "cns_device.h")
+
+
+@pytest.fixture(scope="module")
+def cns():
+    import torch
+    import counted_notify_sync_gb300 as c
+    c.build()
+    torch.cuda.set_device(0)
+    return c
+
+
+@pytest.fixture(scope="module")
+def user(cns):
+    from counted_notify_sync_gb300 import builder
+    newest = max(os.path.getmtime(p) for p in (SRC, HDR, os.path.join(ROOT, "include", "cns.h")))
+    if not os.path.exists(OUT) or os.path.getmtime(OUT) < newest:
+        os.makedirs(os.path.dirname(OUT), exist_ok=True)
+        tmp = OUT + f".tmp{os.getpid()}"
+        nvcc = os.path.join(builder.cuda_home(), "bin", "nvcc")
+        subprocess.run([nvcc, *builder.ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+                        "-I", os.path.join(ROOT, "include"), "-o", tmp, SRC], check=True)
+        os.replace(tmp, OUT)
+    L = ctypes.CDLL(OUT)
+    i32, u32, i64, u64, vp = ctypes.c_int32, ctypes.c_uint32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
+    L.user_ring.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
+    L.user_record.argtypes = [vp, ctypes.c_int, u32, i32, i32, ctypes.c_int]
+    L.user_wait.argtypes = [vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp]
+    for f in (L.user_ring, L.user_record, L.user_wait):
+        f.restype = ctypes.c_int
+    return L
+
+
+def _ring(cns, user, ctas, P, rounds, start=0, threads=256, short_cta=0xFFFFFFFF, timeout_ns=0):
+    import torch
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P, 4)
+    b0 = to_dev_u32(np.vstack([v0, np.zeros((ctas - P, 4), np.uint32)]))
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace(start_value=start, die_local=False)
+    status = torch.full((ctas,), -1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    rc = user.user_ring(ctas, threads, P, rounds, b0.data_ptr(), b1.data_ptr(), ws.data_ptr(), timeout_ns,
+                        short_cta, status.data_ptr())
+    assert rc == 0, rc
+    got = from_dev_u32(b0 if rounds % 2 == 0 else b1).reshape(ctas, 4)[:P]
+    return v0, got, from_dev_u32(ws), status.cpu().numpy()
+
+
+@pytest.mark.parametrize("ctas,P,rounds,threads", [(148, 148, 10001, 256), (8, 8, 1000, 256), (111, 111, 777, 96),
+                                                     (148, 64, 2001, 256), (5, 5, 3, 32), (1, 1, 10, 64)])
+def test_fused_soft_barrier_ring_matches_oracle(cns, user, ctas, P, rounds, threads):
+    v0, got, ws, status = _ring(cns, user, ctas, P, rounds, threads=threads)
+    want, fc, rc = oracle.syncall_run_ring(oracle.WL_RING_ROTATE, v0, rounds)
+    assert rc == oracle.OK
+    np.testing.assert_array_equal(got, want)
+    assert int(ws[0]) == fc == (rounds * P) % oracle.counter_modulus(P)
+    assert (status[:P] == 0).all() and (status[P:] == -1).all()   # CTAs past P never called it
+
+
+@pytest.mark.parametrize("P", [148, 111, 7])
+def test_fused_soft_barrier_through_the_wrap(cns, user, P):
+    M = oracle.counter_modulus(P)
+    start = M - 5 * P
+    v0, got, ws, status = _ring(cns, user, P, P, 12, start=start)
+    want, fc, rc = oracle.syncall_run_ring(oracle.WL_RING_ROTATE, v0, 12, start=start)
+    assert rc == oracle.OK
+    np.testing.assert_array_equal(got, want)
+    assert int(ws[0]) == fc == (start + 12 * P) % M
+    assert (status == 0).all()
+
+
+def test_fused_soft_barrier_times_out_when_a_cta_stops_short(cns, user):
+    """CTA 5 takes one barrier fewer: the others give up on the last barrier
+    after their 20 ms limit, with CNS_ERR_TIMEOUT in every CTA and in the
+    workspace's status line, and no CTA is left waiting."""
+    P = 8
+    v0, got, ws, status = _ring(cns, user, P, P, 4, short_cta=5, timeout_ns=20_000_000)
+    line = ws[32:36]
+    assert int(line[0]) == cns.CNS_ERR_TIMEOUT and int(line[1]) == 1 and int(line[3]) != 5
+    assert status[5] == 0
+    assert all(status[p] == cns.CNS_ERR_TIMEOUT for p in range(P) if p != 5)
+
+
+def test_fused_records_released_by_the_library_wait(cns, user):
+    import torch
+    rc, h = cns.cntnotify_create(0)
+    assert rc == 0
+    try:
+        rc, word = cns.cntnotify_get_device_ptr(h)
+        assert rc == 0
+        assert user.user_record(word, cns.CNS_REC_ADD, 1, 64, 32, 2) == 0   # 4096 records of ADD 1
+        s = torch.cuda.Stream()
+        assert cns.cntnotify_wait_with_timeout(h, s, cns.CNS_WAIT_BIGGER_OR_EQUAL, 4096, 5, 1) == 0
+        s.synchronize()
+        rc, st, c = cns.cntnotify_query_status(h)
+        assert rc == 0 and st == 0 and c == 0   # released, then cleared
+        assert user.user_record(word, cns.CNS_REC_SET, 0xDEADBEEF, 1, 1, 1) == 0
+        assert user.user_record(word, cns.CNS_REC_BIT_AND, 0xFFFF0000, 1, 1, 1) == 0
+        assert user.user_record(word, cns.CNS_REC_BIT_OR, 0x0000000F, 1, 1, 1) == 0
+        assert user.user_record(word, 3, 0x12345678, 1, 1, 1) == 0   # no such mode: nothing happens
+        rc, st, c = cns.cntnotify_query_status(h)
+        assert c == ((0xDEADBEEF & 0xFFFF0000) | 0xF)
+    finally:
+        cns.cntnotify_destroy(h)
+
+
+CASES = [(c, m, v, clr) for c in (0, 1, 5, 0xFFFFFFFF, 0x0F0F0F0F)
+         for m in range(5) for v in (0, 1, 5, 0xFFFFFFFF, 0x0000000F) for clr in (0, 1)]
+
+
+def test_fused_device_wait_follows_the_rules(cns, user):
+    """Each (count, mode, value, isClear): the device wait releases exactly
+    when the oracle's rule holds (else it runs out after 200 us), reports the
+    count it saw, and clears only when released with isClear."""
+    import torch
+    rc, h = cns.cntnotify_create(0)
+    assert rc == 0
+    try:
+        rc, word = cns.cntnotify_get_device_ptr(h)
+        out = torch.zeros(2, dtype=torch.int32, device="cuda")
+        for c, m, v, clr in CASES:
+            assert user.user_record(word, cns.CNS_REC_SET, c, 1, 1, 1) == 0
+            assert user.user_wait(word, m, v, clr, 200_000, out.data_ptr(), out.data_ptr() + 4) == 0
+            got_rc, seen = out.cpu().numpy().view(np.uint32).tolist()
+            sat = oracle.cnt_wait_satisfied(c, m, v)
+            assert got_rc == (0 if sat else cns.CNS_ERR_TIMEOUT), (c, m, v, clr)
+            rc, st, now = cns.cntnotify_query_status(h)
+            if sat:
+                assert seen == c
+                assert now == (0 if clr else c), (c, m, v, clr)
+            else:
+                assert now == c
+    finally:
+        cns.cntnotify_destroy(h)
+
+
+def test_fused_device_wait_rejects_unknown_modes(cns, user):
+    import torch
+    rc, h = cns.cntnotify_create(0)
+    try:
+        rc, word = cns.cntnotify_get_device_ptr(h)
+        out = torch.zeros(2, dtype=torch.int32, device="cuda")
+        for m in (-1, 5, 9):
+            assert user.user_wait(word, m, 0, 0, 1000, out.data_ptr(), out.data_ptr() + 4) == 0
+            assert int(out[0]) == cns.CNS_ERR_INVALID_VALUE
+    finally:
+        cns.cntnotify_destroy(h)
