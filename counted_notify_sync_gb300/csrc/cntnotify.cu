@@ -265,14 +265,17 @@ __device__ __forceinline__ uint4 sm_micro(const uint4 &op)
 }
 
 // One micro-op applied to count c; *outcome gets the op's CNS_OUT_* code.
+// Only the compare, the two flag tests and the final select lie on the chain
+// from one count to the next.
 __device__ __forceinline__ uint32_t sm_apply_micro(uint32_t c, const uint4 m, uint32_t *outcome)
 {
     const uint32_t x = c & m.x;
-    const uint32_t idx = (x > m.y ? 1u : 0u) + (x >= m.y ? 1u : 0u);   // 0 below, 1 equal, 2 above
-    const uint32_t f = m.w >> idx;   // a record's bits 0-6 are 0: it is never released nor cleared
+    const uint32_t bit = x < m.y ? 1u : (x == m.y ? 2u : 4u);   // the compare result, as the flag it tests
+    const bool rel = (m.w & bit) != 0u;          // a record's bits 0-6 are 0: never released nor cleared
+    const bool clr = (m.w & (bit << 4)) != 0u;
     const uint32_t keep = (m.w & kMicroWait) ? c : (x | m.y) + m.z;
-    *outcome = (f & 1u) + ((m.w >> 9) & 3u);   // a wait: HELD (0) or RELEASED (1)
-    return (f & 16u) ? 0u : keep;
+    *outcome = rel ? 1u : ((m.w >> 9) & 3u);    // a wait: RELEASED (1) or HELD (0)
+    return clr ? 0u : keep;
 }
 
 constexpr uint64_t kSmLinkTimeoutNs = 10ull * 1000000000ull;
@@ -316,6 +319,10 @@ constexpr size_t kFSmemBytes = static_cast<size_t>(kFThreads) * kFPad * (sizeof(
 
 __device__ __forceinline__ int f_slot(int i) { return (i / kFChunk) * kFPad + (i % kFChunk); }
 
+// Length classes of the stretches: floor(log2(length)) for lengths 1 .. 4096,
+// longest first, and a last class for chunks without a stretch.
+constexpr int kJobClasses = 14;
+
 // Position of the tile's first SET at or after `from` (cnt if none) from the
 // tile's SET bits; positions at or past cnt carry no SET bit.
 __device__ __forceinline__ int f_next_set(const uint32_t *s_setm, int from, int cnt)
@@ -330,16 +337,26 @@ __device__ __forceinline__ int f_next_set(const uint32_t *s_setm, int from, int 
 }
 
 // Apply ops [p, end) of the tile to count c, writing their trace entries.
+// The next op is loaded while the current one is applied.
 __device__ __forceinline__ uint32_t f_walk(const uint4 *s_ops, uint2 *s_tr, int p, int end, uint32_t c)
 {
+    if (p >= end)
+        return c;
     int slot = f_slot(p);
-    for (; p < end; ++p) {
+    uint4 m = s_ops[slot];
+    for (;;) {
+        const int next = slot + ((p & (kFChunk - 1)) == kFChunk - 1 ? 2 : 1);   // over the chunk's pad entry
+        const bool more = p + 1 < end;
+        const uint4 mn = more ? s_ops[next] : m;
         uint32_t o;
-        c = sm_apply_micro(c, s_ops[slot], &o);
+        c = sm_apply_micro(c, m, &o);
         s_tr[slot] = make_uint2(c, o);
-        slot += (p & (kFChunk - 1)) == kFChunk - 1 ? 2 : 1;   // step over the chunk's pad entry
+        if (!more)
+            return c;
+        m = mn;
+        slot = next;
+        ++p;
     }
-    return c;
 }
 
 __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *ops, int64_t n, int tile_ops,
@@ -350,12 +367,16 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
     uint4 *s_ops = f_smem;
     uint2 *s_tr = reinterpret_cast<uint2 *>(f_smem + kFThreads * kFPad);
     uint32_t *s_setm = reinterpret_cast<uint32_t *>(s_tr + kFThreads * kFPad);
+    __shared__ uint32_t s_job[kFThreads];   // stretch handed to thread i: (start << 16) | end
+    __shared__ int s_cls[kJobClasses];       // per length class: count, then first slot
     const int64_t tiles = (n + tile_ops - 1) / tile_ops;
     const int k = threadIdx.x;
     const int lane = k & 31;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t base = t * tile_ops;
         const int cnt = (n - base < tile_ops) ? static_cast<int>(n - base) : tile_ops;
+        if (k < kJobClasses)
+            s_cls[k] = 0;
         {   // stage: the 8 loads of a thread in flight four at a time, turned into micro-ops on the way in
             const uint4 *src = ops + base;
 #pragma unroll
@@ -380,13 +401,46 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
         }
         __syncthreads();
         const bool last_tile = base + cnt == n;
-        const int chunk0 = k * kFChunk;
-        if (chunk0 < cnt) {   // A
-            const int start = f_next_set(s_setm, chunk0, cnt);
-            if (start < chunk0 + kFChunk && start < cnt) {   // the chunk has a SET
-                const int end = f_next_set(s_setm, chunk0 + kFChunk, cnt);
-                const uint32_t c = f_walk(s_ops, s_tr, start, end, 0u);   // starts with a SET: any count will do
-                if (end >= cnt) {
+        {   // A
+            // this chunk's stretch, if it has a SET
+            const int chunk0 = k * kFChunk;
+            int start = cnt, end = cnt;
+            if (chunk0 < cnt) {
+                const int s0 = f_next_set(s_setm, chunk0, cnt);
+                if (s0 < chunk0 + kFChunk && s0 < cnt) {
+                    start = s0;
+                    end = f_next_set(s_setm, chunk0 + kFChunk, cnt);
+                }
+            }
+            // The stretches are handed to threads longest class first (class = floor(log2(length)),
+            // counted per warp, placed by a scan over the classes), so that a warp's lanes walk
+            // stretches of similar length instead of waiting for one long stretch among short ones.
+            const int len = end - start;   // 0: none
+            const int cls = len > 0 ? kJobClasses - 2 - min(31 - __clz(len), kJobClasses - 2) : kJobClasses - 1;
+            const uint32_t same = __match_any_sync(0xffffffffu, cls);
+            const int leader = __ffs(same) - 1;
+            int wbase = 0;
+            if (lane == leader)
+                wbase = atomicAdd(&s_cls[cls], __popc(same));
+            wbase = __shfl_sync(0xffffffffu, wbase, leader) + __popc(same & ((1u << lane) - 1u));
+            __syncthreads();
+            if (k == 0) {
+                int acc = 0;
+                for (int q = 0; q < kJobClasses; ++q) {
+                    const int n_q = s_cls[q];
+                    s_cls[q] = acc;
+                    acc += n_q;
+                }
+            }
+            __syncthreads();
+            if (len > 0)
+                s_job[s_cls[cls] + wbase] = (static_cast<uint32_t>(start) << 16) | static_cast<uint32_t>(end);
+            const int jobs = s_cls[kJobClasses - 1];
+            __syncthreads();
+            if (k < jobs) {
+                const int js = static_cast<int>(s_job[k] >> 16), je = static_cast<int>(s_job[k] & 0xFFFFu);
+                const uint32_t c = f_walk(s_ops, s_tr, js, je, 0u);   // starts with a SET: any count will do
+                if (je >= cnt) {
                     sm_publish(link + t, tag, c);
                     if (last_tile)
                         *final_count = c;
