@@ -312,9 +312,12 @@ __device__ __forceinline__ int cns_cnt_wait_dev(uint32_t *count, int mode, uint3
  *                the CTA that gave up) and raises its abort flag; the other
  *                participants' waits then give up too.
  * Returns CNS_SUCCESS, or CNS_ERR_TIMEOUT in every thread of the CTA once
- * the barrier failed (the caller should then leave its kernel). */
+ * the barrier failed (the caller should then leave its kernel);
+ * CNS_ERR_INVALID_VALUE without arriving when participants is 0. */
 __device__ __forceinline__ int cns_syncall_soft(void *workspace, uint32_t participants, uint64_t timeout_ns)
 {
+    if (participants == 0u)
+        return CNS_ERR_INVALID_VALUE;
     uint32_t *ctr = static_cast<uint32_t *>(workspace);
     uint32_t *status = ctr + CNS_SYNCALL_LINE_BYTES / 4;
     int stop = 0;
