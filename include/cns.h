@@ -465,8 +465,9 @@ typedef struct {
     int64_t tiles;           /* (in) K tiles per round, >= 1 */
     int32_t tile_words;      /* (in) words per tile, multiple of 4, 4..8192 */
     int32_t producer_ctas;   /* (in) producer grid of 256-thread CTAs; 0 = one CTA per tile.
-                                Capped at the tile count and so that the producer holds at most
-                                half of the GPU's thread slots (4 CTAs per SM on GB300) */
+                                Capped at the tile count and so that a producer grid holds at most
+                                half of the GPU's thread slots with one area (4 CTAs per SM on
+                                GB300), an eighth with two (1 CTA per SM) */
     int64_t rounds;          /* (in) rounds */
     cns_stream_t producer_stream; /* (in) the recording stream */
     cns_stream_t consumer_stream; /* (in) the waiting stream */
