@@ -452,3 +452,42 @@ def test_pipeline_rejects_bad_area_count(cns):
     finally:
         cns.cntnotify_destroy(done)
         cns.cntnotify_destroy(ack)
+
+
+def _pipeline_configs(n, seed=77):
+    rng = np.random.RandomState(seed)
+    out = []
+    for i in range(n):
+        words = 4 * int(rng.randint(1, 2049))                       # 4 .. 8192
+        tiles = int(rng.randint(1, max(2, min(6000, (1 << 22) // words))))
+        out.append(dict(tiles=tiles, words=words, rounds=int(rng.randint(1, 61)),
+                        pctas=int(rng.choice([0, 1, 7, 100, 1000])), areas=int(rng.choice([1, 2])),
+                        one_stream=bool(rng.rand() < 0.25)))
+    return out
+
+
+@pytest.mark.parametrize("c", _pipeline_configs(24),
+                         ids=lambda c: f"t{c['tiles']}w{c['words']}r{c['rounds']}p{c['pctas']}a{c['areas']}"
+                                       f"{'s' if c['one_stream'] else 'm'}")
+def test_pipeline_random_configs(cns, c):
+    """Seeded random pipelines (tile count, tile size, rounds, producer grid, one or two areas, one or two
+    streams): every round's checksum and release count equal the oracle's, and the notifies end where
+    the protocol leaves them."""
+    import torch
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    assert rc == rc2 == 0
+    try:
+        s1 = torch.cuda.Stream()
+        s2 = s1 if c["one_stream"] else torch.cuda.Stream()
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, c["tiles"], c["words"], c["rounds"], s1, s2,
+                                                        timeout_s=10, producer_ctas=c["pctas"], areas=c["areas"])
+        assert rc == 0 and cfg.device_status == 0
+        want_cs, want_rel = oracle.pipeline(c["tiles"], c["words"], c["rounds"])
+        np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
+        np.testing.assert_array_equal(from_dev_u32(released), want_rel)
+        assert count_of(cns, done) == (0, 0)
+        assert count_of(cns, ack) == (0, (c["rounds"] * cfg.consumer_ctas) % (1 << 32))
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
