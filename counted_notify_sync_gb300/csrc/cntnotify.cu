@@ -202,7 +202,7 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 //      up to the tile's next SET after the chunk (or the tile's end, in which
 //      case it publishes the tile's end count, tagged with this call's tag,
 //      for the next tile) -- one contiguous stretch of ops per thread;
-//   C  thread 0 takes the previous tile's end count (init for tile 0),
+//   C  the last thread takes the previous tile's end count (init for tile 0),
 //      waiting on the device until it is published, and replays the ops in
 //      front of the tile's first SET -- all of them if the tile has none, in
 //      which case it publishes the tile's end count itself.
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
                 }
             }
         }
-        if (k == 0) {   // C
+        if (k == kFThreads - 1) {   // C, on the thread handed the shortest stretch (or none)
             const int lead = f_next_set(s_setm, 0, cnt);
             uint32_t cp = init;
             if (t == 0 || sm_take(link + t - 1, tag, &cp)) {
