@@ -52,10 +52,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-secondary", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--variant", type=int, default=2, choices=range(7),
-                    help="barrier variant of the headline (cns_barrier_variant_t); 2, the pages' arithmetic with "
-                         "relaxed polls and one acquire fence (the last arrival skips its poll), measured fastest "
-                         "with the ring payload")
+    ap.add_argument("--variant", type=int, default=5, choices=range(7),
+                    help="barrier variant of the headline (cns_barrier_variant_t); 5, the pages' arithmetic on "
+                         "die-local counter copies (on a die-local workspace that starts on an 8 KB boundary), "
+                         "measured fastest with the ring payload")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
     ap.add_argument("--clocks-dir", default=None,
                     help="where the nvidia-smi clock samples of the timed region are written (default: temp dir)")
@@ -317,7 +317,7 @@ def timed_run(torch, fn):
 def secondary(cns, torch, peaks):
     out = {}
 
-    def ring(mode, core, wl, ctas, P, slots, R, ratio=0, used=0, label="", variant=2):
+    def ring(mode, core, wl, ctas, P, slots, R, ratio=0, used=0, label="", variant=5):
         v0 = ci.ring_payload(1, P, slots)
         b0 = torch.from_numpy(v0.view(np.int32).copy()).cuda() if v0.size else None
         b1 = torch.zeros_like(b0) if v0.size else None
@@ -461,13 +461,13 @@ def secondary(cns, torch, peaks):
     return out
 
 
-def barrier_context(sec, rtt_mean, far):
+def barrier_context(sec, rtt_mean, far, variant):
     """The empty-round barrier in its two contracts, against the same round trips: with the release and
-    acquire that data rounds need (variant 2), and arrival only as the pages define SYNCALL (variant 8,
-    on die-local counter copies)."""
+    acquire that data rounds need (the headline's variant), and arrival only as the pages define SYNCALL
+    (variant 8, on die-local counter copies)."""
     out = {}
     far_mean = statistics.mean(far) if far else None
-    for key, label in (("soft_148_empty_variant2", "empty_release_acquire"),
+    for key, label in ((f"soft_148_empty_variant{variant}", "empty_release_acquire"),
                        ("soft_148_empty_variant8", "empty_arrival_only_die_local")):
         v = sec.get(key, {}).get("ns_per_round")
         if v:
@@ -536,7 +536,7 @@ def run_native(args):
     cpu = time_oracle(args.cpu_seconds) if world == 1 else None
     if cpu is not None and not args.no_secondary:
         cpu["twin"] = time_twin()
-    traffic = load_traffic().get("syncall_soft_ring_rotate_148", {})
+    traffic = load_traffic().get(f"syncall_soft_ring_rotate_148_variant{args.variant}", {})
     achieved = 1e3 / ns_round            # barrier rounds per microsecond
     peak = 1e3 / rtt_mean                # one round per L2 atomic round trip (mean over SMs)
     line = {
@@ -563,7 +563,7 @@ def run_native(args):
                                 "atom_max": round(rtt_max, 1), "arrive_poll_pair_median": round(pair_med, 1),
                                 "ld_relaxed_median": round(ld_med, 1)},
                      "ns_per_round_over_rtt": round(ns_round / rtt_mean, 3),
-                     "context": barrier_context(sec, rtt_mean, far)},
+                     "context": barrier_context(sec, rtt_mean, far, args.variant)},
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,

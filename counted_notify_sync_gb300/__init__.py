@@ -28,10 +28,16 @@ def _torch():
 
 def new_workspace(device=None, start_value: int = 0, stream=None, die_local: bool = True):
     """A zeroed SYNCALL workspace on `device`: CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES long (usable by every
-    barrier variant) or, with die_local=False, the minimal CNS_SYNCALL_WORKSPACE_BYTES."""
+    barrier variant) or, with die_local=False, the minimal CNS_SYNCALL_WORKSPACE_BYTES.  The die-local size
+    starts on a CNS_SYNCALL_DIE_LOCAL_ALIGN boundary, so that its two counter copies sit on different dies."""
     torch = _torch()
-    nbytes = _native.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES if die_local else _native.CNS_SYNCALL_WORKSPACE_BYTES
-    ws = torch.empty(nbytes // 4, dtype=torch.int32, device=device or "cuda")
+    if not die_local:
+        ws = torch.empty(_native.CNS_SYNCALL_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device or "cuda")
+    else:
+        nbytes, align = _native.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES, _native.CNS_SYNCALL_DIE_LOCAL_ALIGN
+        raw = torch.empty((nbytes + align) // 4, dtype=torch.int32, device=device or "cuda")
+        skip = (-raw.data_ptr()) % align // 4
+        ws = raw[skip:skip + nbytes // 4]   # a view: keeps `raw` alive
     _native.check(_native.syncall_workspace_init(ws, ws.numel() * 4, start_value, stream), "syncall_workspace_init")
     return ws
 

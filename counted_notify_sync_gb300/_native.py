@@ -50,6 +50,7 @@ CNS_BARRIER_ARRIVAL_ONLY = 7
 CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL = 8
 CNS_SYNCALL_REPLICA_OFFSET = 4096
 CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES = 8192
+CNS_SYNCALL_DIE_LOCAL_ALIGN = 8192
 CNS_CTA_DONE = 1
 CNS_CTA_IDLE = 2
 CNS_CTA_ABORTED = 4

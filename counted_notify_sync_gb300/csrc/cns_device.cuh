@@ -176,8 +176,9 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //      round of this scheme can produce stops the run (CNS_ERR_INVALID_VALUE).
 //   7  arrival only: the guide's bare contract (arrival, no visibility of
 //      other participants' writes): a relaxed increment and relaxed polls, no
-//      fence.  Only for rounds that exchange no data through memory (the host
-//      refuses it for workloads with a payload).
+//      fence; the last arrival skips the poll.  Only for rounds that exchange
+//      no data through memory (the host refuses it for workloads with a
+//      payload).
 //   8  arrival only on die-local copies: 7's contract with 5's counters (a
 //      relaxed increment of each copy, relaxed polls of the near one).
 //   5  die-local replicas: the counter is kept twice, 4 KB apart.  On GB300
@@ -187,9 +188,10 @@ __device__ __forceinline__ void raise_timeout(uint32_t *status_line, uint32_t ro
 //      by timing both at start.  Every arrival adds one to both copies -- a
 //      returning increment on the near copy, whose old value gives the target,
 //      and a fire-and-forget one on the far copy -- after one release fence;
-//      the participant then polls its near copy.  Each copy sees all P
-//      arrivals of every round, so each runs the same epoch arithmetic; which
-//      die homes which copy only changes the speed, never the result.
+//      the participant then polls its near copy (the round's last arrival
+//      there skips the poll, as in 1).  Each copy sees all P arrivals of every
+//      round, so each runs the same epoch arithmetic; which die homes which
+//      copy only changes the speed, never the result.
 enum : int { kBvCounterAcquire = 0, kBvLastSkips = 1, kBvRelaxedPoll = 2, kBvBackoff = 3, kBvFlag = 4,
              kBvDieLocal = 5, kBvSenseFlip = 6, kBvArrivalOnly = 7, kBvArrivalDieLocal = 8, kBvCount = 9 };
 
@@ -316,9 +318,19 @@ __device__ __forceinline__ Pending barrier_arrive(const Barrier &b, EpochCursor 
             red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             pd.target = epoch_target(before, b.e, c);
+            // every arrival reaches both copies, so an increment of the near
+            // copy that completes the round read all the others (as in 1)
+            const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;
+            if (epoch_reached(mine, pd.target, b.e)) {
+                if constexpr (V == kBvDieLocal)
+                    fence_acquire_gpu();
+                pd.released = true;
+            }
         } else if constexpr (V == kBvArrivalOnly) {
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             pd.target = epoch_target(before, b.e, c);
+            const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;
+            pd.released = epoch_reached(mine, pd.target, b.e);
         } else {
             const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
             pd.target = epoch_target(before, b.e, c);
@@ -386,13 +398,24 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
             red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);
-            stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who, true);
+            const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;
+            if (epoch_reached(mine, target, b.e)) {
+                // the round's last arrival on the near copy: every other arrival
+                // reached this copy too, and the increment read them all
+                fence_acquire_gpu();
+                stop = false;
+            } else {
+                stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who, true);
+            }
         } else if constexpr (V == kBvArrivalDieLocal) {
             red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);
-            stop = poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, target, b.e); }, b.status_line,
-                              b.timeout_ns, round, who, true, 0, false);
+            const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;
+            stop = epoch_reached(mine, target, b.e)
+                       ? false
+                       : poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, target, b.e); },
+                                    b.status_line, b.timeout_ns, round, who, true, 0, false);
         } else if constexpr (V == kBvCounterAcquire) {
             const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);
@@ -400,8 +423,11 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
         } else if constexpr (V == kBvArrivalOnly) {
             const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);
-            stop = poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, target, b.e); }, b.status_line,
-                              b.timeout_ns, round, who, true, 0, false);
+            const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;
+            stop = epoch_reached(mine, target, b.e)
+                       ? false
+                       : poll_until(b.ctr, [&](uint32_t cur) { return epoch_reached(cur, target, b.e); },
+                                    b.status_line, b.timeout_ns, round, who, true, 0, false);
         } else {
             const uint32_t before = atom_inc_release_gpu(b.ctr, b.e.Mm1);
             target = epoch_target(before, b.e, c);

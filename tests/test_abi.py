@@ -179,3 +179,16 @@ def test_no_device_is_an_error_not_a_crash(built):
 def test_error_strings(built):
     assert cns.error_string(cns.CNS_ERR_TIMEOUT) == "timeout"
     assert cns.error_string(12345) == "unknown error"
+
+
+def test_python_constants_match_the_header():
+    """Every integer #define of cns.h has the same value in the binding."""
+    import re
+    src = open(HEADER, encoding="utf-8").read()
+    found = 0
+    for name, val in re.findall(r"^#define (CNS_[A-Z0-9_]+) \(?(\d+)u?\)?", src, flags=re.M):
+        if hasattr(_native, name):
+            assert getattr(_native, name) == int(val), name
+            found += 1
+    assert found >= 10
+    assert _native.CNS_SYNCALL_DIE_LOCAL_ALIGN == 8192
