@@ -520,3 +520,30 @@ def test_largest_resident_grid(cns, mode):
         d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_XORSHIFT, P + 4, ci.ring_payload(77, P + 4, 4), 1,
                                   threads=32, cluster_dim=4 if mode == HARD else 0, check=False)
         assert rc == cns.CNS_ERR_NOT_RESIDENT
+
+
+def test_new_workspace_is_aligned_for_die_local_copies(cns):
+    for _ in range(4):
+        ws = cns.new_workspace()
+        assert ws.data_ptr() % cns.CNS_SYNCALL_DIE_LOCAL_ALIGN == 0
+        assert ws.numel() * 4 == cns.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES
+
+
+@pytest.mark.parametrize("offset", [0, 1024, 4096, 5120, 128])
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_die_local_results_do_not_depend_on_placement(cns, offset, mode):
+    """Die-local copies on a workspace at any 128-byte-aligned place: where the copies land decides only
+    whether they share a die (the speed), never the result."""
+    import torch
+    big = torch.zeros(1 << 16, dtype=torch.int32, device="cuda")
+    skip = ((-big.data_ptr()) % 8192 + offset) // 4
+    ws = big[skip:skip + cns.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES // 4]
+    assert cns.syncall_workspace_init(ws, ws.numel() * 4, 0, None) == 0
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    b0 = to_dev_u32(v0)
+    b1 = torch.zeros_like(b0)
+    d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_RING_ROTATE, 148, b0, b1, 3001, elems=4, workspace=ws,
+                            variant=cns.CNS_BARRIER_DIE_LOCAL)
+    assert rc == 0 and d.device_status == 0
+    np.testing.assert_array_equal(from_dev_u32(b1).reshape(148, 4), np.roll(v0, -3001, axis=0))
+    assert d.final_counter == 3001 * (148 if mode == SOFT else 148 // d.cluster_used)
