@@ -301,6 +301,36 @@ __device__ __forceinline__ Pending arrive_flip(const Barrier &b, uint32_t round,
     return Pending{before & kSense, false, false};
 }
 
+// The arrival of variants 5 and 8 on the two counter copies; returns the
+// near copy's old value and sets *target.  The far increment is issued with
+// the near one, so the two may land in either order and another
+// participant's next-round increment may reach the near copy before this
+// one does: the returned value can then lie one epoch ahead.  So from the
+// second barrier on the target is the cursor's (the last target plus P),
+// whatever the returned value; in the first barrier, whose target comes from
+// the returned value, the far increment is a release that lands after the
+// near one, so no participant can leave the first barrier before every
+// first-round increment is on every copy.  (The all-interleavings model of
+// both copies shows the returned value's target failing without these two
+// rules and holding with them.)
+template <int V>
+__device__ __forceinline__ uint32_t die_local_arrive(const Barrier &b, const EpochCursor &c, uint32_t *target)
+{
+    if constexpr (V == kBvDieLocal)
+        fence_release_gpu();
+    uint32_t before;
+    if (c.valid) {
+        red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
+        before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
+        *target = c.end;
+    } else {
+        before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
+        red_inc_release_gpu(b.ctr2, b.e.Mm1);
+        *target = epoch_target(before, b.e);
+    }
+    return before;
+}
+
 // The variant is a compile-time parameter of everything below: each
 // variant's kernel carries only its own path.  (With one kernel for all
 // variants, a change in one variant's code moved another's round time by
@@ -313,11 +343,7 @@ __device__ __forceinline__ Pending barrier_arrive(const Barrier &b, EpochCursor 
     } else {
         Pending pd{0u, false, false};
         if constexpr (V == kBvDieLocal || V == kBvArrivalDieLocal) {
-            if constexpr (V == kBvDieLocal)
-                fence_release_gpu();
-            red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
-            const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
-            pd.target = epoch_target(before, b.e, c);
+            const uint32_t before = die_local_arrive<V>(b, c, &pd.target);
             // every arrival reaches both copies, so an increment of the near
             // copy that completes the round read all the others (as in 1)
             const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;
@@ -394,10 +420,7 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
         uint32_t target;
         bool stop;
         if constexpr (V == kBvDieLocal) {
-            fence_release_gpu();
-            red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
-            const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
-            target = epoch_target(before, b.e, c);
+            const uint32_t before = die_local_arrive<V>(b, c, &target);
             const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;
             if (epoch_reached(mine, target, b.e)) {
                 // the round's last arrival on the near copy: every other arrival
@@ -408,9 +431,7 @@ __device__ __forceinline__ bool arrive_and_wait(const Barrier &b, EpochCursor &c
                 stop = poll_epoch(b.ctr, target, b.e, b.status_line, b.timeout_ns, round, who, true);
             }
         } else if constexpr (V == kBvArrivalDieLocal) {
-            red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
-            const uint32_t before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
-            target = epoch_target(before, b.e, c);
+            const uint32_t before = die_local_arrive<V>(b, c, &target);
             const uint32_t mine = (before == b.e.Mm1) ? 0u : before + 1u;
             stop = epoch_reached(mine, target, b.e)
                        ? false

@@ -101,6 +101,11 @@ __device__ __forceinline__ void red_inc_relaxed_gpu(uint32_t *p, uint32_t bound)
     asm volatile("red.relaxed.gpu.global.inc.u32 [%0], %1;" ::"l"(p), "r"(bound) : "memory");
 }
 
+__device__ __forceinline__ void red_inc_release_gpu(uint32_t *p, uint32_t bound)
+{
+    asm volatile("red.release.gpu.global.inc.u32 [%0], %1;" ::"l"(p), "r"(bound) : "memory");
+}
+
 __device__ __forceinline__ void fence_release_gpu()
 {
     asm volatile("fence.release.gpu;" ::: "memory");

@@ -362,3 +362,96 @@ def explore_hard_one_barrier(P: int, C: int, rounds: int, M: int | None = None, 
                 res.deadlocks += 1
         stack.extend(succ)
     return res
+
+
+# Die-local counter copies ---------------------------------------------------
+#
+# Two copies of the counter; participant i calls copy near[i] its near copy.
+# One arrival is a fire-and-forget increment of the far copy and a returning
+# increment of the near copy, issued together after one release fence: the
+# two land in either order, and the far one may still be in flight when the
+# participant has left the barrier.  Its next arrival's fence waits for both,
+# so a participant has at most one round's increments in flight.  The
+# returned old value of the near copy gives the target; the participant then
+# polls its near copy (the arrival whose increment completed the round there
+# leaves at once).
+#
+#   target="formula"  target = ((before / P) + 1) * P from the returned value,
+#                     in every round (the pages' arithmetic)
+#   target="cursor"   from the second round on, the target is the last one
+#                     plus P (the formula only in the first round)
+#   safe_first=True   in the first round the far increment is issued only
+#                     after the near one has returned (a release increment
+#                     of the far copy orders it after the near one)
+
+def explore_die_local(near, rounds: int, M: int | None = None, start: int = 0, target: str = "cursor",
+                      safe_first: bool = True, max_states: int = 2_000_000) -> Result:
+    P = len(near)
+    arith = Arith("modular", P, M if M is not None else 4 * P)
+    res = Result()
+    # participant: (k, phase, target, cursor end or -1, far pending, near pending)
+    #   phase 0 between barriers, 1 waiting for the near increment, 2 polling
+    init = ((start % arith.M, start % arith.M), tuple((0, 0, 0, -1, False, False) for _ in range(P)))
+    seen = set()
+    stack = [init]
+
+    def arrived(m, k):
+        return m[0] > k or (m[0] == k and m[1] >= 1)
+
+    while stack:
+        state = stack.pop()
+        if state in seen:
+            continue
+        seen.add(state)
+        res.states += 1
+        if res.states > max_states:
+            raise RuntimeError("state space larger than max_states")
+        cs, parts = state
+        succ = []
+        for i, (k, ph, t, cend, pf, pn) in enumerate(parts):
+            me, other = near[i], 1 - near[i]
+
+            def put(v, ncs=cs):
+                succ.append((ncs, parts[:i] + (v,) + parts[i + 1:]))
+
+            def bump(copy):
+                nc = list(cs)
+                nc[copy] = arith.arrive(nc[copy])
+                return tuple(nc)
+
+            if pf:   # the far increment lands (any time while in flight)
+                put((k, ph, t, cend, False, pn), bump(other))
+            if k == rounds:
+                continue
+            if ph == 0:
+                if pf or pn:
+                    continue   # the next arrival's fence waits for the last one's increments
+                first_safe = safe_first and k == 0
+                put((k, 1, 0, cend, not first_safe, True))
+            elif ph == 1 and pn:
+                before = cs[me]
+                if target == "cursor" and cend >= 0:
+                    tgt = cend
+                else:
+                    tgt = arith.target(before)
+                if tgt != (start + (k + 1) * P) % arith.M:
+                    res.epoch_violations += 1
+                far_now = pf or (safe_first and k == 0)
+                nxt = (tgt + P) % arith.M
+                if arith.reached(arith.arrive(before), tgt):
+                    if not all(arrived(m, k) for m in parts):
+                        res.safety_violations += 1
+                    put((k + 1, 0, 0, nxt, far_now, False), bump(me))
+                else:
+                    put((k, 2, tgt, nxt, far_now, False), bump(me))
+            elif ph == 2 and arith.reached(cs[me], t):
+                if not all(arrived(m, k) for m in parts):
+                    res.safety_violations += 1
+                put((k + 1, 0, 0, cend, pf, pn))
+        if not succ:
+            if all(p[0] == rounds for p in parts):
+                res.completed += 1
+            else:
+                res.deadlocks += 1
+        stack.extend(succ)
+    return res

@@ -156,3 +156,55 @@ def test_hard_one_barrier_misaligned_start_is_caught():
 def test_hard_one_barrier_wrong_member_prediction_is_caught(step):
     # G = 2: members that step by anything else leave early or never
     assert not explore_hard_one_barrier(4, 2, 3, member_step=step).ok
+
+
+# --- die-local counter copies (variants 5 and 8) ------------------------------------
+
+from oracle.protocol import explore_die_local  # noqa: E402
+
+NEARS = [(0, 1), (1, 0), (0, 1, 1), (0, 0, 1), (0, 1, 0, 1), (0, 0), (1, 1, 1)]
+
+
+@pytest.mark.parametrize("near", NEARS)
+@pytest.mark.parametrize("R", [1, 2, 3])
+def test_die_local_copies_safe_and_live(near, R):
+    """Cursor targets after the first barrier and a first barrier whose far
+    increment lands after the near one: safe, every epoch right, no deadlock,
+    whichever order the two increments of each arrival land in."""
+    r = explore_die_local(near, R)
+    assert r.ok and r.completed > 0, r
+
+
+@pytest.mark.parametrize("near", [(0, 1), (0, 1, 1)])
+@pytest.mark.parametrize("mult", [1, 2, 3])
+def test_die_local_copies_through_the_wrap(near, mult):
+    P = len(near)
+    M = 4 * P
+    r = explore_die_local(near, 3, M=M, start=(M - mult * P) % M)
+    assert r.ok and r.completed > 0, r
+
+
+@pytest.mark.parametrize("near", [(0, 1), (0, 1, 1), (0, 1, 0, 1)])
+def test_die_local_target_from_the_returned_value_fails_later(near):
+    """Taking every round's target from the near copy's returned value: a
+    participant whose near increment lands after another's next-round
+    increment computes the next epoch's target and the barrier deadlocks."""
+    r = explore_die_local(near, 3, target="formula")
+    assert r.epoch_violations > 0 and r.deadlocks > 0
+
+
+@pytest.mark.parametrize("near", [(0, 1), (0, 0, 1)])
+def test_die_local_unordered_first_barrier_fails(near):
+    """Cursor targets alone are not enough: with the far increment free to
+    land before the near one in the first barrier, that barrier's target (from
+    the returned value) can be an epoch ahead."""
+    r = explore_die_local(near, 2, target="cursor", safe_first=False)
+    assert r.epoch_violations > 0 and r.deadlocks > 0
+
+
+def test_die_local_start_off_the_epoch_grid_is_caught():
+    """A count that does not start at a multiple of P (a workspace reused with another P) breaks the
+    epochs on the copies: the model reports it, as the library documents for this variant."""
+    assert explore_die_local((0, 1, 1), 2).ok
+    bad = explore_die_local((0, 1), 2, start=1)
+    assert bad.epoch_violations > 0
