@@ -492,6 +492,10 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     if ((d->barrier_variant == CNS_BARRIER_DIE_LOCAL || d->barrier_variant == CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL) &&
         d->workspace_bytes < CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES)
         return CNS_ERR_INVALID_VALUE;
+    if ((d->barrier_variant == CNS_BARRIER_DIE_LOCAL || d->barrier_variant == CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL) &&
+        reinterpret_cast<uintptr_t>(d->workspace_dev) % CNS_SYNCALL_DIE_LOCAL_ALIGN != 0)
+        CNS_LOG(2, "die-local workspace %p is not %d-byte aligned: its counter copies may share a die (slower, "
+                   "same results)", d->workspace_dev, CNS_SYNCALL_DIE_LOCAL_ALIGN);
     if (rounds < 0 || used_cores < 0 || aiv_ratio < 0 || d->launch_ctas <= 0 || d->elems < 0)
         return CNS_ERR_INVALID_VALUE;
     const int threads = d->threads ? d->threads : 256;
