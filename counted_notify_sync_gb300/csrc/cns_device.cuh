@@ -110,32 +110,6 @@ __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// The epoch that the caller's previous barrier closed: [start, start + P) in
-// Z_M, start a multiple of P.  In a well-formed round an arrival's `before`
-// lies in that epoch, so ((before / P) + 1) * P mod M is just `end`; the
-// cursor gives the same target as the formula without the division, and the
-// formula is still evaluated whenever `before` falls outside (first round, or
-// a counter that someone else moved).
-struct EpochCursor {
-    uint32_t start;
-    uint32_t end;     // start + P in Z_M
-    bool valid;
-};
-
-__device__ __forceinline__ uint32_t epoch_target(uint32_t before, const Epoch &e, const EpochCursor &c)
-{
-    if (c.valid && before - c.start < e.P)   // wraps to >= P when before < start (start <= M - P)
-        return c.end;
-    return epoch_target(before, e);
-}
-
-__device__ __forceinline__ void epoch_advance(EpochCursor &c, uint32_t target, const Epoch &e)
-{
-    c.start = target;
-    c.end = (target == e.Mm1 + 1u - e.P) ? 0u : target + e.P;   // M - P wraps to 0
-    c.valid = true;
-}
-
 // Status line of the workspace: [0] status, [1] abort flag, [2] round of the
 // first timeout, [3] CTA of the first timeout.
 __device__ __forceinline__ void raise_status(uint32_t *status_line, uint32_t code, uint32_t round, uint32_t who)
@@ -254,20 +228,9 @@ __device__ __forceinline__ bool poll_epoch(const uint32_t *word, uint32_t target
 // The elected thread's part of one barrier: arrive, compute the target from
 // the returned value, wait for it.  Returns true if the caller must stop.
 // Variant 5: make b.ctr the copy whose atomics return sooner from this SM.
-// Adding 0 leaves both counts unchanged, whoever else is arriving.
 __device__ __forceinline__ void choose_near_copy(Barrier &b)
 {
-    // a dependent chain: each address depends on the last result; (x >> 31)
-    // picks word 0 or 1 of the same (otherwise unused) 128-byte line
-    uint32_t x = 0;
-    const uint64_t t0 = globaltimer_ns();
-    for (int i = 0; i < 8; ++i)
-        x = atom_add_relaxed_gpu(b.ctr + (x >> 31), 0u);
-    const uint64_t t1 = globaltimer_ns();
-    for (int i = 0; i < 8; ++i)
-        x = atom_add_relaxed_gpu(b.ctr2 + (x >> 31), 0u);
-    const uint64_t t2 = globaltimer_ns();
-    if (t2 - t1 < t1 - t0) {
+    if (copy_is_farther(b.ctr, b.ctr2)) {
         uint32_t *t = b.ctr;
         b.ctr = b.ctr2;
         b.ctr2 = t;
@@ -303,34 +266,12 @@ __device__ __forceinline__ Pending arrive_flip(const Barrier &b, uint32_t round,
     return Pending{before & kSense, false, false};
 }
 
-// The arrival of variants 5 and 8 on the two counter copies; returns the
-// near copy's old value and sets *target.  The far increment is issued with
-// the near one, so the two may land in either order and another
-// participant's next-round increment may reach the near copy before this
-// one does: the returned value can then lie one epoch ahead.  So from the
-// second barrier on the target is the cursor's (the last target plus P),
-// whatever the returned value; in the first barrier, whose target comes from
-// the returned value, the far increment is a release that lands after the
-// near one, so no participant can leave the first barrier before every
-// first-round increment is on every copy.  (The all-interleavings model of
-// both copies shows the returned value's target failing without these two
-// rules and holding with them.)
+// The arrival of variants 5 and 8 on the two counter copies (the rules that
+// keep both landing orders safe are at copies_arrive).
 template <int V>
 __device__ __forceinline__ uint32_t die_local_arrive(const Barrier &b, const EpochCursor &c, uint32_t *target)
 {
-    if constexpr (V == kBvDieLocal)
-        fence_release_gpu();
-    uint32_t before;
-    if (c.valid) {
-        red_inc_relaxed_gpu(b.ctr2, b.e.Mm1);
-        before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
-        *target = c.end;
-    } else {
-        before = atom_inc_relaxed_gpu(b.ctr, b.e.Mm1);
-        red_inc_release_gpu(b.ctr2, b.e.Mm1);
-        *target = epoch_target(before, b.e);
-    }
-    return before;
+    return copies_arrive<V == kBvDieLocal>(b.ctr, b.ctr2, b.e, c, target);
 }
 
 // The variant is a compile-time parameter of everything below: each

@@ -36,6 +36,35 @@ __global__ void ring_kernel(uint4 *b0, uint4 *b1, uint32_t participants, int64_t
         status[p] = st;
 }
 
+// The same rounds with the die-local barrier: the CTA's state lives in shared
+// memory, set before the first barrier.
+__global__ void ring_kernel_die_local(uint4 *b0, uint4 *b1, uint32_t participants, int64_t rounds, void *ws,
+                                      uint64_t timeout_ns, uint32_t short_cta, int *status)
+{
+    __shared__ cns_soft_state_t st;
+    const uint32_t p = blockIdx.x;
+    if (p >= participants)
+        return;
+    if (threadIdx.x == 0)
+        st = cns_soft_state_t CNS_SOFT_STATE_INIT;
+    __syncthreads();
+    const int64_t mine = (p == short_cta) ? rounds - 1 : rounds;
+    int rc = 0;
+    for (int64_t r = 0; r < rounds; ++r) {
+        const uint4 *src = (r & 1) ? b1 : b0;
+        uint4 *dst = (r & 1) ? b0 : b1;
+        if (threadIdx.x == 0)
+            dst[p] = src[(p + 1 == participants) ? 0 : p + 1];
+        if (r >= mine)
+            break;
+        rc = cns_syncall_soft_die_local(ws, participants, timeout_ns, &st);
+        if (rc != CNS_SUCCESS)
+            break;
+    }
+    if (threadIdx.x == 0)
+        status[p] = rc;
+}
+
 __global__ void record_kernel(uint32_t *count, int mode, uint32_t v, int per_thread)
 {
     for (int i = 0; i < per_thread; ++i)
@@ -56,6 +85,17 @@ extern "C" int user_ring(int32_t ctas, int32_t threads, uint32_t participants, i
 {
     void *args[] = {&b0, &b1, &participants, &rounds, &ws, &timeout_ns, &short_cta, &status};
     cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ring_kernel), dim3(ctas),
+                                                dim3(threads), args, 0, 0);
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    return static_cast<int>(e);
+}
+
+extern "C" int user_ring_die_local(int32_t ctas, int32_t threads, uint32_t participants, int64_t rounds, void *b0,
+                                   void *b1, void *ws, uint64_t timeout_ns, uint32_t short_cta, int *status)
+{
+    void *args[] = {&b0, &b1, &participants, &rounds, &ws, &timeout_ns, &short_cta, &status};
+    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ring_kernel_die_local), dim3(ctas),
                                                 dim3(threads), args, 0, 0);
     if (e == cudaSuccess)
         e = cudaDeviceSynchronize();

@@ -47,44 +47,50 @@ def user(cns):
     L = ctypes.CDLL(OUT)
     i32, u32, i64, u64, vp = ctypes.c_int32, ctypes.c_uint32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
     L.user_ring.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
+    L.user_ring_die_local.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
     L.user_record.argtypes = [vp, ctypes.c_int, u32, i32, i32, ctypes.c_int]
     L.user_wait.argtypes = [vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp]
-    for f in (L.user_ring, L.user_record, L.user_wait):
+    for f in (L.user_ring, L.user_ring_die_local, L.user_record, L.user_wait):
         f.restype = ctypes.c_int
     return L
 
 
-def _ring(cns, user, ctas, P, rounds, start=0, threads=256, short_cta=0xFFFFFFFF, timeout_ns=0):
+def _ring(cns, user, ctas, P, rounds, start=0, threads=256, short_cta=0xFFFFFFFF, timeout_ns=0, die_local=False):
     import torch
     v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P, 4)
     b0 = to_dev_u32(np.vstack([v0, np.zeros((ctas - P, 4), np.uint32)]))
     b1 = torch.zeros_like(b0)
-    ws = cns.new_workspace(start_value=start, die_local=False)
+    ws = cns.new_workspace(start_value=start, die_local=die_local)
     status = torch.full((ctas,), -1, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
-    rc = user.user_ring(ctas, threads, P, rounds, b0.data_ptr(), b1.data_ptr(), ws.data_ptr(), timeout_ns,
-                        short_cta, status.data_ptr())
+    launch = user.user_ring_die_local if die_local else user.user_ring
+    rc = launch(ctas, threads, P, rounds, b0.data_ptr(), b1.data_ptr(), ws.data_ptr(), timeout_ns, short_cta,
+                status.data_ptr())
     assert rc == 0, rc
     got = from_dev_u32(b0 if rounds % 2 == 0 else b1).reshape(ctas, 4)[:P]
     return v0, got, from_dev_u32(ws), status.cpu().numpy()
 
 
+@pytest.mark.parametrize("die_local", [False, True])
 @pytest.mark.parametrize("ctas,P,rounds,threads", [(148, 148, 10001, 256), (8, 8, 1000, 256), (111, 111, 777, 96),
                                                      (148, 64, 2001, 256), (5, 5, 3, 32), (1, 1, 10, 64)])
-def test_fused_soft_barrier_ring_matches_oracle(cns, user, ctas, P, rounds, threads):
-    v0, got, ws, status = _ring(cns, user, ctas, P, rounds, threads=threads)
+def test_fused_soft_barrier_ring_matches_oracle(cns, user, ctas, P, rounds, threads, die_local):
+    v0, got, ws, status = _ring(cns, user, ctas, P, rounds, threads=threads, die_local=die_local)
     want, fc, rc = oracle.syncall_run_ring(oracle.WL_RING_ROTATE, v0, rounds)
     assert rc == oracle.OK
     np.testing.assert_array_equal(got, want)
     assert int(ws[0]) == fc == (rounds * P) % oracle.counter_modulus(P)
+    if die_local:
+        assert int(ws[1024]) == fc   # the second copy counted every arrival too
     assert (status[:P] == 0).all() and (status[P:] == -1).all()   # CTAs past P never called it
 
 
+@pytest.mark.parametrize("die_local", [False, True])
 @pytest.mark.parametrize("P", [148, 111, 7])
-def test_fused_soft_barrier_through_the_wrap(cns, user, P):
+def test_fused_soft_barrier_through_the_wrap(cns, user, P, die_local):
     M = oracle.counter_modulus(P)
     start = M - 5 * P
-    v0, got, ws, status = _ring(cns, user, P, P, 12, start=start)
+    v0, got, ws, status = _ring(cns, user, P, P, 12, start=start, die_local=die_local)
     want, fc, rc = oracle.syncall_run_ring(oracle.WL_RING_ROTATE, v0, 12, start=start)
     assert rc == oracle.OK
     np.testing.assert_array_equal(got, want)
@@ -92,12 +98,13 @@ def test_fused_soft_barrier_through_the_wrap(cns, user, P):
     assert (status == 0).all()
 
 
-def test_fused_soft_barrier_times_out_when_a_cta_stops_short(cns, user):
+@pytest.mark.parametrize("die_local", [False, True])
+def test_fused_soft_barrier_times_out_when_a_cta_stops_short(cns, user, die_local):
     """CTA 5 takes one barrier fewer: the others give up on the last barrier
     after their 20 ms limit, with CNS_ERR_TIMEOUT in every CTA and in the
     workspace's status line, and no CTA is left waiting."""
     P = 8
-    v0, got, ws, status = _ring(cns, user, P, P, 4, short_cta=5, timeout_ns=20_000_000)
+    v0, got, ws, status = _ring(cns, user, P, P, 4, short_cta=5, timeout_ns=20_000_000, die_local=die_local)
     line = ws[32:36]
     assert int(line[0]) == cns.CNS_ERR_TIMEOUT and int(line[1]) == 1 and int(line[3]) != 5
     assert status[5] == 0
