@@ -155,6 +155,25 @@ __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// 16-byte relaxed gpu-scope load and store: served by L2, past the SM's L1
+// (data that other SMs write every round gains nothing from L1).
+__device__ __forceinline__ uint4 ld_relaxed_gpu_v4(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_v4(uint4 *p, const uint4 &v)
+{
+    asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t *p)
 {
     uint64_t v;
