@@ -40,8 +40,8 @@ __global__ void probe_rtt_kernel(int kind, int probe_cta, int iters, uint32_t *l
     out[1] = smid() | (static_cast<uint64_t>(x & 0u) << 32);
 }
 
-// The same ring-rotate rounds as the headline workload, separated by the
-// CUDA runtime's own grid barrier (cooperative groups), for comparison.
+// The ring-rotate rounds of CNS_WL_RING_ROTATE (one uint4 per CTA), separated
+// by the CUDA runtime's own grid barrier (cooperative groups), for comparison.
 __global__ void probe_grid_sync_kernel(uint4 *buf0, uint4 *buf1, int64_t rounds)
 {
     cooperative_groups::grid_group grid = cooperative_groups::this_grid();

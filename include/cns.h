@@ -556,8 +556,9 @@ int cns_probe_same_address_throughput(int32_t grid, int32_t threads, int32_t ite
                                       cns_stream_t stream);
 
 /*
- * cns_probe_grid_sync -- the headline's ring-rotate rounds (each CTA copies
- * one uint4 from its ring neighbour, buffers swap every round) separated by
+ * cns_probe_grid_sync -- ring-rotate rounds of syncall_run's
+ * CNS_WL_RING_ROTATE workload (each CTA copies one uint4 from its ring
+ * neighbour, buffers swap every round) separated by
  * the CUDA runtime's cooperative-groups grid barrier instead of SYNCALL: a
  * reference point for the barrier's cost.  No timeout: the launch is
  * cooperative, so the grid is co-resident or the call fails.
