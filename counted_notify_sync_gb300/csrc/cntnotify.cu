@@ -240,28 +240,25 @@ constexpr int kChunk = 16;
 constexpr uint32_t kMicroWait = 1u << 8;
 constexpr uint32_t kMicroSet = 1u << 11;
 
+// Built with selects, not branches: the lanes of a warp stage ops of every
+// kind and mode at once.
 __device__ __forceinline__ uint4 sm_micro(const uint4 &op)
 {
     const uint32_t kind = op.x, mode = op.y, v = op.z;
-    const bool clear = op.w != 0u;
-    const uint32_t rec = static_cast<uint32_t>(CNS_OUT_RECORD) << 9;
-    if (kind == 0u) {
-        switch (mode) {
-        case CNS_REC_SET: return make_uint4(0u, v, 0u, rec | kMicroSet);
-        case CNS_REC_ADD: return make_uint4(~0u, 0u, v, rec);
-        case CNS_REC_BIT_OR: return make_uint4(~0u, v, 0u, rec);
-        case CNS_REC_BIT_AND: return make_uint4(v, 0u, 0u, rec);
-        default: break;
-        }
-    } else if (kind == 1u && mode <= 4u) {
-        const uint32_t bits = mode == CNS_WAIT_LESS ? 1u
-                            : mode == CNS_WAIT_BIGGER ? 4u
-                            : mode == CNS_WAIT_BIGGER_OR_EQUAL ? 6u
-                                                               : 2u;   // EQUAL, EQUAL_WITH_BITMASK
-        const uint32_t mask = mode == CNS_WAIT_EQUAL_WITH_BITMASK ? v : ~0u;
-        return make_uint4(mask, v, 0u, bits | (clear ? bits << 4 : 0u) | kMicroWait);
-    }
-    return make_uint4(~0u, 0u, 0u, static_cast<uint32_t>(CNS_OUT_INVALID) << 9);
+    const bool rec = kind == 0u && (mode <= 2u || mode == 4u);   // SET, ADD, BIT_OR, BIT_AND
+    const bool wait = kind == 1u && mode <= 4u;
+    // record: ((c & a) | o) + d
+    const uint32_t a = mode == CNS_REC_SET ? 0u : (mode == CNS_REC_BIT_AND ? v : ~0u);
+    const uint32_t o = (mode == CNS_REC_SET || mode == CNS_REC_BIT_OR) ? v : 0u;
+    const uint32_t d = mode == CNS_REC_ADD ? v : 0u;
+    // wait: the compare results that release it, 4 bits per mode (LESS 1, EQUAL 2, BIGGER 4,
+    // BIGGER_OR_EQUAL 6, EQUAL_WITH_BITMASK 2)
+    const uint32_t bits = (0x26421u >> (4u * (mode & 7u))) & 0xFu;
+    const uint32_t wflags = bits | (op.w != 0u ? bits << 4 : 0u) | kMicroWait;
+    const uint32_t rflags = (static_cast<uint32_t>(CNS_OUT_RECORD) << 9) | (mode == CNS_REC_SET ? kMicroSet : 0u);
+    const uint32_t mask = mode == CNS_WAIT_EQUAL_WITH_BITMASK ? v : ~0u;
+    return make_uint4(rec ? a : (wait ? mask : ~0u), rec ? o : (wait ? v : 0u), rec ? d : 0u,
+                      rec ? rflags : (wait ? wflags : static_cast<uint32_t>(CNS_OUT_INVALID) << 9));
 }
 
 // One micro-op applied to count c; *outcome gets the op's CNS_OUT_* code.
