@@ -430,11 +430,24 @@ def secondary(cns, torch, peaks):
                 best = (cfg, rc)
         cfg, rc = best
         ok = rc == 0 and np.array_equal(bufs[1].cpu().numpy().view(np.uint32), want_cs)
+        # the host's side: one run enqueued without waiting (sync = 0), the call's own time against the
+        # time until the GPU is done
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        _, rc_async, _, _ = cns.run_pipeline(done, ack, 4096, 256, 1000, s1, s2, timeout_s=10, buffers=bufs,
+                                             areas=areas, sync=False)
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        t2 = time.perf_counter()
+        ok = ok and rc_async == 0 and cns.cntnotify_query_status(done)[1] == 0 \
+            and cns.cntnotify_query_status(ack)[1] == 0 \
+            and np.array_equal(bufs[1].cpu().numpy().view(np.uint32), want_cs)
         by_areas[areas] = {
             "status": rc, "correct": bool(ok), "elapsed_ms": round(cfg.elapsed_ms, 3),
             "producer_ms": round(cfg.producer_ms, 3),
             "records_per_s": round(4096 * 1000 / max(cfg.producer_ms * 1e-3, 1e-12), 0),
-            "round_trips_per_s": round(1000 / max(cfg.elapsed_ms * 1e-3, 1e-12), 1)}
+            "round_trips_per_s": round(1000 / max(cfg.elapsed_ms * 1e-3, 1e-12), 1),
+            "host_submit_us_per_round": round((t1 - t0) * 1e3, 2), "until_done_us_per_round": round((t2 - t0) * 1e3, 2)}
     cns.cntnotify_destroy(done)
     cns.cntnotify_destroy(ack)
     out["notify_pipeline_4096x1000"] = dict(
