@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="run one small launch pattern for a profiler capture and exit")
     ap.add_argument("--areas", type=int, default=2, choices=(1, 2), help="tile areas of --case pipeline")
+    ap.add_argument("--consumer-wait", type=int, default=0, choices=(0, 1),
+                    help="--case pipeline: 0 = the wait as a stream task, 1 = inside the consumer kernel")
     return ap.parse_args()
 
 
@@ -417,12 +419,14 @@ def secondary(cns, torch, peaks):
     n = 4096 * 256
     want_cs = np.array([(2654435761 * (n * (n - 1) // 2) + n * r) % (1 << 32) for r in range(1000)], dtype=np.uint32)
     by_areas = {}
-    for areas in (2, 1):
-        cns.run_pipeline(done, ack, 4096, 256, 20, s1, s2, timeout_s=10, buffers=bufs, areas=areas)   # warm-up
+    # consumer_wait 0: the wait is a stream task before the consumer kernel; 1: the consumer kernel takes it
+    for areas, cw in ((2, 0), (2, 1), (1, 0), (1, 1)):
+        cns.run_pipeline(done, ack, 4096, 256, 20, s1, s2, timeout_s=10, buffers=bufs, areas=areas,
+                         consumer_wait=cw)   # warm-up
         best = None
         for _ in range(3):
             cfg, rc, cs, rel = cns.run_pipeline(done, ack, 4096, 256, 1000, s1, s2, timeout_s=10, buffers=bufs,
-                                                areas=areas)
+                                                areas=areas, consumer_wait=cw)
             if rc != 0:
                 best = (cfg, rc)
                 break
@@ -435,14 +439,14 @@ def secondary(cns, torch, peaks):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         _, rc_async, _, _ = cns.run_pipeline(done, ack, 4096, 256, 1000, s1, s2, timeout_s=10, buffers=bufs,
-                                             areas=areas, sync=False)
+                                             areas=areas, consumer_wait=cw, sync=False)
         t1 = time.perf_counter()
         torch.cuda.synchronize()
         t2 = time.perf_counter()
         ok = ok and rc_async == 0 and cns.cntnotify_query_status(done)[1] == 0 \
             and cns.cntnotify_query_status(ack)[1] == 0 \
             and np.array_equal(bufs[1].cpu().numpy().view(np.uint32), want_cs)
-        by_areas[areas] = {
+        by_areas[areas, cw] = {
             "status": rc, "correct": bool(ok), "elapsed_ms": round(cfg.elapsed_ms, 3),
             "producer_ms": round(cfg.producer_ms, 3),
             "records_per_s": round(4096 * 1000 / max(cfg.producer_ms * 1e-3, 1e-12), 0),
@@ -451,7 +455,8 @@ def secondary(cns, torch, peaks):
     cns.cntnotify_destroy(done)
     cns.cntnotify_destroy(ack)
     out["notify_pipeline_4096x1000"] = dict(
-        by_areas[2], areas=2, one_area=by_areas[1],
+        by_areas[2, 0], areas=2, consumer_wait="stream", in_kernel_wait=by_areas[2, 1], one_area=by_areas[1, 0],
+        one_area_in_kernel_wait=by_areas[1, 1],
         note="best of 3 runs; records/s over the summed recording phases (device clock: from the producer's "
              "CTA 0 being allowed to record to the consumer-side wait releasing), round trips/s over the whole "
              "run (events)")
@@ -669,14 +674,16 @@ def case_statemachine(args):
 
 
 def case_pipeline(args):
-    """The two-stream pipeline, 4096 tiles x 256 words, 20 rounds, --areas tile areas (profiling)."""
+    """The two-stream pipeline, 4096 tiles x 256 words, 20 rounds, --areas tile areas, --consumer-wait
+    (profiling)."""
     import torch
     import counted_notify_sync_gb300 as cns
     cns.build()
     rc1, done = cns.cntnotify_create(0)
     rc2, ack = cns.cntnotify_create(0)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
-    cfg, rc, cs, rel = cns.run_pipeline(done, ack, 4096, 256, 20, s1, s2, timeout_s=10, areas=args.areas)
+    cfg, rc, cs, rel = cns.run_pipeline(done, ack, 4096, 256, 20, s1, s2, timeout_s=10, areas=args.areas,
+                                        consumer_wait=args.consumer_wait)
     cns.cntnotify_destroy(done)
     cns.cntnotify_destroy(ack)
     assert rc == 0, rc

@@ -83,9 +83,11 @@ def run_statemachine(ops_dev, init: int, stream=None):
 
 
 def run_pipeline(done, ack, tiles: int, tile_words: int, rounds: int, producer_stream, consumer_stream,
-                 timeout_s: int = 10, producer_ctas: int = 0, sync: bool = True, buffers=None, areas: int = 1):
+                 timeout_s: int = 10, producer_ctas: int = 0, sync: bool = True, buffers=None, areas: int = 1,
+                 consumer_wait: int = 0):
     """Run the two-stream counting pipeline; returns (Pipeline struct, code, checksums, released).
-    areas = 2 alternates the rounds between two tile areas (the tile buffer then holds both)."""
+    areas = 2 alternates the rounds between two tile areas (the tile buffer then holds both);
+    consumer_wait = 1 (CNS_PIPE_WAIT_IN_KERNEL) has the consumer kernel take the wait itself."""
     torch = _torch()
     if buffers is None:
         tiles_buf = torch.empty(max(1, areas) * tiles * tile_words, dtype=torch.int32, device="cuda")
@@ -108,5 +110,6 @@ def run_pipeline(done, ack, tiles: int, tile_words: int, rounds: int, producer_s
     cfg.timeout_s = timeout_s
     cfg.sync = 1 if sync else 0
     cfg.areas = areas
+    cfg.consumer_wait = consumer_wait
     rc = _native.cns_pipeline_run(cfg)
     return cfg, rc, checksums, released

@@ -68,6 +68,8 @@ CNS_OUT_WAIT_HELD = 0
 CNS_OUT_WAIT_RELEASED = 1
 CNS_OUT_RECORD = 2
 CNS_OUT_INVALID = 3
+CNS_PIPE_WAIT_STREAM = 0
+CNS_PIPE_WAIT_IN_KERNEL = 1
 
 
 class CnsError(RuntimeError):
@@ -103,7 +105,7 @@ class Pipeline(Structure):
         ("released_dev", c_void_p), ("tiles", c_int64), ("tile_words", c_int32), ("producer_ctas", c_int32),
         ("rounds", c_int64), ("producer_stream", c_void_p), ("consumer_stream", c_void_p), ("timeout_s", c_uint32),
         ("sync", c_int32), ("elapsed_ms", c_float), ("producer_ms", c_float), ("device_status", c_int32),
-        ("consumer_ctas", c_int32), ("areas", c_int32), ("reserved", c_int32),
+        ("consumer_ctas", c_int32), ("areas", c_int32), ("consumer_wait", c_int32),
     ]
 
 

@@ -536,18 +536,22 @@ __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
 // ---------------------------------------------------------------------------
 
 // The pipeline's device-side waits: thread 0 polls *word (relaxed) until
-// `ok(value)`, then an acquire fence.  Returns true if the caller must skip
-// the round: the pipeline's abort word is raised, or the wait ran out, in
-// which case it records CNS_ERR_TIMEOUT in status_word and raises the abort.
+// `ok(value)`, then an acquire fence; the value that passed goes to *seen if
+// given.  Returns true if the caller must skip the round: the pipeline's abort
+// word is raised, or the wait ran out, in which case it records
+// CNS_ERR_TIMEOUT in status_word and raises the abort.
 template <class Ok>
 __device__ __forceinline__ bool pipe_wait(const uint32_t *word, Ok ok, uint64_t timeout_ns, uint32_t *abort,
-                                          uint32_t *status_word)
+                                          uint32_t *status_word, uint32_t *seen = nullptr)
 {
     uint32_t spins = 0;
     uint64_t deadline = 0;
     for (;;) {
-        if (ok(ld_relaxed_gpu(word))) {
+        const uint32_t v = ld_relaxed_gpu(word);
+        if (ok(v)) {
             fence_acquire_gpu();
+            if (seen)
+                *seen = v;
             return false;
         }
         if ((++spins & 63u) == 0u) {
@@ -656,12 +660,60 @@ __global__ void __launch_bounds__(kPipeProducerThreads, 8)
 //   kTwoAreas: the next round's wait is launched the same way behind this
 // kernel; once the CTA is past its own dependency wait (the wait before it,
 // and its clear, are complete), it lets that wait be scheduled.
+//   kInKernelWait: there is no wait kernel; the consumer itself takes the
+// counted-notify wait (BIGGER_OR_EQUAL tiles, isClear) at its start.  CTA 0
+// waits on `done`, clears it, and publishes the round on a `go` word of its
+// own line (release); the other CTAs wait for that word.  (They may not all
+// poll `done`: once CTA 0 has cleared it, a CTA that had not yet looked
+// would wait for ever.)  CTA 0 first waits for the previous round's `go`,
+// which its CTA 0 published after clearing, so the count it then sees holds
+// this round's records only.  With two areas the grid is launched behind the
+// previous consumer with programmatic stream serialization and takes its wait
+// while that one still reads; only then does it wait for the previous grid to
+// complete (so at most two consumer grids are resident) and let the next be
+// scheduled.
 constexpr int kPipeConsumerThreads = 256;
 
-template <bool kTwoAreas>
+struct PipeConsumerWait {   // kInKernelWait only
+    uint32_t *done;         // the notify line: [0] count, [1] status
+    uint32_t *go;           // round + 1 once round's wait has released and cleared
+    uint32_t *abort;
+    uint32_t *observed;     // optional: count seen at release
+    uint64_t *released_at;  // optional: device time of the release
+    uint64_t timeout_ns;
+    uint32_t tiles;
+    uint32_t round;
+};
+
+template <bool kTwoAreas, bool kInKernelWait>
 __global__ void __launch_bounds__(kPipeConsumerThreads, 8)
-    pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words, uint32_t *checksum, uint32_t *ack)
+    pipeline_consumer_kernel(const uint32_t *tiles, int64_t n_words, uint32_t *checksum, uint32_t *ack,
+                             PipeConsumerWait w)
 {
+    if constexpr (kInKernelWait) {
+        if (threadIdx.x == 0) {
+            if (blockIdx.x == 0) {
+                uint32_t seen = 0;
+                const bool stop =
+                    pipe_wait(w.go, [&](uint32_t g) { return static_cast<int32_t>(g - w.round) >= 0; }, w.timeout_ns,
+                              w.abort, w.done + 1) ||
+                    pipe_wait(w.done, [&](uint32_t c) { return c >= w.tiles; }, w.timeout_ns, w.abort, w.done + 1,
+                              &seen);
+                if (!stop) {
+                    if (w.released_at)
+                        *w.released_at = globaltimer_ns();
+                    if (w.observed)
+                        *w.observed = seen;
+                    atom_exch_relaxed_gpu(w.done, 0u);   // the clear comes after the release ...
+                    st_release_gpu(w.go, w.round + 1u);  // ... and before the round is published
+                }
+            } else {
+                pipe_wait(w.go, [&](uint32_t g) { return static_cast<int32_t>(g - (w.round + 1u)) >= 0; },
+                          w.timeout_ns, w.abort, w.done + 1);
+            }
+        }
+        __syncthreads();
+    }
     grid_dependency_wait();
     if (kTwoAreas)
         grid_launch_dependents();
@@ -976,7 +1028,8 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
         return CNS_ERR_NULL_PTR;
     if (cfg->tiles < 1 || cfg->rounds < 0 || cfg->tile_words < 4 || cfg->tile_words > 8192 ||
         cfg->tile_words % 4 != 0 || cfg->producer_ctas < 0 || cfg->tiles > (int64_t(1) << 32) / cfg->tile_words ||
-        cfg->areas < 0 || cfg->areas > 2)
+        cfg->areas < 0 || cfg->areas > 2 || cfg->consumer_wait < CNS_PIPE_WAIT_STREAM ||
+        cfg->consumer_wait > CNS_PIPE_WAIT_IN_KERNEL)
         return CNS_ERR_INVALID_VALUE;
     if (reinterpret_cast<uintptr_t>(cfg->tiles_dev) & 15)
         return CNS_ERR_INVALID_VALUE;
@@ -1082,6 +1135,12 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
                   "stamp buffer"))
             check(cudaMemsetAsync(stamps, 0, 2 * cfg->rounds * sizeof(uint64_t), sp), "memset stamps");
     }
+    const bool in_kernel = cfg->consumer_wait == CNS_PIPE_WAIT_IN_KERNEL;
+    uint32_t *go = nullptr;   // in-kernel waits: the last round released, on a line of its own
+    if (in_kernel && cfg->rounds > 0) {
+        if (check(cudaMallocAsync(reinterpret_cast<void **>(&go), 128, sp), "go word"))
+            check(cudaMemsetAsync(go, 0, 128, sp), "memset go word");
+    }
     check(cudaEventRecord(join, sp), "event");
     check(cudaStreamWaitEvent(sc, join, 0), "stream wait");
     if (timed)
@@ -1112,19 +1171,29 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
         }
         uint32_t *observed = cfg->released_dev ? cfg->released_dev + r : nullptr;
         uint64_t *released = stamps ? stamps + cfg->rounds + r : nullptr;
-        if (two) {
+        if (in_kernel) {
+            const PipeConsumerWait cw = {done->line, go,    abort,           observed, released,
+                                         ack_timeout, static_cast<uint32_t>(cfg->tiles), r32};
+            check(cudaLaunchKernelEx(&ccfg, two ? pipeline_consumer_kernel<true, true>
+                                                : pipeline_consumer_kernel<false, true>,
+                                     static_cast<const uint32_t *>(area), n_words, cfg->checksums_dev + r, ack->line,
+                                     cw),
+                  "consumer launch");
+        } else if (two) {
             check(cudaLaunchKernelEx(&wcfg, cnt_wait_kernel<true, true>, done->line,
                                      static_cast<uint32_t>(w_done.mode), w_done.value, 1u,
                                      wait_timeout_ns(w_done.timeout), observed, abort, released),
                   "wait launch");
-            check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel<true>, static_cast<const uint32_t *>(area),
-                                     n_words, cfg->checksums_dev + r, ack->line),
+            check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel<true, false>,
+                                     static_cast<const uint32_t *>(area), n_words, cfg->checksums_dev + r, ack->line,
+                                     PipeConsumerWait{}),
                   "consumer launch");
         } else {
             if (int e = enqueue_wait(done, sc, &w_done, observed, abort, true, released))
                 rc = e;
-            check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel<false>, static_cast<const uint32_t *>(area),
-                                     n_words, cfg->checksums_dev + r, ack->line),
+            check(cudaLaunchKernelEx(&ccfg, pipeline_consumer_kernel<false, false>,
+                                     static_cast<const uint32_t *>(area), n_words, cfg->checksums_dev + r, ack->line,
+                                     PipeConsumerWait{}),
                   "consumer launch");
         }
     }
@@ -1132,6 +1201,8 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     check(cudaStreamWaitEvent(sp, join, 0), "stream wait");
     if (timed)
         check(cudaEventRecord(T(1), sp), "event");
+    if (go)
+        check(cudaFreeAsync(go, sp), "free go word");
     std::vector<uint64_t> host_stamps;
     if (stamps) {
         host_stamps.resize(2 * cfg->rounds);

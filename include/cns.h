@@ -466,6 +466,11 @@ int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, uint32_t in
 
 /* Two-stream counting pipeline ([CNTN] §5: producers record ADD 1, the waiter
  * waits BIGGER_OR_EQUAL N with isClear = 1 and then continues). */
+
+/* Where the consumer side takes its wait (cns_pipeline_t.consumer_wait). */
+#define CNS_PIPE_WAIT_STREAM 0    /* a cntnotify wait on the consumer stream, before the consumer kernel */
+#define CNS_PIPE_WAIT_IN_KERNEL 1 /* the consumer kernel takes the same wait itself, at its start */
+
 typedef struct {
     cns_cnt_notify_t done;   /* (in) producer -> consumer: ADD 1 per tile */
     cns_cnt_notify_t ack;    /* (in) consumer -> producer: ADD 1 per consumer CTA once it has read
@@ -493,7 +498,7 @@ typedef struct {
     int32_t areas;           /* (in) tile areas: 0 or 1 = one area of tiles * tile_words uint32 at
                                 tiles_dev; 2 = two such areas back to back (2 * tiles * tile_words
                                 uint32), round r writing and reading area r % 2 */
-    int32_t reserved;
+    int32_t consumer_wait;   /* (in) CNS_PIPE_WAIT_STREAM (0) or CNS_PIPE_WAIT_IN_KERNEL (1) */
 } cns_pipeline_t;
 
 /*
@@ -520,12 +525,19 @@ typedef struct {
  *     CTAs may be scheduled while the wait polls and wait on the device for
  *     it to end.  Grids are sized so that producer and consumer CTAs always
  *     fit on the GPU together (producers half of its thread slots -- two
- *     grids of a quarter each with two areas -- consumers a quarter).
+ *     grids of an eighth each with two areas -- consumers a quarter, two
+ *     grids of a quarter each with two areas);
+ *   consumer_wait = CNS_PIPE_WAIT_IN_KERNEL: no wait on the consumer stream;
+ *     the consumer kernel takes that wait itself.  Its CTA 0 waits on `done`
+ *     (BIGGER_OR_EQUAL tiles), clears it and then publishes the round on a
+ *     word of a 128-byte line the call allocates (cudaMallocAsync on the
+ *     producer stream, freed at the end); its other CTAs wait for that word.
+ *     One launch a round fewer; the results are the same.
  * The call first clears both notifies (count and status); `done` ends at 0
  * and `ack` at rounds * consumer_ctas (mod 2^32).  Once a wait times out the pipeline's remaining
  * waits return at once, so a lost signal costs one timeout, not one per round.
- * Errors: INVALID_HANDLE, NULL_PTR, INVALID_VALUE (also areas outside 0..2),
- * CUDA; with sync=1 also TIMEOUT.
+ * Errors: INVALID_HANDLE, NULL_PTR, INVALID_VALUE (also areas outside 0..2,
+ * consumer_wait outside 0..1), CUDA; with sync=1 also TIMEOUT.
  */
 int cns_pipeline_run(cns_pipeline_t *cfg);
 

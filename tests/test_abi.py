@@ -65,7 +65,7 @@ int main(void) {
   printf("cns_pipeline_t %zu\n", sizeof(cns_pipeline_t));
   F(cns_pipeline_t, tiles); F(cns_pipeline_t, rounds); F(cns_pipeline_t, timeout_s);
   F(cns_pipeline_t, elapsed_ms); F(cns_pipeline_t, device_status); F(cns_pipeline_t, consumer_ctas);
-  F(cns_pipeline_t, areas);
+  F(cns_pipeline_t, areas); F(cns_pipeline_t, consumer_wait);
   return 0;
 }
 """
@@ -91,7 +91,8 @@ def test_ctypes_structs_match_c_layout():
     assert lay["cns_wait_info_t"] == ctypes.sizeof(W) == 16
     assert lay["cns_wait_info_t.is_clear"] == W.is_clear.offset
     assert lay["cns_pipeline_t"] == ctypes.sizeof(P)
-    for f in ["tiles", "rounds", "timeout_s", "elapsed_ms", "device_status", "consumer_ctas", "areas"]:
+    for f in ["tiles", "rounds", "timeout_s", "elapsed_ms", "device_status", "consumer_ctas", "areas",
+              "consumer_wait"]:
         assert lay[f"cns_pipeline_t.{f}"] == getattr(P, f).offset, f
 
 
@@ -192,3 +193,4 @@ def test_python_constants_match_the_header():
             found += 1
     assert found >= 10
     assert _native.CNS_SYNCALL_DIE_LOCAL_ALIGN == 8192
+    assert (_native.CNS_PIPE_WAIT_STREAM, _native.CNS_PIPE_WAIT_IN_KERNEL) == (0, 1)

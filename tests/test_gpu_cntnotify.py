@@ -293,8 +293,9 @@ def test_statemachine_all_sets_and_invalid_ops(cns):
 
 # --- two-stream counting pipeline --------------------------------------------------------
 
+@pytest.mark.parametrize("consumer_wait", [0, 1])
 @pytest.mark.parametrize("areas", [1, 2])
-def test_pipeline_4096_tiles_1000_rounds(cns, areas):
+def test_pipeline_4096_tiles_1000_rounds(cns, areas, consumer_wait):
     import torch
     rc, done = cns.cntnotify_create(0)
     rc2, ack = cns.cntnotify_create(0)
@@ -302,7 +303,7 @@ def test_pipeline_4096_tiles_1000_rounds(cns, areas):
     try:
         s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
         cfg, rc, checksums, released = cns.run_pipeline(done, ack, 4096, 256, 1000, s1, s2, timeout_s=10,
-                                                        areas=areas)
+                                                        areas=areas, consumer_wait=consumer_wait)
         assert rc == 0 and cfg.device_status == 0
         want_cs, want_rel = oracle.pipeline(4096, 256, 1000)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
@@ -315,15 +316,16 @@ def test_pipeline_4096_tiles_1000_rounds(cns, areas):
         cns.cntnotify_destroy(ack)
 
 
+@pytest.mark.parametrize("consumer_wait", [0, 1])
 @pytest.mark.parametrize("areas", [0, 1, 2])
-def test_pipeline_small_odd_shapes(cns, areas):
+def test_pipeline_small_odd_shapes(cns, areas, consumer_wait):
     import torch
     rc, done = cns.cntnotify_create(0)
     rc2, ack = cns.cntnotify_create(0)
     try:
         s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
         cfg, rc, checksums, released = cns.run_pipeline(done, ack, 7, 12, 5, s1, s2, timeout_s=10,
-                                                        producer_ctas=3, areas=areas)
+                                                        producer_ctas=3, areas=areas, consumer_wait=consumer_wait)
         assert rc == 0
         want_cs, want_rel = oracle.pipeline(7, 12, 5)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
@@ -341,15 +343,17 @@ def test_pipeline_small_odd_shapes(cns, areas):
     (40, 8192, 6, 0),          # large tiles, 2048 uint4 each
     (1, 4, 3, 0),              # one tile
 ])
+@pytest.mark.parametrize("consumer_wait", [0, 1])
 @pytest.mark.parametrize("areas", [1, 2])
-def test_pipeline_producer_grids(cns, tiles, tile_words, rounds, producer_ctas, areas):
+def test_pipeline_producer_grids(cns, tiles, tile_words, rounds, producer_ctas, areas, consumer_wait):
     import torch
     rc, done = cns.cntnotify_create(0)
     rc2, ack = cns.cntnotify_create(0)
     try:
         s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
         cfg, rc, checksums, released = cns.run_pipeline(done, ack, tiles, tile_words, rounds, s1, s2, timeout_s=10,
-                                                        producer_ctas=producer_ctas, areas=areas)
+                                                        producer_ctas=producer_ctas, areas=areas,
+                                                        consumer_wait=consumer_wait)
         assert rc == 0 and cfg.device_status == 0
         want_cs, want_rel = oracle.pipeline(tiles, tile_words, rounds)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
@@ -388,8 +392,9 @@ def test_grid_sync_probe_ring_rotate(cns):
     np.testing.assert_array_equal(from_dev_u32(b1).reshape(148, 4), np.roll(v0, -1001, axis=0))
 
 
+@pytest.mark.parametrize("consumer_wait", [0, 1])
 @pytest.mark.parametrize("areas", [1, 2])
-def test_pipeline_on_one_stream(cns, areas):
+def test_pipeline_on_one_stream(cns, areas, consumer_wait):
     """Producer and consumer on the same stream: every device wait is then
     already satisfied when it starts, and the result is the same."""
     import torch
@@ -397,7 +402,8 @@ def test_pipeline_on_one_stream(cns, areas):
     rc2, ack = cns.cntnotify_create(0)
     try:
         s = torch.cuda.Stream()
-        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 300, 64, 12, s, s, timeout_s=10, areas=areas)
+        cfg, rc, checksums, released = cns.run_pipeline(done, ack, 300, 64, 12, s, s, timeout_s=10, areas=areas,
+                                                        consumer_wait=consumer_wait)
         assert rc == 0 and cfg.device_status == 0
         want_cs, want_rel = oracle.pipeline(300, 64, 12)
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
@@ -407,8 +413,9 @@ def test_pipeline_on_one_stream(cns, areas):
         cns.cntnotify_destroy(ack)
 
 
+@pytest.mark.parametrize("consumer_wait", [0, 1])
 @pytest.mark.parametrize("rounds", [1, 2, 7, 8])
-def test_pipeline_two_areas_hold_the_last_two_rounds(cns, rounds):
+def test_pipeline_two_areas_hold_the_last_two_rounds(cns, rounds, consumer_wait):
     """With two areas, round r writes area r % 2: after the run the area of the
     last round holds its words and the other area those of the round before
     (or is untouched after a single round)."""
@@ -422,7 +429,7 @@ def test_pipeline_two_areas_hold_the_last_two_rounds(cns, rounds):
         cs = torch.empty(rounds, dtype=torch.int32, device="cuda")
         rel = torch.empty(rounds, dtype=torch.int32, device="cuda")
         cfg, rc, checksums, released = cns.run_pipeline(done, ack, tiles, words, rounds, s1, s2, timeout_s=10,
-                                                        buffers=(buf, cs, rel), areas=2)
+                                                        buffers=(buf, cs, rel), areas=2, consumer_wait=consumer_wait)
         assert rc == 0 and cfg.device_status == 0
         got = from_dev_u32(buf).reshape(2, tiles * words)
         w = np.arange(tiles * words, dtype=np.uint64)
@@ -449,6 +456,9 @@ def test_pipeline_rejects_bad_area_count(cns):
         for areas in (-1, 3):
             cfg, rc, _, _ = cns.run_pipeline(done, ack, 8, 4, 2, s1, s2, timeout_s=10, areas=areas)
             assert rc == cns.CNS_ERR_INVALID_VALUE
+        for cw in (-1, 2):
+            cfg, rc, _, _ = cns.run_pipeline(done, ack, 8, 4, 2, s1, s2, timeout_s=10, areas=2, consumer_wait=cw)
+            assert rc == cns.CNS_ERR_INVALID_VALUE
     finally:
         cns.cntnotify_destroy(done)
         cns.cntnotify_destroy(ack)
@@ -462,16 +472,16 @@ def _pipeline_configs(n, seed=77):
         tiles = int(rng.randint(1, max(2, min(6000, (1 << 22) // words))))
         out.append(dict(tiles=tiles, words=words, rounds=int(rng.randint(1, 61)),
                         pctas=int(rng.choice([0, 1, 7, 100, 1000])), areas=int(rng.choice([1, 2])),
-                        one_stream=bool(rng.rand() < 0.25)))
+                        one_stream=bool(rng.rand() < 0.25), consumer_wait=i % 2))
     return out
 
 
 @pytest.mark.parametrize("c", _pipeline_configs(24),
                          ids=lambda c: f"t{c['tiles']}w{c['words']}r{c['rounds']}p{c['pctas']}a{c['areas']}"
-                                       f"{'s' if c['one_stream'] else 'm'}")
+                                       f"{'s' if c['one_stream'] else 'm'}{'k' if c['consumer_wait'] else ''}")
 def test_pipeline_random_configs(cns, c):
     """Seeded random pipelines (tile count, tile size, rounds, producer grid, one or two areas, one or two
-    streams): every round's checksum and release count equal the oracle's, and the notifies end where
+    streams, the wait on the stream or in the consumer kernel): every round's checksum and release count equal the oracle's, and the notifies end where
     the protocol leaves them."""
     import torch
     rc, done = cns.cntnotify_create(0)
@@ -481,7 +491,8 @@ def test_pipeline_random_configs(cns, c):
         s1 = torch.cuda.Stream()
         s2 = s1 if c["one_stream"] else torch.cuda.Stream()
         cfg, rc, checksums, released = cns.run_pipeline(done, ack, c["tiles"], c["words"], c["rounds"], s1, s2,
-                                                        timeout_s=10, producer_ctas=c["pctas"], areas=c["areas"])
+                                                        timeout_s=10, producer_ctas=c["pctas"], areas=c["areas"],
+                                                        consumer_wait=c["consumer_wait"])
         assert rc == 0 and cfg.device_status == 0
         want_cs, want_rel = oracle.pipeline(c["tiles"], c["words"], c["rounds"])
         np.testing.assert_array_equal(from_dev_u32(checksums), want_cs)
