@@ -29,6 +29,11 @@ Counter arithmetic variants:
              an unsigned >= compare, wrapping at W;
   "equal"    modular counter but the poll waits for cur == target exactly.
 The last two exist to show that the explorer does catch broken protocols.
+
+The later explorers take the same approach to the library's other
+protocols: the two-level (cluster) barrier, the sense-flip counter, the
+one-barrier hard path, the die-local counter copies, and the two-stream
+counted-notify pipeline's handshakes (explore_pipeline).
 """
 from __future__ import annotations
 
@@ -451,6 +456,153 @@ def explore_die_local(near, rounds: int, M: int | None = None, start: int = 0, t
         if not succ:
             if all(p[0] == rounds for p in parts):
                 res.completed += 1
+            else:
+                res.deadlocks += 1
+        stack.extend(succ)
+    return res
+
+
+def explore_pipeline(tiles: int, consumers: int, rounds: int, areas: int = 2, form: str = "in_kernel",
+                     go_gate: bool = True, clear_before_go: bool = True, clear_wait: bool = True,
+                     all_poll: bool = False, max_states: int = 3_000_000) -> Result:
+    """All interleavings of the two-stream counting pipeline's handshakes
+    ("CANN Runtime CntNotify" §5: producers record ADD 1 per tile, the waiter
+    waits BIGGER_OR_EQUAL tiles with isClear and continues), as this library
+    runs it: `tiles` producer CTAs of one tile each per round, `consumers`
+    consumer CTAs, `areas` tile areas, every atomic step taken in any order.
+
+    Words: done (the count), ack (consumer CTAs that finished reading), go
+    (form "in_kernel": the last round whose wait has released and cleared),
+    and one tag per tile of each area (the round whose data it holds).
+    Producer tile j of round r: waits until the consumers that last read its
+    area have all recorded on ack (one area: ack >= r * consumers; two:
+    ack >= (r - 1) * consumers), stores (tag = r); with two areas it then
+    waits for the previous producer grid to complete and for done < tiles;
+    then records ADD 1 on done.  With one area a producer grid starts after
+    the previous one completes (stream order).
+    form "in_kernel": consumer CTA 0 waits for go >= r, then done >= tiles,
+    clears done, publishes go = r + 1; the other CTAs wait for go >= r + 1.
+    Their start is not ordered at all with two areas (the go gate alone must
+    keep them right); with one area a grid starts after the previous one
+    completes.  Every CTA then waits for the previous consumer grid to
+    complete (two areas), reads its area and records ADD 1 on ack.
+    form "stream": a wait task per round polls done >= tiles and clears it;
+    it starts after the previous round's wait task has completed and
+    completes after the previous consumer grid; the round's consumer CTAs
+    start after it completes, read and record on ack.
+
+    Checks: every read finds the round's own data in every tile of its area;
+    every wait releases on exactly `tiles` (no record of another round is
+    counted or lost); no reachable state is stuck; at the end done = 0 and
+    ack = rounds * consumers.  The flags break one rule each, to show that
+    the checks see it: go_gate (CTA 0 waits for the previous round's go),
+    clear_before_go (the clear comes before the publish), clear_wait (two
+    areas: records wait for done < tiles); all_poll = True has every consumer
+    CTA poll done itself (and CTA 0 still clear it) instead of waiting for go.
+    """
+    K, C, R, A = tiles, consumers, rounds, areas
+    assert A in (1, 2) and form in ("in_kernel", "stream")
+    res = Result()
+    # state: (done, ack, go, tags, producers, consumers, waits)
+    #   producer phase: 0 start, 1 stored, 2 may record, 3 recorded
+    #   consumer phase (in_kernel, CTA 0): 0 start, 1 released (seen checked), 2 cleared, 3 past the wait,
+    #   4 read, 5 recorded on ack; other CTAs: 0 start, 3 past the wait, 4, 5
+    #   consumer phase (stream): 0 start, 3 past the wait (the task completed), 4, 5
+    #   wait task phase (stream): 0 start, 1 released, 2 cleared, 3 completed
+    init = (0, 0, 0, tuple(-1 for _ in range(A * K)), tuple(0 for _ in range(R * K)),
+            tuple(0 for _ in range(R * C)), tuple(0 for _ in range(R)))
+    seen = set()
+    stack = [init]
+    while stack:
+        state = stack.pop()
+        if state in seen:
+            continue
+        seen.add(state)
+        res.states += 1
+        if res.states > max_states:
+            raise RuntimeError("state space larger than max_states")
+        done, ack, go, tags, pr, co, wt = state
+        succ = []
+
+        def p_complete(r):
+            return r < 0 or all(pr[r * K + j] == 3 for j in range(K))
+
+        def c_complete(r):
+            return r < 0 or all(co[r * C + c] == 5 for c in range(C))
+
+        def check_seen(v):
+            if v != K:
+                res.epoch_violations += 1
+
+        for r in range(R):
+            for j in range(K):
+                i, ph = r * K + j, pr[r * K + j]
+                npr = lambda v: pr[:i] + (v,) + pr[i + 1:]  # noqa: E731
+                if ph == 0:
+                    need = (r - A + 1) * C
+                    if (A == 1 and not p_complete(r - 1)) or (r >= A and ack < need):
+                        continue
+                    nt = tags[:(r % A) * K + j] + (r,) + tags[(r % A) * K + j + 1:]
+                    succ.append((done, ack, go, nt, npr(1), co, wt))
+                elif ph == 1:
+                    if A == 2 and (not p_complete(r - 1) or (clear_wait and done >= K)):
+                        continue
+                    succ.append((done, ack, go, tags, npr(2), co, wt))
+                elif ph == 2:
+                    succ.append((done + 1, ack, go, tags, npr(3), co, wt))
+            if form == "stream":
+                ph = wt[r]
+                nwt = lambda v: wt[:r] + (v,) + wt[r + 1:]  # noqa: E731
+                if ph == 0 and (r == 0 or wt[r - 1] == 3) and (A == 2 or c_complete(r - 1)) and done >= K:
+                    check_seen(done)
+                    succ.append((done, ack, go, tags, pr, co, nwt(1)))
+                elif ph == 1:
+                    succ.append((0, ack, go, tags, pr, co, nwt(2)))
+                elif ph == 2 and c_complete(r - 1):
+                    succ.append((done, ack, go, tags, pr, co, nwt(3)))
+            for c in range(C):
+                i, ph = r * C + c, co[r * C + c]
+                nco = lambda v: co[:i] + (v,) + co[i + 1:]  # noqa: E731
+                if ph == 0:
+                    if form == "stream":
+                        if wt[r] == 3:
+                            succ.append((done, ack, go, tags, pr, nco(3), wt))
+                        continue
+                    if A == 1 and not c_complete(r - 1):
+                        continue
+                    if c == 0:
+                        if (go_gate and go < r) or done < K:
+                            continue
+                        check_seen(done)
+                        if clear_before_go:
+                            succ.append((done, ack, go, tags, pr, nco(1), wt))
+                        else:
+                            succ.append((done, ack, r + 1, tags, pr, nco(1), wt))
+                    elif all_poll:
+                        if (go_gate and go < r) or done < K:
+                            continue
+                        check_seen(done)
+                        succ.append((done, ack, go, tags, pr, nco(3), wt))
+                    elif go >= r + 1:
+                        succ.append((done, ack, go, tags, pr, nco(3), wt))
+                elif ph == 1:
+                    succ.append((0, ack, go, tags, pr, nco(2), wt))
+                elif ph == 2:
+                    succ.append((done, ack, max(go, r + 1), tags, pr, nco(3), wt))
+                elif ph == 3:
+                    if A == 2 and form == "in_kernel" and not c_complete(r - 1):
+                        continue
+                    if any(tags[(r % A) * K + j] != r for j in range(K)):
+                        res.safety_violations += 1
+                    succ.append((done, ack, go, tags, pr, nco(4), wt))
+                elif ph == 4:
+                    succ.append((done, ack + 1, go, tags, pr, nco(5), wt))
+        if not succ:
+            if all(p == 3 for p in pr) and all(c == 5 for c in co) and all(w in (0, 3) for w in wt) \
+                    and (form == "in_kernel" or all(w == 3 for w in wt)):
+                res.completed += 1
+                if done != 0 or ack != R * C:
+                    res.epoch_violations += 1
             else:
                 res.deadlocks += 1
         stack.extend(succ)

@@ -208,3 +208,44 @@ def test_die_local_start_off_the_epoch_grid_is_caught():
     assert explore_die_local((0, 1, 1), 2).ok
     bad = explore_die_local((0, 1), 2, start=1)
     assert bad.epoch_violations > 0
+
+
+# --- the two-stream pipeline's handshakes ("CANN Runtime CntNotify" §5) ------------------
+
+from oracle.protocol import explore_pipeline  # noqa: E402
+
+
+@pytest.mark.parametrize("form", ["in_kernel", "stream"])
+@pytest.mark.parametrize("areas", [1, 2])
+@pytest.mark.parametrize("K,C,R", [(1, 1, 3), (2, 2, 3), (3, 3, 4), (2, 3, 5), (4, 2, 4)])
+def test_pipeline_handshakes_safe_and_live(form, areas, K, C, R):
+    """Every interleaving: each read finds its round's data in every tile, each wait releases on
+    exactly K records, nothing is stuck, and the run ends at done = 0, ack = R * C."""
+    r = explore_pipeline(K, C, R, areas=areas, form=form)
+    assert r.ok and r.completed == 1, r
+
+
+@pytest.mark.parametrize("flag", ["go_gate", "clear_before_go"])
+def test_pipeline_in_kernel_wait_rules_are_needed_with_two_areas(flag):
+    """Without the previous round's go (or with go published before the clear), CTA 0 of the next
+    consumer grid, scheduled early, can take the previous round's count for its own: reads of stale
+    tiles, releases on the wrong count, stuck rounds."""
+    r = explore_pipeline(2, 2, 3, areas=2, form="in_kernel", **{flag: False})
+    assert r.safety_violations > 0 and r.epoch_violations > 0 and r.deadlocks > 0
+    # with one area the consumer grids run one after another, and neither rule is needed
+    assert explore_pipeline(2, 2, 3, areas=1, form="in_kernel", **{flag: False}).ok
+
+
+@pytest.mark.parametrize("form", ["in_kernel", "stream"])
+def test_pipeline_records_must_wait_for_the_clear(form):
+    """Two areas: a record that lands before the previous round's clear is wiped by it."""
+    r = explore_pipeline(2, 2, 3, areas=2, form=form, clear_wait=False)
+    assert r.epoch_violations > 0 and r.deadlocks > 0
+
+
+@pytest.mark.parametrize("areas", [1, 2])
+def test_pipeline_consumer_ctas_cannot_all_poll_the_count(areas):
+    """With more than one consumer CTA polling done and CTA 0 clearing it, a CTA that looks after the
+    clear waits for ever: the reason for the go word."""
+    assert explore_pipeline(2, 2, 3, areas=areas, all_poll=True).deadlocks > 0
+    assert explore_pipeline(2, 1, 3, areas=areas, all_poll=True).ok
