@@ -1054,7 +1054,10 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
     // bounds), so registers run in step with thread slots.  A CTA (256
     // threads) that found no SM with room would need every SM to have more
     // than (slots - 256) threads in use, i.e. more than 7/8 of the GPU, while
-    // everything here holds at most 3/4 plus two one-warp wait kernels.  (Work
+    // everything here holds at most 3/4 plus two one-warp wait kernels.  With
+    // the wait inside the consumer there are no wait kernels, and a consumer
+    // grid is scheduled early only once every CTA of the one before it is past
+    // its dependency wait, so the same two consumer grids at most.  (Work
     // of other streams running at the same time can still starve a round; the
     // bounded waits then end it with CNS_ERR_TIMEOUT.)
     const bool two = cfg->areas == 2;
