@@ -502,3 +502,34 @@ def test_pipeline_random_configs(cns, c):
     finally:
         cns.cntnotify_destroy(done)
         cns.cntnotify_destroy(ack)
+
+
+@pytest.mark.parametrize("consumer_wait", [0, 1])
+@pytest.mark.parametrize("areas", [1, 2])
+def test_pipeline_without_released_array(cns, areas, consumer_wait):
+    """released_dev is optional: through the C ABI with it NULL, unsynchronised (sync = 0), the
+    checksums still match the oracle and the notifies end where the protocol leaves them."""
+    import torch
+    from counted_notify_sync_gb300 import _native
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    try:
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        tiles, words, rounds = 500, 32, 9
+        buf = torch.empty(2 * tiles * words, dtype=torch.int32, device="cuda")
+        cs = torch.empty(rounds, dtype=torch.int32, device="cuda")
+        cfg = _native.Pipeline()
+        cfg.done, cfg.ack = done, ack
+        cfg.tiles_dev, cfg.checksums_dev, cfg.released_dev = _native.ptr(buf), _native.ptr(cs), None
+        cfg.tiles, cfg.tile_words, cfg.rounds = tiles, words, rounds
+        cfg.producer_stream = _native.stream_handle(s1)
+        cfg.consumer_stream = _native.stream_handle(s2)
+        cfg.timeout_s, cfg.sync, cfg.areas, cfg.consumer_wait = 10, 0, areas, consumer_wait
+        assert _native.cns_pipeline_run(cfg) == 0
+        torch.cuda.synchronize()
+        want_cs, _ = oracle.pipeline(tiles, words, rounds)
+        np.testing.assert_array_equal(from_dev_u32(cs), want_cs)
+        assert count_of(cns, done) == (0, 0) and count_of(cns, ack) == (0, rounds * cfg.consumer_ctas)
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
