@@ -402,6 +402,100 @@ __device__ __forceinline__ int cns_cnt_wait_dev(uint32_t *count, int mode, uint3
     }
 }
 
+namespace cns {
+
+// The bounded poll of cns_cnt_wait_grid_dev: on word w until ok(value), or
+// until go[1] is raised or the time runs out (then it raises go[1] itself if
+// it is still 0).  The value that passed goes to *seen if given.
+template <class Ok>
+__device__ __forceinline__ int grid_wait_poll(const uint32_t *w, Ok ok, uint32_t *go, uint64_t limit,
+                                              uint32_t *seen)
+{
+    uint32_t spins = 0;
+    uint64_t deadline = 0;
+    for (;;) {
+        const uint32_t c = ld_relaxed_gpu(w);
+        if (ok(c)) {
+            fence_acquire_gpu();
+            if (seen)
+                *seen = c;
+            return CNS_SUCCESS;
+        }
+        if ((++spins & 63u) == 0u) {
+            if (ld_relaxed_gpu(go + 1) != 0u)
+                return CNS_ERR_TIMEOUT;
+            const uint64_t now = globaltimer_ns();
+            if (deadline == 0) {
+                deadline = now + limit;
+            } else if (now > deadline) {
+                atom_cas_relaxed_gpu(go + 1, 0u, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
+                return CNS_ERR_TIMEOUT;
+            }
+        }
+    }
+}
+
+}  // namespace cns
+
+/* A counted-notify wait taken by several CTAs of a grid together, call after
+ * call (CntNotify §3.2 with isClear, for a consumer that is a whole grid).
+ * They cannot all poll the count: once one of them had cleared it, a CTA
+ * that had not yet looked would wait until its timeout.  So thread 0 of CTA
+ * 0 waits on the count (mode, v), clears it if is_clear, and then publishes
+ * the call on go[0] (release); thread 0 of every other calling CTA waits
+ * until go[0] shows the call.  CTA 0 first waits for go[0] to show the
+ * previous call, so when grids that follow one another overlap, the count it
+ * then looks at was cleared by the call before.  Writes released by the
+ * records are visible to every thread of the calling CTAs afterwards.
+ *   count       the notify's count word (cntnotify_get_device_ptr)
+ *   go          two words on a line of their own, zeroed before the first
+ *               call and shared by no other grid-wide wait: go[0] counts the
+ *               calls published, go[1] holds the first failure's code
+ *   call        the call's index, 0, 1, 2, ..., the same in every CTA (a grid
+ *               that follows another continues its count)
+ *   timeout_ns  per wait; 0 = 2 s.  A wait that runs out stores
+ *               CNS_ERR_TIMEOUT in go[1] (if it is still 0), and the other
+ *               CTAs' waits then give up too
+ *   observed    if not NULL, CTA 0 stores the count that released its wait
+ * All threads of every calling CTA call it, and CTA 0 must be among them.
+ * Returns, in every thread, CNS_SUCCESS, CNS_ERR_TIMEOUT (this or an earlier
+ * call failed: go[1] stays set until the caller zeroes it), or
+ * CNS_ERR_INVALID_VALUE for a mode outside 0..4 (no wait taken). */
+__device__ __forceinline__ int cns_cnt_wait_grid_dev(uint32_t *count, uint32_t *go, uint32_t call, int mode,
+                                                     uint32_t v, int is_clear, uint64_t timeout_ns,
+                                                     uint32_t *observed)
+{
+    if (mode < 0 || mode > 4)
+        return CNS_ERR_INVALID_VALUE;
+    int rc = CNS_SUCCESS;
+    if (threadIdx.x == 0) {
+        const uint64_t limit = timeout_ns ? timeout_ns : 2000000000ull;
+        const uint32_t m = static_cast<uint32_t>(mode);
+        if (cns::ld_relaxed_gpu(go + 1) != 0u) {
+            rc = CNS_ERR_TIMEOUT;
+        } else if (blockIdx.x == 0) {
+            uint32_t seen = 0;
+            rc = cns::grid_wait_poll(go, [=](uint32_t g) { return static_cast<int32_t>(g - call) >= 0; }, go, limit,
+                                     nullptr);
+            if (rc == CNS_SUCCESS)
+                rc = cns::grid_wait_poll(count, [=](uint32_t c) { return cns::cnt_wait_released(c, m, v); }, go,
+                                         limit, &seen);
+            if (rc == CNS_SUCCESS) {
+                if (observed)
+                    *observed = seen;
+                if (is_clear)
+                    cns::atom_exch_relaxed_gpu(count, 0u);   // the clear comes after the release ...
+                cns::st_release_gpu(go, call + 1u);          // ... and before the call is published
+            }
+        } else {
+            const uint32_t next = call + 1u;
+            rc = cns::grid_wait_poll(go, [=](uint32_t g) { return static_cast<int32_t>(g - next) >= 0; }, go, limit,
+                                     nullptr);
+        }
+    }
+    return __syncthreads_or(rc != CNS_SUCCESS) ? CNS_ERR_TIMEOUT : CNS_SUCCESS;
+}
+
 /* The soft SYNCALL barrier among CTAs 0 .. participants - 1 of the grid.
  * Every thread of each participating CTA calls it, the same number of times
  * in each CTA; CTAs with blockIdx.x >= participants must not call it.  The

@@ -22,6 +22,7 @@ def test_device_header_compiles_alone(tmp_path):
                    "    cns_cnt_record_dev(w, CNS_REC_ADD, 1u);\n"
                    "    rc[0] = cns_cnt_wait_dev(w, CNS_WAIT_BIGGER_OR_EQUAL, 1u, 1, 0, nullptr);\n"
                    "    rc[1] = cns_syncall_soft(ws, gridDim.x, 0);\n"
+                   "    rc[2] = cns_cnt_wait_grid_dev(w, w + 32, 0u, CNS_WAIT_BIGGER_OR_EQUAL, 1u, 1, 0, nullptr);\n"
                    "}\n")
     subprocess.run([nvcc, *arch, "-std=c++17", "-I", INC, "-c", "-o", str(tmp_path / "alone.o"), str(src)],
                    check=True)

@@ -3,8 +3,9 @@
 barrier between ring rounds against the sequential oracle, over a subset of
 the grid and through the counter's wrap; records from user threads released
 by the library's stream wait; device waits on every mode against the oracle's
-rule; and bounded timeouts (a barrier one CTA never reaches, a count nobody
-records)."""
+rule; a grid-wide consumer on cns_cnt_wait_grid_dev against the oracle's
+pipeline checksums; and bounded timeouts (a barrier one CTA never reaches, a
+count nobody records, a grid-wide wait nobody releases)."""
 import ctypes
 import os
 import subprocess
@@ -50,7 +51,10 @@ def user(cns):
     L.user_ring_die_local.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
     L.user_record.argtypes = [vp, ctypes.c_int, u32, i32, i32, ctypes.c_int]
     L.user_wait.argtypes = [vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp]
-    for f in (L.user_ring, L.user_ring_die_local, L.user_record, L.user_wait):
+    L.user_grid_wait.argtypes = [i32, i32, vp, vp, vp, vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp, vp]
+    L.user_grid_wait_only.argtypes = [i32, vp, vp, u32, ctypes.c_int, u32, u64, vp]
+    for f in (L.user_ring, L.user_ring_die_local, L.user_record, L.user_wait, L.user_grid_wait,
+              L.user_grid_wait_only):
         f.restype = ctypes.c_int
     return L
 
@@ -175,3 +179,85 @@ def test_fused_device_wait_rejects_unknown_modes(cns, user):
             assert int(out[0]) == cns.CNS_ERR_INVALID_VALUE
     finally:
         cns.cntnotify_destroy(h)
+
+
+# --- the grid-wide wait (cns_cnt_wait_grid_dev) --------------------------------------------
+
+def _lines(n=3):
+    import torch
+    return [torch.zeros(32, dtype=torch.int32, device="cuda") for _ in range(n)]
+
+
+@pytest.mark.parametrize("G,threads,words,k,rounds", [(8, 128, 1024, 5, 40), (147, 256, 4096, 1, 20),
+                                                       (1, 64, 100, 3, 10), (32, 96, 257, 64, 25)])
+def test_grid_wait_consumer_rounds_match_oracle(cns, user, G, threads, words, k, rounds):
+    """G consumer CTAs take a grid-wide wait (>= k, clear) per round and each sums the round's area; one
+    producer CTA records k per round after the previous call was published: every CTA's sum equals the
+    oracle's checksum of its round, each release saw exactly k, and the words end where the protocol
+    leaves them."""
+    import torch
+    count, go, ack = _lines()
+    area = torch.zeros(2 * words, dtype=torch.int32, device="cuda")
+    sums = torch.zeros(rounds * G, dtype=torch.int32, device="cuda")
+    rcs = torch.full((rounds * G,), -1, dtype=torch.int32, device="cuda")
+    observed = torch.zeros(rounds, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    rc = user.user_grid_wait(G, threads, count.data_ptr(), go.data_ptr(), ack.data_ptr(), area.data_ptr(), words,
+                             k, rounds, 0, sums.data_ptr(), rcs.data_ptr(), observed.data_ptr())
+    assert rc == 0, rc
+    assert (rcs.cpu().numpy() == 0).all()
+    want_cs, _ = oracle.pipeline(1, words, rounds)
+    got = from_dev_u32(sums).reshape(rounds, G)
+    np.testing.assert_array_equal(got, np.repeat(want_cs[:, None], G, axis=1))
+    assert (from_dev_u32(observed) == k).all()
+    assert from_dev_u32(count)[0] == 0
+    assert tuple(from_dev_u32(go)[:2]) == (rounds, 0)
+    assert from_dev_u32(ack)[0] == rounds * G
+
+
+def test_grid_wait_calls_continue_across_launches(cns, user):
+    """A grid that follows another continues the call count: call 0 released by a count of 5 (>= 5, then
+    cleared), call 1 by a count of 3 (== 3)."""
+    import torch
+    count, go, _ = _lines()
+    rcs = torch.full((64,), -1, dtype=torch.int32, device="cuda")
+    count[0] = 5
+    torch.cuda.synchronize()
+    assert user.user_grid_wait_only(64, count.data_ptr(), go.data_ptr(), 0, cns.CNS_WAIT_BIGGER_OR_EQUAL, 5,
+                                    0, rcs.data_ptr()) == 0
+    assert (rcs.cpu().numpy() == 0).all() and from_dev_u32(count)[0] == 0 and from_dev_u32(go)[0] == 1
+    count[0] = 3
+    rcs.fill_(-1)
+    torch.cuda.synchronize()
+    assert user.user_grid_wait_only(64, count.data_ptr(), go.data_ptr(), 1, cns.CNS_WAIT_EQUAL, 3, 0,
+                                    rcs.data_ptr()) == 0
+    assert (rcs.cpu().numpy() == 0).all() and from_dev_u32(count)[0] == 0 and from_dev_u32(go)[0] == 2
+
+
+def test_grid_wait_times_out_everywhere(cns, user):
+    """A count nobody records: CTA 0's wait runs out (2 ms), raises go[1], and every other CTA gives up
+    with it; a later call on the same words returns the failure at once."""
+    import torch
+    count, go, _ = _lines()
+    rcs = torch.full((16,), -1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    assert user.user_grid_wait_only(16, count.data_ptr(), go.data_ptr(), 0, cns.CNS_WAIT_BIGGER_OR_EQUAL, 1,
+                                    2_000_000, rcs.data_ptr()) == 0
+    assert (rcs.cpu().numpy() == cns.CNS_ERR_TIMEOUT).all()
+    assert tuple(from_dev_u32(go)[:2]) == (0, cns.CNS_ERR_TIMEOUT)
+    count[0] = 1
+    rcs.fill_(-1)
+    torch.cuda.synchronize()
+    assert user.user_grid_wait_only(16, count.data_ptr(), go.data_ptr(), 0, cns.CNS_WAIT_BIGGER_OR_EQUAL, 1,
+                                    2_000_000, rcs.data_ptr()) == 0
+    assert (rcs.cpu().numpy() == cns.CNS_ERR_TIMEOUT).all() and from_dev_u32(count)[0] == 1
+
+
+def test_grid_wait_rejects_a_bad_mode(cns, user):
+    import torch
+    count, go, _ = _lines()
+    rcs = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    assert user.user_grid_wait_only(4, count.data_ptr(), go.data_ptr(), 0, 7, 1, 0, rcs.data_ptr()) == 0
+    assert (rcs.cpu().numpy() == cns.CNS_ERR_INVALID_VALUE).all()
+    assert tuple(from_dev_u32(go)[:2]) == (0, 0)
