@@ -13,6 +13,9 @@
  *   cns_cnt_wait_dev     a bounded wait on that word (§3.2: LESS, EQUAL,
  *                        BIGGER, BIGGER_OR_EQUAL, EQUAL_WITH_BITMASK, with
  *                        isClear) from one thread
+ *   cns_cnt_wait_grid_dev  the same wait taken by several CTAs of a grid
+ *                        together, call after call: CTA 0 waits and clears,
+ *                        the others follow a `go` word it publishes
  *   cns_syncall_soft     the soft SYNCALL barrier ("PTO-ISA SYNCALL
  *                        cross-core barrier guide" §5.2) among the first P
  *                        CTAs of a grid, on a workspace that
@@ -24,8 +27,9 @@
  *
  * Every wait is bounded and reports CNS_ERR_TIMEOUT instead of trapping.  The
  * caller makes the participating CTAs co-resident (a cooperative launch, or a
- * grid no larger than the GPU holds at once): a barrier whose participants
- * are not all running at the same time ends in that timeout.
+ * grid no larger than the GPU holds at once): a barrier or grid-wide wait
+ * whose participants are not all running at the same time ends in that
+ * timeout.
  *
  * The library's own kernels are built on the same primitives (namespace cns).
  */
