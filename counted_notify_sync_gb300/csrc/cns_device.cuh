@@ -32,6 +32,16 @@ __device__ __forceinline__ uint32_t cluster_nctarank()
     return r;
 }
 
+// Clusters in the grid (x; the library's grids are one-dimensional).  A
+// launch without the cluster attribute makes each CTA a cluster of its own,
+// so this is then the CTA count.
+__device__ __forceinline__ uint32_t nclusters_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
 // Every thread of every CTA in the cluster arrives (release) and waits
 // (acquire): the cluster-scope barrier.  The calling warp must be converged.
 __device__ __forceinline__ void cluster_sync_all()

@@ -251,6 +251,27 @@ __device__ __forceinline__ void data_phase(const SyncallParams &p, int64_t r, ui
 // The persistent kernel
 // ---------------------------------------------------------------------------
 
+// Words of the workspace's status line (line 1) beyond the status itself.
+constexpr uint32_t kBaseWordSoft = 5;   // base count of the soft counter
+constexpr uint32_t kBaseWordHard = 6;   // base count of the hard counter
+constexpr uint32_t kTagWord = 7;        // CNS_SYNCALL_WORKSPACE_TAG, _TAG_FLIP or 0
+
+// Whether the workspace check refuses a run: a tag the library did not write
+// (0 is accepted with a base of 0: a zeroed workspace), or, for the variants
+// on the pages' arithmetic, a base count that is not a multiple of P below M
+// (it would put the participants in different epochs).  The sense-flip
+// variant checks its own count at every arrival.
+template <int V>
+__device__ __forceinline__ bool workspace_refused(uint32_t tag, uint32_t base, const Epoch &e)
+{
+    if constexpr (V == kBvSenseFlip) {
+        return !(tag == CNS_SYNCALL_WORKSPACE_TAG || tag == CNS_SYNCALL_WORKSPACE_TAG_FLIP || tag == 0u);
+    } else {
+        const bool tag_ok = tag == CNS_SYNCALL_WORKSPACE_TAG || (tag == 0u && base == 0u);
+        return !tag_ok || base > e.Mm1 || base % e.P != 0u;
+    }
+}
+
 __device__ __forceinline__ uint32_t cta_role(const SyncallParams &p, uint32_t b)
 {
     if (p.core_type == CNS_MIX)
@@ -293,6 +314,51 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
     // the elected thread's copy of the barrier description (variant 5 turns
     // its counter pair into near / far for this SM)
     Barrier bar = p.bar;
+    if constexpr (MODE == CNS_SYNCALL_HARD) {
+        // The hard path's participants are the clusters the launch really
+        // has, and each cluster's members are the CTAs it really holds: both
+        // come from the launch, not from the cluster size the host asked for
+        // (a tool or a replay may launch the kernel without the cluster
+        // attribute, and every CTA is then a cluster leader of its own).  The
+        // observed size goes to the status line for the host to report.
+        bar.e = epoch_of(nclusters_x());
+        if (b == 0 && threadIdx.x == 0)
+            st_relaxed_gpu(bar.status_line + 4, cluster_nctarank());
+    }
+    // The workspace check, before anyone arrives: every participant reads the
+    // same words and takes the same decision, so a refused run leaves no CTA
+    // behind at a barrier (see CNS_SYNCALL_WORKSPACE_TAG in cns.h).
+    uint32_t *base_word = bar.status_line + (MODE == CNS_SYNCALL_SOFT ? kBaseWordSoft : kBaseWordHard);
+    uint32_t base = 0;
+    {
+        int refuse = 0;
+        if (threadIdx.x == 0) {
+            const uint32_t tag = ld_relaxed_gpu(bar.status_line + kTagWord);
+            base = ld_relaxed_gpu(base_word);
+            // a status or abort flag left by an earlier run that failed
+            const bool failed = (ld_relaxed_gpu(bar.status_line) | ld_relaxed_gpu(bar.status_line + 1)) != 0u;
+            refuse = (failed || workspace_refused<V>(tag, base, bar.e)) ? 1 : 0;
+        }
+        if (__syncthreads_or(refuse)) {
+            if (threadIdx.x == 0) {
+                if (b == 0) {
+                    // keep an earlier failure's code; anything else in the
+                    // status word (garbage) becomes INVALID_VALUE
+                    const uint32_t cur = ld_relaxed_gpu(bar.status_line);
+                    if (cur != static_cast<uint32_t>(CNS_ERR_TIMEOUT) &&
+                        cur != static_cast<uint32_t>(CNS_ERR_INVALID_VALUE)) {
+                        st_relaxed_gpu(bar.status_line + 2, 0u);
+                        st_relaxed_gpu(bar.status_line + 3, 0u);
+                        st_relaxed_gpu(bar.status_line, static_cast<uint32_t>(CNS_ERR_INVALID_VALUE));
+                    }
+                    atom_exch_release_gpu(bar.status_line + 1, 1u);
+                }
+                if (p.cta_status)
+                    p.cta_status[b] = static_cast<int32_t>(CNS_CTA_ABORTED | (role << 8));
+            }
+            return;
+        }
+    }
     if ((V == kBvDieLocal || V == kBvArrivalDieLocal) && threadIdx.x == 0)
         choose_near_copy(bar);   // every CTA polls its own near copy (hard path: the leader arrives on both)
     EpochCursor cursor{0u, 0u, false};
@@ -337,6 +403,18 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         if constexpr (MODE == CNS_SYNCALL_HARD)
             stop = hard_barrier_finish(&s_flag);
     }
+    if (threadIdx.x == 0 && b == 0 && !stop) {
+        // every arrival of the run has landed once CTA 0 is past its last
+        // barrier: the counter stands at base + rounds * P (mod M)
+        if constexpr (V == kBvSenseFlip) {
+            st_relaxed_gpu(bar.status_line + kTagWord, CNS_SYNCALL_WORKSPACE_TAG_FLIP);
+        } else {
+            const uint64_t M = static_cast<uint64_t>(bar.e.Mm1) + 1u;
+            const uint64_t steps = static_cast<uint64_t>(p.rounds) % (M / bar.e.P);
+            st_relaxed_gpu(base_word, static_cast<uint32_t>((base + steps * bar.e.P) % M));
+            st_relaxed_gpu(bar.status_line + kTagWord, CNS_SYNCALL_WORKSPACE_TAG);
+        }
+    }
     if (threadIdx.x == 0 && p.cta_status)
         p.cta_status[b] = static_cast<int32_t>((stop ? CNS_CTA_ABORTED : CNS_CTA_DONE) | (role << 8));
 }
@@ -355,6 +433,10 @@ __global__ void workspace_init_kernel(uint32_t *ws, uint32_t n_words, uint32_t s
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+        uint32_t *status_line = ws + CNS_SYNCALL_LINE_BYTES / 4;
+        status_line[kBaseWordSoft] = start;
+        status_line[kBaseWordHard] = start;
+        status_line[kTagWord] = CNS_SYNCALL_WORKSPACE_TAG;
         ws[0] = start;                                  // soft counter
         ws[2 * CNS_SYNCALL_LINE_BYTES / 4] = start;     // hard counter
         ws[3 * CNS_SYNCALL_LINE_BYTES / 4] = start;     // soft release word
@@ -494,6 +576,8 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return CNS_ERR_INVALID_VALUE;
     if (d->workspace_bytes != 0 && d->workspace_bytes < CNS_SYNCALL_WORKSPACE_BYTES)
         return CNS_ERR_INVALID_VALUE;
+    if (d->launch_flags & ~CNS_LAUNCH_NO_CLUSTER_ATTR)
+        return CNS_ERR_INVALID_VALUE;
     if ((d->barrier_variant == CNS_BARRIER_DIE_LOCAL || d->barrier_variant == CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL) &&
         d->workspace_bytes < CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES)
         return CNS_ERR_INVALID_VALUE;
@@ -626,7 +710,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     attrs[na].id = cudaLaunchAttributeCooperative;
     attrs[na].val.cooperative = 1;
     ++na;
-    if (mode == CNS_SYNCALL_HARD) {
+    if (mode == CNS_SYNCALL_HARD && !(d->launch_flags & CNS_LAUNCH_NO_CLUSTER_ATTR)) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
         attrs[na].val.clusterDim.x = C;
         attrs[na].val.clusterDim.y = 1;
@@ -641,7 +725,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         (void)cudaGetLastError();
         return CNS_ERR_NOT_RESIDENT;
     }
-    if (le != cudaSuccess && mode == CNS_SYNCALL_HARD) {
+    if (le != cudaSuccess && mode == CNS_SYNCALL_HARD && na == 2) {
         // the cooperative attribute together with clusters may be refused;
         // residency was checked above, so launch without it
         CNS_LOG(1, "cooperative cluster launch refused (%s); launching without it", cudaGetErrorString(le));
@@ -671,5 +755,11 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return rc;
     d->final_counter = mode == CNS_SYNCALL_SOFT ? sc : hc;
     d->device_status = st;
+    if (mode == CNS_SYNCALL_HARD) {
+        uint32_t seen = 0;
+        CNS_CUDA(cudaMemcpy(&seen, ws + CNS_SYNCALL_LINE_BYTES / 4 + 4, sizeof(seen), cudaMemcpyDeviceToHost));
+        if (seen >= 1 && seen <= 16)
+            d->cluster_used = static_cast<int32_t>(seen);
+    }
     return (st == CNS_ERR_TIMEOUT || st == CNS_ERR_INVALID_VALUE) ? st : CNS_SUCCESS;
 }

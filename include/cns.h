@@ -86,8 +86,14 @@ typedef enum {
 /* Workspace layout: four 128-byte lines (the GB300 L2 line; also one of the
  * 64-byte lines [SYNCALL] §4.1 asks the counter to own exclusively):
  *   line 0  word 0: soft counter
- *   line 1  words 0..3: status (0 or CNS_ERR_TIMEOUT), abort flag,
- *           round at which a wait gave up, CTA that gave up
+ *   line 1  words 0..3: status (0, CNS_ERR_TIMEOUT or CNS_ERR_INVALID_VALUE),
+ *           abort flag, round at which a wait gave up, CTA that gave up;
+ *           word 4: CTAs per cluster in the last HARD launch, as the device
+ *           saw it; words 5 and 6: the count at which the soft and the hard
+ *           counter stand between runs (the start value, then the count the
+ *           last complete run of syncall_run left); word 7: a tag that
+ *           syncall_workspace_init sets (CNS_SYNCALL_WORKSPACE_TAG; 0 in a
+ *           zeroed workspace, whose base counts are then 0)
  *   line 2  word 0: hard-path counter (one arrival per cluster)
  *   line 3  word 0: soft release word, word 16: hard release word (used by
  *           CNS_BARRIER_FLAG_BROADCAST only)
@@ -95,6 +101,27 @@ typedef enum {
  * before first use and shared with no other data. */
 #define CNS_SYNCALL_LINE_BYTES 128
 #define CNS_SYNCALL_WORKSPACE_BYTES 512
+
+/* Workspace check.  Before its first arrival, every participant of a
+ * syncall_run reads the base count of the counter it will use (line 1, word 5
+ * or 6) and the tag (word 7), and the run is refused on the device with
+ * CNS_ERR_INVALID_VALUE (no participant arrives; every CTA reports
+ * CNS_CTA_ABORTED) unless the status and abort words are 0 (no earlier run
+ * failed on it; a failure's status is kept), the tag is
+ * CNS_SYNCALL_WORKSPACE_TAG, or 0 with a base count of 0 (a zeroed
+ * workspace), and the base count is a multiple of the run's participant
+ * count below its wrap modulus.  This is the "counter
+ * garbage" row of [SYNCALL] §8: a workspace that was never initialised, one
+ * initialised with a start that puts the participants in different epochs,
+ * or one reused by a run with another participant count.  A run that ends
+ * without a failure moves the base count to where it left the counter, so
+ * runs may follow one another on one workspace.  SENSE_FLIP keeps its own
+ * check (below) and leaves the tag at CNS_SYNCALL_WORKSPACE_TAG_FLIP, which
+ * the other variants refuse until the workspace is initialised again.  The
+ * check sees the base count, not the counter: writes into the workspace from
+ * outside the library go unnoticed. */
+#define CNS_SYNCALL_WORKSPACE_TAG 0x434E5331u      /* "CNS1" */
+#define CNS_SYNCALL_WORKSPACE_TAG_FLIP 0x434E5346u /* "CNSF" */
 
 /* The die-local variant keeps a second copy of each counter 4 KB further on:
  * soft counter copy at byte CNS_SYNCALL_REPLICA_OFFSET, hard counter copy two
@@ -140,10 +167,9 @@ typedef enum {
  *                     runs the same epoch arithmetic.  Needs a workspace of
  *                     CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES.  Each copy sees
  *                     the arrivals in its own order, so a count that does not
- *                     start at a multiple of P (a workspace reused across runs
- *                     with different P without re-initialising it) can release
- *                     participants early rather than time out: re-initialise
- *                     the workspace whenever P changes.
+ *                     start at a multiple of P could release participants
+ *                     early rather than time out; the workspace check (above)
+ *                     refuses such a start before anyone arrives.
  *   SENSE_FLIP        not the guide's arithmetic (the scheme of the CUDA
  *                     runtime's grid barrier, for comparison): participant 0
  *                     (CTA 0) adds 2^31 - (P - 1) and every other participant 1,
@@ -190,11 +216,12 @@ typedef enum {
  *   bytes        >= CNS_SYNCALL_WORKSPACE_BYTES; with at least
  *                CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES the counter copies of
  *                the die-local variant are initialised too
- *   start_value  value of both counters before the first arrival; 0 is the
- *                documented initial state ([SYNCALL] §4.1).  A multiple of
- *                the participant count below its wrap modulus models a
- *                workspace reused after earlier complete runs; any other
- *                value desynchronises the epochs and the run times out.
+ *   start_value  value of both counters before the first arrival, and their
+ *                base count (line 1, words 5 and 6); 0 is the documented
+ *                initial state ([SYNCALL] §4.1).  A multiple of the
+ *                participant count below its wrap modulus models a workspace
+ *                reused after earlier complete runs; syncall_run refuses any
+ *                other value with CNS_ERR_INVALID_VALUE (the workspace check).
  *   stream       stream to enqueue on (asynchronous)
  * Errors: NULL_PTR, INVALID_VALUE (size or alignment), CUDA.
  */
@@ -230,11 +257,21 @@ typedef struct {
     int32_t device_status;   /* (out, sync=1) 0 or CNS_ERR_TIMEOUT */
     int32_t grid_ctas;       /* (out) CTAs launched */
     int32_t participants;    /* (out) resolved participant count P */
-    int32_t cluster_used;    /* (out) CTAs per cluster (1 for SOFT) */
+    int32_t cluster_used;    /* (out) CTAs per cluster (1 for SOFT).  HARD with sync=1: the
+                                size the device saw in the launch; with sync=0: the size
+                                requested */
     int32_t barrier_variant; /* (in) cns_barrier_variant_t; 0 = the guide's counter poll */
     uint32_t workspace_bytes;/* (in) size of workspace_dev; 0 = CNS_SYNCALL_WORKSPACE_BYTES */
-    int32_t reserved[2];
+    uint32_t launch_flags;   /* (in) 0, or CNS_LAUNCH_NO_CLUSTER_ATTR (testing) */
+    int32_t reserved;
 } cns_syncall_data_t;
+
+/* cns_syncall_data_t.launch_flags.  CNS_LAUNCH_NO_CLUSTER_ATTR launches the
+ * HARD path without the cluster-dimension attribute, so that every CTA forms
+ * a cluster of its own, as some tools and replays launch it.  The hard path
+ * takes its cluster count and size from the launch it really got, so the
+ * results are the same; cluster_used then reports 1.  For tests. */
+#define CNS_LAUNCH_NO_CLUSTER_ATTR 1u
 
 /*
  * syncall_run -- one persistent launch that runs `rounds` rounds of
@@ -273,15 +310,16 @@ typedef struct {
  * this is stronger.
  *
  * The launch is cooperative (co-residency is guaranteed or the launch fails
- * with CNS_ERR_NOT_RESIDENT).  A workspace left by a timed-out run keeps its
- * abort flag: re-initialise it before reusing it.
+ * with CNS_ERR_NOT_RESIDENT).  A workspace left by a run that failed keeps its
+ * status and abort flag, and the workspace check refuses it: re-initialise it
+ * before reusing it.
  *
  * Errors: NULL_PTR (data, workspace, payload buffers the workload needs),
  * INVALID_VALUE (enum, sizes, used_cores > launched CTAs, cluster shape,
  * alignment), ARCH, NOT_RESIDENT, CUDA; with sync=1 also TIMEOUT when a
- * barrier wait ran out on the device, and INVALID_VALUE when a SENSE_FLIP
- * arrival found a count that the scheme cannot produce (device_status says
- * which).
+ * barrier wait ran out on the device, and INVALID_VALUE when the workspace
+ * check refused the run or a SENSE_FLIP arrival found a count that the scheme
+ * cannot produce (device_status says which).
  */
 int syncall_run(int mode, int core_type, int32_t used_cores, int32_t aiv_ratio,
                 int64_t rounds, cns_syncall_data_t *data);
@@ -343,7 +381,9 @@ typedef struct {
 /*
  * cntnotify_create -- create a counted notify with count 0 on the current
  * device ([CNTN] §4.1).  Its counter is one uint32 on a 128-byte line of a
- * device-resident pool owned by the library.
+ * device-resident pool owned by the library.  The first call on a device
+ * makes the pool and loads the library's notify kernels there (see the
+ * submission-order note at cntnotify_wait_with_timeout).
  *   out   receives the handle
  *   flag  reserved, must be 0
  * Errors: NULL_PTR (out), INVALID_VALUE (flag != 0), RESOURCE (pool of
@@ -368,10 +408,21 @@ int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const cns_record_i
  * release; a record that lands between the two is overwritten).  If the
  * timeout passes first, the wait records CNS_ERR_TIMEOUT in the notify's
  * sticky status (see cntnotify_query_status) and the stream continues.
- * Submission order: CUDA may run two streams through one hardware queue in
- * the order their work was submitted.  A wait submitted before the records
- * that release it can then hold those records back until it times out, so
- * submit (from the host) the records a wait depends on before the wait.
+ * Submission order ([CNTN] §5, §7 item 6 put none on the host): a wait may
+ * be submitted before the records that release it, on another stream, with
+ * two exceptions that come from how CUDA feeds streams to the GPU, not from
+ * the notify.  (1) Work submitted on the wait's own stream behind the wait
+ * cannot start before the wait ends; if the recording stream shares a
+ * hardware queue with it (CUDA_DEVICE_MAX_CONNECTIONS, default 8, fewer
+ * than the streams in use), records submitted after that work queue behind
+ * it, and the wait ends only by its timeout.  (2) Under CUDA's lazy module
+ * loading (the default), the first launch of a kernel can wait for kernels
+ * already running: the library loads all of its own kernels when the first
+ * notify is created on a device, but a caller's own kernel that records on
+ * the count (cns_cnt_record_dev) must be loaded before a wait it releases is
+ * running (cudaFuncGetAttributes on it, a launch, or
+ * CUDA_MODULE_LOADING=EAGER).  Submitting the records before the wait avoids
+ * both.
  * Errors: INVALID_HANDLE, NULL_PTR (info), INVALID_VALUE (mode), CUDA.
  */
 int cntnotify_wait_with_timeout(cns_cnt_notify_t h, cns_stream_t stream, const cns_wait_info_t *info);
@@ -453,8 +504,9 @@ int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t init, uint
  *   ops_dev, n, init, trace_dev, final_dev, stream: as cns_statemachine_run;
  *   n may be at most CNS_STATEMACHINE_NOALLOC_MAX_OPS.
  * The first call on each device looks up the array's device address there
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls on a device share the one array and
+ * (cudaGetSymbolAddress, with that device current), and so does the first
+ * call after a device reset, whose new context may place the array
+ * elsewhere; make such a first call before any stream capture.  All calls on a device share the one array and
  * it keeps what the last call left in it (nothing in it needs to start at
  * zero): calls whose kernels overlap on the GPU, e.g. on two streams at once,
  * race and give wrong traces.  No allocation happens in any call.

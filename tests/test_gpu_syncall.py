@@ -22,18 +22,35 @@ def cns():
     return c
 
 
+# Word offsets (int32) of the counters in a die-local workspace: soft counter, hard counter, and their
+# second copies 4 KB further on.
+COUNTER_WORDS = (0, 64, 1024, 1024 + 64)
+
+
+def garble_counters(ws, value):
+    """Counter garbage written over an initialised workspace's counters (not through the library): the
+    base count that the workspace check reads still says 0, so the run starts and the counts desynchronise
+    the epochs."""
+    for w in COUNTER_WORDS:
+        ws[w] = value
+
+
 def run_ring(cns, mode, core, wl, launch_ctas, v0, rounds, used=0, ratio=0, start=0, threads=256,
-             cluster_dim=0, timeout_ms=0, check=True, variant=0):
+             cluster_dim=0, timeout_ms=0, check=True, variant=0, garble=None, launch_flags=0, ws=None):
     import torch
     P, slots = v0.shape
     b0 = to_dev_u32(v0) if v0.size else None
     b1 = torch.zeros_like(b0) if v0.size else None
-    ws = cns.new_workspace(start_value=start)
+    if ws is None:
+        ws = cns.new_workspace(start_value=start)
+    if garble is not None:
+        garble_counters(ws, garble)
     group = (1 + (ratio or 1)) if core == MIX else 1
     status = torch.zeros(launch_ctas * group, dtype=torch.int32, device="cuda")
     d, rc = cns.run_syncall(mode, core, wl, launch_ctas, b0, b1, rounds, used_cores=used, aiv_ratio=ratio,
                             elems=slots, threads=threads, cluster_dim=cluster_dim, workspace=ws,
-                            cta_status=status, timeout_ms=timeout_ms, check=check, variant=variant)
+                            cta_status=status, timeout_ms=timeout_ms, check=check, variant=variant,
+                            launch_flags=launch_flags)
     torch.cuda.synchronize()
     final = from_dev_u32(b1 if rounds & 1 else b0).reshape(P, slots) if v0.size else v0.copy()
     return d, rc, final, status.cpu().numpy()
@@ -76,10 +93,13 @@ def test_zero_rounds_leaves_everything(cns):
 
 # --- ring-rotate, 148 participants, 100000 rounds, soft and hard -------------------------
 
-@pytest.mark.parametrize("mode", [SOFT, HARD])
-def test_ring_rotate_p148_100000_rounds(cns, mode):
+@pytest.mark.parametrize("mode,variant", [(SOFT, 0), (HARD, 0), (SOFT, 5), (HARD, 5)])
+def test_ring_rotate_p148_100000_rounds(cns, mode, variant):
+    """The full ring-rotate configuration against the oracle, in the guide's
+    form (variant 0) and in the bench's headline form (variant 5, die-local
+    counter copies)."""
     v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
-    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, 100000)
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, 100000, variant=variant)
     want, fc = expect_ring(oracle.WL_RING_ROTATE, v0, 100000)
     np.testing.assert_array_equal(got, want)
     np.testing.assert_array_equal(got, np.roll(v0, -100000, axis=0))
@@ -183,13 +203,13 @@ def test_workspace_reused_across_runs(cns):
 
 # --- Jacobi -------------------------------------------------------------------------------
 
-def run_jacobi(cns, u0, sweeps, ctas, mode=SOFT, threads=256):
+def run_jacobi(cns, u0, sweeps, ctas, mode=SOFT, threads=256, variant=0):
     import torch
     b0 = to_dev_f32(u0)
     b1 = torch.zeros_like(b0)
     ws = cns.new_workspace()
     d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_JACOBI, ctas, b0, b1, sweeps, elems=u0.size,
-                            threads=threads, workspace=ws)
+                            threads=threads, workspace=ws, variant=variant)
     out = (b1 if sweeps & 1 else b0).cpu().numpy()
     return d, out
 
@@ -235,6 +255,32 @@ def test_jacobi_hard_path(cns):
     np.testing.assert_array_equal(got, want)
 
 
+@pytest.fixture(scope="module")
+def jacobi_full_size_oracle():
+    """The oracle's whole field after 200 sweeps of N = 2^26 points on 592 participants (about 20 s on one
+    host core), computed once for the full-size tests below."""
+    N, S, C = 1 << 26, 200, 592
+    u0 = ci.jacobi_field(N)
+    want, fc, rc = oracle.syncall_run_jacobi(u0, S, C)
+    assert rc == oracle.OK and fc == S * C
+    return u0, want
+
+
+@pytest.mark.parametrize("mode,variant", [(SOFT, 0), (SOFT, 2), (SOFT, 5), (HARD, 5)])
+def test_jacobi_full_size_whole_field(cns, jacobi_full_size_oracle, mode, variant):
+    """The full Jacobi configuration -- 2^26 fp32 points, 592 persistent CTAs,
+    200 sweeps with a barrier between sweeps -- compared with the oracle on
+    every point: bit for bit (the bar is 1e-5 relative).  The variants the
+    bench measures, and the hard path."""
+    u0, want = jacobi_full_size_oracle
+    d, got = run_jacobi(cns, u0, 200, 592, mode=mode, variant=variant)
+    assert d.device_status == 0
+    if mode == SOFT:
+        assert d.final_counter == 200 * 592
+    np.testing.assert_allclose(got, want, rtol=1e-5, atol=0)
+    np.testing.assert_array_equal(got, want)
+
+
 def test_jacobi_full_size_sampled(cns):
     """2^26 points, 592 CTAs, 200 sweeps: sampled points from the oracle's
     light-cone evaluation, plus chunk edges and both ends."""
@@ -272,10 +318,11 @@ def test_host_in_host_out(cns):
 # --- failures reported as status, never a hang ---------------------------------------------
 
 def test_unzeroed_workspace_times_out_and_context_survives(cns):
-    """A counter left at 1 ("counter garbage": the workspace was not zeroed) puts
-    the participants in different epochs; the bounded poll gives up."""
+    """A counter at 1 ("counter garbage", written behind the library's back so
+    that the workspace check passes) puts the participants in different epochs;
+    the bounded poll gives up."""
     v0 = ci.ring_payload(3, 4, 4)
-    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3, start=1, timeout_ms=300,
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3, garble=1, timeout_ms=300,
                               check=False)
     assert rc == cns.CNS_ERR_TIMEOUT and d.device_status == cns.CNS_ERR_TIMEOUT
     assert ((st & 0xFF) == cns.CNS_CTA_ABORTED).any()
@@ -288,14 +335,14 @@ def test_unzeroed_workspace_times_out_and_context_survives(cns):
 @pytest.mark.parametrize("variant", [0, 1, 4])
 @pytest.mark.parametrize("rounds", [1, 3, 6])
 def test_hard_path_unzeroed_workspace_times_out(cns, variant, rounds):
-    """The hard path with a counter left at 1: the clusters' leaders fall into
+    """The hard path with a counter garbled to 1: the clusters' leaders fall into
     different epochs and the bounded waits give up.  A CTA that stops takes its
     whole cluster with it at the next cluster barrier, so the run ends (no CTA
     is left at a cluster barrier) and reports the timeout.  (Not the die-local
     variant: each copy sees the arrivals in its own order, so a misaligned
     start need not put anyone in a later epoch there.)"""
     v0 = ci.ring_payload(3, 8, 4)
-    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, rounds, start=1, timeout_ms=300,
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, rounds, garble=1, timeout_ms=300,
                               cluster_dim=4, check=False, variant=variant)
     assert rc == cns.CNS_ERR_TIMEOUT and d.device_status == cns.CNS_ERR_TIMEOUT
     assert ((st & 0xFF) == cns.CNS_CTA_ABORTED).any()
@@ -374,22 +421,135 @@ def test_variants_wrap_and_jacobi(cns, variant):
 
 @pytest.mark.parametrize("variant", [v for v in VARIANTS if v != 5])
 def test_variants_time_out_cleanly(cns, variant):
-    """A misaligned counter (start 1) ends a single-counter run in a timeout.
-    The die-local variant is left out: each of its copies sees the arrivals in
-    its own order, so a misaligned start need not leave anyone behind there."""
+    """A single counter garbled to 1 behind the library's back ends the run in a
+    timeout.  The die-local variant is left out: each of its copies sees the
+    arrivals in its own order, so a garbled count need not leave anyone behind
+    there (the workspace check below guards its start)."""
     v0 = ci.ring_payload(3, 4, 4)
-    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3, start=1, timeout_ms=200,
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3, garble=1, timeout_ms=200,
                               check=False, variant=variant)
     assert rc == cns.CNS_ERR_TIMEOUT
 
 
+# --- the workspace check ("counter garbage", SYNCALL guide §8) -----------------------------
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+@pytest.mark.parametrize("variant", [0, 2, 5])
+@pytest.mark.parametrize("start", [1, 3, 0xFFFFFFFF])
+def test_misaligned_start_is_refused_before_any_arrival(cns, mode, variant, start):
+    """A workspace initialised with a start that is not a multiple of P (P = 4
+    participants, or 2 clusters of 2): refused with INVALID_VALUE at once, every
+    CTA aborted, and no counter moved -- the die-local variant included, which
+    could otherwise release participants early."""
+    v0 = ci.ring_payload(3, 4, 4)
+    # an even round count: the result would be in buffer 0, which holds the input untouched
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 4, start=start, timeout_ms=2000,
+                              check=False, variant=variant, cluster_dim=2 if mode == HARD else 0)
+    assert rc == cns.CNS_ERR_INVALID_VALUE and d.device_status == cns.CNS_ERR_INVALID_VALUE
+    assert d.elapsed_ms < 100.0
+    assert ((st & 0xFF) == cns.CNS_CTA_ABORTED).all()
+    assert d.final_counter == start
+    np.testing.assert_array_equal(got, v0)
+
+
 def test_die_local_misaligned_start_ends(cns):
-    """The die-local variant from a misaligned start: whatever the copies'
-    orders, the run ends (released or timed out), never hangs."""
+    """The die-local variant from a misaligned start never reports success: the
+    workspace check refuses it before anyone arrives."""
     v0 = ci.ring_payload(3, 4, 4)
     d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_AFFINE, 4, v0, 3, start=1, timeout_ms=200,
                               check=False, variant=5)
-    assert rc in (0, cns.CNS_ERR_TIMEOUT)
+    assert rc != 0 and rc == cns.CNS_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("variant", [0, 5])
+def test_workspace_reused_with_another_participant_count(cns, variant):
+    """Runs continue on one workspace from where the last one left the counter;
+    a run whose P does not divide that count is refused, one whose P does runs
+    exactly as the oracle does from that start."""
+    import torch
+    ws = cns.new_workspace()
+    v4 = ci.ring_payload(21, 4, 8)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_XORSHIFT, 4, v4, 3, ws=ws, variant=variant)
+    assert rc == 0 and d.final_counter == 12
+    v5 = ci.ring_payload(22, 5, 8)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_XORSHIFT, 5, v5, 4, ws=ws, variant=variant, check=False)
+    assert rc == cns.CNS_ERR_INVALID_VALUE and d.final_counter == 12
+    np.testing.assert_array_equal(got, v5)
+    # the refusal raised the status: initialise a fresh one at the count the P = 4 run left
+    ws = cns.new_workspace(start_value=12)
+    v6 = ci.ring_payload(23, 6, 8)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_XORSHIFT, 6, v6, 7, ws=ws, variant=variant)
+    want, fc = expect_ring(oracle.WL_XORSHIFT, v6, 7, start=12)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == fc == 12 + 42
+    # and a second run on it continues from 54
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_XORSHIFT, 6, v6, 5, ws=ws, variant=variant)
+    want, fc = expect_ring(oracle.WL_XORSHIFT, v6, 5, start=54)
+    np.testing.assert_array_equal(got, want)
+    assert d.final_counter == fc == 84
+
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_zeroed_workspace_is_accepted_and_garbage_refused(cns, mode):
+    """A workspace zeroed by the caller (the guide's own preparation, §4.1)
+    works without syncall_workspace_init; one full of garbage is refused."""
+    import torch
+    v0 = ci.ring_payload(5, 8, 4)
+    ws = torch.zeros(cns.CNS_SYNCALL_WORKSPACE_BYTES // 4, dtype=torch.int32, device="cuda")
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 8, v0, 10, ws=ws,
+                              cluster_dim=2 if mode == HARD else 0)
+    np.testing.assert_array_equal(got, np.roll(v0, -10, axis=0))
+    g = torch.from_numpy(ci.ring_payload(99, 1, cns.CNS_SYNCALL_WORKSPACE_BYTES // 4)[0].view(np.int32).copy())
+    ws = g.cuda()
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 8, v0, 10, ws=ws, check=False,
+                              cluster_dim=2 if mode == HARD else 0)
+    assert rc == cns.CNS_ERR_INVALID_VALUE
+    np.testing.assert_array_equal(got, v0)
+
+
+def test_sense_flip_tags_the_workspace(cns):
+    """After a sense-flip run the count is no longer on the pages' epoch grid:
+    the other variants refuse the workspace, the sense-flip variant goes on."""
+    v0 = ci.ring_payload(6, 8, 4)
+    ws = cns.new_workspace()
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_ROTATE, 8, v0, 3, ws=ws, variant=6)
+    assert rc == 0
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_ROTATE, 8, v0, 3, ws=ws, variant=0, check=False)
+    assert rc == cns.CNS_ERR_INVALID_VALUE
+
+
+# --- the hard path takes its cluster shape from the launch it got ---------------------------
+
+@pytest.mark.parametrize("variant", [0, 2, 5, 6])
+@pytest.mark.parametrize("wl", ["rotate", "xorshift"])
+def test_hard_path_without_the_cluster_attribute(cns, variant, wl):
+    """The hard kernel launched without the cluster attribute (as a tool's
+    replay may launch it): each CTA is a cluster of its own, the kernel counts
+    the clusters itself, and the run is exact and fast (no timeout)."""
+    P = 148
+    R = 3001
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P, 4)
+    code = cns.CNS_WL_RING_ROTATE if wl == "rotate" else cns.CNS_WL_XORSHIFT
+    d, rc, got, st = run_ring(cns, HARD, AIV, code, P, v0, R, cluster_dim=4, variant=variant,
+                              launch_flags=cns.CNS_LAUNCH_NO_CLUSTER_ATTR)
+    want, _ = expect_ring(oracle.WL_RING_ROTATE if wl == "rotate" else oracle.WL_XORSHIFT, v0, R)
+    np.testing.assert_array_equal(got, want)
+    assert rc == 0 and d.device_status == 0 and d.cluster_used == 1
+    if variant != 6:
+        assert d.final_counter == (R * P) % oracle.counter_modulus(P)
+    assert (st == cns.CNS_CTA_DONE).all()
+    assert d.elapsed_ms < 1000.0
+    # the same workspace, now with clusters: the base count R * 148 is a multiple of 37 clusters too
+    if variant != 6:
+        d, rc, got, st = run_ring(cns, HARD, AIV, code, P, v0, R, cluster_dim=4, variant=variant)
+        assert rc == 0 and d.cluster_used == 4
+        np.testing.assert_array_equal(got, want)
+
+
+def test_launch_flags_outside_the_defined_bits_are_refused(cns):
+    v0 = ci.ring_payload(3, 4, 4)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_ROTATE, 4, v0, 3, check=False, launch_flags=2)
+    assert rc == cns.CNS_ERR_INVALID_VALUE
 
 
 # --- sense-flip comparison variant (not the guide's arithmetic) ---------------------------
@@ -480,13 +640,14 @@ def test_arrival_only_refused_with_a_payload(cns, variant):
 @pytest.mark.parametrize("mode", [SOFT, HARD])
 def test_jacobi_unzeroed_workspace_times_out(cns, mode):
     """Jacobi sweeps (split phase on the soft path, fused on the hard path)
-    with the counter left at 1: the bounded waits end the run with a timeout,
+    with the counter garbled to 1: the bounded waits end the run with a timeout,
     and the device keeps working."""
     import torch
     u0 = ci.jacobi_field(100003, seed=5)
     b0 = to_dev_f32(u0)
     b1 = torch.zeros_like(b0)
-    ws = cns.new_workspace(start_value=1)
+    ws = cns.new_workspace()
+    garble_counters(ws, 1)
     d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_JACOBI, 16, b0, b1, 6, elems=u0.size, workspace=ws,
                             timeout_ms=300, check=False, cluster_dim=4 if mode == HARD else 0)
     assert rc == cns.CNS_ERR_TIMEOUT and d.device_status == cns.CNS_ERR_TIMEOUT
