@@ -8,6 +8,7 @@
 // word 2 an abort word used by the pipeline.  A record is one device atomic
 // (release); a wait is one thread polling the count with acquire loads under
 // a time bound, so the *stream* is blocked, not the host (§4.3).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -760,6 +761,39 @@ using namespace cns;
 // Handle lifecycle
 // ---------------------------------------------------------------------------
 
+// Load every kernel that the notify calls and the pipeline launch, on the
+// current device.  Under CUDA's lazy loading (the default) a kernel's code is
+// loaded at its first launch, and that load can wait for kernels already
+// running: a record launched for the first time on one stream while a wait
+// kernel polls on another is then held back until the wait times out (a
+// test measured exactly that: a 1 s timeout on the first wait of a process,
+// 49 us for the same calls once both kernels had been loaded).  Getting a
+// kernel's attributes loads it; done once per device, when its notify pool is
+// made.
+static int preload_notify_kernels()
+{
+    const void *kernels[] = {
+        reinterpret_cast<const void *>(cnt_record_kernel),
+        reinterpret_cast<const void *>(cnt_wait_kernel<false, false>),
+        reinterpret_cast<const void *>(cnt_wait_kernel<true, false>),
+        reinterpret_cast<const void *>(cnt_wait_kernel<true, true>),
+        reinterpret_cast<const void *>(cnt_clear_line_kernel),
+        reinterpret_cast<const void *>(write_word_kernel),
+        reinterpret_cast<const void *>(sm_onepass_kernel),
+        reinterpret_cast<const void *>(pipeline_producer_kernel<true>),
+        reinterpret_cast<const void *>(pipeline_producer_kernel<false>),
+        reinterpret_cast<const void *>(pipeline_consumer_kernel<true, true>),
+        reinterpret_cast<const void *>(pipeline_consumer_kernel<false, true>),
+        reinterpret_cast<const void *>(pipeline_consumer_kernel<true, false>),
+        reinterpret_cast<const void *>(pipeline_consumer_kernel<false, false>),
+    };
+    for (const void *k : kernels) {
+        cudaFuncAttributes a;
+        CNS_CUDA(cudaFuncGetAttributes(&a, k));
+    }
+    return CNS_SUCCESS;
+}
+
 extern "C" int cntnotify_create(cns_cnt_notify_t *out, uint64_t flag)
 {
     if (!out)
@@ -772,6 +806,8 @@ extern "C" int cntnotify_create(cns_cnt_notify_t *out, uint64_t flag)
     std::lock_guard<std::mutex> lk(g_mu);
     Pool &pool = g_pools[dev.device];
     if (!pool.base) {
+        if (int rc = preload_notify_kernels())
+            return rc;
         const uint32_t cap = pool_cap();
         void *p = nullptr;
         CNS_CUDA(cudaMalloc(&p, static_cast<size_t>(cap) * kWordsPerSlot * 4));
@@ -959,14 +995,50 @@ extern "C" int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t
 // 1 MiB array, part of the library's own device image: every GPU that loads
 // the library holds it until the process exits.  On the host the name is
 // only a stand-in for the symbol, not a device address; the address comes
-// from cudaGetSymbolAddress, looked up once per device on first use.
+// from cudaGetSymbolAddress, looked up once per device on first use, and
+// again after a device reset (cudaDeviceReset destroys the context; the next
+// one loads the library's device image anew, and the array may move).
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 static_assert(static_cast<size_t>(CNS_STATEMACHINE_NOALLOC_MAX_OPS) / kChunk * sizeof(uint2) == kNoAllocScratchBytes,
               "the op limit must match the scratch array");
 static __device__ __align__(256) uint2 g_sm_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint2)];
 
+struct NoAllocScratch {
+    uint2 *addr = nullptr;          // device address of the array in the context below
+    unsigned long long ctx_id = 0;  // unique id of that context (0: unknown)
+};
 static std::mutex g_noalloc_mu;
-static uint2 *g_noalloc_scratch_addr[64];   // per device; filled on the first call there
+static NoAllocScratch g_noalloc_scratch[64];   // per device
+
+// Unique id of the calling thread's current context (the driver's cuCtxGetId,
+// reached through the runtime without linking the driver library): ids are
+// never reused within a process, so a context made after a device reset
+// gets a new one.  False when there is no current context or the driver
+// cannot tell.
+static bool current_context_id(unsigned long long *id)
+{
+    using GetCurrentFn = CUresult (*)(CUcontext *);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(f);
+        (void)cudaGetLastError();
+    });
+    CUcontext c = nullptr;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c)
+        return false;
+    return get_id(c, id) == CUDA_SUCCESS;
+}
 
 extern "C" int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, uint32_t init, uint32_t *trace_dev,
                                             uint32_t *final_dev, cns_stream_t stream)
@@ -988,16 +1060,25 @@ extern "C" int cns_statemachine_run_noalloc(const uint32_t *ops_dev, int64_t n, 
         std::lock_guard<std::mutex> lk(g_noalloc_mu);
         if (dev.device < 0 || dev.device >= 64)
             return CNS_ERR_CUDA;
-        if (!g_noalloc_scratch_addr[dev.device]) {
+        NoAllocScratch &cache = g_noalloc_scratch[dev.device];
+        unsigned long long ctx = 0;
+        const bool known = current_context_id(&ctx);
+        if (!cache.addr || !known || cache.ctx_id != ctx) {
+            // first call on this device, or its context changed (a device
+            // reset): look the array up in the current context
             void *p = nullptr;
             cudaError_t e = cudaGetSymbolAddress(&p, g_sm_noalloc_scratch);
             if (e != cudaSuccess || !p) {
                 (void)cudaGetLastError();
+                cache = NoAllocScratch{};
                 return cuda_fail(e, "cudaGetSymbolAddress(state-machine scratch)");
             }
-            g_noalloc_scratch_addr[dev.device] = static_cast<uint2 *>(p);
+            // the lookup made the context current if nothing had yet
+            unsigned long long now = 0;
+            cache.addr = static_cast<uint2 *>(p);
+            cache.ctx_id = current_context_id(&now) ? now : 0;
         }
-        summ = g_noalloc_scratch_addr[dev.device];
+        summ = cache.addr;
     }
     cudaStream_t s = to_stream(stream);
     if (n == 0) {
