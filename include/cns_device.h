@@ -462,9 +462,18 @@ __device__ __forceinline__ int grid_wait_poll(const uint32_t *w, Ok ok, uint32_t
  *               CTAs' waits then give up too
  *   observed    if not NULL, CTA 0 stores the count that released its wait
  * All threads of every calling CTA call it, and CTA 0 must be among them.
+ * With is_clear, the records meant for call r must land after call r - 1 has
+ * cleared the count, or that clear wipes them and call r waits until its
+ * timeout.  A producer that may run ahead of the consumer therefore records
+ * for call r only once it has seen go[0] >= r (call r - 1 published after its
+ * clear), or after some other event ordered after that clear.  With
+ * is_clear = 0 there is no such rule: nothing is wiped.
+ * The CTAs other than 0 wait up to twice the limit for go[0]: CTA 0 may take
+ * one limit for the previous call's go and one for the count.
  * Returns, in every thread, CNS_SUCCESS, CNS_ERR_TIMEOUT (this or an earlier
- * call failed: go[1] stays set until the caller zeroes it), or
- * CNS_ERR_INVALID_VALUE for a mode outside 0..4 (no wait taken). */
+ * call failed: go[1] stays set until the caller zeroes it, and every later
+ * call fails at once until then), or CNS_ERR_INVALID_VALUE for a mode outside
+ * 0..4 (no wait taken). */
 __device__ __forceinline__ int cns_cnt_wait_grid_dev(uint32_t *count, uint32_t *go, uint32_t call, int mode,
                                                      uint32_t v, int is_clear, uint64_t timeout_ns,
                                                      uint32_t *observed)
@@ -492,9 +501,11 @@ __device__ __forceinline__ int cns_cnt_wait_grid_dev(uint32_t *count, uint32_t *
                 cns::st_release_gpu(go, call + 1u);          // ... and before the call is published
             }
         } else {
+            // CTA 0 may spend one limit on the previous call's go and one on
+            // the count before it publishes: wait for both
             const uint32_t next = call + 1u;
-            rc = cns::grid_wait_poll(go, [=](uint32_t g) { return static_cast<int32_t>(g - next) >= 0; }, go, limit,
-                                     nullptr);
+            rc = cns::grid_wait_poll(go, [=](uint32_t g) { return static_cast<int32_t>(g - next) >= 0; }, go,
+                                     2u * limit, nullptr);
         }
     }
     return __syncthreads_or(rc != CNS_SUCCESS) ? CNS_ERR_TIMEOUT : CNS_SUCCESS;
