@@ -501,6 +501,57 @@ def secondary(cns, torch, peaks):
     return out
 
 
+PHASES = ("payload_load", "payload_store_issue", "release_fence", "near_increment_round_trip", "wait",
+          "acquire_fence", "cursor")
+
+
+def round_budget(stamps):
+    """Where one CTA's round goes, from cns_probe_round_phases stamps ([K rounds][P CTAs][8] ns): the mean
+    over rounds and CTAs of each phase, in ns.  The parts add up to the mean round (last stamp minus first).
+    The wait (from the near increment's value to the releasing count) is split at the moment the round's
+    last arrival had passed its release fence (the latest stamp 3 of the round): the part before it is
+    waiting for the last participant, the part after it the time the last increments took to land and be
+    seen by the polls."""
+    t = np.asarray(stamps, dtype=np.int64)
+    d = np.diff(t, axis=2)                                  # [K][P][7]
+    last_fence = t[:, :, 3].max(axis=1, keepdims=True)      # [K][1]: the round's last arrival issued
+    wait = d[:, :, 4]
+    for_last = np.clip(last_fence - t[:, :, 4], 0, None)
+    for_last = np.minimum(for_last, wait)
+    out = {name: float(d[:, :, i].mean()) for i, name in enumerate(PHASES)}
+    out["wait_for_last_arrival"] = float(for_last.mean())
+    out["wait_landing_and_detection"] = float((wait - for_last).mean())
+    out["round"] = float((t[:, :, 7] - t[:, :, 0]).mean())
+    # the chain of the round's last arrival: its own phases up to its release fence, from the start of
+    # its round
+    k_idx = np.arange(t.shape[0])
+    L = t[:, :, 3].argmax(axis=1)
+    out["last_arrival_start_lag"] = float((t[k_idx, L, 0] - t[:, :, 0].min(axis=1)).mean())
+    out["last_arrival_load_to_fence_done"] = float((t[k_idx, L, 3] - t[k_idx, L, 0]).mean())
+    return {k: round(v, 1) for k, v in out.items()}
+
+
+def probe_phases(cns, torch, ctas=P_HEAD, rounds=20000, stamp_rounds=512):
+    """The headline round with phase stamps (cns_probe_round_phases); returns the budget and the probe's own
+    ns/round (the stamps' timer reads make it a little slower than the headline kernel)."""
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, ctas, SLOTS_HEAD)
+    b0 = torch.from_numpy(v0.view(np.int32).copy()).cuda()
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    st = torch.zeros(stamp_rounds * ctas * 8, dtype=torch.int64, device="cuda")
+    ms, rc = timed_run(torch, lambda: cns.cns_probe_round_phases(ctas, 256, rounds, stamp_rounds, b0, b1, ws, st))
+    budget_mirror = ws.numel() * 4 >= cns.CNS_SYNCALL_WORKSPACE_MIRROR_BYTES and ctas <= cns.CNS_SYNCALL_MIRROR_MAX_P
+    cns.check(rc, "cns_probe_round_phases")
+    ok = np.array_equal((b1 if rounds & 1 else b0).cpu().numpy().view(np.uint32).reshape(ctas, SLOTS_HEAD),
+                        np.roll(v0, -(rounds % ctas), axis=0))
+    budget = round_budget(st.cpu().numpy().reshape(stamp_rounds, ctas, 8))
+    budget["probe_ns_per_round"] = round(ms * 1e6 / rounds, 1)
+    budget["payload_copies_per_die"] = bool(budget_mirror)
+    budget["stamped_rounds"] = stamp_rounds
+    budget["correct"] = bool(ok)
+    return budget
+
+
 def barrier_context(sec, rtt_mean, far, variant):
     """The empty-round barrier in its two contracts, against the same round trips: with the release and
     acquire that data rounds need (the headline's variant), and arrival only as the pages define SYNCALL
@@ -576,6 +627,7 @@ def run_native(args):
     cpu = time_oracle(args.cpu_seconds) if world == 1 else None
     if cpu is not None and not args.no_secondary:
         cpu["twin"] = time_twin()
+    budget = probe_phases(cns, torch) if args.variant == 5 else None
     traffic = load_traffic().get(f"syncall_soft_ring_rotate_148_variant{args.variant}", {})
     achieved = 1e3 / ns_round            # barrier rounds per microsecond
     peak = 1e3 / rtt_mean                # one round per L2 atomic round trip (mean over SMs)
@@ -603,7 +655,8 @@ def run_native(args):
                                 "atom_max": round(rtt_max, 1), "arrive_poll_pair_median": round(pair_med, 1),
                                 "ld_relaxed_median": round(ld_med, 1)},
                      "ns_per_round_over_rtt": round(ns_round / rtt_mean, 3),
-                     "context": barrier_context(sec, rtt_mean, far, args.variant)},
+                     "context": dict(barrier_context(sec, rtt_mean, far, args.variant),
+                                     round_budget_ns=budget)},
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,
@@ -690,7 +743,16 @@ def case_pipeline(args):
     print("case pipeline: ok")
 
 
-CASES = {"soft148-small": case_soft148_small, "hard148-small": case_hard148_small,
+def case_phases(args):
+    """The headline round with phase stamps: prints the budget (one launch, 20000 rounds)."""
+    import torch
+    import counted_notify_sync_gb300 as cns
+    cns.build()
+    torch.cuda.set_device(0)
+    print(json.dumps(probe_phases(cns, torch)))
+
+
+CASES = {"phases": case_phases, "soft148-small": case_soft148_small, "hard148-small": case_hard148_small,
          "jacobi-small": case_jacobi_small, "statemachine": case_statemachine, "pipeline": case_pipeline}
 
 

@@ -26,15 +26,18 @@ def _torch():
     return torch
 
 
-def new_workspace(device=None, start_value: int = 0, stream=None, die_local: bool = True):
-    """A zeroed SYNCALL workspace on `device`: CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES long (usable by every
-    barrier variant) or, with die_local=False, the minimal CNS_SYNCALL_WORKSPACE_BYTES.  The die-local size
-    starts on a CNS_SYNCALL_DIE_LOCAL_ALIGN boundary, so that its two counter copies sit on different dies."""
+def new_workspace(device=None, start_value: int = 0, stream=None, die_local: bool = True, mirror: bool = True):
+    """An initialised SYNCALL workspace on `device`: CNS_SYNCALL_WORKSPACE_MIRROR_BYTES long (usable by every
+    barrier variant, with room for the die-local variant's per-die payload copies), or
+    CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES with mirror=False, or the minimal CNS_SYNCALL_WORKSPACE_BYTES with
+    die_local=False.  The die-local sizes start on a CNS_SYNCALL_DIE_LOCAL_ALIGN boundary, so that the two
+    copies of each counter sit on different dies."""
     torch = _torch()
     if not die_local:
         ws = torch.empty(_native.CNS_SYNCALL_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device or "cuda")
     else:
-        nbytes, align = _native.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES, _native.CNS_SYNCALL_DIE_LOCAL_ALIGN
+        nbytes = _native.CNS_SYNCALL_WORKSPACE_MIRROR_BYTES if mirror else _native.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES
+        align = _native.CNS_SYNCALL_DIE_LOCAL_ALIGN
         raw = torch.empty((nbytes + align) // 4, dtype=torch.int32, device=device or "cuda")
         skip = (-raw.data_ptr()) % align // 4
         ws = raw[skip:skip + nbytes // 4]   # a view: keeps `raw` alive

@@ -51,6 +51,8 @@ CNS_BARRIER_ARRIVAL_ONLY_DIE_LOCAL = 8
 CNS_SYNCALL_REPLICA_OFFSET = 4096
 CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES = 8192
 CNS_SYNCALL_DIE_LOCAL_ALIGN = 8192
+CNS_SYNCALL_WORKSPACE_MIRROR_BYTES = 24576
+CNS_SYNCALL_MIRROR_MAX_P = 255
 CNS_CTA_DONE = 1
 CNS_CTA_IDLE = 2
 CNS_CTA_ABORTED = 4
@@ -129,6 +131,8 @@ _SIGS = {
     "cns_probe_atomic_rtt": (c_int, [c_int, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "cns_probe_same_address_throughput": (c_int, [c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "cns_probe_grid_sync": (c_int, [c_int32, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
+    "cns_probe_round_phases": (c_int, [c_int32, c_int32, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_size_t,
+                                       c_void_p, c_void_p]),
     "cns_version": (c_int, [POINTER(c_int32), POINTER(c_int32)]),
     "cns_error_string": (c_char_p, [c_int]),
 }
@@ -290,6 +294,14 @@ def cns_probe_same_address_throughput(grid: int, threads: int, iters: int, word,
 
 def cns_probe_grid_sync(ctas: int, threads: int, rounds: int, buf0, buf1, stream=None) -> int:
     return lib().cns_probe_grid_sync(ctas, threads, rounds, ptr(buf0), ptr(buf1), stream_handle(stream))
+
+
+def cns_probe_round_phases(ctas: int, threads: int, rounds: int, stamp_rounds: int, buf0, buf1, workspace, stamps,
+                           stream=None, workspace_bytes: int | None = None) -> int:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+    return lib().cns_probe_round_phases(ctas, threads, rounds, stamp_rounds, ptr(buf0), ptr(buf1), ptr(workspace),
+                                        workspace_bytes, ptr(stamps), stream_handle(stream))
 
 
 def cns_version():

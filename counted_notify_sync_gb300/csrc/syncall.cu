@@ -33,6 +33,8 @@ struct SyncallParams {
     uint32_t P;             // participants (ring length / Jacobi chunks)
     uint32_t group;         // MIX group size, else 1
     int32_t core_type;
+    int32_t solo;           // soft path, thread 0 alone touches memory: the other threads leave at once
+    uint32_t *mirror;       // soft die-local one-uint4 rings: the per-die payload copies, else null
 };
 
 // ---------------------------------------------------------------------------
@@ -279,6 +281,146 @@ __device__ __forceinline__ uint32_t cta_role(const SyncallParams &p, uint32_t b)
     return p.core_type == CNS_AIC_ONLY ? 1u : 0u;
 }
 
+// The workspace check's decision for the calling thread (see
+// workspace_refused), reading the status, abort, tag and base words.
+template <int V>
+__device__ __forceinline__ bool workspace_check_refuses(const Barrier &bar, const uint32_t *base_word, uint32_t *base)
+{
+    const uint32_t tag = ld_relaxed_gpu(bar.status_line + kTagWord);
+    *base = ld_relaxed_gpu(base_word);
+    // a status or abort flag left by an earlier run that failed
+    const bool failed = (ld_relaxed_gpu(bar.status_line) | ld_relaxed_gpu(bar.status_line + 1)) != 0u;
+    return failed || workspace_refused<V>(tag, *base, bar.e);
+}
+
+// A refused run: CTA 0 reports it (keeping an earlier failure's code;
+// anything else in the status word, garbage, becomes INVALID_VALUE).
+__device__ __forceinline__ void report_refusal(const Barrier &bar, uint32_t b)
+{
+    if (b != 0)
+        return;
+    const uint32_t cur = ld_relaxed_gpu(bar.status_line);
+    if (cur != static_cast<uint32_t>(CNS_ERR_TIMEOUT) && cur != static_cast<uint32_t>(CNS_ERR_INVALID_VALUE)) {
+        st_relaxed_gpu(bar.status_line + 2, 0u);
+        st_relaxed_gpu(bar.status_line + 3, 0u);
+        st_relaxed_gpu(bar.status_line, static_cast<uint32_t>(CNS_ERR_INVALID_VALUE));
+    }
+    atom_exch_release_gpu(bar.status_line + 1, 1u);
+}
+
+// After a run that CTA 0 finished without a failure: every arrival of the run
+// has landed once CTA 0 is past its last barrier, so the counter stands at
+// base + rounds * P (mod M); that becomes the base count.
+template <int V>
+__device__ __forceinline__ void record_base(const SyncallParams &p, const Barrier &bar, uint32_t *base_word,
+                                            uint32_t base)
+{
+    if constexpr (V == kBvSenseFlip) {
+        st_relaxed_gpu(bar.status_line + kTagWord, CNS_SYNCALL_WORKSPACE_TAG_FLIP);
+    } else {
+        const uint64_t M = static_cast<uint64_t>(bar.e.Mm1) + 1u;
+        const uint64_t steps = static_cast<uint64_t>(p.rounds) % (M / bar.e.P);
+        st_relaxed_gpu(base_word, static_cast<uint32_t>((base + steps * bar.e.P) % M));
+        st_relaxed_gpu(bar.status_line + kTagWord, CNS_SYNCALL_WORKSPACE_TAG);
+    }
+}
+
+// The per-die payload copies of a one-uint4 ring (die-local variant, on a
+// workspace of CNS_SYNCALL_WORKSPACE_MIRROR_BYTES).  The states of the rounds
+// live in two pairs of 4 KB blocks after the die-local counters: pair k holds
+// the state that round k's parity reads, as row p of each block; the two
+// blocks of a pair differ in address bit 12, so they sit on different dies.
+// A participant writes its new row into both blocks of a pair and reads its
+// neighbour's row from the block on its own die, so every payload load stays
+// on its die.  Round 0 reads the caller's buffer 0, and the last two rounds
+// also write the caller's buffers, which then end exactly as without copies.
+constexpr uint32_t kMirrorPairWords = 2048;        // 8 KB: two 4 KB blocks
+constexpr uint32_t kMirrorBlockRows = 256;         // uint4 rows per 4 KB block
+constexpr uint32_t kMirrorTimingRow = kMirrorBlockRows - 1;   // never a payload row (P <= 255)
+
+struct MirrorState {
+    const uint4 *near_src[2];   // the block of pair k on this SM's die
+    uint4 *blk[2][2];           // pair k, block c
+};
+
+__device__ __forceinline__ MirrorState mirror_setup(uint32_t *mirror)
+{
+    MirrorState m;
+    for (int k = 0; k < 2; ++k) {
+        uint4 *b0 = reinterpret_cast<uint4 *>(mirror + k * kMirrorPairWords);
+        uint4 *b1 = b0 + kMirrorBlockRows;
+        m.blk[k][0] = b0;
+        m.blk[k][1] = b1;
+        // time both blocks on their timing row (adds of 0: nothing changes)
+        const bool far0 = copy_is_farther(reinterpret_cast<uint32_t *>(b0 + kMirrorTimingRow),
+                                          reinterpret_cast<uint32_t *>(b1 + kMirrorTimingRow));
+        m.near_src[k] = far0 ? b1 : b0;
+    }
+    return m;
+}
+
+template <int WL>
+__device__ __forceinline__ void mirror_round(const SyncallParams &p, const MirrorState &m, uint32_t b, int64_t r)
+{
+    const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
+    const int src = static_cast<int>(r & 1), dst = src ^ 1;
+    uint4 v = ld_relaxed_gpu_v4((r == 0 ? static_cast<const uint4 *>(p.buf0) : m.near_src[src]) + q);
+    const uint32_t rr = static_cast<uint32_t>(r);
+    v.x = ring_op<WL>(v.x, rr);
+    v.y = ring_op<WL>(v.y, rr);
+    v.z = ring_op<WL>(v.z, rr);
+    v.w = ring_op<WL>(v.w, rr);
+    st_relaxed_gpu_v4(m.blk[dst][0] + b, v);
+    st_relaxed_gpu_v4(m.blk[dst][1] + b, v);
+    if (r + 2 >= p.rounds)
+        st_relaxed_gpu_v4(static_cast<uint4 *>(dst ? p.buf1 : p.buf0) + b, v);
+}
+
+// The soft rounds when thread 0 alone touches memory (no payload, or a row of
+// one uint4 or one word): the other threads of the CTA have left, and the
+// barrier needs no drain and no closing block barrier -- thread 0 arrives
+// and waits itself.  Same arithmetic, same memory operations otherwise.
+template <int WL, int V>
+__device__ __forceinline__ void solo_rounds(const SyncallParams &p, uint32_t b, uint32_t role)
+{
+    Barrier bar = p.bar;
+    uint32_t *base_word = bar.status_line + kBaseWordSoft;
+    uint32_t base = 0;
+    if (workspace_check_refuses<V>(bar, base_word, &base)) {
+        report_refusal(bar, b);
+        if (p.cta_status)
+            p.cta_status[b] = static_cast<int32_t>(CNS_CTA_ABORTED | (role << 8));
+        return;
+    }
+    if constexpr (V == kBvDieLocal || V == kBvArrivalDieLocal)
+        choose_near_copy(bar);
+    MirrorState m{};
+    const bool mirrored = (V == kBvDieLocal) && p.mirror != nullptr;
+    if (mirrored)
+        m = mirror_setup(p.mirror);
+    EpochCursor cursor{0u, 0u, false};
+    bool stop = false;
+    for (int64_t r = 0; r < p.rounds; ++r) {
+        if (WL != CNS_WL_EMPTY) {
+            if (mirrored) {
+                mirror_round<WL>(p, m, b, r);
+            } else {
+                const bool odd = (r & 1) != 0;
+                ring_phase<WL>(static_cast<const uint32_t *>(odd ? p.buf1 : p.buf0),
+                               static_cast<uint32_t *>(odd ? p.buf0 : p.buf1), b, p.P, p.elems,
+                               static_cast<uint32_t>(r));
+            }
+        }
+        stop = arrive_and_wait<V>(bar, cursor, static_cast<uint32_t>(r), b);
+        if (stop)
+            break;
+    }
+    if (b == 0 && !stop)
+        record_base<V>(p, bar, base_word, base);
+    if (p.cta_status)
+        p.cta_status[b] = static_cast<int32_t>((stop ? CNS_CTA_ABORTED : CNS_CTA_DONE) | (role << 8));
+}
+
 template <int MODE, int WL, int V>
 __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
 {
@@ -294,6 +436,13 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         if (threadIdx.x == 0 && p.cta_status)
             p.cta_status[b] = static_cast<int32_t>(CNS_CTA_IDLE | (role << 8));
         return;
+    }
+    if constexpr (MODE == CNS_SYNCALL_SOFT && WL != CNS_WL_JACOBI) {
+        if (p.solo) {
+            if (threadIdx.x == 0)
+                solo_rounds<WL, V>(p, b, role);
+            return;
+        }
     }
     JacState js{s_jac_stage, &s_jac_bar, 0u, &s_jac_flag};
     if (threadIdx.x == 0) {
@@ -332,27 +481,11 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
     uint32_t base = 0;
     {
         int refuse = 0;
-        if (threadIdx.x == 0) {
-            const uint32_t tag = ld_relaxed_gpu(bar.status_line + kTagWord);
-            base = ld_relaxed_gpu(base_word);
-            // a status or abort flag left by an earlier run that failed
-            const bool failed = (ld_relaxed_gpu(bar.status_line) | ld_relaxed_gpu(bar.status_line + 1)) != 0u;
-            refuse = (failed || workspace_refused<V>(tag, base, bar.e)) ? 1 : 0;
-        }
+        if (threadIdx.x == 0)
+            refuse = workspace_check_refuses<V>(bar, base_word, &base) ? 1 : 0;
         if (__syncthreads_or(refuse)) {
             if (threadIdx.x == 0) {
-                if (b == 0) {
-                    // keep an earlier failure's code; anything else in the
-                    // status word (garbage) becomes INVALID_VALUE
-                    const uint32_t cur = ld_relaxed_gpu(bar.status_line);
-                    if (cur != static_cast<uint32_t>(CNS_ERR_TIMEOUT) &&
-                        cur != static_cast<uint32_t>(CNS_ERR_INVALID_VALUE)) {
-                        st_relaxed_gpu(bar.status_line + 2, 0u);
-                        st_relaxed_gpu(bar.status_line + 3, 0u);
-                        st_relaxed_gpu(bar.status_line, static_cast<uint32_t>(CNS_ERR_INVALID_VALUE));
-                    }
-                    atom_exch_release_gpu(bar.status_line + 1, 1u);
-                }
+                report_refusal(bar, b);
                 if (p.cta_status)
                     p.cta_status[b] = static_cast<int32_t>(CNS_CTA_ABORTED | (role << 8));
             }
@@ -403,20 +536,113 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         if constexpr (MODE == CNS_SYNCALL_HARD)
             stop = hard_barrier_finish(&s_flag);
     }
-    if (threadIdx.x == 0 && b == 0 && !stop) {
-        // every arrival of the run has landed once CTA 0 is past its last
-        // barrier: the counter stands at base + rounds * P (mod M)
-        if constexpr (V == kBvSenseFlip) {
-            st_relaxed_gpu(bar.status_line + kTagWord, CNS_SYNCALL_WORKSPACE_TAG_FLIP);
-        } else {
-            const uint64_t M = static_cast<uint64_t>(bar.e.Mm1) + 1u;
-            const uint64_t steps = static_cast<uint64_t>(p.rounds) % (M / bar.e.P);
-            st_relaxed_gpu(base_word, static_cast<uint32_t>((base + steps * bar.e.P) % M));
-            st_relaxed_gpu(bar.status_line + kTagWord, CNS_SYNCALL_WORKSPACE_TAG);
-        }
-    }
+    if (threadIdx.x == 0 && b == 0 && !stop)
+        record_base<V>(p, bar, base_word, base);
     if (threadIdx.x == 0 && p.cta_status)
         p.cta_status[b] = static_cast<int32_t>((stop ? CNS_CTA_ABORTED : CNS_CTA_DONE) | (role << 8));
+}
+
+// ---------------------------------------------------------------------------
+// Where the headline round's time goes (a probe)
+// ---------------------------------------------------------------------------
+//
+// The round of syncall_kernel<SOFT, RING_ROTATE, die-local> as syncall_run
+// runs it for rows of one uint4 (thread 0 alone, through the per-die payload
+// copies when the workspace has room for them), step for step, with
+// %globaltimer stamps at the phase boundaries.  A stamp that follows a load
+// or an atomic is taken only once its value has arrived.  The stamps of the
+// last `stamp_rounds` rounds stay in shared memory until the run ends, so the
+// probe adds no memory operation to the chain it measures (only the timer
+// reads).  Per round and CTA:
+//   [0] round start
+//   [1] the neighbour's row has arrived
+//   [2] the new row's stores are issued
+//   [3] the release fence is done (the stores performed)
+//   [4] the near copy's returning increment has arrived (the far one issued)
+//   [5] the count that releases the round has arrived (= [4] for the round's
+//       last arrival on the copy)
+//   [6] the acquire fence is done
+//   [7] the cursor is advanced (the next round's start)
+constexpr int kPhaseStamps = 8;
+
+// The global timer, read only once `dep` (a loaded value) is known.
+__device__ __forceinline__ uint64_t globaltimer_after(uint32_t dep)
+{
+    uint64_t t;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0x9E3779B9;\n\tmov.u64 %0, 0;\n\t"
+                 "@p mov.u64 %0, %%globaltimer;\n\t@!p mov.u64 %0, %%globaltimer;\n\t}"
+                 : "=l"(t)
+                 : "r"(dep));
+    return t;
+}
+
+__global__ void __launch_bounds__(1024) round_phase_probe_kernel(const SyncallParams p, uint64_t *stamps,
+                                                                 int32_t stamp_rounds)
+{
+    extern __shared__ uint64_t s_stamp[];   // stamp_rounds * kPhaseStamps
+    if (threadIdx.x != 0)
+        return;
+    const uint32_t b = blockIdx.x;
+    Barrier bar = p.bar;
+    choose_near_copy(bar);
+    MirrorState m{};
+    if (p.mirror)
+        m = mirror_setup(p.mirror);
+    EpochCursor cursor{0u, 0u, false};
+    const int64_t first = p.rounds - stamp_rounds;
+    const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
+    uint64_t t[kPhaseStamps];
+    t[7] = globaltimer_ns();
+    bool stop = false;
+    for (int64_t r = 0; r < p.rounds && !stop; ++r) {
+        const int src = static_cast<int>(r & 1), dst = src ^ 1;
+        t[0] = t[7];
+        const uint4 *from = p.mirror ? (r == 0 ? static_cast<const uint4 *>(p.buf0) : m.near_src[src])
+                                     : static_cast<const uint4 *>(src ? p.buf1 : p.buf0);
+        const uint4 v = ld_relaxed_gpu_v4(from + q);   // ring rotate: the row as it is
+        t[1] = globaltimer_after(v.x ^ v.w);
+        if (p.mirror) {
+            st_relaxed_gpu_v4(m.blk[dst][0] + b, v);
+            st_relaxed_gpu_v4(m.blk[dst][1] + b, v);
+            if (r + 2 >= p.rounds)
+                st_relaxed_gpu_v4(static_cast<uint4 *>(dst ? p.buf1 : p.buf0) + b, v);
+        } else {
+            st_relaxed_gpu_v4(static_cast<uint4 *>(dst ? p.buf1 : p.buf0) + b, v);
+        }
+        t[2] = globaltimer_ns();
+        fence_release_gpu();
+        t[3] = globaltimer_ns();
+        uint32_t target;
+        const uint32_t before = copies_arrive<false>(bar.ctr, bar.ctr2, bar.e, cursor, &target);
+        t[4] = globaltimer_after(before);
+        const uint32_t mine = (before == bar.e.Mm1) ? 0u : before + 1u;
+        if (epoch_reached(mine, target, bar.e)) {
+            t[5] = t[4];
+        } else {
+            uint32_t seen = 0;
+            stop = poll_until(bar.ctr,
+                              [&](uint32_t cur) {
+                                  seen = cur;
+                                  return epoch_reached(cur, target, bar.e);
+                              },
+                              bar.status_line, bar.timeout_ns, static_cast<uint32_t>(r), b, true, 0, false);
+            t[5] = globaltimer_after(seen);
+        }
+        fence_acquire_gpu();
+        t[6] = globaltimer_ns();
+        epoch_advance(cursor, target, bar.e);
+        t[7] = globaltimer_ns();
+        if (r >= first) {
+            uint64_t *row = s_stamp + (r - first) * kPhaseStamps;
+            for (int k = 0; k < kPhaseStamps; ++k)
+                row[k] = t[k];
+        }
+    }
+    if (!stop) {
+        for (int32_t k = 0; k < stamp_rounds; ++k)
+            for (int i = 0; i < kPhaseStamps; ++i)
+                stamps[(static_cast<int64_t>(k) * gridDim.x + b) * kPhaseStamps + i] = s_stamp[k * kPhaseStamps + i];
+    }
 }
 
 // Word offsets of the second copies of the counters (die-local variant).
@@ -674,6 +900,16 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     prm.P = P;
     prm.group = static_cast<uint32_t>(group);
     prm.core_type = core_type;
+    // thread 0 alone touches memory: no payload, or rows of one uint4 or one word
+    const bool ring = d->workload == CNS_WL_RING_AFFINE || d->workload == CNS_WL_RING_ROTATE ||
+                      d->workload == CNS_WL_XORSHIFT;
+    prm.solo = (mode == CNS_SYNCALL_SOFT &&
+                (d->workload == CNS_WL_EMPTY || (ring && (d->elems == 4 || d->elems <= 1)))) ? 1 : 0;
+    // the per-die payload copies: die-local variant, one-uint4 rows, P <= 255, room in the workspace
+    prm.mirror = (prm.solo && ring && d->elems == 4 && d->barrier_variant == CNS_BARRIER_DIE_LOCAL &&
+                  P <= CNS_SYNCALL_MIRROR_MAX_P && d->workspace_bytes >= CNS_SYNCALL_WORKSPACE_MIRROR_BYTES)
+                     ? ws + CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES / 4
+                     : nullptr;
     if (mode == CNS_SYNCALL_SOFT) {
         prm.bar.ctr = ws;
         prm.bar.ctr2 = ws + kSoftCopyWord;
@@ -762,4 +998,57 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
             d->cluster_used = static_cast<int32_t>(seen);
     }
     return (st == CNS_ERR_TIMEOUT || st == CNS_ERR_INVALID_VALUE) ? st : CNS_SUCCESS;
+}
+
+extern "C" int cns_probe_round_phases(int32_t ctas, int32_t threads, int64_t rounds, int32_t stamp_rounds,
+                                      void *buf0_dev, void *buf1_dev, void *workspace_dev, size_t workspace_bytes,
+                                      uint64_t *stamps_dev, cns_stream_t stream)
+{
+    TraceRange tr("cns_probe_round_phases", static_cast<uint64_t>(rounds));
+    if (!buf0_dev || !buf1_dev || !workspace_dev || !stamps_dev)
+        return CNS_ERR_NULL_PTR;
+    if (ctas < 1 || threads < 32 || threads > 1024 || threads % 32 != 0 || stamp_rounds < 1 ||
+        stamp_rounds > 1024 || rounds < stamp_rounds)
+        return CNS_ERR_INVALID_VALUE;
+    if (!aligned(workspace_dev, CNS_SYNCALL_LINE_BYTES) || !aligned(buf0_dev, 16) || !aligned(buf1_dev, 16) ||
+        !aligned(stamps_dev, 8) || workspace_bytes < CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES)
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    cudaStream_t s = to_stream(stream);
+    const size_t smem = static_cast<size_t>(stamp_rounds) * kPhaseStamps * sizeof(uint64_t);
+    const void *k = reinterpret_cast<const void *>(round_phase_probe_kernel);
+    if (smem > 48 * 1024)
+        CNS_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+    int per_sm = 0;
+    CNS_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem));
+    if (static_cast<int64_t>(per_sm) * dev.sm_count < ctas)
+        return CNS_ERR_NOT_RESIDENT;
+    workspace_init_kernel<<<1, 128, 0, s>>>(static_cast<uint32_t *>(workspace_dev), CNS_SYNCALL_WORKSPACE_BYTES / 4,
+                                            0u, 1);
+    CNS_CUDA(cudaGetLastError());
+    SyncallParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    uint32_t *ws = static_cast<uint32_t *>(workspace_dev);
+    prm.buf0 = buf0_dev;
+    prm.buf1 = buf1_dev;
+    prm.elems = 4;
+    prm.rounds = rounds;
+    prm.bar.ctr = ws;
+    prm.bar.ctr2 = ws + kSoftCopyWord;
+    prm.bar.status_line = ws + CNS_SYNCALL_LINE_BYTES / 4;
+    prm.bar.timeout_ns = barrier_timeout_ns(0);
+    prm.bar.variant = CNS_BARRIER_DIE_LOCAL;
+    prm.bar.e.P = static_cast<uint32_t>(ctas);
+    prm.bar.e.Mm1 = counter_bound(prm.bar.e.P);
+    prm.P = static_cast<uint32_t>(ctas);
+    prm.group = 1;
+    prm.solo = 1;
+    prm.mirror = (workspace_bytes >= CNS_SYNCALL_WORKSPACE_MIRROR_BYTES && ctas <= CNS_SYNCALL_MIRROR_MAX_P)
+                     ? ws + CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES / 4
+                     : nullptr;
+    void *args[] = {&prm, &stamps_dev, &stamp_rounds};
+    CNS_CUDA(cudaLaunchCooperativeKernel(k, dim3(ctas), dim3(threads), args, smem, s));
+    return CNS_SUCCESS;
 }

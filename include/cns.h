@@ -137,6 +137,19 @@ typedef enum {
 #define CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES 8192
 #define CNS_SYNCALL_DIE_LOCAL_ALIGN 8192
 
+/* A die-local workspace of CNS_SYNCALL_WORKSPACE_MIRROR_BYTES (same 8 KB
+ * alignment) also carries per-die copies of a ring payload of one uint4 per
+ * participant: with CNS_BARRIER_DIE_LOCAL on the soft path and at most
+ * CNS_SYNCALL_MIRROR_MAX_P participants, each round's rows are written into
+ * two 4 KB blocks on different dies (bytes 8192..24575 of the workspace) and
+ * every participant reads its neighbour's row from the block on its own die.
+ * Round 0 reads buffer 0 and the last two rounds also write the caller's
+ * buffers, so buf0_dev and buf1_dev end exactly as without the copies; the
+ * rounds in between leave them untouched.  The blocks need no
+ * initialisation. */
+#define CNS_SYNCALL_WORKSPACE_MIRROR_BYTES 24576
+#define CNS_SYNCALL_MIRROR_MAX_P 255
+
 /* How a participant learns that a round's target was reached
  * (cns_syncall_data_t.barrier_variant).  Variants 0-5 arrive with one atomic
  * increment and take target = (before / P + 1) * P from the value returned
@@ -631,6 +644,33 @@ int cns_probe_same_address_throughput(int32_t grid, int32_t threads, int32_t ite
  */
 int cns_probe_grid_sync(int32_t ctas, int32_t threads, int64_t rounds, void *buf0_dev, void *buf1_dev,
                         cns_stream_t stream);
+
+/*
+ * cns_probe_round_phases -- where the time of one round of the headline goes:
+ * the soft SYNCALL round on die-local counter copies (CNS_BARRIER_DIE_LOCAL)
+ * with the ring-rotate payload of one uint4 per CTA ([SYNCALL] §5.2: arrive,
+ * target, poll), run as syncall_run runs it (thread 0 alone; the per-die
+ * payload copies when workspace_bytes allows them), with %globaltimer stamps
+ * (ns) at the phase boundaries.  The call initialises the workspace (start
+ * 0) and makes one cooperative launch of `ctas` CTAs; the stamps of the last
+ * stamp_rounds rounds are kept in shared memory and written to stamps_dev at
+ * the end.
+ *   buf0_dev, buf1_dev  ctas uint4 each, 16-byte aligned (round 0 reads buf0)
+ *   workspace_dev       workspace_bytes >= CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES,
+ *                       128-byte aligned (8 KB-aligned puts the copies on
+ *                       different dies)
+ *   stamps_dev          out uint64[stamp_rounds][ctas][8]; per round and CTA:
+ *                       round start, neighbour's row arrived, new row's stores
+ *                       issued, release fence done, near increment's value
+ *                       arrived, releasing count arrived (= the previous stamp
+ *                       for the round's last arrival on the copy), acquire
+ *                       fence done, cursor advanced (the next round's start)
+ *   rounds >= stamp_rounds, 1 <= stamp_rounds <= 1024
+ * Errors: NULL_PTR, INVALID_VALUE, NOT_RESIDENT, CUDA.
+ */
+int cns_probe_round_phases(int32_t ctas, int32_t threads, int64_t rounds, int32_t stamp_rounds, void *buf0_dev,
+                           void *buf1_dev, void *workspace_dev, size_t workspace_bytes, uint64_t *stamps_dev,
+                           cns_stream_t stream);
 
 /* Library version and the compute capability it was built for (103). */
 int cns_version(int32_t *version, int32_t *built_sm);

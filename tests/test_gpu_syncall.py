@@ -687,7 +687,68 @@ def test_new_workspace_is_aligned_for_die_local_copies(cns):
     for _ in range(4):
         ws = cns.new_workspace()
         assert ws.data_ptr() % cns.CNS_SYNCALL_DIE_LOCAL_ALIGN == 0
+        assert ws.numel() * 4 == cns.CNS_SYNCALL_WORKSPACE_MIRROR_BYTES
+        ws = cns.new_workspace(mirror=False)
+        assert ws.data_ptr() % cns.CNS_SYNCALL_DIE_LOCAL_ALIGN == 0
         assert ws.numel() * 4 == cns.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES
+
+
+# --- rounds on thread 0 alone, and the die-local payload copies ----------------------------
+
+def _both_buffers(cns, wl, v0, R, variant, ws_bytes_kind, mode=SOFT):
+    import torch
+    P = v0.shape[0]
+    b0 = to_dev_u32(v0)
+    b1 = torch.zeros_like(b0)
+    if ws_bytes_kind == "mirror":
+        ws = cns.new_workspace()
+    elif ws_bytes_kind == "die_local":
+        ws = cns.new_workspace(mirror=False)
+    else:
+        ws = cns.new_workspace(die_local=False)
+    status = torch.zeros(P, dtype=torch.int32, device="cuda")
+    d, rc = cns.run_syncall(mode, AIV, wl, P, b0, b1, R, elems=v0.shape[1], workspace=ws, cta_status=status,
+                            variant=variant)
+    assert rc == 0 and d.device_status == 0 and (status.cpu().numpy() == cns.CNS_CTA_DONE).all()
+    M = oracle.counter_modulus(P)
+    if mode == SOFT:
+        assert d.final_counter == (R * P) % M
+    return from_dev_u32(b0).reshape(P, -1), from_dev_u32(b1).reshape(P, -1)
+
+
+WLS = {"rotate": (2, oracle.WL_RING_ROTATE), "affine": (1, oracle.WL_RING_AFFINE), "xorshift": (3, oracle.WL_XORSHIFT)}
+
+
+@pytest.mark.parametrize("wl", sorted(WLS))
+@pytest.mark.parametrize("P", [1, 2, 3, 148, 255, 256])
+@pytest.mark.parametrize("R", [1, 2, 3, 8, 1001])
+def test_one_uint4_rings_through_the_payload_copies(cns, wl, P, R):
+    """Rows of one uint4 on the die-local variant with a mirror-size workspace
+    (per-die payload copies up to 255 participants; 256 runs without them):
+    both caller buffers end as the oracle's last two states -- buffer R & 1
+    holds round R's state and the other round R - 1's -- exactly as on a plain
+    die-local workspace and on the guide's counter poll."""
+    code, owl = WLS[wl]
+    v0 = ci.ring_payload(31 + P, P, 4)
+    states = {R: expect_ring(owl, v0, R)[0], R - 1: expect_ring(owl, v0, R - 1)[0] if R > 1 else v0}
+    for kind, variant in (("mirror", 5), ("die_local", 5), ("plain", 0)):
+        b0, b1 = _both_buffers(cns, code, v0, R, variant, kind)
+        fin, prev = (b1, b0) if R & 1 else (b0, b1)
+        np.testing.assert_array_equal(fin, states[R], err_msg=kind)
+        np.testing.assert_array_equal(prev, states[R - 1], err_msg=kind)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 5, 6])
+@pytest.mark.parametrize("slots", [0, 1, 4])
+def test_solo_rounds_every_variant(cns, variant, slots):
+    """Rounds that thread 0 runs alone (no payload, one word or one uint4 per
+    row) with every data-carrying variant: exact against the oracle over 3001
+    rounds of 148 participants."""
+    v0 = ci.ring_payload(5, 148, slots)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_XORSHIFT, 148, v0, 3001, variant=variant)
+    want, fc = expect_ring(oracle.WL_XORSHIFT, v0, 3001)
+    np.testing.assert_array_equal(got, want)
+    assert d.device_status == 0 and (st == cns.CNS_CTA_DONE).all()
 
 
 @pytest.mark.parametrize("offset", [0, 1024, 4096, 5120, 128])
@@ -708,3 +769,38 @@ def test_die_local_results_do_not_depend_on_placement(cns, offset, mode):
     assert rc == 0 and d.device_status == 0
     np.testing.assert_array_equal(from_dev_u32(b1).reshape(148, 4), np.roll(v0, -3001, axis=0))
     assert d.final_counter == 3001 * (148 if mode == SOFT else 148 // d.cluster_used)
+
+
+# --- the headline round with phase stamps (cns_probe_round_phases) -------------------------
+
+def test_round_phase_probe(cns):
+    """The stamped copy of the headline round computes the same ring as syncall_run; its stamps come in
+    phase order for every CTA and round, and the bench's budget adds up to the mean round."""
+    import torch
+    import bench
+    P, R, K = 148, 3001, 256
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P, 4)
+    b0 = to_dev_u32(v0)
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace()
+    st = torch.zeros(K * P * 8, dtype=torch.int64, device="cuda")
+    assert cns.cns_probe_round_phases(P, 256, R, K, b0, b1, ws, st) == 0
+    torch.cuda.synchronize()
+    want, fc = expect_ring(oracle.WL_RING_ROTATE, v0, R)
+    np.testing.assert_array_equal(from_dev_u32(b1).reshape(P, 4), want)
+    t = st.cpu().numpy().reshape(K, P, 8)
+    assert (np.diff(t, axis=2) >= 0).all()
+    assert (t[1:, :, 0] == t[:-1, :, 7]).all()     # a round starts where the last one closed
+    b = bench.round_budget(t)
+    parts = sum(b[k] for k in bench.PHASES)
+    assert abs(parts - b["round"]) < 1.0
+    assert abs(b["wait_for_last_arrival"] + b["wait_landing_and_detection"] - b["wait"]) < 1.0
+    assert 100.0 < b["round"] < 100000.0
+    # the same on a workspace without room for the payload copies (the caller's buffers every round)
+    ws8 = cns.new_workspace(mirror=False)
+    b0.copy_(to_dev_u32(v0))
+    assert cns.cns_probe_round_phases(P, 256, R, K, b0, b1, ws8, st) == 0
+    np.testing.assert_array_equal(from_dev_u32(b1).reshape(P, 4), want)
+    # bad arguments are refused before any launch
+    assert cns.cns_probe_round_phases(P, 256, 10, 20, b0, b1, ws, st) == cns.CNS_ERR_INVALID_VALUE
+    assert cns.cns_probe_round_phases(P, 256, R, 2000, b0, b1, ws, st) == cns.CNS_ERR_INVALID_VALUE
