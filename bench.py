@@ -461,25 +461,61 @@ def secondary(cns, torch, peaks):
              "CTA 0 being allowed to record to the consumer-side wait releasing), round trips/s over the whole "
              "run (events)")
 
-    # op-stream state machine, 1e6 ops: buffers allocated once, 20 back-to-back C-ABI calls timed
+    # op-stream state machine, 1e6 ops: buffers allocated once, 20 back-to-back C-ABI calls timed (warm L2),
+    # and calls with L2 flushed before each one (cold, each timed alone); then a stream without SET records
+    # (one dependent chain), against the chain of the rule itself on one thread (cns_probe_op_chain)
     n = 1_000_000
-    ops_d = torch.from_numpy(ci.notify_ops(n).view(np.int32)).cuda()
-    trace = torch.empty((n, 2), dtype=torch.int32, device="cuda")
-    final = torch.empty(1, dtype=torch.int32, device="cuda")
-    sb = cns.cns_statemachine_scratch_bytes(n)
-    scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
 
-    def sm_calls(k):
-        for _ in range(k):
-            cns.check(cns.cns_statemachine_run(ops_d, n, 0, trace, final, scratch, sb,
-                                               torch.cuda.current_stream()), "statemachine")
-    sm_calls(3)
+    def statemachine_figures(ops_np, label_reps=20):
+        ops_d = torch.from_numpy(ops_np.view(np.int32)).cuda()
+        m = ops_np.shape[0]
+        trace = torch.empty((m, 2), dtype=torch.int32, device="cuda")
+        final = torch.empty(1, dtype=torch.int32, device="cuda")
+        sb = cns.cns_statemachine_scratch_bytes(m)
+        scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
+
+        def calls(k):
+            for _ in range(k):
+                cns.check(cns.cns_statemachine_run(ops_d, m, 0, trace, final, scratch, sb,
+                                                   torch.cuda.current_stream()), "statemachine")
+        calls(3)
+        torch.cuda.synchronize()
+        warm, _ = timed_run(torch, lambda: calls(label_reps))
+        warm /= label_reps
+        cold = []
+        for _ in range(5):
+            flush.zero_()
+            ms_c, _ = timed_run(torch, lambda: calls(1))
+            cold.append(ms_c)
+        return warm, statistics.median(cold)
+
+    warm, cold = statemachine_figures(ci.notify_ops(n))
+    hbm_ops = peaks["hbm_gbs"] * 1e9 / 24 if peaks.get("hbm_gbs") else None
+    ops_sf = ci.notify_ops(n + n // 7, seed=ci.SEED_NOTIFY_OPS ^ 0x5E7F)
+    ops_sf = ops_sf[~((ops_sf[:, 0] == 0) & (ops_sf[:, 1] == 0))][:n]     # no SET record anywhere
+    warm_sf, cold_sf = statemachine_figures(np.ascontiguousarray(ops_sf), label_reps=3)
+    chain_ops = torch.from_numpy(np.ascontiguousarray(ops_sf[:16]).view(np.int32)).cuda()
+    chain_out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    iters = 20000
+    cns.check(cns.cns_probe_op_chain(chain_ops, iters, chain_out), "op chain")
     torch.cuda.synchronize()
-    ms, _ = timed_run(torch, lambda: sm_calls(20))
-    ms /= 20
-    out["notify_statemachine_1e6"] = {"ms": round(ms, 4), "ops_per_s": round(n / (ms * 1e-3), 0),
-                                      "bytes_per_op": 24,
-                                      "gbs_algorithmic": round(24 * n / (ms * 1e-3) / 1e9, 1)}
+    chain_ns = chain_out[0].item() / (16 * iters)
+    sf_ns = warm_sf * 1e6 / ops_sf.shape[0]
+    out["notify_statemachine_1e6"] = {
+        "ms": round(warm, 4), "ops_per_s": round(n / (warm * 1e-3), 0), "bytes_per_op": 24,
+        "gbs_algorithmic": round(24 * n / (warm * 1e-3) / 1e9, 1),
+        "cold_l2_ms": round(cold, 4), "cold_l2_ops_per_s": round(n / (cold * 1e-3), 0),
+        "cold_l2_frac_of_measured_hbm": round(24 * n / (cold * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+        if peaks.get("hbm_gbs") else None,
+        "bound_note": "24 B per op (16 in, 8 out) against the measured HBM copy peak; the ops are cut at SET "
+                      "records, so the walks run in parallel",
+        "set_free": {"ops": int(ops_sf.shape[0]), "ms": round(warm_sf, 3), "cold_l2_ms": round(cold_sf, 3),
+                     "ns_per_op": round(sf_ns, 3),
+                     "chain_bound_ns_per_op": round(chain_ns, 3),
+                     "frac_of_chain_bound": round(chain_ns / sf_ns, 4),
+                     "note": "no SET record: the whole stream is one dependent chain; the bound is one thread "
+                             "applying the same rule to ops held in registers (cns_probe_op_chain)"}}
 
     # the same ring-rotate rounds separated by the CUDA runtime's cooperative-groups grid barrier
     v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P_HEAD, SLOTS_HEAD)
@@ -497,7 +533,13 @@ def secondary(cns, torch, peaks):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     word = torch.zeros(1, dtype=torch.int32, device="cuda")
     ms, _ = timed_run(torch, lambda: cns.cns_probe_same_address_throughput(sms, 256, 64, word))
-    out["same_address_red_ops_per_s"] = round(sms * 256 * 64 / (ms * 1e-3), 0)
+    red = sms * 256 * 64 / (ms * 1e-3)
+    out["same_address_red_ops_per_s"] = round(red, 0)
+    pipe = out["notify_pipeline_4096x1000"]
+    for form in (pipe, pipe["in_kernel_wait"], pipe["one_area"], pipe["one_area_in_kernel_wait"]):
+        # the lanes of one warp instruction reach the count's line as one L2 operation, so records can
+        # outnumber the L2's same-address operations
+        form["records_frac_of_same_address_red"] = round(form["records_per_s"] / red, 4)
     return out
 
 

@@ -131,6 +131,7 @@ _SIGS = {
     "cns_probe_atomic_rtt": (c_int, [c_int, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "cns_probe_same_address_throughput": (c_int, [c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "cns_probe_grid_sync": (c_int, [c_int32, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
+    "cns_probe_op_chain": (c_int, [c_void_p, c_int32, c_void_p, c_void_p]),
     "cns_probe_round_phases": (c_int, [c_int32, c_int32, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_size_t,
                                        c_void_p, c_void_p]),
     "cns_version": (c_int, [POINTER(c_int32), POINTER(c_int32)]),
@@ -294,6 +295,10 @@ def cns_probe_same_address_throughput(grid: int, threads: int, iters: int, word,
 
 def cns_probe_grid_sync(ctas: int, threads: int, rounds: int, buf0, buf1, stream=None) -> int:
     return lib().cns_probe_grid_sync(ctas, threads, rounds, ptr(buf0), ptr(buf1), stream_handle(stream))
+
+
+def cns_probe_op_chain(ops, iters: int, out, stream=None) -> int:
+    return lib().cns_probe_op_chain(ptr(ops), iters, ptr(out), stream_handle(stream))
 
 
 def cns_probe_round_phases(ctas: int, threads: int, rounds: int, stamp_rounds: int, buf0, buf1, workspace, stamps,

@@ -225,21 +225,23 @@ constexpr int kChunk = 16;
 
 // An op turned into a micro-op that one short branch-free sequence applies
 // (neighbouring lanes of a warp apply different kinds and modes):
-//   x  AND mask a (record) / compare mask (wait: the value for
-//      EQUAL_WITH_BITMASK, all ones otherwise)
-//   y  OR value o (record) / compare value (wait)
-//   z  addend d (record) / 0 (wait)
-//   w  flags: bits 0-2 the compare results that release a wait (1 below,
-//      2 equal, 4 above), bits 4-6 the same when the wait also clears, bit 8
-//      wait, bits 9-10 the outcome of anything else (CNS_OUT_RECORD or
-//      CNS_OUT_INVALID), bit 11 SET.
-// A record makes the count ((c & a) | o) + d: SET v is (0, v, 0), ADD v
-// (~0, 0, v), OR v (~0, v, 0), AND v (v, 0, 0).  A wait compares (c & mask)
-// with its value: LESS releases below, EQUAL and EQUAL_WITH_BITMASK on equal,
-// BIGGER above, BIGGER_OR_EQUAL on equal or above.  An op of no valid kind
-// and mode is the record (~0, 0, 0) with outcome CNS_OUT_INVALID.
+//   record  x = AND mask a, y = OR value o, z = addend d: the count becomes
+//           ((c & a) | o) + d.  SET v is (0, v, 0), ADD v (~0, 0, v), OR v
+//           (~0, v, 0), AND v (v, 0, 0).
+//   wait    x = compare mask, y = lo, z = span: released when
+//           (c & mask) - lo <= span, unsigned -- every wait mode is a range of
+//           (c & mask): LESS v is [0, v - 1], EQUAL v [v, v], BIGGER v
+//           [v + 1, 2^32 - 1], BIGGER_OR_EQUAL v [v, 2^32 - 1], and
+//           EQUAL_WITH_BITMASK v is c & v in [v, v].  An empty range (LESS 0,
+//           BIGGER 2^32 - 1) is mask 0, lo 1, span 0: 0 - 1 is never <= 0.
+//   w       flags: bit 8 wait, bit 12 the wait clears once released, bits
+//           9-10 the outcome of anything else (CNS_OUT_RECORD or
+//           CNS_OUT_INVALID), bit 11 SET.
+// An op of no valid kind and mode is the record (~0, 0, 0) with outcome
+// CNS_OUT_INVALID.
 constexpr uint32_t kMicroWait = 1u << 8;
 constexpr uint32_t kMicroSet = 1u << 11;
+constexpr uint32_t kMicroClear = 1u << 12;
 
 // Built with selects, not branches: the lanes of a warp stage ops of every
 // kind and mode at once.
@@ -252,28 +254,36 @@ __device__ __forceinline__ uint4 sm_micro(const uint4 &op)
     const uint32_t a = mode == CNS_REC_SET ? 0u : (mode == CNS_REC_BIT_AND ? v : ~0u);
     const uint32_t o = (mode == CNS_REC_SET || mode == CNS_REC_BIT_OR) ? v : 0u;
     const uint32_t d = mode == CNS_REC_ADD ? v : 0u;
-    // wait: the compare results that release it, 4 bits per mode (LESS 1, EQUAL 2, BIGGER 4,
-    // BIGGER_OR_EQUAL 6, EQUAL_WITH_BITMASK 2)
-    const uint32_t bits = (0x26421u >> (4u * (mode & 7u))) & 0xFu;
-    const uint32_t wflags = bits | (op.w != 0u ? bits << 4 : 0u) | kMicroWait;
+    // wait: the range of (c & mask) that releases it
+    const bool never = (mode == CNS_WAIT_LESS && v == 0u) || (mode == CNS_WAIT_BIGGER && v == ~0u);
+    const uint32_t mask = never ? 0u : (mode == CNS_WAIT_EQUAL_WITH_BITMASK ? v : ~0u);
+    const uint32_t lo = never ? 1u
+                        : mode == CNS_WAIT_LESS ? 0u
+                        : mode == CNS_WAIT_BIGGER ? v + 1u
+                                                  : v;   // EQUAL, BIGGER_OR_EQUAL, EQUAL_WITH_BITMASK
+    const uint32_t span = never ? 0u
+                          : mode == CNS_WAIT_LESS ? v - 1u
+                          : (mode == CNS_WAIT_BIGGER || mode == CNS_WAIT_BIGGER_OR_EQUAL) ? ~0u - lo
+                                                                                          : 0u;
+    const uint32_t wflags = kMicroWait | (op.w != 0u ? kMicroClear : 0u);
     const uint32_t rflags = (static_cast<uint32_t>(CNS_OUT_RECORD) << 9) | (mode == CNS_REC_SET ? kMicroSet : 0u);
-    const uint32_t mask = mode == CNS_WAIT_EQUAL_WITH_BITMASK ? v : ~0u;
-    return make_uint4(rec ? a : (wait ? mask : ~0u), rec ? o : (wait ? v : 0u), rec ? d : 0u,
+    return make_uint4(rec ? a : (wait ? mask : ~0u), rec ? o : (wait ? lo : 0u), rec ? d : (wait ? span : 0u),
                       rec ? rflags : (wait ? wflags : static_cast<uint32_t>(CNS_OUT_INVALID) << 9));
 }
 
 // One micro-op applied to count c; *outcome gets the op's CNS_OUT_* code.
-// Only the compare, the two flag tests and the final select lie on the chain
-// from one count to the next.
+// The chain from one count to the next is four dependent instructions: the
+// AND, the subtraction, the range compare (with the clear flag folded in)
+// and the final select; the record's update and the outcome are computed
+// beside it.
 __device__ __forceinline__ uint32_t sm_apply_micro(uint32_t c, const uint4 m, uint32_t *outcome)
 {
+    const bool wait = (m.w & kMicroWait) != 0u;
     const uint32_t x = c & m.x;
-    const uint32_t bit = x < m.y ? 1u : (x == m.y ? 2u : 4u);   // the compare result, as the flag it tests
-    const bool rel = (m.w & bit) != 0u;          // a record's bits 0-6 are 0: never released nor cleared
-    const bool clr = (m.w & (bit << 4)) != 0u;
-    const uint32_t keep = (m.w & kMicroWait) ? c : (x | m.y) + m.z;
-    *outcome = rel ? 1u : ((m.w >> 9) & 3u);    // a wait: RELEASED (1) or HELD (0)
-    return clr ? 0u : keep;
+    const bool in_range = x - m.y <= m.z;                         // a wait's release test
+    const uint32_t keep = wait ? c : (x | m.y) + m.z;              // a record's update, or the count as it is
+    *outcome = wait ? (in_range ? 1u : 0u) : ((m.w >> 9) & 3u);   // a wait: RELEASED (1) or HELD (0)
+    return (in_range && (m.w & kMicroClear) != 0u) ? 0u : keep;
 }
 
 constexpr uint64_t kSmLinkTimeoutNs = 10ull * 1000000000ull;
@@ -531,6 +541,32 @@ static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, u
 }
 
 __global__ void write_word_kernel(uint32_t *w, uint32_t v) { *w = v; }
+
+// The dependent chain of the state machine's rule on its own: one thread
+// applies 16 micro-ops held in registers, over and over, with the walks' own
+// sm_apply_micro (a stream without SETs is one such chain).
+__global__ void sm_chain_probe_kernel(const uint4 *ops, int32_t iters, uint64_t *out)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0)
+        return;
+    uint4 m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        m[i] = sm_micro(ops[i]);
+    uint32_t c = 0u, acc = 0u;
+    const uint64_t t0 = globaltimer_ns();
+    for (int32_t it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            uint32_t o;
+            c = sm_apply_micro(c, m[i], &o);
+            acc += o;
+        }
+    }
+    const uint64_t t1 = globaltimer_ns();
+    out[0] = t1 - t0;
+    out[1] = (static_cast<uint64_t>(acc) << 32) | c;
+}
 
 // ---------------------------------------------------------------------------
 // Two-stream pipeline kernels
@@ -1322,4 +1358,18 @@ extern "C" int cns_pipeline_run(cns_pipeline_t *cfg)
         return e;
     cfg->device_status = (st_done || st_ack) ? CNS_ERR_TIMEOUT : 0;
     return rc != CNS_SUCCESS ? rc : (cfg->device_status ? CNS_ERR_TIMEOUT : CNS_SUCCESS);
+}
+
+extern "C" int cns_probe_op_chain(const uint32_t *ops_dev, int32_t iters, uint64_t *out_dev, cns_stream_t stream)
+{
+    if (!ops_dev || !out_dev)
+        return CNS_ERR_NULL_PTR;
+    if (iters < 1 || (reinterpret_cast<uintptr_t>(ops_dev) & 15) || (reinterpret_cast<uintptr_t>(out_dev) & 7))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    sm_chain_probe_kernel<<<1, 32, 0, to_stream(stream)>>>(reinterpret_cast<const uint4 *>(ops_dev), iters, out_dev);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
 }

@@ -646,6 +646,19 @@ int cns_probe_grid_sync(int32_t ctas, int32_t threads, int64_t rounds, void *buf
                         cns_stream_t stream);
 
 /*
+ * cns_probe_op_chain -- the op-stream state machine's rule as one dependent
+ * chain: one thread applies the 16 ops at ops_dev (four uint32 each, as in
+ * cns_statemachine_run) to a count, in order, iters times over, and times it
+ * with the global timer.  A stream without SET records is one such chain, so
+ * out_dev[0] / (16 * iters) is the time per op that bounds it.
+ *   ops_dev  [16][4] uint32, 16-byte aligned
+ *   out_dev  uint64[2]: total nanoseconds; the final count and the sum of the
+ *            outcomes (which keep the chain live)
+ * Errors: NULL_PTR, INVALID_VALUE, CUDA.
+ */
+int cns_probe_op_chain(const uint32_t *ops_dev, int32_t iters, uint64_t *out_dev, cns_stream_t stream);
+
+/*
  * cns_probe_round_phases -- where the time of one round of the headline goes:
  * the soft SYNCALL round on die-local counter copies (CNS_BARRIER_DIE_LOCAL)
  * with the ring-rotate payload of one uint4 per CTA ([SYNCALL] §5.2: arrive,

@@ -533,3 +533,20 @@ def test_pipeline_without_released_array(cns, areas, consumer_wait):
     finally:
         cns.cntnotify_destroy(done)
         cns.cntnotify_destroy(ack)
+
+
+def test_op_chain_probe_applies_the_rule(cns):
+    """cns_probe_op_chain applies its 16 ops iters times over to a count that starts at 0: the final count
+    and the sum of the outcomes are the oracle's for the same ops repeated."""
+    import torch
+    ops = ci.notify_ops(16, seed=99)
+    ops_d = torch.from_numpy(ops.view(np.int32).copy()).cuda()
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    assert cns.cns_probe_op_chain(ops_d, 3, out) == 0
+    torch.cuda.synchronize()
+    ns, packed = (int(v) for v in out.cpu().numpy().view(np.uint64))
+    trace, fin = oracle.cnt_statemachine(np.tile(ops, (3, 1)), 0)
+    assert packed & 0xFFFFFFFF == fin
+    assert packed >> 32 == int(trace[:, 1].astype(np.uint64).sum())
+    assert ns > 0
+    assert cns.cns_probe_op_chain(ops_d, 0, out) == cns.CNS_ERR_INVALID_VALUE
