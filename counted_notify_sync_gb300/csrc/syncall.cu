@@ -338,24 +338,38 @@ constexpr uint32_t kMirrorPairWords = 2048;        // 8 KB: two 4 KB blocks
 constexpr uint32_t kMirrorBlockRows = 256;         // uint4 rows per 4 KB block
 constexpr uint32_t kMirrorTimingRow = kMirrorBlockRows - 1;   // never a payload row (P <= 255)
 
+// A participant's rows in the copies, worked out once: the row it reads in
+// each pair (its neighbour's, in the block on its own die) and the rows it
+// writes (its own, in both blocks).  Held as separate pointers and picked by
+// the round's parity with selects: an array indexed by the parity would sit
+// in local memory, and every round's payload load would first wait for a
+// local load of its address (measured: ~90 ns a round).
 struct MirrorState {
-    const uint4 *near_src[2];   // the block of pair k on this SM's die
-    uint4 *blk[2][2];           // pair k, block c
+    const uint4 *src0, *src1;   // pair 0 / pair 1: the neighbour's row, near block
+    uint4 *dst00, *dst01;       // pair 0: own row in block 0 / block 1
+    uint4 *dst10, *dst11;       // pair 1: own row in block 0 / block 1
 };
 
-__device__ __forceinline__ MirrorState mirror_setup(uint32_t *mirror)
+__device__ __forceinline__ MirrorState mirror_setup(uint32_t *mirror, uint32_t b, uint32_t q)
 {
-    MirrorState m;
+    uint4 *blk[2][2];
+    bool far0[2];
     for (int k = 0; k < 2; ++k) {
         uint4 *b0 = reinterpret_cast<uint4 *>(mirror + k * kMirrorPairWords);
         uint4 *b1 = b0 + kMirrorBlockRows;
-        m.blk[k][0] = b0;
-        m.blk[k][1] = b1;
+        blk[k][0] = b0;
+        blk[k][1] = b1;
         // time both blocks on their timing row (adds of 0: nothing changes)
-        const bool far0 = copy_is_farther(reinterpret_cast<uint32_t *>(b0 + kMirrorTimingRow),
-                                          reinterpret_cast<uint32_t *>(b1 + kMirrorTimingRow));
-        m.near_src[k] = far0 ? b1 : b0;
+        far0[k] = copy_is_farther(reinterpret_cast<uint32_t *>(b0 + kMirrorTimingRow),
+                                  reinterpret_cast<uint32_t *>(b1 + kMirrorTimingRow));
     }
+    MirrorState m;
+    m.src0 = (far0[0] ? blk[0][1] : blk[0][0]) + q;
+    m.src1 = (far0[1] ? blk[1][1] : blk[1][0]) + q;
+    m.dst00 = blk[0][0] + b;
+    m.dst01 = blk[0][1] + b;
+    m.dst10 = blk[1][0] + b;
+    m.dst11 = blk[1][1] + b;
     return m;
 }
 
@@ -363,17 +377,17 @@ template <int WL>
 __device__ __forceinline__ void mirror_round(const SyncallParams &p, const MirrorState &m, uint32_t b, int64_t r)
 {
     const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
-    const int src = static_cast<int>(r & 1), dst = src ^ 1;
-    uint4 v = ld_relaxed_gpu_v4((r == 0 ? static_cast<const uint4 *>(p.buf0) : m.near_src[src]) + q);
+    const bool odd = (r & 1) != 0;   // reads pair r & 1, writes the other
+    uint4 v = ld_relaxed_gpu_v4(r == 0 ? static_cast<const uint4 *>(p.buf0) + q : (odd ? m.src1 : m.src0));
     const uint32_t rr = static_cast<uint32_t>(r);
     v.x = ring_op<WL>(v.x, rr);
     v.y = ring_op<WL>(v.y, rr);
     v.z = ring_op<WL>(v.z, rr);
     v.w = ring_op<WL>(v.w, rr);
-    st_relaxed_gpu_v4(m.blk[dst][0] + b, v);
-    st_relaxed_gpu_v4(m.blk[dst][1] + b, v);
+    st_relaxed_gpu_v4(odd ? m.dst00 : m.dst10, v);
+    st_relaxed_gpu_v4(odd ? m.dst01 : m.dst11, v);
     if (r + 2 >= p.rounds)
-        st_relaxed_gpu_v4(static_cast<uint4 *>(dst ? p.buf1 : p.buf0) + b, v);
+        st_relaxed_gpu_v4(static_cast<uint4 *>(odd ? p.buf0 : p.buf1) + b, v);
 }
 
 // The soft rounds when thread 0 alone touches memory (no payload, or a row of
@@ -397,7 +411,7 @@ __device__ __forceinline__ void solo_rounds(const SyncallParams &p, uint32_t b, 
     MirrorState m{};
     const bool mirrored = (V == kBvDieLocal) && p.mirror != nullptr;
     if (mirrored)
-        m = mirror_setup(p.mirror);
+        m = mirror_setup(p.mirror, b, (b + 1u == p.P) ? 0u : b + 1u);
     EpochCursor cursor{0u, 0u, false};
     bool stop = false;
     for (int64_t r = 0; r < p.rounds; ++r) {
@@ -419,6 +433,27 @@ __device__ __forceinline__ void solo_rounds(const SyncallParams &p, uint32_t b, 
         record_base<V>(p, bar, base_word, base);
     if (p.cta_status)
         p.cta_status[b] = static_cast<int32_t>((stop ? CNS_CTA_ABORTED : CNS_CTA_DONE) | (role << 8));
+}
+
+// The same solo rounds in a kernel of their own, for CTAs of up to 256
+// threads.  Within syncall_kernel they are held to the 64 registers a thread
+// that its 1024-thread bound allows, and the headline round spilled there;
+// here thread 0 has the registers it needs.  Same rounds, same memory
+// operations.
+template <int WL, int V>
+__global__ void __launch_bounds__(256) syncall_solo_kernel(const SyncallParams p)
+{
+    if (threadIdx.x != 0)
+        return;
+    const uint32_t b = blockIdx.x;
+    const uint32_t role = cta_role(p, b);
+    if (b >= p.P) {
+        // not a participant: never touches the counter ([SYNCALL] §4.2, §7.2)
+        if (p.cta_status)
+            p.cta_status[b] = static_cast<int32_t>(CNS_CTA_IDLE | (role << 8));
+        return;
+    }
+    solo_rounds<WL, V>(p, b, role);
 }
 
 template <int MODE, int WL, int V>
@@ -585,29 +620,29 @@ __global__ void __launch_bounds__(1024) round_phase_probe_kernel(const SyncallPa
     const uint32_t b = blockIdx.x;
     Barrier bar = p.bar;
     choose_near_copy(bar);
+    const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
     MirrorState m{};
     if (p.mirror)
-        m = mirror_setup(p.mirror);
+        m = mirror_setup(p.mirror, b, q);
     EpochCursor cursor{0u, 0u, false};
     const int64_t first = p.rounds - stamp_rounds;
-    const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
     uint64_t t[kPhaseStamps];
     t[7] = globaltimer_ns();
     bool stop = false;
     for (int64_t r = 0; r < p.rounds && !stop; ++r) {
-        const int src = static_cast<int>(r & 1), dst = src ^ 1;
+        const bool odd = (r & 1) != 0;
         t[0] = t[7];
-        const uint4 *from = p.mirror ? (r == 0 ? static_cast<const uint4 *>(p.buf0) : m.near_src[src])
-                                     : static_cast<const uint4 *>(src ? p.buf1 : p.buf0);
-        const uint4 v = ld_relaxed_gpu_v4(from + q);   // ring rotate: the row as it is
+        const uint4 *from = p.mirror ? (r == 0 ? static_cast<const uint4 *>(p.buf0) + q : (odd ? m.src1 : m.src0))
+                                     : static_cast<const uint4 *>(odd ? p.buf1 : p.buf0) + q;
+        const uint4 v = ld_relaxed_gpu_v4(from);   // ring rotate: the row as it is
         t[1] = globaltimer_after(v.x ^ v.w);
         if (p.mirror) {
-            st_relaxed_gpu_v4(m.blk[dst][0] + b, v);
-            st_relaxed_gpu_v4(m.blk[dst][1] + b, v);
+            st_relaxed_gpu_v4(odd ? m.dst00 : m.dst10, v);
+            st_relaxed_gpu_v4(odd ? m.dst01 : m.dst11, v);
             if (r + 2 >= p.rounds)
-                st_relaxed_gpu_v4(static_cast<uint4 *>(dst ? p.buf1 : p.buf0) + b, v);
+                st_relaxed_gpu_v4(static_cast<uint4 *>(odd ? p.buf0 : p.buf1) + b, v);
         } else {
-            st_relaxed_gpu_v4(static_cast<uint4 *>(dst ? p.buf1 : p.buf0) + b, v);
+            st_relaxed_gpu_v4(static_cast<uint4 *>(odd ? p.buf0 : p.buf1) + b, v);
         }
         t[2] = globaltimer_ns();
         fence_release_gpu();
@@ -687,6 +722,26 @@ template <int MODE, int... WLs>
 static constexpr std::array<std::array<KernelFn, kBvCount>, sizeof...(WLs)> table_of(std::integer_sequence<int, WLs...>)
 {
     return {{variants_of<MODE, WLs>(std::make_integer_sequence<int, kBvCount>{})...}};
+}
+
+template <int WL, int... Vs>
+static constexpr std::array<KernelFn, sizeof...(Vs)> solo_variants_of(std::integer_sequence<int, Vs...>)
+{
+    return {{syncall_solo_kernel<WL, Vs>...}};
+}
+
+template <int... WLs>
+static constexpr std::array<std::array<KernelFn, kBvCount>, sizeof...(WLs)> solo_table_of(std::integer_sequence<int, WLs...>)
+{
+    return {{solo_variants_of<WLs>(std::make_integer_sequence<int, kBvCount>{})...}};
+}
+
+// The solo kernel of a soft run whose rounds thread 0 alone performs (the
+// empty workload and the rings: wl < CNS_WL_JACOBI).
+static KernelFn pick_solo_kernel(int wl, int variant)
+{
+    static constexpr auto solo = solo_table_of(std::make_integer_sequence<int, CNS_WL_JACOBI>{});
+    return solo[wl][variant];
 }
 
 static KernelFn pick_kernel(int mode, int wl, int variant)
@@ -861,8 +916,23 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     cudaStream_t s = to_stream(d->stream);
     KernelFn k = pick_kernel(mode, d->workload, d->barrier_variant);
     const size_t smem = d->workload == CNS_WL_JACOBI ? kJacSmemBytes : 0;
+    // thread 0 alone touches memory: no payload, or rows of one uint4 or one word
+    const bool ring = d->workload == CNS_WL_RING_AFFINE || d->workload == CNS_WL_RING_ROTATE ||
+                      d->workload == CNS_WL_XORSHIFT;
+    const bool solo = mode == CNS_SYNCALL_SOFT &&
+                      (d->workload == CNS_WL_EMPTY || (ring && (d->elems == 4 || d->elems <= 1)));
     bool ok = false;
-    if (mode == CNS_SYNCALL_HARD && C == 0) {
+    if (solo && threads <= 256) {
+        // the solo kernel when its grid can be resident, else syncall_kernel's own solo branch
+        KernelFn ks = pick_solo_kernel(d->workload, d->barrier_variant);
+        if (int rc = fits(ks, grid, threads, 0, 0, s, dev, &ok))
+            return rc;
+        if (ok)
+            k = ks;
+    }
+    if (ok) {
+        // the solo kernel fits
+    } else if (mode == CNS_SYNCALL_HARD && C == 0) {
         // clusters of 2 first: measured 1634-1663 ns/round on the 148-CTA ring
         // against 1786-1819 for clusters of 4 (a cluster barrier waits for its
         // slowest member's payload) and 1616-1648 for clusters of 1, which
@@ -900,11 +970,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     prm.P = P;
     prm.group = static_cast<uint32_t>(group);
     prm.core_type = core_type;
-    // thread 0 alone touches memory: no payload, or rows of one uint4 or one word
-    const bool ring = d->workload == CNS_WL_RING_AFFINE || d->workload == CNS_WL_RING_ROTATE ||
-                      d->workload == CNS_WL_XORSHIFT;
-    prm.solo = (mode == CNS_SYNCALL_SOFT &&
-                (d->workload == CNS_WL_EMPTY || (ring && (d->elems == 4 || d->elems <= 1)))) ? 1 : 0;
+    prm.solo = solo ? 1 : 0;
     // the per-die payload copies: die-local variant, one-uint4 rows, P <= 255, room in the workspace
     prm.mirror = (prm.solo && ring && d->elems == 4 && d->barrier_variant == CNS_BARRIER_DIE_LOCAL &&
                   P <= CNS_SYNCALL_MIRROR_MAX_P && d->workspace_bytes >= CNS_SYNCALL_WORKSPACE_MIRROR_BYTES)
