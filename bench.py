@@ -529,6 +529,25 @@ def secondary(cns, torch, peaks):
                         np.roll(v0, -(3 * 100000) % P_HEAD, axis=0))
     out["cg_grid_sync_148_ring_rotate"] = {"ns_per_round": round(min(runs) * 1e6 / 100000, 2), "correct": bool(ok)}
 
+    # the device-side hand-off of a counted notify (record -> wait) between two CTAs, at gpu scope and at
+    # the system scope of a notify prepared for other GPUs (cntnotify_enable_peer)
+    lines = torch.zeros(64, dtype=torch.int32, device="cuda")
+    po = torch.zeros(4, dtype=torch.int64, device="cuda")
+    hand = {}
+    for scope, name in ((0, "gpu_scope"), (1, "system_scope")):
+        best = None
+        for _ in range(3):
+            cns.check(cns.cns_probe_notify_pingpong(scope, 20000, lines, po), "notify ping-pong")
+            torch.cuda.synchronize()
+            o = po.cpu().numpy()
+            if o[1] == 0:
+                best = o[0] if best is None else min(best, o[0])
+        hand[name + "_ns_per_handoff"] = round(float(best) / (2 * 20000), 1) if best is not None else None
+    hand["sms"] = [int(po[2].item()), int(po[3].item())]
+    hand["note"] = ("two co-resident CTAs pass a signal back and forth with the library's record (ADD 1, release) "
+                    "and wait (relaxed polls, acquire fence) rules; one hand-off = one record seen by one wait")
+    out["notify_handoff"] = hand
+
     # same-address reduction throughput (all SMs)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     word = torch.zeros(1, dtype=torch.int32, device="cuda")

@@ -26,6 +26,7 @@ CNS_ERR_TIMEOUT = 5
 CNS_ERR_NOT_RESIDENT = 6
 CNS_ERR_CUDA = 7
 CNS_ERR_ARCH = 8
+CNS_ERR_NO_PEER_ACCESS = 9
 
 CNS_SYNCALL_HARD = 0
 CNS_SYNCALL_SOFT = 1
@@ -124,6 +125,7 @@ _SIGS = {
     "cntnotify_destroy": (c_int, [c_void_p]),
     "cntnotify_get_device_ptr": (c_int, [c_void_p, POINTER(c_void_p)]),
     "cntnotify_query_status": (c_int, [c_void_p, POINTER(c_int32), POINTER(c_uint32)]),
+    "cntnotify_enable_peer": (c_int, [c_void_p, c_int]),
     "cns_statemachine_scratch_bytes": (c_size_t, [c_int64]),
     "cns_statemachine_run": (c_int, [c_void_p, c_int64, c_uint32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "cns_statemachine_run_noalloc": (c_int, [c_void_p, c_int64, c_uint32, c_void_p, c_void_p, c_void_p]),
@@ -132,6 +134,7 @@ _SIGS = {
     "cns_probe_same_address_throughput": (c_int, [c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "cns_probe_grid_sync": (c_int, [c_int32, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
     "cns_probe_op_chain": (c_int, [c_void_p, c_int32, c_void_p, c_void_p]),
+    "cns_probe_notify_pingpong": (c_int, [c_int, c_int32, c_void_p, c_void_p, c_void_p]),
     "cns_probe_round_phases": (c_int, [c_int32, c_int32, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_size_t,
                                        c_void_p, c_void_p]),
     "cns_version": (c_int, [POINTER(c_int32), POINTER(c_int32)]),
@@ -263,6 +266,14 @@ def cntnotify_query_status(h):
     st, c = c_int32(0), c_uint32(0)
     rc = lib().cntnotify_query_status(h, ctypes.byref(st), ctypes.byref(c))
     return rc, st.value, c.value
+
+
+def cntnotify_enable_peer(h, peer_device: int) -> int:
+    return lib().cntnotify_enable_peer(h, peer_device)
+
+
+def cns_probe_notify_pingpong(scope: int, iters: int, lines, out, stream=None) -> int:
+    return lib().cns_probe_notify_pingpong(scope, iters, ptr(lines), ptr(out), stream_handle(stream))
 
 
 def cns_statemachine_scratch_bytes(n: int) -> int:

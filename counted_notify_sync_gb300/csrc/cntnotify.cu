@@ -29,6 +29,11 @@ struct cns_cnt_notify_s {
     int device;
     uint32_t slot;
     uint32_t *line;   // device: [0] count, [1] sticky status, [2] abort word
+    // cntnotify_enable_peer: the devices (bit d) whose streams may record on
+    // and wait on this notify besides its own, and whether its stream-ordered
+    // operations run at system scope (set by the first enable)
+    std::atomic<uint64_t> peers{0};
+    std::atomic<int> sys{0};
 };
 
 namespace cns {
@@ -96,14 +101,36 @@ struct DeviceGuard {
     }
 };
 
+// The device a stream-ordered operation on notify n runs on: the stream's own
+// device.  A NULL stream (and the special handles cudaStreamLegacy and
+// cudaStreamPerThread) means the default stream of the notify's device.  A
+// device other than the notify's must have been given access by
+// cntnotify_enable_peer.
+static int launch_device(const cns_cnt_notify_s *n, cudaStream_t s, int *dev)
+{
+    if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) {
+        *dev = n->device;
+        return CNS_SUCCESS;
+    }
+    int d = -1;
+    const cudaError_t e = cudaStreamGetDevice(s, &d);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaStreamGetDevice");
+    if (d != n->device && (d < 0 || d >= 64 || ((n->peers.load(std::memory_order_acquire) >> d) & 1u) == 0))
+        return CNS_ERR_NO_PEER_ACCESS;
+    *dev = d;
+    return CNS_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // Record / wait kernels
 // ---------------------------------------------------------------------------
 
+template <int S>
 __global__ void cnt_record_kernel(uint32_t *count, uint32_t mode, uint32_t v)
 {
     if (threadIdx.x == 0)
-        cnt_record_device(count, mode, v);
+        cnt_record_scoped<S>(count, mode, v);
 }
 
 // One thread polls the count until the predicate holds; then the optional
@@ -118,39 +145,42 @@ __global__ void cnt_record_kernel(uint32_t *count, uint32_t mode, uint32_t v)
 // previous consumer): before it ends, the kernel waits on the device for
 // that consumer to complete, so the kernels of the stream still complete in
 // stream order.
-template <bool kEarlyNext, bool kAfterPrev>
+// S: kScopeGpu, or kScopeSys for a notify that other GPUs record on or wait
+// on (cntnotify_enable_peer); then the line may also be another GPU's,
+// reached through a peer mapping.
+template <bool kEarlyNext, bool kAfterPrev, int S = kScopeGpu>
 __global__ void cnt_wait_kernel(uint32_t *line, uint32_t mode, uint32_t v, uint32_t clear, uint64_t timeout_ns,
                                 uint32_t *observed, uint32_t *abort, uint64_t *released_at)
 {
     if (kEarlyNext)
         grid_launch_dependents();
-    if (threadIdx.x == 0 && !(abort && ld_relaxed_gpu(abort) != 0u)) {
+    if (threadIdx.x == 0 && !(abort && ld_relaxed_scoped<S>(abort) != 0u)) {
         uint32_t spins = 0;
         uint64_t deadline = 0;
         for (;;) {
             // relaxed polls; the fence after the one that releases makes it an
             // acquire of the records it read from (they are release operations)
-            const uint32_t c = ld_relaxed_gpu(line);
+            const uint32_t c = ld_relaxed_scoped<S>(line);
             if (cnt_wait_released(c, mode, v)) {
-                fence_acquire_gpu();
+                fence_acquire_scoped<S>();
                 if (released_at)
                     *released_at = globaltimer_ns();
                 if (observed)
                     *observed = c;
                 if (clear)
-                    atom_exch_relaxed_gpu(line, 0u);   // the clear comes after the release
+                    atom_exch_relaxed_scoped<S>(line, 0u);   // the clear comes after the release
                 break;
             }
             if ((++spins & 63u) == 0u) {
-                if (abort && ld_relaxed_gpu(abort) != 0u)
+                if (abort && ld_relaxed_scoped<S>(abort) != 0u)
                     break;
                 const uint64_t now = globaltimer_ns();
                 if (deadline == 0)
                     deadline = now + timeout_ns;
                 else if (now > deadline) {
-                    atom_exch_relaxed_gpu(line + 1, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
+                    atom_exch_relaxed_scoped<S>(line + 1, static_cast<uint32_t>(CNS_ERR_TIMEOUT));
                     if (abort)
-                        atom_exch_relaxed_gpu(abort, 1u);
+                        atom_exch_relaxed_scoped<S>(abort, 1u);
                     break;
                 }
             }
@@ -184,7 +214,9 @@ static bool record_mode_ok(int32_t m)
 static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info_t *info, uint32_t *observed,
                         uint32_t *abort = nullptr, bool early_next = false, uint64_t *released_at = nullptr)
 {
-    auto k = early_next ? cnt_wait_kernel<true, false> : cnt_wait_kernel<false, false>;
+    const bool sys = n->sys.load(std::memory_order_acquire) != 0;
+    auto k = sys ? (early_next ? cnt_wait_kernel<true, false, kScopeSys> : cnt_wait_kernel<false, false, kScopeSys>)
+                 : (early_next ? cnt_wait_kernel<true, false> : cnt_wait_kernel<false, false>);
     k<<<1, 32, 0, s>>>(n->line, static_cast<uint32_t>(info->mode), info->value, info->is_clear ? 1u : 0u,
                        wait_timeout_ns(info->timeout), observed, abort, released_at);
     CNS_CUDA(cudaGetLastError());
@@ -809,7 +841,10 @@ using namespace cns;
 static int preload_notify_kernels()
 {
     const void *kernels[] = {
-        reinterpret_cast<const void *>(cnt_record_kernel),
+        reinterpret_cast<const void *>(cnt_record_kernel<kScopeGpu>),
+        reinterpret_cast<const void *>(cnt_record_kernel<kScopeSys>),
+        reinterpret_cast<const void *>(cnt_wait_kernel<false, false, kScopeSys>),
+        reinterpret_cast<const void *>(cnt_wait_kernel<true, false, kScopeSys>),
         reinterpret_cast<const void *>(cnt_wait_kernel<false, false>),
         reinterpret_cast<const void *>(cnt_wait_kernel<true, false>),
         reinterpret_cast<const void *>(cnt_wait_kernel<true, true>),
@@ -863,7 +898,11 @@ extern "C" int cntnotify_create(cns_cnt_notify_t *out, uint64_t flag)
     // a fresh notify starts at count 0 with a clear status
     CNS_CUDA(cudaMemset(line, 0, kWordsPerSlot * 4));
     pool.free_slots.pop_back();
-    auto *h = new cns_cnt_notify_s{kMagic, dev.device, slot, line};
+    auto *h = new cns_cnt_notify_s;
+    h->magic = kMagic;
+    h->device = dev.device;
+    h->slot = slot;
+    h->line = line;
     g_live.insert(h);
     *out = h;
     return CNS_SUCCESS;
@@ -908,6 +947,62 @@ extern "C" int cntnotify_get_device_ptr(cns_cnt_notify_t h, uint32_t **count_dev
 // Stream-ordered operations
 // ---------------------------------------------------------------------------
 
+// One record (mode, v) on stream s, launched on the stream's device, at
+// system scope once the notify has peers.
+static int enqueue_record(cns_cnt_notify_s *n, cudaStream_t s, uint32_t mode, uint32_t v)
+{
+    int dev = -1;
+    if (int rc = launch_device(n, s, &dev))
+        return rc;
+    DeviceGuard g;
+    if (int rc = g.set(dev))
+        return rc;
+    if (n->sys.load(std::memory_order_acquire))
+        cnt_record_kernel<kScopeSys><<<1, 32, 0, s>>>(n->line, mode, v);
+    else
+        cnt_record_kernel<kScopeGpu><<<1, 32, 0, s>>>(n->line, mode, v);
+    CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+extern "C" int cntnotify_enable_peer(cns_cnt_notify_t h, int peer_device)
+{
+    cns_cnt_notify_s *n = lookup(h);
+    if (!n)
+        return CNS_ERR_INVALID_HANDLE;
+    TraceRange tr("cntnotify_enable_peer", n->slot);
+    if (peer_device < 0 || peer_device >= 64)
+        return CNS_ERR_INVALID_VALUE;
+    int count = 0;
+    CNS_CUDA(cudaGetDeviceCount(&count));
+    if (peer_device >= count)
+        return CNS_ERR_INVALID_VALUE;
+    if (peer_device != n->device) {
+        int can = 0;
+        CNS_CUDA(cudaDeviceCanAccessPeer(&can, peer_device, n->device));
+        if (!can)
+            return CNS_ERR_NO_PEER_ACCESS;
+        DeviceGuard g;
+        if (int rc = g.set(peer_device))
+            return rc;
+        DeviceInfo dev;   // the peer runs the library's kernels too: same architecture check
+        if (int rc = current_device(&dev))
+            return rc;
+        const cudaError_t e = cudaDeviceEnablePeerAccess(n->device, 0);
+        if (e == cudaErrorPeerAccessAlreadyEnabled)
+            (void)cudaGetLastError();
+        else if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceEnablePeerAccess");
+        // the peer's streams will launch the notify kernels: load them there now
+        // (see preload_notify_kernels)
+        if (int rc = preload_notify_kernels())
+            return rc;
+    }
+    n->sys.store(1, std::memory_order_release);
+    n->peers.fetch_or(1ull << peer_device, std::memory_order_acq_rel);
+    return CNS_SUCCESS;
+}
+
 extern "C" int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const cns_record_info_t *info)
 {
     cns_cnt_notify_s *n = lookup(h);
@@ -918,12 +1013,7 @@ extern "C" int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const c
         return CNS_ERR_NULL_PTR;
     if (!record_mode_ok(info->mode))
         return CNS_ERR_INVALID_VALUE;
-    DeviceGuard g;
-    if (int rc = g.set(n->device))
-        return rc;
-    cnt_record_kernel<<<1, 32, 0, to_stream(stream)>>>(n->line, static_cast<uint32_t>(info->mode), info->value);
-    CNS_CUDA(cudaGetLastError());
-    return CNS_SUCCESS;
+    return enqueue_record(n, to_stream(stream), static_cast<uint32_t>(info->mode), info->value);
 }
 
 extern "C" int cntnotify_wait_with_timeout(cns_cnt_notify_t h, cns_stream_t stream, const cns_wait_info_t *info)
@@ -936,8 +1026,11 @@ extern "C" int cntnotify_wait_with_timeout(cns_cnt_notify_t h, cns_stream_t stre
         return CNS_ERR_NULL_PTR;
     if (info->mode < CNS_WAIT_LESS || info->mode > CNS_WAIT_EQUAL_WITH_BITMASK)
         return CNS_ERR_INVALID_VALUE;
+    int dev = -1;
+    if (int rc = launch_device(n, to_stream(stream), &dev))
+        return rc;
     DeviceGuard g;
-    if (int rc = g.set(n->device))
+    if (int rc = g.set(dev))
         return rc;
     return enqueue_wait(n, to_stream(stream), info, nullptr);
 }
@@ -948,12 +1041,7 @@ extern "C" int cntnotify_reset(cns_cnt_notify_t h, cns_stream_t stream)
     if (!n)
         return CNS_ERR_INVALID_HANDLE;
     TraceRange tr("cntnotify_reset", n->slot);
-    DeviceGuard g;
-    if (int rc = g.set(n->device))
-        return rc;
-    cnt_record_kernel<<<1, 32, 0, to_stream(stream)>>>(n->line, CNS_REC_SET, 0u);
-    CNS_CUDA(cudaGetLastError());
-    return CNS_SUCCESS;
+    return enqueue_record(n, to_stream(stream), CNS_REC_SET, 0u);
 }
 
 extern "C" int cntnotify_query_status(cns_cnt_notify_t h, int32_t *status, uint32_t *count)

@@ -55,6 +55,41 @@ __global__ void probe_grid_sync_kernel(uint4 *buf0, uint4 *buf1, int64_t rounds)
     }
 }
 
+// Two CTAs hand a counted-notify signal back and forth `iters` times with the
+// library's record and wait rules at scope S: CTA 0 records ADD 1 on count a
+// and waits for count b to reach i + 1; CTA 1 waits for a to reach i + 1 and
+// records ADD 1 on b.  out[0] = CTA 0's time for all iterations (two
+// hand-offs each), out[1] = 0 or the first wait's failure (each wait is
+// bounded by timeout_ns), out[2] / out[3] = the SMs of CTA 0 / CTA 1.
+template <int S>
+__global__ void probe_pingpong_kernel(int iters, uint32_t *a, uint32_t *b, uint64_t timeout_ns, uint64_t *out)
+{
+    if (threadIdx.x != 0 || blockIdx.x > 1)
+        return;
+    const bool first = blockIdx.x == 0;
+    uint32_t *mine = first ? a : b;
+    uint32_t *theirs = first ? b : a;
+    int rc = CNS_SUCCESS;
+    const uint64_t t0 = globaltimer_ns();
+    for (int i = 0; i < iters && rc == CNS_SUCCESS; ++i) {
+        const uint32_t want = static_cast<uint32_t>(i) + 1u;
+        if (first) {
+            cnt_record_scoped<S>(mine, CNS_REC_ADD, 1u);
+            rc = cnt_wait_scoped<S>(theirs, CNS_WAIT_BIGGER_OR_EQUAL, want, false, timeout_ns, nullptr);
+        } else {
+            rc = cnt_wait_scoped<S>(theirs, CNS_WAIT_BIGGER_OR_EQUAL, want, false, timeout_ns, nullptr);
+            if (rc == CNS_SUCCESS)
+                cnt_record_scoped<S>(mine, CNS_REC_ADD, 1u);
+        }
+    }
+    const uint64_t t1 = globaltimer_ns();
+    if (first)
+        out[0] = t1 - t0;
+    if (rc != CNS_SUCCESS)
+        out[1] = static_cast<uint64_t>(rc);
+    out[2 + blockIdx.x] = smid();
+}
+
 __global__ void probe_red_kernel(int iters, uint32_t *word)
 {
     for (int i = 0; i < iters; ++i)
@@ -123,5 +158,31 @@ extern "C" int cns_probe_grid_sync(int32_t ctas, int32_t threads, int64_t rounds
     }
     if (e != cudaSuccess)
         return cuda_fail(e, "grid-sync probe launch");
+    return CNS_SUCCESS;
+}
+
+extern "C" int cns_probe_notify_pingpong(int scope, int32_t iters, uint32_t *lines_dev, uint64_t *out_dev,
+                                         cns_stream_t stream)
+{
+    if (!lines_dev || !out_dev)
+        return CNS_ERR_NULL_PTR;
+    if ((scope != 0 && scope != 1) || iters < 1 || iters > (1 << 24))
+        return CNS_ERR_INVALID_VALUE;
+    if (reinterpret_cast<uintptr_t>(lines_dev) & (CNS_SYNCALL_LINE_BYTES - 1))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    cudaStream_t s = to_stream(stream);
+    CNS_CUDA(cudaMemsetAsync(lines_dev, 0, 2 * CNS_SYNCALL_LINE_BYTES, s));
+    CNS_CUDA(cudaMemsetAsync(out_dev, 0, 4 * sizeof(uint64_t), s));
+    uint32_t *a = lines_dev;
+    uint32_t *b = lines_dev + CNS_SYNCALL_LINE_BYTES / 4;
+    uint64_t timeout_ns = 1000000000ull;
+    void *args[] = {&iters, &a, &b, &timeout_ns, &out_dev};
+    // both CTAs must run at once: a cooperative launch guarantees it or refuses
+    const void *k = scope == 1 ? reinterpret_cast<const void *>(probe_pingpong_kernel<kScopeSys>)
+                               : reinterpret_cast<const void *>(probe_pingpong_kernel<kScopeGpu>);
+    CNS_CUDA(cudaLaunchCooperativeKernel(k, dim3(2), dim3(32), args, 0, s));
     return CNS_SUCCESS;
 }

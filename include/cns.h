@@ -48,7 +48,9 @@ typedef enum {
     CNS_ERR_TIMEOUT = 5,        /* a bounded device wait ran out ([SYNCALL] §5.2, [CNTN] §3.3) */
     CNS_ERR_NOT_RESIDENT = 6,   /* the grid cannot be co-resident ([SYNCALL] §6.3) */
     CNS_ERR_CUDA = 7,           /* a CUDA runtime call failed (or no device) */
-    CNS_ERR_ARCH = 8            /* the device is not compute capability 10.3 */
+    CNS_ERR_ARCH = 8,           /* the device is not compute capability 10.3 */
+    CNS_ERR_NO_PEER_ACCESS = 9  /* a stream of another device, which has no access to the notify
+                                   ([CNTN] §1: notifies between devices; cntnotify_enable_peer) */
 } cns_error_t;
 
 /* ========================================================================= */
@@ -408,8 +410,11 @@ int cntnotify_create(cns_cnt_notify_t *out, uint64_t flag);
  * cntnotify_record -- enqueue one record on `stream` ([CNTN] §4.2): when the
  * stream reaches it, the count becomes f(count, value) for info->mode, as one
  * device atomic with release semantics (work earlier on `stream` is visible
- * to whoever observes the new count).  Asynchronous.
- * Errors: INVALID_HANDLE, NULL_PTR (info), INVALID_VALUE (mode), CUDA.
+ * to whoever observes the new count).  Asynchronous.  The record runs on the
+ * stream's own device; a NULL stream is the default stream of the notify's
+ * device.  A stream of another device needs cntnotify_enable_peer first.
+ * Errors: INVALID_HANDLE, NULL_PTR (info), INVALID_VALUE (mode),
+ * NO_PEER_ACCESS (a stream of a device not enabled for this notify), CUDA.
  */
 int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const cns_record_info_t *info);
 
@@ -435,13 +440,17 @@ int cntnotify_record(cns_cnt_notify_t h, cns_stream_t stream, const cns_record_i
  * the count (cns_cnt_record_dev) must be loaded before a wait it releases is
  * running (cudaFuncGetAttributes on it, a launch, or
  * CUDA_MODULE_LOADING=EAGER).  Submitting the records before the wait avoids
- * both.
- * Errors: INVALID_HANDLE, NULL_PTR (info), INVALID_VALUE (mode), CUDA.
+ * both.  Like a record, the wait runs on the stream's own device (a NULL
+ * stream: the notify's device); on another device, enabled by
+ * cntnotify_enable_peer, it polls the count through the peer mapping.
+ * Errors: INVALID_HANDLE, NULL_PTR (info), INVALID_VALUE (mode),
+ * NO_PEER_ACCESS, CUDA.
  */
 int cntnotify_wait_with_timeout(cns_cnt_notify_t h, cns_stream_t stream, const cns_wait_info_t *info);
 
-/* cntnotify_reset -- enqueue count = 0 on `stream` ([CNTN] §4.4).
- * Errors: INVALID_HANDLE, CUDA. */
+/* cntnotify_reset -- enqueue count = 0 on `stream` ([CNTN] §4.4), on the
+ * stream's device like a record.
+ * Errors: INVALID_HANDLE, NO_PEER_ACCESS, CUDA. */
 int cntnotify_reset(cns_cnt_notify_t h, cns_stream_t stream);
 
 /* cntnotify_get_id -- the notify's id, unique among live notifies of the
@@ -458,6 +467,28 @@ int cntnotify_destroy(cns_cnt_notify_t h);
  * of the hardware notify slice of [CNTN] §6.2).  Valid until destroy.
  * Errors: INVALID_HANDLE, NULL_PTR. */
 int cntnotify_get_device_ptr(cns_cnt_notify_t h, uint32_t **count_dev);
+
+/*
+ * cntnotify_enable_peer -- let the streams of device `peer_device` record on,
+ * wait on and reset notify `h`, whose count lives on another device
+ * ([CNTN] §1: a counted notify also carries state and action notifications
+ * between devices).  Enables peer access from peer_device to the notify's
+ * device (an access already enabled is fine), loads the library's notify
+ * kernels on peer_device, and switches the notify to system scope: from then
+ * on every record, wait and reset on it is a system-scope operation (a
+ * record's release orders the recording GPU's earlier writes, to any GPU's
+ * memory, before a wait on another GPU sees the count), whichever device
+ * runs it.  Operations already enqueued keep the scope they were enqueued
+ * with, so call it before the first operation that involves the peer.  The
+ * same count word, from cntnotify_get_device_ptr, is valid in kernels on
+ * peer_device (use cns_cnt_record_sys_dev / cns_cnt_wait_sys_dev there).
+ * peer_device may be the notify's own device: nothing is mapped, and the
+ * notify only switches to system scope.  Calling it again adds a device.
+ * Errors: INVALID_HANDLE, INVALID_VALUE (peer_device outside the devices
+ * present), NO_PEER_ACCESS (the two devices cannot access each other), ARCH
+ * (peer_device is not compute capability 10.3), CUDA.
+ */
+int cntnotify_enable_peer(cns_cnt_notify_t h, int peer_device);
 
 /* cntnotify_query_status -- read the notify's sticky status (0 or
  * CNS_ERR_TIMEOUT left by a wait that timed out) and, if count is not NULL,
@@ -657,6 +688,22 @@ int cns_probe_grid_sync(int32_t ctas, int32_t threads, int64_t rounds, void *buf
  * Errors: NULL_PTR, INVALID_VALUE, CUDA.
  */
 int cns_probe_op_chain(const uint32_t *ops_dev, int32_t iters, uint64_t *out_dev, cns_stream_t stream);
+
+/*
+ * cns_probe_notify_pingpong -- the hand-off latency of a counted notify on the
+ * device: two co-resident CTAs pass a signal back and forth `iters` times, each
+ * pass a record (ADD 1, release) on one count and a bounded wait (BIGGER_OR_EQUAL)
+ * on the other, at gpu scope (scope 0) or system scope (scope 1, the scope of a
+ * notify that cntnotify_enable_peer prepared for other GPUs).  lines_dev: two
+ * 128-byte lines (256 B, 128-byte aligned), zeroed by the probe, each ending at
+ * iters.  out_dev: 4 uint64 -- [0] CTA 0's time in ns for all iterations (2 x
+ * iters hand-offs), [1] 0 or CNS_ERR_TIMEOUT (each wait is bounded by 1 s),
+ * [2] and [3] the SMs the two CTAs ran on.  Stream-ordered.
+ * Errors: NULL_PTR, INVALID_VALUE (scope, iters outside 1..2^24, alignment),
+ * CUDA.
+ */
+int cns_probe_notify_pingpong(int scope, int32_t iters, uint32_t *lines_dev, uint64_t *out_dev,
+                              cns_stream_t stream);
 
 /*
  * cns_probe_round_phases -- where the time of one round of the headline goes:

@@ -24,6 +24,10 @@
  *   cns_syncall_soft_die_local  the same on the two counter copies of a
  *                        die-local workspace, one on each of GB300's dies
  *                        (faster; the caller keeps a small per-CTA state)
+ *   cns_cnt_record_sys_dev, cns_cnt_wait_sys_dev  record and wait at system
+ *                        scope, for a count word that GPUs other than its
+ *                        own also record on or wait on (§1: CntNotify between
+ *                        devices), through a peer mapping
  *
  * Every wait is bounded and reports CNS_ERR_TIMEOUT instead of trapping.  The
  * caller makes the participating CTAs co-resident (a cooperative launch, or a
@@ -209,6 +213,82 @@ __device__ __forceinline__ uint32_t smid()
     return s;
 }
 
+// System scope (.sys): the same operations, ordered with threads of other
+// GPUs too.  A count word that a peer GPU records on through a peer mapping
+// (or waits on) is accessed with these on both sides; a gpu-scope acquire
+// does not synchronise with a release performed on another GPU.
+__device__ __forceinline__ uint32_t ld_relaxed_sys(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t atom_exch_release_sys(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.release.sys.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_exch_relaxed_sys(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.sys.global.exch.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void red_add_release_sys(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.sys.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_or_release_sys(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.sys.global.or.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_and_release_sys(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.sys.global.and.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acquire_sys()
+{
+    asm volatile("fence.acquire.sys;" ::: "memory");
+}
+
+// The scope of a counted notify's operations: kScopeGpu for a count that only
+// its own GPU touches, kScopeSys once other GPUs record on or wait on it.
+enum : int { kScopeGpu = 0, kScopeSys = 1 };
+
+template <int S>
+__device__ __forceinline__ uint32_t ld_relaxed_scoped(const uint32_t *p)
+{
+    if constexpr (S == kScopeSys)
+        return ld_relaxed_sys(p);
+    else
+        return ld_relaxed_gpu(p);
+}
+
+template <int S>
+__device__ __forceinline__ void fence_acquire_scoped()
+{
+    if constexpr (S == kScopeSys)
+        fence_acquire_sys();
+    else
+        fence_acquire_gpu();
+}
+
+template <int S>
+__device__ __forceinline__ uint32_t atom_exch_relaxed_scoped(uint32_t *p, uint32_t v)
+{
+    if constexpr (S == kScopeSys)
+        return atom_exch_relaxed_sys(p, v);
+    else
+        return atom_exch_relaxed_gpu(p, v);
+}
+
 // ---------------------------------------------------------------------------
 // Epoch arithmetic of the soft barrier ("PTO-ISA SYNCALL cross-core barrier
 // guide", §5.2).  The counter lives in Z_M with M = P * floor(2^32 / P): the
@@ -347,16 +427,61 @@ __device__ __forceinline__ bool cnt_wait_released(uint32_t c, uint32_t mode, uin
                                               : mask;   // CNS_WAIT_EQUAL_WITH_BITMASK
 }
 
-// A record as one device atomic with release semantics.  Usable from inside
-// any kernel (one thread per record).
+// A record as one device atomic with release semantics, at scope S.  Usable
+// from inside any kernel (one thread per record).
+template <int S>
+__device__ __forceinline__ void cnt_record_scoped(uint32_t *count, uint32_t mode, uint32_t v)
+{
+    if constexpr (S == kScopeSys) {
+        switch (mode) {
+        case CNS_REC_SET: atom_exch_release_sys(count, v); break;
+        case CNS_REC_ADD: red_add_release_sys(count, v); break;
+        case CNS_REC_BIT_OR: red_or_release_sys(count, v); break;
+        case CNS_REC_BIT_AND: red_and_release_sys(count, v); break;
+        default: break;
+        }
+    } else {
+        switch (mode) {
+        case CNS_REC_SET: atom_exch_release_gpu(count, v); break;
+        case CNS_REC_ADD: red_add_release_gpu(count, v); break;
+        case CNS_REC_BIT_OR: red_or_release_gpu(count, v); break;
+        case CNS_REC_BIT_AND: red_and_release_gpu(count, v); break;
+        default: break;
+        }
+    }
+}
+
 __device__ __forceinline__ void cnt_record_device(uint32_t *count, uint32_t mode, uint32_t v)
 {
-    switch (mode) {
-    case CNS_REC_SET: atom_exch_release_gpu(count, v); break;
-    case CNS_REC_ADD: red_add_release_gpu(count, v); break;
-    case CNS_REC_BIT_OR: red_or_release_gpu(count, v); break;
-    case CNS_REC_BIT_AND: red_and_release_gpu(count, v); break;
-    default: break;
+    cnt_record_scoped<kScopeGpu>(count, mode, v);
+}
+
+// A bounded wait on a count word from the calling thread, at scope S: relaxed
+// polls, one acquire fence once released, then the optional clear.  Returns
+// CNS_SUCCESS or CNS_ERR_TIMEOUT.
+template <int S>
+__device__ __forceinline__ int cnt_wait_scoped(uint32_t *count, uint32_t mode, uint32_t v, bool is_clear,
+                                               uint64_t limit, uint32_t *observed)
+{
+    uint32_t spins = 0;
+    uint64_t deadline = 0;
+    for (;;) {
+        const uint32_t c = ld_relaxed_scoped<S>(count);
+        if (cnt_wait_released(c, mode, v)) {
+            fence_acquire_scoped<S>();
+            if (observed)
+                *observed = c;
+            if (is_clear)
+                atom_exch_relaxed_scoped<S>(count, 0u);
+            return CNS_SUCCESS;
+        }
+        if ((++spins & 63u) == 0u) {
+            const uint64_t now = globaltimer_ns();
+            if (deadline == 0)
+                deadline = now + limit;
+            else if (now > deadline)
+                return CNS_ERR_TIMEOUT;
+        }
     }
 }
 
@@ -383,27 +508,30 @@ __device__ __forceinline__ int cns_cnt_wait_dev(uint32_t *count, int mode, uint3
 {
     if (mode < 0 || mode > 4)
         return CNS_ERR_INVALID_VALUE;
-    const uint64_t limit = timeout_ns ? timeout_ns : 2000000000ull;
-    uint32_t spins = 0;
-    uint64_t deadline = 0;
-    for (;;) {
-        const uint32_t c = cns::ld_relaxed_gpu(count);
-        if (cns::cnt_wait_released(c, static_cast<uint32_t>(mode), v)) {
-            cns::fence_acquire_gpu();
-            if (observed)
-                *observed = c;
-            if (is_clear)
-                cns::atom_exch_relaxed_gpu(count, 0u);
-            return CNS_SUCCESS;
-        }
-        if ((++spins & 63u) == 0u) {
-            const uint64_t now = cns::globaltimer_ns();
-            if (deadline == 0)
-                deadline = now + limit;
-            else if (now > deadline)
-                return CNS_ERR_TIMEOUT;
-        }
-    }
+    return cns::cnt_wait_scoped<cns::kScopeGpu>(count, static_cast<uint32_t>(mode), v, is_clear != 0,
+                                                timeout_ns ? timeout_ns : 2000000000ull, observed);
+}
+
+/* cns_cnt_record_dev at system scope: for a count word that threads of other
+ * GPUs also record on or wait on (a notify prepared by cntnotify_enable_peer,
+ * recorded from a peer GPU through the same address).  The caller's earlier
+ * writes, to any GPU's memory, are visible to whoever is released by it. */
+__device__ __forceinline__ void cns_cnt_record_sys_dev(uint32_t *count, int mode, uint32_t v)
+{
+    cns::cnt_record_scoped<cns::kScopeSys>(count, static_cast<uint32_t>(mode), v);
+}
+
+/* cns_cnt_wait_dev at system scope: released by records made at system scope
+ * on any GPU (cntnotify_record on a notify prepared by cntnotify_enable_peer,
+ * or cns_cnt_record_sys_dev); the count word may live on another GPU, reached
+ * through a peer mapping.  Same arguments and results as cns_cnt_wait_dev. */
+__device__ __forceinline__ int cns_cnt_wait_sys_dev(uint32_t *count, int mode, uint32_t v, int is_clear,
+                                                    uint64_t timeout_ns, uint32_t *observed)
+{
+    if (mode < 0 || mode > 4)
+        return CNS_ERR_INVALID_VALUE;
+    return cns::cnt_wait_scoped<cns::kScopeSys>(count, static_cast<uint32_t>(mode), v, is_clear != 0,
+                                                timeout_ns ? timeout_ns : 2000000000ull, observed);
 }
 
 namespace cns {

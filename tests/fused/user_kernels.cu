@@ -79,6 +79,20 @@ __global__ void wait_kernel(uint32_t *count, int mode, uint32_t v, int is_clear,
         *rc = cns_cnt_wait_dev(count, mode, v, is_clear, timeout_ns, observed);
 }
 
+// The same at system scope (a count word that peer GPUs also use).
+__global__ void record_sys_kernel(uint32_t *count, int mode, uint32_t v, int per_thread)
+{
+    for (int i = 0; i < per_thread; ++i)
+        cns_cnt_record_sys_dev(count, mode, v);
+}
+
+__global__ void wait_sys_kernel(uint32_t *count, int mode, uint32_t v, int is_clear, uint64_t timeout_ns, int *rc,
+                                uint32_t *observed)
+{
+    if (threadIdx.x == 0)
+        *rc = cns_cnt_wait_sys_dev(count, mode, v, is_clear, timeout_ns, observed);
+}
+
 // A grid-wide consumer: CTAs 0 .. G-1 take cns_cnt_wait_grid_dev (count >=
 // k, clear) as call r of `rounds`, then each sums the `words` words of area
 // r % 2 into sums[r * G + cta] and records ADD 1 on ack.  CTA G produces:
@@ -208,6 +222,25 @@ extern "C" int user_wait(uint32_t *count, int mode, uint32_t v, int is_clear, ui
                          uint32_t *observed)
 {
     wait_kernel<<<1, 32>>>(count, mode, v, is_clear, timeout_ns, rc, observed);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    return static_cast<int>(e);
+}
+
+extern "C" int user_record_sys(uint32_t *count, int mode, uint32_t v, int32_t ctas, int32_t threads, int per_thread)
+{
+    record_sys_kernel<<<ctas, threads>>>(count, mode, v, per_thread);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    return static_cast<int>(e);
+}
+
+extern "C" int user_wait_sys(uint32_t *count, int mode, uint32_t v, int is_clear, uint64_t timeout_ns, int *rc,
+                             uint32_t *observed)
+{
+    wait_sys_kernel<<<1, 32>>>(count, mode, v, is_clear, timeout_ns, rc, observed);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess)
         e = cudaDeviceSynchronize();

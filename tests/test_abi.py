@@ -114,6 +114,7 @@ def test_invalid_handles(built):
         assert cns.cntnotify_destroy(h) == cns.CNS_ERR_INVALID_HANDLE
         assert cns.cntnotify_get_device_ptr(h)[0] == cns.CNS_ERR_INVALID_HANDLE
         assert cns.cntnotify_query_status(h)[0] == cns.CNS_ERR_INVALID_HANDLE
+        assert cns.cntnotify_enable_peer(h, 0) == cns.CNS_ERR_INVALID_HANDLE
 
 
 def test_syncall_argument_checks(built):

@@ -6,24 +6,14 @@ by the library's stream wait; device waits on every mode against the oracle's
 rule; a grid-wide consumer on cns_cnt_wait_grid_dev against the oracle's
 pipeline checksums; and bounded timeouts (a barrier one CTA never reaches, a
 count nobody records, a grid-wide wait nobody releases)."""
-import ctypes
-import os
-import subprocess
-
 import numpy as np
 import pytest
 
 import cns_inputs as ci
 import oracle
-from tests.gpu_helpers import from_dev_u32, to_dev_u32
+from tests.gpu_helpers import from_dev_u32, load_user_kernels, to_dev_u32
 
 pytestmark = pytest.mark.gpu
-
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SRC = os.path.join(ROOT, "tests", "fused", "user_kernels.cu")
-OUT = os.path.join(ROOT, "tests", "fused", "_build", "libcns_user_kernels.so")
-HDR = os.path.join(ROOT, "include", "cns_device.h")
-
 
 @pytest.fixture(scope="module")
 def cns():
@@ -36,27 +26,7 @@ def cns():
 
 @pytest.fixture(scope="module")
 def user(cns):
-    from counted_notify_sync_gb300 import builder
-    newest = max(os.path.getmtime(p) for p in (SRC, HDR, os.path.join(ROOT, "include", "cns.h")))
-    if not os.path.exists(OUT) or os.path.getmtime(OUT) < newest:
-        os.makedirs(os.path.dirname(OUT), exist_ok=True)
-        tmp = OUT + f".tmp{os.getpid()}"
-        nvcc = os.path.join(builder.cuda_home(), "bin", "nvcc")
-        subprocess.run([nvcc, *builder.ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-                        "-I", os.path.join(ROOT, "include"), "-o", tmp, SRC], check=True)
-        os.replace(tmp, OUT)
-    L = ctypes.CDLL(OUT)
-    i32, u32, i64, u64, vp = ctypes.c_int32, ctypes.c_uint32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
-    L.user_ring.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
-    L.user_ring_die_local.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
-    L.user_record.argtypes = [vp, ctypes.c_int, u32, i32, i32, ctypes.c_int]
-    L.user_wait.argtypes = [vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp]
-    L.user_grid_wait.argtypes = [i32, i32, vp, vp, vp, vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp, vp]
-    L.user_grid_wait_only.argtypes = [i32, vp, vp, u32, ctypes.c_int, u32, u64, vp]
-    for f in (L.user_ring, L.user_ring_die_local, L.user_record, L.user_wait, L.user_grid_wait,
-              L.user_grid_wait_only):
-        f.restype = ctypes.c_int
-    return L
+    return load_user_kernels()
 
 
 def _ring(cns, user, ctas, P, rounds, start=0, threads=256, short_cta=0xFFFFFFFF, timeout_ns=0, die_local=False):
