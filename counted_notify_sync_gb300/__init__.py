@@ -47,7 +47,8 @@ def new_workspace(device=None, start_value: int = 0, stream=None, die_local: boo
 
 def run_syncall(mode, core_type, workload, launch_ctas, buf0, buf1, rounds, *, used_cores=0, aiv_ratio=0,
                 elems=0, threads=256, cluster_dim=0, timeout_ms=0, workspace=None, cta_status=None,
-                stream=None, sync=True, host_in=None, host_out=None, check=True, variant=0, launch_flags=0):
+                stream=None, sync=True, host_in=None, host_out=None, check=True, variant=0, launch_flags=0,
+                hard_step=0):
     """Call syncall_run with device buffers (torch tensors); returns the filled SyncallData and the code."""
     d = _native.SyncallData()
     d.workload = workload
@@ -66,6 +67,7 @@ def run_syncall(mode, core_type, workload, launch_ctas, buf0, buf1, rounds, *, u
     d.host_out = _native.ptr(host_out)
     d.barrier_variant = variant
     d.launch_flags = launch_flags
+    d.hard_step = hard_step
     d.workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
     rc = _native.syncall_run(mode, core_type, used_cores, aiv_ratio, rounds, d)
     if check and rc != _native.CNS_SUCCESS:

@@ -58,6 +58,8 @@ CNS_CTA_DONE = 1
 CNS_CTA_IDLE = 2
 CNS_CTA_ABORTED = 4
 CNS_LAUNCH_NO_CLUSTER_ATTR = 1
+CNS_HARD_STEP_CLUSTER_BARRIER = 0
+CNS_HARD_STEP_PAIRED_MBARRIER = 1
 
 CNS_REC_SET = 0
 CNS_REC_ADD = 1
@@ -90,7 +92,7 @@ class SyncallData(Structure):
         ("cta_status_dev", c_void_p), ("stream", c_void_p), ("timeout_ms", c_uint32), ("sync", c_int32),
         ("host_in", c_void_p), ("host_out", c_void_p), ("elapsed_ms", c_float), ("final_counter", c_uint32),
         ("device_status", c_int32), ("grid_ctas", c_int32), ("participants", c_int32), ("cluster_used", c_int32),
-        ("barrier_variant", c_int32), ("workspace_bytes", c_uint32), ("launch_flags", c_uint32), ("reserved", c_int32),
+        ("barrier_variant", c_int32), ("workspace_bytes", c_uint32), ("launch_flags", c_uint32), ("hard_step", c_int32),
     ]
 
 

@@ -553,6 +553,142 @@ __device__ __forceinline__ bool hard_barrier(const Barrier &b, EpochCursor &c, u
     return false;
 }
 
+// ---------------------------------------------------------------------------
+// The hard path's other intra-cluster step: paired mbarriers over DSMEM
+// ---------------------------------------------------------------------------
+//
+// The guide's MIX hard path pairs each AIC core with its AIV cores through
+// intra-block flags (§5.1): the AIVs set a flag the AIC waits for
+// (wait_intra_block), the AIC takes part in the cross-core step, then sets a
+// flag each AIV waits for (set_intra_block).  Here the flags are shared-memory
+// mbarriers reached over distributed shared memory: every member CTA arrives
+// (release, cluster scope) on the leader's gather mbarrier; the leader waits
+// for all of them (acquire), arrives on the device-wide counter and waits for
+// the round, then arrives on each member's release mbarrier, which the member
+// waits on.  Only the leader touches the counter.
+enum : int { kHardStepClusterBarrier = 0, kHardStepPairedMbarrier = 1 };
+
+// One arrival (release, cluster scope) on the mbarrier at the address that
+// `local` has, in the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ void mbar_arrive_remote(const uint64_t *local, uint32_t rank)
+{
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+
+// Whether the phase with this parity has completed; acquire at cluster scope
+// (the arrivals' releases come from other CTAs of the cluster).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(a), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of *bar, bounded: gives up (returns true) when the
+// cluster's stop flag is raised, when the workspace's abort flag is, or after
+// `limit` ns (then it records CNS_ERR_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, const int *s_flag,
+                                                  uint32_t *status_line, uint64_t limit, uint32_t round,
+                                                  uint32_t who)
+{
+    uint32_t spins = 0;
+    uint64_t deadline = 0;
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (*reinterpret_cast<const volatile int *>(s_flag) != 0)
+            return true;
+        if ((++spins & 15u) == 0u) {
+            if (ld_relaxed_gpu(status_line + 1) != 0u)
+                return true;
+            const uint64_t now = globaltimer_ns();
+            if (deadline == 0) {
+                deadline = now + limit;
+            } else if (now > deadline) {
+                raise_timeout(status_line, round, who);
+                return true;
+            }
+        }
+    }
+    return false;
+}
+
+// The mbarriers of the paired step, in each CTA's shared memory: `gather`
+// (the leader's: one arrival per member and phase) and `release` (each
+// member's: one arrival from the leader per phase), with the phase parities
+// the CTA's elected thread waits for next.
+struct PairedBars {
+    uint64_t *gather;
+    uint64_t *release;
+    uint32_t gather_parity;
+    uint32_t release_parity;
+};
+
+// Set up by thread 0 of every CTA of the cluster before the cluster barrier
+// that precedes the first round (the init must be visible to the remote
+// arrivals).
+__device__ __forceinline__ void paired_bars_init(const PairedBars &pb)
+{
+    const uint32_t n = cluster_nctarank();
+    mbar_init(pb.gather, n > 1u ? n - 1u : 1u);
+    mbar_init(pb.release, 1u);
+    mbar_init_fence();
+}
+
+// One hard barrier with the paired step.  All threads of all CTAs of the
+// cluster call it; returns true if the CTA must stop.  A CTA that stops
+// raises the stop flag in every CTA of its cluster; a leader that stops
+// still arrives on every member's release mbarrier, so no member waits for
+// it in vain.  The members allow for the leader's two bounded waits (the
+// gather and the counter) before they give up themselves.
+template <int V>
+__device__ __forceinline__ bool paired_barrier(const Barrier &b, EpochCursor &c, uint32_t round, int *s_flag,
+                                               PairedBars &pb)
+{
+    __syncthreads();   // the CTA's writes are done before its elected thread signals
+    int stop = 0;
+    if (threadIdx.x == 0) {
+        const uint32_t n = cluster_nctarank();
+        if (cluster_ctarank() != 0) {
+            mbar_arrive_remote(pb.gather, 0);
+            stop = mbar_wait_bounded(pb.release, pb.release_parity, s_flag, b.status_line, 2u * b.timeout_ns,
+                                     round, blockIdx.x) ? 1 : 0;
+            pb.release_parity ^= 1u;
+        } else {
+            if (n > 1u) {
+                stop = mbar_wait_bounded(pb.gather, pb.gather_parity, s_flag, b.status_line, b.timeout_ns, round,
+                                         blockIdx.x) ? 1 : 0;
+                pb.gather_parity ^= 1u;
+            }
+            if (!stop) {
+                const Pending pd = barrier_arrive<V>(b, c, round, blockIdx.x);
+                stop = barrier_wait<V>(b, pd, round, blockIdx.x) ? 1 : 0;
+            }
+            if (stop) {
+                for (uint32_t m = 0; m < n; ++m)
+                    st_shared_cluster(s_flag, m, 1u);
+            }
+            for (uint32_t m = 1; m < n; ++m)
+                mbar_arrive_remote(pb.release, m);
+        }
+        if (*reinterpret_cast<volatile int *>(s_flag) != 0)
+            stop = 1;
+        if (stop) {
+            const uint32_t n2 = cluster_nctarank();
+            for (uint32_t m = 0; m < n2; ++m)
+                st_shared_cluster(s_flag, m, 1u);
+        }
+    }
+    return __syncthreads_or(stop) != 0;
+}
+
 // After the last round: one more cluster barrier so that a stop raised in the
 // last round reaches the whole cluster.  Returns true if it did.
 __device__ __forceinline__ bool hard_barrier_finish(int *s_flag)

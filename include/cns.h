@@ -278,8 +278,30 @@ typedef struct {
     int32_t barrier_variant; /* (in) cns_barrier_variant_t; 0 = the guide's counter poll */
     uint32_t workspace_bytes;/* (in) size of workspace_dev; 0 = CNS_SYNCALL_WORKSPACE_BYTES */
     uint32_t launch_flags;   /* (in) 0, or CNS_LAUNCH_NO_CLUSTER_ATTR (testing) */
-    int32_t reserved;
+    int32_t hard_step;       /* (in) HARD: cns_hard_step_t, the intra-cluster step; 0 = the
+                                cluster barrier.  SOFT: must be 0. */
 } cns_syncall_data_t;
+
+/* cns_syncall_data_t.hard_step: how the hard path's cluster takes part in a
+ * barrier ([SYNCALL] §5.1: the AIC core and its AIV cores first meet on
+ * intra-block flags, the AIC core joins the cross-core step, then releases
+ * its AIVs).
+ *   CLUSTER_BARRIER  every CTA takes one hardware cluster barrier
+ *                    (barrier.cluster), cluster rank 0 arrives on the hard
+ *                    counter, and every CTA then polls the counter itself
+ *                    (the default; measured faster).
+ *   PAIRED_MBARRIER  the guide's pairing over distributed shared memory:
+ *                    each member CTA arrives on an mbarrier in cluster rank
+ *                    0's shared memory (wait_intra_block's flag), rank 0
+ *                    waits for all of them, arrives on the hard counter and
+ *                    waits for the round, then arrives on an mbarrier in
+ *                    each member's shared memory (set_intra_block's flag),
+ *                    which the member waits on.  Only rank 0 touches the
+ *                    counter.  Same results, same status line. */
+typedef enum {
+    CNS_HARD_STEP_CLUSTER_BARRIER = 0,
+    CNS_HARD_STEP_PAIRED_MBARRIER = 1
+} cns_hard_step_t;
 
 /* cns_syncall_data_t.launch_flags.  CNS_LAUNCH_NO_CLUSTER_ATTR launches the
  * HARD path without the cluster-dimension attribute, so that every CTA forms

@@ -24,6 +24,9 @@
  *   cns_syncall_soft_die_local  the same on the two counter copies of a
  *                        die-local workspace, one on each of GB300's dies
  *                        (faster; the caller keeps a small per-CTA state)
+ *   cns_syncall_soft_sys  the soft barrier at system scope, for participants
+ *                        on several GPUs arriving on one workspace through
+ *                        peer mappings
  *   cns_cnt_record_sys_dev, cns_cnt_wait_sys_dev  record and wait at system
  *                        scope, for a count word that GPUs other than its
  *                        own also record on or wait on (§1: CntNotify between
@@ -251,6 +254,25 @@ __device__ __forceinline__ void red_or_release_sys(uint32_t *p, uint32_t v)
 __device__ __forceinline__ void red_and_release_sys(uint32_t *p, uint32_t v)
 {
     asm volatile("red.release.sys.global.and.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_inc_release_sys(uint32_t *p, uint32_t bound)
+{
+    uint32_t old;
+    asm volatile("atom.release.sys.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(bound) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint32_t atom_cas_relaxed_sys(uint32_t *p, uint32_t cmp, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.relaxed.sys.global.cas.b32 %0, [%1], %2, %3;" : "=r"(old) : "l"(p), "r"(cmp), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void st_relaxed_sys(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.relaxed.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void fence_acquire_sys()
@@ -639,6 +661,66 @@ __device__ __forceinline__ int cns_cnt_wait_grid_dev(uint32_t *count, uint32_t *
     return __syncthreads_or(rc != CNS_SUCCESS) ? CNS_ERR_TIMEOUT : CNS_SUCCESS;
 }
 
+namespace cns {
+
+// The soft barrier of cns_syncall_soft at scope S (kScopeSys: participants on
+// several GPUs, the workspace reached through peer mappings).
+template <int S>
+__device__ __forceinline__ int syncall_soft_scoped(void *workspace, uint32_t participants, uint64_t timeout_ns)
+{
+    if (participants == 0u)
+        return CNS_ERR_INVALID_VALUE;
+    uint32_t *ctr = static_cast<uint32_t *>(workspace);
+    uint32_t *status = ctr + CNS_SYNCALL_LINE_BYTES / 4;
+    int stop = 0;
+    __syncthreads();
+    if (threadIdx.x == 0 && threadIdx.y == 0 && threadIdx.z == 0) {
+        const Epoch e = epoch_of(participants);
+        const uint32_t before = (S == kScopeSys) ? atom_inc_release_sys(ctr, e.Mm1) : atom_inc_release_gpu(ctr, e.Mm1);
+        const uint32_t target = epoch_target(before, e);
+        const uint32_t mine = (before == e.Mm1) ? 0u : before + 1u;
+        if (epoch_reached(mine, target, e)) {
+            fence_acquire_scoped<S>();   // the last arrival: its increment read every other one's
+        } else {
+            const uint64_t limit = timeout_ns ? timeout_ns : 2000000000ull;
+            uint32_t spins = 0;
+            uint64_t deadline = 0;
+            for (;;) {
+                if (epoch_reached(ld_relaxed_scoped<S>(ctr), target, e)) {
+                    fence_acquire_scoped<S>();
+                    break;
+                }
+                if ((++spins & 63u) == 0u) {
+                    if (ld_relaxed_scoped<S>(status + 1) != 0u) {
+                        stop = 1;
+                        break;
+                    }
+                    const uint64_t now = globaltimer_ns();
+                    if (deadline == 0) {
+                        deadline = now + limit;
+                    } else if (now > deadline) {
+                        const uint32_t code = static_cast<uint32_t>(CNS_ERR_TIMEOUT);
+                        if constexpr (S == kScopeSys) {
+                            if (atom_cas_relaxed_sys(status, 0u, code) == 0u)
+                                st_relaxed_sys(status + 3, blockIdx.x);
+                            atom_exch_release_sys(status + 1, 1u);
+                        } else {
+                            if (atom_cas_relaxed_gpu(status, 0u, code) == 0u)
+                                st_relaxed_gpu(status + 3, blockIdx.x);
+                            atom_exch_release_gpu(status + 1, 1u);
+                        }
+                        stop = 1;
+                        break;
+                    }
+                }
+            }
+        }
+    }
+    return __syncthreads_or(stop) ? CNS_ERR_TIMEOUT : CNS_SUCCESS;
+}
+
+}  // namespace cns
+
 /* The soft SYNCALL barrier among CTAs 0 .. participants - 1 of the grid.
  * Every thread of each participating CTA calls it, the same number of times
  * in each CTA; CTAs with blockIdx.x >= participants must not call it.  The
@@ -662,48 +744,24 @@ __device__ __forceinline__ int cns_cnt_wait_grid_dev(uint32_t *count, uint32_t *
  * CNS_ERR_INVALID_VALUE without arriving when participants is 0. */
 __device__ __forceinline__ int cns_syncall_soft(void *workspace, uint32_t participants, uint64_t timeout_ns)
 {
-    if (participants == 0u)
-        return CNS_ERR_INVALID_VALUE;
-    uint32_t *ctr = static_cast<uint32_t *>(workspace);
-    uint32_t *status = ctr + CNS_SYNCALL_LINE_BYTES / 4;
-    int stop = 0;
-    __syncthreads();
-    if (threadIdx.x == 0 && threadIdx.y == 0 && threadIdx.z == 0) {
-        const cns::Epoch e = cns::epoch_of(participants);
-        const uint32_t before = cns::atom_inc_release_gpu(ctr, e.Mm1);
-        const uint32_t target = cns::epoch_target(before, e);
-        const uint32_t mine = (before == e.Mm1) ? 0u : before + 1u;
-        if (cns::epoch_reached(mine, target, e)) {
-            cns::fence_acquire_gpu();   // the last arrival: its increment read every other one's
-        } else {
-            const uint64_t limit = timeout_ns ? timeout_ns : 2000000000ull;
-            uint32_t spins = 0;
-            uint64_t deadline = 0;
-            for (;;) {
-                if (cns::epoch_reached(cns::ld_relaxed_gpu(ctr), target, e)) {
-                    cns::fence_acquire_gpu();
-                    break;
-                }
-                if ((++spins & 63u) == 0u) {
-                    if (cns::ld_relaxed_gpu(status + 1) != 0u) {
-                        stop = 1;
-                        break;
-                    }
-                    const uint64_t now = cns::globaltimer_ns();
-                    if (deadline == 0) {
-                        deadline = now + limit;
-                    } else if (now > deadline) {
-                        if (cns::atom_cas_relaxed_gpu(status, 0u, static_cast<uint32_t>(CNS_ERR_TIMEOUT)) == 0u)
-                            cns::st_relaxed_gpu(status + 3, blockIdx.x);
-                        cns::atom_exch_release_gpu(status + 1, 1u);
-                        stop = 1;
-                        break;
-                    }
-                }
-            }
-        }
-    }
-    return __syncthreads_or(stop) ? CNS_ERR_TIMEOUT : CNS_SUCCESS;
+    return cns::syncall_soft_scoped<cns::kScopeGpu>(workspace, participants, timeout_ns);
+}
+
+/* cns_syncall_soft at system scope, for participants on several GPUs (the
+ * SYNCALL barrier across devices): every participating CTA of every GPU
+ * calls it with the same workspace -- one syncall_workspace_init prepared on
+ * one GPU, reached from the others through a peer mapping (the caller
+ * enables peer access, cudaDeviceEnablePeerAccess, from each other GPU to
+ * the workspace's) -- and `participants` = the participating CTAs of all
+ * GPUs together.  Arrivals are system-scope release increments and the wait
+ * acquires at system scope, so each GPU's writes before the barrier are
+ * visible to every participant after it.  The caller makes every
+ * participating CTA of every GPU co-resident for the whole run, as for
+ * cns_syncall_soft; a participant that never arrives ends the others' wait
+ * in CNS_ERR_TIMEOUT.  Same results and status line as cns_syncall_soft. */
+__device__ __forceinline__ int cns_syncall_soft_sys(void *workspace, uint32_t participants, uint64_t timeout_ns)
+{
+    return cns::syncall_soft_scoped<cns::kScopeSys>(workspace, participants, timeout_ns);
 }
 
 /* Per-CTA state of cns_syncall_soft_die_local, held by the caller (shared

@@ -1,5 +1,6 @@
 // Test-only user kernels built on include/cns_device.h: the ring-rotate rounds
-// separated by cns_syncall_soft, records with cns_cnt_record_dev, waits with
+// separated by cns_syncall_soft (or its system-scope form), records with
+// cns_cnt_record_dev, waits with
 // cns_cnt_wait_dev, and a grid-wide consumer on cns_cnt_wait_grid_dev, each
 // behind a plain C launcher.  Compiled by the GPU
 // tests into a shared library of their own.
@@ -14,6 +15,8 @@ namespace {
 // buffers swapping each round), each followed by the soft barrier; CTA
 // `short_cta` (if below participants) takes one barrier fewer.  Other CTAs
 // return at once.  status[p] = the first non-zero barrier result, or 0.
+// kSys: the barrier at system scope (cns_syncall_soft_sys).
+template <bool kSys>
 __global__ void ring_kernel(uint4 *b0, uint4 *b1, uint32_t participants, int64_t rounds, void *ws,
                             uint64_t timeout_ns, uint32_t short_cta, int *status)
 {
@@ -29,7 +32,7 @@ __global__ void ring_kernel(uint4 *b0, uint4 *b1, uint32_t participants, int64_t
             dst[p] = src[(p + 1 == participants) ? 0 : p + 1];
         if (r >= mine)
             break;
-        st = cns_syncall_soft(ws, participants, timeout_ns);
+        st = kSys ? cns_syncall_soft_sys(ws, participants, timeout_ns) : cns_syncall_soft(ws, participants, timeout_ns);
         if (st != CNS_SUCCESS)
             break;
     }
@@ -191,7 +194,18 @@ extern "C" int user_ring(int32_t ctas, int32_t threads, uint32_t participants, i
                          void *ws, uint64_t timeout_ns, uint32_t short_cta, int *status)
 {
     void *args[] = {&b0, &b1, &participants, &rounds, &ws, &timeout_ns, &short_cta, &status};
-    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ring_kernel), dim3(ctas),
+    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ring_kernel<false>), dim3(ctas),
+                                                dim3(threads), args, 0, 0);
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    return static_cast<int>(e);
+}
+
+extern "C" int user_ring_sys(int32_t ctas, int32_t threads, uint32_t participants, int64_t rounds, void *b0,
+                             void *b1, void *ws, uint64_t timeout_ns, uint32_t short_cta, int *status)
+{
+    void *args[] = {&b0, &b1, &participants, &rounds, &ws, &timeout_ns, &short_cta, &status};
+    cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(ring_kernel<true>), dim3(ctas),
                                                 dim3(threads), args, 0, 0);
     if (e == cudaSuccess)
         e = cudaDeviceSynchronize();

@@ -44,13 +44,14 @@ def load_user_kernels():
     i32, u32, i64, u64, vp = ctypes.c_int32, ctypes.c_uint32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
     L.user_ring.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
     L.user_ring_die_local.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
+    L.user_ring_sys.argtypes = [i32, i32, u32, i64, vp, vp, vp, u64, u32, vp]
     L.user_record.argtypes = [vp, ctypes.c_int, u32, i32, i32, ctypes.c_int]
     L.user_wait.argtypes = [vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp]
     L.user_record_sys.argtypes = [vp, ctypes.c_int, u32, i32, i32, ctypes.c_int]
     L.user_wait_sys.argtypes = [vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp]
     L.user_grid_wait.argtypes = [i32, i32, vp, vp, vp, vp, ctypes.c_int, u32, ctypes.c_int, u64, vp, vp, vp]
     L.user_grid_wait_only.argtypes = [i32, vp, vp, u32, ctypes.c_int, u32, u64, vp]
-    for f in (L.user_ring, L.user_ring_die_local, L.user_record, L.user_wait, L.user_record_sys, L.user_wait_sys,
+    for f in (L.user_ring, L.user_ring_die_local, L.user_ring_sys, L.user_record, L.user_wait, L.user_record_sys, L.user_wait_sys,
               L.user_grid_wait, L.user_grid_wait_only):
         f.restype = ctypes.c_int
     return L

@@ -58,7 +58,7 @@ int main(void) {
   F(cns_syncall_data_t, buf0_dev); F(cns_syncall_data_t, elems); F(cns_syncall_data_t, stream);
   F(cns_syncall_data_t, timeout_ms); F(cns_syncall_data_t, host_in); F(cns_syncall_data_t, elapsed_ms);
   F(cns_syncall_data_t, final_counter); F(cns_syncall_data_t, cluster_used); F(cns_syncall_data_t, barrier_variant);
-  F(cns_syncall_data_t, workspace_bytes); F(cns_syncall_data_t, launch_flags); F(cns_syncall_data_t, reserved);
+  F(cns_syncall_data_t, workspace_bytes); F(cns_syncall_data_t, launch_flags); F(cns_syncall_data_t, hard_step);
   printf("cns_record_info_t %zu\n", sizeof(cns_record_info_t));
   printf("cns_wait_info_t %zu\n", sizeof(cns_wait_info_t));
   F(cns_wait_info_t, is_clear);
@@ -85,7 +85,7 @@ def test_ctypes_structs_match_c_layout():
     S, P, W = _native.SyncallData, _native.Pipeline, _native.WaitInfo
     assert lay["cns_syncall_data_t"] == ctypes.sizeof(S)
     for f in ["buf0_dev", "elems", "stream", "timeout_ms", "host_in", "elapsed_ms", "final_counter",
-              "cluster_used", "barrier_variant", "workspace_bytes", "launch_flags", "reserved"]:
+              "cluster_used", "barrier_variant", "workspace_bytes", "launch_flags", "hard_step"]:
         assert lay[f"cns_syncall_data_t.{f}"] == getattr(S, f).offset, f
     assert lay["cns_record_info_t"] == ctypes.sizeof(_native.RecordInfo) == 8
     assert lay["cns_wait_info_t"] == ctypes.sizeof(W) == 16

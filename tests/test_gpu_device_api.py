@@ -1,7 +1,8 @@
 """The device-side API of include/cns_device.h inside user kernels
 (tests/fused/user_kernels.cu, built here into a library of its own): the soft
-barrier between ring rounds against the sequential oracle, over a subset of
-the grid and through the counter's wrap; records from user threads released
+barrier between ring rounds (one counter, die-local copies, and the
+system-scope form for participants on several GPUs) against the sequential
+oracle, over a subset of the grid and through the counter's wrap; records from user threads released
 by the library's stream wait; device waits on every mode against the oracle's
 rule; a grid-wide consumer on cns_cnt_wait_grid_dev against the oracle's
 pipeline checksums; and bounded timeouts (a barrier one CTA never reaches, a
@@ -29,7 +30,14 @@ def user(cns):
     return load_user_kernels()
 
 
-def _ring(cns, user, ctas, P, rounds, start=0, threads=256, short_cta=0xFFFFFFFF, timeout_ns=0, die_local=False):
+# the three forms of the device-side soft barrier: one counter (cns_syncall_soft), die-local counter copies
+# (cns_syncall_soft_die_local), and the system-scope form for participants on several GPUs
+# (cns_syncall_soft_sys; one GPU here, the same arithmetic at system scope)
+FORMS = {"counter": {}, "die_local": {"die_local": True}, "system_scope": {"sys": True}}
+
+
+def _ring(cns, user, ctas, P, rounds, start=0, threads=256, short_cta=0xFFFFFFFF, timeout_ns=0, die_local=False,
+          sys=False):
     import torch
     v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P, 4)
     b0 = to_dev_u32(np.vstack([v0, np.zeros((ctas - P, 4), np.uint32)]))
@@ -37,7 +45,7 @@ def _ring(cns, user, ctas, P, rounds, start=0, threads=256, short_cta=0xFFFFFFFF
     ws = cns.new_workspace(start_value=start, die_local=die_local)
     status = torch.full((ctas,), -1, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
-    launch = user.user_ring_die_local if die_local else user.user_ring
+    launch = user.user_ring_die_local if die_local else user.user_ring_sys if sys else user.user_ring
     rc = launch(ctas, threads, P, rounds, b0.data_ptr(), b1.data_ptr(), ws.data_ptr(), timeout_ns, short_cta,
                 status.data_ptr())
     assert rc == 0, rc
@@ -45,11 +53,12 @@ def _ring(cns, user, ctas, P, rounds, start=0, threads=256, short_cta=0xFFFFFFFF
     return v0, got, from_dev_u32(ws), status.cpu().numpy()
 
 
-@pytest.mark.parametrize("die_local", [False, True])
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("ctas,P,rounds,threads", [(148, 148, 10001, 256), (8, 8, 1000, 256), (111, 111, 777, 96),
                                                      (148, 64, 2001, 256), (5, 5, 3, 32), (1, 1, 10, 64)])
-def test_fused_soft_barrier_ring_matches_oracle(cns, user, ctas, P, rounds, threads, die_local):
-    v0, got, ws, status = _ring(cns, user, ctas, P, rounds, threads=threads, die_local=die_local)
+def test_fused_soft_barrier_ring_matches_oracle(cns, user, ctas, P, rounds, threads, form):
+    die_local = form == "die_local"
+    v0, got, ws, status = _ring(cns, user, ctas, P, rounds, threads=threads, **FORMS[form])
     want, fc, rc = oracle.syncall_run_ring(oracle.WL_RING_ROTATE, v0, rounds)
     assert rc == oracle.OK
     np.testing.assert_array_equal(got, want)
@@ -59,12 +68,12 @@ def test_fused_soft_barrier_ring_matches_oracle(cns, user, ctas, P, rounds, thre
     assert (status[:P] == 0).all() and (status[P:] == -1).all()   # CTAs past P never called it
 
 
-@pytest.mark.parametrize("die_local", [False, True])
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("P", [148, 111, 7])
-def test_fused_soft_barrier_through_the_wrap(cns, user, P, die_local):
+def test_fused_soft_barrier_through_the_wrap(cns, user, P, form):
     M = oracle.counter_modulus(P)
     start = M - 5 * P
-    v0, got, ws, status = _ring(cns, user, P, P, 12, start=start, die_local=die_local)
+    v0, got, ws, status = _ring(cns, user, P, P, 12, start=start, **FORMS[form])
     want, fc, rc = oracle.syncall_run_ring(oracle.WL_RING_ROTATE, v0, 12, start=start)
     assert rc == oracle.OK
     np.testing.assert_array_equal(got, want)
@@ -72,13 +81,13 @@ def test_fused_soft_barrier_through_the_wrap(cns, user, P, die_local):
     assert (status == 0).all()
 
 
-@pytest.mark.parametrize("die_local", [False, True])
-def test_fused_soft_barrier_times_out_when_a_cta_stops_short(cns, user, die_local):
+@pytest.mark.parametrize("form", FORMS)
+def test_fused_soft_barrier_times_out_when_a_cta_stops_short(cns, user, form):
     """CTA 5 takes one barrier fewer: the others give up on the last barrier
     after their 20 ms limit, with CNS_ERR_TIMEOUT in every CTA and in the
     workspace's status line, and no CTA is left waiting."""
     P = 8
-    v0, got, ws, status = _ring(cns, user, P, P, 4, short_cta=5, timeout_ns=20_000_000, die_local=die_local)
+    v0, got, ws, status = _ring(cns, user, P, P, 4, short_cta=5, timeout_ns=20_000_000, **FORMS[form])
     line = ws[32:36]
     assert int(line[0]) == cns.CNS_ERR_TIMEOUT and int(line[1]) == 1 and int(line[3]) != 5
     assert status[5] == 0

@@ -36,7 +36,7 @@ def garble_counters(ws, value):
 
 
 def run_ring(cns, mode, core, wl, launch_ctas, v0, rounds, used=0, ratio=0, start=0, threads=256,
-             cluster_dim=0, timeout_ms=0, check=True, variant=0, garble=None, launch_flags=0, ws=None):
+             cluster_dim=0, timeout_ms=0, check=True, variant=0, garble=None, launch_flags=0, ws=None, hard_step=0):
     import torch
     P, slots = v0.shape
     b0 = to_dev_u32(v0) if v0.size else None
@@ -50,7 +50,7 @@ def run_ring(cns, mode, core, wl, launch_ctas, v0, rounds, used=0, ratio=0, star
     d, rc = cns.run_syncall(mode, core, wl, launch_ctas, b0, b1, rounds, used_cores=used, aiv_ratio=ratio,
                             elems=slots, threads=threads, cluster_dim=cluster_dim, workspace=ws,
                             cta_status=status, timeout_ms=timeout_ms, check=check, variant=variant,
-                            launch_flags=launch_flags)
+                            launch_flags=launch_flags, hard_step=hard_step)
     torch.cuda.synchronize()
     final = from_dev_u32(b1 if rounds & 1 else b0).reshape(P, slots) if v0.size else v0.copy()
     return d, rc, final, status.cpu().numpy()
@@ -203,13 +203,13 @@ def test_workspace_reused_across_runs(cns):
 
 # --- Jacobi -------------------------------------------------------------------------------
 
-def run_jacobi(cns, u0, sweeps, ctas, mode=SOFT, threads=256, variant=0):
+def run_jacobi(cns, u0, sweeps, ctas, mode=SOFT, threads=256, variant=0, hard_step=0):
     import torch
     b0 = to_dev_f32(u0)
     b1 = torch.zeros_like(b0)
     ws = cns.new_workspace()
     d, rc = cns.run_syncall(mode, AIV, cns.CNS_WL_JACOBI, ctas, b0, b1, sweeps, elems=u0.size,
-                            threads=threads, workspace=ws, variant=variant)
+                            threads=threads, workspace=ws, variant=variant, hard_step=hard_step)
     out = (b1 if sweeps & 1 else b0).cpu().numpy()
     return d, out
 
@@ -549,6 +549,84 @@ def test_hard_path_without_the_cluster_attribute(cns, variant, wl):
 def test_launch_flags_outside_the_defined_bits_are_refused(cns):
     v0 = ci.ring_payload(3, 4, 4)
     d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_ROTATE, 4, v0, 3, check=False, launch_flags=2)
+    assert rc == cns.CNS_ERR_INVALID_VALUE
+
+
+# --- the hard path's paired-mbarrier step (the guide's intra-block flags, §5.1) -------------
+
+PAIRED = 1
+
+
+@pytest.mark.parametrize("variant", [0, 2, 5, 6])
+@pytest.mark.parametrize("C", [2, 4])
+def test_paired_step_ring_rotate_148(cns, variant, C):
+    """Members meet their cluster's rank 0 on shared-memory mbarriers; only rank 0 touches the counter."""
+    R = 20001
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, R, cluster_dim=C, variant=variant,
+                              hard_step=PAIRED)
+    want, _ = expect_ring(oracle.WL_RING_ROTATE, v0, R)
+    np.testing.assert_array_equal(got, want)
+    assert rc == 0 and d.device_status == 0 and d.cluster_used == C
+    if variant != FLIP:
+        assert d.final_counter == (R * (148 // C)) % oracle.counter_modulus(148 // C)
+    assert (st == cns.CNS_CTA_DONE).all()
+
+
+def test_paired_step_mix_37x3_and_affine(cns):
+    """MIX (37 groups of 1 AIC + 2 AIV CTAs, one cluster each) with the xorshift payload, and a ring-affine
+    run with ragged rows, both against the oracle."""
+    v0 = ci.ring_payload(ci.SEED_XORSHIFT, 111, 256)
+    d, rc, got, st = run_ring(cns, HARD, MIX, cns.CNS_WL_XORSHIFT, 37, v0, 10000, ratio=2, hard_step=PAIRED)
+    want, _ = expect_ring(oracle.WL_XORSHIFT, v0, 10000)
+    np.testing.assert_array_equal(got, want)
+    assert d.cluster_used == 3 and d.final_counter == 10000 * 37
+    np.testing.assert_array_equal(st >> 8, (np.arange(111) % 3 == 0).astype(np.int32))
+    v0 = ci.ring_payload(7, 16, 13)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_AFFINE, 16, v0, 301, cluster_dim=8, hard_step=PAIRED)
+    want, _ = expect_ring(oracle.WL_RING_AFFINE, v0, 301)
+    np.testing.assert_array_equal(got, want)
+    assert d.cluster_used == 8 and d.final_counter == 301 * 2
+
+
+def test_paired_step_jacobi(cns):
+    u0 = ci.jacobi_field(200003)
+    d, got = run_jacobi(cns, u0, 10, 64, mode=HARD, hard_step=PAIRED)
+    want, _, _ = oracle.syncall_run_jacobi(u0, 10, 64)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("rounds", [1, 3, 6])
+def test_paired_step_unzeroed_workspace_times_out(cns, rounds):
+    """A garbled counter puts the clusters' rank-0 CTAs in different epochs: their bounded waits give up,
+    each releases its members with the stop flag, and every CTA of a cluster reports the same outcome."""
+    v0 = ci.ring_payload(3, 8, 4)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, rounds, garble=1, timeout_ms=300,
+                              cluster_dim=4, check=False, hard_step=PAIRED)
+    assert rc == cns.CNS_ERR_TIMEOUT and d.device_status == cns.CNS_ERR_TIMEOUT
+    assert ((st & 0xFF) == cns.CNS_CTA_ABORTED).any()
+    assert len(set((st[:4] & 0xFF).tolist())) == 1 and len(set((st[4:] & 0xFF).tolist())) == 1
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_AFFINE, 8, v0, 5, cluster_dim=4, hard_step=PAIRED)
+    want, _ = expect_ring(oracle.WL_RING_AFFINE, v0, 5)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_paired_step_without_the_cluster_attribute(cns):
+    """Clusters of one: rank 0 has no members and arrives for itself."""
+    R = 3001
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, R, cluster_dim=4,
+                              launch_flags=cns.CNS_LAUNCH_NO_CLUSTER_ATTR, hard_step=PAIRED)
+    want, _ = expect_ring(oracle.WL_RING_ROTATE, v0, R)
+    np.testing.assert_array_equal(got, want)
+    assert rc == 0 and d.cluster_used == 1 and d.final_counter == (R * 148) % oracle.counter_modulus(148)
+
+
+def test_paired_step_is_refused_where_it_has_no_meaning(cns):
+    v0 = ci.ring_payload(3, 4, 4)
+    d, rc, got, st = run_ring(cns, SOFT, AIV, cns.CNS_WL_RING_ROTATE, 4, v0, 3, check=False, hard_step=PAIRED)
+    assert rc == cns.CNS_ERR_INVALID_VALUE
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_ROTATE, 4, v0, 3, check=False, hard_step=2)
     assert rc == cns.CNS_ERR_INVALID_VALUE
 
 
