@@ -764,9 +764,9 @@ def case_hard148_small(args):
     b1 = torch.zeros_like(b0)
     ws = cns.new_workspace()
     for _ in range(3):
-        cns.run_syncall(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1, 2000,
-                        elems=SLOTS_HEAD, workspace=ws)
-    print("case hard148-small: ok")
+        d, _ = cns.run_syncall(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1, 2000,
+                               elems=SLOTS_HEAD, workspace=ws)
+    print(f"case hard148-small: ok (clusters of {d.cluster_used} CTAs, as the device saw the launch)")
 
 
 def case_jacobi_small(args):
