@@ -577,7 +577,9 @@ PHASES = ("payload_load", "payload_store_issue", "release_fence", "near_incremen
 
 def round_budget(stamps):
     """Where one CTA's round goes, from cns_probe_round_phases stamps ([K rounds][P CTAs][8] ns): the mean
-    over rounds and CTAs of each phase, in ns.  The parts add up to the mean round (last stamp minus first).
+    over rounds and CTAs of each phase, in ns.  The parts add up to the mean stamped round (last stamp minus
+    first); the time from one round's last stamp to the next round's first is the probe's own bookkeeping
+    (saving the stamps), reported apart.
     The wait (from the near increment's value to the releasing count) is split at the moment the round's
     last arrival had passed its release fence (the latest stamp 3 of the round): the part before it is
     waiting for the last participant, the part after it the time the last increments took to land and be
@@ -592,6 +594,7 @@ def round_budget(stamps):
     out["wait_for_last_arrival"] = float(for_last.mean())
     out["wait_landing_and_detection"] = float((wait - for_last).mean())
     out["round"] = float((t[:, :, 7] - t[:, :, 0]).mean())
+    out["probe_bookkeeping"] = float((t[1:, :, 0] - t[:-1, :, 7]).mean()) if t.shape[0] > 1 else 0.0
     # the chain of the round's last arrival: its own phases up to its release fence, from the start of
     # its round
     k_idx = np.arange(t.shape[0])

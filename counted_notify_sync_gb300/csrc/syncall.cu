@@ -31,7 +31,9 @@ namespace cns {
 // last `stamp_rounds` rounds stay in shared memory until the run ends, so the
 // probe adds no memory operation to the chain it measures (only the timer
 // reads).  Per round and CTA:
-//   [0] round start
+//   [0] round start (taken afresh each round, after the previous round's
+//       stamps were saved, so the probe's own bookkeeping falls between
+//       rounds and in no phase)
 //   [1] the neighbour's row has arrived
 //   [2] the new row's stores are issued
 //   [3] the release fence is done (the stores performed)
@@ -39,7 +41,7 @@ namespace cns {
 //   [5] the count that releases the round has arrived (= [4] for the round's
 //       last arrival on the copy)
 //   [6] the acquire fence is done
-//   [7] the cursor is advanced (the next round's start)
+//   [7] the cursor is advanced
 constexpr int kPhaseStamps = 8;
 
 // The global timer, read only once `dep` (a loaded value) is known.
@@ -69,11 +71,10 @@ __global__ void __launch_bounds__(1024) round_phase_probe_kernel(const SyncallPa
     EpochCursor cursor{0u, 0u, false};
     const int64_t first = p.rounds - stamp_rounds;
     uint64_t t[kPhaseStamps];
-    t[7] = globaltimer_ns();
     bool stop = false;
     for (int64_t r = 0; r < p.rounds && !stop; ++r) {
         const bool odd = (r & 1) != 0;
-        t[0] = t[7];
+        t[0] = globaltimer_ns();
         const uint4 *from = p.mirror ? (r == 0 ? static_cast<const uint4 *>(p.buf0) + q : (odd ? m.src1 : m.src0))
                                      : static_cast<const uint4 *>(odd ? p.buf1 : p.buf0) + q;
         const uint4 v = ld_relaxed_gpu_v4(from);   // ring rotate: the row as it is
