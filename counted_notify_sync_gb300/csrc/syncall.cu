@@ -67,25 +67,27 @@ __global__ void __launch_bounds__(1024) round_phase_probe_kernel(const SyncallPa
     const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
     MirrorState m{};
     if (p.mirror)
-        m = mirror_setup(p.mirror, b, q);
+        m = mirror_setup(p.mirror);
     EpochCursor cursor{0u, 0u, false};
     const int64_t first = p.rounds - stamp_rounds;
     uint64_t t[kPhaseStamps];
     bool stop = false;
     for (int64_t r = 0; r < p.rounds && !stop; ++r) {
-        const bool odd = (r & 1) != 0;
+        const uint32_t k = static_cast<uint32_t>(r) & 1u;   // reads pair k (buffer k), writes the other
         t[0] = globaltimer_ns();
-        const uint4 *from = p.mirror ? (r == 0 ? static_cast<const uint4 *>(p.buf0) + q : (odd ? m.src1 : m.src0))
-                                     : static_cast<const uint4 *>(odd ? p.buf1 : p.buf0) + q;
+        const uint4 *from = p.mirror ? (r == 0 ? static_cast<const uint4 *>(p.buf0) + q
+                                               : mirror_pair(p.mirror, k) + ((m.near_bits >> k) & 1u) * kMirrorBlockRows + q)
+                                     : static_cast<const uint4 *>(k ? p.buf1 : p.buf0) + q;
         const uint4 v = ld_relaxed_gpu_v4(from);   // ring rotate: the row as it is
         t[1] = globaltimer_after(v.x ^ v.w);
         if (p.mirror) {
-            st_relaxed_gpu_v4(odd ? m.dst00 : m.dst10, v);
-            st_relaxed_gpu_v4(odd ? m.dst01 : m.dst11, v);
+            uint4 *dst = mirror_pair(p.mirror, k ^ 1u) + b;
+            st_relaxed_gpu_v4(dst, v);
+            st_relaxed_gpu_v4(dst + kMirrorBlockRows, v);
             if (r + 2 >= p.rounds)
-                st_relaxed_gpu_v4(static_cast<uint4 *>(odd ? p.buf0 : p.buf1) + b, v);
+                st_relaxed_gpu_v4(static_cast<uint4 *>(k ? p.buf0 : p.buf1) + b, v);
         } else {
-            st_relaxed_gpu_v4(static_cast<uint4 *>(odd ? p.buf0 : p.buf1) + b, v);
+            st_relaxed_gpu_v4(static_cast<uint4 *>(k ? p.buf0 : p.buf1) + b, v);
         }
         t[2] = globaltimer_ns();
         fence_release_gpu();
@@ -378,7 +380,9 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     prm.core_type = core_type;
     prm.solo = solo ? 1 : 0;
     // the per-die payload copies: die-local variant, one-uint4 rows, P <= 255, room in the workspace
-    prm.mirror = (prm.solo && ring && d->elems == 4 && d->barrier_variant == CNS_BARRIER_DIE_LOCAL &&
+    // the per-die payload copies: die-local variant, one-uint4 rows, at most CNS_SYNCALL_MIRROR_MAX_P ring
+    // participants (on the hard path every CTA), room in the workspace
+    prm.mirror = (ring && d->elems == 4 && d->barrier_variant == CNS_BARRIER_DIE_LOCAL &&
                   P <= CNS_SYNCALL_MIRROR_MAX_P && d->workspace_bytes >= CNS_SYNCALL_WORKSPACE_MIRROR_BYTES)
                      ? ws + CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES / 4
                      : nullptr;

@@ -335,56 +335,57 @@ constexpr uint32_t kMirrorPairWords = 2048;        // 8 KB: two 4 KB blocks
 constexpr uint32_t kMirrorBlockRows = 256;         // uint4 rows per 4 KB block
 constexpr uint32_t kMirrorTimingRow = kMirrorBlockRows - 1;   // never a payload row (P <= 255)
 
-// A participant's rows in the copies, worked out once: the row it reads in
-// each pair (its neighbour's, in the block on its own die) and the rows it
-// writes (its own, in both blocks).  Held as separate pointers and picked by
-// the round's parity with selects: an array indexed by the parity would sit
-// in local memory, and every round's payload load would first wait for a
-// local load of its address (measured: ~90 ns a round).
+// Which block of each pair is on this SM's die, as one word (bit k: block 1
+// of pair k is the near one).  The rows' addresses are worked out from it
+// each round with a few integer operations, so the state stays one register:
+// kept as an array of pointers indexed by the round's parity it went to local
+// memory (every payload load then first waited for a local load of its
+// address, ~90 ns a round), and as six pointers it made the hard kernel,
+// held to 64 registers by its 1024-thread bound, spill.
 struct MirrorState {
-    const uint4 *src0, *src1;   // pair 0 / pair 1: the neighbour's row, near block
-    uint4 *dst00, *dst01;       // pair 0: own row in block 0 / block 1
-    uint4 *dst10, *dst11;       // pair 1: own row in block 0 / block 1
+    uint32_t near_bits;
 };
 
-__device__ __forceinline__ MirrorState mirror_setup(uint32_t *mirror, uint32_t b, uint32_t q)
+__device__ __forceinline__ MirrorState mirror_setup(uint32_t *mirror)
 {
-    uint4 *blk[2][2];
-    bool far0[2];
+    MirrorState m{0u};
     for (int k = 0; k < 2; ++k) {
         uint4 *b0 = reinterpret_cast<uint4 *>(mirror + k * kMirrorPairWords);
         uint4 *b1 = b0 + kMirrorBlockRows;
-        blk[k][0] = b0;
-        blk[k][1] = b1;
         // time both blocks on their timing row (adds of 0: nothing changes)
-        far0[k] = copy_is_farther(reinterpret_cast<uint32_t *>(b0 + kMirrorTimingRow),
-                                  reinterpret_cast<uint32_t *>(b1 + kMirrorTimingRow));
+        if (copy_is_farther(reinterpret_cast<uint32_t *>(b0 + kMirrorTimingRow),
+                            reinterpret_cast<uint32_t *>(b1 + kMirrorTimingRow)))
+            m.near_bits |= 1u << k;
     }
-    MirrorState m;
-    m.src0 = (far0[0] ? blk[0][1] : blk[0][0]) + q;
-    m.src1 = (far0[1] ? blk[1][1] : blk[1][0]) + q;
-    m.dst00 = blk[0][0] + b;
-    m.dst01 = blk[0][1] + b;
-    m.dst10 = blk[1][0] + b;
-    m.dst11 = blk[1][1] + b;
     return m;
 }
 
-template <int WL>
-__device__ __forceinline__ void mirror_round(const SyncallParams &p, const MirrorState &m, uint32_t b, int64_t r)
+// Pair k's block 0 (block 1 follows it, kMirrorBlockRows rows on).
+__device__ __forceinline__ uint4 *mirror_pair(uint32_t *mirror, uint32_t k)
 {
-    const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
-    const bool odd = (r & 1) != 0;   // reads pair r & 1, writes the other
-    uint4 v = ld_relaxed_gpu_v4(r == 0 ? static_cast<const uint4 *>(p.buf0) + q : (odd ? m.src1 : m.src0));
+    return reinterpret_cast<uint4 *>(mirror) + k * 2u * kMirrorBlockRows;
+}
+
+// Round r of participant b: read the neighbour q's row of pair r & 1 from its
+// near block (buffer 0 in round 0), write the new row into both blocks of
+// the other pair (and, in the last two rounds, into the caller's buffer).
+template <int WL>
+__device__ __forceinline__ void mirror_round(const SyncallParams &p, MirrorState m, uint32_t b, uint32_t q, int64_t r)
+{
+    const uint32_t k = static_cast<uint32_t>(r) & 1u;
+    const uint4 *src = (r == 0) ? static_cast<const uint4 *>(p.buf0) + q
+                                : mirror_pair(p.mirror, k) + ((m.near_bits >> k) & 1u) * kMirrorBlockRows + q;
+    uint4 v = ld_relaxed_gpu_v4(src);
     const uint32_t rr = static_cast<uint32_t>(r);
     v.x = ring_op<WL>(v.x, rr);
     v.y = ring_op<WL>(v.y, rr);
     v.z = ring_op<WL>(v.z, rr);
     v.w = ring_op<WL>(v.w, rr);
-    st_relaxed_gpu_v4(odd ? m.dst00 : m.dst10, v);
-    st_relaxed_gpu_v4(odd ? m.dst01 : m.dst11, v);
+    uint4 *dst = mirror_pair(p.mirror, k ^ 1u) + b;
+    st_relaxed_gpu_v4(dst, v);
+    st_relaxed_gpu_v4(dst + kMirrorBlockRows, v);
     if (r + 2 >= p.rounds)
-        st_relaxed_gpu_v4(static_cast<uint4 *>(odd ? p.buf0 : p.buf1) + b, v);
+        st_relaxed_gpu_v4(static_cast<uint4 *>(k ? p.buf0 : p.buf1) + b, v);
 }
 
 // The soft rounds when thread 0 alone touches memory (no payload, or a row of
@@ -408,13 +409,14 @@ __device__ __forceinline__ void solo_rounds(const SyncallParams &p, uint32_t b, 
     MirrorState m{};
     const bool mirrored = (V == kBvDieLocal) && p.mirror != nullptr;
     if (mirrored)
-        m = mirror_setup(p.mirror, b, (b + 1u == p.P) ? 0u : b + 1u);
+        m = mirror_setup(p.mirror);
+    const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
     EpochCursor cursor{0u, 0u, false};
     bool stop = false;
     for (int64_t r = 0; r < p.rounds; ++r) {
         if (WL != CNS_WL_EMPTY) {
             if (mirrored) {
-                mirror_round<WL>(p, m, b, r);
+                mirror_round<WL>(p, m, b, q, r);
             } else {
                 const bool odd = (r & 1) != 0;
                 ring_phase<WL>(static_cast<const uint32_t *>(odd ? p.buf1 : p.buf0),
@@ -563,8 +565,21 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         if (!stop && p.rounds > 0)
             stop = soft_wait<V>(bar, pd, static_cast<uint32_t>(p.rounds - 1));
     } else {
+        // One-uint4 rings through the per-die payload copies (die-local
+        // variant, on a workspace with room for them): thread 0 moves the row.
+        constexpr bool kRing = WL == CNS_WL_RING_AFFINE || WL == CNS_WL_RING_ROTATE || WL == CNS_WL_XORSHIFT;
+        MirrorState m{};
+        const bool mirrored = kRing && V == kBvDieLocal && p.mirror != nullptr;
+        if (mirrored && threadIdx.x == 0)
+            m = mirror_setup(p.mirror);
+        const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
         for (int64_t r = 0; r < p.rounds; ++r) {
-            data_phase<WL>(p, r, b, js);
+            if (kRing && mirrored) {
+                if (threadIdx.x == 0)
+                    mirror_round<WL>(p, m, b, q, r);
+            } else {
+                data_phase<WL>(p, r, b, js);
+            }
             if constexpr (MODE == CNS_SYNCALL_SOFT)
                 stop = soft_barrier<V>(bar, cursor, static_cast<uint32_t>(r));
             else if constexpr (kPaired)

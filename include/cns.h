@@ -141,7 +141,7 @@ typedef enum {
 
 /* A die-local workspace of CNS_SYNCALL_WORKSPACE_MIRROR_BYTES (same 8 KB
  * alignment) also carries per-die copies of a ring payload of one uint4 per
- * participant: with CNS_BARRIER_DIE_LOCAL on the soft path and at most
+ * participant: with CNS_BARRIER_DIE_LOCAL (soft or hard path) and at most
  * CNS_SYNCALL_MIRROR_MAX_P participants, each round's rows are written into
  * two 4 KB blocks on different dies (bytes 8192..24575 of the workspace) and
  * every participant reads its neighbour's row from the block on its own die.

@@ -868,10 +868,11 @@ def test_round_phase_probe(cns):
     np.testing.assert_array_equal(from_dev_u32(b1).reshape(P, 4), want)
     t = st.cpu().numpy().reshape(K, P, 8)
     assert (np.diff(t, axis=2) >= 0).all()
-    assert (t[1:, :, 0] == t[:-1, :, 7]).all()     # a round starts where the last one closed
-    b = bench.round_budget(t)
+    assert (t[1:, :, 0] >= t[:-1, :, 7]).all()     # a round starts after the last one closed (the stamps'
+    b = bench.round_budget(t)                      # bookkeeping in between)
     parts = sum(b[k] for k in bench.PHASES)
     assert abs(parts - b["round"]) < 1.0
+    assert b["probe_bookkeeping"] >= 0.0
     assert abs(b["wait_for_last_arrival"] + b["wait_landing_and_detection"] - b["wait"]) < 1.0
     assert 100.0 < b["round"] < 100000.0
     # the same on a workspace without room for the payload copies (the caller's buffers every round)
