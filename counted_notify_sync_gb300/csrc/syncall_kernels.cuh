@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "cns.h"
 #include "cns_device.cuh"
@@ -565,29 +566,47 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         if (!stop && p.rounds > 0)
             stop = soft_wait<V>(bar, pd, static_cast<uint32_t>(p.rounds - 1));
     } else {
-        // One-uint4 rings through the per-die payload copies (die-local
-        // variant, on a workspace with room for them): thread 0 moves the row.
-        constexpr bool kRing = WL == CNS_WL_RING_AFFINE || WL == CNS_WL_RING_ROTATE || WL == CNS_WL_XORSHIFT;
-        MirrorState m{};
-        const bool mirrored = kRing && V == kBvDieLocal && p.mirror != nullptr;
-        if (mirrored && threadIdx.x == 0)
-            m = mirror_setup(p.mirror);
-        const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
-        for (int64_t r = 0; r < p.rounds; ++r) {
-            if (kRing && mirrored) {
+        // The rounds, in one of two forms fixed at compile time, so that the
+        // form without payload copies carries none of their state (a run-time
+        // branch inside one loop kept it live and made the 1 KB-row rings of
+        // this kernel spill).  With copies (one-uint4 rings of the die-local
+        // variant, on a workspace with room for them) thread 0 moves the row.
+        auto rounds = [&](auto with_copies) {
+            constexpr bool kCopies = decltype(with_copies)::value;
+            MirrorState m{0u};
+            uint32_t q = 0;
+            if constexpr (kCopies) {
                 if (threadIdx.x == 0)
-                    mirror_round<WL>(p, m, b, q, r);
-            } else {
-                data_phase<WL>(p, r, b, js);
+                    m = mirror_setup(p.mirror);
+                q = (b + 1u == p.P) ? 0u : b + 1u;
             }
-            if constexpr (MODE == CNS_SYNCALL_SOFT)
-                stop = soft_barrier<V>(bar, cursor, static_cast<uint32_t>(r));
-            else if constexpr (kPaired)
-                stop = paired_barrier<V>(bar, cursor, static_cast<uint32_t>(r), &s_flag, pb);
+            bool halt = false;
+            for (int64_t r = 0; r < p.rounds; ++r) {
+                if constexpr (kCopies) {
+                    if (threadIdx.x == 0)
+                        mirror_round<WL>(p, m, b, q, r);
+                } else {
+                    data_phase<WL>(p, r, b, js);
+                }
+                if constexpr (MODE == CNS_SYNCALL_SOFT)
+                    halt = soft_barrier<V>(bar, cursor, static_cast<uint32_t>(r));
+                else if constexpr (kPaired)
+                    halt = paired_barrier<V>(bar, cursor, static_cast<uint32_t>(r), &s_flag, pb);
+                else
+                    halt = hard_barrier<V>(bar, cursor, static_cast<uint32_t>(r), r == 0, &s_flag, &s_epoch);
+                if (halt)
+                    break;
+            }
+            return halt;
+        };
+        constexpr bool kRing = WL == CNS_WL_RING_AFFINE || WL == CNS_WL_RING_ROTATE || WL == CNS_WL_XORSHIFT;
+        if constexpr (kRing && V == kBvDieLocal) {
+            if (p.mirror != nullptr)
+                stop = rounds(std::true_type{});
             else
-                stop = hard_barrier<V>(bar, cursor, static_cast<uint32_t>(r), r == 0, &s_flag, &s_epoch);
-            if (stop)
-                break;
+                stop = rounds(std::false_type{});
+        } else {
+            stop = rounds(std::false_type{});
         }
         if constexpr (MODE == CNS_SYNCALL_HARD)
             stop = hard_barrier_finish(&s_flag);
