@@ -768,7 +768,7 @@ def case_soft148_small(args):
 
 
 def case_hard148_small(args):
-    """Three launches of the hard-path kernel with 2000 rounds each (profiling)."""
+    """Three launches of the hard-path kernel (bench's --variant) with 2000 rounds each (profiling)."""
     import torch
     import counted_notify_sync_gb300 as cns
     cns.build()
@@ -778,7 +778,7 @@ def case_hard148_small(args):
     ws = cns.new_workspace()
     for _ in range(3):
         d, _ = cns.run_syncall(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1, 2000,
-                               elems=SLOTS_HEAD, workspace=ws)
+                               elems=SLOTS_HEAD, workspace=ws, variant=args.variant)
     print(f"case hard148-small: ok (clusters of {d.cluster_used} CTAs, as the device saw the launch)")
 
 
