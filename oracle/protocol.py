@@ -32,8 +32,9 @@ The last two exist to show that the explorer does catch broken protocols.
 
 The later explorers take the same approach to the library's other
 protocols: the two-level (cluster) barrier, the sense-flip counter, the
-one-barrier hard path, the die-local counter copies, and the two-stream
-counted-notify pipeline's handshakes (explore_pipeline).
+one-barrier hard path, its paired gather / release step (explore_paired),
+the die-local counter copies, and the two-stream counted-notify pipeline's
+handshakes (explore_pipeline).
 """
 from __future__ import annotations
 
@@ -360,6 +361,104 @@ def explore_hard_one_barrier(P: int, C: int, rounds: int, M: int | None = None, 
                 leader = grp[0]
                 tgt = t if lead else (leader[2] if leader[0] == 0 else leader[3])
                 put((1, 0, 0, tgt))
+        if not succ:
+            if all(p[0] == rounds for p in parts):
+                res.completed += 1
+            else:
+                res.deadlocks += 1
+        stack.extend(succ)
+    return res
+
+
+# The hard path's paired step -------------------------------------------------
+#
+# The guide's MIX hard path pairs each AIC core with its AIV cores on
+# intra-block flags (SYNCALL §5.1): the AIVs set a flag the AIC waits for, the
+# AIC takes part in the cross-core step, then sets a flag each AIV waits for.
+# Participant i belongs to group i // C; its rank 0 is the leader.  A member's
+# barrier k is one arrival on its leader's gather count, then a wait until the
+# leader has released round k.  The leader's barrier k is a wait until all
+# C - 1 members have arrived for round k, then the device-wide step on the
+# counter (one arrival per group, the pages' arithmetic over the groups), then
+# the release of its members.
+#
+#   wait_gather=False     the leader arrives on the counter without waiting
+#                         for its members (a planted mistake)
+#   poll_first=False      the leader releases its members before its poll of
+#                         the counter has seen the round (a planted mistake)
+#   members_wait=False    members leave without waiting for the release (a
+#                         planted mistake)
+
+def explore_paired(P: int, C: int, rounds: int, M: int | None = None, start: int = 0,
+                   max_states: int = 2_000_000, wait_gather: bool = True, poll_first: bool = True,
+                   members_wait: bool = True) -> Result:
+    """All interleavings of the paired (gather / release) hard step."""
+    assert P % C == 0
+    G = P // C
+    arith = Arith("modular", G, M if M is not None else 4 * G)
+    res = Result()
+    # participant: (k barriers finished, phase, target)
+    #   member  phase 0 before barrier k, 1 arrived on the gather count, waiting for the release
+    #   leader  phase 0 before barrier k, 1 in it waiting for the gather, 3 polling the counter
+    # per group: the members' gather arrivals so far, and the rounds released so far
+    init = (start % arith.M, (0,) * G, (0,) * G, tuple((0, 0, 0) for _ in range(P)))
+    seen = set()
+    stack = [init]
+
+    def arrived(m, k):
+        return m[0] > k or (m[0] == k and m[1] >= 1)
+
+    while stack:
+        state = stack.pop()
+        if state in seen:
+            continue
+        seen.add(state)
+        res.states += 1
+        if res.states > max_states:
+            raise RuntimeError("state space larger than max_states")
+        c, gathered, released, parts = state
+        succ = []
+
+        def leave(i, k):
+            if not all(arrived(m, k) for m in parts):
+                res.safety_violations += 1
+            return parts[:i] + ((k + 1, 0, 0),) + parts[i + 1:]
+
+        for i, (k, ph, t) in enumerate(parts):
+            if k == rounds:
+                continue
+            g, lead = i // C, (i % C == 0)
+
+            def put(v, nc=c, ng=gathered, nr=released):
+                succ.append((nc, ng, nr, parts[:i] + (v,) + parts[i + 1:]))
+
+            if not lead:
+                if ph == 0:
+                    ng = gathered[:g] + (gathered[g] + 1,) + gathered[g + 1:]
+                    put((k, 1, 0), ng=ng)
+                elif not members_wait or released[g] >= k + 1:
+                    succ.append((c, gathered, released, leave(i, k)))
+                continue
+            if ph == 0:
+                put((k, 1, 0))
+            elif ph == 1:
+                if wait_gather and gathered[g] < (k + 1) * (C - 1):
+                    continue
+                before = c
+                if (before - start - k * G) % arith.M >= G:
+                    res.epoch_violations += 1
+                tgt = arith.target(before)
+                if poll_first:
+                    put((k, 3, tgt), nc=arith.arrive(c))
+                else:
+                    # the members are released at once; the leader still polls
+                    nr = released[:g] + (k + 1,) + released[g + 1:]
+                    put((k, 3, tgt), nc=arith.arrive(c), nr=nr)
+            elif ph == 3:
+                if not arith.reached(c, t):
+                    continue
+                nr = released[:g] + (max(released[g], k + 1),) + released[g + 1:]
+                succ.append((c, gathered, nr, leave(i, k)))
         if not succ:
             if all(p[0] == rounds for p in parts):
                 res.completed += 1

@@ -160,6 +160,37 @@ def test_hard_one_barrier_wrong_member_prediction_is_caught(step):
 
 # --- die-local counter copies (variants 5 and 8) ------------------------------------
 
+# --- the hard path's paired gather / release step (SYNCALL §5.1's intra-block flags) -------
+
+from oracle.protocol import explore_paired  # noqa: E402
+
+
+@pytest.mark.parametrize("P,C", [(2, 2), (4, 2), (4, 4), (6, 2), (6, 3), (8, 2), (8, 4)])
+@pytest.mark.parametrize("R", [1, 2, 3])
+def test_paired_step_safe_and_live(P, C, R):
+    res = explore_paired(P, C, R)
+    assert res.ok and res.completed == 1
+
+
+@pytest.mark.parametrize("start_mult", [1, 3])
+def test_paired_step_from_an_aligned_start_near_the_wrap(start_mult):
+    G = 2
+    M = 4 * G
+    assert explore_paired(4, 2, 3, M=M, start=M - start_mult * G).ok
+
+
+def test_paired_step_misaligned_start_is_caught():
+    assert not explore_paired(4, 2, 2, start=1).ok
+
+
+@pytest.mark.parametrize("mistake", [{"wait_gather": False}, {"poll_first": False}, {"members_wait": False}])
+def test_paired_step_planted_mistakes_are_caught(mistake):
+    """A leader that arrives before its members, a leader that releases them before the round is seen, and
+    members that do not wait for the release: each lets someone leave a barrier early."""
+    res = explore_paired(4, 2, 2, **mistake)
+    assert res.safety_violations > 0
+
+
 from oracle.protocol import explore_die_local  # noqa: E402
 
 NEARS = [(0, 1), (1, 0), (0, 1, 1), (0, 0, 1), (0, 1, 0, 1), (0, 0), (1, 1, 1)]
