@@ -152,6 +152,11 @@ def test_syncall_argument_checks(built):
     assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # die-local needs 8 KB
     d.barrier_variant, d.workspace_bytes = 0, 256
     assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # workspace too small
+    d.workspace_bytes, d.hard_step = 0, cns.CNS_HARD_STEP_PAIRED_MBARRIER
+    assert cns.syncall_run(1, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # paired step on the soft path
+    d.hard_step = 2
+    assert cns.syncall_run(0, 0, 0, 0, 1, d) == cns.CNS_ERR_INVALID_VALUE          # no such hard step
+    d.hard_step = 0
     assert L.syncall_workspace_init(None, 512, 0, None) == cns.CNS_ERR_NULL_PTR
     assert L.syncall_workspace_init(0x1000, 511, 0, None) == cns.CNS_ERR_INVALID_VALUE
 
