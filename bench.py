@@ -323,7 +323,7 @@ def secondary(cns, torch, peaks):
         v0 = ci.ring_payload(1, P, slots)
         b0 = torch.from_numpy(v0.view(np.int32).copy()).cuda() if v0.size else None
         b1 = torch.zeros_like(b0) if v0.size else None
-        ws = cns.new_workspace()
+        ws = cns.new_workspace(participants=P, elems=slots)   # room for the die-local payload copies
         runs = []
         for _ in range(3):
             ms, (d, rc) = timed_run(torch, lambda: cns.run_syncall(

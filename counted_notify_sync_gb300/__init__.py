@@ -26,17 +26,23 @@ def _torch():
     return torch
 
 
-def new_workspace(device=None, start_value: int = 0, stream=None, die_local: bool = True, mirror: bool = True):
-    """An initialised SYNCALL workspace on `device`: CNS_SYNCALL_WORKSPACE_MIRROR_BYTES long (usable by every
-    barrier variant, with room for the die-local variant's per-die payload copies), or
-    CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES with mirror=False, or the minimal CNS_SYNCALL_WORKSPACE_BYTES with
-    die_local=False.  The die-local sizes start on a CNS_SYNCALL_DIE_LOCAL_ALIGN boundary, so that the two
-    copies of each counter sit on different dies."""
+def new_workspace(device=None, start_value: int = 0, stream=None, die_local: bool = True, mirror: bool = True,
+                  participants: int | None = None, elems: int | None = None):
+    """An initialised SYNCALL workspace on `device`, usable by every barrier variant.  With die_local (the
+    default) it starts on a CNS_SYNCALL_DIE_LOCAL_ALIGN boundary, so that the two copies of each counter sit
+    on different dies, and has room for the die-local variant's per-die payload copies: of rows of one uint4
+    and up to CNS_SYNCALL_MIRROR_MAX_P participants (CNS_SYNCALL_WORKSPACE_MIRROR_BYTES), or, given
+    participants and elems, of that ring (syncall_workspace_bytes).  mirror=False gives
+    CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES, die_local=False the minimal CNS_SYNCALL_WORKSPACE_BYTES."""
     torch = _torch()
     if not die_local:
         ws = torch.empty(_native.CNS_SYNCALL_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device or "cuda")
     else:
         nbytes = _native.CNS_SYNCALL_WORKSPACE_MIRROR_BYTES if mirror else _native.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES
+        if mirror and participants is not None and elems is not None:
+            rc, need = _native.syncall_workspace_bytes(participants, elems)
+            _native.check(rc, "syncall_workspace_bytes")
+            nbytes = max(nbytes, need)
         align = _native.CNS_SYNCALL_DIE_LOCAL_ALIGN
         raw = torch.empty((nbytes + align) // 4, dtype=torch.int32, device=device or "cuda")
         skip = (-raw.data_ptr()) % align // 4

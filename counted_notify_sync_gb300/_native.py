@@ -117,6 +117,7 @@ class Pipeline(Structure):
 
 _SIGS = {
     "syncall_workspace_init": (c_int, [c_void_p, c_size_t, c_uint32, c_void_p]),
+    "syncall_workspace_bytes": (c_int, [c_int32, c_int64, POINTER(c_size_t)]),
     "syncall_run": (c_int, [c_int, c_int, c_int32, c_int32, c_int64, POINTER(SyncallData)]),
     "syncall_read_workspace": (c_int, [c_void_p, c_void_p, POINTER(c_uint32), POINTER(c_uint32), POINTER(c_int32)]),
     "cntnotify_create": (c_int, [POINTER(c_void_p), c_uint64]),
@@ -268,6 +269,13 @@ def cntnotify_query_status(h):
     st, c = c_int32(0), c_uint32(0)
     rc = lib().cntnotify_query_status(h, ctypes.byref(st), ctypes.byref(c))
     return rc, st.value, c.value
+
+
+def syncall_workspace_bytes(participants: int, elems: int, out: bool = True):
+    """(code, bytes); out=False passes a NULL bytes pointer."""
+    v = c_size_t(0)
+    rc = lib().syncall_workspace_bytes(participants, elems, ctypes.byref(v) if out else None)
+    return rc, v.value
 
 
 def cntnotify_enable_peer(h, peer_device: int) -> int:

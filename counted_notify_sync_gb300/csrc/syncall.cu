@@ -66,24 +66,29 @@ __global__ void __launch_bounds__(1024) round_phase_probe_kernel(const SyncallPa
     choose_near_copy(bar);
     const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
     MirrorState m{};
-    if (p.mirror)
-        m = mirror_setup(p.mirror);
+    uint32_t q_slot = 0, b_slot = 0;   // one-uint4 rows
+    if (p.mirror) {
+        q_slot = mirror_slot(p, q, 1u);
+        b_slot = mirror_slot(p, b, 1u);
+        m = mirror_setup(p, q_slot);
+    }
     EpochCursor cursor{0u, 0u, false};
     const int64_t first = p.rounds - stamp_rounds;
     uint64_t t[kPhaseStamps];
     bool stop = false;
     for (int64_t r = 0; r < p.rounds && !stop; ++r) {
-        const uint32_t k = static_cast<uint32_t>(r) & 1u;   // reads pair k (buffer k), writes the other
+        const uint32_t k = static_cast<uint32_t>(r) & 1u;   // reads region k (buffer k), writes the other
+        uint4 *base = reinterpret_cast<uint4 *>(p.mirror);
         t[0] = globaltimer_ns();
         const uint4 *from = p.mirror ? (r == 0 ? static_cast<const uint4 *>(p.buf0) + q
-                                               : mirror_pair(p.mirror, k) + ((m.near_bits >> k) & 1u) * kMirrorBlockRows + q)
+                                               : base + k * p.mirror_region4 + q_slot + ((m.near_bits >> k) & 1u) * kMirrorBlock4)
                                      : static_cast<const uint4 *>(k ? p.buf1 : p.buf0) + q;
         const uint4 v = ld_relaxed_gpu_v4(from);   // ring rotate: the row as it is
         t[1] = globaltimer_after(v.x ^ v.w);
         if (p.mirror) {
-            uint4 *dst = mirror_pair(p.mirror, k ^ 1u) + b;
+            uint4 *dst = base + (k ^ 1u) * p.mirror_region4 + b_slot;
             st_relaxed_gpu_v4(dst, v);
-            st_relaxed_gpu_v4(dst + kMirrorBlockRows, v);
+            st_relaxed_gpu_v4(dst + kMirrorBlock4, v);
             if (r + 2 >= p.rounds)
                 st_relaxed_gpu_v4(static_cast<uint4 *>(k ? p.buf0 : p.buf1) + b, v);
         } else {
@@ -128,6 +133,26 @@ __global__ void __launch_bounds__(1024) round_phase_probe_kernel(const SyncallPa
 // Word offsets of the second copies of the counters (die-local variant).
 constexpr uint32_t kSoftCopyWord = CNS_SYNCALL_REPLICA_OFFSET / 4;
 constexpr uint32_t kHardCopyWord = (CNS_SYNCALL_REPLICA_OFFSET + 2 * CNS_SYNCALL_LINE_BYTES) / 4;
+
+// The per-die payload copies' layout for P rows of `elems` uint32 (see
+// mirror_slot): rows per 4 KB block and 8 KB pairs per region.  False when
+// the rows cannot be copied: not a whole number of 16-byte units, or longer
+// than a block less its timing slot (4080 bytes).
+static bool mirror_layout(uint32_t P, int64_t elems, uint32_t *rows, uint32_t *pairs)
+{
+    if (P == 0 || elems < 4 || (elems & 3) != 0 || elems / 4 > kMirrorTiming4)
+        return false;
+    const uint32_t row4 = static_cast<uint32_t>(elems / 4);
+    *rows = kMirrorTiming4 / row4;
+    *pairs = (P + *rows - 1) / *rows;
+    return true;
+}
+
+// Workspace bytes for the die-local counters and `pairs` pairs per region.
+static uint64_t mirror_workspace_bytes(uint32_t pairs)
+{
+    return CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES + 2ull * pairs * kMirrorPair4 * 16u;
+}
 
 __global__ void workspace_init_kernel(uint32_t *ws, uint32_t n_words, uint32_t start, int with_copies)
 {
@@ -235,6 +260,19 @@ extern "C" int syncall_read_workspace(const void *ws_dev, cns_stream_t stream, u
         *status = static_cast<int32_t>(w[CNS_SYNCALL_LINE_BYTES / 4]);
     if (hard_counter)
         *hard_counter = w[2 * CNS_SYNCALL_LINE_BYTES / 4];
+    return CNS_SUCCESS;
+}
+
+extern "C" int syncall_workspace_bytes(int32_t participants, int64_t elems, size_t *bytes)
+{
+    if (!bytes)
+        return CNS_ERR_NULL_PTR;
+    if (participants < 1 || elems < 0)
+        return CNS_ERR_INVALID_VALUE;
+    uint32_t rows = 0, pairs = 0;
+    *bytes = mirror_layout(static_cast<uint32_t>(participants), elems, &rows, &pairs)
+                 ? static_cast<size_t>(mirror_workspace_bytes(pairs))
+                 : static_cast<size_t>(CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES);
     return CNS_SUCCESS;
 }
 
@@ -379,13 +417,15 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     prm.group = static_cast<uint32_t>(group);
     prm.core_type = core_type;
     prm.solo = solo ? 1 : 0;
-    // the per-die payload copies: die-local variant, one-uint4 rows, P <= 255, room in the workspace
-    // the per-die payload copies: die-local variant, one-uint4 rows, at most CNS_SYNCALL_MIRROR_MAX_P ring
-    // participants (on the hard path every CTA), room in the workspace
-    prm.mirror = (ring && d->elems == 4 && d->barrier_variant == CNS_BARRIER_DIE_LOCAL &&
-                  P <= CNS_SYNCALL_MIRROR_MAX_P && d->workspace_bytes >= CNS_SYNCALL_WORKSPACE_MIRROR_BYTES)
-                     ? ws + CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES / 4
-                     : nullptr;
+    // the per-die payload copies: die-local variant, a ring whose rows can be copied (P rows; on the hard
+    // path every CTA is a participant), room for them in the workspace
+    uint32_t mrows = 0, mpairs = 0;
+    const bool copies = ring && d->barrier_variant == CNS_BARRIER_DIE_LOCAL &&
+                        mirror_layout(P, d->elems, &mrows, &mpairs) &&
+                        d->workspace_bytes >= mirror_workspace_bytes(mpairs);
+    prm.mirror = copies ? ws + CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES / 4 : nullptr;
+    prm.mirror_rows = copies ? mrows : 0u;
+    prm.mirror_region4 = copies ? mpairs * kMirrorPair4 : 0u;
     if (mode == CNS_SYNCALL_SOFT) {
         prm.bar.ctr = ws;
         prm.bar.ctr2 = ws + kSoftCopyWord;
@@ -521,9 +561,12 @@ extern "C" int cns_probe_round_phases(int32_t ctas, int32_t threads, int64_t rou
     prm.P = static_cast<uint32_t>(ctas);
     prm.group = 1;
     prm.solo = 1;
-    prm.mirror = (workspace_bytes >= CNS_SYNCALL_WORKSPACE_MIRROR_BYTES && ctas <= CNS_SYNCALL_MIRROR_MAX_P)
-                     ? ws + CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES / 4
-                     : nullptr;
+    uint32_t mrows = 0, mpairs = 0;
+    const bool copies = mirror_layout(static_cast<uint32_t>(ctas), 4, &mrows, &mpairs) &&
+                        workspace_bytes >= mirror_workspace_bytes(mpairs);
+    prm.mirror = copies ? ws + CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES / 4 : nullptr;
+    prm.mirror_rows = copies ? mrows : 0u;
+    prm.mirror_region4 = copies ? mpairs * kMirrorPair4 : 0u;
     void *args[] = {&prm, &stamps_dev, &stamp_rounds};
     CNS_CUDA(cudaLaunchCooperativeKernel(k, dim3(ctas), dim3(threads), args, smem, s));
     return CNS_SUCCESS;

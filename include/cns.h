@@ -139,16 +139,20 @@ typedef enum {
 #define CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES 8192
 #define CNS_SYNCALL_DIE_LOCAL_ALIGN 8192
 
-/* A die-local workspace of CNS_SYNCALL_WORKSPACE_MIRROR_BYTES (same 8 KB
- * alignment) also carries per-die copies of a ring payload of one uint4 per
- * participant: with CNS_BARRIER_DIE_LOCAL (soft or hard path) and at most
- * CNS_SYNCALL_MIRROR_MAX_P participants, each round's rows are written into
- * two 4 KB blocks on different dies (bytes 8192..24575 of the workspace) and
- * every participant reads its neighbour's row from the block on its own die.
- * Round 0 reads buffer 0 and the last two rounds also write the caller's
- * buffers, so buf0_dev and buf1_dev end exactly as without the copies; the
- * rounds in between leave them untouched.  The blocks need no
- * initialisation. */
+/* A die-local workspace (same 8 KB alignment) can also carry per-die copies
+ * of a ring payload, used with CNS_BARRIER_DIE_LOCAL (soft or hard path) when
+ * the rows are a whole number of 16-byte units, at most 4080 bytes, and the
+ * workspace is at least syncall_workspace_bytes(P, elems) long.  After the
+ * die-local counters come two regions, one per round parity, each a run of
+ * 8 KB pairs of 4 KB blocks; row p is written into slot p % rows of BOTH
+ * blocks of pair p / rows (rows = floor(4080 / row bytes); the last 16 bytes
+ * of each block are reserved).  The two blocks of a pair sit on different
+ * dies, and every participant reads its neighbour's row from the block on its
+ * own die.  Round 0 reads buffer 0 and the last two rounds also write the
+ * caller's buffers, so buf0_dev and buf1_dev end exactly as without the
+ * copies; the rounds in between leave them untouched.  The blocks need no
+ * initialisation.  CNS_SYNCALL_WORKSPACE_MIRROR_BYTES is the size for rows of
+ * one uint4 and up to CNS_SYNCALL_MIRROR_MAX_P participants. */
 #define CNS_SYNCALL_WORKSPACE_MIRROR_BYTES 24576
 #define CNS_SYNCALL_MIRROR_MAX_P 255
 
@@ -241,6 +245,17 @@ typedef enum {
  * Errors: NULL_PTR, INVALID_VALUE (size or alignment), CUDA.
  */
 int syncall_workspace_init(void *ws_dev, size_t bytes, uint32_t start_value, cns_stream_t stream);
+
+/*
+ * syncall_workspace_bytes -- the workspace size that lets a die-local run of
+ * `participants` ring rows of `elems` uint32 use the per-die payload copies
+ * (see above): CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES plus two regions of
+ * ceil(participants / floor(4080 / (4 * elems))) 8 KB pairs; for rows that
+ * cannot be copied (elems not a multiple of 4, or above 1020), the die-local
+ * size alone.  Host only, no CUDA call.
+ * Errors: NULL_PTR (bytes), INVALID_VALUE (participants < 1, elems < 0).
+ */
+int syncall_workspace_bytes(int32_t participants, int64_t elems, size_t *bytes);
 
 /* Description of one syncall_run: the launch, the payload and the outputs.
  * Fields marked (in) are read, (out) are written by syncall_run. */

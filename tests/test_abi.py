@@ -200,3 +200,18 @@ def test_python_constants_match_the_header():
     assert found >= 10
     assert _native.CNS_SYNCALL_DIE_LOCAL_ALIGN == 8192
     assert (_native.CNS_PIPE_WAIT_STREAM, _native.CNS_PIPE_WAIT_IN_KERNEL) == (0, 1)
+
+
+def test_workspace_bytes_for_the_payload_copies(built):
+    """The die-local workspace size that makes room for the per-die payload copies (host only)."""
+    rows = lambda slots: 255 // (slots // 4)   # noqa: E731  (rows per 4 KB block)
+    for P, slots in [(148, 4), (255, 4), (256, 4), (8, 256), (111, 256), (5, 1020), (4864, 4)]:
+        rc, nbytes = cns.syncall_workspace_bytes(P, slots)
+        pairs = -(-P // rows(slots))
+        assert rc == 0 and nbytes == cns.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES + 2 * pairs * 8192
+    for P, slots in [(8, 1024), (8, 6), (8, 0)]:
+        assert cns.syncall_workspace_bytes(P, slots) == (0, cns.CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES)
+    assert cns.syncall_workspace_bytes(148, 4)[1] == cns.CNS_SYNCALL_WORKSPACE_MIRROR_BYTES
+    assert cns.syncall_workspace_bytes(0, 4)[0] == cns.CNS_ERR_INVALID_VALUE
+    assert cns.syncall_workspace_bytes(8, -1)[0] == cns.CNS_ERR_INVALID_VALUE
+    assert cns.syncall_workspace_bytes(8, 4, out=False)[0] == cns.CNS_ERR_NULL_PTR

@@ -42,7 +42,7 @@ def run_ring(cns, mode, core, wl, launch_ctas, v0, rounds, used=0, ratio=0, star
     b0 = to_dev_u32(v0) if v0.size else None
     b1 = torch.zeros_like(b0) if v0.size else None
     if ws is None:
-        ws = cns.new_workspace(start_value=start)
+        ws = cns.new_workspace(start_value=start, participants=P, elems=slots)
     if garble is not None:
         garble_counters(ws, garble)
     group = (1 + (ratio or 1)) if core == MIX else 1
@@ -773,20 +773,22 @@ def test_new_workspace_is_aligned_for_die_local_copies(cns):
 
 # --- rounds on thread 0 alone, and the die-local payload copies ----------------------------
 
-def _both_buffers(cns, wl, v0, R, variant, ws_bytes_kind, mode=SOFT):
+def _both_buffers(cns, wl, v0, R, variant, ws_bytes_kind, mode=SOFT, threads=256):
     import torch
     P = v0.shape[0]
     b0 = to_dev_u32(v0)
     b1 = torch.zeros_like(b0)
     if ws_bytes_kind == "mirror":
         ws = cns.new_workspace()
+    elif ws_bytes_kind == "sized":
+        ws = cns.new_workspace(participants=P, elems=v0.shape[1])
     elif ws_bytes_kind == "die_local":
         ws = cns.new_workspace(mirror=False)
     else:
         ws = cns.new_workspace(die_local=False)
     status = torch.zeros(P, dtype=torch.int32, device="cuda")
     d, rc = cns.run_syncall(mode, AIV, wl, P, b0, b1, R, elems=v0.shape[1], workspace=ws, cta_status=status,
-                            variant=variant)
+                            variant=variant, threads=threads)
     assert rc == 0 and d.device_status == 0 and (status.cpu().numpy() == cns.CNS_CTA_DONE).all()
     M = oracle.counter_modulus(P)
     if mode == SOFT:
@@ -798,22 +800,40 @@ WLS = {"rotate": (2, oracle.WL_RING_ROTATE), "affine": (1, oracle.WL_RING_AFFINE
 
 
 @pytest.mark.parametrize("wl", sorted(WLS))
-@pytest.mark.parametrize("P", [1, 2, 3, 148, 255, 256])
+@pytest.mark.parametrize("P", [1, 2, 3, 148, 255, 256, 600])
 @pytest.mark.parametrize("R", [1, 2, 3, 8, 1001])
 def test_one_uint4_rings_through_the_payload_copies(cns, wl, P, R):
     """Rows of one uint4 on the die-local variant with a mirror-size workspace
-    (per-die payload copies up to 255 participants; 256 runs without them):
-    both caller buffers end as the oracle's last two states -- buffer R & 1
-    holds round R's state and the other round R - 1's -- exactly as on a plain
-    die-local workspace and on the guide's counter poll."""
+    (per-die payload copies up to 255 participants; more run without them) and
+    with one sized for the run (copies in as many 8 KB pairs as the rows
+    need): both caller buffers end as the oracle's last two states -- buffer
+    R & 1 holds round R's state and the other round R - 1's -- exactly as on a
+    plain die-local workspace and on the guide's counter poll."""
     code, owl = WLS[wl]
     v0 = ci.ring_payload(31 + P, P, 4)
     states = {R: expect_ring(owl, v0, R)[0], R - 1: expect_ring(owl, v0, R - 1)[0] if R > 1 else v0}
-    for kind, variant in (("mirror", 5), ("die_local", 5), ("plain", 0)):
+    for kind, variant in (("mirror", 5), ("sized", 5), ("die_local", 5), ("plain", 0)):
         b0, b1 = _both_buffers(cns, code, v0, R, variant, kind)
         fin, prev = (b1, b0) if R & 1 else (b0, b1)
         np.testing.assert_array_equal(fin, states[R], err_msg=kind)
         np.testing.assert_array_equal(prev, states[R - 1], err_msg=kind)
+
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+@pytest.mark.parametrize("wl", sorted(WLS))
+@pytest.mark.parametrize("P,slots", [(1, 8), (3, 12), (8, 256), (111, 256), (5, 1020), (8, 1024), (4, 6)])
+@pytest.mark.parametrize("R", [1, 2, 1001])
+def test_longer_rows_through_the_payload_copies(cns, mode, wl, P, slots, R):
+    """Rows of several uint4 (up to 1020 words: 255 uint4, one row per block pair) through the per-die
+    copies on a workspace sized for them, on both paths: both caller buffers end as the oracle's last two
+    states.  Rows of 1024 words, or of a length that is not a multiple of 4, run without copies."""
+    code, owl = WLS[wl]
+    v0 = ci.ring_payload(7 * P + slots, P, slots)
+    states = {R: expect_ring(owl, v0, R)[0], R - 1: expect_ring(owl, v0, R - 1)[0] if R > 1 else v0}
+    b0, b1 = _both_buffers(cns, code, v0, R, 5, "sized", mode=mode)
+    fin, prev = (b1, b0) if R & 1 else (b0, b1)
+    np.testing.assert_array_equal(fin, states[R])
+    np.testing.assert_array_equal(prev, states[R - 1])
 
 
 @pytest.mark.parametrize("variant", [0, 1, 2, 5, 6])
