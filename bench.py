@@ -635,6 +635,21 @@ def probe_phases(cns, torch, ctas=P_HEAD, rounds=20000, stamp_rounds=512):
     return budget
 
 
+def probe_release_fence(cns, torch, iters=2000):
+    """What one gpu-scope release fence costs a thread, by what it touched since its previous fence
+    (cns_probe_release_fence): nothing, one store on its own die, one store on the other die."""
+    raw = torch.zeros(3 * 2048, dtype=torch.int32, device="cuda")
+    off = (-raw.data_ptr()) % 8192 // 4
+    region = raw[off:off + 2048]
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    cns.check(cns.cns_probe_release_fence(region, iters, out), "cns_probe_release_fence")
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    return {"after_nothing": int(o[0]), "after_a_store_on_its_die": int(o[1]),
+            "after_a_store_on_the_other_die": int(o[2]),
+            "note": "one thread; the headline's release follows the round's store into the far-die payload copy"}
+
+
 def barrier_context(sec, rtt_mean, far, variant):
     """The empty-round barrier in its two contracts, against the same round trips: with the release and
     acquire that data rounds need (the headline's variant), and arrival only as the pages define SYNCALL
@@ -711,6 +726,7 @@ def run_native(args):
     if cpu is not None and not args.no_secondary:
         cpu["twin"] = time_twin()
     budget = probe_phases(cns, torch) if args.variant == 5 else None
+    fence = probe_release_fence(cns, torch)
     traffic = load_traffic().get(f"syncall_soft_ring_rotate_148_variant{args.variant}", {})
     achieved = 1e3 / ns_round            # barrier rounds per microsecond
     peak = 1e3 / rtt_mean                # one round per L2 atomic round trip (mean over SMs)
@@ -739,7 +755,7 @@ def run_native(args):
                                 "ld_relaxed_median": round(ld_med, 1)},
                      "ns_per_round_over_rtt": round(ns_round / rtt_mean, 3),
                      "context": dict(barrier_context(sec, rtt_mean, far, args.variant),
-                                     round_budget_ns=budget)},
+                                     round_budget_ns=budget, release_fence_ns=fence)},
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,

@@ -137,6 +137,7 @@ _SIGS = {
     "cns_probe_same_address_throughput": (c_int, [c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "cns_probe_grid_sync": (c_int, [c_int32, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
     "cns_probe_op_chain": (c_int, [c_void_p, c_int32, c_void_p, c_void_p]),
+    "cns_probe_release_fence": (c_int, [c_void_p, c_int32, c_void_p, c_void_p]),
     "cns_probe_notify_pingpong": (c_int, [c_int, c_int32, c_void_p, c_void_p, c_void_p]),
     "cns_probe_round_phases": (c_int, [c_int32, c_int32, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_size_t,
                                        c_void_p, c_void_p]),
@@ -280,6 +281,10 @@ def syncall_workspace_bytes(participants: int, elems: int, out: bool = True):
 
 def cntnotify_enable_peer(h, peer_device: int) -> int:
     return lib().cntnotify_enable_peer(h, peer_device)
+
+
+def cns_probe_release_fence(region, iters: int, out, stream=None) -> int:
+    return lib().cns_probe_release_fence(ptr(region), iters, ptr(out), stream_handle(stream))
 
 
 def cns_probe_notify_pingpong(scope: int, iters: int, lines, out, stream=None) -> int:

@@ -903,3 +903,18 @@ def test_round_phase_probe(cns):
     # bad arguments are refused before any launch
     assert cns.cns_probe_round_phases(P, 256, 10, 20, b0, b1, ws, st) == cns.CNS_ERR_INVALID_VALUE
     assert cns.cns_probe_round_phases(P, 256, R, 2000, b0, b1, ws, st) == cns.CNS_ERR_INVALID_VALUE
+
+
+def test_release_fence_probe(cns):
+    """The fence-cost probe runs, refuses a misaligned region, and finds a release after a store on the other
+    die dearer than one after a store on the SM's own die (its two blocks sit on different dies)."""
+    import torch
+    import bench
+    f = bench.probe_release_fence(cns, torch, iters=300)
+    assert 0 < f["after_nothing"] < f["after_a_store_on_the_other_die"]
+    assert f["after_a_store_on_its_die"] < f["after_a_store_on_the_other_die"]
+    raw = torch.zeros(4096, dtype=torch.int32, device="cuda")
+    off = ((-raw.data_ptr()) % 8192 + 4096) // 4
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    assert cns.cns_probe_release_fence(raw[off:], 10, out) == cns.CNS_ERR_INVALID_VALUE
+    assert cns.cns_probe_release_fence(raw, 0, out) == cns.CNS_ERR_INVALID_VALUE   # no samples
