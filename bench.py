@@ -463,9 +463,18 @@ def secondary(cns, torch, peaks):
             "host_submit_us_per_round": round((t1 - t0) * 1e3, 2), "until_done_us_per_round": round((t2 - t0) * 1e3, 2)}
     cns.cntnotify_destroy(done)
     cns.cntnotify_destroy(ack)
+    # the host-launch roofline: a round can be no shorter than the submission of its launches (three with the
+    # wait as a stream task, two with it inside the consumer), at the host's measured cost per launch
+    rc_l, launch_us = cns.cns_probe_launch_cost(3000, 1, s1)
+    cns.check(rc_l, "cns_probe_launch_cost")
+    for (areas, cw), form in by_areas.items():
+        n_launch = 3 if cw == 0 else 2
+        form["host_launch_bound_us_per_round"] = round(n_launch * launch_us, 3)
+        form["frac_of_host_launch_bound"] = round(n_launch * launch_us / max(form["until_done_us_per_round"], 1e-9), 4)
     out["notify_pipeline_4096x1000"] = dict(
         by_areas[2, 0], areas=2, consumer_wait="stream", in_kernel_wait=by_areas[2, 1], one_area=by_areas[1, 0],
         one_area_in_kernel_wait=by_areas[1, 1],
+        host_launch_us=round(launch_us, 3),
         note="best of 3 runs; records/s over the summed recording phases (device clock: from the producer's "
              "CTA 0 being allowed to record to the consumer-side wait releasing), round trips/s over the whole "
              "run (events)")

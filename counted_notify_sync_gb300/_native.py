@@ -10,7 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
-from ctypes import (POINTER, Structure, c_char_p, c_float, c_int, c_int32, c_int64, c_size_t, c_uint8, c_uint32,
+from ctypes import (POINTER, Structure, c_char_p, c_double, c_float, c_int, c_int32, c_int64, c_size_t, c_uint8, c_uint32,
                     c_uint64, c_void_p)
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -137,6 +137,7 @@ _SIGS = {
     "cns_probe_same_address_throughput": (c_int, [c_int32, c_int32, c_int32, c_void_p, c_void_p]),
     "cns_probe_grid_sync": (c_int, [c_int32, c_int32, c_int64, c_void_p, c_void_p, c_void_p]),
     "cns_probe_op_chain": (c_int, [c_void_p, c_int32, c_void_p, c_void_p]),
+    "cns_probe_launch_cost": (c_int, [c_int32, c_int32, POINTER(c_double), c_void_p]),
     "cns_probe_release_fence": (c_int, [c_void_p, c_int32, c_void_p, c_void_p]),
     "cns_probe_notify_pingpong": (c_int, [c_int, c_int32, c_void_p, c_void_p, c_void_p]),
     "cns_probe_round_phases": (c_int, [c_int32, c_int32, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_size_t,
@@ -281,6 +282,13 @@ def syncall_workspace_bytes(participants: int, elems: int, out: bool = True):
 
 def cntnotify_enable_peer(h, peer_device: int) -> int:
     return lib().cntnotify_enable_peer(h, peer_device)
+
+
+def cns_probe_launch_cost(launches: int, early: int = 1, stream=None):
+    """(code, host microseconds per kernel launch)"""
+    v = c_double(0.0)
+    rc = lib().cns_probe_launch_cost(launches, early, ctypes.byref(v), stream_handle(stream))
+    return rc, v.value
 
 
 def cns_probe_release_fence(region, iters: int, out, stream=None) -> int:

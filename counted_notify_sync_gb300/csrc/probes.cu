@@ -5,6 +5,7 @@
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
+#include <chrono>
 #include <cstdint>
 
 #include "cns.h"
@@ -129,6 +130,8 @@ __global__ void probe_fence_kernel(uint32_t *region, int iters, uint64_t *out)
     }
 }
 
+__global__ void probe_empty_kernel() {}
+
 __global__ void probe_red_kernel(int iters, uint32_t *word)
 {
     for (int i = 0; i < iters; ++i)
@@ -239,5 +242,35 @@ extern "C" int cns_probe_release_fence(uint32_t *region_dev, int32_t iters, uint
         return rc;
     probe_fence_kernel<<<1, 32, 0, to_stream(stream)>>>(region_dev, iters, out_dev);
     CNS_CUDA(cudaGetLastError());
+    return CNS_SUCCESS;
+}
+
+extern "C" int cns_probe_launch_cost(int32_t launches, int32_t early, double *us_per_launch, cns_stream_t stream)
+{
+    if (!us_per_launch)
+        return CNS_ERR_NULL_PTR;
+    if (launches < 1 || launches > 1000000 || (early != 0 && early != 1))
+        return CNS_ERR_INVALID_VALUE;
+    DeviceInfo dev;
+    if (int rc = current_device(&dev))
+        return rc;
+    cudaStream_t s = to_stream(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(32);
+    cfg.stream = s;
+    cfg.attrs = early ? attr : nullptr;
+    cfg.numAttrs = early ? 1 : 0;
+    CNS_CUDA(cudaLaunchKernelEx(&cfg, probe_empty_kernel));   // loaded and warm before the clock starts
+    CNS_CUDA(cudaStreamSynchronize(s));
+    const auto t0 = std::chrono::steady_clock::now();
+    for (int32_t i = 0; i < launches; ++i)
+        CNS_CUDA(cudaLaunchKernelEx(&cfg, probe_empty_kernel));
+    const auto t1 = std::chrono::steady_clock::now();
+    CNS_CUDA(cudaStreamSynchronize(s));
+    *us_per_launch = std::chrono::duration<double, std::micro>(t1 - t0).count() / launches;
     return CNS_SUCCESS;
 }

@@ -727,6 +727,19 @@ int cns_probe_grid_sync(int32_t ctas, int32_t threads, int64_t rounds, void *buf
 int cns_probe_op_chain(const uint32_t *ops_dev, int32_t iters, uint64_t *out_dev, cns_stream_t stream);
 
 /*
+ * cns_probe_launch_cost -- the host's cost of submitting one kernel launch
+ * the way the pipeline does (cudaLaunchKernelEx; with early = 1 also the
+ * programmatic-stream-serialization attribute): `launches` launches of an
+ * empty one-warp kernel on `stream`, timed on the host clock around the
+ * submissions only; *us_per_launch gets the mean in microseconds.  Waits for
+ * the stream afterwards (not timed).  The roofline of a host-bound pipeline:
+ * a round can be no shorter than its launches' submission.
+ * Errors: NULL_PTR, INVALID_VALUE (launches outside 1..1000000, early not
+ * 0/1), CUDA.
+ */
+int cns_probe_launch_cost(int32_t launches, int32_t early, double *us_per_launch, cns_stream_t stream);
+
+/*
  * cns_probe_release_fence -- what one fence.release.gpu costs a thread, by
  * what it touched since its previous fence: out_dev[0] nothing, [1] one store
  * to a line on its own die, [2] one store to a line on the other die (the mean

@@ -550,3 +550,15 @@ def test_op_chain_probe_applies_the_rule(cns):
     assert packed >> 32 == int(trace[:, 1].astype(np.uint64).sum())
     assert ns > 0
     assert cns.cns_probe_op_chain(ops_d, 0, out) == cns.CNS_ERR_INVALID_VALUE
+
+
+def test_launch_cost_probe(cns):
+    """The host's cost per kernel launch (the pipeline's roofline): positive, a few microseconds at most; bad
+    arguments are refused."""
+    import torch
+    s = torch.cuda.Stream()
+    for early in (0, 1):
+        rc, us = cns.cns_probe_launch_cost(500, early, s)
+        assert rc == 0 and 0.0 < us < 50.0
+    assert cns.cns_probe_launch_cost(0, 1, s)[0] == cns.CNS_ERR_INVALID_VALUE
+    assert cns.cns_probe_launch_cost(10, 2, s)[0] == cns.CNS_ERR_INVALID_VALUE
