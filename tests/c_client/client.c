@@ -1,7 +1,10 @@
 /* A plain C program that uses libcns.so through include/cns.h only (no Python):
  * a die-local soft SYNCALL ring of 148 CTAs on an 8 KB-aligned workspace, the
- * same through the hard path, and a counted notify recorded on one stream and
- * waited on another.  Expected values are closed forms: after R ring-rotate
+ * same through the hard path (with the cluster barrier and with the paired
+ * step), each also on a workspace sized by syncall_workspace_bytes for the
+ * per-die payload copies, and a counted notify recorded on one stream and
+ * waited on another, at gpu scope and after cntnotify_enable_peer (system
+ * scope, the peer being this device).  Expected values are closed forms: after R ring-rotate
  * rounds participant p holds participant (p + R) mod P's starting row; the soft
  * counter ends at R * P.  Prints "ok" and exits 0, or names the first failure
  * and exits 1.  Built and run by the GPU tests. */
@@ -23,18 +26,22 @@ static int fail(const char *what, int code)
     return 1;
 }
 
-static int ring(int mode)
+static int ring(int mode, int copies, int hard_step)
 {
     uint32_t host0[P * 4], host_out[P * 4];
     for (int i = 0; i < P * 4; ++i)
         host0[i] = (uint32_t)i * 2654435761u + 12345u;
+    size_t ws_bytes = CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES;
+    int rc;
+    if (copies && (rc = syncall_workspace_bytes(P, 4, &ws_bytes)))
+        return fail("syncall_workspace_bytes", rc);
     void *b0, *b1, *raw;
     if (cudaMalloc(&b0, sizeof host0) || cudaMalloc(&b1, sizeof host0) ||
-        cudaMalloc(&raw, CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES + CNS_SYNCALL_DIE_LOCAL_ALIGN))
+        cudaMalloc(&raw, ws_bytes + CNS_SYNCALL_DIE_LOCAL_ALIGN))
         return fail("cudaMalloc", 0);
     void *ws = (void *)(((uintptr_t)raw + CNS_SYNCALL_DIE_LOCAL_ALIGN - 1) &
                         ~(uintptr_t)(CNS_SYNCALL_DIE_LOCAL_ALIGN - 1));
-    int rc = syncall_workspace_init(ws, CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES, 0, NULL);
+    rc = syncall_workspace_init(ws, ws_bytes, 0, NULL);
     if (rc)
         return fail("syncall_workspace_init", rc);
     cns_syncall_data_t d;
@@ -46,8 +53,9 @@ static int ring(int mode)
     d.buf1_dev = b1;
     d.elems = 4;
     d.workspace_dev = ws;
-    d.workspace_bytes = CNS_SYNCALL_WORKSPACE_DIE_LOCAL_BYTES;
+    d.workspace_bytes = (uint32_t)ws_bytes;
     d.barrier_variant = CNS_BARRIER_DIE_LOCAL;
+    d.hard_step = hard_step;
     d.sync = 1;
     d.host_in = host0;
     d.host_out = host_out;
@@ -67,7 +75,7 @@ static int ring(int mode)
     return 0;
 }
 
-static int notify(void)
+static int notify(int peer)
 {
     cudaStream_t s1, s2;
     if (cudaStreamCreate(&s1) || cudaStreamCreate(&s2))
@@ -76,6 +84,9 @@ static int notify(void)
     int rc = cntnotify_create(&n, 0);
     if (rc)
         return fail("cntnotify_create", rc);
+    int dev = 0;
+    if (peer && (cudaGetDevice(&dev) || (rc = cntnotify_enable_peer(n, dev))))
+        return fail("cntnotify_enable_peer", rc);
     const cns_record_info_t add = {CNS_REC_ADD, 1};
     const cns_wait_info_t wait = {CNS_WAIT_BIGGER_OR_EQUAL, 3, 10, 1, {0, 0, 0}};
     for (int i = 0; i < 3; ++i)
@@ -100,7 +111,12 @@ int main(void)
     int32_t version = 0, sm = 0;
     if (cns_version(&version, &sm) || sm != 103)
         return fail("cns_version", sm);
-    if (ring(CNS_SYNCALL_SOFT) || ring(CNS_SYNCALL_HARD) || notify())
+    for (int copies = 0; copies < 2; ++copies)
+        if (ring(CNS_SYNCALL_SOFT, copies, CNS_HARD_STEP_CLUSTER_BARRIER) ||
+            ring(CNS_SYNCALL_HARD, copies, CNS_HARD_STEP_CLUSTER_BARRIER) ||
+            ring(CNS_SYNCALL_HARD, copies, CNS_HARD_STEP_PAIRED_MBARRIER))
+            return 1;
+    if (notify(0) || notify(1))
         return 1;
     printf("ok\n");
     return 0;

@@ -1,7 +1,8 @@
 """The C ABI from a plain C program, no Python in between: tests/c_client/client.c
 is compiled with gcc against include/cns.h, linked with libcns.so and the CUDA
-runtime, and run; it checks its own results against closed forms and prints
-"ok"."""
+runtime, and run (soft and hard rings, the paired hard step, workspaces sized
+for the per-die payload copies, and counted notifies at gpu and at system
+scope); it checks its own results against closed forms and prints "ok"."""
 import os
 import subprocess
 
