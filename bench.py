@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--case", choices=sorted(CASES), default=None,
                     help="run one small launch pattern for a profiler capture and exit")
     ap.add_argument("--areas", type=int, default=2, choices=(1, 2), help="tile areas of --case pipeline")
+    ap.add_argument("--no-cooperative", action="store_true",
+                    help="--case hard148-small: launch without the cooperative attribute (CNS_LAUNCH_NO_COOPERATIVE_ATTR)")
     ap.add_argument("--consumer-wait", type=int, default=0, choices=(0, 1),
                     help="--case pipeline: 0 = the wait as a stream task, 1 = inside the consumer kernel")
     return ap.parse_args()
@@ -803,7 +805,8 @@ def case_hard148_small(args):
     ws = cns.new_workspace()
     for _ in range(3):
         d, _ = cns.run_syncall(cns.CNS_SYNCALL_HARD, cns.CNS_AIV_ONLY, cns.CNS_WL_RING_ROTATE, P_HEAD, b0, b1, 2000,
-                               elems=SLOTS_HEAD, workspace=ws, variant=args.variant)
+                               elems=SLOTS_HEAD, workspace=ws, variant=args.variant,
+                               launch_flags=cns.CNS_LAUNCH_NO_COOPERATIVE_ATTR if args.no_cooperative else 0)
     print(f"case hard148-small: ok (clusters of {d.cluster_used} CTAs, as the device saw the launch)")
 
 

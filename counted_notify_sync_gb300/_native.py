@@ -58,6 +58,7 @@ CNS_CTA_DONE = 1
 CNS_CTA_IDLE = 2
 CNS_CTA_ABORTED = 4
 CNS_LAUNCH_NO_CLUSTER_ATTR = 1
+CNS_LAUNCH_NO_COOPERATIVE_ATTR = 2
 CNS_HARD_STEP_CLUSTER_BARRIER = 0
 CNS_HARD_STEP_PAIRED_MBARRIER = 1
 

@@ -298,7 +298,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         return CNS_ERR_INVALID_VALUE;
     if (d->workspace_bytes != 0 && d->workspace_bytes < CNS_SYNCALL_WORKSPACE_BYTES)
         return CNS_ERR_INVALID_VALUE;
-    if (d->launch_flags & ~CNS_LAUNCH_NO_CLUSTER_ATTR)
+    if (d->launch_flags & ~(CNS_LAUNCH_NO_CLUSTER_ATTR | CNS_LAUNCH_NO_COOPERATIVE_ATTR))
         return CNS_ERR_INVALID_VALUE;
     if (d->hard_step != CNS_HARD_STEP_CLUSTER_BARRIER &&
         !(mode == CNS_SYNCALL_HARD && d->hard_step == CNS_HARD_STEP_PAIRED_MBARRIER))
@@ -459,9 +459,12 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
     cfg.stream = s;
     cudaLaunchAttribute attrs[2];
     int na = 0;
-    attrs[na].id = cudaLaunchAttributeCooperative;
-    attrs[na].val.cooperative = 1;
-    ++na;
+    const bool cooperative = !(d->launch_flags & CNS_LAUNCH_NO_COOPERATIVE_ATTR);
+    if (cooperative) {
+        attrs[na].id = cudaLaunchAttributeCooperative;
+        attrs[na].val.cooperative = 1;
+        ++na;
+    }
     if (mode == CNS_SYNCALL_HARD && !(d->launch_flags & CNS_LAUNCH_NO_CLUSTER_ATTR)) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
         attrs[na].val.clusterDim.x = C;
@@ -477,7 +480,7 @@ extern "C" int syncall_run(int mode, int core_type, int32_t used_cores, int32_t 
         (void)cudaGetLastError();
         return CNS_ERR_NOT_RESIDENT;
     }
-    if (le != cudaSuccess && mode == CNS_SYNCALL_HARD && na == 2) {
+    if (le != cudaSuccess && mode == CNS_SYNCALL_HARD && cooperative && na == 2) {
         // the cooperative attribute together with clusters may be refused;
         // residency was checked above, so launch without it
         CNS_LOG(1, "cooperative cluster launch refused (%s); launching without it", cudaGetErrorString(le));

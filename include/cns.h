@@ -292,7 +292,7 @@ typedef struct {
                                 requested */
     int32_t barrier_variant; /* (in) cns_barrier_variant_t; 0 = the guide's counter poll */
     uint32_t workspace_bytes;/* (in) size of workspace_dev; 0 = CNS_SYNCALL_WORKSPACE_BYTES */
-    uint32_t launch_flags;   /* (in) 0, or CNS_LAUNCH_NO_CLUSTER_ATTR (testing) */
+    uint32_t launch_flags;   /* (in) 0, or CNS_LAUNCH_* bits (testing and profiling) */
     int32_t hard_step;       /* (in) HARD: cns_hard_step_t, the intra-cluster step; 0 = the
                                 cluster barrier.  SOFT: must be 0. */
 } cns_syncall_data_t;
@@ -324,6 +324,14 @@ typedef enum {
  * takes its cluster count and size from the launch it really got, so the
  * results are the same; cluster_used then reports 1.  For tests. */
 #define CNS_LAUNCH_NO_CLUSTER_ATTR 1u
+
+/* CNS_LAUNCH_NO_COOPERATIVE_ATTR launches without the cooperative attribute.
+ * The grid's residency is still checked before the launch (the occupancy
+ * query that refuses a grid with CNS_ERR_NOT_RESIDENT), but nothing then
+ * guarantees it if other work shares the GPU: the bounded waits end such a
+ * run with CNS_ERR_TIMEOUT.  For tools that do not keep a cooperative cluster
+ * launch's cluster shape when they capture it. */
+#define CNS_LAUNCH_NO_COOPERATIVE_ATTR 2u
 
 /*
  * syncall_run -- one persistent launch that runs `rounds` rounds of

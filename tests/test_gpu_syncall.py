@@ -548,8 +548,22 @@ def test_hard_path_without_the_cluster_attribute(cns, variant, wl):
 
 def test_launch_flags_outside_the_defined_bits_are_refused(cns):
     v0 = ci.ring_payload(3, 4, 4)
-    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_ROTATE, 4, v0, 3, check=False, launch_flags=2)
+    d, rc, got, st = run_ring(cns, HARD, AIV, cns.CNS_WL_RING_ROTATE, 4, v0, 3, check=False, launch_flags=4)
     assert rc == cns.CNS_ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+def test_launch_without_the_cooperative_attribute(cns, mode):
+    """The residency check alone (no cooperative attribute): exact, and the hard path keeps its clusters."""
+    R = 3001
+    v0 = ci.ring_payload(ci.SEED_RING_ROTATE, 148, 4)
+    d, rc, got, st = run_ring(cns, mode, AIV, cns.CNS_WL_RING_ROTATE, 148, v0, R, variant=5,
+                              launch_flags=cns.CNS_LAUNCH_NO_COOPERATIVE_ATTR)
+    want, _ = expect_ring(oracle.WL_RING_ROTATE, v0, R)
+    np.testing.assert_array_equal(got, want)
+    assert rc == 0 and d.device_status == 0
+    if mode == HARD:
+        assert d.cluster_used == 2 and d.final_counter == R * 74
 
 
 # --- the hard path's paired-mbarrier step (the guide's intra-block flags, §5.1) -------------
