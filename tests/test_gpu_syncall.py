@@ -850,6 +850,32 @@ def test_longer_rows_through_the_payload_copies(cns, mode, wl, P, slots, R):
     np.testing.assert_array_equal(prev, states[R - 1])
 
 
+@pytest.mark.parametrize("mode", [SOFT, HARD])
+@pytest.mark.parametrize("threads", [32, 64])
+def test_rows_longer_than_the_cta_through_the_payload_copies(cns, mode, threads):
+    """Rows of 255 uint4 moved by CTAs of 32 or 64 threads (each thread loops over several uint4 of the row)
+    through the per-die copies: exact against the oracle."""
+    v0 = ci.ring_payload(404, 6, 1020)
+    want, _ = expect_ring(oracle.WL_XORSHIFT, v0, 77)
+    b0, b1 = _both_buffers(cns, cns.CNS_WL_XORSHIFT, v0, 77, 5, "sized", mode=mode, threads=threads)
+    np.testing.assert_array_equal(b1, want)
+
+
+def test_subset_rows_through_the_payload_copies(cns):
+    """64 participants of a 148-CTA launch with 1 KB rows through the per-die copies (the others idle):
+    exact against the oracle, and the workspace sized for the 64 participants is enough."""
+    v0 = ci.ring_payload(ci.SEED_XORSHIFT, 64, 256)
+    import torch
+    b0 = to_dev_u32(np.vstack([v0, np.zeros((84, 256), np.uint32)]))
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace(participants=64, elems=256)
+    d, rc = cns.run_syncall(SOFT, AIV, cns.CNS_WL_XORSHIFT, 148, b0, b1, 1001, used_cores=64, elems=256,
+                            workspace=ws, variant=5)
+    want, fc = expect_ring(oracle.WL_XORSHIFT, v0, 1001)
+    np.testing.assert_array_equal(from_dev_u32(b1).reshape(148, 256)[:64], want)
+    assert rc == 0 and d.final_counter == fc
+
+
 @pytest.mark.parametrize("variant", [0, 1, 2, 5, 6])
 @pytest.mark.parametrize("slots", [0, 1, 4])
 def test_solo_rounds_every_variant(cns, variant, slots):
