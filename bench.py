@@ -483,7 +483,8 @@ def secondary(cns, torch, peaks):
 
     # op-stream state machine, 1e6 ops: buffers allocated once, 20 back-to-back C-ABI calls timed (warm L2),
     # and calls with L2 flushed before each one (cold, each timed alone); then a stream without SET records
-    # (one dependent chain), against the chain of the rule itself on one thread (cns_probe_op_chain)
+    # (cut only where other ops fix the count), and a stream where no op ever fixes it (one dependent chain),
+    # against the chain of the rule itself on one thread (cns_probe_op_chain)
     n = 1_000_000
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
 
@@ -511,31 +512,42 @@ def secondary(cns, torch, peaks):
         return warm, statistics.median(cold)
 
     warm, cold = statemachine_figures(ci.notify_ops(n))
-    hbm_ops = peaks["hbm_gbs"] * 1e9 / 24 if peaks.get("hbm_gbs") else None
     ops_sf = ci.notify_ops(n + n // 7, seed=ci.SEED_NOTIFY_OPS ^ 0x5E7F)
-    ops_sf = ops_sf[~((ops_sf[:, 0] == 0) & (ops_sf[:, 1] == 0))][:n]     # no SET record anywhere
-    warm_sf, cold_sf = statemachine_figures(np.ascontiguousarray(ops_sf), label_reps=3)
-    chain_ops = torch.from_numpy(np.ascontiguousarray(ops_sf[:16]).view(np.int32)).cuda()
+    ops_sf = np.ascontiguousarray(ops_sf[~((ops_sf[:, 0] == 0) & (ops_sf[:, 1] == 0))][:n])   # no SET record
+    warm_sf, cold_sf = statemachine_figures(ops_sf)
+    ops_ch = ci.notify_ops(n, seed=ci.SEED_NOTIFY_OPS ^ 0xC4A1)
+    ops_ch[ops_ch[:, 0] == 0, 1] = 1          # every record an ADD
+    ops_ch[:, 3] = 0                          # and no clearing wait: nothing ever fixes the count
+    ops_ch = np.ascontiguousarray(ops_ch)
+    warm_ch, cold_ch = statemachine_figures(ops_ch, label_reps=3)
+    chain_ops = torch.from_numpy(np.ascontiguousarray(ops_ch[:16]).view(np.int32)).cuda()
     chain_out = torch.zeros(2, dtype=torch.int64, device="cuda")
     iters = 20000
     cns.check(cns.cns_probe_op_chain(chain_ops, iters, chain_out), "op chain")
     torch.cuda.synchronize()
     chain_ns = chain_out[0].item() / (16 * iters)
-    sf_ns = warm_sf * 1e6 / ops_sf.shape[0]
+    ch_ns = warm_ch * 1e6 / ops_ch.shape[0]
+
+    def hbm_frac(ms):
+        return round(24 * n / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4) if peaks.get("hbm_gbs") else None
+
     out["notify_statemachine_1e6"] = {
         "ms": round(warm, 4), "ops_per_s": round(n / (warm * 1e-3), 0), "bytes_per_op": 24,
         "gbs_algorithmic": round(24 * n / (warm * 1e-3) / 1e9, 1),
         "cold_l2_ms": round(cold, 4), "cold_l2_ops_per_s": round(n / (cold * 1e-3), 0),
-        "cold_l2_frac_of_measured_hbm": round(24 * n / (cold * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
-        if peaks.get("hbm_gbs") else None,
-        "bound_note": "24 B per op (16 in, 8 out) against the measured HBM copy peak; the ops are cut at SET "
-                      "records, so the walks run in parallel",
-        "set_free": {"ops": int(ops_sf.shape[0]), "ms": round(warm_sf, 3), "cold_l2_ms": round(cold_sf, 3),
-                     "ns_per_op": round(sf_ns, 3),
-                     "chain_bound_ns_per_op": round(chain_ns, 3),
-                     "frac_of_chain_bound": round(chain_ns / sf_ns, 4),
-                     "note": "no SET record: the whole stream is one dependent chain; the bound is one thread "
-                             "applying the same rule to ops held in registers (cns_probe_op_chain)"}}
+        "cold_l2_frac_of_measured_hbm": hbm_frac(cold),
+        "bound_note": "24 B per op (16 in, 8 out) against the measured HBM copy peak; the ops are cut where the "
+                      "count is fixed (a SET, or an op after which every bit of the count is known), so the "
+                      "walks run in parallel",
+        "set_free": {"ops": int(ops_sf.shape[0]), "ms": round(warm_sf, 4), "cold_l2_ms": round(cold_sf, 4),
+                     "cold_l2_frac_of_measured_hbm": hbm_frac(cold_sf),
+                     "note": "no SET record: cut only where other ops fix the count"},
+        "one_chain": {"ops": int(ops_ch.shape[0]), "ms": round(warm_ch, 3), "ns_per_op": round(ch_ns, 3),
+                      "chain_bound_ns_per_op": round(chain_ns, 3),
+                      "frac_of_chain_bound": round(chain_ns / ch_ns, 4),
+                      "note": "records all ADDs and no clearing wait: no op fixes the count, the whole stream is "
+                              "one dependent chain; the bound is one thread applying the same rule to ops held "
+                              "in registers (cns_probe_op_chain)"}}
 
     # the same ring-rotate rounds separated by the CUDA runtime's cooperative-groups grid barrier
     v0 = ci.ring_payload(ci.SEED_RING_ROTATE, P_HEAD, SLOTS_HEAD)
@@ -834,6 +846,19 @@ def case_statemachine(args):
     for _ in range(3):
         cns.run_statemachine(ops_d, 0)
     torch.cuda.synchronize()
+    ops_sf = ci.notify_ops(1_150_000, seed=ci.SEED_NOTIFY_OPS ^ 0x5E7F)
+    ops_sf = np.ascontiguousarray(ops_sf[~((ops_sf[:, 0] == 0) & (ops_sf[:, 1] == 0))][:1_000_000])
+    sf_d = torch.from_numpy(ops_sf.view(np.int32)).cuda()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for label, d in (("bench stream", ops_d), ("no SET record", sf_d)):
+        cns.run_statemachine(d, 0)
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(20):
+            cns.run_statemachine(d, 0)
+        e.record()
+        torch.cuda.synchronize()
+        print(f"case statemachine: {label}: {s.elapsed_time(e) / 20 * 1e3:.1f} us per 1e6 ops (warm)")
     print("case statemachine: ok")
 
 

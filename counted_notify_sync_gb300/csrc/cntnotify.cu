@@ -226,24 +226,40 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 // ---------------------------------------------------------------------------
 // Op-stream state machine.  A SET record gives a count that does not depend
 // on what came before, so the stream can be cut at SETs: from a SET on, the
-// trace can be computed without knowing the earlier count.
+// trace can be computed without knowing the earlier count.  Other ops can fix
+// the count too: an AND with few bits set leaves few unknown bits, an OR sets
+// them, an add with a known carry keeps them known, a clearing wait whose
+// test does not depend on the unknown bits releases to 0.  So where a tile's
+// SETs leave a long stretch, each chunk's thread follows which bits of the
+// count are known (known zeros and known ones, starting from nothing known at
+// the chunk's first op) and marks the first op of its chunk after which every
+// bit is known, together with that op's outcome: a "fixing" op, which then
+// starts a stretch as a SET does.  The marking is exact (a bit is only called
+// known when every count the earlier ops could have left gives it the same
+// value), so the trace is the same as the sequential one; it only shortens
+// the stretches.
 //
 // One persistent cooperative launch.  The stream is cut into tiles of up to
 // 4096 ops; CTA b takes tiles b, b + grid, b + 2 grid, ...  Within a tile, 512
 // threads each own a chunk of 8 ops:
-//   A  the thread of every chunk with a SET walks from the chunk's first SET
-//      up to the tile's next SET after the chunk (or the tile's end, in which
-//      case it publishes the tile's end count, tagged with this call's tag,
-//      for the next tile) -- one contiguous stretch of ops per thread;
+//   F  if a stretch between SETs is long (or the tile holds no SET), every
+//      thread marks its chunk's first fixing op, if any, and turns it into a
+//      SET of the count it fixes (same outcome);
+//   A  the thread of every chunk with a start (its first SET, or the fixing
+//      op F marked) walks from it up to the tile's next start after the
+//      chunk (or the tile's end, in which case it publishes the tile's end
+//      count, tagged with this call's tag, for the next tile) -- one
+//      contiguous stretch of ops per thread;
 //   C  the last thread takes the previous tile's end count (init for tile 0),
 //      waiting on the device until it is published, and replays the ops in
-//      front of the tile's first SET -- all of them if the tile has none, in
-//      which case it publishes the tile's end count itself.
+//      front of the tile's first start -- all of them if the tile has none,
+//      in which case it publishes the tile's end count itself.
 // Every op is applied exactly once, in stream order along its stretch.  A
-// tile with a SET publishes before it waits, so a wait lasts only as long as
-// a run of SET-free tiles in front of it.  Every CTA is resident (cooperative
-// launch) and takes its tiles in increasing order, so the tile a CTA waits
-// for is always held by a running CTA (or done).  The tag makes the link words
+// tile with a start publishes before it waits, so a wait lasts only as long
+// as a run of tiles without one in front of it (a stream of adds alone, for
+// instance, has none: it is one dependent chain).  Every CTA is resident
+// (cooperative launch) and takes its tiles in increasing order, so the tile a
+// CTA waits for is always held by a running CTA (or done).  The tag makes the link words
 // need no initial content: a word holds (tag << 32) | count, and a word from
 // an earlier call carries an earlier tag.  The wait is bounded; if it runs out
 // (only a stalled GPU can make it), the tile's leading entries get count 0 and
@@ -268,7 +284,8 @@ constexpr int kChunk = 16;
 //           BIGGER 2^32 - 1) is mask 0, lo 1, span 0: 0 - 1 is never <= 0.
 //   w       flags: bit 8 wait, bit 12 the wait clears once released, bits
 //           9-10 the outcome of anything else (CNS_OUT_RECORD or
-//           CNS_OUT_INVALID), bit 11 SET.
+//           CNS_OUT_INVALID, or, for a fixing op turned into a SET, the
+//           op's own outcome), bit 11 SET.
 // An op of no valid kind and mode is the record (~0, 0, 0) with outcome
 // CNS_OUT_INVALID.
 constexpr uint32_t kMicroWait = 1u << 8;
@@ -317,6 +334,56 @@ __device__ __forceinline__ uint32_t sm_apply_micro(uint32_t c, const uint4 m, ui
     *outcome = wait ? (in_range ? 1u : 0u) : ((m.w >> 9) & 3u);   // a wait: RELEASED (1) or HELD (0)
     return (in_range && (m.w & kMicroClear) != 0u) ? 0u : keep;
 }
+
+// What one micro-op does to the known bits of a count: kz the bits known to
+// be 0, ko those known to be 1 (a count consistent with them is any value
+// that has them).  A record's AND and OR fix bits outright.  Its add keeps a
+// sum bit known when the addend bit's partner in the count is known and the
+// carry into that bit is: the carry into bit i rises monotonically with the
+// count's low i bits, so it is known when the smallest and the largest
+// consistent counts (unknown bits 0, unknown bits 1) give the same carry.  A
+// wait is decided when every bit under its compare mask is known; a decided
+// clearing wait that releases leaves 0, an undecided one leaves 0 or the
+// count (so only the known zeros stay).  Returns whether the op's outcome is
+// known, and writes it to *outcome.
+__device__ __forceinline__ bool sm_known_step(uint32_t &kz, uint32_t &ko, const uint4 m, uint32_t *outcome)
+{
+    const bool wait = (m.w & kMicroWait) != 0u;
+    const bool clears = (m.w & kMicroClear) != 0u;
+    // record ((c & a) | o) + d
+    const uint32_t z = (kz | ~m.x) & ~m.y;
+    const uint32_t o = (ko & m.x) | m.y;
+    const uint32_t cmin = (o + m.z) ^ o ^ m.z;      // carries with every unknown bit 0
+    const uint32_t cmax = (~z + m.z) ^ ~z ^ m.z;    // and with every unknown bit 1
+    const uint32_t known = (z | o) & ~(cmin ^ cmax);
+    const uint32_t rko = (o ^ m.z ^ cmin) & known;
+    // wait on the range of (c & mask)
+    const bool decided = ((kz | ko) & m.x) == m.x;
+    const bool in_range = (ko & m.x) - m.y <= m.z;
+    if (!wait) {
+        kz = known & ~rko;
+        ko = rko;
+        *outcome = (m.w >> 9) & 3u;
+        return true;
+    }
+    if (clears) {
+        if (decided && in_range) {
+            kz = ~0u;
+            ko = 0u;
+        } else if (!decided) {
+            ko = 0u;
+        }
+    }
+    *outcome = in_range ? 1u : 0u;
+    return decided;
+}
+
+// A tile looks for fixing ops only when this many of its chunks in a row hold
+// no SET (a stretch between SETs, or in front of the first, of more than
+// kFixRun * 8 ops), or when it holds no SET at all (its count would otherwise
+// wait for the tiles before it).  Shorter stretches are walked sooner than the
+// search would run.
+constexpr int kFixRun = 16;
 
 constexpr uint64_t kSmLinkTimeoutNs = 10ull * 1000000000ull;
 
@@ -374,6 +441,17 @@ __device__ __forceinline__ int f_next_set(const uint32_t *s_setm, int from, int 
     while (bits == 0u && ++w < kTileOps / 32)
         bits = s_setm[w];
     return bits ? (w << 5) + __ffs(bits) - 1 : cnt;
+}
+
+// The stretch of the chunk at chunk0, if the chunk has a start: from its first
+// start to the tile's next start after the chunk (or the tile's end).
+__device__ __forceinline__ void f_stretch(const uint32_t *s_setm, int chunk0, int cnt, int *start, int *end)
+{
+    const uint32_t own = reinterpret_cast<const uint8_t *>(s_setm)[chunk0 / kFChunk];   // no bits at or past cnt
+    if (own != 0u) {
+        *start = chunk0 + __ffs(own) - 1;
+        *end = f_next_set(s_setm, chunk0 + kFChunk, cnt);
+    }
 }
 
 // Apply ops [p, end) of the tile to count c, writing their trace entries.
@@ -441,17 +519,43 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
         }
         __syncthreads();
         const bool last_tile = base + cnt == n;
-        {   // A
-            // this chunk's stretch, if it has a SET
-            const int chunk0 = k * kFChunk;
-            int start = cnt, end = cnt;
-            if (chunk0 < cnt) {
-                const int s0 = f_next_set(s_setm, chunk0, cnt);
-                if (s0 < chunk0 + kFChunk && s0 < cnt) {
-                    start = s0;
-                    end = f_next_set(s_setm, chunk0 + kFChunk, cnt);
+        const int chunk0 = k * kFChunk;
+        const uint8_t *s_setb = reinterpret_cast<const uint8_t *>(s_setm);   // byte k: chunk k
+        // chunks k .. k + kFixRun - 1 of the tile hold no SET, or the tile holds none at all
+        const int chunks = (cnt + kFChunk - 1) / kFChunk;
+        bool gap = false;
+        if (k < chunks) {
+            const int upto = min(chunks, k + kFixRun);
+            bool clear = true;
+            for (int j = k; j < upto && clear; ++j)
+                clear = s_setb[j] == 0u;
+            gap = clear && (upto - k == kFixRun || (k == 0 && upto == chunks));
+        }
+        if (__syncthreads_or(gap)) {
+            // F: a stretch between SETs (or in front of the first) is long enough that the
+            // fixing ops are worth finding: this chunk's first one (byte k of the start bits
+            // covers chunk k) becomes a SET of the count it fixes, with the op's outcome
+            const int stop = min(cnt, chunk0 + kFChunk);
+            uint32_t kz = 0u, ko = 0u, fixed_at = 0u, out = 0u;
+            int fix = -1;
+            for (int i = chunk0; i < stop; ++i) {
+                uint32_t o;
+                const bool known_out = sm_known_step(kz, ko, s_ops[f_slot(i)], &o);
+                if (known_out && (kz | ko) == ~0u) {
+                    fix = i;
+                    fixed_at = ko;
+                    out = o;
+                    break;
                 }
             }
+            reinterpret_cast<uint8_t *>(s_setm)[k] = fix >= 0 ? static_cast<uint8_t>(1u << (fix - chunk0)) : 0u;
+            __syncthreads();   // every start bit in place
+            if (fix >= 0)
+                s_ops[f_slot(fix)] = make_uint4(0u, fixed_at, 0u, (out << 9) | kMicroSet);
+        }
+        int start = cnt, end = cnt;   // this chunk's stretch, if it has a start
+        f_stretch(s_setm, chunk0, cnt, &start, &end);
+        {   // A
             // The stretches are handed to threads longest class first (class = floor(log2(length)),
             // counted per warp, placed by a scan over the classes), so that a warp's lanes walk
             // stretches of similar length instead of waiting for one long stretch among short ones.

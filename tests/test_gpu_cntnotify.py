@@ -201,13 +201,92 @@ def test_statemachine_ragged_lengths(cns, n):
 
 
 def test_statemachine_without_any_set(cns):
-    """No SET record at all: one chain runs the whole stream."""
+    """No SET record at all: the stream is cut only where other ops fix the
+    count (an AND that leaves few unknown bits, an OR that sets them, a
+    clearing wait decided by the known bits)."""
     ops = ci.notify_ops(50_000, seed=77)
     ops = ops[~((ops[:, 0] == 0) & (ops[:, 1] == 0))]
     got_t, got_f = run_sm(cns, ops, 3)
     want_t, want_f = oracle.cnt_statemachine(ops, 3)
     np.testing.assert_array_equal(got_t, want_t)
     assert got_f == want_f
+
+
+@pytest.mark.parametrize("n", [5_000, 200_000])
+def test_statemachine_one_chain(cns, n):
+    """No op ever fixes the count: one dependent chain through every tile."""
+    ops = _chain_ops(n, 31)
+    got_t, got_f = run_sm(cns, ops, 0xFFFFFFF0)
+    want_t, want_f = oracle.cnt_statemachine(ops, 0xFFFFFFF0)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
+def _near_fixing_ops(n, seed):
+    """Ops that fix, or nearly fix, the count in every way the known-bits
+    walk looks at: ANDs with sparse masks and ORs with dense ones (bits fixed
+    outright), adds whose carries run through known and unknown bits (small,
+    all-ones, one below a power of two, random), and waits whose compare mask
+    covers few bits (the bitmask mode, decided early) that clear half the
+    time -- with no SET record."""
+    ops = ci.notify_ops(n, seed=seed)
+    r = ci.splitmix64(seed ^ 0x0F1C5ED, 3 * n).reshape(n, 3)
+    lo32 = np.uint64(0xFFFFFFFF)
+    rnd = (r[:, 0] & lo32).astype(np.uint32)
+    sparse = (rnd & (r[:, 1] >> np.uint64(32)).astype(np.uint32) & (r[:, 2] & lo32).astype(np.uint32))
+    dense = rnd | (r[:, 1] & lo32).astype(np.uint32) | (r[:, 2] >> np.uint64(32)).astype(np.uint32)
+    pick = (r[:, 0] >> np.uint64(60)).astype(np.int64)          # 0..15
+    k = ((r[:, 1] >> np.uint64(27)) & np.uint64(31)).astype(np.uint32)
+    below_pow2 = (np.left_shift(np.uint32(1), k, dtype=np.uint32) - np.uint32(1)).astype(np.uint32)
+    rec = ops[:, 0] == 0
+    mode = np.select([pick < 5, pick < 9, pick < 15], [4, 2, 1], 1).astype(np.uint32)   # AND, OR, ADD
+    val = np.select([pick < 5, pick < 9, pick < 11, pick < 13, pick < 14],
+                    [sparse, dense, rnd & np.uint32(15), below_pow2, np.uint32(0xFFFFFFFF)], rnd).astype(np.uint32)
+    ops[rec, 1] = mode[rec]
+    ops[rec, 2] = val[rec]
+    wait = ~rec
+    bitmask = wait & (pick < 8)
+    ops[bitmask, 1] = 4                                            # EQUAL_WITH_BITMASK
+    ops[bitmask, 2] = np.where(pick[bitmask] < 4, sparse[bitmask], rnd[bitmask] & np.uint32(7))
+    ops[wait, 3] = (pick[wait] & 1).astype(np.uint32)
+    return ops
+
+
+@pytest.mark.parametrize("n,seed", [(3_000, 1), (70_001, 2), (1_000_000, 3)])
+def test_statemachine_near_fixing_ops(cns, n, seed):
+    """The known-bits cut on ops chosen to sit at its edges (no SET record):
+    bit for bit against the sequential oracle."""
+    ops = _near_fixing_ops(n, seed)
+    assert not ((ops[:, 0] == 0) & (ops[:, 1] == 0)).any()
+    got_t, got_f = run_sm(cns, ops, 0x80000001)
+    want_t, want_f = oracle.cnt_statemachine(ops, 0x80000001)
+    np.testing.assert_array_equal(got_t, want_t)
+    assert got_f == want_f
+
+
+def test_statemachine_fixing_ops_by_hand(cns):
+    """Short hand-made streams where a known count is reached without a SET,
+    each after a different count: an AND then an OR; an AND, an add whose
+    carry stops in known bits, then an OR; a bitmask wait decided by one
+    known bit that releases and clears (outcome RELEASED, count 0); and the
+    same wait undecided (the count stays unknown)."""
+    AND, OR, ADD = 4, 2, 1
+    WAIT, EQB = 1, 4
+    pad = [[WAIT, 3, 0, 0]] * 9          # waits that fix nothing, to move the ops across chunks
+    streams = [
+        [[0, AND, 0x3, 0], [0, OR, 0x3, 0]],
+        [[0, AND, 0xF0, 0], [0, ADD, 5, 0], [0, OR, 0xF0, 0], [0, ADD, 0xFFFFFFFF, 0]],
+        [[0, OR, 1, 0], [WAIT, EQB, 1, 1], [0, ADD, 7, 0]],
+        [[0, ADD, 1, 0], [WAIT, EQB, 1, 1], [0, ADD, 7, 0]],
+    ]
+    for init in (0, 6, 0xFFFFFFFF):
+        for st in streams:
+            for lead in (0, 3, 7, 8, 15):
+                ops = np.array(pad[:lead] + st + pad[:5], dtype=np.uint32).reshape(-1, 4)
+                got_t, got_f = run_sm(cns, ops, init)
+                want_t, want_f = oracle.cnt_statemachine(ops, init)
+                np.testing.assert_array_equal(got_t, want_t)
+                assert got_f == want_f
 
 
 def _fused_limit():
@@ -242,14 +321,23 @@ def test_statemachine_spread_over_all_ctas(cns, n):
     assert got_f == want_f
 
 
+def _chain_ops(n, seed):
+    """Ops that never fix the count: every record an ADD, no clearing wait (an
+    add of a constant to a count with unknown bits leaves them unknown, and a
+    wait that does not clear changes nothing)."""
+    ops = ci.notify_ops(n, seed=seed)
+    ops[ops[:, 0] == 0, 1] = 1
+    ops[:, 3] = 0
+    return ops
+
+
 @pytest.mark.parametrize("gap", [1000, 9000, 70000])
 def test_statemachine_rare_sets(cns, gap):
-    """SET records only every `gap` ops: chains cross many CTAs (each CTA
-    without a SET waits for the one before it and replays all its ops)."""
-    ops = ci.notify_ops(400_000, seed=gap)
-    is_set = (ops[:, 0] == 0) & (ops[:, 1] == 0)
-    ops[is_set, 1] = 1                                   # every SET becomes an ADD ...
-    ops[::gap, 0] = 0                                    # ... except one every `gap` ops
+    """SET records only every `gap` ops, and no other op that fixes the count:
+    chains cross many CTAs (each tile without a SET waits for the one before
+    it and replays all its ops)."""
+    ops = _chain_ops(400_000, gap)
+    ops[::gap, 0] = 0                                    # a SET every `gap` ops
     ops[::gap, 1] = 0
     got_t, got_f = run_sm(cns, ops, 11)
     want_t, want_f = oracle.cnt_statemachine(ops, 11)
