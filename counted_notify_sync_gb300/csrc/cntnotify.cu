@@ -378,12 +378,12 @@ __device__ __forceinline__ bool sm_known_step(uint32_t &kz, uint32_t &ko, const 
     return decided;
 }
 
-// A tile looks for fixing ops only when this many of its chunks in a row hold
-// no SET (a stretch between SETs, or in front of the first, of more than
-// kFixRun * 8 ops), or when it holds no SET at all (its count would otherwise
-// wait for the tiles before it).  Shorter stretches are walked sooner than the
-// search would run.
-constexpr int kFixRun = 16;
+// A tile looks for fixing ops only when this many words of its start bits in a
+// row (32 ops each) hold no SET -- a stretch between SETs, or in front of the
+// first, of at least kFixWords * 32 ops -- or when it holds no SET at all (its
+// count would otherwise wait for the tiles before it).  Shorter stretches are
+// walked sooner than the search would run.
+constexpr int kFixWords = 3;
 
 constexpr uint64_t kSmLinkTimeoutNs = 10ull * 1000000000ull;
 
@@ -520,16 +520,16 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
         __syncthreads();
         const bool last_tile = base + cnt == n;
         const int chunk0 = k * kFChunk;
-        const uint8_t *s_setb = reinterpret_cast<const uint8_t *>(s_setm);   // byte k: chunk k
-        // chunks k .. k + kFixRun - 1 of the tile hold no SET, or the tile holds none at all
-        const int chunks = (cnt + kFChunk - 1) / kFChunk;
+        // words k .. k + kFixWords - 1 of the start bits (4 chunks each) hold no SET, or the tile
+        // holds none at all
+        const int words = (cnt + 32 - 1) / 32;
         bool gap = false;
-        if (k < chunks) {
-            const int upto = min(chunks, k + kFixRun);
-            bool clear = true;
-            for (int j = k; j < upto && clear; ++j)
-                clear = s_setb[j] == 0u;
-            gap = clear && (upto - k == kFixRun || (k == 0 && upto == chunks));
+        if (k < words) {
+            const int upto = min(words, k + kFixWords);
+            uint32_t any = 0u;
+            for (int j = k; j < upto; ++j)
+                any |= s_setm[j];
+            gap = any == 0u && (upto - k == kFixWords || (k == 0 && upto == words));
         }
         if (__syncthreads_or(gap)) {
             // F: a stretch between SETs (or in front of the first) is long enough that the
