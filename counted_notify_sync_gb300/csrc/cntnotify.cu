@@ -568,13 +568,17 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
                 wbase = atomicAdd(&s_cls[cls], __popc(same));
             wbase = __shfl_sync(0xffffffffu, wbase, leader) + __popc(same & ((1u << lane) - 1u));
             __syncthreads();
-            if (k == 0) {
-                int acc = 0;
-                for (int q = 0; q < kJobClasses; ++q) {
-                    const int n_q = s_cls[q];
-                    s_cls[q] = acc;
-                    acc += n_q;
+            if (k < 32) {   // exclusive scan of the class counts, one class per lane of warp 0
+                const int n_q = k < kJobClasses ? s_cls[k] : 0;
+                int incl = n_q;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int up = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d)
+                        incl += up;
                 }
+                if (k < kJobClasses)
+                    s_cls[k] = incl - n_q;
             }
             __syncthreads();
             if (len > 0)
