@@ -259,11 +259,14 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 // as a run of tiles without one in front of it (a stream of adds alone, for
 // instance, has none: it is one dependent chain).  Every CTA is resident
 // (cooperative launch) and takes its tiles in increasing order, so the tile a
-// CTA waits for is always held by a running CTA (or done).  The tag makes the link words
-// need no initial content: a word holds (tag << 32) | count, and a word from
-// an earlier call carries an earlier tag.  The wait is bounded; if it runs out
-// (only a stalled GPU can make it), the tile's leading entries get count 0 and
-// outcome CNS_OUT_INVALID.
+// CTA waits for is always held by a running CTA (or done).  The tag makes the
+// link words need no initial content: a word holds (tag << 32) | count, and a
+// word from an earlier call carries an earlier tag.  A replay of a CUDA graph
+// that captured the call repeats the call's tag, so the thread that takes a
+// word sets it to 0 (no call has tag 0): the only word a launch leaves behind
+// is its last tile's, which no tile of a launch of the same size reads.  The
+// wait is bounded; if it runs out (only a stalled GPU can make it), the tile's
+// leading entries get count 0 and outcome CNS_OUT_INVALID.
 // ---------------------------------------------------------------------------
 
 // Granularity of cns_statemachine_scratch_bytes (8 bytes per 16 ops): at
@@ -599,6 +602,8 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
             const int lead = f_next_set(s_setm, 0, cnt);
             uint32_t cp = init;
             if (t == 0 || sm_take(link + t - 1, tag, &cp)) {
+                if (t > 0)   // taken: tag 0 is no call's, so no later launch can take this word again
+                    *reinterpret_cast<volatile uint64_t *>(link + t - 1) = 0ull;
                 cp = f_walk(s_ops, s_tr, 0, lead, cp);
             } else {
                 for (int i = 0; i < lead; ++i)

@@ -569,7 +569,10 @@ size_t cns_statemachine_scratch_bytes(int64_t n);
  *   scratch_dev  cns_statemachine_scratch_bytes(n) bytes, no initial content
  *   stream       stream to run on (asynchronous)
  * The result is the sequential result exactly; the kernels split the stream
- * at SET records (whose result does not depend on the count before them).
+ * at SET records (whose result does not depend on the count before them) and,
+ * where SETs are far apart, at ops after which every bit of the count is
+ * known whatever came before.  The call may be captured into a CUDA graph:
+ * each replay gives the sequential result of the ops the buffer then holds.
  * Errors: NULL_PTR, INVALID_VALUE (n < 0, alignment, scratch too small), CUDA.
  */
 int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t init, uint32_t *trace_dev,

@@ -365,6 +365,69 @@ def test_statemachine_back_to_back_calls_reuse_scratch(cns):
         assert int(final.cpu().numpy().view(np.uint32)[0]) == want_f
 
 
+@pytest.mark.parametrize("n,kind", [(200_000, "bench"), (1_300_000, "bench"), (300_000, "chain")])
+def test_statemachine_replayed_from_a_cuda_graph(cns, n, kind):
+    """The call captured once into a CUDA graph and replayed with new ops in the same buffer each time:
+    every replay bit for bit against the oracle.  A replay repeats the captured call's link tag, so a
+    link word left by the previous replay must never be taken (streams with one tile per CTA, several
+    waves of tiles, and one long chain through every tile)."""
+    import torch
+    streams = [(_chain_ops(n, s) if kind == "chain" else ci.notify_ops(n, seed=s)) for s in (41, 42, 43)]
+    d = to_dev_u32(streams[0])
+    trace = torch.empty((n, 2), dtype=torch.int32, device="cuda")
+    final = torch.empty(1, dtype=torch.int32, device="cuda")
+    sb = cns.cns_statemachine_scratch_bytes(n)
+    scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+
+    def call():
+        cns.check(cns.cns_statemachine_run(d, n, 9, trace, final, scratch, sb, torch.cuda.current_stream()),
+                  "statemachine")
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        call()
+    for ops in (streams[1], streams[2], streams[0], streams[1]):
+        d.copy_(to_dev_u32(ops))
+        g.replay()
+        torch.cuda.synchronize()
+        want_t, want_f = oracle.cnt_statemachine(ops, 9)
+        np.testing.assert_array_equal(from_dev_u32(trace), want_t)
+        assert int(from_dev_u32(final)[0]) == want_f
+
+
+def test_statemachine_noalloc_replayed_from_a_cuda_graph(cns):
+    """The allocation-free entry point, captured into a CUDA graph and replayed with new ops."""
+    import torch
+    n = 250_000
+    streams = [ci.notify_ops(n, seed=s) for s in (51, 52)]
+    d = to_dev_u32(streams[0])
+    trace = torch.empty((n, 2), dtype=torch.int32, device="cuda")
+    final = torch.empty(1, dtype=torch.int32, device="cuda")
+    L = cns._native.lib()
+    side = torch.cuda.Stream()
+
+    def call():
+        rc = L.cns_statemachine_run_noalloc(d.data_ptr(), n, 3, trace.data_ptr(), final.data_ptr(),
+                                            torch.cuda.current_stream().cuda_stream)
+        assert rc == cns.CNS_SUCCESS
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        call()
+    for ops in (streams[1], streams[0], streams[1]):
+        d.copy_(to_dev_u32(ops))
+        g.replay()
+        torch.cuda.synchronize()
+        want_t, want_f = oracle.cnt_statemachine(ops, 3)
+        np.testing.assert_array_equal(from_dev_u32(trace), want_t)
+        assert int(from_dev_u32(final)[0]) == want_f
+
+
 def test_statemachine_all_sets_and_invalid_ops(cns):
     ops = ci.notify_ops(3000, seed=5)
     ops[::2, 0] = 0
