@@ -374,6 +374,10 @@ typedef enum {
  * status and abort flag, and the workspace check refuses it: re-initialise it
  * before reusing it.
  *
+ * With sync = 0 and no host buffers the call may be captured into a CUDA
+ * graph: each replay runs the rounds again on what the buffers then hold, and
+ * the workspace counter carries on from replay to replay.
+ *
  * Errors: NULL_PTR (data, workspace, payload buffers the workload needs),
  * INVALID_VALUE (enum, sizes, used_cores > launched CTAs, cluster shape,
  * alignment), ARCH, NOT_RESIDENT, CUDA; with sync=1 also TIMEOUT when a

@@ -958,3 +958,48 @@ def test_release_fence_probe(cns):
     out = torch.zeros(3, dtype=torch.int64, device="cuda")
     assert cns.cns_probe_release_fence(raw[off:], 10, out) == cns.CNS_ERR_INVALID_VALUE
     assert cns.cns_probe_release_fence(raw, 0, out) == cns.CNS_ERR_INVALID_VALUE   # no samples
+
+
+# --- the run captured into a CUDA graph --------------------------------------------------
+
+@pytest.mark.parametrize("mode,variant,wl,P,slots", [
+    (SOFT, 5, "rotate", 148, 4),        # the headline's solo rounds through the per-die copies
+    (SOFT, 5, "xorshift", 64, 256),     # 1 KB rows through the copies, every thread moving them
+    (SOFT, 0, "affine", 8, 256),        # the guide's counter poll, no copies
+    (HARD, 5, "rotate", 148, 4),        # clusters of 2, one arrival per cluster
+])
+def test_syncall_replayed_from_a_cuda_graph(cns, mode, variant, wl, P, slots):
+    """syncall_run captured once into a CUDA graph and replayed with a new payload in buf0 each time:
+    every replay's result against the oracle, and the counter carrying on from replay to replay."""
+    import torch
+    wl_c = {"rotate": cns.CNS_WL_RING_ROTATE, "xorshift": cns.CNS_WL_XORSHIFT, "affine": cns.CNS_WL_RING_AFFINE}[wl]
+    wl_o = {"rotate": oracle.WL_RING_ROTATE, "xorshift": oracle.WL_XORSHIFT, "affine": oracle.WL_RING_AFFINE}[wl]
+    R = 1001
+    payloads = [ci.ring_payload(seed, P, slots) for seed in (61, 62, 63)]
+    b0 = to_dev_u32(payloads[0])
+    b1 = torch.zeros_like(b0)
+    ws = cns.new_workspace(participants=P, elems=slots)
+    side = torch.cuda.Stream()
+
+    def call():
+        cns.run_syncall(mode, AIV, wl_c, P, b0, b1, R, elems=slots, workspace=ws, variant=variant, sync=False,
+                        stream=torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        call()
+    runs = 1
+    for v in (payloads[1], payloads[2], payloads[0]):
+        b0.copy_(to_dev_u32(v))
+        g.replay()
+        torch.cuda.synchronize()
+        runs += 1
+        want, _ = expect_ring(wl_o, v, R)
+        np.testing.assert_array_equal(from_dev_u32(b1).reshape(P, slots), want)
+        rc, soft, hard, st = cns.syncall_read_workspace(ws)
+        assert rc == 0 and st == 0
+        arrivals = P if mode == SOFT else P // 2
+        counter = soft if mode == SOFT else hard
+        assert counter == (runs * R * arrivals) % oracle.counter_modulus(arrivals)
