@@ -457,7 +457,27 @@ def secondary(cns, torch, peaks):
         ok = ok and rc_async == 0 and cns.cntnotify_query_status(done)[1] == 0 \
             and cns.cntnotify_query_status(ack)[1] == 0 \
             and np.array_equal(bufs[1].cpu().numpy().view(np.uint32), want_cs)
+        # the same run captured once into a CUDA graph (sync = 0) and replayed: no host work per round
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s1):
+            _, rc_g, _, _ = cns.run_pipeline(done, ack, 4096, 256, 1000, s1, s2, timeout_s=10, buffers=bufs,
+                                             areas=areas, consumer_wait=cw, sync=False)
+        graph.replay()   # warm-up (the first replay uploads the graph)
+        torch.cuda.synchronize()
+        g_best = None
+        for _ in range(3):
+            bufs[1].zero_()
+            ms_g, _ = timed_run(torch, graph.replay)
+            g_ok = rc_g == 0 and cns.cntnotify_query_status(done)[1] == 0 \
+                and cns.cntnotify_query_status(ack)[1] == 0 \
+                and np.array_equal(bufs[1].cpu().numpy().view(np.uint32), want_cs)
+            if g_best is None or ms_g < g_best[0]:
+                g_best = (ms_g, g_ok)
+        del graph
         by_areas[areas, cw] = {
+            "graph_replay_us_per_round": round(g_best[0], 3),
+            "graph_round_trips_per_s": round(1000 / max(g_best[0] * 1e-3, 1e-12), 1),
+            "graph_correct": bool(g_best[1]),
             "status": rc, "correct": bool(ok), "elapsed_ms": round(cfg.elapsed_ms, 3),
             "producer_ms": round(cfg.producer_ms, 3),
             "records_per_s": round(4096 * 1000 / max(cfg.producer_ms * 1e-3, 1e-12), 0),
@@ -479,7 +499,8 @@ def secondary(cns, torch, peaks):
         host_launch_us=round(launch_us, 3),
         note="best of 3 runs; records/s over the summed recording phases (device clock: from the producer's "
              "CTA 0 being allowed to record to the consumer-side wait releasing), round trips/s over the whole "
-             "run (events)")
+             "run (events); graph_*: the same call captured once into a CUDA graph and replayed (best of 3 "
+             "replays after one warm-up, events around the replay; 1000 rounds per replay)")
 
     # op-stream state machine, 1e6 ops: buffers allocated once, 20 back-to-back C-ABI calls timed (warm L2),
     # and calls with L2 flushed before each one (cold, each timed alone); then a stream without SET records

@@ -682,7 +682,10 @@ typedef struct {
  *     producer stream, freed at the end); its other CTAs wait for that word.
  *     One launch a round fewer; the results are the same.
  * The call first clears both notifies (count and status); `done` ends at 0
- * and `ack` at rounds * consumer_ctas (mod 2^32).  Once a wait times out the pipeline's remaining
+ * and `ack` at rounds * consumer_ctas (mod 2^32).  With sync = 0 the call may
+ * be captured into a CUDA graph on the producer stream (the consumer stream
+ * joins the capture through an event, and returns to it at the end): a
+ * replay runs the whole pipeline with no host work per round.  Once a wait times out the pipeline's remaining
  * waits return at once, so a lost signal costs one timeout, not one per round.
  * Errors: INVALID_HANDLE, NULL_PTR, INVALID_VALUE (also areas outside 0..2,
  * consumer_wait outside 0..1), CUDA; with sync=1 also TIMEOUT.

@@ -468,6 +468,42 @@ def test_pipeline_4096_tiles_1000_rounds(cns, areas, consumer_wait):
 
 
 @pytest.mark.parametrize("consumer_wait", [0, 1])
+@pytest.mark.parametrize("areas", [1, 2])
+def test_pipeline_replayed_from_a_cuda_graph(cns, areas, consumer_wait):
+    """cns_pipeline_run (sync = 0) captured once into a CUDA graph, the consumer stream joined into the
+    capture, and replayed: every replay's checksums and release counts against the oracle, both notifies
+    back at their end counts, no timeout."""
+    import torch
+    rc, done = cns.cntnotify_create(0)
+    rc2, ack = cns.cntnotify_create(0)
+    assert rc == rc2 == 0
+    try:
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        tiles, words, rounds = 4096, 64, 300
+        bufs = (torch.empty(areas * tiles * words, dtype=torch.int32, device="cuda"),
+                torch.empty(rounds, dtype=torch.int32, device="cuda"),
+                torch.empty(rounds, dtype=torch.int32, device="cuda"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s1):
+            cfg, rc, _, _ = cns.run_pipeline(done, ack, tiles, words, rounds, s1, s2, timeout_s=10, sync=False,
+                                             buffers=bufs, areas=areas, consumer_wait=consumer_wait)
+        assert rc == 0
+        want_cs, want_rel = oracle.pipeline(tiles, words, rounds)
+        for _ in range(3):
+            bufs[1].zero_()
+            bufs[2].zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(from_dev_u32(bufs[1]), want_cs)
+            np.testing.assert_array_equal(from_dev_u32(bufs[2]), want_rel)
+            assert count_of(cns, done) == (0, 0)
+            assert count_of(cns, ack) == (0, (rounds * cfg.consumer_ctas) % (1 << 32))
+    finally:
+        cns.cntnotify_destroy(done)
+        cns.cntnotify_destroy(ack)
+
+
+@pytest.mark.parametrize("consumer_wait", [0, 1])
 @pytest.mark.parametrize("areas", [0, 1, 2])
 def test_pipeline_small_odd_shapes(cns, areas, consumer_wait):
     import torch
