@@ -530,17 +530,27 @@ def secondary(cns, torch, peaks):
             flush.zero_()
             ms_c, _ = timed_run(torch, lambda: calls(1))
             cold.append(ms_c)
-        return warm, statistics.median(cold)
+        graph_ms = None
+        if label_reps >= 20:   # the same calls replayed from a CUDA graph: no host work, no launch gaps
+            side = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                calls(label_reps)
+            g.replay()
+            torch.cuda.synchronize()
+            graph_ms = min(timed_run(torch, g.replay)[0] for _ in range(3)) / label_reps
+            del g
+        return warm, statistics.median(cold), graph_ms
 
-    warm, cold = statemachine_figures(ci.notify_ops(n))
+    warm, cold, graph_sm = statemachine_figures(ci.notify_ops(n))
     ops_sf = ci.notify_ops(n + n // 7, seed=ci.SEED_NOTIFY_OPS ^ 0x5E7F)
     ops_sf = np.ascontiguousarray(ops_sf[~((ops_sf[:, 0] == 0) & (ops_sf[:, 1] == 0))][:n])   # no SET record
-    warm_sf, cold_sf = statemachine_figures(ops_sf)
+    warm_sf, cold_sf, _ = statemachine_figures(ops_sf)
     ops_ch = ci.notify_ops(n, seed=ci.SEED_NOTIFY_OPS ^ 0xC4A1)
     ops_ch[ops_ch[:, 0] == 0, 1] = 1          # every record an ADD
     ops_ch[:, 3] = 0                          # and no clearing wait: nothing ever fixes the count
     ops_ch = np.ascontiguousarray(ops_ch)
-    warm_ch, cold_ch = statemachine_figures(ops_ch, label_reps=3)
+    warm_ch, cold_ch, _ = statemachine_figures(ops_ch, label_reps=3)
     chain_ops = torch.from_numpy(np.ascontiguousarray(ops_ch[:16]).view(np.int32)).cuda()
     chain_out = torch.zeros(2, dtype=torch.int64, device="cuda")
     iters = 20000
@@ -554,6 +564,7 @@ def secondary(cns, torch, peaks):
 
     out["notify_statemachine_1e6"] = {
         "ms": round(warm, 4), "ops_per_s": round(n / (warm * 1e-3), 0), "bytes_per_op": 24,
+        "graph_replay_ms": round(graph_sm, 4) if graph_sm else None,
         "gbs_algorithmic": round(24 * n / (warm * 1e-3) / 1e9, 1),
         "cold_l2_ms": round(cold, 4), "cold_l2_ops_per_s": round(n / (cold * 1e-3), 0),
         "cold_l2_frac_of_measured_hbm": hbm_frac(cold),
