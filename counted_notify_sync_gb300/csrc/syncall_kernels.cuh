@@ -403,6 +403,45 @@ __device__ __forceinline__ void mirror_move(const SyncallParams &p, MirrorState 
         st_relaxed_gpu_v4(static_cast<uint4 *>(k ? p.buf0 : p.buf1) + b_row + i, v);
 }
 
+// mirror_move's rounds for rows of one uint4 moved by thread 0, with the
+// loop's addresses fixed before it: the row is read from region r & 1 in the
+// block of its pair on this SM's die (from buffer 0 in round 0) and written
+// into both blocks of region (r & 1) ^ 1 (and, in the last two rounds, into
+// the caller's buffer).  Worked out from the round number each time, as
+// mirror_move does, the addresses cost ~25 ns a round on the chain.  Returns
+// true if the caller must stop.
+template <int WL, int V>
+__device__ __forceinline__ bool solo_copy_rounds(const SyncallParams &p, Barrier &bar, EpochCursor &cursor,
+                                                 MirrorState m, uint32_t q, uint32_t b, uint32_t q_slot,
+                                                 uint32_t b_slot)
+{
+    uint4 *base = reinterpret_cast<uint4 *>(p.mirror);
+    const uint4 *src0 = base + q_slot + (m.near_bits & 1u) * kMirrorBlock4;
+    const uint4 *src1 = base + p.mirror_region4 + q_slot + ((m.near_bits >> 1) & 1u) * kMirrorBlock4;
+    uint4 *dst0 = base + b_slot;                      // region 0, written in odd rounds
+    uint4 *dst1 = base + p.mirror_region4 + b_slot;   // region 1, written in even rounds
+    const uint4 *first = static_cast<const uint4 *>(p.buf0) + q;
+    uint4 *last0 = static_cast<uint4 *>(p.buf0) + b, *last1 = static_cast<uint4 *>(p.buf1) + b;
+    const int64_t R = p.rounds;
+    for (int64_t r = 0; r < R; ++r) {
+        const bool odd = (r & 1) != 0;
+        uint4 v = ld_relaxed_gpu_v4(r == 0 ? first : (odd ? src1 : src0));
+        const uint32_t rr = static_cast<uint32_t>(r);
+        v.x = ring_op<WL>(v.x, rr);
+        v.y = ring_op<WL>(v.y, rr);
+        v.z = ring_op<WL>(v.z, rr);
+        v.w = ring_op<WL>(v.w, rr);
+        uint4 *dst = odd ? dst0 : dst1;
+        st_relaxed_gpu_v4(dst, v);
+        st_relaxed_gpu_v4(dst + kMirrorBlock4, v);
+        if (r + 2 >= R)
+            st_relaxed_gpu_v4(odd ? last0 : last1, v);
+        if (arrive_and_wait<V>(bar, cursor, rr, b))
+            return true;
+    }
+    return false;
+}
+
 // The soft rounds when thread 0 alone touches memory (no payload, or a row of
 // one uint4 or one word): the other threads of the CTA have left, and the
 // barrier needs no drain and no closing block barrier -- thread 0 arrives
@@ -432,20 +471,20 @@ __device__ __forceinline__ void solo_rounds(const SyncallParams &p, uint32_t b, 
     }
     EpochCursor cursor{0u, 0u, false};
     bool stop = false;
-    for (int64_t r = 0; r < p.rounds; ++r) {
-        if (WL != CNS_WL_EMPTY) {
-            if (mirrored) {
-                mirror_move<WL>(p, m, q_slot, b_slot, q, b, r, 0u);
-            } else {
+    if (WL != CNS_WL_EMPTY && mirrored) {
+        stop = solo_copy_rounds<WL, V>(p, bar, cursor, m, q, b, q_slot, b_slot);
+    } else {
+        for (int64_t r = 0; r < p.rounds; ++r) {
+            if (WL != CNS_WL_EMPTY) {
                 const bool odd = (r & 1) != 0;
                 ring_phase<WL>(static_cast<const uint32_t *>(odd ? p.buf1 : p.buf0),
                                static_cast<uint32_t *>(odd ? p.buf0 : p.buf1), b, p.P, p.elems,
                                static_cast<uint32_t>(r));
             }
+            stop = arrive_and_wait<V>(bar, cursor, static_cast<uint32_t>(r), b);
+            if (stop)
+                break;
         }
-        stop = arrive_and_wait<V>(bar, cursor, static_cast<uint32_t>(r), b);
-        if (stop)
-            break;
     }
     if (b == 0 && !stop)
         record_base<V>(p, bar, base_word, base);
