@@ -377,69 +377,53 @@ __device__ __forceinline__ MirrorState mirror_setup(const SyncallParams &p, uint
     return m;
 }
 
-// Uint4 i of round r for participant b: read uint4 i of the neighbour's row
-// from region r & 1 (buffer 0 in round 0), write the result into both blocks
-// of b's pair in the other region (and, in the last two rounds, into the
-// caller's buffer).  row4 uint4 per row; q_slot / b_slot from mirror_slot;
-// q_row / b_row the rows' uint4 offsets in the caller's buffers.
-template <int WL>
-__device__ __forceinline__ void mirror_move(const SyncallParams &p, MirrorState m, uint32_t q_slot,
-                                            uint32_t b_slot, int64_t q_row, int64_t b_row, int64_t r, uint32_t i)
+// The addresses one participant's rows use through the copies, fixed for the
+// whole run: round r reads the neighbour's row from region r & 1, in the block
+// of its pair on this SM's die (from buffer 0 in round 0), and writes its own
+// row into both blocks of region (r & 1) ^ 1 (and, in the last two rounds,
+// into the caller's buffer: buffer 1 after an even round, 0 after an odd one).
+// Worked out from the round number in every round instead, the addresses cost
+// ~25 ns a round of the headline on the chain from the acquire to the stores.
+struct MirrorRow {
+    const uint4 *src0, *src1;   // the neighbour's row, region 0 / 1, near block
+    uint4 *dst0, *dst1;         // this row, region 0 / 1, first block (the other is kMirrorBlock4 on)
+    const uint4 *first;         // the neighbour's row in buffer 0 (round 0)
+    uint4 *last0, *last1;       // this row in buffer 0 / 1
+};
+
+// q / b the neighbour's and this participant's index, row4 uint4 per row,
+// q_slot / b_slot from mirror_slot, m from mirror_setup.
+__device__ __forceinline__ MirrorRow mirror_row(const SyncallParams &p, MirrorState m, uint32_t q, uint32_t b,
+                                                uint32_t row4, uint32_t q_slot, uint32_t b_slot)
 {
-    const uint32_t k = static_cast<uint32_t>(r) & 1u;
     uint4 *base = reinterpret_cast<uint4 *>(p.mirror);
-    const uint4 *src = (r == 0) ? static_cast<const uint4 *>(p.buf0) + q_row + i
-                                : base + k * p.mirror_region4 + q_slot + ((m.near_bits >> k) & 1u) * kMirrorBlock4 + i;
-    uint4 v = ld_relaxed_gpu_v4(src);
+    MirrorRow w;
+    w.src0 = base + q_slot + (m.near_bits & 1u) * kMirrorBlock4;
+    w.src1 = base + p.mirror_region4 + q_slot + ((m.near_bits >> 1) & 1u) * kMirrorBlock4;
+    w.dst0 = base + b_slot;
+    w.dst1 = base + p.mirror_region4 + b_slot;
+    w.first = static_cast<const uint4 *>(p.buf0) + static_cast<int64_t>(q) * row4;
+    w.last0 = static_cast<uint4 *>(p.buf0) + static_cast<int64_t>(b) * row4;
+    w.last1 = static_cast<uint4 *>(p.buf1) + static_cast<int64_t>(b) * row4;
+    return w;
+}
+
+// Uint4 i of round r (of R) through the copies.
+template <int WL>
+__device__ __forceinline__ void mirror_move(const MirrorRow &w, int64_t r, int64_t R, uint32_t i)
+{
+    const bool odd = (r & 1) != 0;
+    uint4 v = ld_relaxed_gpu_v4((r == 0 ? w.first : (odd ? w.src1 : w.src0)) + i);
     const uint32_t rr = static_cast<uint32_t>(r);
     v.x = ring_op<WL>(v.x, rr);
     v.y = ring_op<WL>(v.y, rr);
     v.z = ring_op<WL>(v.z, rr);
     v.w = ring_op<WL>(v.w, rr);
-    uint4 *dst = base + (k ^ 1u) * p.mirror_region4 + b_slot + i;
+    uint4 *dst = (odd ? w.dst0 : w.dst1) + i;
     st_relaxed_gpu_v4(dst, v);
     st_relaxed_gpu_v4(dst + kMirrorBlock4, v);
-    if (r + 2 >= p.rounds)
-        st_relaxed_gpu_v4(static_cast<uint4 *>(k ? p.buf0 : p.buf1) + b_row + i, v);
-}
-
-// mirror_move's rounds for rows of one uint4 moved by thread 0, with the
-// loop's addresses fixed before it: the row is read from region r & 1 in the
-// block of its pair on this SM's die (from buffer 0 in round 0) and written
-// into both blocks of region (r & 1) ^ 1 (and, in the last two rounds, into
-// the caller's buffer).  Worked out from the round number each time, as
-// mirror_move does, the addresses cost ~25 ns a round on the chain.  Returns
-// true if the caller must stop.
-template <int WL, int V>
-__device__ __forceinline__ bool solo_copy_rounds(const SyncallParams &p, Barrier &bar, EpochCursor &cursor,
-                                                 MirrorState m, uint32_t q, uint32_t b, uint32_t q_slot,
-                                                 uint32_t b_slot)
-{
-    uint4 *base = reinterpret_cast<uint4 *>(p.mirror);
-    const uint4 *src0 = base + q_slot + (m.near_bits & 1u) * kMirrorBlock4;
-    const uint4 *src1 = base + p.mirror_region4 + q_slot + ((m.near_bits >> 1) & 1u) * kMirrorBlock4;
-    uint4 *dst0 = base + b_slot;                      // region 0, written in odd rounds
-    uint4 *dst1 = base + p.mirror_region4 + b_slot;   // region 1, written in even rounds
-    const uint4 *first = static_cast<const uint4 *>(p.buf0) + q;
-    uint4 *last0 = static_cast<uint4 *>(p.buf0) + b, *last1 = static_cast<uint4 *>(p.buf1) + b;
-    const int64_t R = p.rounds;
-    for (int64_t r = 0; r < R; ++r) {
-        const bool odd = (r & 1) != 0;
-        uint4 v = ld_relaxed_gpu_v4(r == 0 ? first : (odd ? src1 : src0));
-        const uint32_t rr = static_cast<uint32_t>(r);
-        v.x = ring_op<WL>(v.x, rr);
-        v.y = ring_op<WL>(v.y, rr);
-        v.z = ring_op<WL>(v.z, rr);
-        v.w = ring_op<WL>(v.w, rr);
-        uint4 *dst = odd ? dst0 : dst1;
-        st_relaxed_gpu_v4(dst, v);
-        st_relaxed_gpu_v4(dst + kMirrorBlock4, v);
-        if (r + 2 >= R)
-            st_relaxed_gpu_v4(odd ? last0 : last1, v);
-        if (arrive_and_wait<V>(bar, cursor, rr, b))
-            return true;
-    }
-    return false;
+    if (r + 2 >= R)
+        st_relaxed_gpu_v4((odd ? w.last0 : w.last1) + i, v);
 }
 
 // The soft rounds when thread 0 alone touches memory (no payload, or a row of
@@ -472,7 +456,12 @@ __device__ __forceinline__ void solo_rounds(const SyncallParams &p, uint32_t b, 
     EpochCursor cursor{0u, 0u, false};
     bool stop = false;
     if (WL != CNS_WL_EMPTY && mirrored) {
-        stop = solo_copy_rounds<WL, V>(p, bar, cursor, m, q, b, q_slot, b_slot);
+        const MirrorRow w = mirror_row(p, m, q, b, 1u, q_slot, b_slot);
+        const int64_t R = p.rounds;
+        for (int64_t r = 0; r < R && !stop; ++r) {
+            mirror_move<WL>(w, r, R, 0u);
+            stop = arrive_and_wait<V>(bar, cursor, static_cast<uint32_t>(r), b);
+        }
     } else {
         for (int64_t r = 0; r < p.rounds; ++r) {
             if (WL != CNS_WL_EMPTY) {
@@ -631,26 +620,22 @@ __global__ void __launch_bounds__(1024) syncall_kernel(const SyncallParams p)
         // variant, on a workspace with room for them) thread 0 moves the row.
         auto rounds = [&](auto with_copies) {
             constexpr bool kCopies = decltype(with_copies)::value;
-            MirrorState m{0u};
-            uint32_t row4 = 0, q_slot = 0, b_slot = 0;
-            int64_t q_row = 0, b_row = 0;
+            uint32_t row4 = 0;
+            MirrorRow w{};
             if constexpr (kCopies) {
                 const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
                 row4 = static_cast<uint32_t>(p.elems >> 2);
-                q_slot = mirror_slot(p, q, row4);
-                b_slot = mirror_slot(p, b, row4);
-                q_row = static_cast<int64_t>(q) * row4;
-                b_row = static_cast<int64_t>(b) * row4;
+                const uint32_t q_slot = mirror_slot(p, q, row4);
                 if (threadIdx.x == 0)
                     s_near_bits = mirror_setup(p, q_slot).near_bits;
                 __syncthreads();
-                m.near_bits = s_near_bits;
+                w = mirror_row(p, MirrorState{s_near_bits}, q, b, row4, q_slot, mirror_slot(p, b, row4));
             }
             bool halt = false;
             for (int64_t r = 0; r < p.rounds; ++r) {
                 if constexpr (kCopies) {
                     for (uint32_t i = threadIdx.x; i < row4; i += blockDim.x)
-                        mirror_move<WL>(p, m, q_slot, b_slot, q_row, b_row, r, i);
+                        mirror_move<WL>(w, r, p.rounds, i);
                 } else {
                     data_phase<WL>(p, r, b, js);
                 }
