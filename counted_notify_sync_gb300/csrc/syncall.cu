@@ -65,12 +65,10 @@ __global__ void __launch_bounds__(1024) round_phase_probe_kernel(const SyncallPa
     Barrier bar = p.bar;
     choose_near_copy(bar);
     const uint32_t q = (b + 1u == p.P) ? 0u : b + 1u;
-    MirrorState m{};
-    uint32_t q_slot = 0, b_slot = 0;   // one-uint4 rows
+    MirrorRow w{};   // one-uint4 rows through the copies, as the headline kernel moves them
     if (p.mirror) {
-        q_slot = mirror_slot(p, q, 1u);
-        b_slot = mirror_slot(p, b, 1u);
-        m = mirror_setup(p, q_slot);
+        const uint32_t q_slot = mirror_slot(p, q, 1u);
+        w = mirror_row(p, mirror_setup(p, q_slot), q, b, 1u, q_slot, mirror_slot(p, b, 1u));
     }
     EpochCursor cursor{0u, 0u, false};
     const int64_t first = p.rounds - stamp_rounds;
@@ -78,19 +76,18 @@ __global__ void __launch_bounds__(1024) round_phase_probe_kernel(const SyncallPa
     bool stop = false;
     for (int64_t r = 0; r < p.rounds && !stop; ++r) {
         const uint32_t k = static_cast<uint32_t>(r) & 1u;   // reads region k (buffer k), writes the other
-        uint4 *base = reinterpret_cast<uint4 *>(p.mirror);
+        const bool odd = k != 0u;
         t[0] = globaltimer_ns();
-        const uint4 *from = p.mirror ? (r == 0 ? static_cast<const uint4 *>(p.buf0) + q
-                                               : base + k * p.mirror_region4 + q_slot + ((m.near_bits >> k) & 1u) * kMirrorBlock4)
+        const uint4 *from = p.mirror ? (r == 0 ? w.first : (odd ? w.src1 : w.src0))
                                      : static_cast<const uint4 *>(k ? p.buf1 : p.buf0) + q;
         const uint4 v = ld_relaxed_gpu_v4(from);   // ring rotate: the row as it is
         t[1] = globaltimer_after(v.x ^ v.w);
         if (p.mirror) {
-            uint4 *dst = base + (k ^ 1u) * p.mirror_region4 + b_slot;
+            uint4 *dst = odd ? w.dst0 : w.dst1;
             st_relaxed_gpu_v4(dst, v);
             st_relaxed_gpu_v4(dst + kMirrorBlock4, v);
             if (r + 2 >= p.rounds)
-                st_relaxed_gpu_v4(static_cast<uint4 *>(k ? p.buf0 : p.buf1) + b, v);
+                st_relaxed_gpu_v4(odd ? w.last0 : w.last1, v);
         } else {
             st_relaxed_gpu_v4(static_cast<uint4 *>(k ? p.buf0 : p.buf1) + b, v);
         }
