@@ -735,7 +735,8 @@ int cns_probe_grid_sync(int32_t ctas, int32_t threads, int64_t rounds, void *buf
  * cns_probe_op_chain -- the op-stream state machine's rule as one dependent
  * chain: one thread applies the 16 ops at ops_dev (four uint32 each, as in
  * cns_statemachine_run) to a count, in order, iters times over, and times it
- * with the global timer.  A stream without SET records is one such chain, so
+ * with the global timer.  A stream in which no op fixes the count (no SET
+ * record, every record an ADD, no clearing wait) is one such chain, so
  * out_dev[0] / (16 * iters) is the time per op that bounds it.
  *   ops_dev  [16][4] uint32, 16-byte aligned
  *   out_dev  uint64[2]: total nanoseconds; the final count and the sum of the
