@@ -487,15 +487,24 @@ def explore_paired(P: int, C: int, rounds: int, M: int | None = None, start: int
 #   safe_first=True   in the first round the far increment is issued only
 #                     after the near one has returned (a release increment
 #                     of the far copy orders it after the near one)
+#   release=False     no fence before an arrival (the arrival-only contract):
+#                     a participant's next increments may leave while its
+#                     last ones are still in flight (one thread's increments
+#                     of one copy land in the order they were issued; they
+#                     are all +1, so only their number matters here)
+#   near_red=True     from the second round on (cursor targets), the near
+#                     increment is fire-and-forget too and the participant
+#                     polls at once: nothing needs the near copy's old value
 
 def explore_die_local(near, rounds: int, M: int | None = None, start: int = 0, target: str = "cursor",
-                      safe_first: bool = True, max_states: int = 2_000_000) -> Result:
+                      safe_first: bool = True, release: bool = True, near_red: bool = False,
+                      max_states: int = 2_000_000) -> Result:
     P = len(near)
     arith = Arith("modular", P, M if M is not None else 4 * P)
     res = Result()
-    # participant: (k, phase, target, cursor end or -1, far pending, near pending)
-    #   phase 0 between barriers, 1 waiting for the near increment, 2 polling
-    init = ((start % arith.M, start % arith.M), tuple((0, 0, 0, -1, False, False) for _ in range(P)))
+    # participant: (k, phase, target, cursor end or -1, far increments in flight, near ones in flight)
+    #   phase 0 between barriers, 1 waiting for the returning near increment, 2 polling
+    init = ((start % arith.M, start % arith.M), tuple((0, 0, 0, -1, 0, 0) for _ in range(P)))
     seen = set()
     stack = [init]
 
@@ -523,16 +532,25 @@ def explore_die_local(near, rounds: int, M: int | None = None, start: int = 0, t
                 nc[copy] = arith.arrive(nc[copy])
                 return tuple(nc)
 
-            if pf:   # the far increment lands (any time while in flight)
-                put((k, ph, t, cend, False, pn), bump(other))
+            if pf:   # a far increment lands (any time while in flight)
+                put((k, ph, t, cend, pf - 1, pn), bump(other))
+            if pn and ph != 1:   # a fire-and-forget near increment lands
+                put((k, ph, t, cend, pf, pn - 1), bump(me))
             if k == rounds:
                 continue
             if ph == 0:
-                if pf or pn:
+                if release and (pf or pn):
                     continue   # the next arrival's fence waits for the last one's increments
+                if near_red and target == "cursor" and cend >= 0:
+                    if cend != (start + (k + 1) * P) % arith.M:
+                        res.epoch_violations += 1
+                    put((k, 2, cend, (cend + P) % arith.M, pf + 1, pn + 1))
+                    continue
+                if pn:
+                    continue   # a returning increment is issued once the last ones have landed
                 first_safe = safe_first and k == 0
-                put((k, 1, 0, cend, not first_safe, True))
-            elif ph == 1 and pn:
+                put((k, 1, 0, cend, pf + (0 if first_safe else 1), 1))
+            elif ph == 1:
                 before = cs[me]
                 if target == "cursor" and cend >= 0:
                     tgt = cend
@@ -540,14 +558,14 @@ def explore_die_local(near, rounds: int, M: int | None = None, start: int = 0, t
                     tgt = arith.target(before)
                 if tgt != (start + (k + 1) * P) % arith.M:
                     res.epoch_violations += 1
-                far_now = pf or (safe_first and k == 0)
+                far_now = pf + (1 if (safe_first and k == 0) else 0)
                 nxt = (tgt + P) % arith.M
                 if arith.reached(arith.arrive(before), tgt):
                     if not all(arrived(m, k) for m in parts):
                         res.safety_violations += 1
-                    put((k + 1, 0, 0, nxt, far_now, False), bump(me))
+                    put((k + 1, 0, 0, nxt, far_now, 0), bump(me))
                 else:
-                    put((k, 2, tgt, nxt, far_now, False), bump(me))
+                    put((k, 2, tgt, nxt, far_now, 0), bump(me))
             elif ph == 2 and arith.reached(cs[me], t):
                 if not all(arrived(m, k) for m in parts):
                     res.safety_violations += 1

@@ -233,6 +233,34 @@ def test_die_local_unordered_first_barrier_fails(near):
     assert r.epoch_violations > 0 and r.deadlocks > 0
 
 
+@pytest.mark.parametrize("near", NEARS)
+@pytest.mark.parametrize("R", [1, 2, 3])
+@pytest.mark.parametrize("release,near_red", [(False, False), (False, True), (True, True)])
+def test_die_local_arrival_forms_safe_and_live(near, R, release, near_red):
+    """The arrival-only form (no fence: a participant's next increments may leave while its last ones
+    are in flight) and the form whose near increment is fire-and-forget from the second barrier on
+    (the participant polls at once): safe, every epoch right, no deadlock."""
+    r = explore_die_local(near, R, release=release, near_red=near_red)
+    assert r.ok and r.completed > 0, r
+
+
+@pytest.mark.parametrize("near", [(0, 1), (0, 1, 1)])
+@pytest.mark.parametrize("mult", [1, 2, 3])
+def test_die_local_fire_and_forget_through_the_wrap(near, mult):
+    P = len(near)
+    M = 4 * P
+    r = explore_die_local(near, 3, M=M, start=(M - mult * P) % M, release=False, near_red=True)
+    assert r.ok and r.completed > 0, r
+
+
+@pytest.mark.parametrize("near", [(0, 1), (0, 0, 1)])
+def test_die_local_fire_and_forget_needs_the_ordered_first_barrier(near):
+    """The first barrier still takes its target from the returned value, so it still needs the far
+    increment ordered after the near one."""
+    r = explore_die_local(near, 2, safe_first=False, release=False, near_red=True)
+    assert r.epoch_violations > 0 and r.deadlocks > 0
+
+
 def test_die_local_start_off_the_epoch_grid_is_caught():
     """A count that does not start at a multiple of P (a workspace reused with another P) breaks the
     epochs on the copies: the model reports it, as the library documents for this variant."""
