@@ -269,10 +269,24 @@ static int enqueue_wait(cns_cnt_notify_s *n, cudaStream_t s, const cns_wait_info
 // leading entries get count 0 and outcome CNS_OUT_INVALID.
 // ---------------------------------------------------------------------------
 
-// Granularity of cns_statemachine_scratch_bytes (8 bytes per 16 ops): at
-// least the one link word per tile the kernel uses (a tile holds 16 ops or
-// more).
-constexpr int kChunk = 16;
+// The link words between tiles, one to a 128-byte line: a tile's word is
+// written once and polled by the next tile's CTA, and words that shared lines
+// (16 to a line) made every call ~1.4 us slower (1e6 ops, an A/B on one box).
+// A tile holds 16 to 4096 ops, and the kernel has at most kMaxSmCtas CTAs, so
+// a call has at most min(ceil(n / 16), max(ceil(n / 4096), kMaxSmCtas)) tiles.
+constexpr int kLinkStride = 16;   // uint64 words from one tile's link word to the next
+constexpr int64_t kMaxSmCtas = 4096;
+constexpr int64_t sm_max_tiles(int64_t n)
+{
+    return n <= 0 ? 0
+                  : ((n + 15) / 16 < ((n + 4095) / 4096 > kMaxSmCtas ? (n + 4095) / 4096 : kMaxSmCtas)
+                         ? (n + 15) / 16
+                         : ((n + 4095) / 4096 > kMaxSmCtas ? (n + 4095) / 4096 : kMaxSmCtas));
+}
+constexpr size_t sm_scratch_bytes(int64_t n)
+{
+    return static_cast<size_t>(sm_max_tiles(n)) * kLinkStride * sizeof(uint64_t);
+}
 
 // An op turned into a micro-op that one short branch-free sequence applies
 // (neighbouring lanes of a warp apply different kinds and modes):
@@ -592,7 +606,7 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
                 const int js = static_cast<int>(s_job[k] >> 16), je = static_cast<int>(s_job[k] & 0xFFFFu);
                 const uint32_t c = f_walk(s_ops, s_tr, js, je, 0u);   // starts with a SET: any count will do
                 if (je >= cnt) {
-                    sm_publish(link + t, tag, c);
+                    sm_publish(link + t * kLinkStride, tag, c);
                     if (last_tile)
                         *final_count = c;
                 }
@@ -601,9 +615,9 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
         if (k == kFThreads - 1) {   // C, on the thread handed the shortest stretch (or none)
             const int lead = f_next_set(s_setm, 0, cnt);
             uint32_t cp = init;
-            if (t == 0 || sm_take(link + t - 1, tag, &cp)) {
+            if (t == 0 || sm_take(link + (t - 1) * kLinkStride, tag, &cp)) {
                 if (t > 0)   // taken: tag 0 is no call's, so no later launch can take this word again
-                    *reinterpret_cast<volatile uint64_t *>(link + t - 1) = 0ull;
+                    *reinterpret_cast<volatile uint64_t *>(link + (t - 1) * kLinkStride) = 0ull;
                 cp = f_walk(s_ops, s_tr, 0, lead, cp);
             } else {
                 for (int i = 0; i < lead; ++i)
@@ -611,7 +625,7 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
                 cp = 0u;
             }
             if (lead >= cnt) {
-                sm_publish(link + t, tag, cp);
+                sm_publish(link + t * kLinkStride, tag, cp);
                 if (last_tile)
                     *final_count = cp;
             }
@@ -645,7 +659,7 @@ static int sm_prepare(int device)
         CNS_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
         if (per_sm < 1)
             return CNS_ERR_CUDA;
-        g_sm_max_ctas[device] = static_cast<int64_t>(per_sm) * sms;
+        g_sm_max_ctas[device] = std::min<int64_t>(static_cast<int64_t>(per_sm) * sms, kMaxSmCtas);
         done[device] = true;
     }
     return CNS_SUCCESS;
@@ -655,8 +669,8 @@ static int sm_prepare(int device)
 // CTAs as fit at once.  A tile holds up to 4096 ops; when the GPU holds more
 // CTAs than that needs, the ops are spread evenly over all of them instead
 // (tiles of ceil(n / CTAs) ops rounded up to a multiple of 8, at least 16), so
-// that every SM gets the same share.  `link` needs one 8-byte word per tile,
-// at most one per 16 ops.
+// that every SM gets the same share.  `link` needs one 128-byte line per tile
+// (sm_scratch_bytes(n) bytes).
 static int sm_launch(const uint4 *ops, int64_t n, uint32_t init, uint2 *trace, uint64_t *link, uint32_t *final_dev,
                      int device, cudaStream_t s)
 {
@@ -1190,9 +1204,7 @@ extern "C" int cntnotify_query_status(cns_cnt_notify_t h, int32_t *status, uint3
 
 extern "C" size_t cns_statemachine_scratch_bytes(int64_t n)
 {
-    if (n <= 0)
-        return 0;
-    return static_cast<size_t>((n + kChunk - 1) / kChunk) * sizeof(uint2);
+    return sm_scratch_bytes(n);
 }
 
 extern "C" int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t init, uint32_t *trace_dev,
@@ -1236,8 +1248,8 @@ extern "C" int cns_statemachine_run(const uint32_t *ops_dev, int64_t n, uint32_t
 // again after a device reset (cudaDeviceReset destroys the context; the next
 // one loads the library's device image anew, and the array may move).
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
-static_assert(static_cast<size_t>(CNS_STATEMACHINE_NOALLOC_MAX_OPS) / kChunk * sizeof(uint2) == kNoAllocScratchBytes,
-              "the op limit must match the scratch array");
+static_assert(sm_scratch_bytes(CNS_STATEMACHINE_NOALLOC_MAX_OPS) <= kNoAllocScratchBytes,
+              "the op limit must fit the scratch array");
 static __device__ __align__(256) uint2 g_sm_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint2)];
 
 struct NoAllocScratch {

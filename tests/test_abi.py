@@ -163,8 +163,12 @@ def test_syncall_argument_checks(built):
 
 def test_statemachine_and_pipeline_argument_checks(built):
     L = _native.lib()
+    # one 128-byte line per tile: at most ceil(n / 16) tiles, and at most max(ceil(n / 4096), 4096)
     assert cns.cns_statemachine_scratch_bytes(0) == 0
-    assert cns.cns_statemachine_scratch_bytes(17) == 16
+    assert cns.cns_statemachine_scratch_bytes(17) == 2 * 128
+    assert cns.cns_statemachine_scratch_bytes(16 * 4096) == 4096 * 128
+    assert cns.cns_statemachine_scratch_bytes(1_000_000) == 4096 * 128
+    assert cns.cns_statemachine_scratch_bytes(4096 * 5000 + 1) == 5001 * 128
     assert L.cns_statemachine_run(None, -1, 0, None, None, None, 0, None) == cns.CNS_ERR_INVALID_VALUE
     assert L.cns_statemachine_run(None, 4, 0, None, 0x1000, None, 0, None) == cns.CNS_ERR_NULL_PTR
     assert L.cns_statemachine_run(0x1008, 4, 0, 0x2000, 0x3000, 0x4000, 8, None) == cns.CNS_ERR_INVALID_VALUE
