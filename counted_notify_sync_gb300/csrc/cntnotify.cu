@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
     uint2 *s_tr = reinterpret_cast<uint2 *>(f_smem + kFThreads * kFPad);
     uint32_t *s_setm = reinterpret_cast<uint32_t *>(s_tr + kFThreads * kFPad);
     __shared__ uint32_t s_job[kFThreads];   // stretch handed to thread i: (start << 16) | end
-    __shared__ int s_cls[kJobClasses];       // per length class: count, then first slot
+    __shared__ int s_cls[kJobClasses];       // per length class: its stretches' count
     const int64_t tiles = (n + tile_ops - 1) / tile_ops;
     const int k = threadIdx.x;
     const int lane = k & 31;
@@ -574,8 +574,9 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
         f_stretch(s_setm, chunk0, cnt, &start, &end);
         {   // A
             // The stretches are handed to threads longest class first (class = floor(log2(length)),
-            // counted per warp, placed by a scan over the classes), so that a warp's lanes walk
-            // stretches of similar length instead of waiting for one long stretch among short ones.
+            // counted per warp; each thread then adds up the counts of the longer classes for its
+            // place), so that a warp's lanes walk stretches of similar length instead of waiting for
+            // one long stretch among short ones.
             const int len = end - start;   // 0: none
             const int cls = len > 0 ? kJobClasses - 2 - min(31 - __clz(len), kJobClasses - 2) : kJobClasses - 1;
             const uint32_t same = __match_any_sync(0xffffffffu, cls);
@@ -584,23 +585,16 @@ __global__ void __launch_bounds__(kFThreads, 2) sm_onepass_kernel(const uint4 *o
             if (lane == leader)
                 wbase = atomicAdd(&s_cls[cls], __popc(same));
             wbase = __shfl_sync(0xffffffffu, wbase, leader) + __popc(same & ((1u << lane) - 1u));
-            __syncthreads();
-            if (k < 32) {   // exclusive scan of the class counts, one class per lane of warp 0
-                const int n_q = k < kJobClasses ? s_cls[k] : 0;
-                int incl = n_q;
+            __syncthreads();   // every class's count in
+            int place = wbase, jobs = 0;   // the jobs of the longer classes come first
 #pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const int up = __shfl_up_sync(0xffffffffu, incl, d);
-                    if (lane >= d)
-                        incl += up;
-                }
-                if (k < kJobClasses)
-                    s_cls[k] = incl - n_q;
+            for (int q = 0; q < kJobClasses - 1; ++q) {
+                const int n_q = s_cls[q];
+                place += q < cls ? n_q : 0;
+                jobs += n_q;
             }
-            __syncthreads();
             if (len > 0)
-                s_job[s_cls[cls] + wbase] = (static_cast<uint32_t>(start) << 16) | static_cast<uint32_t>(end);
-            const int jobs = s_cls[kJobClasses - 1];
+                s_job[place] = (static_cast<uint32_t>(start) << 16) | static_cast<uint32_t>(end);
             __syncthreads();
             if (k < jobs) {
                 const int js = static_cast<int>(s_job[k] >> 16), je = static_cast<int>(s_job[k] & 0xFFFFu);
