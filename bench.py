@@ -760,7 +760,11 @@ def run_native(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     import counted_notify_sync_gb300 as cns
+    if world > 1 and rank != 0:
+        dist.barrier()   # rank 0 builds (or finds the build up to date) first: one writer of the library
     cns.build()
+    if world > 1 and rank == 0:
+        dist.barrier()
     cns._native.lib()
     peaks = load_peaks()
     sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
