@@ -33,8 +33,9 @@ The last two exist to show that the explorer does catch broken protocols.
 The later explorers take the same approach to the library's other
 protocols: the two-level (cluster) barrier, the sense-flip counter, the
 one-barrier hard path, its paired gather / release step (explore_paired),
-the die-local counter copies, and the two-stream counted-notify pipeline's
-handshakes (explore_pipeline).
+the die-local counter copies, the two-stream counted-notify pipeline's
+handshakes (explore_pipeline), and the op-stream state machine's link words
+between tiles across repeated launches (explore_links).
 """
 from __future__ import annotations
 
@@ -722,5 +723,76 @@ def explore_pipeline(tiles: int, consumers: int, rounds: int, areas: int = 2, fo
                     res.epoch_violations += 1
             else:
                 res.deadlocks += 1
+        stack.extend(succ)
+    return res
+
+
+# The op-stream state machine's links between tiles, across launches ---------
+#
+# One launch walks T tiles; tile t's end count goes to the next tile through a
+# link word tagged with the launch's tag: the tile publishes the word (after
+# taking its predecessor's, if the tile holds no start, else at once), and
+# the next tile waits until the word carries the tag, then takes it.  A CUDA
+# graph replays a captured launch with the same tag, launch after launch (each
+# launch starts once the one before it has ended).  The explorer enumerates
+# every order of the tiles' steps within each of L launches and checks that
+# every take reads the word its own launch published.
+#
+#   clear=True    the thread that takes a word sets it to 0 (no launch's tag)
+#   starts        per tile, whether it holds a start (publishes before it
+#                 waits) or not (its count needs its predecessor's)
+#   same_tag      every launch carries the same tag (graph replays); False:
+#                 a tag per launch (calls submitted one by one)
+#
+# Result.safety_violations counts takes of a word another launch published.
+
+def explore_links(T: int, launches: int, starts=None, clear: bool = True, same_tag: bool = True,
+                  max_states: int = 2_000_000) -> Result:
+    starts = tuple(starts) if starts is not None else tuple(True for _ in range(T))
+    res = Result()
+    # link word: (tag, launch that published it) or None; tile: (published, taken)
+    init = (0, tuple(None for _ in range(T)), tuple((False, False) for _ in range(T)))
+    seen = set()
+    stack = [init]
+    while stack:
+        state = stack.pop()
+        if state in seen:
+            continue
+        seen.add(state)
+        res.states += 1
+        if res.states > max_states:
+            raise RuntimeError("state space larger than max_states")
+        k, words, tiles = state
+        if k == launches:
+            res.completed += 1
+            continue
+        tag = 1 if same_tag else k + 1
+        succ = []
+
+        def done(t, pub, took):
+            return (pub or t == T - 1) and (took or t == 0)
+
+        if all(done(t, *tiles[t]) for t in range(T)):   # the launch has ended: the next one starts
+            succ.append((k + 1, words, tuple((False, False) for _ in range(T))))
+        for t in range(T):
+            pub, took = tiles[t]
+
+            def put(nw, npub, ntook):
+                succ.append((k, nw, tiles[:t] + ((npub, ntook),) + tiles[t + 1:]))
+
+            # publish: a tile with a start at any time (its last stretch needs no earlier count); one
+            # without, once it has taken its predecessor's count (tile 0 starts from the call's init)
+            if not pub and t < T - 1 and (starts[t] or took or t == 0):
+                put(words[:t] + ((tag, k),) + words[t + 1:], True, took)
+            # take: once the predecessor's word carries the tag
+            if not took and t > 0:
+                got = words[t - 1]
+                if got is not None and got[0] == tag:
+                    if got[1] != k:
+                        res.safety_violations += 1
+                    nw = words[:t - 1] + (None,) + words[t:] if clear else words
+                    put(nw, pub, True)
+        if not succ:
+            res.deadlocks += 1
         stack.extend(succ)
     return res

@@ -308,3 +308,39 @@ def test_pipeline_consumer_ctas_cannot_all_poll_the_count(areas):
     clear waits for ever: the reason for the go word."""
     assert explore_pipeline(2, 2, 3, areas=areas, all_poll=True).deadlocks > 0
     assert explore_pipeline(2, 1, 3, areas=areas, all_poll=True).ok
+
+
+# --- the state machine's links between tiles, across launches ----------------------------
+
+from oracle.protocol import explore_links  # noqa: E402
+
+LINK_STARTS = [None, (False, False, False), (True, False, True), (False, True, False, True), (False,) * 4]
+
+
+@pytest.mark.parametrize("starts", LINK_STARTS)
+@pytest.mark.parametrize("launches", [1, 2, 3])
+def test_links_taken_words_cleared_are_never_stale(starts, launches):
+    """A tile takes its predecessor's link word once it carries the call's tag and sets it to 0: every
+    take reads the word its own launch published, even when every launch carries the same tag (a
+    CUDA graph replaying one captured call), and every launch completes."""
+    T = len(starts) if starts else 3
+    r = explore_links(T, launches, starts)
+    assert r.ok and r.completed > 0, r
+
+
+@pytest.mark.parametrize("starts", LINK_STARTS)
+def test_links_without_the_clear_go_stale_under_replays(starts):
+    """Without the clear, a replay's tile can take the word its predecessor published in the replay
+    before (same tag): the model finds it, as the GPU did (wrong trace entries when the ops changed
+    between replays)."""
+    T = len(starts) if starts else 3
+    r = explore_links(T, 2, starts, clear=False)
+    assert r.safety_violations > 0
+
+
+@pytest.mark.parametrize("starts", LINK_STARTS)
+def test_links_without_the_clear_hold_with_a_tag_per_call(starts):
+    """Calls submitted one by one each carry a new tag, and then the words need no clearing."""
+    T = len(starts) if starts else 3
+    r = explore_links(T, 3, starts, clear=False, same_tag=False)
+    assert r.ok and r.completed > 0, r
